@@ -1,0 +1,461 @@
+/*
+ * kivi_oracle.c -- plain, slow, single-threaded CPU oracle for KIVI-style
+ * group-affine KV-cache quantization and decode attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the library's product path may link,
+ * load or call this file; only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg do.  It shares no code, header, table or helper with the
+ * CUDA library.
+ *
+ * What it follows (VeloxQuant-MLX pages):
+ *  - Changelog, v0.8.0 "New", KIVI entry: keys are quantized per channel,
+ *    values per token, asymmetric group quantization, an fp16 residual window
+ *    (`residual_length`) and a group size (`kivi_group_size`, default 32).
+ *  - Changelog, v0.42.0 "Added", scalar_fused_decode_attend: the cache is
+ *    integer codes plus one (scale, zero) pair per group from the group's
+ *    min/max; attention runs over k_hat/v_hat rebuilt from those codes, with
+ *    softmax accumulated in higher precision than fp16.
+ *  - Method overview, AgeTieredKV entry: the residual window is gated purely
+ *    by recency and the group quantizer is a shared min/max quantizer.
+ *  - Changelog, v0.28.0 (NSNQuant-adapted): the fp16 residual buffer is
+ *    flushed in whole chunks ("chunk-flush ... KIVI's idiom"), and prefill
+ *    and decode produce identical quantized state.
+ * The pages print no formula; the fp32 formula used here is the plain reading
+ * (scale = (max-min)/(2^b-1); code = clamp(rint((x-min)/scale), 0, 2^b-1);
+ * scale stored as fp16 round-to-nearest-even, zero = min stored exactly).
+ *
+ * Precision: quantization arithmetic in IEEE fp32 exactly as written (this
+ * file must be compiled without fast-math and with -ffp-contract=off);
+ * dequantization and attention in double (k_hat = code*scale + zero is exact
+ * in double).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef _Float16 half_t;
+
+static float h2f(uint16_t bits) {
+  half_t h;
+  memcpy(&h, &bits, sizeof h);
+  return (float)h;
+}
+
+static uint16_t f2h(float f) {
+  half_t h = (half_t)f; /* IEEE conversion, round to nearest even */
+  uint16_t bits;
+  memcpy(&bits, &h, sizeof bits);
+  return bits;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The group quantizer (one group of n values).                              */
+/* ------------------------------------------------------------------------ */
+
+/* x[i*stride], i < n: fp32 copies of fp16 inputs.  Writes codes[i*cstride],
+ * the fp32 scale, and the stored fp16 scale / zero bit patterns. */
+static void quant_group(const float *x, long stride, int n, int bits,
+                        uint8_t *codes, long cstride, float *scale32,
+                        uint16_t *s16, uint16_t *z16) {
+  const int levels = (1 << bits) - 1;
+  float mn = x[0], mx = x[0];
+  for (int i = 1; i < n; ++i) {
+    float v = x[(long)i * stride];
+    if (v < mn) mn = v;
+    if (v > mx) mx = v;
+  }
+  float range = mx - mn;
+  float scale = range / (float)levels;
+  for (int i = 0; i < n; ++i) {
+    int c = 0;
+    if (scale != 0.0f) {
+      float diff = x[(long)i * stride] - mn;
+      float t = diff / scale;
+      float r = nearbyintf(t); /* default rounding mode: ties to even */
+      if (r < 0.0f) r = 0.0f;
+      if (r > (float)levels) r = (float)levels;
+      c = (int)r;
+    }
+    codes[(long)i * cstride] = (uint8_t)c;
+  }
+  if (scale32) *scale32 = scale;
+  *s16 = f2h(scale);
+  *z16 = f2h(mn);
+}
+
+void orc_quant_group_f32(const float *x, int n, int bits, uint8_t *codes,
+                         float *scale32, uint16_t *s16, uint16_t *z16) {
+  quant_group(x, 1, n, bits, codes, 1, scale32, s16, z16);
+}
+
+/* Sub-byte packing: the code of element e of a row sits in byte e*b/8 at bit
+ * (e*b) mod 8, least significant bits first (2-bit: 4 per byte, 4-bit: 2 per
+ * byte, 8-bit: 1 per byte). */
+void orc_pack_codes(const uint8_t *codes, int n, int bits, uint8_t *out) {
+  int nbytes = (n * bits + 7) / 8;
+  memset(out, 0, (size_t)nbytes);
+  for (int e = 0; e < n; ++e) {
+    int bit = e * bits;
+    out[bit / 8] |= (uint8_t)(codes[e] << (bit % 8));
+  }
+}
+
+void orc_unpack_codes(const uint8_t *packed, int n, int bits, uint8_t *codes) {
+  int mask = (1 << bits) - 1;
+  for (int e = 0; e < n; ++e) {
+    int bit = e * bits;
+    codes[e] = (uint8_t)((packed[bit / 8] >> (bit % 8)) & mask);
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* The cache.                                                                 */
+/* ------------------------------------------------------------------------ */
+
+typedef struct orc_cache {
+  int B, Hq, Hkv, D, bits, g, R, max_seq;
+  int Tcap; /* quantized-token capacity, a multiple of g */
+  int Rcap; /* residual capacity, R + g */
+  int row;  /* packed bytes per token row: D*bits/8 */
+  uint8_t *Kc, *Vc;        /* [B][Hkv][Tcap][row] */
+  uint16_t *Ks, *Kz;       /* [B][Hkv][Tcap/g][D] */
+  uint16_t *Vs, *Vz;       /* [B][Hkv][Tcap][D/g] */
+  uint16_t *Kr, *Vr;       /* [B][Hkv][Rcap][D]; slot i holds token Tq+i */
+  int32_t *S, *Tq, *nres;  /* [B] */
+} orc_cache;
+
+static int n_quantized(int S, int R, int g) {
+  /* Quantized prefix length for a sequence of S tokens: whole groups only,
+   * leaving between R and R+g-1 tokens (or all S, when S < R) in fp16. */
+  if (S < R) return 0;
+  return g * ((S - R) / g);
+}
+
+orc_cache *orc_new(int B, int Hq, int Hkv, int D, int bits, int g, int R,
+                   int max_seq) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || g <= 0 || R < 0 ||
+      max_seq < 0)
+    return NULL;
+  if (bits != 2 && bits != 4 && bits != 8) return NULL;
+  if (Hq % Hkv != 0 || D % g != 0 || (D * bits) % 8 != 0) return NULL;
+  if (D > 4096) return NULL; /* per-row scratch below is sized for 4096 */
+  orc_cache *c = (orc_cache *)calloc(1, sizeof *c);
+  if (!c) return NULL;
+  c->B = B; c->Hq = Hq; c->Hkv = Hkv; c->D = D; c->bits = bits; c->g = g;
+  c->R = R; c->max_seq = max_seq;
+  c->Tcap = ((max_seq + g - 1) / g) * g;
+  if (c->Tcap == 0) c->Tcap = g;
+  c->Rcap = R + g;
+  c->row = D * bits / 8;
+  size_t bh = (size_t)B * Hkv;
+  c->Kc = (uint8_t *)calloc(bh * c->Tcap * c->row, 1);
+  c->Vc = (uint8_t *)calloc(bh * c->Tcap * c->row, 1);
+  c->Ks = (uint16_t *)calloc(bh * (c->Tcap / g) * D, 2);
+  c->Kz = (uint16_t *)calloc(bh * (c->Tcap / g) * D, 2);
+  c->Vs = (uint16_t *)calloc(bh * c->Tcap * (D / g), 2);
+  c->Vz = (uint16_t *)calloc(bh * c->Tcap * (D / g), 2);
+  c->Kr = (uint16_t *)calloc(bh * c->Rcap * D, 2);
+  c->Vr = (uint16_t *)calloc(bh * c->Rcap * D, 2);
+  c->S = (int32_t *)calloc(B, 4);
+  c->Tq = (int32_t *)calloc(B, 4);
+  c->nres = (int32_t *)calloc(B, 4);
+  if (!c->Kc || !c->Vc || !c->Ks || !c->Kz || !c->Vs || !c->Vz || !c->Kr ||
+      !c->Vr || !c->S || !c->Tq || !c->nres) {
+    free(c->Kc); free(c->Vc); free(c->Ks); free(c->Kz); free(c->Vs);
+    free(c->Vz); free(c->Kr); free(c->Vr); free(c->S); free(c->Tq);
+    free(c->nres); free(c);
+    return NULL;
+  }
+  return c;
+}
+
+void orc_free(orc_cache *c) {
+  if (!c) return;
+  free(c->Kc); free(c->Vc); free(c->Ks); free(c->Kz); free(c->Vs);
+  free(c->Vz); free(c->Kr); free(c->Vr); free(c->S); free(c->Tq);
+  free(c->nres); free(c);
+}
+
+/* Quantize one key group (g tokens, all D channels, per channel) and the
+ * values of the same g tokens (per token, groups of g channels).  ktok/vtok
+ * return a pointer to the fp16 row of token i of the group. */
+typedef const uint16_t *(*row_fn)(const void *ctx, int i);
+
+static void quantize_group_of_tokens(orc_cache *c, int b, int h, int G,
+                                     row_fn krow, row_fn vrow,
+                                     const void *ctx) {
+  const int D = c->D, g = c->g;
+  size_t bh = (size_t)b * c->Hkv + h;
+  float *x = (float *)malloc(sizeof(float) * (size_t)g * D);
+  uint8_t *codes = (uint8_t *)malloc((size_t)g * D);
+  /* keys: per channel over the g tokens */
+  for (int i = 0; i < g; ++i) {
+    const uint16_t *r = krow(ctx, i);
+    for (int ch = 0; ch < D; ++ch) x[(size_t)i * D + ch] = h2f(r[ch]);
+  }
+  for (int ch = 0; ch < D; ++ch) {
+    uint16_t s16, z16;
+    quant_group(x + ch, D, g, c->bits, codes + ch, D, NULL, &s16, &z16);
+    c->Ks[(bh * (c->Tcap / g) + G) * D + ch] = s16;
+    c->Kz[(bh * (c->Tcap / g) + G) * D + ch] = z16;
+  }
+  for (int i = 0; i < g; ++i) {
+    size_t t = (size_t)G * g + i;
+    orc_pack_codes(codes + (size_t)i * D, D, c->bits,
+                   c->Kc + (bh * c->Tcap + t) * c->row);
+  }
+  /* values: per token over groups of g consecutive channels */
+  for (int i = 0; i < g; ++i) {
+    const uint16_t *r = vrow(ctx, i);
+    size_t t = (size_t)G * g + i;
+    float xv[4096];
+    uint8_t cv[4096];
+    for (int ch = 0; ch < D; ++ch) xv[ch] = h2f(r[ch]);
+    for (int j = 0; j < D / g; ++j) {
+      uint16_t s16, z16;
+      quant_group(xv + j * g, 1, g, c->bits, cv + j * g, 1, NULL, &s16, &z16);
+      c->Vs[(bh * c->Tcap + t) * (D / g) + j] = s16;
+      c->Vz[(bh * c->Tcap + t) * (D / g) + j] = z16;
+    }
+    orc_pack_codes(cv, D, c->bits, c->Vc + (bh * c->Tcap + t) * c->row);
+  }
+  free(x);
+  free(codes);
+}
+
+typedef struct {
+  const uint16_t *base; /* [S_max][D] block of one (b, h) */
+  int D, first;
+} dense_ctx;
+
+static const uint16_t *dense_row(const void *ctx, int i) {
+  const dense_ctx *d = (const dense_ctx *)ctx;
+  return d->base + (size_t)(d->first + i) * d->D;
+}
+
+typedef struct {
+  const dense_ctx *kd, *vd;
+} kv_pair_ctx;
+
+static const uint16_t *pair_k(const void *ctx, int i) {
+  const kv_pair_ctx *p = (const kv_pair_ctx *)ctx;
+  return dense_row(p->kd, i);
+}
+static const uint16_t *pair_v(const void *ctx, int i) {
+  const kv_pair_ctx *p = (const kv_pair_ctx *)ctx;
+  return dense_row(p->vd, i);
+}
+
+/* Prefill: K, V fp16 [B][Hkv][s_stride][D]; sequence b has seq_lens[b]
+ * tokens.  Replaces the whole cache state.  Returns 0, or -1 on a bad length. */
+int orc_quantize(orc_cache *c, const uint16_t *K, const uint16_t *V,
+                 long s_stride, const int32_t *seq_lens) {
+  for (int b = 0; b < c->B; ++b)
+    if (seq_lens[b] < 0 || seq_lens[b] > c->max_seq || seq_lens[b] > s_stride)
+      return -1;
+  for (int b = 0; b < c->B; ++b) {
+    int S = seq_lens[b];
+    int Tq = n_quantized(S, c->R, c->g);
+    c->S[b] = S;
+    c->Tq[b] = Tq;
+    c->nres[b] = S - Tq;
+    for (int h = 0; h < c->Hkv; ++h) {
+      size_t off = ((size_t)b * c->Hkv + h) * (size_t)s_stride * c->D;
+      for (int G = 0; G < Tq / c->g; ++G) {
+        dense_ctx kd = {K + off, c->D, G * c->g};
+        dense_ctx vd = {V + off, c->D, G * c->g};
+        kv_pair_ctx p = {&kd, &vd};
+        quantize_group_of_tokens(c, b, h, G, pair_k, pair_v, &p);
+      }
+      size_t bh = (size_t)b * c->Hkv + h;
+      for (int i = 0; i < S - Tq; ++i) {
+        memcpy(c->Kr + (bh * c->Rcap + i) * c->D,
+               K + off + (size_t)(Tq + i) * c->D, 2 * (size_t)c->D);
+        memcpy(c->Vr + (bh * c->Rcap + i) * c->D,
+               V + off + (size_t)(Tq + i) * c->D, 2 * (size_t)c->D);
+      }
+    }
+  }
+  return 0;
+}
+
+/* Decode-time append, done the incremental way: push the new tokens onto
+ * the fp16 residual, then flush the oldest whole groups while at least R+g
+ * tokens are waiting.  Kn, Vn fp16 [B][Hkv][n_stride][D]. */
+int orc_append(orc_cache *c, const uint16_t *Kn, const uint16_t *Vn,
+               long n_stride, const int32_t *n_new) {
+  for (int b = 0; b < c->B; ++b)
+    if (n_new[b] < 0 || n_new[b] > n_stride ||
+        (long)c->S[b] + n_new[b] > c->max_seq)
+      return -1;
+  const int D = c->D;
+  for (int b = 0; b < c->B; ++b) {
+    int n = n_new[b];
+    for (int h = 0; h < c->Hkv; ++h) {
+      size_t bh = (size_t)b * c->Hkv + h;
+      /* a growing fp16 staging list: old residual followed by new tokens */
+      int total = c->nres[b] + n;
+      uint16_t *ks = (uint16_t *)malloc(2 * (size_t)D * (total ? total : 1));
+      uint16_t *vs = (uint16_t *)malloc(2 * (size_t)D * (total ? total : 1));
+      memcpy(ks, c->Kr + bh * c->Rcap * D, 2 * (size_t)D * c->nres[b]);
+      memcpy(vs, c->Vr + bh * c->Rcap * D, 2 * (size_t)D * c->nres[b]);
+      const uint16_t *kin = Kn + bh * (size_t)n_stride * D;
+      const uint16_t *vin = Vn + bh * (size_t)n_stride * D;
+      memcpy(ks + (size_t)c->nres[b] * D, kin, 2 * (size_t)D * n);
+      memcpy(vs + (size_t)c->nres[b] * D, vin, 2 * (size_t)D * n);
+      int head = 0; /* index of the oldest unflushed staged token */
+      int Tq = c->Tq[b];
+      while (total - head >= c->R + c->g) {
+        dense_ctx kd = {ks, D, head};
+        dense_ctx vd = {vs, D, head};
+        kv_pair_ctx p = {&kd, &vd};
+        quantize_group_of_tokens(c, b, h, Tq / c->g, pair_k, pair_v, &p);
+        head += c->g;
+        Tq += c->g;
+      }
+      for (int i = 0; i < total - head; ++i) {
+        memcpy(c->Kr + (bh * c->Rcap + i) * D, ks + (size_t)(head + i) * D,
+               2 * (size_t)D);
+        memcpy(c->Vr + (bh * c->Rcap + i) * D, vs + (size_t)(head + i) * D,
+               2 * (size_t)D);
+      }
+      if (h == c->Hkv - 1) {
+        c->Tq[b] = Tq;
+        c->nres[b] = total - head;
+        c->S[b] += n;
+      }
+      free(ks);
+      free(vs);
+    }
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dequantization and attention (double).                                   */
+/* ------------------------------------------------------------------------ */
+
+/* k_hat and v_hat of token t of sequence (b, h), all D channels, in double. */
+static void token_hat(const orc_cache *c, int b, int h, int t, double *k,
+                      double *v) {
+  const int D = c->D, g = c->g;
+  size_t bh = (size_t)b * c->Hkv + h;
+  if (t < c->Tq[b]) {
+    uint8_t codes[4096];
+    int G = t / g;
+    orc_unpack_codes(c->Kc + (bh * c->Tcap + t) * c->row, D, c->bits, codes);
+    for (int ch = 0; ch < D; ++ch) {
+      double s = h2f(c->Ks[(bh * (c->Tcap / g) + G) * D + ch]);
+      double z = h2f(c->Kz[(bh * (c->Tcap / g) + G) * D + ch]);
+      k[ch] = (double)codes[ch] * s + z;
+    }
+    orc_unpack_codes(c->Vc + (bh * c->Tcap + t) * c->row, D, c->bits, codes);
+    for (int ch = 0; ch < D; ++ch) {
+      double s = h2f(c->Vs[(bh * c->Tcap + t) * (D / g) + ch / g]);
+      double z = h2f(c->Vz[(bh * c->Tcap + t) * (D / g) + ch / g]);
+      v[ch] = (double)codes[ch] * s + z;
+    }
+  } else {
+    int i = t - c->Tq[b];
+    for (int ch = 0; ch < D; ++ch) {
+      k[ch] = h2f(c->Kr[(bh * c->Rcap + i) * D + ch]);
+      v[ch] = h2f(c->Vr[(bh * c->Rcap + i) * D + ch]);
+    }
+  }
+}
+
+/* One query head: softmax(scale * q . k_hat_t) over every token t of
+ * sequence b (quantized prefix and fp16 residual; no mask), weighted sum of
+ * v_hat_t.  Query head hq reads kv head hq / (Hq/Hkv).  out: D doubles.
+ * Returns 0, or -1 for an empty sequence (out is then all zero). */
+int orc_attend_one(const orc_cache *c, int b, int hq, const uint16_t *q_row,
+                   double scale, double *out) {
+  const int D = c->D;
+  const int h = hq / (c->Hq / c->Hkv);
+  const int S = c->S[b];
+  for (int ch = 0; ch < D; ++ch) out[ch] = 0.0;
+  if (S == 0) return -1;
+  double *q = (double *)malloc(sizeof(double) * D);
+  double *k = (double *)malloc(sizeof(double) * D);
+  double *v = (double *)malloc(sizeof(double) * D);
+  double *s = (double *)malloc(sizeof(double) * (size_t)S);
+  for (int ch = 0; ch < D; ++ch) q[ch] = h2f(q_row[ch]);
+  double m = -INFINITY;
+  for (int t = 0; t < S; ++t) {
+    token_hat(c, b, h, t, k, v);
+    double dot = 0.0;
+    for (int ch = 0; ch < D; ++ch) dot += q[ch] * k[ch];
+    s[t] = scale * dot;
+    if (s[t] > m) m = s[t];
+  }
+  double l = 0.0;
+  for (int t = 0; t < S; ++t) {
+    double p = exp(s[t] - m);
+    l += p;
+    token_hat(c, b, h, t, k, v);
+    for (int ch = 0; ch < D; ++ch) out[ch] += p * v[ch];
+  }
+  for (int ch = 0; ch < D; ++ch) out[ch] /= l;
+  free(q); free(k); free(v); free(s);
+  return 0;
+}
+
+/* All heads: q fp16 [B][Hq][D] -> out fp32 [B][Hq][D]. */
+int orc_attend(const orc_cache *c, const uint16_t *q, double scale,
+               float *out) {
+  double *o = (double *)malloc(sizeof(double) * c->D);
+  for (int b = 0; b < c->B; ++b)
+    for (int hq = 0; hq < c->Hq; ++hq) {
+      size_t off = ((size_t)b * c->Hq + hq) * c->D;
+      orc_attend_one(c, b, hq, q + off, scale, o);
+      for (int ch = 0; ch < c->D; ++ch) out[off + ch] = (float)o[ch];
+    }
+  free(o);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Accessors.                                                                 */
+/* ------------------------------------------------------------------------ */
+
+void orc_lengths(const orc_cache *c, int32_t *S, int32_t *Tq, int32_t *nres) {
+  memcpy(S, c->S, 4 * (size_t)c->B);
+  memcpy(Tq, c->Tq, 4 * (size_t)c->B);
+  memcpy(nres, c->nres, 4 * (size_t)c->B);
+}
+
+void orc_dims(const orc_cache *c, int32_t *Tcap, int32_t *Rcap) {
+  *Tcap = c->Tcap;
+  *Rcap = c->Rcap;
+}
+
+/* which: 0 Kc, 1 Ks, 2 Kz, 3 Vc, 4 Vs, 5 Vz, 6 Kr, 7 Vr.  Copies the whole
+ * plane into dst (size given by orc_plane_bytes). */
+size_t orc_plane_bytes(const orc_cache *c, int which) {
+  size_t bh = (size_t)c->B * c->Hkv;
+  switch (which) {
+    case 0: case 3: return bh * c->Tcap * c->row;
+    case 1: case 2: return bh * (c->Tcap / c->g) * c->D * 2;
+    case 4: case 5: return bh * c->Tcap * (c->D / c->g) * 2;
+    case 6: case 7: return bh * c->Rcap * c->D * 2;
+    default: return 0;
+  }
+}
+
+int orc_get_plane(const orc_cache *c, int which, void *dst) {
+  const void *src = NULL;
+  switch (which) {
+    case 0: src = c->Kc; break;
+    case 1: src = c->Ks; break;
+    case 2: src = c->Kz; break;
+    case 3: src = c->Vc; break;
+    case 4: src = c->Vs; break;
+    case 5: src = c->Vz; break;
+    case 6: src = c->Kr; break;
+    case 7: src = c->Vr; break;
+    default: return -1;
+  }
+  memcpy(dst, src, orc_plane_bytes(c, which));
+  return 0;
+}
