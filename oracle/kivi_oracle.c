@@ -22,7 +22,8 @@
  *    and decode produce identical quantized state.
  * The pages print no formula; the fp32 formula used here is the plain reading
  * (scale = (max-min)/(2^b-1); code = clamp(rint((x-min)/scale), 0, 2^b-1);
- * scale stored as fp16 round-to-nearest-even, zero = min stored exactly).
+ * scale stored as fp16 round-to-nearest-even, zero = min stored exactly,
+ * with a minimum of -0.0 stored as +0.0).
  *
  * Precision: quantization arithmetic in IEEE fp32 exactly as written (this
  * file must be compiled without fast-math and with -ffp-contract=off);
@@ -65,6 +66,10 @@ static void quant_group(const float *x, long stride, int n, int bits,
     if (v < mn) mn = v;
     if (v > mx) mx = v;
   }
+  /* A group minimum of -0.0 is stored as +0.0 (the pages leave signed zero
+   * open; -0 + +0 = +0 under round-to-nearest).  No code changes: x - min
+   * is the same number either way. */
+  mn = mn + 0.0f;
   float range = mx - mn;
   float scale = range / (float)levels;
   for (int i = 0; i < n; ++i) {

@@ -406,3 +406,15 @@ def test_large_scores_stay_finite(oracle_mod):
     want = (V[0, 0, S - 1].astype(np.float64) + V[0, 0, S - 3]) / 2
     assert np.isfinite(out).all()
     assert np.allclose(out[0, 0], want, atol=1e-6)
+
+
+def test_negative_zero_minimum_stored_as_positive_zero(oracle_mod):
+    """A group whose minimum is -0.0 stores zero = +0.0 (bit pattern 0x0000);
+    the codes are those of the same group with +0.0."""
+    x = np.array([-0.0, 1.0, 2.0, 3.0], np.float32)
+    codes, s32, s16, z16 = oracle_mod.quant_group(x, 2)
+    assert z16 == 0x0000
+    assert codes.tolist() == [0, 1, 2, 3]
+    x2 = np.array([0.0, -0.0, 0.0, -0.0], np.float32)
+    codes, s32, s16, z16 = oracle_mod.quant_group(x2, 2)
+    assert z16 == 0x0000 and s16 == 0 and (codes == 0).all()
