@@ -1,0 +1,410 @@
+"""Benchmark of the fused KIVI decode step on one GPU (or N replicas).
+
+A step is one serving decode step over the pages' decode shape (VeloxQuant-MLX
+changelog v0.42.0 "Added": B=1, H=32, D=128, b=2, g=32, S_q=1; S_kv=65536,
+the long end of its sweep) with the KIVI cache of changelog v0.8.0 (fp16
+residual window of 32 tokens): append the new token's K/V to every sequence
+(flushing a group to 2-bit codes whenever the residual fills) and run the
+fused decode-attend over the whole cache.
+
+Prints one JSON line.  `value` is microseconds per step (lower is better),
+device-timed with CUDA events over K back-to-back steps that rotate over
+enough identical cache copies to exceed 4x L2, so every step streams its
+cache from HBM.  The roofline object reports the decode kernel's achieved
+HBM bandwidth over the algorithmic bytes (packed codes + fp16 scale/zero
+planes + fp16 residual + q + out).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused 2-bit KV decode-attend: µs/step and HBM GB/s (% of GB300 peak)"
+UNIT = "us/step"
+DEFAULT_WORKLOAD = "pages_S65536"
+
+
+# ---------------------------------------------------------------------------
+# byte accounting (the roofline numerator)
+# ---------------------------------------------------------------------------
+
+def decode_bytes(w, seq_lens):
+    """Algorithmic bytes of one fused decode over caches of the given lengths:
+    per (b, h_kv): T_q * (2 packed rows + fp16 K scale/zero per token + fp16
+    V scale/zero per token) + n_res * fp16 K and V rows + q + out."""
+    D, g, bits, R = w.D, w.group, w.bits, w.residual
+    row = D * bits // 8
+    per_q_tok = 2 * row + (2 * D * 2) / g + 2 * (D // g) * 2
+    gq = w.H_q // w.H_kv
+    total = 0.0
+    for S in seq_lens:
+        Tq = 0 if S < R else g * ((S - R) // g)
+        nres = S - Tq
+        total += w.H_kv * (Tq * per_q_tok + nres * D * 4 + gq * D * 2 + gq * D * 4)
+    return int(total)
+
+
+def append_bytes(w, n_new):
+    """Algorithmic bytes of appending n_new tokens per sequence without a
+    flush: read the new fp16 K/V rows, write them to the residual ring."""
+    return w.B * w.H_kv * n_new * w.D * 2 * 2 * 2
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, period_ms: int = 20):
+        self.index, self.period_ms = index, period_ms
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms", str(self.period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        time.sleep(0.1)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: no data-path collective)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def measured_peak_gbs():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_steps(w, budget_s: float = 12.0, max_steps: int = 8, inputs=None):
+    """Time the CPU oracle on the same step (append one token per sequence,
+    then decode-attend every head) on a bounded sample: whole steps until
+    `budget_s` seconds of stepping or `max_steps` steps.  Returns
+    (us_per_step, steps, setup_s)."""
+    import numpy as np
+    import torch
+    import oracle
+    from bit_kv_cache_05_gb300 import synth
+    t0 = time.perf_counter()
+    if inputs is None:
+        inputs = synth.make_inputs(w, device="cpu")
+    K = inputs["K"].cpu().numpy()
+    V = inputs["V"].cpu().numpy()
+    oc = oracle.OracleCache(w.B, w.H_q, w.H_kv, w.D, w.bits, w.group,
+                            w.residual, w.max_seq + max_steps + 1)
+    oc.quantize(K, V, w.seq_lens)
+    K1, V1, q = synth.decode_tokens(w, max_steps, device="cpu")
+    K1, V1, q = K1.numpy(), V1.numpy(), q.numpy()
+    setup = time.perf_counter() - t0
+    times = []
+    start = time.perf_counter()
+    for i in range(max_steps):
+        a = time.perf_counter()
+        oc.append(K1[i], V1[i], [1] * w.B)
+        oc.attend(q[i])
+        times.append(time.perf_counter() - a)
+        if time.perf_counter() - start > budget_s:
+            break
+    del oc
+    return 1e6 * sum(times) / len(times), len(times), setup
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return
+    us, n, setup = oracle_steps(w)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(us, 3),
+        "unit": UNIT, "n_gpus": args.gpus, "steps": n, "warmup": 0,
+        "ms_per_step": round(us / 1e3, 6), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, N(0,1) fp16 K/V/q)",
+        "config": config_of(w),
+        "cpu_baseline": {"kind": "oracle", "value": round(us, 3), "unit": UNIT,
+                         "cores": 1,
+                         "sample": f"{n} whole steps (append 1 token/seq + "
+                                   f"decode-attend all heads) after an "
+                                   f"untimed {setup:.1f}s prefill"},
+        "e2e": {"value": round(us, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w):
+    return {"workload": w.name, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv,
+            "D": w.D, "bits": w.bits, "group": w.group,
+            "residual": w.residual, "S_kv": w.seq_lens[0] if w.B == 1
+            else w.seq_lens, "S_q": 1,
+            "step": "append 1 token per sequence + fused decode-attend"}
+
+
+def run_ours(args, w, rank, world, local):
+    import torch
+    from bit_kv_cache_05_gb300 import _lib, synth
+    from bit_kv_cache_05_gb300.cache import KiviCache
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _lib.load()
+    K_steps = args.steps
+    W = args.warmup
+    n_total = W + K_steps
+    inp = synth.make_inputs(w, device=dev)
+    K1, V1, q = synth.decode_tokens(w, max(n_total, 1), device=dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20
+    step_bytes = decode_bytes(w, w.seq_lens)
+    n_copies = max(2, -(-4 * l2 // step_bytes))
+    headroom = n_total + 64
+    caches = [KiviCache(inp["K"], inp["V"], w.seq_lens, H_q=w.H_q,
+                        bits=w.bits, group=w.group, residual=w.residual,
+                        max_seq=w.max_seq + 3 * headroom)
+              for _ in range(n_copies)]
+    del inp
+    out = torch.empty(w.B, w.H_q, w.D, dtype=torch.float32, device=dev)
+    ones = [1] * w.B
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+
+    def step(i):
+        c = caches[i % n_copies]
+        c.append(K1[i], V1[i], ones)
+        c.decode_attend(q[i], out)
+
+    # warm-up
+    for i in range(W):
+        step(i)
+    torch.cuda.synchronize(dev)
+
+    peak, peak_kind = measured_peak_gbs()
+    with ClockSampler(local) as clk:
+        # (1) the timed steps
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        l0 = _lib.launch_count()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(W, n_total):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        launches = _lib.launch_count() - l0
+        ms = e0.elapsed_time(e1) / K_steps
+        ms = max_over_ranks(ms, world, dev)
+        barrier(world)
+
+        # (2) the decode launch alone, per-launch events, rotating copies
+        ev = [(torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in range(K_steps)]
+        for i in range(K_steps):
+            c = caches[(i + 1) % n_copies]
+            ev[i][0].record(stream)
+            c.decode_attend(q[i], out)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        dec_ms = [a.elapsed_time(b) for a, b in ev]
+        dec_avg = sum(dec_ms) / len(dec_ms)
+
+        # (3) end to end through the public API from pinned host memory
+        hK = K1.cpu().pin_memory()
+        hV = V1.cpu().pin_memory()
+        hq = q.cpu().pin_memory()
+        hout = torch.empty(K_steps, w.B, w.H_q, w.D, dtype=torch.float32
+                           ).pin_memory()
+        dK = torch.empty_like(K1[0])
+        dV = torch.empty_like(V1[0])
+        dq = torch.empty_like(q[0])
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(K_steps):
+            c = caches[(i + 2) % n_copies]
+            dK.copy_(hK[W + i], non_blocking=True)
+            dV.copy_(hV[W + i], non_blocking=True)
+            dq.copy_(hq[W + i], non_blocking=True)
+            c.append(dK, dV, ones)
+            c.decode_attend(dq, out)
+            hout[i].copy_(out, non_blocking=True)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(t0.elapsed_time(t1) / K_steps, world, dev)
+
+    clocks = clk.summary()
+    S_now = [s + n_total for s in w.seq_lens]
+    dec_bytes = decode_bytes(w, S_now)
+    achieved = dec_bytes / (dec_avg * 1e-3) / 1e9
+    h2d = (K1[0].numel() + V1[0].numel() + q[0].numel()) * 2
+    d2h = out.numel() * 4
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        us, n, setup = oracle_steps(w)
+        cpu = {"kind": "oracle", "value": round(us, 3), "unit": UNIT,
+               "cores": 1,
+               "sample": f"{n} whole steps (append 1 token/seq + decode-attend "
+                         f"all heads) after an untimed {setup:.1f}s prefill"}
+    for c in caches:
+        c.close()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(ms * 1e3, 3), "unit": UNIT,
+        "n_gpus": world, "steps": K_steps, "warmup": W,
+        "ms_per_step": round(ms, 6), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded, N(0,1) fp16 K/V/q)",
+        "config": dict(config_of(w), l2=f"rotating {n_copies} cache copies "
+                       f"({n_copies * step_bytes / 1e6:.0f} MB > 4x L2)",
+                       parallelism=f"replicas x{world}"),
+        "decode_us": round(dec_avg * 1e3, 3),
+        "decode_gbs": round(achieved, 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "fused decode-attend (split + combine)",
+                     "algorithmic_bytes": dec_bytes},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_ms * 1e3, 3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from bit_kv_cache_05_gb300 import synth
+    w = synth.workload(args.workload)
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if args.impl == "ours":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, w, rank, world)
+        else:
+            run_ours(args, w, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,157 @@
+"""Python handle over the C ABI (include/vq_kivi.h): passes torch tensor
+pointers, sizes and the current CUDA stream; holds no arithmetic.
+
+Method: VeloxQuant-MLX changelog v0.8.0 "New" (KIVI cache with an fp16
+residual window) and v0.42.0 "Added" (fused decode-attend over the
+group-affine cache).
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib
+
+PLANES = ("Kc", "Ks", "Kz", "Vc", "Vs", "Vz", "Kr", "Vr")
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev_ptr(t: torch.Tensor, dtype: torch.dtype, name: str) -> ctypes.c_void_p:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _i32_array(xs: Sequence[int]):
+    arr = (ctypes.c_int32 * len(xs))(*[int(x) for x in xs])
+    return arr
+
+
+class KiviCache:
+    """A KIVI cache on the current CUDA device.
+
+    K, V: fp16 CUDA tensors [B][H_kv][S_stride][D]; seq_lens: B ints.
+    """
+
+    def __init__(self, K: torch.Tensor, V: torch.Tensor, seq_lens, *, H_q: int,
+                 bits: int, group: int, residual: int,
+                 max_seq: Optional[int] = None,
+                 stream: Optional[torch.cuda.Stream] = None):
+        L = _lib.load()
+        if K.shape != V.shape or K.dim() != 4:
+            raise ValueError("K and V must both be [B][H_kv][S][D]")
+        B, H_kv, S_stride, D = K.shape
+        lens = [int(x) for x in seq_lens]
+        if len(lens) != B:
+            raise ValueError("seq_lens must have B entries")
+        self.params = _lib.Params(B, H_q, H_kv, D, bits, group, residual,
+                                  max(lens + [0]) if max_seq is None else max_seq)
+        self.B, self.H_q, self.H_kv, self.D = B, H_q, H_kv, D
+        self.bits, self.group, self.residual = bits, group, residual
+        self.max_seq = self.params.max_seq
+        self._h = ctypes.c_void_p()
+        kp = _dev_ptr(K, torch.float16, "K")
+        vp = _dev_ptr(V, torch.float16, "V")
+        _lib.check(L.vq_kivi_quantize(ctypes.byref(self.params), kp, vp,
+                                      S_stride, _i32_array(lens),
+                                      _stream_handle(stream),
+                                      ctypes.byref(self._h)))
+        self.device = K.device
+
+    # -- steps ---------------------------------------------------------------
+
+    def append(self, K_new: torch.Tensor, V_new: torch.Tensor, n_new,
+               stream: Optional[torch.cuda.Stream] = None):
+        n = [int(x) for x in n_new]
+        if len(n) != self.B:
+            raise ValueError("n_new must have B entries")
+        if K_new.shape != V_new.shape or K_new.dim() != 4:
+            raise ValueError("K_new and V_new must both be [B][H_kv][N][D]")
+        _lib.check(_lib.load().vq_kivi_append(
+            self._h, _dev_ptr(K_new, torch.float16, "K_new"),
+            _dev_ptr(V_new, torch.float16, "V_new"), K_new.shape[2],
+            _i32_array(n), _stream_handle(stream)))
+
+    def decode_attend(self, q: torch.Tensor, out: Optional[torch.Tensor] = None,
+                      scale: float = 0.0,
+                      stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+        if tuple(q.shape) != (self.B, self.H_q, self.D):
+            raise ValueError(f"q must be [{self.B}][{self.H_q}][{self.D}]")
+        if out is None:
+            out = torch.empty((self.B, self.H_q, self.D), dtype=torch.float32,
+                              device=q.device)
+        _lib.check(_lib.load().vq_kivi_decode_attend(
+            self._h, _dev_ptr(q, torch.float16, "q"),
+            _dev_ptr(out, torch.float32, "out"), float(scale),
+            _stream_handle(stream)))
+        return out
+
+    # -- inspection ------------------------------------------------------------
+
+    def lengths(self):
+        S = (ctypes.c_int32 * self.B)()
+        Tq = (ctypes.c_int32 * self.B)()
+        nres = (ctypes.c_int32 * self.B)()
+        _lib.check(_lib.load().vq_kivi_lengths(self._h, S, Tq, nres))
+        return list(S), list(Tq), list(nres)
+
+    def plane_bytes(self, name: str) -> int:
+        return int(_lib.load().vq_kivi_plane_bytes(self._h, PLANES.index(name)))
+
+    def export(self, name: str, stream: Optional[torch.cuda.Stream] = None):
+        """Canonical plane as a CUDA tensor (layouts in include/vq_kivi.h)."""
+        which = PLANES.index(name)
+        nbytes = self.plane_bytes(name)
+        raw = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        _lib.check(_lib.load().vq_kivi_export(
+            self._h, which, ctypes.c_void_p(raw.data_ptr()), nbytes,
+            _stream_handle(stream)))
+        B, H, D, g = self.B, self.H_kv, self.D, self.group
+        row = D * self.bits // 8
+        if name in ("Kc", "Vc"):
+            return raw.view(B, H, -1, row)
+        raw = raw.view(torch.float16)
+        if name in ("Ks", "Kz"):
+            return raw.view(B, H, -1, D)
+        if name in ("Vs", "Vz"):
+            return raw.view(B, H, -1, D // g)
+        return raw.view(B, H, -1, D)
+
+    def cache_bytes(self) -> dict:
+        b = _lib.Bytes()
+        _lib.check(_lib.load().vq_kivi_cache_bytes(self._h, ctypes.byref(b)))
+        return {n: int(getattr(b, n)) for n, _ in _lib.Bytes._fields_}
+
+    def set_split_tokens(self, n: int):
+        _lib.check(_lib.load().vq_kivi_set_split_tokens(self._h, int(n)))
+
+    # -- lifetime ------------------------------------------------------------
+
+    def close(self):
+        if self._h:
+            rc = _lib.load().vq_kivi_free(self._h)
+            self._h = ctypes.c_void_p()
+            _lib.check(rc)
+
+    def __del__(self):
+        try:
+            if getattr(self, "_h", None):
+                self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()

@@ -1,0 +1,447 @@
+// C ABI of the KIVI cache: argument checks, the cache handle, device memory
+// and the launch sequence of each call.  See include/vq_kivi.h.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "vqk_internal.cuh"
+
+using namespace vqk;
+
+struct vq_kivi_cache {
+  vq_kivi_params p;
+  Geometry geo;
+  Planes pl;
+  void *block;
+  size_t block_bytes;
+  int device;
+  int sm_count;
+  cudaStream_t last_stream;
+  int32_t split_tokens;   // 0 = automatic
+  int32_t tps_min;        // smallest split the workspace allows
+  int32_t S[kMaxB], Tq[kMaxB], nres[kMaxB];
+};
+
+namespace {
+
+thread_local std::string g_err;
+std::atomic<uint64_t> g_launches{0};
+
+int fail(int code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+  return fail(VQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, size_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+int32_t n_quantized(int32_t S, int32_t R, int32_t g) {
+  if (S < R) return 0;
+  return g * ((S - R) / g);
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int check_params(const vq_kivi_params *p) {
+  if (!p) return fail(VQ_ERR_ARG, "params is NULL");
+  if (p->B < 1 || p->H_q < 1 || p->H_kv < 1 || p->D < 1 || p->group < 1 ||
+      p->residual < 0 || p->max_seq < 0)
+    return fail(VQ_ERR_ARG, "params: sizes must be positive (B=%d H_q=%d "
+                "H_kv=%d D=%d group=%d residual=%d max_seq=%d)", p->B, p->H_q,
+                p->H_kv, p->D, p->group, p->residual, p->max_seq);
+  if (p->B > kMaxB) return fail(VQ_ERR_UNSUPPORTED, "B=%d > %d", p->B, kMaxB);
+  if (p->H_q % p->H_kv != 0)
+    return fail(VQ_ERR_UNSUPPORTED, "H_q=%d is not a multiple of H_kv=%d",
+                p->H_q, p->H_kv);
+  if (p->H_q / p->H_kv > kMaxGroupHeads)
+    return fail(VQ_ERR_UNSUPPORTED, "H_q/H_kv=%d > %d", p->H_q / p->H_kv,
+                kMaxGroupHeads);
+  if (p->D != 64 && p->D != 128 && p->D != 256)
+    return fail(VQ_ERR_UNSUPPORTED, "D=%d (supported: 64, 128, 256)", p->D);
+  if (p->bits != 2 && p->bits != 4 && p->bits != 8)
+    return fail(VQ_ERR_UNSUPPORTED, "bits=%d (supported: 2, 4, 8)", p->bits);
+  if (p->group != 16 && p->group != 32 && p->group != 64 && p->group != 128)
+    return fail(VQ_ERR_UNSUPPORTED, "group=%d (supported: 16, 32, 64, 128)",
+                p->group);
+  if (p->D % p->group != 0)
+    return fail(VQ_ERR_UNSUPPORTED, "group=%d does not divide D=%d", p->group,
+                p->D);
+  if (p->residual > 4096)
+    return fail(VQ_ERR_UNSUPPORTED, "residual=%d > 4096", p->residual);
+  if (p->max_seq > (1 << 24))
+    return fail(VQ_ERR_UNSUPPORTED, "max_seq=%d > 2^24", p->max_seq);
+  return VQ_OK;
+}
+
+int check_cache(const vq_kivi_cache *c) {
+  if (!c) return fail(VQ_ERR_ARG, "cache is NULL");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != c->device)
+    return fail(VQ_ERR_ARG, "cache lives on device %d, current device is %d",
+                c->device, dev);
+  return VQ_OK;
+}
+
+// Split unit: a multiple of the key group and of 64 tokens.
+int32_t split_unit(int g) { return g > 64 ? g : 64; }
+
+}  // namespace
+
+namespace vqk {
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n); }
+}  // namespace vqk
+
+extern "C" {
+
+const char *vq_kivi_last_error(void) { return g_err.c_str(); }
+
+uint64_t vq_kivi_launch_count(void) { return g_launches.load(); }
+
+int vq_kivi_quantize(const vq_kivi_params *p, const void *K, const void *V,
+                     int64_t s_stride, const int32_t *seq_lens, void *stream,
+                     vq_kivi_cache **out) {
+  int rc = check_params(p);
+  if (rc) return rc;
+  if (!out) return fail(VQ_ERR_ARG, "out is NULL");
+  if (!seq_lens) return fail(VQ_ERR_ARG, "seq_lens is NULL");
+  int32_t smax = 0;
+  for (int b = 0; b < p->B; ++b) {
+    if (seq_lens[b] < 0 || seq_lens[b] > p->max_seq)
+      return fail(seq_lens[b] < 0 ? VQ_ERR_ARG : VQ_ERR_CAPACITY,
+                  "seq_lens[%d]=%d outside [0, max_seq=%d]", b, seq_lens[b],
+                  p->max_seq);
+    smax = seq_lens[b] > smax ? seq_lens[b] : smax;
+  }
+  if (smax > 0) {
+    if (!K || !V) return fail(VQ_ERR_ARG, "K or V is NULL");
+    if (s_stride < smax)
+      return fail(VQ_ERR_ARG, "s_stride=%lld < longest sequence %d",
+                  (long long)s_stride, smax);
+    if (!aligned(K, 16) || !aligned(V, 16))
+      return fail(VQ_ERR_ARG, "K and V must be 16-byte aligned");
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+
+  vq_kivi_cache *c = new (std::nothrow) vq_kivi_cache();
+  if (!c) return fail(VQ_ERR_OOM, "host allocation of the cache handle failed");
+  c->p = *p;
+  cudaError_t e = cudaGetDevice(&c->device);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount,
+                               c->device);
+  if (e != cudaSuccess) {
+    delete c;
+    return cuda_fail(e, "device query");
+  }
+
+  Geometry &geo = c->geo;
+  const int g = p->group;
+  geo.B = p->B; geo.H_q = p->H_q; geo.H_kv = p->H_kv; geo.D = p->D;
+  geo.bits = p->bits; geo.g = g; geo.R = p->residual;
+  geo.Tcap = (int)round_up(p->max_seq > 0 ? p->max_seq : 1, g);
+  geo.Rcap = p->residual + g;
+  geo.row = p->D * p->bits / 8;
+  const int32_t unit = split_unit(g);
+  const int32_t tps_for_cap = (int32_t)round_up((geo.Tcap + 1023) / 1024, unit);
+  c->tps_min = tps_for_cap > 256 ? tps_for_cap : 256;
+  geo.max_items = (geo.Tcap + c->tps_min - 1) / c->tps_min + 1;
+
+  const size_t BH = (size_t)p->B * p->H_kv;
+  const size_t sz_codes = BH * geo.Tcap * geo.row;
+  const size_t sz_kmeta = BH * (geo.Tcap / g) * p->D * sizeof(__half);
+  const size_t sz_vmeta = BH * geo.Tcap * (p->D / g) * sizeof(__half);
+  const size_t sz_res = BH * geo.Rcap * p->D * sizeof(__half);
+  const size_t sz_part =
+      (size_t)p->B * p->H_q * geo.max_items * (p->D + 2) * sizeof(float);
+  const size_t A = 256;
+  size_t off = 0;
+  size_t o_Kc = off; off += round_up(sz_codes, A);
+  size_t o_Vc = off; off += round_up(sz_codes, A);
+  size_t o_Ks = off; off += round_up(sz_kmeta, A);
+  size_t o_Kz = off; off += round_up(sz_kmeta, A);
+  size_t o_Vs = off; off += round_up(sz_vmeta, A);
+  size_t o_Vz = off; off += round_up(sz_vmeta, A);
+  size_t o_Kr = off; off += round_up(sz_res, A);
+  size_t o_Vr = off; off += round_up(sz_res, A);
+  size_t o_part = off; off += round_up(sz_part, A);
+  c->block_bytes = off;
+
+  e = cudaMallocAsync(&c->block, c->block_bytes, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    delete c;
+    return fail(VQ_ERR_OOM, "cudaMallocAsync(%zu bytes): %s", off,
+                cudaGetErrorString(e));
+  }
+  uint8_t *base = (uint8_t *)c->block;
+  Planes &pl = c->pl;
+  pl.Kc = base + o_Kc;
+  pl.Vc = base + o_Vc;
+  pl.Ks = (__half *)(base + o_Ks);
+  pl.Kz = (__half *)(base + o_Kz);
+  pl.Vs = (__half *)(base + o_Vs);
+  pl.Vz = (__half *)(base + o_Vz);
+  pl.Kr = (__half *)(base + o_Kr);
+  pl.Vr = (__half *)(base + o_Vr);
+  pl.part = (float *)(base + o_part);
+  c->last_stream = st;
+
+  auto abort_create = [&](cudaError_t err, const char *what) {
+    cudaFreeAsync(c->block, st);
+    cudaStreamSynchronize(st);
+    delete c;
+    return cuda_fail(err, what);
+  };
+
+  // planes start zeroed so that exported padding is deterministic
+  e = cudaMemsetAsync(c->block, 0, o_part, st);
+  if (e != cudaSuccess) return abort_create(e, "cudaMemsetAsync");
+
+  FlushTable ft;
+  TailTable tt;
+  ft.prefix[0] = 0;
+  tt.prefix[0] = 0;
+  for (int b = 0; b < p->B; ++b) {
+    const int32_t S = seq_lens[b];
+    const int32_t Tq = n_quantized(S, p->residual, g);
+    c->S[b] = S; c->Tq[b] = Tq; c->nres[b] = S - Tq;
+    ft.prefix[b + 1] = ft.prefix[b] + Tq / g;
+    ft.first_pos[b] = 0;
+    ft.src_split[b] = 0;
+    tt.prefix[b + 1] = tt.prefix[b] + (S - Tq);
+    tt.row0[b] = Tq;
+    tt.pos0[b] = Tq;
+  }
+  e = launch_flush(geo, pl, (const __half *)K, (const __half *)V, s_stride, ft,
+                   ft.prefix[p->B], st);
+  if (e != cudaSuccess) return abort_create(e, "quantize kernel launch");
+  e = launch_tail(geo, pl, (const __half *)K, (const __half *)V, s_stride, tt,
+                  tt.prefix[p->B], st);
+  if (e != cudaSuccess) return abort_create(e, "residual kernel launch");
+  *out = c;
+  return VQ_OK;
+}
+
+int vq_kivi_append(vq_kivi_cache *c, const void *K_new, const void *V_new,
+                   int64_t n_stride, const int32_t *n_new, void *stream) {
+  int rc = check_cache(c);
+  if (rc) return rc;
+  if (!n_new) return fail(VQ_ERR_ARG, "n_new is NULL");
+  const vq_kivi_params &p = c->p;
+  int32_t nmax = 0;
+  for (int b = 0; b < p.B; ++b) {
+    if (n_new[b] < 0) return fail(VQ_ERR_ARG, "n_new[%d]=%d < 0", b, n_new[b]);
+    if ((int64_t)c->S[b] + n_new[b] > p.max_seq)
+      return fail(VQ_ERR_CAPACITY, "sequence %d: %d + %d tokens > max_seq=%d",
+                  b, c->S[b], n_new[b], p.max_seq);
+    nmax = n_new[b] > nmax ? n_new[b] : nmax;
+  }
+  if (nmax == 0) return VQ_OK;
+  if (!K_new || !V_new) return fail(VQ_ERR_ARG, "K_new or V_new is NULL");
+  if (n_stride < nmax)
+    return fail(VQ_ERR_ARG, "n_stride=%lld < largest n_new %d",
+                (long long)n_stride, nmax);
+  if (!aligned(K_new, 16) || !aligned(V_new, 16))
+    return fail(VQ_ERR_ARG, "K_new and V_new must be 16-byte aligned");
+  cudaStream_t st = (cudaStream_t)stream;
+  const int g = p.group;
+
+  FlushTable ft;
+  TailTable tt;
+  int32_t Tq_new[kMaxB];
+  ft.prefix[0] = 0;
+  tt.prefix[0] = 0;
+  for (int b = 0; b < p.B; ++b) {
+    const int32_t S_old = c->S[b], S_new = S_old + n_new[b];
+    Tq_new[b] = n_quantized(S_new, p.residual, g);
+    ft.prefix[b + 1] = ft.prefix[b] + (Tq_new[b] - c->Tq[b]) / g;
+    ft.first_pos[b] = c->Tq[b];
+    ft.src_split[b] = S_old;
+    const int32_t keep0 = S_old > Tq_new[b] ? S_old : Tq_new[b];
+    tt.prefix[b + 1] = tt.prefix[b] + (S_new - keep0);
+    tt.row0[b] = keep0 - S_old;
+    tt.pos0[b] = keep0;
+  }
+  cudaError_t e = launch_flush(c->geo, c->pl, (const __half *)K_new,
+                               (const __half *)V_new, n_stride, ft,
+                               ft.prefix[p.B], st);
+  if (e != cudaSuccess) return cuda_fail(e, "flush kernel launch");
+  e = launch_tail(c->geo, c->pl, (const __half *)K_new, (const __half *)V_new,
+                  n_stride, tt, tt.prefix[p.B], st);
+  if (e != cudaSuccess) return cuda_fail(e, "residual kernel launch");
+  for (int b = 0; b < p.B; ++b) {
+    c->S[b] += n_new[b];
+    c->Tq[b] = Tq_new[b];
+    c->nres[b] = c->S[b] - Tq_new[b];
+  }
+  c->last_stream = st;
+  return VQ_OK;
+}
+
+int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
+                          float softmax_scale, void *stream) {
+  int rc = check_cache(c);
+  if (rc) return rc;
+  if (!q || !out) return fail(VQ_ERR_ARG, "q or out is NULL");
+  if (!aligned(q, 16) || !aligned(out, 16))
+    return fail(VQ_ERR_ARG, "q and out must be 16-byte aligned");
+  if (!std::isfinite(softmax_scale))
+    return fail(VQ_ERR_ARG, "softmax_scale is not finite");
+  const vq_kivi_params &p = c->p;
+  cudaStream_t st = (cudaStream_t)stream;
+
+  int64_t total_tq = 0;
+  for (int b = 0; b < p.B; ++b) total_tq += c->Tq[b];
+  int32_t tps = c->split_tokens;
+  const int32_t unit = split_unit(p.group);
+  if (tps == 0) {
+    const int64_t target_items = 4LL * c->sm_count;
+    int64_t t = (total_tq * p.H_kv + target_items - 1) / target_items;
+    tps = (int32_t)round_up((size_t)(t > 1 ? t : 1), unit);
+  }
+  if (tps < c->tps_min) tps = c->tps_min;
+
+  DecodeTable tab;
+  tab.prefix[0] = 0;
+  for (int b = 0; b < p.B; ++b) {
+    tab.Tq[b] = c->Tq[b];
+    tab.nres[b] = c->nres[b];
+    tab.nq[b] = (c->Tq[b] + tps - 1) / tps;
+    tab.prefix[b + 1] = tab.prefix[b] + tab.nq[b] + (c->nres[b] > 0 ? 1 : 0);
+  }
+  DecodeArgs args;
+  args.q = (const __half *)q;
+  args.out = out;
+  const float scale = softmax_scale > 0.f ? softmax_scale
+                                          : 1.0f / std::sqrt((float)p.D);
+  args.scale_log2 = scale * 1.4426950408889634f;
+  args.tps = tps;
+  args.total_items = tab.prefix[p.B];
+  cudaError_t e = launch_decode(c->geo, c->pl, args, tab, st);
+  if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+  c->last_stream = st;
+  return VQ_OK;
+}
+
+int vq_kivi_free(vq_kivi_cache *c) {
+  if (!c) return VQ_OK;
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (dev != c->device) cudaSetDevice(c->device);
+  cudaError_t e = cudaFreeAsync(c->block, c->last_stream);
+  cudaError_t e2 = cudaStreamSynchronize(c->last_stream);
+  if (dev != c->device && dev >= 0) cudaSetDevice(dev);
+  delete c;
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaStreamSynchronize");
+  return VQ_OK;
+}
+
+int vq_kivi_lengths(const vq_kivi_cache *c, int32_t *S, int32_t *T_q,
+                    int32_t *n_res) {
+  if (!c) return fail(VQ_ERR_ARG, "cache is NULL");
+  const size_t n = sizeof(int32_t) * c->p.B;
+  if (S) memcpy(S, c->S, n);
+  if (T_q) memcpy(T_q, c->Tq, n);
+  if (n_res) memcpy(n_res, c->nres, n);
+  return VQ_OK;
+}
+
+int vq_kivi_get_params(const vq_kivi_cache *c, vq_kivi_params *p) {
+  if (!c || !p) return fail(VQ_ERR_ARG, "NULL argument");
+  *p = c->p;
+  return VQ_OK;
+}
+
+size_t vq_kivi_plane_bytes(const vq_kivi_cache *c, int which) {
+  if (!c) return 0;
+  const Geometry &geo = c->geo;
+  const size_t BH = (size_t)geo.B * geo.H_kv;
+  switch (which) {
+    case 0: case 3: return BH * geo.Tcap * geo.row;
+    case 1: case 2: return BH * (geo.Tcap / geo.g) * geo.D * sizeof(__half);
+    case 4: case 5: return BH * geo.Tcap * (geo.D / geo.g) * sizeof(__half);
+    case 6: case 7: return BH * geo.Rcap * geo.D * sizeof(__half);
+    default: return 0;
+  }
+}
+
+int vq_kivi_export(const vq_kivi_cache *c, int which, void *dst,
+                   size_t dst_bytes, void *stream) {
+  int rc = check_cache(c);
+  if (rc) return rc;
+  const size_t need = vq_kivi_plane_bytes(c, which);
+  if (need == 0) return fail(VQ_ERR_ARG, "which=%d is not a plane", which);
+  if (!dst) return fail(VQ_ERR_ARG, "dst is NULL");
+  if (dst_bytes < need)
+    return fail(VQ_ERR_ARG, "dst holds %zu bytes, plane needs %zu", dst_bytes,
+                need);
+  cudaStream_t st = (cudaStream_t)stream;
+  const void *src = nullptr;
+  switch (which) {
+    case 0: src = c->pl.Kc; break;
+    case 1: src = c->pl.Ks; break;
+    case 2: src = c->pl.Kz; break;
+    case 3: src = c->pl.Vc; break;
+    case 4: src = c->pl.Vs; break;
+    case 5: src = c->pl.Vz; break;
+    default: break;
+  }
+  cudaError_t e;
+  if (src) {
+    e = cudaMemcpyAsync(dst, src, need, cudaMemcpyDeviceToDevice, st);
+  } else {
+    e = launch_export_residual(c->geo, c->pl, which, dst, c->Tq, c->nres, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "export");
+  return VQ_OK;
+}
+
+int vq_kivi_cache_bytes(const vq_kivi_cache *c, vq_kivi_bytes *out) {
+  if (!c || !out) return fail(VQ_ERR_ARG, "NULL argument");
+  const vq_kivi_params &p = c->p;
+  const uint64_t row = (uint64_t)c->geo.row;
+  vq_kivi_bytes r = {0, 0, 0, 0};
+  for (int b = 0; b < p.B; ++b) {
+    const uint64_t Tq = (uint64_t)c->Tq[b], H = (uint64_t)p.H_kv;
+    r.code_bytes += 2 * H * Tq * row;
+    r.meta_bytes += H * ((Tq / p.group) * p.D * 4 + Tq * (p.D / p.group) * 4);
+    r.residual_bytes += H * (uint64_t)c->nres[b] * p.D * 4;
+    r.fp16_bytes += H * (uint64_t)c->S[b] * p.D * 4;
+  }
+  *out = r;
+  return VQ_OK;
+}
+
+int vq_kivi_set_split_tokens(vq_kivi_cache *c, int32_t tokens_per_split) {
+  if (!c) return fail(VQ_ERR_ARG, "cache is NULL");
+  if (tokens_per_split != 0) {
+    const int32_t unit = split_unit(c->p.group);
+    if (tokens_per_split < 64 || tokens_per_split % unit != 0)
+      return fail(VQ_ERR_ARG, "tokens_per_split=%d must be a positive "
+                  "multiple of %d", tokens_per_split, unit);
+    if (tokens_per_split < c->tps_min)
+      return fail(VQ_ERR_ARG, "tokens_per_split=%d below the workspace "
+                  "minimum %d for this capacity", tokens_per_split, c->tps_min);
+  }
+  c->split_tokens = tokens_per_split;
+  return VQ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,95 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "vq_kivi.h"
+
+namespace vqk {
+
+constexpr int kMaxB = 256;        // sequences per cache
+constexpr int kMaxGroupHeads = 8; // H_q / H_kv
+constexpr int kMaxD = 256;
+
+// Device memory of one cache, carved from a single cudaMallocAsync block.
+struct Planes {
+  uint8_t *Kc, *Vc;          // [B][H_kv][Tcap][row]        packed codes
+  __half *Ks, *Kz;           // [B][H_kv][Tcap/g][D]        key scale / zero
+  __half *Vs, *Vz;           // [B][H_kv][Tcap][D/g]        value scale / zero
+  __half *Kr, *Vr;           // [B][H_kv][Rcap][D]          residual ring
+  float *part;               // [B][H_q][max_items][D+2]    split partials
+};
+
+struct Geometry {
+  int B, H_q, H_kv, D, bits, g, R;
+  int Tcap;   // quantized-token capacity per sequence (multiple of g)
+  int Rcap;   // residual ring slots per sequence (R + g)
+  int row;    // packed bytes per token row (D*bits/8)
+  int max_items;  // decode work items per sequence (quantized splits + 1)
+};
+
+// ---- quantize / flush ------------------------------------------------------
+
+// One launch quantizes whole groups of g tokens of every (b, h).  Group k of
+// sequence b (k in [0, n_groups[b])) covers token positions
+// first_pos[b] + k*g ... + g-1.  Token position p of sequence b is read from
+// the residual ring (slot p % Rcap) when p < src_split[b], otherwise from row
+// p - src_split[b] of the input block [b][h] (stride in_stride rows).
+struct FlushTable {
+  int32_t prefix[kMaxB + 1];  // group-item prefix sums over b
+  int32_t first_pos[kMaxB];
+  int32_t src_split[kMaxB];
+};
+
+// Copy of input rows into the residual ring: for sequence b, input rows
+// [row0[b], row0[b] + count[b]) go to token positions pos0[b] + i, stored at
+// ring slot (pos0[b] + i) % Rcap.
+struct TailTable {
+  int32_t prefix[kMaxB + 1];  // token prefix sums over b
+  int32_t row0[kMaxB];
+  int32_t pos0[kMaxB];
+};
+
+cudaError_t launch_flush(const Geometry &geo, const Planes &pl,
+                         const __half *Kin, const __half *Vin,
+                         int64_t in_stride, const FlushTable &tab,
+                         int total_groups, cudaStream_t st);
+cudaError_t launch_tail(const Geometry &geo, const Planes &pl,
+                        const __half *Kin, const __half *Vin,
+                        int64_t in_stride, const TailTable &tab,
+                        int total_tokens, cudaStream_t st);
+cudaError_t launch_export_residual(const Geometry &geo, const Planes &pl,
+                                   int which, void *dst, const int32_t *Tq,
+                                   const int32_t *nres, cudaStream_t st);
+
+// ---- decode ----------------------------------------------------------------
+
+// Work list of one decode: for sequence b, items prefix[b] ... prefix[b+1]-1;
+// local item k < nq[b] covers quantized tokens [k*tps, min((k+1)*tps, Tq[b])),
+// local item k == nq[b] (present when nres[b] > 0) covers the residual.
+struct DecodeTable {
+  int32_t prefix[kMaxB + 1];
+  int32_t Tq[kMaxB];
+  int32_t nres[kMaxB];
+  int32_t nq[kMaxB];
+};
+
+struct DecodeArgs {
+  const __half *q;  // [B][H_q][D]
+  float *out;       // [B][H_q][D]
+  float scale_log2; // softmax scale * log2(e)
+  int tps;          // quantized tokens per split item
+  int total_items;
+};
+
+cudaError_t launch_decode(const Geometry &geo, const Planes &pl,
+                          const DecodeArgs &args, const DecodeTable &tab,
+                          cudaStream_t st);
+
+// counts every kernel launch made by the library
+void count_launch(int n = 1);
+
+}  // namespace vqk

@@ -1,0 +1,178 @@
+/*
+ * vq_kivi.h -- C ABI of a KIVI-style 2/4/8-bit KV cache with a fused decode
+ * step, for NVIDIA GB300 (sm_103a).
+ *
+ * The method (VeloxQuant-MLX pages):
+ *  - Changelog v0.8.0 "New", KIVI: asymmetric group quantization with keys
+ *    grouped per channel and values per token, an fp16 residual window
+ *    (`residual_length`) and a group size (`kivi_group_size`).
+ *  - Changelog v0.42.0 "Added", scalar_fused_decode_attend: attention runs
+ *    directly over the quantized cache; k_hat / v_hat are rebuilt in
+ *    registers inside a FlashAttention-style online softmax with fp32
+ *    accumulation, so no dequantized K/V is ever written to memory.
+ *  - Changelog v0.28.0: the residual is flushed in whole chunks and prefill
+ *    and decode give the same quantized state.
+ *  - veloxquant_mlx.cache API, KVCacheConfig fields residual_length
+ *    (default 128) and kivi_group_size (default 32).
+ *
+ * Quantization (per group of g values x, fp32 arithmetic, IEEE rounding):
+ *   scale = (max(x) - min(x)) / (2^b - 1)
+ *   code  = scale == 0 ? 0 : clamp(rint((x - min(x)) / scale), 0, 2^b - 1)
+ *   stored scale = fp16 round-to-nearest-even of scale; stored zero = min(x)
+ * Keys: a group is g consecutive tokens of one channel.  Values: a group is
+ * g consecutive channels of one token.  Dequantized value: code*scale + zero.
+ *
+ * Residual rule: a sequence of S tokens keeps its newest n_res tokens in
+ * fp16 and the older T_q = S - n_res tokens quantized, where
+ *   T_q = (S < R) ? 0 : g * floor((S - R) / g),   so R <= n_res < R + g
+ * (or n_res = S when S < R).  Appends flush whole groups of g tokens.
+ *
+ * Decode (S_q = 1, no mask): for query head h (kv head h / (H_q/H_kv)),
+ *   out[b][h] = sum_t softmax_t(scale * q[b][h] . k_hat_t) * v_hat_t
+ * over every token t of sequence b, quantized and residual; fp32 result.
+ * Empty sequences give an all-zero output row.
+ *
+ * Conventions for every entry point:
+ *  - Device pointers are addresses in the memory of the CUDA device that is
+ *    current on the calling thread; a cache must be used on the device that
+ *    created it.  Host pointers are ordinary process memory.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *    are asynchronous and stream-ordered; nothing synchronizes the device
+ *    except vq_kivi_free (see there).  A cache must not be used from two
+ *    streams at once.
+ *  - Every call returns a status: VQ_OK (0) or a negative VQ_ERR_* code.  A
+ *    failing call leaves the cache as it was (except VQ_ERR_CUDA from an
+ *    asynchronous fault, after which the cache contents are undefined).
+ *    vq_kivi_last_error() gives a message for the last failure on the
+ *    calling thread.  No call throws, aborts or traps.
+ */
+#ifndef VQ_KIVI_H
+#define VQ_KIVI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define VQ_OK 0
+#define VQ_ERR_ARG (-1)         /* null pointer, negative size, bad length */
+#define VQ_ERR_UNSUPPORTED (-2) /* a shape or bit width the kernels lack */
+#define VQ_ERR_CAPACITY (-3)    /* a sequence would exceed max_seq */
+#define VQ_ERR_OOM (-4)         /* device or host allocation failed */
+#define VQ_ERR_CUDA (-5)        /* a CUDA runtime call or launch failed */
+
+/* Problem statement (changelog v0.42.0 workload: B, H, D, b, g, S_q=1, S_kv;
+ * KVCacheConfig residual_length, kivi_group_size).
+ *   B        batch (sequences), 1 <= B <= 256
+ *   H_q      query heads; H_q % H_kv == 0, H_q / H_kv <= 8
+ *   H_kv     key/value heads
+ *   D        head dimension: 64, 128 or 256
+ *   bits     code width: 2, 4 or 8
+ *   group    g: 16, 32, 64 or 128, dividing D
+ *   residual R: fp16 window, 0 <= R <= 4096
+ *   max_seq  capacity in tokens per sequence, >= 0 */
+typedef struct vq_kivi_params {
+  int32_t B, H_q, H_kv, D, bits, group, residual, max_seq;
+} vq_kivi_params;
+
+/* Opaque cache handle.  It owns (device memory, from cudaMallocAsync on the
+ * creating stream) the packed code planes, the fp16 scale/zero planes, the
+ * fp16 residual ring and the split-KV workspace, and (host memory) the
+ * per-sequence lengths, so no call needs a device-to-host read. */
+typedef struct vq_kivi_cache vq_kivi_cache;
+
+/* Prefill: build a cache from K, V and quantize each sequence's old tokens.
+ * (Changelog v0.8.0 KIVI; the residual rule above.)
+ *   p         parameters (host)
+ *   K, V      device, fp16, [B][H_kv][s_stride][D] row-major; sequence b
+ *             uses rows [0, seq_lens[b]) of its (b, h) block
+ *   s_stride  rows per (b, h) block, >= max(seq_lens)
+ *   seq_lens  host int32[B], 0 <= seq_lens[b] <= max_seq
+ *   stream    cudaStream_t
+ *   out       receives the new handle (unchanged on failure)
+ * K and V are read by kernels on `stream`; keep them alive until then. */
+int vq_kivi_quantize(const vq_kivi_params *p, const void *K, const void *V,
+                     int64_t s_stride, const int32_t *seq_lens, void *stream,
+                     vq_kivi_cache **out);
+
+/* Append n_new[b] tokens to sequence b: push them onto the fp16 residual and
+ * flush the oldest whole groups so that the residual rule holds again
+ * (changelog v0.8.0 update_and_fetch; v0.28.0 chunk-flush).  The result is
+ * bit-identical to a prefill of the whole sequence.
+ *   K_new, V_new  device, fp16, [B][H_kv][n_stride][D]; rows [0, n_new[b])
+ *   n_new         host int32[B], >= 0, S + n_new[b] <= max_seq
+ * Returns VQ_ERR_CAPACITY (cache unchanged) if a sequence would overflow. */
+int vq_kivi_append(vq_kivi_cache *c, const void *K_new, const void *V_new,
+                   int64_t n_stride, const int32_t *n_new, void *stream);
+
+/* Fused decode step over the quantized cache (changelog v0.42.0,
+ * scalar_fused_decode_attend): split-KV online softmax rebuilding k_hat and
+ * v_hat in registers, then a log-sum-exp merge of the splits.
+ *   q              device, fp16, [B][H_q][D]  (one query token per sequence)
+ *   out            device, fp32, [B][H_q][D]
+ *   softmax_scale  <= 0 selects 1/sqrt(D)
+ * Uses the cache's split workspace: one decode per cache in flight. */
+int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
+                          float softmax_scale, void *stream);
+
+/* Release the cache.  NULL is accepted.  Frees are stream-ordered on the
+ * stream of the last call that used the cache, then that stream is
+ * synchronized, so the handle's memory is gone when this returns. */
+int vq_kivi_free(vq_kivi_cache *c);
+
+/* ---- helpers ----------------------------------------------------------- */
+
+/* Message of the last failure on the calling thread ("" if none).  The
+ * string stays valid until the thread's next failing call. */
+const char *vq_kivi_last_error(void);
+
+/* Host copies of the per-sequence lengths: S (tokens), T_q (quantized),
+ * n_res (fp16 residual).  Each pointer may be NULL; else int32[B]. */
+int vq_kivi_lengths(const vq_kivi_cache *c, int32_t *S, int32_t *T_q,
+                    int32_t *n_res);
+
+/* The cache's parameters (host copy). */
+int vq_kivi_get_params(const vq_kivi_cache *c, vq_kivi_params *p);
+
+/* Canonical planes, for parity checks and inspection.  `which`:
+ *   0 Kc  uint8 [B][H_kv][Tcap][D*bits/8]  key codes, LSB-first packing:
+ *         code of channel e at byte e*bits/8, bit (e*bits) mod 8
+ *   1 Ks  fp16  [B][H_kv][Tcap/g][D]       key scales (per channel, group)
+ *   2 Kz  fp16  [B][H_kv][Tcap/g][D]       key zeros
+ *   3 Vc  uint8 [B][H_kv][Tcap][D*bits/8]  value codes, same packing
+ *   4 Vs  fp16  [B][H_kv][Tcap][D/g]       value scales (per token, group)
+ *   5 Vz  fp16  [B][H_kv][Tcap][D/g]       value zeros
+ *   6 Kr  fp16  [B][H_kv][R+g][D]          residual keys, slot i = token T_q+i
+ *   7 Vr  fp16  [B][H_kv][R+g][D]          residual values
+ * where Tcap = ceil(max_seq/g)*g (at least g).  vq_kivi_plane_bytes gives
+ * the size (0 for a bad `which`); vq_kivi_export writes the whole plane to
+ * device memory `dst` of at least that size, on `stream`.  Only the valid
+ * rows (tokens < T_q, slots < n_res) are defined. */
+size_t vq_kivi_plane_bytes(const vq_kivi_cache *c, int which);
+int vq_kivi_export(const vq_kivi_cache *c, int which, void *dst,
+                   size_t dst_bytes, void *stream);
+
+/* Bytes held, per the cache's byte accounting (changelog v0.8.0 "full
+ * byte-accounting"): packed codes, fp16 scale/zero metadata and the fp16
+ * residual, over the tokens currently stored (not the capacity), and the
+ * fp16 size of the same tokens for comparison. */
+typedef struct vq_kivi_bytes {
+  uint64_t code_bytes, meta_bytes, residual_bytes, fp16_bytes;
+} vq_kivi_bytes;
+int vq_kivi_cache_bytes(const vq_kivi_cache *c, vq_kivi_bytes *out);
+
+/* Decode work partition: tokens per split-KV work item (a multiple of 64
+ * and of g, >= 64), or 0 for the automatic choice (the default).  Results
+ * are invariant to it up to fp32 rounding; exposed for tests and tuning. */
+int vq_kivi_set_split_tokens(vq_kivi_cache *c, int32_t tokens_per_split);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t vq_kivi_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VQ_KIVI_H */

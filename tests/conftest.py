@@ -18,3 +18,19 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def vqlib():
+    """The compiled CUDA library (built on demand; nvcc cross-compiles)."""
+    from bit_kv_cache_05_gb300 import _lib, build
+    build.build()
+    return _lib.load()
+
+
+def cuda_ok() -> bool:
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
