@@ -27,7 +27,7 @@ EXPORTS = ("vq_kivi_quantize", "vq_kivi_append", "vq_kivi_decode_attend",
            "vq_kivi_free", "vq_kivi_last_error", "vq_kivi_lengths",
            "vq_kivi_get_params", "vq_kivi_plane_bytes", "vq_kivi_export",
            "vq_kivi_cache_bytes", "vq_kivi_set_split_tokens",
-           "vq_kivi_launch_count")
+           "vq_kivi_launch_count", "vq_kivi_decode_attend_static")
 
 
 class VqError(RuntimeError):
@@ -40,6 +40,11 @@ class Params(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("B", "H_q", "H_kv", "D", "bits", "group", "residual",
                  "max_seq")]
+
+
+class Planes(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("Kc", "Ks", "Kz", "Vc", "Vs", "Vz", "Kr", "Vr")]
 
 
 class Bytes(ctypes.Structure):
@@ -83,6 +88,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         L.vq_kivi_cache_bytes.argtypes = [P, ctypes.POINTER(Bytes)]
         L.vq_kivi_set_split_tokens.argtypes = [P, i32]
         L.vq_kivi_launch_count.restype = ctypes.c_uint64
+        L.vq_kivi_decode_attend_static.argtypes = [
+            ctypes.POINTER(Params), ctypes.POINTER(Planes), P, P, P,
+            ctypes.c_float, P]
         for name in EXPORTS:
             getattr(L, name).restype = getattr(L, name).restype or ctypes.c_int
         L.vq_kivi_plane_bytes.restype = ctypes.c_size_t

@@ -105,6 +105,7 @@ int32_t split_unit(int g) { return g > 64 ? g : 64; }
 
 namespace vqk {
 void count_launch(int n) { g_launches.fetch_add((uint64_t)n); }
+void set_last_error(const char *msg) { g_err = msg; }
 }  // namespace vqk
 
 extern "C" {

@@ -92,4 +92,7 @@ cudaError_t launch_decode(const Geometry &geo, const Planes &pl,
 // counts every kernel launch made by the library
 void count_launch(int n = 1);
 
+// sets the message vq_kivi_last_error() returns on the calling thread
+void set_last_error(const char *msg);
+
 }  // namespace vqk

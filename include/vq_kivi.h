@@ -171,6 +171,51 @@ int vq_kivi_set_split_tokens(vq_kivi_cache *c, int32_t tokens_per_split);
 /* Number of kernels this library has launched in this process. */
 uint64_t vq_kivi_launch_count(void);
 
+/* ---- decode without any allocation ------------------------------------- */
+
+/* The pages have no counterpart to this entry point; it exists for callers
+ * that may not allocate device memory once they run (engines that reserve
+ * all device memory at start-up and serve only from their own pool, plugins
+ * whose host forbids allocations, latency-critical loops where cudaMalloc
+ * would synchronize the device).  It computes the same fused decode step as
+ * vq_kivi_decode_attend, from cache planes that the caller keeps in its own
+ * device memory, and allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library call.
+ *
+ * Scratch: the split-KV partial results go to one fixed array of
+ * VQ_KIVI_STATIC_SCRATCH_BYTES in this library's device memory, which every
+ * GPU that loads the library holds until the process exits.  Every call
+ * shares it and it keeps the last call's contents (nothing in it needs to
+ * start at zero), so calls that overlap on the GPU -- on two streams, or
+ * from two threads -- race and give wrong results: serialize them.  The first
+ * call on each device looks up the array's device address on that device
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.
+ *
+ * Planes (device memory, 16-byte aligned; Tcap = ceil(max_seq/g)*g, at least
+ * g; R = residual; per sequence T_q and n_res follow the residual rule):
+ *   Kc, Vc  uint8 [B][H_kv][Tcap][D*bits/8]   as vq_kivi_export planes 0, 3
+ *   Ks, Kz  fp16  [B][H_kv][Tcap/g][D]        as planes 1, 2
+ *   Vs, Vz  fp16  [B][H_kv][Tcap][D/g]        as planes 4, 5
+ *   Kr, Vr  fp16  [B][H_kv][R+g][D]  residual ring: the token at position p
+ *           (T_q <= p < S) is in slot p mod (R+g)
+ *   seq_lens host int32[B] (S per sequence); q, out, softmax_scale and stream
+ *   as in vq_kivi_decode_attend.
+ * Errors: VQ_ERR_CAPACITY when B*H_q*(D+2)*4 bytes times two work items
+ * exceeds the scratch (or a length exceeds max_seq), VQ_ERR_ARG /
+ * VQ_ERR_UNSUPPORTED as elsewhere; the message is in vq_kivi_last_error(). */
+#define VQ_KIVI_STATIC_SCRATCH_BYTES (8u << 20)
+
+typedef struct vq_kivi_planes {
+  const void *Kc, *Ks, *Kz, *Vc, *Vs, *Vz, *Kr, *Vr;
+} vq_kivi_planes;
+
+int vq_kivi_decode_attend_static(const vq_kivi_params *p,
+                                 const vq_kivi_planes *planes,
+                                 const int32_t *seq_lens, const void *q,
+                                 float *out, float softmax_scale,
+                                 void *stream);
+
 #ifdef __cplusplus
 }
 #endif
