@@ -132,6 +132,16 @@ class KiviCache:
         _lib.check(_lib.load().vq_kivi_cache_bytes(self._h, ctypes.byref(b)))
         return {n: int(getattr(b, n)) for n, _ in _lib.Bytes._fields_}
 
+    def device_status(self):
+        """Raise if a decode kernel gave up a bounded pipeline wait."""
+        _lib.check(_lib.load().vq_kivi_device_status(self._h))
+
+    def decode_kernel(self) -> str:
+        k = _lib.load().vq_kivi_decode_kernel(self._h)
+        if k < 0:
+            _lib.check(k)
+        return "tensor-core" if k == 1 else "cuda-core"
+
     def set_split_tokens(self, n: int):
         _lib.check(_lib.load().vq_kivi_set_split_tokens(self._h, int(n)))
 

@@ -23,6 +23,9 @@ struct vq_kivi_cache {
   cudaStream_t last_stream;
   int32_t split_tokens;   // 0 = automatic
   int32_t tps_min;        // smallest split the workspace allows
+  bool use_mma;           // tensor-core decode kernel for this shape
+  MmaPlan plan;
+  unsigned *err;          // device word set by a kernel whose wait gave up
   int32_t S[kMaxB], Tq[kMaxB], nres[kMaxB];
 };
 
@@ -168,8 +171,13 @@ int vq_kivi_quantize(const vq_kivi_params *p, const void *K, const void *V,
   const size_t sz_kmeta = BH * (geo.Tcap / g) * p->D * sizeof(__half);
   const size_t sz_vmeta = BH * geo.Tcap * (p->D / g) * sizeof(__half);
   const size_t sz_res = BH * geo.Rcap * p->D * sizeof(__half);
-  const size_t sz_part =
-      (size_t)p->B * p->H_q * geo.max_items * (p->D + 2) * sizeof(float);
+  c->use_mma = mma_plan(geo, c->sm_count, &c->plan);
+  size_t n_part = (size_t)p->B * p->H_q * geo.max_items * (p->D + 2);
+  if (c->use_mma) {
+    const size_t n_mma = mma_part_floats(geo, c->plan);
+    if (n_mma > n_part) n_part = n_mma;
+  }
+  const size_t sz_part = n_part * sizeof(float);
   const size_t A = 256;
   size_t off = 0;
   size_t o_Kc = off; off += round_up(sz_codes, A);
@@ -181,6 +189,7 @@ int vq_kivi_quantize(const vq_kivi_params *p, const void *K, const void *V,
   size_t o_Kr = off; off += round_up(sz_res, A);
   size_t o_Vr = off; off += round_up(sz_res, A);
   size_t o_part = off; off += round_up(sz_part, A);
+  size_t o_err = off; off += A;
   c->block_bytes = off;
 
   e = cudaMallocAsync(&c->block, c->block_bytes, st);
@@ -201,6 +210,7 @@ int vq_kivi_quantize(const vq_kivi_params *p, const void *K, const void *V,
   pl.Kr = (__half *)(base + o_Kr);
   pl.Vr = (__half *)(base + o_Vr);
   pl.part = (float *)(base + o_part);
+  c->err = (unsigned *)(base + o_err);
   c->last_stream = st;
 
   auto abort_create = [&](cudaError_t err, const char *what) {
@@ -212,6 +222,7 @@ int vq_kivi_quantize(const vq_kivi_params *p, const void *K, const void *V,
 
   // planes start zeroed so that exported padding is deterministic
   e = cudaMemsetAsync(c->block, 0, o_part, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->err, 0, A, st);
   if (e != cudaSuccess) return abort_create(e, "cudaMemsetAsync");
 
   FlushTable ft;
@@ -307,6 +318,38 @@ int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
   const vq_kivi_params &p = c->p;
   cudaStream_t st = (cudaStream_t)stream;
 
+  const float scale = softmax_scale > 0.f ? softmax_scale
+                                          : 1.0f / std::sqrt((float)p.D);
+  if (c->use_mma) {
+    MmaTable tab;
+    tab.bprefix[0] = 0;
+    for (int b = 0; b < p.B; ++b) {
+      tab.Tq[b] = c->Tq[b];
+      tab.nres[b] = c->nres[b];
+      tab.nq[b] = (c->Tq[b] + c->plan.chunk - 1) / c->plan.chunk;
+      tab.nc[b] = tab.nq[b] + (c->nres[b] > 0 ? 1 : 0);
+      tab.bprefix[b + 1] = tab.bprefix[b] + p.H_kv * tab.nc[b];
+    }
+    MmaArgs args;
+    args.q = (const __half *)q;
+    args.out = out;
+    args.part = c->pl.part;
+    args.err = c->err;
+    args.scale_log2 = scale * 1.4426950408889634f;
+    args.N = tab.bprefix[p.B];
+    MmaPlan plan = c->plan;
+    if (c->split_tokens > 0) {
+      // a fixed partition: about split_tokens quantized tokens per warp
+      const int64_t w = ((int64_t)args.N * plan.chunk + c->split_tokens - 1) /
+                        c->split_tokens;
+      if (w < plan.warps_max) plan.warps_max = (int)(w > 0 ? w : 1);
+    }
+    cudaError_t e = launch_decode_mma(c->geo, c->pl, plan, args, tab, st);
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+    c->last_stream = st;
+    return VQ_OK;
+  }
+
   int64_t total_tq = 0;
   for (int b = 0; b < p.B; ++b) total_tq += c->Tq[b];
   int32_t tps = c->split_tokens;
@@ -329,8 +372,6 @@ int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
   DecodeArgs args;
   args.q = (const __half *)q;
   args.out = out;
-  const float scale = softmax_scale > 0.f ? softmax_scale
-                                          : 1.0f / std::sqrt((float)p.D);
   args.scale_log2 = scale * 1.4426950408889634f;
   args.tps = tps;
   args.total_items = tab.prefix[p.B];
@@ -428,6 +469,27 @@ int vq_kivi_cache_bytes(const vq_kivi_cache *c, vq_kivi_bytes *out) {
   }
   *out = r;
   return VQ_OK;
+}
+
+int vq_kivi_device_status(vq_kivi_cache *c) {
+  int rc = check_cache(c);
+  if (rc) return rc;
+  unsigned flag = 0;
+  cudaError_t e = cudaMemcpyAsync(&flag, c->err, sizeof flag,
+                                  cudaMemcpyDeviceToHost, c->last_stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(c->last_stream);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status");
+  if (flag) {
+    cudaMemsetAsync(c->err, 0, sizeof flag, c->last_stream);
+    return fail(VQ_ERR_CUDA, "a decode kernel gave up waiting for its "
+                "shared-memory copies; its outputs are not valid");
+  }
+  return VQ_OK;
+}
+
+int vq_kivi_decode_kernel(const vq_kivi_cache *c) {
+  if (!c) return fail(VQ_ERR_ARG, "cache is NULL");
+  return c->use_mma ? 1 : 0;
 }
 
 int vq_kivi_set_split_tokens(vq_kivi_cache *c, int32_t tokens_per_split) {

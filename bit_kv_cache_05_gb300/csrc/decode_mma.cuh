@@ -1,0 +1,828 @@
+// Fused decode step over the quantized cache on the tensor cores (mma.sync
+// m16n8k16, fp16 operands, fp32 accumulation): the kernel template.  One
+// instantiation per (D, bits, padded query heads per kv head, group size);
+// decode_mma_b{2,4,8}.cu instantiate it, decode_mma.cu plans and launches.
+//
+// Method: VeloxQuant-MLX changelog v0.42.0 "Added", scalar_fused_decode_attend:
+// SDP attention directly over the group-affine cache; k_hat / v_hat are
+// never written to memory; online softmax accumulated in fp32.
+//
+// Algebra (base-2 scores, q' = q * softmax_scale * log2(e)):
+//   key group G:    q'.k_hat_t = sum_c (q'_c s_Gc) code_tc + sum_c q'_c z_Gc
+//   value token t:  o_c += p_t (s_t,j(c) code_tc + z_t,j(c))
+// The code sums run on the tensor cores:
+//   scores   S^T[tok][col]  = codes[tok][ch] . A[ch][col],  A = q' s  (hi + lo)
+//   values   O^T[ch][col]  += codes^T[ch][tok] . W[tok][col], W = p s  (hi + lo)
+// The codes enter as exact fp16 subnormals (the b-bit field masked out of the
+// packed word, value = code * 2^(bit position - 24)); each fp32 factor is
+// split into two fp16 operands hi (top 11 bits) and lo (the fp32 remainder
+// rounded to fp16) in adjacent columns, so products keep about 21 bits.  The
+// zero-point sums (sum_c q'_c z_Gc and sum_t p_t z_t,j) run on the CUDA cores
+// in fp32.
+//
+// MMA columns.  Scores: 8 columns = 4 (query head, key group) pairs x (hi,
+// lo): with GQP query heads per kv head, a "window" of 4/GQP consecutive key
+// groups shares one B operand (for one head: four groups, so the operand is
+// rebuilt once per 4g tokens).  Values: 8 columns = 4 (query head, value
+// group) pairs x (hi, lo); an m16 channel tile uses the block that holds its
+// value group.
+//
+// Work split: the (sequence, kv head, 64-token chunk) space, with each head's
+// fp16 residual window as one extra chunk, is cut into W equal contiguous
+// ranges, one per warp of a persistent grid.  A warp streams its chunks
+// through its own cp.async.bulk pipeline (one mbarrier per stage, bounded
+// waits), keeps (m, l, O) for the head it is in, and writes one partial per
+// head segment; k_combine_mma merges the partials of each head.
+#pragma once
+
+#include <type_traits>
+
+#include "vqk_internal.cuh"
+
+namespace vqk {
+namespace mma {
+
+constexpr int kC = 64;          // tokens per chunk (4 m16 tiles)
+constexpr int kNW = 4;          // warps per CTA
+constexpr int kMaxStages = 4;
+constexpr unsigned kFull = 0xffffffffu;
+
+// ---- PTX helpers -----------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile(
+      "mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: gives up after ~0.5 s and reports false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > 500000000ull) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src,
+                                         uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0,
+                                         uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 2^x for x <= 0 (softmax weights): the hardware approximation, flushing
+// results below 2^-126 to zero.
+__device__ __forceinline__ float exp2_neg(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// The fp16 "hi" part (hl == 0) or the "lo" remainder (hl == 1) of x, as an
+// fp32 value to be rounded to fp16: hi keeps x's sign, exponent and top 10
+// mantissa bits (exact in fp16 while |x| is in fp16's normal range), lo =
+// x - hi is exact in fp32, so hi + fp16(lo) carries ~21 bits of x.
+__device__ __forceinline__ float hilo(float x, int hl) {
+  const float h = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+  return hl ? x - h : h;
+}
+
+// 2^e as a float, e in [-126, 127]
+__device__ __forceinline__ float exp2i(int e) {
+  return __int_as_float((127 + e) << 23);
+}
+
+// NJ consecutive fp16 values (NJ a power of two, naturally aligned) -> fp32
+template <int NJ>
+__device__ __forceinline__ void load_halves(const __half *p, float (&out)[NJ]) {
+  if constexpr (NJ == 1) {
+    out[0] = __half2float(p[0]);
+  } else if constexpr (NJ == 2) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(p));
+    out[0] = f.x; out[1] = f.y;
+  } else {
+#pragma unroll
+    for (int q = 0; q < NJ / 4; ++q) {
+      const uint2 r = reinterpret_cast<const uint2 *>(p)[q];
+      const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&r.x));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&r.y));
+      out[4 * q] = a.x; out[4 * q + 1] = a.y;
+      out[4 * q + 2] = b.x; out[4 * q + 3] = b.y;
+    }
+  }
+}
+
+// ---- per-bit-width code layout --------------------------------------------
+//
+// Score A fragment (rows = 16 tokens, K = 16 channels of K-step ks): lane
+// (gid, tig) holds K slots 2tig, 2tig+1 (register "lo") and 2tig+8, 2tig+9
+// ("hi") of tokens gid and gid+8.  slot_ch(tig, e), e = 0..3, is the channel
+// of those four slots.  The codes arrive scaled by 2^(score_pos(tig) - 24);
+// the score B operand is scaled by 2^-score_pos(tig) so every product carries
+// exactly 2^-24.  Words: a uint4 of a token row holds WPQ K-steps.
+//
+// Value A fragment (rows = channels 2gid, 2gid+1 of an m16 tile, K = tokens
+// of the K-step): lane (gid, tig) permutes the bytes of two tokens' words
+// (vsel) and masks channel 2gid (vmask0) and 2gid+1 (vmask1), whose codes
+// arrive scaled by 2^(vpos0 - 24) and 2^(vpos1 - 24); the output rows are
+// scaled back at the end.  A uint4 of a token row covers VTPQ m16 tiles;
+// tile u of it uses word vword(x, u, gid).
+template <int BITS> struct Layout;
+
+template <> struct Layout<2> {
+  static constexpr int WPQ = 4;    // K-steps per uint4 (one word each)
+  static constexpr int VTPQ = 4;   // value tiles per uint4
+  static __device__ __forceinline__ void score_a(const uint4 &q, int ks, int tig,
+                                                 uint32_t &lo, uint32_t &hi) {
+    const uint32_t w = (&q.x)[ks & 3];
+    const uint32_t m = 0x00030003u << (2 * tig);
+    lo = w & m;            // channels tig, tig+8
+    hi = (w >> 8) & m;     // channels tig+4, tig+12
+  }
+  static __device__ __forceinline__ int slot_ch(int tig, int e) {
+    return tig + 8 * (e & 1) + 4 * (e >> 1);
+  }
+  static __device__ __forceinline__ int score_pos(int tig) { return 2 * tig; }
+  // word of m16 tile u (0..VTPQ-1) within a uint4 of a token row
+  static __device__ __forceinline__ uint32_t vword(const uint4 &x, int u, int) {
+    return (&x.x)[u];
+  }
+  static __device__ __forceinline__ uint32_t vsel(int gid) {
+    const uint32_t b = gid >> 1;
+    return b | (b << 4) | ((4 + b) << 8) | ((4 + b) << 12);
+  }
+  static __device__ __forceinline__ int vpos0(int gid) { return 4 * (gid & 1); }
+  static __device__ __forceinline__ int vpos1(int gid) { return 4 * (gid & 1) + 2; }
+  static __device__ __forceinline__ void value_a(uint32_t x, int gid,
+                                                 uint32_t &r0, uint32_t &r1) {
+    r0 = x & (0x00030003u << vpos0(gid));
+    r1 = x & (0x00030003u << vpos1(gid));
+  }
+};
+
+template <> struct Layout<4> {
+  static constexpr int WPQ = 2;
+  static constexpr int VTPQ = 2;
+  static __device__ __forceinline__ void score_a(const uint4 &q, int ks, int tig,
+                                                 uint32_t &lo, uint32_t &hi) {
+    const uint32_t sh = 8 * (tig >> 1);
+    const uint32_t m = 0x000F000Fu << (4 * (tig & 1));
+    lo = ((&q.x)[2 * (ks & 1)] >> sh) & m;      // channels tig, tig+4
+    hi = ((&q.x)[2 * (ks & 1) + 1] >> sh) & m;  // channels 8+tig, 12+tig
+  }
+  static __device__ __forceinline__ int slot_ch(int tig, int e) {
+    return tig + 4 * e;
+  }
+  static __device__ __forceinline__ int score_pos(int tig) { return 4 * (tig & 1); }
+  static __device__ __forceinline__ uint32_t vword(const uint4 &x, int u, int gid) {
+    const uint32_t w0 = u ? x.z : x.x, w1 = u ? x.w : x.y;
+    return (gid >> 2) ? w1 : w0;   // word 2u + gid/4
+  }
+  static __device__ __forceinline__ uint32_t vsel(int gid) {
+    const uint32_t b = gid & 3;
+    return b | (b << 4) | ((4 + b) << 8) | ((4 + b) << 12);
+  }
+  static __device__ __forceinline__ int vpos0(int) { return 0; }
+  static __device__ __forceinline__ int vpos1(int) { return 4; }
+  static __device__ __forceinline__ void value_a(uint32_t x, int,
+                                                 uint32_t &r0, uint32_t &r1) {
+    r0 = x & 0x000F000Fu;
+    r1 = x & 0x00F000F0u;
+  }
+};
+
+template <> struct Layout<8> {
+  static constexpr int WPQ = 1;    // uint4 = one K-step (4 words, one per tig)
+  static constexpr int VTPQ = 1;
+  static __device__ __forceinline__ void score_a(const uint4 &q, int, int tig,
+                                                 uint32_t &lo, uint32_t &hi) {
+    const uint32_t w = (tig & 2) ? ((tig & 1) ? q.w : q.z) : ((tig & 1) ? q.y : q.x);
+    lo = w & 0x00FF00FFu;          // channels 4tig, 4tig+2
+    hi = (w >> 8) & 0x00FF00FFu;   // channels 4tig+1, 4tig+3
+  }
+  static __device__ __forceinline__ int slot_ch(int tig, int e) {
+    return 4 * tig + 2 * (e & 1) + (e >> 1);
+  }
+  static __device__ __forceinline__ int score_pos(int) { return 0; }
+  static __device__ __forceinline__ uint32_t vword(const uint4 &x, int, int gid) {
+    // word gid/2: bit 1 of gid picks the odd word, bit 2 the upper pair
+    return (gid & 4) ? ((gid & 2) ? x.w : x.z) : ((gid & 2) ? x.y : x.x);
+  }
+  static __device__ __forceinline__ uint32_t vsel(int gid) {
+    const uint32_t b = 2 * (gid & 1);
+    return b | ((b + 1) << 4) | ((4 + b) << 8) | ((5 + b) << 12);
+  }
+  static __device__ __forceinline__ int vpos0(int) { return 0; }
+  static __device__ __forceinline__ int vpos1(int) { return 0; }
+  static __device__ __forceinline__ void value_a(uint32_t x, int,
+                                                 uint32_t &r0, uint32_t &r1) {
+    r0 = x & 0x00FF00FFu;
+    r1 = (x >> 8) & 0x00FF00FFu;
+  }
+};
+
+// ---- compile-time configuration ---------------------------------------------
+
+template <int D_, int BITS_, int GQP_, int G_>
+struct Cfg {
+  static constexpr int D = D_, BITS = BITS_, GQP = GQP_, G = G_;
+  static constexpr int KS = D / 16;            // score K-steps = value m16 tiles
+  static constexpr int NJ = D / G;             // value groups per row
+  static constexpr int WG = 4 / GQP;           // key groups per score window
+  static constexpr int ROW = D * BITS / 8;     // bytes per token row
+  static constexpr int ROWQ = ROW / 16;        // uint4 per token row
+  static constexpr int NVB = (GQP * NJ + 3) / 4;         // value B blocks
+  static constexpr int WT = WG * G;            // tokens per score window
+  static constexpr int NWIN = WT >= kC ? 1 : kC / WT;    // windows per chunk
+  static constexpr int MPW = 4 / NWIN;         // m16 tiles per window
+  static constexpr int CG = G >= kC ? 1 : kC / G;        // key groups per chunk
+  static constexpr int KG = WG > CG ? WG : CG;           // key groups staged
+  // stage layout (bytes)
+  static constexpr uint32_t S_KC = 0;
+  static constexpr uint32_t S_VC = S_KC + kC * ROW;
+  static constexpr uint32_t S_KS = S_VC + kC * ROW;
+  static constexpr uint32_t S_KZ = S_KS + KG * D * 2;
+  static constexpr uint32_t S_VS = S_KZ + KG * D * 2;
+  static constexpr uint32_t S_VZ = S_VS + kC * NJ * 2;
+  static constexpr uint32_t S_BYTES = (S_VZ + kC * NJ * 2 + 127) / 128 * 128;
+  // per-warp layout: [mbarriers][q' 4 x D f32 in slot order][residual o
+  // 4 x D f32][residual m, l][stages]
+  static constexpr uint32_t W_QF = 128;
+  static constexpr uint32_t W_ORES = W_QF + 4 * D * 4;
+  static constexpr uint32_t W_MRES = W_ORES + 4 * D * 4;
+  static constexpr uint32_t W_STAGE0 = (W_MRES + 32 + 127) / 128 * 128;
+  static __host__ __device__ constexpr uint32_t warp_bytes(int ST) {
+    return W_STAGE0 + ST * S_BYTES;
+  }
+};
+
+// reduce over the lanes that share this lane's query head: all lanes with the
+// same tig % GQP (xor over gid, and over the tig bits at and above GQP)
+template <int GQP, typename F>
+__device__ __forceinline__ float head_reduce(float v, F op) {
+  v = op(v, __shfl_xor_sync(kFull, v, 4));
+  v = op(v, __shfl_xor_sync(kFull, v, 8));
+  v = op(v, __shfl_xor_sync(kFull, v, 16));
+  if constexpr (GQP < 2) v = op(v, __shfl_xor_sync(kFull, v, 1));
+  if constexpr (GQP < 4) v = op(v, __shfl_xor_sync(kFull, v, 2));
+  return v;
+}
+
+struct MaxOp {
+  __device__ float operator()(float a, float b) const { return fmaxf(a, b); }
+};
+struct AddOp {
+  __device__ float operator()(float a, float b) const { return a + b; }
+};
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+  return v;
+}
+
+__device__ __forceinline__ int find_seq(const int32_t *prefix, int B,
+                                        int item) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Position in the flattened chunk space, advanced one chunk at a time.
+struct Cursor {
+  int b, h, k;
+  __device__ __forceinline__ void init(int c, const Geometry &geo,
+                                       const MmaTable &tab) {
+    b = find_seq(tab.bprefix, geo.B, c);
+    const int local = c - tab.bprefix[b];
+    h = local / tab.nc[b];
+    k = local - h * tab.nc[b];
+  }
+  __device__ __forceinline__ void next(const Geometry &geo, const MmaTable &tab) {
+    if (++k == tab.nc[b]) {
+      k = 0;
+      if (++h == geo.H_kv) {
+        h = 0;
+        do { ++b; } while (b < geo.B && tab.nc[b] == 0);
+      }
+    }
+  }
+};
+
+template <class C>
+__global__ void __launch_bounds__(kNW * 32)
+k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
+  using L = Layout<C::BITS>;
+  constexpr int D = C::D, KS = C::KS, NJ = C::NJ, GQP = C::GQP, WG = C::WG;
+  constexpr int G = C::G, ROW = C::ROW, ROWQ = C::ROWQ;
+  extern __shared__ __align__(128) unsigned char smem[];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int wg = blockIdx.x * kNW + warp;
+  if (wg >= args.W) return;
+  const int64_t N = args.N, W = args.W;
+  const int lo_c = (int)(wg * N / W), hi_c = (int)((wg + 1) * N / W);
+  const int n_mine = hi_c - lo_c;
+  if (n_mine <= 0) return;
+  const int ST = args.ST, GQ = args.GQ;
+
+  unsigned char *ws = smem + warp * C::warp_bytes(ST);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(ws);
+  float *qf = reinterpret_cast<float *>(ws + C::W_QF);      // [4][KS][4 tig][4 e]
+  float *ores = reinterpret_cast<float *>(ws + C::W_ORES);  // [4][D]
+  float *mres = reinterpret_cast<float *>(ws + C::W_MRES);  // m[4], l[4]
+  unsigned char *stage0 = ws + C::W_STAGE0;
+
+  if (lane == 0) {
+    for (int s = 0; s < ST; ++s) mbar_init(&bars[s]);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+
+  // ---- producer: lane 0 issues the bulk copies of the chunk at `cu` -----
+  auto issue = [&](const Cursor &cu, int s) {
+    const int Tq = tab.Tq[cu.b];
+    const int t0 = cu.k * kC;
+    const int rem = Tq - t0;
+    const int nvalid = rem < kC ? rem : kC;
+    unsigned char *st = stage0 + s * C::S_BYTES;
+    const size_t hd = (size_t)cu.b * geo.H_kv + cu.h;
+    const uint32_t b_codes = nvalid * ROW;
+    const int kg0 = ((t0 / G) / C::KG) * C::KG;
+    const int ngv = Tq / G - kg0;
+    const int ng = ngv < C::KG ? ngv : C::KG;
+    const uint32_t b_ks = ng * D * 2;
+    const uint32_t b_vs = nvalid * NJ * 2;
+    mbar_expect_tx(&bars[s], 2 * (b_codes + b_ks + b_vs));
+    bulk_g2s(st + C::S_KC, pl.Kc + (hd * geo.Tcap + t0) * ROW, b_codes, &bars[s]);
+    bulk_g2s(st + C::S_VC, pl.Vc + (hd * geo.Tcap + t0) * ROW, b_codes, &bars[s]);
+    const size_t kidx = (hd * (geo.Tcap / G) + kg0) * D;
+    bulk_g2s(st + C::S_KS, pl.Ks + kidx, b_ks, &bars[s]);
+    bulk_g2s(st + C::S_KZ, pl.Kz + kidx, b_ks, &bars[s]);
+    const size_t vidx = (hd * geo.Tcap + t0) * NJ;
+    bulk_g2s(st + C::S_VS, pl.Vs + vidx, b_vs, &bars[s]);
+    bulk_g2s(st + C::S_VZ, pl.Vz + vidx, b_vs, &bars[s]);
+  };
+  auto is_quant = [&](const Cursor &cu) { return cu.k < tab.nq[cu.b]; };
+
+  Cursor pc;  // producer cursor: the next chunk to issue
+  pc.init(lo_c, geo, tab);
+  uint32_t phase = 0;    // bit s = parity to wait for on stage s
+  uint32_t pending = 0;  // bit s = copies in flight into stage s
+  for (int i = 0; i < ST && i < n_mine; ++i) {
+    if (is_quant(pc)) {
+      if (lane == 0) issue(pc, i);
+      pending |= 1u << i;
+    }
+    pc.next(geo, tab);
+  }
+  bool failed = false;
+
+  // ---- per-lane constants ------------------------------------------------
+  const float bsc = exp2i(-L::score_pos(tig));
+  const uint32_t v_sel = L::vsel(gid);
+  const float rs0 = exp2i(24 - L::vpos0(gid)), rs1 = exp2i(24 - L::vpos1(gid));
+  const int hl = gid & 1;               // B operand column: hi (0) or lo (1)
+  const int pair_b = gid >> 1;          // B operand column pair
+  const int h_b = pair_b % GQP;         // query head of the B column pair
+  const int h_s = tig % GQP;            // this lane's query head (C layout)
+  const int gw_s = tig / GQP;           // this lane's key group in a window
+
+  // ---- running state of the current head segment ---------------------------
+  float O[KS][4];
+  float Z[NJ];
+  float m_run = -INFINITY, l_run = 0.f;
+  uint32_t Bs[KS][2];
+  float beta_t = 0.f;    // zero-point term of pair tig, current window
+  float unscale_t = 1.f; // 2^(24 - k) of pair tig, current window
+  int cur_w = -1;
+  bool has_res = false;
+
+  auto reset_state = [&]() {
+#pragma unroll
+    for (int mv = 0; mv < KS; ++mv)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) O[mv][r] = 0.f;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) Z[j] = 0.f;
+    m_run = -INFINITY;
+    l_run = 0.f;
+    cur_w = -1;
+    has_res = false;
+  };
+
+  // q' of the head's GQP query heads, stored in score-slot order:
+  // qf[((h * KS + ks) * 4 + tig) * 4 + e] = q'[h][16 ks + slot_ch(tig, e)]
+  auto load_q = [&](int b, int h) {
+    for (int i = lane; i < 4 * D; i += 32) {
+      const int hh = i / D, r = i - hh * D;
+      const int ks = r >> 4, t = (r >> 2) & 3, e = r & 3;
+      const int c = 16 * ks + L::slot_ch(t, e);
+      float v = 0.f;
+      if (hh < GQ)
+        v = __half2float(args.q[((size_t)b * geo.H_q + h * GQ + hh) * D + c]) *
+            args.scale_log2;
+      qf[i] = v;
+    }
+    __syncwarp();
+  };
+
+  // B operand of the score MMA for the window starting at key group gw0 (the
+  // stage's key scale/zero region starts at group kg0), and, for this lane's
+  // column pair, the zero-point term beta and the factor that undoes the
+  // operand scaling.  Each column pair is scaled by a power of two 2^k that
+  // puts its largest |a| in [2^13, 2^14): no fp16 overflow, and the lo parts
+  // stay in fp16's normal range.
+  auto build_score_b = [&](const __half *Ks, const __half *Kz, int gw0, int kg0) {
+    const int gr = gw0 + pair_b / GQP - kg0;   // group row in the region
+    const float4 *qh = reinterpret_cast<const float4 *>(qf) + (h_b * KS) * 4 + tig;
+    const __half *ksr = Ks + gr * D;
+    const __half *kzr = Kz + gr * D;
+    float av[KS][4];
+    float zpart = 0.f, amax = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const float4 q4 = qh[ks * 4];
+      const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = 16 * ks + L::slot_ch(tig, e);
+        av[ks][e] = qv[e] * __half2float(ksr[c]) * bsc;
+        zpart = fmaf(qv[e], __half2float(kzr[c]), zpart);
+        amax = fmaxf(amax, fabsf(av[ks][e]));
+      }
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
+    int k = 13 - (((__float_as_int(amax) >> 23) & 0xff) - 127);
+    k = k < -60 ? -60 : (k > 60 ? 60 : k);
+    const float sc = exp2i(k);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      Bs[ks][0] = pack_half2(hilo(av[ks][0] * sc, hl), hilo(av[ks][1] * sc, hl));
+      Bs[ks][1] = pack_half2(hilo(av[ks][2] * sc, hl), hilo(av[ks][3] * sc, hl));
+    }
+    zpart += __shfl_xor_sync(kFull, zpart, 1);
+    zpart += __shfl_xor_sync(kFull, zpart, 2);
+    // lane (gid, tig) needs the values of pair tig, held by lanes gid = 2*tig
+    beta_t = __shfl_sync(kFull, zpart, 8 * tig);
+    unscale_t = exp2i(24 - __shfl_sync(kFull, k, 8 * tig));
+  };
+
+  // residual window of head (b, h): CUDA cores, lanes own channels
+  auto residual = [&](int b, int hd) {
+    constexpr int CPL = D / 32;
+    const int Tq = tab.Tq[b], nres = tab.nres[b];
+    float m[4], l[4], o[4][CPL], qv[4][CPL];
+#pragma unroll
+    for (int hh = 0; hh < 4; ++hh) {
+      m[hh] = -INFINITY; l[hh] = 0.f;
+#pragma unroll
+      for (int u = 0; u < CPL; ++u) {
+        o[hh][u] = 0.f;
+        const int c = lane * CPL + u;
+        // q' of channel c from the slot-ordered copy
+        int ks = c >> 4, cc = c & 15, t, e;
+        if constexpr (C::BITS == 2) { t = cc & 3; e = ((cc >> 3) & 1) | (((cc >> 2) & 1) << 1); }
+        else if constexpr (C::BITS == 4) { t = cc & 3; e = cc >> 2; }
+        else { t = cc >> 2; e = ((cc & 1) << 1) | ((cc >> 1) & 1); }
+        qv[hh][u] = qf[((hh * KS + ks) * 4 + t) * 4 + e];
+      }
+    }
+    for (int i = 0; i < nres; ++i) {
+      const int slot = (Tq + i) % geo.Rcap;
+      const size_t base = ((size_t)hd * geo.Rcap + slot) * D + lane * CPL;
+      float kv[CPL], vv[CPL];
+#pragma unroll
+      for (int u = 0; u < CPL; ++u) {
+        kv[u] = __half2float(pl.Kr[base + u]);
+        vv[u] = __half2float(pl.Vr[base + u]);
+      }
+#pragma unroll
+      for (int hh = 0; hh < GQP; ++hh) {
+        if (hh >= GQ) break;
+        float part = 0.f;
+#pragma unroll
+        for (int u = 0; u < CPL; ++u) part = fmaf(qv[hh][u], kv[u], part);
+        const float s = warp_sum(part);
+        const float mn = fmaxf(m[hh], s);
+        const float al = exp2_neg(m[hh] - mn), p = exp2_neg(s - mn);
+        l[hh] = l[hh] * al + p;
+#pragma unroll
+        for (int u = 0; u < CPL; ++u) o[hh][u] = o[hh][u] * al + p * vv[u];
+        m[hh] = mn;
+      }
+    }
+#pragma unroll
+    for (int hh = 0; hh < GQP; ++hh) {
+#pragma unroll
+      for (int u = 0; u < CPL; ++u) ores[hh * D + lane * CPL + u] = o[hh][u];
+      if (lane == 0) { mres[hh] = m[hh]; mres[4 + hh] = l[hh]; }
+    }
+    has_res = nres > 0;
+    __syncwarp();
+  };
+
+  // write this warp's partial of head hd (slot wg + hd)
+  auto flush = [&](int hd) {
+    float Lsum = head_reduce<GQP>(l_run, AddOp());
+    float Zt[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) Zt[j] = head_reduce<GQP>(Z[j], AddOp());
+    float mf = m_run, aq = 1.f, ar = 0.f;
+    if (has_res) {
+      const float mr = mres[h_s], lr = mres[4 + h_s];
+      mf = fmaxf(m_run, mr);
+      aq = m_run == -INFINITY ? 0.f : exp2_neg(m_run - mf);
+      ar = exp2_neg(mr - mf);
+      Lsum = Lsum * aq + lr * ar;
+    }
+    if (h_s < GQ) {
+      float *dst = args.part + ((size_t)(wg + hd) * GQP + h_s) * (D + 2);
+#pragma unroll
+      for (int mv = 0; mv < KS; ++mv) {
+        constexpr int dummy = 0;
+        (void)dummy;
+        const int j = (16 * mv) / G;
+        const int vb = (j * GQP) >> 2;
+        if ((4 * vb + tig) / GQP != j) continue;
+        const int c0 = 16 * mv + 2 * gid;
+        float o0 = ((O[mv][0] + O[mv][1]) * rs0 + Zt[j]) * aq;
+        float o1 = ((O[mv][2] + O[mv][3]) * rs1 + Zt[j]) * aq;
+        if (has_res) {
+          o0 += ores[h_s * D + c0] * ar;
+          o1 += ores[h_s * D + c0 + 1] * ar;
+        }
+        *reinterpret_cast<float2 *>(dst + c0) = make_float2(o0, o1);
+      }
+      if (gid == 0 && tig < GQP) {
+        dst[D] = mf;
+        dst[D + 1] = Lsum;
+      }
+    }
+    __syncwarp();
+  };
+
+  // ---- main loop over my chunks ---------------------------------------------
+  Cursor cu;
+  cu.init(lo_c, geo, tab);
+  int cur_hd = -1;
+  for (int i = 0; i < n_mine; ++i) {
+    const int s = i % ST;
+    const int hd = cu.b * geo.H_kv + cu.h;
+    if (hd != cur_hd) {
+      reset_state();
+      load_q(cu.b, cu.h);
+      cur_hd = hd;
+    }
+    if (!is_quant(cu)) {
+      residual(cu.b, hd);
+    } else {
+      const bool ok = __all_sync(kFull, mbar_wait(&bars[s], (phase >> s) & 1u));
+      if (!ok) { failed = true; break; }
+      phase ^= 1u << s;
+      pending &= ~(1u << s);
+      const unsigned char *st = stage0 + s * C::S_BYTES;
+      const uint4 *kc = reinterpret_cast<const uint4 *>(st + C::S_KC);
+      const uint4 *vc = reinterpret_cast<const uint4 *>(st + C::S_VC);
+      const __half *Ks = reinterpret_cast<const __half *>(st + C::S_KS);
+      const __half *Kz = reinterpret_cast<const __half *>(st + C::S_KZ);
+      const __half *Vs = reinterpret_cast<const __half *>(st + C::S_VS);
+      const __half *Vz = reinterpret_cast<const __half *>(st + C::S_VZ);
+      const int t0 = cu.k * kC;
+      const int rem = tab.Tq[cu.b] - t0;
+      const int nmt = (rem < kC ? rem : kC) >> 4;   // valid m16 tiles
+      const int G0 = t0 / G;                        // first key group
+      const int kg0 = (G0 / C::KG) * C::KG;
+
+      // ---- scores, window by window; the tiles of a window interleave ----
+      float sv[4][2];
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) sv[mt][0] = sv[mt][1] = -INFINITY;
+#pragma unroll
+      for (int win = 0; win < C::NWIN; ++win) {
+        constexpr int MPW = C::MPW;
+        const int mt0 = win * MPW;
+        if (mt0 < nmt) {
+          const int gw0 = ((G0 + (16 * mt0) / G) / WG) * WG;
+          if (gw0 != cur_w) {
+            build_score_b(Ks, Kz, gw0, kg0);
+            cur_w = gw0;
+          }
+          float acc[MPW][4];
+#pragma unroll
+          for (int m = 0; m < MPW; ++m)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[m][r] = 0.f;
+#pragma unroll
+          for (int q = 0; q < KS / L::WPQ; ++q) {
+            uint4 r0[MPW], r1[MPW];
+#pragma unroll
+            for (int m = 0; m < MPW; ++m) {
+              const uint4 *row = kc + (16 * (mt0 + m) + gid) * ROWQ;
+              r0[m] = row[q];
+              r1[m] = row[8 * ROWQ + q];
+            }
+#pragma unroll
+            for (int kq = 0; kq < L::WPQ; ++kq) {
+              const int ks = q * L::WPQ + kq;
+#pragma unroll
+              for (int m = 0; m < MPW; ++m) {
+                if (mt0 + m < nmt) {
+                  uint32_t a0, a1, a2, a3;
+                  L::score_a(r0[m], ks, tig, a0, a2);
+                  L::score_a(r1[m], ks, tig, a1, a3);
+                  mma16816(acc[m], a0, a1, a2, a3, Bs[ks][0], Bs[ks][1]);
+                }
+              }
+            }
+          }
+#pragma unroll
+          for (int m = 0; m < MPW; ++m) {
+            const int mt = mt0 + m;
+            if (mt < nmt && ((G0 + (16 * mt) / G) % WG) == gw_s) {
+              sv[mt][0] = fmaf(acc[m][0] + acc[m][1], unscale_t, beta_t);
+              sv[mt][1] = fmaf(acc[m][2] + acc[m][3], unscale_t, beta_t);
+            }
+          }
+        }
+      }
+
+      // ---- online softmax update for this lane's head ----
+      float mx = -INFINITY;
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) mx = fmaxf(mx, fmaxf(sv[mt][0], sv[mt][1]));
+      mx = head_reduce<GQP>(mx, MaxOp());
+      const float m_new = fmaxf(m_run, mx);
+      const float alpha = m_run == -INFINITY ? 0.f : exp2_neg(m_run - m_new);
+      float p[4][2];
+      float psum = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          p[mt][r] = exp2_neg(sv[mt][r] - m_new);   // -inf -> 0
+          psum += p[mt][r];
+        }
+      l_run = l_run * alpha + psum;
+      m_run = m_new;
+#pragma unroll
+      for (int mv = 0; mv < KS; ++mv)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) O[mv][r] *= alpha;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) Z[j] *= alpha;
+
+      // ---- values: K-step kt = tokens 16kt ... 16kt+15 of the chunk.  K
+      // slots (2tig, 2tig+1, 2tig+8, 2tig+9) <-> tokens (tig, tig+4, tig+8,
+      // tig+12): the four rows a lane group reads hit distinct banks. ----
+#pragma unroll
+      for (int kt = 0; kt < 4; ++kt) {
+        if (kt < nmt) {
+          // zero-point term in the score layout (tokens gid, gid+8)
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            float vz[NJ];
+            load_halves<NJ>(Vz + (16 * kt + gid + 8 * r) * NJ, vz);
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) Z[j] = fmaf(p[kt][r], vz[j], Z[j]);
+          }
+          // p of head h_b for tokens tig, tig+4, tig+8, tig+12
+          const int src = ((G0 + (16 * kt) / G) % WG) * GQP + h_b;
+          const float p0 = __shfl_sync(kFull, p[kt][0], 4 * tig + src);
+          const float p1 = __shfl_sync(kFull, p[kt][0], 4 * tig + 16 + src);
+          const float p2 = __shfl_sync(kFull, p[kt][1], 4 * tig + src);
+          const float p3 = __shfl_sync(kFull, p[kt][1], 4 * tig + 16 + src);
+          const int ta = 16 * kt + tig;
+          uint32_t bv[C::NVB][2];
+#pragma unroll
+          for (int vb = 0; vb < C::NVB; ++vb) {
+            const int jb = (4 * vb + pair_b) / GQP;
+            float w0 = 0.f, w1 = 0.f, w2 = 0.f, w3 = 0.f;
+            if (jb < NJ) {
+              w0 = hilo(p0 * __half2float(Vs[ta * NJ + jb]), hl);
+              w1 = hilo(p1 * __half2float(Vs[(ta + 4) * NJ + jb]), hl);
+              w2 = hilo(p2 * __half2float(Vs[(ta + 8) * NJ + jb]), hl);
+              w3 = hilo(p3 * __half2float(Vs[(ta + 12) * NJ + jb]), hl);
+            }
+            bv[vb][0] = pack_half2(w0, w1);
+            bv[vb][1] = pack_half2(w2, w3);
+          }
+          // m16 channel tiles, VTPQ per uint4 of the token rows
+#pragma unroll
+          for (int q = 0; q < KS / L::VTPQ; ++q) {
+            const uint4 xa = vc[ta * ROWQ + q];
+            const uint4 xb = vc[(ta + 4) * ROWQ + q];
+            const uint4 xc = vc[(ta + 8) * ROWQ + q];
+            const uint4 xd = vc[(ta + 12) * ROWQ + q];
+#pragma unroll
+            for (int u = 0; u < L::VTPQ; ++u) {
+              const int mv = q * L::VTPQ + u;
+              const int vb = (((16 * mv) / G) * GQP) >> 2;
+              uint32_t a0, a1, a2, a3;
+              L::value_a(__byte_perm(L::vword(xa, u, gid), L::vword(xb, u, gid), v_sel),
+                         gid, a0, a1);
+              L::value_a(__byte_perm(L::vword(xc, u, gid), L::vword(xd, u, gid), v_sel),
+                         gid, a2, a3);
+              mma16816(O[mv], a0, a1, a2, a3, bv[vb][0], bv[vb][1]);
+            }
+          }
+        }
+      }
+    }
+    const bool head_ends = cu.k == tab.nc[cu.b] - 1 || i == n_mine - 1;
+    if (head_ends) flush(hd);
+    __syncwarp();
+    if (i + ST < n_mine) {
+      if (is_quant(pc)) {
+        if (lane == 0) {
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          issue(pc, s);
+        }
+        pending |= 1u << s;
+      }
+      pc.next(geo, tab);
+    }
+    cu.next(geo, tab);
+  }
+
+  if (failed) {
+    if (lane == 0) atomicOr(args.err, 1u);
+    // let every copy still in flight land (bounded) before the CTA's shared
+    // memory can be reused
+    for (int j = 0; j < ST; ++j)
+      if (pending & (1u << j)) mbar_wait(&bars[j], (phase >> j) & 1u);
+  }
+}
+
+using KernelFn = void (*)(Geometry, Planes, MmaArgs, MmaTable);
+
+struct KernelInfo {
+  KernelFn fn;
+  uint32_t stage_bytes, stage0;
+};
+
+template <class C>
+KernelInfo info() {
+  return KernelInfo{&k_decode_mma<C>, C::S_BYTES, C::W_STAGE0};
+}
+
+// the instantiations of one bit width (decode_mma_b{2,4,8}.cu)
+bool kernel_b2(int D, int GQP, int G, KernelInfo *out);
+bool kernel_b4(int D, int GQP, int G, KernelInfo *out);
+bool kernel_b8(int D, int GQP, int G, KernelInfo *out);
+
+}  // namespace mma
+}  // namespace vqk

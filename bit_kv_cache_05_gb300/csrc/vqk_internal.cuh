@@ -89,6 +89,44 @@ cudaError_t launch_decode(const Geometry &geo, const Planes &pl,
                           const DecodeArgs &args, const DecodeTable &tab,
                           cudaStream_t st);
 
+// ---- decode on the tensor cores (D = 64/128, H_q/H_kv <= 4) ---------------
+
+// Flattened chunk space: sequence b owns chunks [bprefix[b], bprefix[b+1]),
+// H_kv heads of nc[b] chunks each: nq[b] quantized 64-token chunks and, when
+// nres[b] > 0, one residual chunk.
+struct MmaTable {
+  int32_t bprefix[kMaxB + 1];
+  int32_t nc[kMaxB];
+  int32_t nq[kMaxB];
+  int32_t Tq[kMaxB];
+  int32_t nres[kMaxB];
+};
+
+struct MmaArgs {
+  const __half *q;   // [B][H_q][D]
+  float *out;        // [B][H_q][D]
+  float *part;       // partials: slot (warp + head) x GQp x (D + 2)
+  unsigned *err;     // set to nonzero when a pipeline wait gave up
+  float scale_log2;  // softmax scale * log2(e)
+  int N;             // total chunks
+  int W;             // warps used (<= N), filled in by the launcher
+  int GQ, GQp, KG, ST;
+};
+
+struct MmaPlan {
+  int GQ, GQp, KG, ST, chunk;
+  unsigned smem;     // dynamic shared memory per CTA
+  int warps_max;     // resident warps of the persistent grid
+};
+
+// false when the shape has no tensor-core kernel (then the CUDA-core kernel
+// of launch_decode serves it)
+bool mma_plan(const Geometry &geo, int sm_count, MmaPlan *plan);
+size_t mma_part_floats(const Geometry &geo, const MmaPlan &plan);
+cudaError_t launch_decode_mma(const Geometry &geo, const Planes &pl,
+                              const MmaPlan &plan, MmaArgs args,
+                              const MmaTable &tab, cudaStream_t st);
+
 // counts every kernel launch made by the library
 void count_launch(int n = 1);
 

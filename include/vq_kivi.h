@@ -163,13 +163,24 @@ typedef struct vq_kivi_bytes {
 } vq_kivi_bytes;
 int vq_kivi_cache_bytes(const vq_kivi_cache *c, vq_kivi_bytes *out);
 
-/* Decode work partition: tokens per split-KV work item (a multiple of 64
- * and of g, >= 64), or 0 for the automatic choice (the default).  Results
- * are invariant to it up to fp32 rounding; exposed for tests and tuning. */
+/* Decode work partition: about this many quantized tokens per split-KV work
+ * item (a multiple of 64 and of g, at least the workspace minimum of 256),
+ * or 0 for the automatic choice (the default).  Results are invariant to it
+ * up to fp32 rounding; exposed for tests and tuning. */
 int vq_kivi_set_split_tokens(vq_kivi_cache *c, int32_t tokens_per_split);
 
 /* Number of kernels this library has launched in this process. */
 uint64_t vq_kivi_launch_count(void);
+
+/* Synchronizes the cache's last stream and reports whether a decode kernel
+ * gave up on a pipeline wait since the last check (its waits are bounded, so
+ * a stuck copy ends the kernel instead of hanging the GPU): VQ_OK, or
+ * VQ_ERR_CUDA with a message (the flag is then cleared). */
+int vq_kivi_device_status(vq_kivi_cache *c);
+
+/* Which decode kernel serves this cache's shape: 1 = tensor-core kernel
+ * (D = 64 or 128, H_q/H_kv <= 4), 0 = CUDA-core kernel; < 0 on error. */
+int vq_kivi_decode_kernel(const vq_kivi_cache *c);
 
 /* ---- decode without any allocation ------------------------------------- */
 

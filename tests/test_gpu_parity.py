@@ -126,6 +126,7 @@ def test_quantize_and_decode_parity(lib, name):
         assert_planes_equal(gp, lens, oc, b, b)
     ref = oc.attend(q.cpu().numpy())
     assert_attn_close(out.cpu().numpy(), ref, name)
+    c.device_status()
     c.close()
 
 
@@ -153,6 +154,9 @@ def test_shape_sweep(lib, D, bits, g, R, Hq, Hkv, lens):
         assert_planes_equal(gp, lens_g, oc, b, b)
     assert_attn_close(out.cpu().numpy(), oc.attend(inp["q"].cpu().numpy()),
                       f"D={D} b={bits} g={g}")
+    c.device_status()
+    want = "tensor-core" if D <= 128 and Hq // Hkv <= 4 else "cuda-core"
+    assert c.decode_kernel() == want
     c.close()
 
 
@@ -253,16 +257,24 @@ def test_capacity_error_leaves_cache_unchanged(lib):
 # split-KV partition invariance
 # ---------------------------------------------------------------------------
 
-def test_split_count_invariance(lib):
-    w = SMALL["pages_S8192"]
+@pytest.mark.parametrize("name", ["pages_S8192", "gqa_small"])
+def test_split_count_invariance(lib, name):
+    w = SMALL[name]
     inp = synth.make_inputs(w, seed=21, device="cuda")
     c = gpu_cache(w, inp)
+    assert c.decode_kernel() == "tensor-core"
     outs = []
     for tps in (0, 256, 512, 1024, 4096, 8192):
         c.set_split_tokens(tps)
         outs.append(c.decode_attend(inp["q"]).cpu().numpy())
+    # Partitions change only the fp32 summation order and the tensor-core
+    # operand scaling per segment; the fp16 hi/lo operands carry ~2^-21
+    # relative precision on sums of magnitude ~2 that cancel to the output
+    # (code part vs zero-point part), so partitions agree to ~1e-5; 1e-4 is
+    # ten times below the parity tolerance.
     for o in outs[1:]:
-        assert np.abs(o - outs[0]).max() <= 1e-5
+        assert np.abs(o - outs[0]).max() <= 1e-4
+    c.device_status()
     c.close()
 
 
@@ -307,7 +319,9 @@ def test_full_size_sampled(lib, name, samples):
     w = synth.workload(name)
     inp = synth.make_inputs(w, device="cuda")
     c = gpu_cache(w, inp)
+    assert c.decode_kernel() == "tensor-core"
     _sampled_parity(w, inp, c, samples)
+    c.device_status()
     c.close()
     del inp
     torch.cuda.empty_cache()
