@@ -1,6 +1,6 @@
 // Host side of the tensor-core decode: kernel choice, launch plan (stages,
-// persistent grid size), launch, and the log-sum-exp merge of the partials.
-// The kernel itself is in decode_mma.cuh.
+// persistent grid size) and launch.  The kernel, including the log-sum-exp
+// merge of the per-warp partials, is in decode_mma.cuh.
 #include "decode_mma.cuh"
 
 namespace vqk {
@@ -17,38 +17,6 @@ bool pick(const Geometry &geo, int GQp, mma::KernelInfo *ki) {
   }
 }
 
-// out[b][hq] = sum_w 2^(m_w - M) o_w / sum_w 2^(m_w - M) l_w over the warps w
-// whose chunk range touches head hd = b*H_kv + hq/GQ (partial slot w + hd)
-__global__ void k_combine_mma(Geometry geo, MmaArgs args, MmaTable tab) {
-  const int b = blockIdx.x / geo.H_q, hq = blockIdx.x % geo.H_q;
-  const int D = geo.D, GQ = args.GQ;
-  const int h = hq / GQ, hh = hq % GQ;
-  const int hd = b * geo.H_kv + h;
-  const int nc = tab.nc[b];
-  float *out = args.out + ((size_t)b * geo.H_q + hq) * D;
-  if (nc == 0) {
-    for (int c = threadIdx.x; c < D; c += blockDim.x) out[c] = 0.f;
-    return;
-  }
-  const int64_t N = args.N, W = args.W;
-  const int64_t cs = tab.bprefix[b] + (int64_t)h * nc, ce = cs + nc;
-  const int w0 = (int)(((cs + 1) * W - 1) / N);
-  const int w1 = (int)((ce * W - 1) / N);
-  auto entry = [&](int w) {
-    return args.part + ((size_t)(w + hd) * args.GQp + hh) * (D + 2);
-  };
-  float M = -INFINITY;
-  for (int w = w0; w <= w1; ++w) M = fmaxf(M, entry(w)[D]);
-  float Lsum = 0.f;
-  for (int w = w0; w <= w1; ++w) Lsum += exp2f(entry(w)[D] - M) * entry(w)[D + 1];
-  const float inv = 1.0f / Lsum;
-  for (int c = threadIdx.x; c < D; c += blockDim.x) {
-    float acc = 0.f;
-    for (int w = w0; w <= w1; ++w) acc += exp2f(entry(w)[D] - M) * entry(w)[c];
-    out[c] = acc * inv;
-  }
-}
-
 }  // namespace
 
 bool mma_plan(const Geometry &geo, int sm_count, MmaPlan *plan) {
@@ -58,25 +26,33 @@ bool mma_plan(const Geometry &geo, int sm_count, MmaPlan *plan) {
   if (GQp > 4 || (geo.D != 64 && geo.D != 128)) return false;
   mma::KernelInfo ki;
   if (!pick(geo, GQp, &ki)) return false;
-  // as many stages (2..4) as keep two CTAs per SM, else fewer CTAs
-  int ST = mma::kMaxStages;
-  const uint32_t budget2 = 110 * 1024;
-  while (ST > 2 && kNW * (ki.stage0 + ST * ki.stage_bytes) > budget2) --ST;
-  const uint32_t smem = kNW * (ki.stage0 + ST * ki.stage_bytes);
-  if (smem > 227 * 1024) return false;
+  // the stage count (2..4) that keeps the most warps resident, and among
+  // those the deepest pipeline
   if (cudaFuncSetAttribute((const void *)ki.fn,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess) {
+                           227 * 1024) != cudaSuccess) {
     cudaGetLastError();
     return false;
   }
-  int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, ki.fn, kNW * 32,
-                                                    smem) != cudaSuccess ||
-      occ < 1) {
-    cudaGetLastError();
-    return false;
+  int best_occ = 0, ST = 0;
+  uint32_t smem = 0;
+  for (int st = 2; st <= mma::kMaxStages; ++st) {
+    const uint32_t sm = kNW * (ki.stage0 + st * ki.stage_bytes);
+    if (sm > 227 * 1024) break;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, ki.fn, kNW * 32,
+                                                      sm) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    if (occ >= 1 && occ >= best_occ) {
+      best_occ = occ;
+      ST = st;
+      smem = sm;
+    }
   }
+  if (best_occ < 1) return false;
+  const int occ = best_occ;
   plan->GQ = GQ;
   plan->GQp = GQp;
   plan->KG = 0;
@@ -99,21 +75,23 @@ cudaError_t launch_decode_mma(const Geometry &geo, const Planes &pl,
   args.GQp = plan.GQp;
   args.KG = plan.KG;
   args.ST = plan.ST;
-  if (args.N > 0) {
-    mma::KernelInfo ki;
-    if (!pick(geo, plan.GQp, &ki)) return cudaErrorInvalidValue;
-    int64_t W = plan.warps_max;
-    if (W > args.N) W = args.N;
-    args.W = (int)W;
-    const int grid = (int)((W + kNW - 1) / kNW);
-    ki.fn<<<grid, kNW * 32, plan.smem, st>>>(geo, pl, args, tab);
-    count_launch();
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  } else {
-    args.W = 1;
+  // sequences without tokens get an all-zero output (the kernel never
+  // visits them)
+  for (int b = 0; b < geo.B; ++b) {
+    if (tab.nc[b] == 0) {
+      cudaError_t e = cudaMemsetAsync(args.out + (size_t)b * geo.H_q * geo.D, 0,
+                                      sizeof(float) * geo.H_q * geo.D, st);
+      if (e != cudaSuccess) return e;
+    }
   }
-  k_combine_mma<<<geo.B * geo.H_q, geo.D, 0, st>>>(geo, args, tab);
+  if (args.N <= 0) return cudaSuccess;
+  mma::KernelInfo ki;
+  if (!pick(geo, plan.GQp, &ki)) return cudaErrorInvalidValue;
+  int64_t W = plan.warps_max;
+  if (W > args.N) W = args.N;
+  args.W = (int)W;
+  const int grid = (int)((W + kNW - 1) / kNW);
+  ki.fn<<<grid, kNW * 32, plan.smem, st>>>(geo, pl, args, tab);
   count_launch();
   return cudaGetLastError();
 }

@@ -32,7 +32,8 @@
 // ranges, one per warp of a persistent grid.  A warp streams its chunks
 // through its own cp.async.bulk pipeline (one mbarrier per stage, bounded
 // waits), keeps (m, l, O) for the head it is in, and writes one partial per
-// head segment; k_combine_mma merges the partials of each head.
+// head segment; the warp that finishes a head last (an atomic ticket per
+// head, no waiting) merges the head's partials with a log-sum-exp.
 #pragma once
 
 #include <type_traits>
@@ -292,11 +293,11 @@ struct Cfg {
   static constexpr uint32_t S_VS = S_KZ + KG * D * 2;
   static constexpr uint32_t S_VZ = S_VS + kC * NJ * 2;
   static constexpr uint32_t S_BYTES = (S_VZ + kC * NJ * 2 + 127) / 128 * 128;
-  // per-warp layout: [mbarriers][q' 4 x D f32 in slot order][residual o
-  // 4 x D f32][residual m, l][stages]
+  // per-warp layout: [mbarriers][q' GQP x D f32 in slot order][residual o
+  // GQP x D f32][residual m, l][stages]
   static constexpr uint32_t W_QF = 128;
-  static constexpr uint32_t W_ORES = W_QF + 4 * D * 4;
-  static constexpr uint32_t W_MRES = W_ORES + 4 * D * 4;
+  static constexpr uint32_t W_ORES = W_QF + GQP * D * 4;
+  static constexpr uint32_t W_MRES = W_ORES + GQP * D * 4;
   static constexpr uint32_t W_STAGE0 = (W_MRES + 32 + 127) / 128 * 128;
   static __host__ __device__ constexpr uint32_t warp_bytes(int ST) {
     return W_STAGE0 + ST * S_BYTES;
@@ -379,8 +380,8 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
 
   unsigned char *ws = smem + warp * C::warp_bytes(ST);
   uint64_t *bars = reinterpret_cast<uint64_t *>(ws);
-  float *qf = reinterpret_cast<float *>(ws + C::W_QF);      // [4][KS][4 tig][4 e]
-  float *ores = reinterpret_cast<float *>(ws + C::W_ORES);  // [4][D]
+  float *qf = reinterpret_cast<float *>(ws + C::W_QF);      // [GQP][KS][4 tig][4 e]
+  float *ores = reinterpret_cast<float *>(ws + C::W_ORES);  // [GQP][D]
   float *mres = reinterpret_cast<float *>(ws + C::W_MRES);  // m[4], l[4]
   unsigned char *stage0 = ws + C::W_STAGE0;
 
@@ -465,7 +466,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   // q' of the head's GQP query heads, stored in score-slot order:
   // qf[((h * KS + ks) * 4 + tig) * 4 + e] = q'[h][16 ks + slot_ch(tig, e)]
   auto load_q = [&](int b, int h) {
-    for (int i = lane; i < 4 * D; i += 32) {
+    for (int i = lane; i < GQP * D; i += 32) {
       const int hh = i / D, r = i - hh * D;
       const int ks = r >> 4, t = (r >> 2) & 3, e = r & 3;
       const int c = 16 * ks + L::slot_ch(t, e);
@@ -525,9 +526,9 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   auto residual = [&](int b, int hd) {
     constexpr int CPL = D / 32;
     const int Tq = tab.Tq[b], nres = tab.nres[b];
-    float m[4], l[4], o[4][CPL], qv[4][CPL];
+    float m[GQP], l[GQP], o[GQP][CPL], qv[GQP][CPL];
 #pragma unroll
-    for (int hh = 0; hh < 4; ++hh) {
+    for (int hh = 0; hh < GQP; ++hh) {
       m[hh] = -INFINITY; l[hh] = 0.f;
 #pragma unroll
       for (int u = 0; u < CPL; ++u) {
@@ -575,8 +576,46 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     __syncwarp();
   };
 
-  // write this warp's partial of head hd (slot wg + hd)
-  auto flush = [&](int hd) {
+  // The last warp to finish head hd merges the head's partials (slots
+  // w + hd for the warps w whose chunk range touches it) into the output.
+  auto combine = [&](int b, int h, int hd) {
+    constexpr int CPL = D / 32;
+    const int64_t cs = tab.bprefix[b] + (int64_t)h * tab.nc[b];
+    const int64_t ce = cs + tab.nc[b];
+    const int w0 = (int)(((cs + 1) * W - 1) / N);
+    const int w1 = (int)((ce * W - 1) / N);
+    for (int hh = 0; hh < GQ; ++hh) {
+      auto entry = [&](int w) {
+        return args.part + ((size_t)(w + hd) * GQP + hh) * (D + 2);
+      };
+      float M = -INFINITY;
+      for (int w = w0 + lane; w <= w1; w += 32) M = fmaxf(M, __ldcg(entry(w) + D));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+      float Ls = 0.f;
+      for (int w = w0 + lane; w <= w1; w += 32)
+        Ls += exp2_neg(__ldcg(entry(w) + D) - M) * __ldcg(entry(w) + D + 1);
+      Ls = warp_sum(Ls);
+      float acc[CPL];
+#pragma unroll
+      for (int u = 0; u < CPL; ++u) acc[u] = 0.f;
+      for (int w = w0; w <= w1; ++w) {
+        const float *e = entry(w);
+        const float f = exp2_neg(__ldcg(e + D) - M);
+#pragma unroll
+        for (int u = 0; u < CPL; ++u) acc[u] = fmaf(f, __ldcg(e + lane * CPL + u), acc[u]);
+      }
+      const float inv = 1.0f / Ls;
+      float *out = args.out + ((size_t)b * geo.H_q + h * GQ + hh) * D + lane * CPL;
+#pragma unroll
+      for (int u = 0; u < CPL; ++u) out[u] = acc[u] * inv;
+    }
+  };
+
+  // write this warp's partial of head hd (slot wg + hd); the warp that
+  // completes the head's ticket count merges the partials
+  auto flush = [&](int b, int h, int hd) {
     float Lsum = head_reduce<GQP>(l_run, AddOp());
     float Zt[NJ];
 #pragma unroll
@@ -593,8 +632,6 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
       float *dst = args.part + ((size_t)(wg + hd) * GQP + h_s) * (D + 2);
 #pragma unroll
       for (int mv = 0; mv < KS; ++mv) {
-        constexpr int dummy = 0;
-        (void)dummy;
         const int j = (16 * mv) / G;
         const int vb = (j * GQP) >> 2;
         if ((4 * vb + tig) / GQP != j) continue;
@@ -605,12 +642,27 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
           o0 += ores[h_s * D + c0] * ar;
           o1 += ores[h_s * D + c0 + 1] * ar;
         }
-        *reinterpret_cast<float2 *>(dst + c0) = make_float2(o0, o1);
+        __stcg(reinterpret_cast<float2 *>(dst + c0), make_float2(o0, o1));
       }
       if (gid == 0 && tig < GQP) {
-        dst[D] = mf;
-        dst[D + 1] = Lsum;
+        __stcg(dst + D, mf);
+        __stcg(dst + D + 1, Lsum);
       }
+    }
+    // ticket: the warp that takes the head's last ticket sees every other
+    // warp's partial (each fenced before its increment) and merges them
+    __threadfence();
+    __syncwarp();
+    const int64_t cs = tab.bprefix[b] + (int64_t)h * tab.nc[b];
+    const int64_t ce = cs + tab.nc[b];
+    const unsigned nw = (unsigned)(((ce * W - 1) / N) - (((cs + 1) * W - 1) / N) + 1);
+    unsigned last = 0;
+    if (lane == 0) last = atomicAdd(&args.cnt[hd], 1u) == nw - 1 ? 1u : 0u;
+    last = __shfl_sync(kFull, last, 0);
+    if (last) {
+      __threadfence();
+      combine(b, h, hd);
+      if (lane == 0) args.cnt[hd] = 0;
     }
     __syncwarp();
   };
@@ -718,12 +770,14 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
         }
       l_run = l_run * alpha + psum;
       m_run = m_new;
+      if (__any_sync(kFull, alpha != 1.f)) {   // some lane's max moved
 #pragma unroll
-      for (int mv = 0; mv < KS; ++mv)
+        for (int mv = 0; mv < KS; ++mv)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) O[mv][r] *= alpha;
+          for (int r = 0; r < 4; ++r) O[mv][r] *= alpha;
 #pragma unroll
-      for (int j = 0; j < NJ; ++j) Z[j] *= alpha;
+        for (int j = 0; j < NJ; ++j) Z[j] *= alpha;
+      }
 
       // ---- values: K-step kt = tokens 16kt ... 16kt+15 of the chunk.  K
       // slots (2tig, 2tig+1, 2tig+8, 2tig+9) <-> tokens (tig, tig+4, tig+8,
@@ -783,7 +837,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
       }
     }
     const bool head_ends = cu.k == tab.nc[cu.b] - 1 || i == n_mine - 1;
-    if (head_ends) flush(hd);
+    if (head_ends) flush(cu.b, cu.h, hd);
     __syncwarp();
     if (i + ST < n_mine) {
       if (is_quant(pc)) {

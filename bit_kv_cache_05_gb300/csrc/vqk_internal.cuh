@@ -106,6 +106,7 @@ struct MmaArgs {
   const __half *q;   // [B][H_q][D]
   float *out;        // [B][H_q][D]
   float *part;       // partials: slot (warp + head) x GQp x (D + 2)
+  unsigned *cnt;     // per-head tickets, [B * H_kv], zero between launches
   unsigned *err;     // set to nonzero when a pipeline wait gave up
   float scale_log2;  // softmax scale * log2(e)
   int N;             // total chunks
