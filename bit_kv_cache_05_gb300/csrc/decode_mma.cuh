@@ -293,10 +293,11 @@ struct Cfg {
   static constexpr uint32_t S_VS = S_KZ + KG * D * 2;
   static constexpr uint32_t S_VZ = S_VS + kC * NJ * 2;
   static constexpr uint32_t S_BYTES = (S_VZ + kC * NJ * 2 + 127) / 128 * 128;
-  // per-warp layout: [mbarriers][q' GQP x D f32 in slot order][residual o
-  // GQP x D f32][residual m, l][stages]
+  // per-warp layout: [mbarriers][q' GQP x D f32 in slot order][q' GQP x D
+  // f32 in channel order][residual o GQP x D f32][residual m, l][stages]
   static constexpr uint32_t W_QF = 128;
-  static constexpr uint32_t W_ORES = W_QF + GQP * D * 4;
+  static constexpr uint32_t W_QN = W_QF + GQP * D * 4;
+  static constexpr uint32_t W_ORES = W_QN + GQP * D * 4;
   static constexpr uint32_t W_MRES = W_ORES + GQP * D * 4;
   static constexpr uint32_t W_STAGE0 = (W_MRES + 32 + 127) / 128 * 128;
   static __host__ __device__ constexpr uint32_t warp_bytes(int ST) {
@@ -381,6 +382,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   unsigned char *ws = smem + warp * C::warp_bytes(ST);
   uint64_t *bars = reinterpret_cast<uint64_t *>(ws);
   float *qf = reinterpret_cast<float *>(ws + C::W_QF);      // [GQP][KS][4 tig][4 e]
+  float *qn = reinterpret_cast<float *>(ws + C::W_QN);      // [GQP][D]
   float *ores = reinterpret_cast<float *>(ws + C::W_ORES);  // [GQP][D]
   float *mres = reinterpret_cast<float *>(ws + C::W_MRES);  // m[4], l[4]
   unsigned char *stage0 = ws + C::W_STAGE0;
@@ -475,6 +477,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
         v = __half2float(args.q[((size_t)b * geo.H_q + h * GQ + hh) * D + c]) *
             args.scale_log2;
       qf[i] = v;
+      qn[hh * D + c] = v;
     }
     __syncwarp();
   };
@@ -522,48 +525,84 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     unscale_t = exp2i(24 - __shfl_sync(kFull, k, 8 * tig));
   };
 
-  // residual window of head (b, h): CUDA cores, lanes own channels
+  // residual window of head (b, h) on the CUDA cores, 32 tokens at a time:
+  // each lane scores one token (its whole key row against every query
+  // head), then the block's values are accumulated with lanes owning
+  // channels.  Many independent loads are in flight at once.
   auto residual = [&](int b, int hd) {
     constexpr int CPL = D / 32;
     const int Tq = tab.Tq[b], nres = tab.nres[b];
-    float m[GQP], l[GQP], o[GQP][CPL], qv[GQP][CPL];
+    float m[GQP], l[GQP], o[GQP][CPL];
 #pragma unroll
     for (int hh = 0; hh < GQP; ++hh) {
       m[hh] = -INFINITY; l[hh] = 0.f;
 #pragma unroll
-      for (int u = 0; u < CPL; ++u) {
-        o[hh][u] = 0.f;
-        const int c = lane * CPL + u;
-        // q' of channel c from the slot-ordered copy
-        int ks = c >> 4, cc = c & 15, t, e;
-        if constexpr (C::BITS == 2) { t = cc & 3; e = ((cc >> 3) & 1) | (((cc >> 2) & 1) << 1); }
-        else if constexpr (C::BITS == 4) { t = cc & 3; e = cc >> 2; }
-        else { t = cc >> 2; e = ((cc & 1) << 1) | ((cc >> 1) & 1); }
-        qv[hh][u] = qf[((hh * KS + ks) * 4 + t) * 4 + e];
-      }
+      for (int u = 0; u < CPL; ++u) o[hh][u] = 0.f;
     }
-    for (int i = 0; i < nres; ++i) {
-      const int slot = (Tq + i) % geo.Rcap;
-      const size_t base = ((size_t)hd * geo.Rcap + slot) * D + lane * CPL;
-      float kv[CPL], vv[CPL];
+    for (int base = 0; base < nres; base += 32) {
+      const int t = base + lane;
+      const bool valid = t < nres;
+      const int slot = (Tq + (valid ? t : 0)) % geo.Rcap;
+      const uint4 *krow = reinterpret_cast<const uint4 *>(
+          pl.Kr + ((size_t)hd * geo.Rcap + slot) * D);
+      float sc[GQP];
 #pragma unroll
-      for (int u = 0; u < CPL; ++u) {
-        kv[u] = __half2float(pl.Kr[base + u]);
-        vv[u] = __half2float(pl.Vr[base + u]);
+      for (int hh = 0; hh < GQP; ++hh) sc[hh] = 0.f;
+#pragma unroll 4
+      for (int q8 = 0; q8 < D / 8; ++q8) {
+        const uint4 kw = krow[q8];
+        const __half2 *kh = reinterpret_cast<const __half2 *>(&kw);
+        float kf[8];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float2 f = __half22float2(kh[u]);
+          kf[2 * u] = f.x; kf[2 * u + 1] = f.y;
+        }
+#pragma unroll
+        for (int hh = 0; hh < GQP; ++hh) {
+          const float4 qa = reinterpret_cast<const float4 *>(qn + hh * D)[2 * q8];
+          const float4 qb = reinterpret_cast<const float4 *>(qn + hh * D)[2 * q8 + 1];
+          sc[hh] = fmaf(qa.x, kf[0], fmaf(qa.y, kf[1], fmaf(qa.z, kf[2],
+                   fmaf(qa.w, kf[3], fmaf(qb.x, kf[4], fmaf(qb.y, kf[5],
+                   fmaf(qb.z, kf[6], fmaf(qb.w, kf[7], sc[hh]))))))));
+        }
       }
+      float pv[GQP];
 #pragma unroll
       for (int hh = 0; hh < GQP; ++hh) {
-        if (hh >= GQ) break;
-        float part = 0.f;
+        const float s_ = valid ? sc[hh] : -INFINITY;
+        float mb = s_;
 #pragma unroll
-        for (int u = 0; u < CPL; ++u) part = fmaf(qv[hh][u], kv[u], part);
-        const float s = warp_sum(part);
-        const float mn = fmaxf(m[hh], s);
-        const float al = exp2_neg(m[hh] - mn), p = exp2_neg(s - mn);
-        l[hh] = l[hh] * al + p;
+        for (int off = 16; off > 0; off >>= 1)
+          mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, off));
+        const float mn = fmaxf(m[hh], mb);
+        const float al = m[hh] == -INFINITY ? 0.f : exp2_neg(m[hh] - mn);
+        pv[hh] = exp2_neg(s_ - mn);
+        l[hh] = l[hh] * al + warp_sum(pv[hh]);
 #pragma unroll
-        for (int u = 0; u < CPL; ++u) o[hh][u] = o[hh][u] * al + p * vv[u];
+        for (int u = 0; u < CPL; ++u) o[hh][u] *= al;
         m[hh] = mn;
+      }
+      const int nb = nres - base < 32 ? nres - base : 32;
+      for (int tt = 0; tt < nb; ++tt) {
+        const int sl = (Tq + base + tt) % geo.Rcap;
+        const __half *vr = pl.Vr + ((size_t)hd * geo.Rcap + sl) * D + lane * CPL;
+        float vf[CPL];
+        if constexpr (CPL == 4) {
+          const uint2 raw = *reinterpret_cast<const uint2 *>(vr);
+          const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
+          const float2 c = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
+          vf[0] = a.x; vf[1] = a.y; vf[2] = c.x; vf[3] = c.y;
+        } else {
+          const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(vr));
+          vf[0] = a.x; vf[1] = a.y;
+        }
+#pragma unroll
+        for (int hh = 0; hh < GQP; ++hh) {
+          const float pt = __shfl_sync(kFull, pv[hh], tt);
+#pragma unroll
+          for (int u = 0; u < CPL; ++u) o[hh][u] = fmaf(pt, vf[u], o[hh][u]);
+        }
       }
     }
 #pragma unroll
