@@ -164,10 +164,11 @@ __device__ __forceinline__ void load_halves(const __half *p, float (&out)[NJ]) {
 //
 // Score A fragment (rows = 16 tokens, K = 16 channels of K-step ks): lane
 // (gid, tig) holds K slots 2tig, 2tig+1 (register "lo") and 2tig+8, 2tig+9
-// ("hi") of tokens gid and gid+8.  slot_ch(tig, e), e = 0..3, is the channel
-// of those four slots.  The codes arrive scaled by 2^(score_pos(tig) - 24);
-// the score B operand is scaled by 2^-score_pos(tig) so every product carries
-// exactly 2^-24.  Words: a uint4 of a token row holds WPQ K-steps.
+// ("hi") of tokens gid and gid+8; those four slots are channels 4tig ...
+// 4tig+3 of the K-step, slot e (0..3) being channel 4tig + off(e).  The code
+// of slot e arrives scaled by 2^(sexp(e) - 24); the score B operand carries
+// 2^-sexp(e) (folded into a copy of q'), so every product carries exactly
+// 2^-24.  Words: a uint4 of a token row holds WPQ K-steps.
 //
 // Value A fragment (rows = channels 2gid, 2gid+1 of an m16 tile, K = tokens
 // of the K-step): lane (gid, tig) permutes the bytes of two tokens' words
@@ -180,17 +181,22 @@ template <int BITS> struct Layout;
 template <> struct Layout<2> {
   static constexpr int WPQ = 4;    // K-steps per uint4 (one word each)
   static constexpr int VTPQ = 4;   // value tiles per uint4
-  static __device__ __forceinline__ void score_a(const uint4 &q, int ks, int tig,
-                                                 uint32_t &lo, uint32_t &hi) {
-    const uint32_t w = (&q.x)[ks & 3];
-    const uint32_t m = 0x00030003u << (2 * tig);
-    lo = w & m;            // channels tig, tig+8
-    hi = (w >> 8) & m;     // channels tig+4, tig+12
+  // byte tig of word ks holds channels 4tig..4tig+3; the byte is copied to
+  // every byte position and each slot's 2-bit field masked in place
+  static __device__ __forceinline__ uint32_t score_sel(int tig) {
+    return 0x1111u * (uint32_t)tig;
   }
-  static __device__ __forceinline__ int slot_ch(int tig, int e) {
-    return tig + 8 * (e & 1) + 4 * (e >> 1);
+  static __device__ __forceinline__ void score_a(const uint4 &q, int ks,
+                                                 uint32_t sel, uint32_t &lo,
+                                                 uint32_t &hi) {
+    const uint32_t x = __byte_perm((&q.x)[ks & 3], 0u, sel);
+    lo = x & 0x000C0003u;   // channel 4tig (x1), 4tig+1 (x4)
+    hi = x & 0x00C00030u;   // channel 4tig+2 (x16), 4tig+3 (x64)
   }
-  static __device__ __forceinline__ int score_pos(int tig) { return 2 * tig; }
+  static __host__ __device__ constexpr int off(int e) { return e; }
+  static __host__ __device__ constexpr int sexp(int e) { return 2 * e; }
+  // exponent of the slot that holds channel offset o (0..3)
+  static __device__ __forceinline__ int oexp(int o) { return 2 * o; }
   // word of m16 tile u (0..VTPQ-1) within a uint4 of a token row
   static __device__ __forceinline__ uint32_t vword(const uint4 &x, int u, int) {
     return (&x.x)[u];
@@ -211,17 +217,23 @@ template <> struct Layout<2> {
 template <> struct Layout<4> {
   static constexpr int WPQ = 2;
   static constexpr int VTPQ = 2;
-  static __device__ __forceinline__ void score_a(const uint4 &q, int ks, int tig,
-                                                 uint32_t &lo, uint32_t &hi) {
-    const uint32_t sh = 8 * (tig >> 1);
-    const uint32_t m = 0x000F000Fu << (4 * (tig & 1));
-    lo = ((&q.x)[2 * (ks & 1)] >> sh) & m;      // channels tig, tig+4
-    hi = ((&q.x)[2 * (ks & 1) + 1] >> sh) & m;  // channels 8+tig, 12+tig
+  // channels 4tig..4tig+3 are bytes B0 = 2(tig&1) and B0+1 of word
+  // 2ks + tig/2; one byte_perm picks the word and places B0 at bytes 0-1 and
+  // B0+1 at bytes 2-3
+  static __device__ __forceinline__ uint32_t score_sel(int tig) {
+    const uint32_t b = 2 * (tig & 1) + 4 * (tig >> 1);
+    return b | (b << 4) | ((b + 1) << 8) | ((b + 1) << 12);
   }
-  static __device__ __forceinline__ int slot_ch(int tig, int e) {
-    return tig + 4 * e;
+  static __device__ __forceinline__ void score_a(const uint4 &q, int ks,
+                                                 uint32_t sel, uint32_t &lo,
+                                                 uint32_t &hi) {
+    const uint32_t x = __byte_perm((&q.x)[2 * (ks & 1)], (&q.x)[2 * (ks & 1) + 1], sel);
+    lo = x & 0x000F000Fu;   // channel 4tig (x1), 4tig+2 (x1)
+    hi = x & 0x00F000F0u;   // channel 4tig+1 (x16), 4tig+3 (x16)
   }
-  static __device__ __forceinline__ int score_pos(int tig) { return 4 * (tig & 1); }
+  static __host__ __device__ constexpr int off(int e) { return (e & 1) * 2 + (e >> 1); }
+  static __host__ __device__ constexpr int sexp(int e) { return 4 * (e >> 1); }
+  static __device__ __forceinline__ int oexp(int o) { return 4 * (o & 1); }
   static __device__ __forceinline__ uint32_t vword(const uint4 &x, int u, int gid) {
     const uint32_t w0 = u ? x.z : x.x, w1 = u ? x.w : x.y;
     return (gid >> 2) ? w1 : w0;   // word 2u + gid/4
@@ -242,16 +254,18 @@ template <> struct Layout<4> {
 template <> struct Layout<8> {
   static constexpr int WPQ = 1;    // uint4 = one K-step (4 words, one per tig)
   static constexpr int VTPQ = 1;
-  static __device__ __forceinline__ void score_a(const uint4 &q, int, int tig,
-                                                 uint32_t &lo, uint32_t &hi) {
+  // channels 4tig..4tig+3 are the bytes of word 4ks + tig (sel carries tig)
+  static __device__ __forceinline__ uint32_t score_sel(int tig) { return tig; }
+  static __device__ __forceinline__ void score_a(const uint4 &q, int,
+                                                 uint32_t tig, uint32_t &lo,
+                                                 uint32_t &hi) {
     const uint32_t w = (tig & 2) ? ((tig & 1) ? q.w : q.z) : ((tig & 1) ? q.y : q.x);
     lo = w & 0x00FF00FFu;          // channels 4tig, 4tig+2
     hi = (w >> 8) & 0x00FF00FFu;   // channels 4tig+1, 4tig+3
   }
-  static __device__ __forceinline__ int slot_ch(int tig, int e) {
-    return 4 * tig + 2 * (e & 1) + (e >> 1);
-  }
-  static __device__ __forceinline__ int score_pos(int) { return 0; }
+  static __host__ __device__ constexpr int off(int e) { return (e & 1) * 2 + (e >> 1); }
+  static __host__ __device__ constexpr int sexp(int) { return 0; }
+  static __device__ __forceinline__ int oexp(int) { return 0; }
   static __device__ __forceinline__ uint32_t vword(const uint4 &x, int, int gid) {
     // word gid/2: bit 1 of gid picks the odd word, bit 2 the upper pair
     return (gid & 4) ? ((gid & 2) ? x.w : x.z) : ((gid & 2) ? x.y : x.x);
@@ -293,8 +307,9 @@ struct Cfg {
   static constexpr uint32_t S_VS = S_KZ + KG * D * 2;
   static constexpr uint32_t S_VZ = S_VS + kC * NJ * 2;
   static constexpr uint32_t S_BYTES = (S_VZ + kC * NJ * 2 + 127) / 128 * 128;
-  // per-warp layout: [mbarriers][q' GQP x D f32 in slot order][q' GQP x D
-  // f32 in channel order][residual o GQP x D f32][residual m, l][stages]
+  // per-warp layout: [mbarriers][q' GQP x D f32, channel c scaled by the
+  // 2^-sexp of its score slot][q' GQP x D f32][residual o GQP x D f32]
+  // [residual m, l][stages]
   static constexpr uint32_t W_QF = 128;
   static constexpr uint32_t W_QN = W_QF + GQP * D * 4;
   static constexpr uint32_t W_ORES = W_QN + GQP * D * 4;
@@ -381,7 +396,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
 
   unsigned char *ws = smem + warp * C::warp_bytes(ST);
   uint64_t *bars = reinterpret_cast<uint64_t *>(ws);
-  float *qf = reinterpret_cast<float *>(ws + C::W_QF);      // [GQP][KS][4 tig][4 e]
+  float *qb = reinterpret_cast<float *>(ws + C::W_QF);      // [GQP][D], slot-scaled
   float *qn = reinterpret_cast<float *>(ws + C::W_QN);      // [GQP][D]
   float *ores = reinterpret_cast<float *>(ws + C::W_ORES);  // [GQP][D]
   float *mres = reinterpret_cast<float *>(ws + C::W_MRES);  // m[4], l[4]
@@ -433,7 +448,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   bool failed = false;
 
   // ---- per-lane constants ------------------------------------------------
-  const float bsc = exp2i(-L::score_pos(tig));
+  const uint32_t s_sel = L::score_sel(tig);
   const uint32_t v_sel = L::vsel(gid);
   const float rs0 = exp2i(24 - L::vpos0(gid)), rs1 = exp2i(24 - L::vpos1(gid));
   const int hl = gid & 1;               // B operand column: hi (0) or lo (1)
@@ -465,19 +480,17 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     has_res = false;
   };
 
-  // q' of the head's GQP query heads, stored in score-slot order:
-  // qf[((h * KS + ks) * 4 + tig) * 4 + e] = q'[h][16 ks + slot_ch(tig, e)]
+  // q' of the head's GQP query heads: qn in channel order, qb with channel
+  // c scaled by 2^-sexp of its score slot
   auto load_q = [&](int b, int h) {
     for (int i = lane; i < GQP * D; i += 32) {
-      const int hh = i / D, r = i - hh * D;
-      const int ks = r >> 4, t = (r >> 2) & 3, e = r & 3;
-      const int c = 16 * ks + L::slot_ch(t, e);
+      const int hh = i / D, c = i - hh * D;
       float v = 0.f;
       if (hh < GQ)
         v = __half2float(args.q[((size_t)b * geo.H_q + h * GQ + hh) * D + c]) *
             args.scale_log2;
-      qf[i] = v;
-      qn[hh * D + c] = v;
+      qn[i] = v;
+      qb[i] = v * exp2i(-L::oexp(c & 3));
     }
     __syncwarp();
   };
@@ -490,20 +503,24 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   // stay in fp16's normal range.
   auto build_score_b = [&](const __half *Ks, const __half *Kz, int gw0, int kg0) {
     const int gr = gw0 + pair_b / GQP - kg0;   // group row in the region
-    const float4 *qh = reinterpret_cast<const float4 *>(qf) + (h_b * KS) * 4 + tig;
-    const __half *ksr = Ks + gr * D;
-    const __half *kzr = Kz + gr * D;
+    const float *qbh = qb + h_b * D + 4 * tig;
+    const float *qnh = qn + h_b * D + 4 * tig;
+    const __half *ksr = Ks + gr * D + 4 * tig;
+    const __half *kzr = Kz + gr * D + 4 * tig;
     float av[KS][4];
     float zpart = 0.f, amax = 0.f;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      const float4 q4 = qh[ks * 4];
-      const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+      const float4 qs = *reinterpret_cast<const float4 *>(qbh + 16 * ks);
+      const float4 qz = *reinterpret_cast<const float4 *>(qnh + 16 * ks);
+      float kf[4], zf[4];
+      load_halves<4>(ksr + 16 * ks, kf);
+      load_halves<4>(kzr + 16 * ks, zf);
+      const float a[4] = {qs.x * kf[0], qs.y * kf[1], qs.z * kf[2], qs.w * kf[3]};
+      zpart = fmaf(qz.x, zf[0], fmaf(qz.y, zf[1], fmaf(qz.z, zf[2], fmaf(qz.w, zf[3], zpart))));
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int c = 16 * ks + L::slot_ch(tig, e);
-        av[ks][e] = qv[e] * __half2float(ksr[c]) * bsc;
-        zpart = fmaf(qv[e], __half2float(kzr[c]), zpart);
+        av[ks][e] = a[L::off(e)];
         amax = fmaxf(amax, fabsf(av[ks][e]));
       }
     }
@@ -773,8 +790,8 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
               for (int m = 0; m < MPW; ++m) {
                 if (mt0 + m < nmt) {
                   uint32_t a0, a1, a2, a3;
-                  L::score_a(r0[m], ks, tig, a0, a2);
-                  L::score_a(r1[m], ks, tig, a1, a3);
+                  L::score_a(r0[m], ks, s_sel, a0, a2);
+                  L::score_a(r1[m], ks, s_sel, a1, a3);
                   mma16816(acc[m], a0, a1, a2, a3, Bs[ks][0], Bs[ks][1]);
                 }
               }
@@ -839,19 +856,31 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
           const float p2 = __shfl_sync(kFull, p[kt][1], 4 * tig + src);
           const float p3 = __shfl_sync(kFull, p[kt][1], 4 * tig + 16 + src);
           const int ta = 16 * kt + tig;
+          // s_V of the four tokens: whole rows when every block needs a
+          // different group, single values otherwise
+          float vs[4][C::NVB];
+          if constexpr (C::NVB == NJ && NJ >= 2) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              float row[NJ];
+              load_halves<NJ>(Vs + (ta + 4 * u) * NJ, row);
+#pragma unroll
+              for (int vb = 0; vb < C::NVB; ++vb) vs[u][vb] = row[(4 * vb + pair_b) / GQP];
+            }
+          } else {
+#pragma unroll
+            for (int vb = 0; vb < C::NVB; ++vb) {
+              const int jb = (4 * vb + pair_b) / GQP;
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                vs[u][vb] = jb < NJ ? __half2float(Vs[(ta + 4 * u) * NJ + jb]) : 0.f;
+            }
+          }
           uint32_t bv[C::NVB][2];
 #pragma unroll
           for (int vb = 0; vb < C::NVB; ++vb) {
-            const int jb = (4 * vb + pair_b) / GQP;
-            float w0 = 0.f, w1 = 0.f, w2 = 0.f, w3 = 0.f;
-            if (jb < NJ) {
-              w0 = hilo(p0 * __half2float(Vs[ta * NJ + jb]), hl);
-              w1 = hilo(p1 * __half2float(Vs[(ta + 4) * NJ + jb]), hl);
-              w2 = hilo(p2 * __half2float(Vs[(ta + 8) * NJ + jb]), hl);
-              w3 = hilo(p3 * __half2float(Vs[(ta + 12) * NJ + jb]), hl);
-            }
-            bv[vb][0] = pack_half2(w0, w1);
-            bv[vb][1] = pack_half2(w2, w3);
+            bv[vb][0] = pack_half2(hilo(p0 * vs[0][vb], hl), hilo(p1 * vs[1][vb], hl));
+            bv[vb][1] = pack_half2(hilo(p2 * vs[2][vb], hl), hilo(p3 * vs[3][vb], hl));
           }
           // m16 channel tiles, VTPQ per uint4 of the token rows
 #pragma unroll
