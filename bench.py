@@ -156,6 +156,35 @@ def barrier(world: int):
         dist.barrier()
 
 
+DECODE_KERNEL_SOURCES = ("bit_kv_cache_05_gb300/csrc/decode_mma.cuh",
+                         "bit_kv_cache_05_gb300/csrc/decode_mma.cu")
+
+
+def decode_kernel_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in DECODE_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes (read + write) of one decode launch from the committed ncu
+    summary, or None when there is none for this workload or the kernel
+    source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(workload)
+    if not entry or entry.get("kernel_source_sha") != decode_kernel_hash():
+        return None
+    return int(entry["dram_bytes_per_launch"])
+
+
 def measured_peak_gbs():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -362,8 +391,9 @@ def run_ours(args, w, rank, world, local):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": None, "peak_kind": peak_kind,
-                     "kernel": "fused decode-attend (split + combine)",
+                     "traffic": measured_traffic(w.name),
+                     "peak_kind": peak_kind,
+                     "kernel": "fused decode-attend (one launch)",
                      "algorithmic_bytes": dec_bytes},
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_ms * 1e3, 3), "unit": UNIT,

@@ -28,7 +28,8 @@ EXPORTS = ("vq_kivi_quantize", "vq_kivi_append", "vq_kivi_decode_attend",
            "vq_kivi_get_params", "vq_kivi_plane_bytes", "vq_kivi_export",
            "vq_kivi_cache_bytes", "vq_kivi_set_split_tokens",
            "vq_kivi_launch_count", "vq_kivi_decode_attend_static",
-           "vq_kivi_device_status", "vq_kivi_decode_kernel")
+           "vq_kivi_device_status", "vq_kivi_decode_kernel",
+           "vq_kivi_debug_fail_chunk")
 
 
 class VqError(RuntimeError):
@@ -90,6 +91,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         L.vq_kivi_set_split_tokens.argtypes = [P, i32]
         L.vq_kivi_device_status.argtypes = [P]
         L.vq_kivi_decode_kernel.argtypes = [P]
+        L.vq_kivi_debug_fail_chunk.argtypes = [P, i32]
         L.vq_kivi_launch_count.restype = ctypes.c_uint64
         L.vq_kivi_decode_attend_static.argtypes = [
             ctypes.POINTER(Params), ctypes.POINTER(Planes), P, P, P,

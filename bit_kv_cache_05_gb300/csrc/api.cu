@@ -24,6 +24,7 @@ struct vq_kivi_cache {
   int32_t split_tokens;   // 0 = automatic
   int32_t tps_min;        // smallest split the workspace allows
   bool use_mma;           // tensor-core decode kernel for this shape
+  int32_t fail_chunk;     // testing hook, -1 = off
   MmaPlan plan;
   unsigned *err;          // device word set by a kernel whose wait gave up
   unsigned *tickets;      // per-head tickets of the tensor-core decode
@@ -146,6 +147,7 @@ int vq_kivi_quantize(const vq_kivi_params *p, const void *K, const void *V,
   vq_kivi_cache *c = new (std::nothrow) vq_kivi_cache();
   if (!c) return fail(VQ_ERR_OOM, "host allocation of the cache handle failed");
   c->p = *p;
+  c->fail_chunk = -1;
   cudaError_t e = cudaGetDevice(&c->device);
   if (e == cudaSuccess)
     e = cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount,
@@ -341,6 +343,8 @@ int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
     args.err = c->err;
     args.scale_log2 = scale * 1.4426950408889634f;
     args.N = tab.bprefix[p.B];
+    args.fail_chunk = c->fail_chunk;
+    c->fail_chunk = -1;
     MmaPlan plan = c->plan;
     if (c->split_tokens > 0) {
       // a fixed partition: about split_tokens quantized tokens per warp
@@ -491,6 +495,12 @@ int vq_kivi_device_status(vq_kivi_cache *c) {
     return fail(VQ_ERR_CUDA, "a decode kernel gave up waiting for its "
                 "shared-memory copies; its outputs are not valid");
   }
+  return VQ_OK;
+}
+
+int vq_kivi_debug_fail_chunk(vq_kivi_cache *c, int32_t chunk) {
+  if (!c) return fail(VQ_ERR_ARG, "cache is NULL");
+  c->fail_chunk = chunk < 0 ? -1 : chunk;
   return VQ_OK;
 }
 

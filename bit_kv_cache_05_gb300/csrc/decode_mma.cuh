@@ -409,7 +409,8 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   __syncwarp();
 
   // ---- producer: lane 0 issues the bulk copies of the chunk at `cu` -----
-  auto issue = [&](const Cursor &cu, int s) {
+  auto issue = [&](const Cursor &cu, int s, int c) {
+    if (c == args.fail_chunk) return;   // testing: a copy that never comes
     const int Tq = tab.Tq[cu.b];
     const int t0 = cu.k * kC;
     const int rem = Tq - t0;
@@ -440,7 +441,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   uint32_t pending = 0;  // bit s = copies in flight into stage s
   for (int i = 0; i < ST && i < n_mine; ++i) {
     if (is_quant(pc)) {
-      if (lane == 0) issue(pc, i);
+      if (lane == 0) issue(pc, i, lo_c + i);
       pending |= 1u << i;
     }
     pc.next(geo, tab);
@@ -911,7 +912,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
       if (is_quant(pc)) {
         if (lane == 0) {
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          issue(pc, s);
+          issue(pc, s, lo_c + i + ST);
         }
         pending |= 1u << s;
       }

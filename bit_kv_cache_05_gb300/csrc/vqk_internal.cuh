@@ -110,6 +110,7 @@ struct MmaArgs {
   unsigned *err;     // set to nonzero when a pipeline wait gave up
   float scale_log2;  // softmax scale * log2(e)
   int N;             // total chunks
+  int fail_chunk;    // testing: chunk whose copies are not issued (-1: none)
   int W;             // warps used (<= N), filled in by the launcher
   int GQ, GQp, KG, ST;
 };

@@ -182,6 +182,15 @@ int vq_kivi_device_status(vq_kivi_cache *c);
  * (D = 64 or 128, H_q/H_kv <= 4), 0 = CUDA-core kernel; < 0 on error. */
 int vq_kivi_decode_kernel(const vq_kivi_cache *c);
 
+/* Testing hook for failure detection.  The next tensor-core decode on this
+ * cache does not issue the shared-memory copies of global chunk `chunk`
+ * (chunks are numbered over sequences, kv heads and 64-token chunks), so
+ * the warp that owns it waits in vain: its bounded wait gives up after about
+ * half a second, the kernel records the failure and returns, and
+ * vq_kivi_device_status reports VQ_ERR_CUDA.  Nothing faults; the outputs
+ * of that decode are not valid.  One-shot; -1 clears it. */
+int vq_kivi_debug_fail_chunk(vq_kivi_cache *c, int32_t chunk);
+
 /* ---- decode without any allocation ------------------------------------- */
 
 /* The pages have no counterpart to this entry point; it exists for callers
