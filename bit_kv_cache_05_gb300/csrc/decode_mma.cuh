@@ -376,8 +376,122 @@ struct Cursor {
   }
 };
 
+// The fp16 residual window of one head on the CUDA cores, 32 tokens at a
+// time: each lane scores one token (its whole key row against every query
+// head), then the block's values are accumulated with lanes owning
+// channels.  Rows are loaded in unrolled batches, all in flight at once, so
+// the window costs a few memory round trips rather than one per token.
+// Writes the window's (o, m, l) per query head to ores / mres.  Kept out of
+// line: it runs once per head, and inlined it would raise the register
+// demand of the whole decode loop.
+template <int D, int GQP>
+__device__ __noinline__ void residual_window(
+    const __half *__restrict__ Kr, const __half *__restrict__ Vr, size_t ring0,
+    int Tq, int nres, int Rcap, int GQ, const float *qn, float *ores,
+    float *mres, int lane) {
+  constexpr int CPL = D / 32;      // value channels per lane
+  constexpr int KQ = D / 8;        // uint4 per key row
+  constexpr int KB = KQ < 4 ? KQ : 4;
+  float m[GQP], l[GQP], o[GQP][CPL];
+#pragma unroll
+  for (int hh = 0; hh < GQP; ++hh) {
+    m[hh] = -INFINITY; l[hh] = 0.f;
+#pragma unroll
+    for (int u = 0; u < CPL; ++u) o[hh][u] = 0.f;
+  }
+  for (int base = 0; base < nres; base += 32) {
+    const int t = base + lane;
+    const bool valid = t < nres;
+    const uint4 *krow = reinterpret_cast<const uint4 *>(
+        Kr + (ring0 + (Tq + (valid ? t : 0)) % Rcap) * D);
+    float sc[GQP];
+#pragma unroll
+    for (int hh = 0; hh < GQP; ++hh) sc[hh] = 0.f;
+#pragma unroll 1
+    for (int q0 = 0; q0 < KQ; q0 += KB) {
+      uint4 kw[KB];
+#pragma unroll
+      for (int u = 0; u < KB; ++u) kw[u] = krow[q0 + u];
+#pragma unroll
+      for (int u = 0; u < KB; ++u) {
+        const __half2 *kh = reinterpret_cast<const __half2 *>(&kw[u]);
+        float kf[8];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const float2 f = __half22float2(kh[v]);
+          kf[2 * v] = f.x; kf[2 * v + 1] = f.y;
+        }
+#pragma unroll
+        for (int hh = 0; hh < GQP; ++hh) {
+          const float4 qa = reinterpret_cast<const float4 *>(qn + hh * D)[2 * (q0 + u)];
+          const float4 qc = reinterpret_cast<const float4 *>(qn + hh * D)[2 * (q0 + u) + 1];
+          sc[hh] = fmaf(qa.x, kf[0], fmaf(qa.y, kf[1], fmaf(qa.z, kf[2],
+                   fmaf(qa.w, kf[3], fmaf(qc.x, kf[4], fmaf(qc.y, kf[5],
+                   fmaf(qc.z, kf[6], fmaf(qc.w, kf[7], sc[hh]))))))));
+        }
+      }
+    }
+    float pv[GQP];
+#pragma unroll
+    for (int hh = 0; hh < GQP; ++hh) {
+      const float s_ = valid ? sc[hh] : -INFINITY;
+      float mb = s_;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+        mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, off));
+      const float mn = fmaxf(m[hh], mb);
+      const float al = m[hh] == -INFINITY ? 0.f : exp2_neg(m[hh] - mn);
+      pv[hh] = exp2_neg(s_ - mn);
+      l[hh] = l[hh] * al + warp_sum(pv[hh]);
+#pragma unroll
+      for (int u = 0; u < CPL; ++u) o[hh][u] *= al;
+      m[hh] = mn;
+    }
+    const int nb = nres - base < 32 ? nres - base : 32;
+#pragma unroll 1
+    for (int t0 = 0; t0 < nb; t0 += 8) {
+      uint32_t raw[8][CPL / 2];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int tt = t0 + u < nb ? t0 + u : 0;
+        const __half *vr = Vr + (ring0 + (Tq + base + tt) % Rcap) * D + lane * CPL;
+        if constexpr (CPL == 4) {
+          const uint2 r2 = *reinterpret_cast<const uint2 *>(vr);
+          raw[u][0] = r2.x; raw[u][1] = r2.y;
+        } else {
+          raw[u][0] = *reinterpret_cast<const uint32_t *>(vr);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        float vf[CPL];
+#pragma unroll
+        for (int c = 0; c < CPL / 2; ++c) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&raw[u][c]));
+          vf[2 * c] = f.x; vf[2 * c + 1] = f.y;
+        }
+#pragma unroll
+        for (int hh = 0; hh < GQP; ++hh) {
+          // lanes past nb hold p = 0, so their shuffled weight adds nothing
+          const float pt = __shfl_sync(kFull, pv[hh], (t0 + u) & 31);
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) o[hh][c] = fmaf(pt, vf[c], o[hh][c]);
+        }
+      }
+    }
+  }
+  (void)GQ;
+#pragma unroll
+  for (int hh = 0; hh < GQP; ++hh) {
+#pragma unroll
+    for (int u = 0; u < CPL; ++u) ores[hh * D + lane * CPL + u] = o[hh][u];
+    if (lane == 0) { mres[hh] = m[hh]; mres[4 + hh] = l[hh]; }
+  }
+  __syncwarp();
+}
+
 template <class C>
-__global__ void __launch_bounds__(kNW * 32)
+__global__ void __launch_bounds__(kNW * 32, 3)
 k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   using L = Layout<C::BITS>;
   constexpr int D = C::D, KS = C::KS, NJ = C::NJ, GQP = C::GQP, WG = C::WG;
@@ -543,94 +657,10 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     unscale_t = exp2i(24 - __shfl_sync(kFull, k, 8 * tig));
   };
 
-  // residual window of head (b, h) on the CUDA cores, 32 tokens at a time:
-  // each lane scores one token (its whole key row against every query
-  // head), then the block's values are accumulated with lanes owning
-  // channels.  Many independent loads are in flight at once.
   auto residual = [&](int b, int hd) {
-    constexpr int CPL = D / 32;
-    const int Tq = tab.Tq[b], nres = tab.nres[b];
-    float m[GQP], l[GQP], o[GQP][CPL];
-#pragma unroll
-    for (int hh = 0; hh < GQP; ++hh) {
-      m[hh] = -INFINITY; l[hh] = 0.f;
-#pragma unroll
-      for (int u = 0; u < CPL; ++u) o[hh][u] = 0.f;
-    }
-    for (int base = 0; base < nres; base += 32) {
-      const int t = base + lane;
-      const bool valid = t < nres;
-      const int slot = (Tq + (valid ? t : 0)) % geo.Rcap;
-      const uint4 *krow = reinterpret_cast<const uint4 *>(
-          pl.Kr + ((size_t)hd * geo.Rcap + slot) * D);
-      float sc[GQP];
-#pragma unroll
-      for (int hh = 0; hh < GQP; ++hh) sc[hh] = 0.f;
-#pragma unroll 4
-      for (int q8 = 0; q8 < D / 8; ++q8) {
-        const uint4 kw = krow[q8];
-        const __half2 *kh = reinterpret_cast<const __half2 *>(&kw);
-        float kf[8];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float2 f = __half22float2(kh[u]);
-          kf[2 * u] = f.x; kf[2 * u + 1] = f.y;
-        }
-#pragma unroll
-        for (int hh = 0; hh < GQP; ++hh) {
-          const float4 qa = reinterpret_cast<const float4 *>(qn + hh * D)[2 * q8];
-          const float4 qb = reinterpret_cast<const float4 *>(qn + hh * D)[2 * q8 + 1];
-          sc[hh] = fmaf(qa.x, kf[0], fmaf(qa.y, kf[1], fmaf(qa.z, kf[2],
-                   fmaf(qa.w, kf[3], fmaf(qb.x, kf[4], fmaf(qb.y, kf[5],
-                   fmaf(qb.z, kf[6], fmaf(qb.w, kf[7], sc[hh]))))))));
-        }
-      }
-      float pv[GQP];
-#pragma unroll
-      for (int hh = 0; hh < GQP; ++hh) {
-        const float s_ = valid ? sc[hh] : -INFINITY;
-        float mb = s_;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-          mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, off));
-        const float mn = fmaxf(m[hh], mb);
-        const float al = m[hh] == -INFINITY ? 0.f : exp2_neg(m[hh] - mn);
-        pv[hh] = exp2_neg(s_ - mn);
-        l[hh] = l[hh] * al + warp_sum(pv[hh]);
-#pragma unroll
-        for (int u = 0; u < CPL; ++u) o[hh][u] *= al;
-        m[hh] = mn;
-      }
-      const int nb = nres - base < 32 ? nres - base : 32;
-      for (int tt = 0; tt < nb; ++tt) {
-        const int sl = (Tq + base + tt) % geo.Rcap;
-        const __half *vr = pl.Vr + ((size_t)hd * geo.Rcap + sl) * D + lane * CPL;
-        float vf[CPL];
-        if constexpr (CPL == 4) {
-          const uint2 raw = *reinterpret_cast<const uint2 *>(vr);
-          const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
-          const float2 c = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
-          vf[0] = a.x; vf[1] = a.y; vf[2] = c.x; vf[3] = c.y;
-        } else {
-          const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(vr));
-          vf[0] = a.x; vf[1] = a.y;
-        }
-#pragma unroll
-        for (int hh = 0; hh < GQP; ++hh) {
-          const float pt = __shfl_sync(kFull, pv[hh], tt);
-#pragma unroll
-          for (int u = 0; u < CPL; ++u) o[hh][u] = fmaf(pt, vf[u], o[hh][u]);
-        }
-      }
-    }
-#pragma unroll
-    for (int hh = 0; hh < GQP; ++hh) {
-#pragma unroll
-      for (int u = 0; u < CPL; ++u) ores[hh * D + lane * CPL + u] = o[hh][u];
-      if (lane == 0) { mres[hh] = m[hh]; mres[4 + hh] = l[hh]; }
-    }
-    has_res = nres > 0;
-    __syncwarp();
+    residual_window<D, GQP>(pl.Kr, pl.Vr, (size_t)hd * geo.Rcap, tab.Tq[b],
+                            tab.nres[b], geo.Rcap, GQ, qn, ores, mres, lane);
+    has_res = tab.nres[b] > 0;
   };
 
   // The last warp to finish head hd merges the head's partials (slots

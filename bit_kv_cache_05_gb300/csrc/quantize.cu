@@ -38,13 +38,26 @@ __device__ __forceinline__ uint32_t quant_code(float x, float mn, float scale,
   return (uint32_t)r;
 }
 
-__device__ __forceinline__ void load4(const __half *row, int c, float v[4]) {
-  // 4 consecutive fp16 channels starting at c (c % 4 == 0): one 8-byte load
-  uint2 raw = *reinterpret_cast<const uint2 *>(row + c);
-  __half2 a = *reinterpret_cast<__half2 *>(&raw.x);
-  __half2 b = *reinterpret_cast<__half2 *>(&raw.y);
-  float2 fa = __half22float2(a), fb = __half22float2(b);
-  v[0] = fa.x; v[1] = fa.y; v[2] = fb.x; v[3] = fb.y;
+// The same code as quant_code, mostly without a division.  With
+// r = RN(1/scale), t' = RN((x - min) * r) differs from the correctly
+// rounded quotient t = RN((x - min) / scale) by at most 1.5 * 2^-23 * t'
+// (two roundings of 2^-24 each against the exact quotient, one more for t).
+// rint(t') and rint(t) can only differ if a half-integer lies within that
+// distance of t' (or t is itself a half-integer), so whenever t' is further
+// than 2^-20 * t' + 2^-30 from the nearest half-integer, rint(t') is the
+// answer; otherwise the exact quotient decides.
+__device__ __forceinline__ uint32_t quant_code_fast(float x, float mn,
+                                                    float scale, float rcp,
+                                                    int levels) {
+  if (scale == 0.0f) return 0u;
+  const float d = __fsub_rn(x, mn);
+  float t = __fmul_rn(d, rcp);
+  const float frac = t - floorf(t);
+  if (fabsf(frac - 0.5f) <= fmaf(t, 9.5367431640625e-7f, 1e-9f))
+    t = __fdiv_rn(d, scale);
+  float r = rintf(t);
+  r = fminf(fmaxf(r, 0.0f), (float)levels);
+  return (uint32_t)r;
 }
 
 // Packs the g x D code tile in shared memory into rows of D*BITS/8 bytes and
@@ -73,110 +86,93 @@ __device__ __forceinline__ void store_packed_tile(const uint8_t *codes, int g,
   }
 }
 
-// One block = one group of g tokens of one (b, h): key codes per channel,
-// value codes per token.
+// Copies the g fp16 rows of one group (token positions P0 ... P0+g-1) into a
+// shared tile [g][D] with 16-byte loads, all in flight at once.  Position p
+// comes from the residual ring when p < split, else from input row p - split.
+__device__ __forceinline__ void load_tile(__half *tile, const __half *ring,
+                                          const __half *in, size_t bh,
+                                          int64_t in_stride, int P0, int split,
+                                          int g, int D, int Rcap) {
+  const int cpr = D / 8;
+  for (int idx = threadIdx.x; idx < g * cpr; idx += blockDim.x) {
+    const int i = idx / cpr, c8 = (idx - i * cpr) * 8;
+    const int p = P0 + i;
+    const __half *src = p < split ? ring + (bh * Rcap + (p % Rcap)) * D
+                                  : in + (bh * in_stride + (p - split)) * D;
+    *reinterpret_cast<uint4 *>(tile + i * D + c8) =
+        *reinterpret_cast<const uint4 *>(src + c8);
+  }
+}
+
+// One block = one group of g tokens of one (b, h), one thread per channel
+// (D threads): the group's key rows, then its value rows, are staged in a
+// shared tile; keys are quantized per channel (thread c walks column c),
+// values per (token, channel group) (thread t takes token t / (D/g), group
+// t % (D/g)).
 template <int BITS>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kMaxD)
 k_flush(Geometry geo, Planes pl, const __half *__restrict__ Kin,
         const __half *__restrict__ Vin, int64_t in_stride, FlushTable tab) {
   constexpr int levels = (1 << BITS) - 1;
-  __shared__ uint8_t codes[128 * kMaxD];  // g x D, g <= 128
-  __shared__ float red_mn[kThreads * 4], red_mx[kThreads * 4];
-  __shared__ float ch_mn[kMaxD], ch_scale[kMaxD];
-
+  extern __shared__ __align__(16) unsigned char fsm[];
   const int D = geo.D, g = geo.g, H = geo.H_kv;
+  __half *tile = reinterpret_cast<__half *>(fsm);                 // [g][D]
+  uint8_t *codes = fsm + (size_t)g * D * sizeof(__half);         // [g][D]
+
   const int item = blockIdx.x, h = blockIdx.y;
   const int b = find_seq(tab.prefix, geo.B, item);
   const int P0 = tab.first_pos[b] + (item - tab.prefix[b]) * g;
   const int split = tab.src_split[b];
   const size_t bh = (size_t)b * H + h;
-
-  const int qpr = D / 4;                 // channel quads per row
-  const int cq = threadIdx.x % qpr;
-  const int r = threadIdx.x / qpr;
-  const int RP = kThreads / qpr;         // rows handled in parallel
-  const int c0 = 4 * cq;
-
-  auto key_row = [&](int i) -> const __half * {
-    const int p = P0 + i;
-    if (p < split) return pl.Kr + (bh * geo.Rcap + (p % geo.Rcap)) * D;
-    return Kin + (bh * in_stride + (p - split)) * D;
-  };
-  auto val_row = [&](int i) -> const __half * {
-    const int p = P0 + i;
-    if (p < split) return pl.Vr + (bh * geo.Rcap + (p % geo.Rcap)) * D;
-    return Vin + (bh * in_stride + (p - split)) * D;
-  };
+  const int c = threadIdx.x;   // blockDim.x == D
 
   // ---- keys: per channel over the g tokens ----
-  float mn[4], mx[4];
-#pragma unroll
-  for (int u = 0; u < 4; ++u) { mn[u] = INFINITY; mx[u] = -INFINITY; }
-  for (int i = r; i < g; i += RP) {
-    float v[4];
-    load4(key_row(i), c0, v);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) { mn[u] = fminf(mn[u], v[u]); mx[u] = fmaxf(mx[u], v[u]); }
-  }
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    red_mn[r * D + c0 + u] = mn[u];
-    red_mx[r * D + c0 + u] = mx[u];
-  }
+  load_tile(tile, pl.Kr, Kin, bh, in_stride, P0, split, g, D, geo.Rcap);
   __syncthreads();
-  if (r == 0) {
-    const size_t G = (size_t)(P0 / g);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      float a = red_mn[c0 + u], z = red_mx[c0 + u];
-      for (int k = 1; k < RP; ++k) {
-        a = fminf(a, red_mn[k * D + c0 + u]);
-        z = fmaxf(z, red_mx[k * D + c0 + u]);
-      }
-      a = __fadd_rn(a, 0.0f);  // a -0.0 minimum is stored as +0.0
-      const float scale = __fdiv_rn(__fsub_rn(z, a), (float)levels);
-      ch_mn[c0 + u] = a;
-      ch_scale[c0 + u] = scale;
-      const size_t idx = (bh * (geo.Tcap / g) + G) * D + c0 + u;
-      pl.Ks[idx] = __float2half_rn(scale);
-      pl.Kz[idx] = __float2half_rn(a);
+  {
+    float mn = INFINITY, mx = -INFINITY;
+    for (int i = 0; i < g; ++i) {
+      const float v = __half2float(tile[i * D + c]);
+      mn = fminf(mn, v);
+      mx = fmaxf(mx, v);
     }
-  }
-  __syncthreads();
-  for (int i = r; i < g; i += RP) {
-    float v[4];
-    load4(key_row(i), c0, v);
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      codes[i * D + c0 + u] =
-          (uint8_t)quant_code(v[u], ch_mn[c0 + u], ch_scale[c0 + u], levels);
+    mn = __fadd_rn(mn, 0.0f);  // a -0.0 minimum is stored as +0.0
+    const float scale = __fdiv_rn(__fsub_rn(mx, mn), (float)levels);
+    const float rcp = scale != 0.0f ? __frcp_rn(scale) : 0.0f;
+    const size_t idx = (bh * (geo.Tcap / g) + P0 / g) * D + c;
+    pl.Ks[idx] = __float2half_rn(scale);
+    pl.Kz[idx] = __float2half_rn(mn);
+    for (int i = 0; i < g; ++i)
+      codes[i * D + c] = (uint8_t)quant_code_fast(__half2float(tile[i * D + c]),
+                                                  mn, scale, rcp, levels);
   }
   __syncthreads();
   store_packed_tile<BITS>(codes, g, D, pl.Kc + (bh * geo.Tcap + P0) * geo.row);
   __syncthreads();
 
-  // ---- values: per token over groups of g channels (warp shuffles) ----
-  const int lanes_per_group = g / 4;     // consecutive, aligned in a warp
-  const int ngroups = D / g;
-  for (int i = r; i < g; i += RP) {
-    float v[4];
-    load4(val_row(i), c0, v);
-    float a = fminf(fminf(v[0], v[1]), fminf(v[2], v[3]));
-    float z = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
-    for (int off = 1; off < lanes_per_group; off <<= 1) {
-      a = fminf(a, __shfl_xor_sync(0xffffffffu, a, off));
-      z = fmaxf(z, __shfl_xor_sync(0xffffffffu, z, off));
-    }
-    a = __fadd_rn(a, 0.0f);  // a -0.0 minimum is stored as +0.0
-    const float scale = __fdiv_rn(__fsub_rn(z, a), (float)levels);
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      codes[i * D + c0 + u] = (uint8_t)quant_code(v[u], a, scale, levels);
-    if (cq % lanes_per_group == 0) {
-      const int j = c0 / g;
-      const size_t idx = (bh * geo.Tcap + P0 + i) * ngroups + j;
-      pl.Vs[idx] = __float2half_rn(scale);
-      pl.Vz[idx] = __float2half_rn(a);
+  // ---- values: per token over groups of g channels ----
+  load_tile(tile, pl.Vr, Vin, bh, in_stride, P0, split, g, D, geo.Rcap);
+  __syncthreads();
+  {
+    const int ngroups = D / g;
+    for (int t = c; t < g * ngroups; t += D) {
+      const int i = t / ngroups, j = t - i * ngroups;
+      const __half *row = tile + i * D + j * g;
+      float mn = INFINITY, mx = -INFINITY;
+      for (int k = 0; k < g; ++k) {
+        const float v = __half2float(row[k]);
+        mn = fminf(mn, v);
+        mx = fmaxf(mx, v);
+      }
+      mn = __fadd_rn(mn, 0.0f);  // a -0.0 minimum is stored as +0.0
+      const float scale = __fdiv_rn(__fsub_rn(mx, mn), (float)levels);
+      const float rcp = scale != 0.0f ? __frcp_rn(scale) : 0.0f;
+      for (int k = 0; k < g; ++k)
+        codes[i * D + j * g + k] =
+            (uint8_t)quant_code_fast(__half2float(row[k]), mn, scale, rcp, levels);
+      const size_t vidx = (bh * geo.Tcap + P0 + i) * ngroups + j;
+      pl.Vs[vidx] = __float2half_rn(scale);
+      pl.Vz[vidx] = __float2half_rn(mn);
     }
   }
   __syncthreads();
@@ -237,11 +233,27 @@ cudaError_t launch_flush(const Geometry &geo, const Planes &pl,
                          int total_groups, cudaStream_t st) {
   if (total_groups <= 0) return cudaSuccess;
   dim3 grid(total_groups, geo.H_kv);
+  const size_t smem = (size_t)geo.g * geo.D * (sizeof(__half) + 1);
+  void *fn = nullptr;
   switch (geo.bits) {
-    case 2: k_flush<2><<<grid, kThreads, 0, st>>>(geo, pl, Kin, Vin, in_stride, tab); break;
-    case 4: k_flush<4><<<grid, kThreads, 0, st>>>(geo, pl, Kin, Vin, in_stride, tab); break;
-    case 8: k_flush<8><<<grid, kThreads, 0, st>>>(geo, pl, Kin, Vin, in_stride, tab); break;
+    case 2: fn = (void *)k_flush<2>; break;
+    case 4: fn = (void *)k_flush<4>; break;
+    case 8: fn = (void *)k_flush<8>; break;
     default: return cudaErrorInvalidValue;
+  }
+  // the largest tile (g = 128, D = 256) needs the opt-in limit; set once
+  static bool opted[9] = {false};
+  if (!opted[geo.bits]) {
+    cudaError_t e = cudaFuncSetAttribute(
+        fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        128 * kMaxD * (int)(sizeof(__half) + 1));
+    if (e != cudaSuccess) return e;
+    opted[geo.bits] = true;
+  }
+  switch (geo.bits) {
+    case 2: k_flush<2><<<grid, geo.D, smem, st>>>(geo, pl, Kin, Vin, in_stride, tab); break;
+    case 4: k_flush<4><<<grid, geo.D, smem, st>>>(geo, pl, Kin, Vin, in_stride, tab); break;
+    case 8: k_flush<8><<<grid, geo.D, smem, st>>>(geo, pl, Kin, Vin, in_stride, tab); break;
   }
   count_launch();
   return cudaGetLastError();
