@@ -65,7 +65,7 @@ bool mma_plan(const Geometry &geo, int sm_count, MmaPlan *plan) {
 
 size_t mma_part_floats(const Geometry &geo, const MmaPlan &plan) {
   return ((size_t)plan.warps_max + (size_t)geo.B * geo.H_kv) * plan.GQp *
-         (geo.D + 2);
+         (geo.D == 64 ? mma::part_stride<64>() : mma::part_stride<128>());
 }
 
 cudaError_t launch_decode_mma(const Geometry &geo, const Planes &pl,

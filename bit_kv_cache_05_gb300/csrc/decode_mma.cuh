@@ -44,8 +44,17 @@ namespace vqk {
 namespace mma {
 
 constexpr int kC = 64;          // tokens per chunk (4 m16 tiles)
-constexpr int kNW = 4;          // warps per CTA
+#ifndef VQK_NW
+#define VQK_NW 4
+#endif
+#ifndef VQK_MINB
+#define VQK_MINB 3
+#endif
+constexpr int kNW = VQK_NW;     // warps per CTA
 constexpr int kMaxStages = 4;
+// a partial (o[D], m, l) per (warp segment, query head), padded to D + 4
+// floats so that the o rows stay 16-byte aligned
+template <int D> __host__ __device__ constexpr int part_stride() { return D + 4; }
 constexpr unsigned kFull = 0xffffffffu;
 
 // ---- PTX helpers -----------------------------------------------------------
@@ -103,6 +112,11 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src,
       : "memory");
 }
 
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0,
                                          uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -126,14 +140,27 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// The fp16 "hi" part (hl == 0) or the "lo" remainder (hl == 1) of x, as an
-// fp32 value to be rounded to fp16: hi keeps x's sign, exponent and top 10
-// mantissa bits (exact in fp16 while |x| is in fp16's normal range), lo =
-// x - hi is exact in fp32, so hi + fp16(lo) carries ~21 bits of x.
-__device__ __forceinline__ float hilo(float x, int hl) {
-  const float h = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
-  return hl ? x - h : h;
+// fp32 factors enter the MMAs as two fp16 operands in adjacent columns:
+// "hi" keeps x's sign, exponent and top 10 mantissa bits (exact in fp16
+// while |x| is in fp16's normal range), "lo" the exact fp32 remainder
+// x - hi, rounded to fp16, so hi + lo carries ~21 bits of x.  A lane builds
+// only its own column, with one and-xor and one fma per value:
+//   hv = (x & 0xFFFFE000) ^ flip,  y = x * d + hv
+// (hi lanes: flip = 0, d = 0 -> y = hi;  lo lanes: flip = sign bit, d = 1
+// -> y = x - hi, exact).
+struct HiLo {
+  uint32_t flip;
+  float d;
+};
+
+__device__ __forceinline__ float2 hilo2(float2 x, const HiLo &s) {
+  const float2 hv = make_float2(
+      __uint_as_float((__float_as_uint(x.x) & 0xFFFFE000u) ^ s.flip),
+      __uint_as_float((__float_as_uint(x.y) & 0xFFFFE000u) ^ s.flip));
+  return __ffma2_rn(x, make_float2(s.d, s.d), hv);
 }
+
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 
 // 2^e as a float, e in [-126, 127]
 __device__ __forceinline__ float exp2i(int e) {
@@ -308,13 +335,14 @@ struct Cfg {
   static constexpr uint32_t S_VZ = S_VS + kC * NJ * 2;
   static constexpr uint32_t S_BYTES = (S_VZ + kC * NJ * 2 + 127) / 128 * 128;
   // per-warp layout: [mbarriers][q' GQP x D f32, channel c scaled by the
-  // 2^-sexp of its score slot][q' GQP x D f32][residual o GQP x D f32]
-  // [residual m, l][stages]
+  // 2^-sexp of its score slot][q' GQP x D f32][stages].  The residual
+  // window's (o, m, l) lives in the stage slot of the residual chunk, which
+  // receives no copy.
   static constexpr uint32_t W_QF = 128;
   static constexpr uint32_t W_QN = W_QF + GQP * D * 4;
-  static constexpr uint32_t W_ORES = W_QN + GQP * D * 4;
-  static constexpr uint32_t W_MRES = W_ORES + GQP * D * 4;
-  static constexpr uint32_t W_STAGE0 = (W_MRES + 32 + 127) / 128 * 128;
+  static constexpr uint32_t W_STAGE0 = (W_QN + GQP * D * 4 + 127) / 128 * 128;
+  static constexpr uint32_t RES_BYTES = GQP * D * 4 + 32;
+  static_assert(RES_BYTES <= S_BYTES, "residual output must fit a stage");
   static __host__ __device__ constexpr uint32_t warp_bytes(int ST) {
     return W_STAGE0 + ST * S_BYTES;
   }
@@ -379,8 +407,10 @@ struct Cursor {
 // The fp16 residual window of one head on the CUDA cores, 32 tokens at a
 // time: each lane scores one token (its whole key row against every query
 // head), then the block's values are accumulated with lanes owning
-// channels.  Rows are loaded in unrolled batches, all in flight at once, so
-// the window costs a few memory round trips rather than one per token.
+// channels.  Rows are loaded in unrolled batches (a quarter of a key row per
+// lane, 8 value rows), all in flight at once, so the window costs a few
+// memory round trips rather than one per token; deeper batches raise the
+// register demand of the call and slow the grouped-query instantiations.
 // Writes the window's (o, m, l) per query head to ores / mres.  Kept out of
 // line: it runs once per head, and inlined it would raise the register
 // demand of the whole decode loop.
@@ -391,7 +421,7 @@ __device__ __noinline__ void residual_window(
     float *mres, int lane) {
   constexpr int CPL = D / 32;      // value channels per lane
   constexpr int KQ = D / 8;        // uint4 per key row
-  constexpr int KB = KQ < 4 ? KQ : 4;
+  constexpr int KB = KQ < 4 ? KQ : 4;   // key uint4 in flight per lane
   float m[GQP], l[GQP], o[GQP][CPL];
 #pragma unroll
   for (int hh = 0; hh < GQP; ++hh) {
@@ -491,7 +521,7 @@ __device__ __noinline__ void residual_window(
 }
 
 template <class C>
-__global__ void __launch_bounds__(kNW * 32, 3)
+__global__ void __launch_bounds__(kNW * 32, VQK_MINB)
 k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   using L = Layout<C::BITS>;
   constexpr int D = C::D, KS = C::KS, NJ = C::NJ, GQP = C::GQP, WG = C::WG;
@@ -512,8 +542,6 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   uint64_t *bars = reinterpret_cast<uint64_t *>(ws);
   float *qb = reinterpret_cast<float *>(ws + C::W_QF);      // [GQP][D], slot-scaled
   float *qn = reinterpret_cast<float *>(ws + C::W_QN);      // [GQP][D]
-  float *ores = reinterpret_cast<float *>(ws + C::W_ORES);  // [GQP][D]
-  float *mres = reinterpret_cast<float *>(ws + C::W_MRES);  // m[4], l[4]
   unsigned char *stage0 = ws + C::W_STAGE0;
 
   if (lane == 0) {
@@ -523,6 +551,9 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   __syncwarp();
 
   // ---- producer: lane 0 issues the bulk copies of the chunk at `cu` -----
+  // The key scale/zero rows are copied only where a score window starts or
+  // the warp's range starts: every other chunk reuses the operand built
+  // from an earlier stage.
   auto issue = [&](const Cursor &cu, int s, int c) {
     if (c == args.fail_chunk) return;   // testing: a copy that never comes
     const int Tq = tab.Tq[cu.b];
@@ -532,22 +563,38 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     unsigned char *st = stage0 + s * C::S_BYTES;
     const size_t hd = (size_t)cu.b * geo.H_kv + cu.h;
     const uint32_t b_codes = nvalid * ROW;
+    const uint32_t b_vs = nvalid * NJ * 2;
+    const bool with_ks = (t0 % C::WT) == 0 || c == lo_c;
     const int kg0 = ((t0 / G) / C::KG) * C::KG;
     const int ngv = Tq / G - kg0;
-    const int ng = ngv < C::KG ? ngv : C::KG;
-    const uint32_t b_ks = ng * D * 2;
-    const uint32_t b_vs = nvalid * NJ * 2;
+    const uint32_t b_ks = with_ks ? (ngv < C::KG ? ngv : C::KG) * D * 2 : 0u;
     mbar_expect_tx(&bars[s], 2 * (b_codes + b_ks + b_vs));
-    bulk_g2s(st + C::S_KC, pl.Kc + (hd * geo.Tcap + t0) * ROW, b_codes, &bars[s]);
-    bulk_g2s(st + C::S_VC, pl.Vc + (hd * geo.Tcap + t0) * ROW, b_codes, &bars[s]);
-    const size_t kidx = (hd * (geo.Tcap / G) + kg0) * D;
-    bulk_g2s(st + C::S_KS, pl.Ks + kidx, b_ks, &bars[s]);
-    bulk_g2s(st + C::S_KZ, pl.Kz + kidx, b_ks, &bars[s]);
-    const size_t vidx = (hd * geo.Tcap + t0) * NJ;
-    bulk_g2s(st + C::S_VS, pl.Vs + vidx, b_vs, &bars[s]);
-    bulk_g2s(st + C::S_VZ, pl.Vz + vidx, b_vs, &bars[s]);
+    const size_t row0 = hd * geo.Tcap + t0;
+    bulk_g2s(st + C::S_KC, pl.Kc + row0 * ROW, b_codes, &bars[s]);
+    bulk_g2s(st + C::S_VC, pl.Vc + row0 * ROW, b_codes, &bars[s]);
+    if (with_ks) {
+      const size_t kidx = (hd * (geo.Tcap / G) + kg0) * D;
+      bulk_g2s(st + C::S_KS, pl.Ks + kidx, b_ks, &bars[s]);
+      bulk_g2s(st + C::S_KZ, pl.Kz + kidx, b_ks, &bars[s]);
+    }
+    bulk_g2s(st + C::S_VS, pl.Vs + row0 * NJ, b_vs, &bars[s]);
+    bulk_g2s(st + C::S_VZ, pl.Vz + row0 * NJ, b_vs, &bars[s]);
   };
   auto is_quant = [&](const Cursor &cu) { return cu.k < tab.nq[cu.b]; };
+  // a head's last chunk is its residual window (when it has one); the
+  // chunks between the quantized ones and it are empty: they only weight
+  // the residual window's cost in the equal split of the chunk space
+  auto is_res = [&](const Cursor &cu) {
+    return cu.k == tab.nc[cu.b] - 1 && tab.nres[cu.b] > 0;
+  };
+  // lane 0, when the producer cursor reaches a residual chunk: pull the
+  // head's residual ring into L2, ST chunks before the window is read
+  auto prefetch_res = [&](const Cursor &cu) {
+    const size_t hd = (size_t)cu.b * geo.H_kv + cu.h;
+    const uint32_t bytes = geo.Rcap * D * 2;
+    prefetch_l2(pl.Kr + hd * geo.Rcap * D, bytes);
+    prefetch_l2(pl.Vr + hd * geo.Rcap * D, bytes);
+  };
 
   Cursor pc;  // producer cursor: the next chunk to issue
   pc.init(lo_c, geo, tab);
@@ -557,6 +604,8 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     if (is_quant(pc)) {
       if (lane == 0) issue(pc, i, lo_c + i);
       pending |= 1u << i;
+    } else if (lane == 0 && is_res(pc)) {
+      prefetch_res(pc);
     }
     pc.next(geo, tab);
   }
@@ -567,6 +616,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   const uint32_t v_sel = L::vsel(gid);
   const float rs0 = exp2i(24 - L::vpos0(gid)), rs1 = exp2i(24 - L::vpos1(gid));
   const int hl = gid & 1;               // B operand column: hi (0) or lo (1)
+  const HiLo hls{hl ? 0x80000000u : 0u, hl ? 1.f : 0.f};
   const int pair_b = gid >> 1;          // B operand column pair
   const int h_b = pair_b % GQP;         // query head of the B column pair
   const int h_s = tig % GQP;            // this lane's query head (C layout)
@@ -577,10 +627,12 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   float Z[NJ];
   float m_run = -INFINITY, l_run = 0.f;
   uint32_t Bs[KS][2];
+  float qmax_b = 0.f;    // max |q'| (slot-scaled) of query head h_b
   float beta_t = 0.f;    // zero-point term of pair tig, current window
   float unscale_t = 1.f; // 2^(24 - k) of pair tig, current window
   int cur_w = -1;
   bool has_res = false;
+  const float *res_o = nullptr;   // residual window (o, m, l), when has_res
 
   auto reset_state = [&]() {
 #pragma unroll
@@ -596,16 +648,32 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   };
 
   // q' of the head's GQP query heads: qn in channel order, qb with channel
-  // c scaled by 2^-sexp of its score slot
+  // c scaled by 2^-sexp of its score slot; qmax_b = max |qb| of head h_b
   auto load_q = [&](int b, int h) {
-    for (int i = lane; i < GQP * D; i += 32) {
-      const int hh = i / D, c = i - hh * D;
+    float mq[GQP];
+#pragma unroll
+    for (int hh = 0; hh < GQP; ++hh) mq[hh] = 0.f;
+#pragma unroll
+    for (int j = 0; j < GQP * D / 32; ++j) {
+      const int i = lane + 32 * j;
+      constexpr int PER = D / 32;
+      const int hh = j / PER, c = i - hh * D;
       float v = 0.f;
       if (hh < GQ)
         v = __half2float(args.q[((size_t)b * geo.H_q + h * GQ + hh) * D + c]) *
             args.scale_log2;
+      const float vb = v * exp2i(-L::oexp(c & 3));
       qn[i] = v;
-      qb[i] = v * exp2i(-L::oexp(c & 3));
+      qb[i] = vb;
+      mq[hh] = fmaxf(mq[hh], fabsf(vb));
+    }
+#pragma unroll
+    for (int hh = 0; hh < GQP; ++hh) {
+      float m = mq[hh];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+        m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+      if (hh == h_b) qmax_b = m;
     }
     __syncwarp();
   };
@@ -613,53 +681,70 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   // B operand of the score MMA for the window starting at key group gw0 (the
   // stage's key scale/zero region starts at group kg0), and, for this lane's
   // column pair, the zero-point term beta and the factor that undoes the
-  // operand scaling.  Each column pair is scaled by a power of two 2^k that
-  // puts its largest |a| in [2^13, 2^14): no fp16 overflow, and the lo parts
-  // stay in fp16's normal range.
+  // operand scaling.  Each column pair is scaled by the power of two 2^k
+  // that puts the bound max|q'| * max s of its products in [2^13, 2^14):
+  // no fp16 overflow, and the lo parts of the large products stay in fp16's
+  // normal range.
   auto build_score_b = [&](const __half *Ks, const __half *Kz, int gw0, int kg0) {
     const int gr = gw0 + pair_b / GQP - kg0;   // group row in the region
     const float *qbh = qb + h_b * D + 4 * tig;
-    const float *qnh = qn + h_b * D + 4 * tig;
     const __half *ksr = Ks + gr * D + 4 * tig;
-    const __half *kzr = Kz + gr * D + 4 * tig;
-    float av[KS][4];
-    float zpart = 0.f, amax = 0.f;
+    uint2 sraw[KS];
+    __half2 smx = __float2half2_rn(0.f);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      sraw[ks] = *reinterpret_cast<const uint2 *>(ksr + 16 * ks);
+      smx = __hmax2(smx, __hmax2(*reinterpret_cast<const __half2 *>(&sraw[ks].x),
+                                 *reinterpret_cast<const __half2 *>(&sraw[ks].y)));
+    }
+    float smax = fmaxf(__low2float(smx), __high2float(smx));
+    smax = fmaxf(smax, __shfl_xor_sync(kFull, smax, 1));
+    smax = fmaxf(smax, __shfl_xor_sync(kFull, smax, 2));
+    int k = 13 - (((__float_as_int(qmax_b * smax) >> 23) & 0xff) - 127);
+    k = k < -60 ? -60 : (k > 60 ? 60 : k);
+    const float2 sc = f2(exp2i(k), exp2i(k));
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       const float4 qs = *reinterpret_cast<const float4 *>(qbh + 16 * ks);
+      const float2 s01 = __half22float2(*reinterpret_cast<const __half2 *>(&sraw[ks].x));
+      const float2 s23 = __half22float2(*reinterpret_cast<const __half2 *>(&sraw[ks].y));
+      // channel order 4tig + 0..3
+      const float2 a01 = hilo2(__fmul2_rn(__fmul2_rn(f2(qs.x, qs.y), sc), s01), hls);
+      const float2 a23 = hilo2(__fmul2_rn(__fmul2_rn(f2(qs.z, qs.w), sc), s23), hls);
+      const float a[4] = {a01.x, a01.y, a23.x, a23.y};
+      // slot order: slot e holds channel 4tig + off(e)
+      Bs[ks][0] = pack_half2(a[L::off(0)], a[L::off(1)]);
+      Bs[ks][1] = pack_half2(a[L::off(2)], a[L::off(3)]);
+    }
+    // zero-point term: the hi and lo lanes of a pair take half the K-steps
+    const float *qnh = qn + h_b * D + 4 * tig;
+    const __half *kzr = Kz + gr * D + 4 * tig;
+    float2 zacc = f2(0.f, 0.f);
+#pragma unroll
+    for (int kk = 0; kk < KS / 2; ++kk) {
+      const int ks = hl * (KS / 2) + kk;
       const float4 qz = *reinterpret_cast<const float4 *>(qnh + 16 * ks);
-      float kf[4], zf[4];
-      load_halves<4>(ksr + 16 * ks, kf);
-      load_halves<4>(kzr + 16 * ks, zf);
-      const float a[4] = {qs.x * kf[0], qs.y * kf[1], qs.z * kf[2], qs.w * kf[3]};
-      zpart = fmaf(qz.x, zf[0], fmaf(qz.y, zf[1], fmaf(qz.z, zf[2], fmaf(qz.w, zf[3], zpart))));
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        av[ks][e] = a[L::off(e)];
-        amax = fmaxf(amax, fabsf(av[ks][e]));
-      }
+      const uint2 zr = *reinterpret_cast<const uint2 *>(kzr + 16 * ks);
+      zacc = __ffma2_rn(f2(qz.x, qz.y),
+                        __half22float2(*reinterpret_cast<const __half2 *>(&zr.x)), zacc);
+      zacc = __ffma2_rn(f2(qz.z, qz.w),
+                        __half22float2(*reinterpret_cast<const __half2 *>(&zr.y)), zacc);
     }
-    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
-    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
-    int k = 13 - (((__float_as_int(amax) >> 23) & 0xff) - 127);
-    k = k < -60 ? -60 : (k > 60 ? 60 : k);
-    const float sc = exp2i(k);
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      Bs[ks][0] = pack_half2(hilo(av[ks][0] * sc, hl), hilo(av[ks][1] * sc, hl));
-      Bs[ks][1] = pack_half2(hilo(av[ks][2] * sc, hl), hilo(av[ks][3] * sc, hl));
-    }
+    float zpart = zacc.x + zacc.y;
     zpart += __shfl_xor_sync(kFull, zpart, 1);
     zpart += __shfl_xor_sync(kFull, zpart, 2);
+    zpart += __shfl_xor_sync(kFull, zpart, 4);   // hi + lo lanes of the pair
     // lane (gid, tig) needs the values of pair tig, held by lanes gid = 2*tig
     beta_t = __shfl_sync(kFull, zpart, 8 * tig);
     unscale_t = exp2i(24 - __shfl_sync(kFull, k, 8 * tig));
   };
 
-  auto residual = [&](int b, int hd) {
+  auto residual = [&](int b, int hd, int s) {
+    float *ores = reinterpret_cast<float *>(stage0 + s * C::S_BYTES);
     residual_window<D, GQP>(pl.Kr, pl.Vr, (size_t)hd * geo.Rcap, tab.Tq[b],
-                            tab.nres[b], geo.Rcap, GQ, qn, ores, mres, lane);
+                            tab.nres[b], geo.Rcap, GQ, qn, ores, ores + GQP * D,
+                            lane);
+    res_o = ores;
     has_res = tab.nres[b] > 0;
   };
 
@@ -673,7 +758,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     const int w1 = (int)((ce * W - 1) / N);
     for (int hh = 0; hh < GQ; ++hh) {
       auto entry = [&](int w) {
-        return args.part + ((size_t)(w + hd) * GQP + hh) * (D + 2);
+        return args.part + ((size_t)(w + hd) * GQP + hh) * part_stride<D>();
       };
       float M = -INFINITY;
       for (int w = w0 + lane; w <= w1; w += 32) M = fmaxf(M, __ldcg(entry(w) + D));
@@ -684,14 +769,41 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
       for (int w = w0 + lane; w <= w1; w += 32)
         Ls += exp2_neg(__ldcg(entry(w) + D) - M) * __ldcg(entry(w) + D + 1);
       Ls = warp_sum(Ls);
+      // partial weights 2^(m_w - M), lane j holding those of partials
+      // w0 + j, w0 + j + 32, ...; the o rows are read kMB at a time, all in
+      // flight together
+      constexpr int kMB = 8;
       float acc[CPL];
 #pragma unroll
       for (int u = 0; u < CPL; ++u) acc[u] = 0.f;
-      for (int w = w0; w <= w1; ++w) {
-        const float *e = entry(w);
-        const float f = exp2_neg(__ldcg(e + D) - M);
+      for (int wb = w0; wb <= w1; wb += 32) {
+        const int wl = wb + lane;
+        const float fl = wl <= w1 ? exp2_neg(__ldcg(entry(wl) + D) - M) : 0.f;
+        const int nbw = w1 - wb + 1 < 32 ? w1 - wb + 1 : 32;
+        for (int j0 = 0; j0 < nbw; j0 += kMB) {
+          float v[kMB][CPL];
 #pragma unroll
-        for (int u = 0; u < CPL; ++u) acc[u] = fmaf(f, __ldcg(e + lane * CPL + u), acc[u]);
+          for (int j = 0; j < kMB; ++j) {
+            const int w = wb + (j0 + j < nbw ? j0 + j : 0);
+            const float *e = entry(w) + lane * CPL;
+            if constexpr (CPL == 4) {
+              const float4 x = __ldcg(reinterpret_cast<const float4 *>(e));
+              v[j][0] = x.x; v[j][1] = x.y; v[j][2] = x.z; v[j][3] = x.w;
+            } else {
+              const float2 x = __ldcg(reinterpret_cast<const float2 *>(e));
+              v[j][0] = x.x; v[j][1] = x.y;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < kMB; ++j) {
+            // lanes past the batch's end weigh 0 (fl = 0 there)
+            const float f = __shfl_sync(kFull, fl, (j0 + j) & 31);
+            if (j0 + j < nbw) {
+#pragma unroll
+              for (int u = 0; u < CPL; ++u) acc[u] = fmaf(f, v[j][u], acc[u]);
+            }
+          }
+        }
       }
       const float inv = 1.0f / Ls;
       float *out = args.out + ((size_t)b * geo.H_q + h * GQ + hh) * D + lane * CPL;
@@ -709,6 +821,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     for (int j = 0; j < NJ; ++j) Zt[j] = head_reduce<GQP>(Z[j], AddOp());
     float mf = m_run, aq = 1.f, ar = 0.f;
     if (has_res) {
+      const float *mres = res_o + GQP * D;
       const float mr = mres[h_s], lr = mres[4 + h_s];
       mf = fmaxf(m_run, mr);
       aq = m_run == -INFINITY ? 0.f : exp2_neg(m_run - mf);
@@ -716,7 +829,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
       Lsum = Lsum * aq + lr * ar;
     }
     if (h_s < GQ) {
-      float *dst = args.part + ((size_t)(wg + hd) * GQP + h_s) * (D + 2);
+      float *dst = args.part + ((size_t)(wg + hd) * GQP + h_s) * part_stride<D>();
 #pragma unroll
       for (int mv = 0; mv < KS; ++mv) {
         const int j = (16 * mv) / G;
@@ -726,8 +839,8 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
         float o0 = ((O[mv][0] + O[mv][1]) * rs0 + Zt[j]) * aq;
         float o1 = ((O[mv][2] + O[mv][3]) * rs1 + Zt[j]) * aq;
         if (has_res) {
-          o0 += ores[h_s * D + c0] * ar;
-          o1 += ores[h_s * D + c0 + 1] * ar;
+          o0 += res_o[h_s * D + c0] * ar;
+          o1 += res_o[h_s * D + c0 + 1] * ar;
         }
         __stcg(reinterpret_cast<float2 *>(dst + c0), make_float2(o0, o1));
       }
@@ -754,6 +867,183 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     __syncwarp();
   };
 
+  // ---- one staged chunk: scores, softmax update, values.  FULL: all four
+  // m16 tiles hold tokens (every chunk but a head's last quantized one). ----
+  auto chunk = [&](auto full_tag, const unsigned char *st, int t0, int nmt) {
+    constexpr bool FULL = decltype(full_tag)::value;
+    const uint4 *kc = reinterpret_cast<const uint4 *>(st + C::S_KC);
+    const uint4 *vc = reinterpret_cast<const uint4 *>(st + C::S_VC);
+    const __half *Ks = reinterpret_cast<const __half *>(st + C::S_KS);
+    const __half *Kz = reinterpret_cast<const __half *>(st + C::S_KZ);
+    const __half *Vs = reinterpret_cast<const __half *>(st + C::S_VS);
+    const __half *Vz = reinterpret_cast<const __half *>(st + C::S_VZ);
+    const int G0 = t0 / G;                        // first key group
+    const int kg0 = (G0 / C::KG) * C::KG;
+
+    // ---- scores, window by window; the tiles of a window interleave ----
+    float sv[4][2];
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) sv[mt][0] = sv[mt][1] = -INFINITY;
+#pragma unroll
+    for (int win = 0; win < C::NWIN; ++win) {
+      constexpr int MPW = C::MPW;
+      const int mt0 = win * MPW;
+      if (FULL || mt0 < nmt) {
+        const int gw0 = ((G0 + (16 * mt0) / G) / WG) * WG;
+        if (gw0 != cur_w) {
+          build_score_b(Ks, Kz, gw0, kg0);
+          cur_w = gw0;
+        }
+        float acc[MPW][4];
+#pragma unroll
+        for (int m = 0; m < MPW; ++m)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) acc[m][r] = 0.f;
+#pragma unroll
+        for (int q = 0; q < KS / L::WPQ; ++q) {
+          uint4 r0[MPW], r1[MPW];
+#pragma unroll
+          for (int m = 0; m < MPW; ++m) {
+            const uint4 *row = kc + (16 * (mt0 + m) + gid) * ROWQ;
+            r0[m] = row[q];
+            r1[m] = row[8 * ROWQ + q];
+          }
+#pragma unroll
+          for (int kq = 0; kq < L::WPQ; ++kq) {
+            const int ks = q * L::WPQ + kq;
+#pragma unroll
+            for (int m = 0; m < MPW; ++m) {
+              if (FULL || mt0 + m < nmt) {
+                uint32_t a0, a1, a2, a3;
+                L::score_a(r0[m], ks, s_sel, a0, a2);
+                L::score_a(r1[m], ks, s_sel, a1, a3);
+                mma16816(acc[m], a0, a1, a2, a3, Bs[ks][0], Bs[ks][1]);
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < MPW; ++m) {
+          const int mt = mt0 + m;
+          if ((FULL || mt < nmt) && ((G0 + (16 * mt) / G) % WG) == gw_s) {
+            sv[mt][0] = fmaf(acc[m][0] + acc[m][1], unscale_t, beta_t);
+            sv[mt][1] = fmaf(acc[m][2] + acc[m][3], unscale_t, beta_t);
+          }
+        }
+      }
+    }
+
+    // ---- online softmax update for this lane's head.  The head maximum
+    // is reduced only when some lane holds a score above the running
+    // maximum (rare once a few chunks are in); otherwise m and the
+    // accumulators stay as they are. ----
+    float lmax = -INFINITY;
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) lmax = fmaxf(lmax, fmaxf(sv[mt][0], sv[mt][1]));
+    float alpha = 1.f;
+    if (__any_sync(kFull, lmax > m_run)) {
+      const float m_new = fmaxf(m_run, head_reduce<GQP>(lmax, MaxOp()));
+      alpha = m_run == -INFINITY ? 0.f : exp2_neg(m_run - m_new);
+      m_run = m_new;
+      const float2 a2 = f2(alpha, alpha);
+#pragma unroll
+      for (int mv = 0; mv < KS; ++mv) {
+        const float2 o01 = __fmul2_rn(f2(O[mv][0], O[mv][1]), a2);
+        const float2 o23 = __fmul2_rn(f2(O[mv][2], O[mv][3]), a2);
+        O[mv][0] = o01.x; O[mv][1] = o01.y; O[mv][2] = o23.x; O[mv][3] = o23.y;
+      }
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) Z[j] *= alpha;
+    }
+    float p[4][2];
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) p[mt][r] = exp2_neg(sv[mt][r] - m_run);   // -inf -> 0
+    const float psum = ((p[0][0] + p[0][1]) + (p[1][0] + p[1][1])) +
+                       ((p[2][0] + p[2][1]) + (p[3][0] + p[3][1]));
+    l_run = fmaf(l_run, alpha, psum);
+
+    // ---- values: K-step kt = tokens 16kt ... 16kt+15 of the chunk.  K
+    // slots (2tig, 2tig+1, 2tig+8, 2tig+9) <-> tokens (tig, tig+4, tig+8,
+    // tig+12): the four rows a lane group reads hit distinct banks. ----
+#pragma unroll
+    for (int kt = 0; kt < 4; ++kt) {
+      if (FULL || kt < nmt) {
+        // zero-point term in the score layout (tokens gid, gid+8)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          float vz[NJ];
+          load_halves<NJ>(Vz + (16 * kt + gid + 8 * r) * NJ, vz);
+          if constexpr (NJ == 1) {
+            Z[0] = fmaf(p[kt][r], vz[0], Z[0]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < NJ; j += 2) {
+              const float2 z = __ffma2_rn(f2(p[kt][r], p[kt][r]), f2(vz[j], vz[j + 1]),
+                                          f2(Z[j], Z[j + 1]));
+              Z[j] = z.x; Z[j + 1] = z.y;
+            }
+          }
+        }
+        // p of head h_b for tokens tig, tig+4, tig+8, tig+12
+        const int src = ((G0 + (16 * kt) / G) % WG) * GQP + h_b;
+        const float p0 = __shfl_sync(kFull, p[kt][0], 4 * tig + src);
+        const float p1 = __shfl_sync(kFull, p[kt][0], 4 * tig + 16 + src);
+        const float p2 = __shfl_sync(kFull, p[kt][1], 4 * tig + src);
+        const float p3 = __shfl_sync(kFull, p[kt][1], 4 * tig + 16 + src);
+        const int ta = 16 * kt + tig;
+        // s_V of the four tokens: whole rows when every block needs a
+        // different group, single values otherwise
+        float vs[4][C::NVB];
+        if constexpr (C::NVB == NJ && NJ >= 2) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            float row[NJ];
+            load_halves<NJ>(Vs + (ta + 4 * u) * NJ, row);
+#pragma unroll
+            for (int vb = 0; vb < C::NVB; ++vb) vs[u][vb] = row[(4 * vb + pair_b) / GQP];
+          }
+        } else {
+#pragma unroll
+          for (int vb = 0; vb < C::NVB; ++vb) {
+            const int jb = (4 * vb + pair_b) / GQP;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              vs[u][vb] = jb < NJ ? __half2float(Vs[(ta + 4 * u) * NJ + jb]) : 0.f;
+          }
+        }
+        uint32_t bv[C::NVB][2];
+#pragma unroll
+        for (int vb = 0; vb < C::NVB; ++vb) {
+          const float2 w01 = hilo2(__fmul2_rn(f2(p0, p1), f2(vs[0][vb], vs[1][vb])), hls);
+          const float2 w23 = hilo2(__fmul2_rn(f2(p2, p3), f2(vs[2][vb], vs[3][vb])), hls);
+          bv[vb][0] = pack_half2(w01.x, w01.y);
+          bv[vb][1] = pack_half2(w23.x, w23.y);
+        }
+        // m16 channel tiles, VTPQ per uint4 of the token rows
+#pragma unroll
+        for (int q = 0; q < KS / L::VTPQ; ++q) {
+          const uint4 xa = vc[ta * ROWQ + q];
+          const uint4 xb = vc[(ta + 4) * ROWQ + q];
+          const uint4 xc = vc[(ta + 8) * ROWQ + q];
+          const uint4 xd = vc[(ta + 12) * ROWQ + q];
+#pragma unroll
+          for (int u = 0; u < L::VTPQ; ++u) {
+            const int mv = q * L::VTPQ + u;
+            const int vb = (((16 * mv) / G) * GQP) >> 2;
+            uint32_t a0, a1, a2, a3;
+            L::value_a(__byte_perm(L::vword(xa, u, gid), L::vword(xb, u, gid), v_sel),
+                       gid, a0, a1);
+            L::value_a(__byte_perm(L::vword(xc, u, gid), L::vword(xd, u, gid), v_sel),
+                       gid, a2, a3);
+            mma16816(O[mv], a0, a1, a2, a3, bv[vb][0], bv[vb][1]);
+          }
+        }
+      }
+    }
+  };
+
   // ---- main loop over my chunks ---------------------------------------------
   Cursor cu;
   cu.init(lo_c, geo, tab);
@@ -766,173 +1056,20 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
       load_q(cu.b, cu.h);
       cur_hd = hd;
     }
-    if (!is_quant(cu)) {
-      residual(cu.b, hd);
-    } else {
+    if (is_res(cu)) {
+      residual(cu.b, hd, s);
+    } else if (is_quant(cu)) {
       const bool ok = __all_sync(kFull, mbar_wait(&bars[s], (phase >> s) & 1u));
       if (!ok) { failed = true; break; }
       phase ^= 1u << s;
       pending &= ~(1u << s);
       const unsigned char *st = stage0 + s * C::S_BYTES;
-      const uint4 *kc = reinterpret_cast<const uint4 *>(st + C::S_KC);
-      const uint4 *vc = reinterpret_cast<const uint4 *>(st + C::S_VC);
-      const __half *Ks = reinterpret_cast<const __half *>(st + C::S_KS);
-      const __half *Kz = reinterpret_cast<const __half *>(st + C::S_KZ);
-      const __half *Vs = reinterpret_cast<const __half *>(st + C::S_VS);
-      const __half *Vz = reinterpret_cast<const __half *>(st + C::S_VZ);
       const int t0 = cu.k * kC;
       const int rem = tab.Tq[cu.b] - t0;
-      const int nmt = (rem < kC ? rem : kC) >> 4;   // valid m16 tiles
-      const int G0 = t0 / G;                        // first key group
-      const int kg0 = (G0 / C::KG) * C::KG;
-
-      // ---- scores, window by window; the tiles of a window interleave ----
-      float sv[4][2];
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt) sv[mt][0] = sv[mt][1] = -INFINITY;
-#pragma unroll
-      for (int win = 0; win < C::NWIN; ++win) {
-        constexpr int MPW = C::MPW;
-        const int mt0 = win * MPW;
-        if (mt0 < nmt) {
-          const int gw0 = ((G0 + (16 * mt0) / G) / WG) * WG;
-          if (gw0 != cur_w) {
-            build_score_b(Ks, Kz, gw0, kg0);
-            cur_w = gw0;
-          }
-          float acc[MPW][4];
-#pragma unroll
-          for (int m = 0; m < MPW; ++m)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) acc[m][r] = 0.f;
-#pragma unroll
-          for (int q = 0; q < KS / L::WPQ; ++q) {
-            uint4 r0[MPW], r1[MPW];
-#pragma unroll
-            for (int m = 0; m < MPW; ++m) {
-              const uint4 *row = kc + (16 * (mt0 + m) + gid) * ROWQ;
-              r0[m] = row[q];
-              r1[m] = row[8 * ROWQ + q];
-            }
-#pragma unroll
-            for (int kq = 0; kq < L::WPQ; ++kq) {
-              const int ks = q * L::WPQ + kq;
-#pragma unroll
-              for (int m = 0; m < MPW; ++m) {
-                if (mt0 + m < nmt) {
-                  uint32_t a0, a1, a2, a3;
-                  L::score_a(r0[m], ks, s_sel, a0, a2);
-                  L::score_a(r1[m], ks, s_sel, a1, a3);
-                  mma16816(acc[m], a0, a1, a2, a3, Bs[ks][0], Bs[ks][1]);
-                }
-              }
-            }
-          }
-#pragma unroll
-          for (int m = 0; m < MPW; ++m) {
-            const int mt = mt0 + m;
-            if (mt < nmt && ((G0 + (16 * mt) / G) % WG) == gw_s) {
-              sv[mt][0] = fmaf(acc[m][0] + acc[m][1], unscale_t, beta_t);
-              sv[mt][1] = fmaf(acc[m][2] + acc[m][3], unscale_t, beta_t);
-            }
-          }
-        }
-      }
-
-      // ---- online softmax update for this lane's head ----
-      float mx = -INFINITY;
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt) mx = fmaxf(mx, fmaxf(sv[mt][0], sv[mt][1]));
-      mx = head_reduce<GQP>(mx, MaxOp());
-      const float m_new = fmaxf(m_run, mx);
-      const float alpha = m_run == -INFINITY ? 0.f : exp2_neg(m_run - m_new);
-      float p[4][2];
-      float psum = 0.f;
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          p[mt][r] = exp2_neg(sv[mt][r] - m_new);   // -inf -> 0
-          psum += p[mt][r];
-        }
-      l_run = l_run * alpha + psum;
-      m_run = m_new;
-      if (__any_sync(kFull, alpha != 1.f)) {   // some lane's max moved
-#pragma unroll
-        for (int mv = 0; mv < KS; ++mv)
-#pragma unroll
-          for (int r = 0; r < 4; ++r) O[mv][r] *= alpha;
-#pragma unroll
-        for (int j = 0; j < NJ; ++j) Z[j] *= alpha;
-      }
-
-      // ---- values: K-step kt = tokens 16kt ... 16kt+15 of the chunk.  K
-      // slots (2tig, 2tig+1, 2tig+8, 2tig+9) <-> tokens (tig, tig+4, tig+8,
-      // tig+12): the four rows a lane group reads hit distinct banks. ----
-#pragma unroll
-      for (int kt = 0; kt < 4; ++kt) {
-        if (kt < nmt) {
-          // zero-point term in the score layout (tokens gid, gid+8)
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            float vz[NJ];
-            load_halves<NJ>(Vz + (16 * kt + gid + 8 * r) * NJ, vz);
-#pragma unroll
-            for (int j = 0; j < NJ; ++j) Z[j] = fmaf(p[kt][r], vz[j], Z[j]);
-          }
-          // p of head h_b for tokens tig, tig+4, tig+8, tig+12
-          const int src = ((G0 + (16 * kt) / G) % WG) * GQP + h_b;
-          const float p0 = __shfl_sync(kFull, p[kt][0], 4 * tig + src);
-          const float p1 = __shfl_sync(kFull, p[kt][0], 4 * tig + 16 + src);
-          const float p2 = __shfl_sync(kFull, p[kt][1], 4 * tig + src);
-          const float p3 = __shfl_sync(kFull, p[kt][1], 4 * tig + 16 + src);
-          const int ta = 16 * kt + tig;
-          // s_V of the four tokens: whole rows when every block needs a
-          // different group, single values otherwise
-          float vs[4][C::NVB];
-          if constexpr (C::NVB == NJ && NJ >= 2) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              float row[NJ];
-              load_halves<NJ>(Vs + (ta + 4 * u) * NJ, row);
-#pragma unroll
-              for (int vb = 0; vb < C::NVB; ++vb) vs[u][vb] = row[(4 * vb + pair_b) / GQP];
-            }
-          } else {
-#pragma unroll
-            for (int vb = 0; vb < C::NVB; ++vb) {
-              const int jb = (4 * vb + pair_b) / GQP;
-#pragma unroll
-              for (int u = 0; u < 4; ++u)
-                vs[u][vb] = jb < NJ ? __half2float(Vs[(ta + 4 * u) * NJ + jb]) : 0.f;
-            }
-          }
-          uint32_t bv[C::NVB][2];
-#pragma unroll
-          for (int vb = 0; vb < C::NVB; ++vb) {
-            bv[vb][0] = pack_half2(hilo(p0 * vs[0][vb], hl), hilo(p1 * vs[1][vb], hl));
-            bv[vb][1] = pack_half2(hilo(p2 * vs[2][vb], hl), hilo(p3 * vs[3][vb], hl));
-          }
-          // m16 channel tiles, VTPQ per uint4 of the token rows
-#pragma unroll
-          for (int q = 0; q < KS / L::VTPQ; ++q) {
-            const uint4 xa = vc[ta * ROWQ + q];
-            const uint4 xb = vc[(ta + 4) * ROWQ + q];
-            const uint4 xc = vc[(ta + 8) * ROWQ + q];
-            const uint4 xd = vc[(ta + 12) * ROWQ + q];
-#pragma unroll
-            for (int u = 0; u < L::VTPQ; ++u) {
-              const int mv = q * L::VTPQ + u;
-              const int vb = (((16 * mv) / G) * GQP) >> 2;
-              uint32_t a0, a1, a2, a3;
-              L::value_a(__byte_perm(L::vword(xa, u, gid), L::vword(xb, u, gid), v_sel),
-                         gid, a0, a1);
-              L::value_a(__byte_perm(L::vword(xc, u, gid), L::vword(xd, u, gid), v_sel),
-                         gid, a2, a3);
-              mma16816(O[mv], a0, a1, a2, a3, bv[vb][0], bv[vb][1]);
-            }
-          }
-        }
+      if (rem >= kC) {
+        chunk(std::true_type{}, st, t0, 4);
+      } else {
+        chunk(std::false_type{}, st, t0, rem >> 4);
       }
     }
     const bool head_ends = cu.k == tab.nc[cu.b] - 1 || i == n_mine - 1;
@@ -945,6 +1082,8 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
           issue(pc, s, lo_c + i + ST);
         }
         pending |= 1u << s;
+      } else if (lane == 0 && is_res(pc)) {
+        prefetch_res(pc);
       }
       pc.next(geo, tab);
     }

@@ -93,7 +93,9 @@ cudaError_t launch_decode(const Geometry &geo, const Planes &pl,
 
 // Flattened chunk space: sequence b owns chunks [bprefix[b], bprefix[b+1]),
 // H_kv heads of nc[b] chunks each: nq[b] quantized 64-token chunks and, when
-// nres[b] > 0, one residual chunk.
+// nres[b] > 0, mma_residual_weight(nres[b]) more, the last of which is the
+// residual window (the ones before it are empty: they give the window, read
+// from global memory on the CUDA cores, its weight in the equal split).
 struct MmaTable {
   int32_t bprefix[kMaxB + 1];
   int32_t nc[kMaxB];
@@ -124,6 +126,10 @@ struct MmaPlan {
 // false when the shape has no tensor-core kernel (then the CUDA-core kernel
 // of launch_decode serves it)
 bool mma_plan(const Geometry &geo, int sm_count, MmaPlan *plan);
+// chunks of the split given to a residual window of nres tokens
+inline int mma_residual_weight(int nres) {
+  return nres > 0 ? 1 + (nres + 31) / 32 : 0;
+}
 size_t mma_part_floats(const Geometry &geo, const MmaPlan &plan);
 cudaError_t launch_decode_mma(const Geometry &geo, const Planes &pl,
                               const MmaPlan &plan, MmaArgs args,
