@@ -27,7 +27,6 @@ struct vq_kivi_cache {
   int32_t fail_chunk;     // testing hook, -1 = off
   MmaPlan plan;
   unsigned *err;          // device word set by a kernel whose wait gave up
-  unsigned *tickets;      // per-head tickets of the tensor-core decode
   int32_t S[kMaxB], Tq[kMaxB], nres[kMaxB];
 };
 
@@ -193,7 +192,6 @@ int vq_kivi_quantize(const vq_kivi_params *p, const void *K, const void *V,
   size_t o_Vr = off; off += round_up(sz_res, A);
   size_t o_part = off; off += round_up(sz_part, A);
   size_t o_err = off; off += A;
-  size_t o_tick = off; off += round_up(BH * sizeof(unsigned), A);
   c->block_bytes = off;
 
   e = cudaMallocAsync(&c->block, c->block_bytes, st);
@@ -215,7 +213,6 @@ int vq_kivi_quantize(const vq_kivi_params *p, const void *K, const void *V,
   pl.Vr = (__half *)(base + o_Vr);
   pl.part = (float *)(base + o_part);
   c->err = (unsigned *)(base + o_err);
-  c->tickets = (unsigned *)(base + o_tick);
   c->last_stream = st;
 
   auto abort_create = [&](cudaError_t err, const char *what) {
@@ -339,7 +336,6 @@ int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
     args.q = (const __half *)q;
     args.out = out;
     args.part = c->pl.part;
-    args.cnt = c->tickets;
     args.err = c->err;
     args.scale_log2 = scale * 1.4426950408889634f;
     args.N = tab.bprefix[p.B];
@@ -488,10 +484,7 @@ int vq_kivi_device_status(vq_kivi_cache *c) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(c->last_stream);
   if (e != cudaSuccess) return cuda_fail(e, "reading the device status");
   if (flag) {
-    // a kernel that gave up may leave head tickets half counted: reset them
     cudaMemsetAsync(c->err, 0, sizeof flag, c->last_stream);
-    cudaMemsetAsync(c->tickets, 0,
-                    sizeof(unsigned) * c->p.B * c->p.H_kv, c->last_stream);
     return fail(VQ_ERR_CUDA, "a decode kernel gave up waiting for its "
                 "shared-memory copies; its outputs are not valid");
   }

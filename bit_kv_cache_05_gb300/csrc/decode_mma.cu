@@ -1,6 +1,6 @@
 // Host side of the tensor-core decode: kernel choice, launch plan (stages,
-// persistent grid size) and launch.  The kernel, including the log-sum-exp
-// merge of the per-warp partials, is in decode_mma.cuh.
+// persistent grid size) and launch of the decode kernel and of the
+// log-sum-exp merge of its per-warp partials (both in decode_mma.cuh).
 #include "decode_mma.cuh"
 
 namespace vqk {
@@ -92,6 +92,34 @@ cudaError_t launch_decode_mma(const Geometry &geo, const Planes &pl,
   args.W = (int)W;
   const int grid = (int)((W + kNW - 1) / kNW);
   ki.fn<<<grid, kNW * 32, plan.smem, st>>>(geo, pl, args, tab);
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  mma::MergeFn mf = nullptr;
+  switch (geo.D * 8 + plan.GQp) {
+    case 64 * 8 + 1: mf = mma::merge_fn<64, 1>(); break;
+    case 64 * 8 + 2: mf = mma::merge_fn<64, 2>(); break;
+    case 64 * 8 + 4: mf = mma::merge_fn<64, 4>(); break;
+    case 128 * 8 + 1: mf = mma::merge_fn<128, 1>(); break;
+    case 128 * 8 + 2: mf = mma::merge_fn<128, 2>(); break;
+    case 128 * 8 + 4: mf = mma::merge_fn<128, 4>(); break;
+    default: return cudaErrorInvalidValue;
+  }
+  // merge warps per CTA: enough for the largest partial count of a head to
+  // be read in one round
+  int64_t n_max = 1;
+  for (int b = 0; b < geo.B; ++b) {
+    if (tab.nc[b] == 0) continue;
+    for (int h = 0; h < geo.H_kv; ++h) {
+      const int64_t cs = tab.bprefix[b] + (int64_t)h * tab.nc[b];
+      const int64_t ce = cs + tab.nc[b];
+      const int64_t n = (ce * W - 1) / args.N - ((cs + 1) * W - 1) / args.N + 1;
+      if (n > n_max) n_max = n;
+    }
+  }
+  int64_t nw = (n_max + mma::kMergeU - 1) / mma::kMergeU;
+  if (nw > mma::kMergeWarps) nw = mma::kMergeWarps;
+  mf<<<dim3(geo.B * geo.H_q, geo.D / 32), (unsigned)nw * 32, 0, st>>>(geo, args, tab);
   count_launch();
   return cudaGetLastError();
 }

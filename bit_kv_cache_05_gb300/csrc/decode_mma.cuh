@@ -44,13 +44,8 @@ namespace vqk {
 namespace mma {
 
 constexpr int kC = 64;          // tokens per chunk (4 m16 tiles)
-#ifndef VQK_NW
-#define VQK_NW 4
-#endif
-#ifndef VQK_MINB
-#define VQK_MINB 3
-#endif
-constexpr int kNW = VQK_NW;     // warps per CTA
+constexpr int kNW = 4;          // warps per CTA
+constexpr int kMinBlocks = 3;   // CTAs per SM the register budget allows
 constexpr int kMaxStages = 4;
 // a partial (o[D], m, l) per (warp segment, query head), padded to D + 4
 // floats so that the o rows stay 16-byte aligned
@@ -521,7 +516,7 @@ __device__ __noinline__ void residual_window(
 }
 
 template <class C>
-__global__ void __launch_bounds__(kNW * 32, VQK_MINB)
+__global__ void __launch_bounds__(kNW * 32, kMinBlocks)
 k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   using L = Layout<C::BITS>;
   constexpr int D = C::D, KS = C::KS, NJ = C::NJ, GQP = C::GQP, WG = C::WG;
@@ -748,73 +743,9 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     has_res = tab.nres[b] > 0;
   };
 
-  // The last warp to finish head hd merges the head's partials (slots
-  // w + hd for the warps w whose chunk range touches it) into the output.
-  auto combine = [&](int b, int h, int hd) {
-    constexpr int CPL = D / 32;
-    const int64_t cs = tab.bprefix[b] + (int64_t)h * tab.nc[b];
-    const int64_t ce = cs + tab.nc[b];
-    const int w0 = (int)(((cs + 1) * W - 1) / N);
-    const int w1 = (int)((ce * W - 1) / N);
-    for (int hh = 0; hh < GQ; ++hh) {
-      auto entry = [&](int w) {
-        return args.part + ((size_t)(w + hd) * GQP + hh) * part_stride<D>();
-      };
-      float M = -INFINITY;
-      for (int w = w0 + lane; w <= w1; w += 32) M = fmaxf(M, __ldcg(entry(w) + D));
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1)
-        M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-      float Ls = 0.f;
-      for (int w = w0 + lane; w <= w1; w += 32)
-        Ls += exp2_neg(__ldcg(entry(w) + D) - M) * __ldcg(entry(w) + D + 1);
-      Ls = warp_sum(Ls);
-      // partial weights 2^(m_w - M), lane j holding those of partials
-      // w0 + j, w0 + j + 32, ...; the o rows are read kMB at a time, all in
-      // flight together
-      constexpr int kMB = 8;
-      float acc[CPL];
-#pragma unroll
-      for (int u = 0; u < CPL; ++u) acc[u] = 0.f;
-      for (int wb = w0; wb <= w1; wb += 32) {
-        const int wl = wb + lane;
-        const float fl = wl <= w1 ? exp2_neg(__ldcg(entry(wl) + D) - M) : 0.f;
-        const int nbw = w1 - wb + 1 < 32 ? w1 - wb + 1 : 32;
-        for (int j0 = 0; j0 < nbw; j0 += kMB) {
-          float v[kMB][CPL];
-#pragma unroll
-          for (int j = 0; j < kMB; ++j) {
-            const int w = wb + (j0 + j < nbw ? j0 + j : 0);
-            const float *e = entry(w) + lane * CPL;
-            if constexpr (CPL == 4) {
-              const float4 x = __ldcg(reinterpret_cast<const float4 *>(e));
-              v[j][0] = x.x; v[j][1] = x.y; v[j][2] = x.z; v[j][3] = x.w;
-            } else {
-              const float2 x = __ldcg(reinterpret_cast<const float2 *>(e));
-              v[j][0] = x.x; v[j][1] = x.y;
-            }
-          }
-#pragma unroll
-          for (int j = 0; j < kMB; ++j) {
-            // lanes past the batch's end weigh 0 (fl = 0 there)
-            const float f = __shfl_sync(kFull, fl, (j0 + j) & 31);
-            if (j0 + j < nbw) {
-#pragma unroll
-              for (int u = 0; u < CPL; ++u) acc[u] = fmaf(f, v[j][u], acc[u]);
-            }
-          }
-        }
-      }
-      const float inv = 1.0f / Ls;
-      float *out = args.out + ((size_t)b * geo.H_q + h * GQ + hh) * D + lane * CPL;
-#pragma unroll
-      for (int u = 0; u < CPL; ++u) out[u] = acc[u] * inv;
-    }
-  };
-
-  // write this warp's partial of head hd (slot wg + hd); the warp that
-  // completes the head's ticket count merges the partials
-  auto flush = [&](int b, int h, int hd) {
+  // write this warp's partial of head hd (slot wg + hd); k_merge_mma, run
+  // after the decode kernel, merges each head's partials
+  auto flush = [&](int hd) {
     float Lsum = head_reduce<GQP>(l_run, AddOp());
     float Zt[NJ];
 #pragma unroll
@@ -849,22 +780,6 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
         __stcg(dst + D + 1, Lsum);
       }
     }
-    // ticket: the warp that takes the head's last ticket sees every other
-    // warp's partial (each fenced before its increment) and merges them
-    __threadfence();
-    __syncwarp();
-    const int64_t cs = tab.bprefix[b] + (int64_t)h * tab.nc[b];
-    const int64_t ce = cs + tab.nc[b];
-    const unsigned nw = (unsigned)(((ce * W - 1) / N) - (((cs + 1) * W - 1) / N) + 1);
-    unsigned last = 0;
-    if (lane == 0) last = atomicAdd(&args.cnt[hd], 1u) == nw - 1 ? 1u : 0u;
-    last = __shfl_sync(kFull, last, 0);
-    if (last) {
-      __threadfence();
-      combine(b, h, hd);
-      if (lane == 0) args.cnt[hd] = 0;
-    }
-    __syncwarp();
   };
 
   // ---- one staged chunk: scores, softmax update, values.  FULL: all four
@@ -1073,7 +988,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
       }
     }
     const bool head_ends = cu.k == tab.nc[cu.b] - 1 || i == n_mine - 1;
-    if (head_ends) flush(cu.b, cu.h, hd);
+    if (head_ends) flush(hd);
     __syncwarp();
     if (i + ST < n_mine) {
       if (is_quant(pc)) {
@@ -1097,6 +1012,93 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     for (int j = 0; j < ST; ++j)
       if (pending & (1u << j)) mbar_wait(&bars[j], (phase >> j) & 1u);
   }
+}
+
+// ---- merge of the per-warp partials ----------------------------------------
+//
+// The partials of kv head hd sit in slots w + hd for the warps w whose chunk
+// range touches the head; the log-sum-exp merge is M = max m_w,
+// L = sum 2^(m_w - M) l_w, o = sum 2^(m_w - M) o_w / L.  One CTA per
+// (sequence, query head, 32-channel slice) with nw <= kMergeWarps warps
+// (nw sized by the launcher to the largest partial count of a head); warp
+// j takes partials j, j + nw, ... with lanes on channels, keeping a running
+// (max, sum) of its own, and the warps' results are combined in shared
+// memory.  A warp reads its partials kMergeU at a time, all in flight, so a
+// head of up to nw * kMergeU partials costs one round of loads.
+constexpr int kMergeWarps = 16;
+constexpr int kMergeU = 8;
+
+template <int D, int GQP>
+__global__ void __launch_bounds__(kMergeWarps * 32)
+k_merge_mma(Geometry geo, MmaArgs args, MmaTable tab) {
+  __shared__ float sm_m[kMergeWarps], sm_l[kMergeWarps];
+  __shared__ float sm_o[kMergeWarps][32];
+  const int b = blockIdx.x / geo.H_q, hq = blockIdx.x - b * geo.H_q;
+  if (tab.nc[b] == 0) return;   // the launcher zeroed this output
+  const int GQ = args.GQ;
+  const int h = hq / GQ, hh = hq - h * GQ;
+  const int hd = b * geo.H_kv + h;
+  const int64_t N = args.N, W = args.W;
+  const int64_t cs = tab.bprefix[b] + (int64_t)h * tab.nc[b];
+  const int64_t ce = cs + tab.nc[b];
+  const int w0 = (int)(((cs + 1) * W - 1) / N);
+  const int n = (int)((ce * W - 1) / N) - w0 + 1;
+  const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
+  const int c = blockIdx.y * 32 + lane;
+  auto entry = [&](int k) {
+    return args.part + ((size_t)(w0 + k + hd) * GQP + hh) * part_stride<D>();
+  };
+
+  float m_run = -INFINITY, l_run = 0.f, o_run = 0.f;
+  for (int k0 = wp; k0 < n; k0 += nw * kMergeU) {
+    float mu[kMergeU], lu[kMergeU], ou[kMergeU];
+#pragma unroll
+    for (int u = 0; u < kMergeU; ++u) {
+      const int k = k0 + u * nw;
+      const bool ok = k < n;
+      const float *e = entry(ok ? k : k0);
+      mu[u] = ok ? __ldcg(e + D) : -INFINITY;
+      lu[u] = ok ? __ldcg(e + D + 1) : 0.f;
+      ou[u] = ok ? __ldcg(e + c) : 0.f;
+    }
+    float mr = m_run;
+#pragma unroll
+    for (int u = 0; u < kMergeU; ++u) mr = fmaxf(mr, mu[u]);
+    const float a = m_run == -INFINITY ? 0.f : exp2_neg(m_run - mr);
+    l_run *= a;
+    o_run *= a;
+#pragma unroll
+    for (int u = 0; u < kMergeU; ++u) {
+      // partials of warps whose range held only empty chunks carry
+      // m = -inf and weigh nothing (also when every m so far is -inf)
+      const float f = mu[u] == -INFINITY ? 0.f : exp2_neg(mu[u] - mr);
+      l_run = fmaf(f, lu[u], l_run);
+      o_run = fmaf(f, ou[u], o_run);
+    }
+    m_run = mr;
+  }
+  if (lane == 0) { sm_m[wp] = m_run; sm_l[wp] = l_run; }
+  sm_o[wp][lane] = o_run;
+  __syncthreads();
+  if (wp == 0) {
+    float M = -INFINITY;
+    for (int j = 0; j < nw; ++j) M = fmaxf(M, sm_m[j]);
+    float L = 0.f, o = 0.f;
+    for (int j = 0; j < nw; ++j) {
+      const float f = sm_m[j] == -INFINITY ? 0.f : exp2_neg(sm_m[j] - M);
+      L = fmaf(f, sm_l[j], L);
+      o = fmaf(f, sm_o[j][lane], o);
+    }
+    args.out[((size_t)b * geo.H_q + hq) * D + c] = o / L;
+  }
+}
+
+using MergeFn = void (*)(Geometry, MmaArgs, MmaTable);
+
+template <int D, int GQP>
+MergeFn merge_fn() {
+  return &k_merge_mma<D, GQP>;
 }
 
 using KernelFn = void (*)(Geometry, Planes, MmaArgs, MmaTable);

@@ -108,7 +108,6 @@ struct MmaArgs {
   const __half *q;   // [B][H_q][D]
   float *out;        // [B][H_q][D]
   float *part;       // partials: slot (warp + head) x GQp x (D + 2)
-  unsigned *cnt;     // per-head tickets, [B * H_kv], zero between launches
   unsigned *err;     // set to nonzero when a pipeline wait gave up
   float scale_log2;  // softmax scale * log2(e)
   int N;             // total chunks
@@ -128,7 +127,7 @@ struct MmaPlan {
 bool mma_plan(const Geometry &geo, int sm_count, MmaPlan *plan);
 // chunks of the split given to a residual window of nres tokens
 inline int mma_residual_weight(int nres) {
-  return nres > 0 ? 1 + (nres + 31) / 32 : 0;
+  return nres > 0 ? 1 + 2 * ((nres + 31) / 32) : 0;
 }
 size_t mma_part_floats(const Geometry &geo, const MmaPlan &plan);
 cudaError_t launch_decode_mma(const Geometry &geo, const Planes &pl,
