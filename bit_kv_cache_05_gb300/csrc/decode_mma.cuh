@@ -188,52 +188,43 @@ __device__ __forceinline__ void load_halves(const __half *p, float (&out)[NJ]) {
 // (gid, tig) holds K slots 2tig, 2tig+1 (register "lo") and 2tig+8, 2tig+9
 // ("hi") of tokens gid and gid+8; those four slots are channels 4tig ...
 // 4tig+3 of the K-step, slot e (0..3) being channel 4tig + off(e).  The code
-// of slot e arrives scaled by 2^(sexp(e) - 24); the score B operand carries
-// 2^-sexp(e) (folded into a copy of q'), so every product carries exactly
-// 2^-24.  Words: a uint4 of a token row holds WPQ K-steps.
+// of channel c arrives scaled by 2^(oexp(c) - 24); the score B operand
+// carries 2^-oexp(c) (folded into a copy of q'), so every product carries
+// exactly 2^-24.  4- and 8-bit codes use the packed order (a uint4 of a token
+// row holds WPQ K-steps, bytes permuted into place); 2-bit codes use the
+// fragment order, where masks alone place the codes.
 //
 // Value A fragment (rows = channels 2gid, 2gid+1 of an m16 tile, K = tokens
-// of the K-step): lane (gid, tig) permutes the bytes of two tokens' words
-// (vsel) and masks channel 2gid (vmask0) and 2gid+1 (vmask1), whose codes
-// arrive scaled by 2^(vpos0 - 24) and 2^(vpos1 - 24); the output rows are
-// scaled back at the end.  A uint4 of a token row covers VTPQ m16 tiles;
-// tile u of it uses word vword(x, u, gid).
+// of the K-step): in the packed order lane (gid, tig) permutes the bytes of
+// two tokens' words (vsel) and masks channel 2gid (vmask0) and 2gid+1
+// (vmask1), whose codes arrive scaled by 2^(vpos0 - 24) and 2^(vpos1 - 24);
+// a uint4 of a token row covers VTPQ m16 tiles, tile u of it uses word
+// vword(x, u, gid).  In the 2-bit fragment order the two tokens of a
+// register share a word and masks alone place them.  The output rows are
+// scaled back at the end.
 template <int BITS> struct Layout;
 
 template <> struct Layout<2> {
-  static constexpr int WPQ = 4;    // K-steps per uint4 (one word each)
-  static constexpr int VTPQ = 4;   // value tiles per uint4
-  // byte tig of word ks holds channels 4tig..4tig+3; the byte is copied to
-  // every byte position and each slot's 2-bit field masked in place
-  static __device__ __forceinline__ uint32_t score_sel(int tig) {
-    return 0x1111u * (uint32_t)tig;
+  // codes in kLayoutFrag2 order: a 32-bit word holds 16 fields, field r of
+  // each half at bits 2r (low half) and 16 + 2r (high half).  Fields 0..4
+  // are masked in place (exponent 2r); fields 5..7 are masked after one
+  // shift of the word by 6 (exponent 2r - 6): a field at bit p of a half is
+  // the fp16 subnormal code * 2^(p - 24).
+  static constexpr bool FRAG = true;
+  static __host__ __device__ constexpr int fexp(int r) { return r < 5 ? 2 * r : 2 * r - 6; }
+  static __device__ __forceinline__ uint32_t field(uint32_t w, uint32_t w6, int r) {
+    return r < 5 ? (w & (0x00030003u << (2 * r))) : (w6 & (0x00030003u << (2 * r - 6)));
   }
-  static __device__ __forceinline__ void score_a(const uint4 &q, int ks,
-                                                 uint32_t sel, uint32_t &lo,
-                                                 uint32_t &hi) {
-    const uint32_t x = __byte_perm((&q.x)[ks & 3], 0u, sel);
-    lo = x & 0x000C0003u;   // channel 4tig (x1), 4tig+1 (x4)
-    hi = x & 0x00C00030u;   // channel 4tig+2 (x16), 4tig+3 (x64)
-  }
+  // score slot e of channel c (K-step c/16, lane group (c/4) mod 4, e = c
+  // mod 4) is field 2 (ks mod 4) + e/2 of half e mod 2
   static __host__ __device__ constexpr int off(int e) { return e; }
-  static __host__ __device__ constexpr int sexp(int e) { return 2 * e; }
-  // exponent of the slot that holds channel offset o (0..3)
-  static __device__ __forceinline__ int oexp(int o) { return 2 * o; }
-  // word of m16 tile u (0..VTPQ-1) within a uint4 of a token row
-  static __device__ __forceinline__ uint32_t vword(const uint4 &x, int u, int) {
-    return (&x.x)[u];
+  static __device__ __forceinline__ int oexp(int c) {
+    return fexp(2 * ((c >> 4) & 3) + ((c & 3) >> 1));
   }
-  static __device__ __forceinline__ uint32_t vsel(int gid) {
-    const uint32_t b = gid >> 1;
-    return b | (b << 4) | ((4 + b) << 8) | ((4 + b) << 12);
-  }
-  static __device__ __forceinline__ int vpos0(int gid) { return 4 * (gid & 1); }
-  static __device__ __forceinline__ int vpos1(int gid) { return 4 * (gid & 1) + 2; }
-  static __device__ __forceinline__ void value_a(uint32_t x, int gid,
-                                                 uint32_t &r0, uint32_t &r1) {
-    r0 = x & (0x00030003u << vpos0(gid));
-    r1 = x & (0x00030003u << vpos1(gid));
-  }
+  static __device__ __forceinline__ uint32_t score_sel(int) { return 0u; }
+  static __device__ __forceinline__ uint32_t vsel(int) { return 0u; }
+  static __device__ __forceinline__ int vpos0(int) { return 0; }
+  static __device__ __forceinline__ int vpos1(int) { return 0; }
 };
 
 template <> struct Layout<4> {
@@ -255,7 +246,8 @@ template <> struct Layout<4> {
   }
   static __host__ __device__ constexpr int off(int e) { return (e & 1) * 2 + (e >> 1); }
   static __host__ __device__ constexpr int sexp(int e) { return 4 * (e >> 1); }
-  static __device__ __forceinline__ int oexp(int o) { return 4 * (o & 1); }
+  static constexpr bool FRAG = false;
+  static __device__ __forceinline__ int oexp(int c) { return 4 * (c & 1); }
   static __device__ __forceinline__ uint32_t vword(const uint4 &x, int u, int gid) {
     const uint32_t w0 = u ? x.z : x.x, w1 = u ? x.w : x.y;
     return (gid >> 2) ? w1 : w0;   // word 2u + gid/4
@@ -287,6 +279,7 @@ template <> struct Layout<8> {
   }
   static __host__ __device__ constexpr int off(int e) { return (e & 1) * 2 + (e >> 1); }
   static __host__ __device__ constexpr int sexp(int) { return 0; }
+  static constexpr bool FRAG = false;
   static __device__ __forceinline__ int oexp(int) { return 0; }
   static __device__ __forceinline__ uint32_t vword(const uint4 &x, int, int gid) {
     // word gid/2: bit 1 of gid picks the odd word, bit 2 the upper pair
@@ -657,7 +650,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
       if (hh < GQ)
         v = __half2float(args.q[((size_t)b * geo.H_q + h * GQ + hh) * D + c]) *
             args.scale_log2;
-      const float vb = v * exp2i(-L::oexp(c & 3));
+      const float vb = v * exp2i(-L::oexp(c));
       qn[i] = v;
       qb[i] = vb;
       mq[hh] = fmaxf(mq[hh], fabsf(vb));
@@ -767,8 +760,15 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
         const int vb = (j * GQP) >> 2;
         if ((4 * vb + tig) / GQP != j) continue;
         const int c0 = 16 * mv + 2 * gid;
-        float o0 = ((O[mv][0] + O[mv][1]) * rs0 + Zt[j]) * aq;
-        float o1 = ((O[mv][2] + O[mv][3]) * rs1 + Zt[j]) * aq;
+        // rows gid / gid+8 of tile mv (channels c0, c0+1) arrive scaled by
+        // 2^(p - 24) for the code's bit position p
+        float sa = rs0, sb = rs1;
+        if constexpr (L::FRAG) {
+          sa = exp2i(24 - L::fexp(2 * (mv & 3)));
+          sb = exp2i(24 - L::fexp(2 * (mv & 3) + 1));
+        }
+        float o0 = ((O[mv][0] + O[mv][1]) * sa + Zt[j]) * aq;
+        float o1 = ((O[mv][2] + O[mv][3]) * sb + Zt[j]) * aq;
         if (has_res) {
           o0 += res_o[h_s * D + c0] * ar;
           o1 += res_o[h_s * D + c0 + 1] * ar;
@@ -814,25 +814,68 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
         for (int m = 0; m < MPW; ++m)
 #pragma unroll
           for (int r = 0; r < 4; ++r) acc[m][r] = 0.f;
-#pragma unroll
-        for (int q = 0; q < KS / L::WPQ; ++q) {
-          uint4 r0[MPW], r1[MPW];
+        if constexpr (L::FRAG) {
+          // fragment order: lane group tig's D/64 words of a token row are
+          // contiguous; word hw holds K-steps 4hw ... 4hw+3
+          constexpr int NH = D / 64;
+          using RowW = std::conditional_t<NH == 2, uint2, uint32_t>;
+          RowW r0[MPW], r1[MPW];
 #pragma unroll
           for (int m = 0; m < MPW; ++m) {
-            const uint4 *row = kc + (16 * (mt0 + m) + gid) * ROWQ;
-            r0[m] = row[q];
-            r1[m] = row[8 * ROWQ + q];
+            const unsigned char *row = st + C::S_KC + (16 * (mt0 + m) + gid) * ROW + 4 * NH * tig;
+            r0[m] = *reinterpret_cast<const RowW *>(row);
+            r1[m] = *reinterpret_cast<const RowW *>(row + 8 * ROW);
           }
 #pragma unroll
-          for (int kq = 0; kq < L::WPQ; ++kq) {
-            const int ks = q * L::WPQ + kq;
+          for (int hw = 0; hw < NH; ++hw) {
+            uint32_t w0[MPW], w1[MPW], s0[MPW], s1[MPW];
 #pragma unroll
             for (int m = 0; m < MPW; ++m) {
-              if (FULL || mt0 + m < nmt) {
-                uint32_t a0, a1, a2, a3;
-                L::score_a(r0[m], ks, s_sel, a0, a2);
-                L::score_a(r1[m], ks, s_sel, a1, a3);
-                mma16816(acc[m], a0, a1, a2, a3, Bs[ks][0], Bs[ks][1]);
+              if constexpr (NH == 2) {
+                w0[m] = hw ? r0[m].y : r0[m].x;
+                w1[m] = hw ? r1[m].y : r1[m].x;
+              } else {
+                w0[m] = r0[m];
+                w1[m] = r1[m];
+              }
+              s0[m] = w0[m] >> 6;
+              s1[m] = w1[m] >> 6;
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const int ks = 4 * hw + kk;
+#pragma unroll
+              for (int m = 0; m < MPW; ++m) {
+                if (FULL || mt0 + m < nmt) {
+                  mma16816(acc[m], L::field(w0[m], s0[m], 2 * kk),
+                           L::field(w1[m], s1[m], 2 * kk),
+                           L::field(w0[m], s0[m], 2 * kk + 1),
+                           L::field(w1[m], s1[m], 2 * kk + 1), Bs[ks][0], Bs[ks][1]);
+                }
+              }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < KS / L::WPQ; ++q) {
+            uint4 r0[MPW], r1[MPW];
+#pragma unroll
+            for (int m = 0; m < MPW; ++m) {
+              const uint4 *row = kc + (16 * (mt0 + m) + gid) * ROWQ;
+              r0[m] = row[q];
+              r1[m] = row[8 * ROWQ + q];
+            }
+#pragma unroll
+            for (int kq = 0; kq < L::WPQ; ++kq) {
+              const int ks = q * L::WPQ + kq;
+#pragma unroll
+              for (int m = 0; m < MPW; ++m) {
+                if (FULL || mt0 + m < nmt) {
+                  uint32_t a0, a1, a2, a3;
+                  L::score_a(r0[m], ks, s_sel, a0, a2);
+                  L::score_a(r1[m], ks, s_sel, a1, a3);
+                  mma16816(acc[m], a0, a1, a2, a3, Bs[ks][0], Bs[ks][1]);
+                }
               }
             }
           }
@@ -936,23 +979,54 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
           bv[vb][0] = pack_half2(w01.x, w01.y);
           bv[vb][1] = pack_half2(w23.x, w23.y);
         }
-        // m16 channel tiles, VTPQ per uint4 of the token rows
+        if constexpr (L::FRAG) {
+          // fragment order: pair (ta, ta+4) is pair tig of block kt, pair
+          // (ta+8, ta+12) pair 4+tig; lane gid's D/64 words of a pair are
+          // contiguous, word hw covering tiles 4hw ... 4hw+3
+          constexpr int NV = D / 64;
+          using PairW = std::conditional_t<NV == 2, uint2, uint32_t>;
+          const unsigned char *blk = st + C::S_VC + kt * 16 * ROW;
+          const PairW pa = *reinterpret_cast<const PairW *>(blk + (8 * tig + gid) * 4 * NV);
+          const PairW pb = *reinterpret_cast<const PairW *>(blk + (8 * (4 + tig) + gid) * 4 * NV);
 #pragma unroll
-        for (int q = 0; q < KS / L::VTPQ; ++q) {
-          const uint4 xa = vc[ta * ROWQ + q];
-          const uint4 xb = vc[(ta + 4) * ROWQ + q];
-          const uint4 xc = vc[(ta + 8) * ROWQ + q];
-          const uint4 xd = vc[(ta + 12) * ROWQ + q];
+          for (int hw = 0; hw < NV; ++hw) {
+            uint32_t wa, wb;
+            if constexpr (NV == 2) {
+              wa = hw ? pa.y : pa.x;
+              wb = hw ? pb.y : pb.x;
+            } else {
+              wa = pa;
+              wb = pb;
+            }
+            const uint32_t sa = wa >> 6, sb = wb >> 6;
 #pragma unroll
-          for (int u = 0; u < L::VTPQ; ++u) {
-            const int mv = q * L::VTPQ + u;
-            const int vb = (((16 * mv) / G) * GQP) >> 2;
-            uint32_t a0, a1, a2, a3;
-            L::value_a(__byte_perm(L::vword(xa, u, gid), L::vword(xb, u, gid), v_sel),
-                       gid, a0, a1);
-            L::value_a(__byte_perm(L::vword(xc, u, gid), L::vword(xd, u, gid), v_sel),
-                       gid, a2, a3);
-            mma16816(O[mv], a0, a1, a2, a3, bv[vb][0], bv[vb][1]);
+            for (int mm = 0; mm < 4; ++mm) {
+              const int mv = 4 * hw + mm;
+              const int vb = (((16 * mv) / G) * GQP) >> 2;
+              mma16816(O[mv], L::field(wa, sa, 2 * mm), L::field(wa, sa, 2 * mm + 1),
+                       L::field(wb, sb, 2 * mm), L::field(wb, sb, 2 * mm + 1),
+                       bv[vb][0], bv[vb][1]);
+            }
+          }
+        } else {
+          // m16 channel tiles, VTPQ per uint4 of the token rows
+#pragma unroll
+          for (int q = 0; q < KS / L::VTPQ; ++q) {
+            const uint4 xa = vc[ta * ROWQ + q];
+            const uint4 xb = vc[(ta + 4) * ROWQ + q];
+            const uint4 xc = vc[(ta + 8) * ROWQ + q];
+            const uint4 xd = vc[(ta + 12) * ROWQ + q];
+#pragma unroll
+            for (int u = 0; u < L::VTPQ; ++u) {
+              const int mv = q * L::VTPQ + u;
+              const int vb = (((16 * mv) / G) * GQP) >> 2;
+              uint32_t a0, a1, a2, a3;
+              L::value_a(__byte_perm(L::vword(xa, u, gid), L::vword(xb, u, gid), v_sel),
+                         gid, a0, a1);
+              L::value_a(__byte_perm(L::vword(xc, u, gid), L::vword(xd, u, gid), v_sel),
+                         gid, a2, a3);
+              mma16816(O[mv], a0, a1, a2, a3, bv[vb][0], bv[vb][1]);
+            }
           }
         }
       }

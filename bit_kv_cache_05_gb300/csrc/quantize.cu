@@ -86,6 +86,47 @@ __device__ __forceinline__ void store_packed_tile(const uint8_t *codes, int g,
   }
 }
 
+// The g x D code tile in kLayoutFrag2 order (2-bit codes): one thread per
+// 32-bit word, whose 16 fields are gathered from the tile.
+__device__ __forceinline__ void store_frag2_keys(const uint8_t *codes, int g,
+                                                 int D, uint8_t *dst) {
+  const int wpr = D / 16, nh = D / 64;
+  for (int w = threadIdx.x; w < g * wpr; w += blockDim.x) {
+    const int i = w / wpr, wi = w - i * wpr;
+    const int tig = wi / nh, hw = wi - tig * nh;
+    uint32_t acc = 0;
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const int ks = 4 * hw + (r >> 1), e = 2 * (r & 1) + s;
+        acc |= (uint32_t)codes[i * D + 16 * ks + 4 * tig + e] << (16 * s + 2 * r);
+      }
+    reinterpret_cast<uint32_t *>(dst)[w] = acc;
+  }
+}
+
+__device__ __forceinline__ void store_frag2_values(const uint8_t *codes, int g,
+                                                   int D, uint8_t *dst) {
+  const int nv = D / 64;
+  for (int w = threadIdx.x; w < g * D / 16; w += blockDim.x) {
+    const int kb = w / D, wb = w - kb * D;
+    const int pi = wb / (8 * nv), rem = wb - pi * 8 * nv;
+    const int j = rem / nv, hw = rem - j * nv;
+    const int tA = 16 * kb + (pi < 4 ? pi : pi + 4);
+    uint32_t acc = 0;
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const int mv = 4 * hw + (r >> 1), rho = r & 1;
+        acc |= (uint32_t)codes[(tA + 4 * s) * D + 16 * mv + 2 * j + rho]
+               << (16 * s + 2 * r);
+      }
+    reinterpret_cast<uint32_t *>(dst)[w] = acc;
+  }
+}
+
 // Copies the g fp16 rows of one group (token positions P0 ... P0+g-1) into a
 // shared tile [g][D] with 16-byte loads, all in flight at once.  Position p
 // comes from the residual ring when p < split, else from input row p - split.
@@ -147,7 +188,10 @@ k_flush(Geometry geo, Planes pl, const __half *__restrict__ Kin,
                                                   mn, scale, rcp, levels);
   }
   __syncthreads();
-  store_packed_tile<BITS>(codes, g, D, pl.Kc + (bh * geo.Tcap + P0) * geo.row);
+  if (BITS == 2 && geo.layout == kLayoutFrag2)
+    store_frag2_keys(codes, g, D, pl.Kc + (bh * geo.Tcap + P0) * geo.row);
+  else
+    store_packed_tile<BITS>(codes, g, D, pl.Kc + (bh * geo.Tcap + P0) * geo.row);
   __syncthreads();
 
   // ---- values: per token over groups of g channels ----
@@ -176,7 +220,10 @@ k_flush(Geometry geo, Planes pl, const __half *__restrict__ Kin,
     }
   }
   __syncthreads();
-  store_packed_tile<BITS>(codes, g, D, pl.Vc + (bh * geo.Tcap + P0) * geo.row);
+  if (BITS == 2 && geo.layout == kLayoutFrag2)
+    store_frag2_values(codes, g, D, pl.Vc + (bh * geo.Tcap + P0) * geo.row);
+  else
+    store_packed_tile<BITS>(codes, g, D, pl.Vc + (bh * geo.Tcap + P0) * geo.row);
 }
 
 // Residual ring writes: 16-byte chunks of fp16 rows.
@@ -268,6 +315,40 @@ cudaError_t launch_tail(const Geometry &geo, const Planes &pl,
   dim3 grid((total_tokens + rows_per_block - 1) / rows_per_block, geo.H_kv);
   k_tail<<<grid, kThreads, 0, st>>>(geo, pl, Kin, Vin, in_stride, tab,
                                     total_tokens);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// kLayoutFrag2 plane -> packed order: one thread per packed 32-bit word
+// (16 codes of one token row), each field gathered from its fragment-order
+// position.  Covers all Tcap rows of every (b, h).
+__global__ void k_export_frag2(Geometry geo, const uint8_t *__restrict__ src,
+                               bool values, uint32_t *__restrict__ dst) {
+  const int D = geo.D, wpr = D / 16;
+  const size_t total = (size_t)geo.B * geo.H_kv * geo.Tcap * wpr;
+  for (size_t w = blockIdx.x * (size_t)blockDim.x + threadIdx.x; w < total;
+       w += (size_t)gridDim.x * blockDim.x) {
+    const size_t row = w / wpr;                 // (b, h, t)
+    const int w16 = (int)(w - row * wpr);
+    const int t = (int)(row % geo.Tcap);
+    const uint32_t *rw = reinterpret_cast<const uint32_t *>(src) + row * wpr;
+    const uint32_t *blk = reinterpret_cast<const uint32_t *>(src) +
+                          (row - (t & 15)) * wpr;   // the token's 16-row block
+    uint32_t acc = 0;
+#pragma unroll 4
+    for (int f = 0; f < 16; ++f) {
+      const int c = 16 * w16 + f;
+      const FragPos pos = values ? frag2_value(D, t & 15, c) : frag2_key(D, c);
+      const uint32_t word = values ? blk[pos.word] : rw[pos.word];
+      acc |= ((word >> pos.bit) & 3u) << (2 * f);
+    }
+    dst[w] = acc;
+  }
+}
+
+cudaError_t launch_export_frag2(const Geometry &geo, const uint8_t *src,
+                                bool values, void *dst, cudaStream_t st) {
+  k_export_frag2<<<1024, 256, 0, st>>>(geo, src, values, (uint32_t *)dst);
   count_launch();
   return cudaGetLastError();
 }
