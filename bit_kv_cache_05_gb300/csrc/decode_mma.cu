@@ -91,9 +91,21 @@ cudaError_t launch_decode_mma(const Geometry &geo, const Planes &pl,
   if (W > args.N) W = args.N;
   args.W = (int)W;
   const int grid = (int)((W + kNW - 1) / kNW);
-  ki.fn<<<grid, kNW * 32, plan.smem, st>>>(geo, pl, args, tab);
+  // both kernels are programmatic dependents of the kernel before them in
+  // the stream (they wait for its writes with griddepcontrol.wait), so a
+  // launch's set-up overlaps the end of the previous kernel
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kNW * 32);
+  cfg.dynamicSmemBytes = plan.smem;
+  cfg.stream = st;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, ki.fn, geo, pl, args, tab);
   count_launch();
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   mma::MergeFn mf = nullptr;
   switch (geo.D * 8 + plan.GQp) {
@@ -119,9 +131,12 @@ cudaError_t launch_decode_mma(const Geometry &geo, const Planes &pl,
   }
   int64_t nw = (n_max + mma::kMergeU - 1) / mma::kMergeU;
   if (nw > mma::kMergeWarps) nw = mma::kMergeWarps;
-  mf<<<dim3(geo.B * geo.H_q, geo.D / 32), (unsigned)nw * 32, 0, st>>>(geo, args, tab);
+  cfg.gridDim = dim3(geo.B * geo.H_q, geo.D / 32);
+  cfg.blockDim = dim3((unsigned)nw * 32);
+  cfg.dynamicSmemBytes = 0;
+  e = cudaLaunchKernelEx(&cfg, mf, geo, args, tab);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace vqk

@@ -516,6 +516,11 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   constexpr int G = C::G, ROW = C::ROW, ROWQ = C::ROWQ;
   extern __shared__ __align__(128) unsigned char smem[];
 
+  // launched as a programmatic dependent of the stream's previous kernel
+  // (an append): wait until its writes are visible, then let the merge
+  // kernel, launched behind this one, be scheduled as CTAs retire
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int wg = blockIdx.x * kNW + warp;
@@ -1107,6 +1112,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 k_merge_mma(Geometry geo, MmaArgs args, MmaTable tab) {
   __shared__ float sm_m[kMergeWarps], sm_l[kMergeWarps];
   __shared__ float sm_o[kMergeWarps][32];
+  // programmatic dependent of the decode kernel: its partials are visible
+  // once this returns
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int b = blockIdx.x / geo.H_q, hq = blockIdx.x - b * geo.H_q;
   if (tab.nc[b] == 0) return;   // the launcher zeroed this output
   const int GQ = args.GQ;
