@@ -371,25 +371,37 @@ __device__ __forceinline__ int find_seq(const int32_t *prefix, int B,
   return lo;
 }
 
-// Position in the flattened chunk space, advanced one chunk at a time.
+// Position in the flattened chunk space, advanced one chunk at a time, with
+// the counts of its sequence cached (nc chunks per head, nq of them
+// quantized, Tq quantized tokens, nres residual tokens).
 struct Cursor {
   int b, h, k;
+  int nc, nq, Tq, nres;
+  __device__ __forceinline__ void load(const MmaTable &tab) {
+    nc = tab.nc[b]; nq = tab.nq[b]; Tq = tab.Tq[b]; nres = tab.nres[b];
+  }
   __device__ __forceinline__ void init(int c, const Geometry &geo,
                                        const MmaTable &tab) {
     b = find_seq(tab.bprefix, geo.B, c);
+    load(tab);
     const int local = c - tab.bprefix[b];
-    h = local / tab.nc[b];
-    k = local - h * tab.nc[b];
+    h = local / nc;
+    k = local - h * nc;
   }
   __device__ __forceinline__ void next(const Geometry &geo, const MmaTable &tab) {
-    if (++k == tab.nc[b]) {
+    if (++k == nc) {
       k = 0;
       if (++h == geo.H_kv) {
         h = 0;
         do { ++b; } while (b < geo.B && tab.nc[b] == 0);
+        if (b < geo.B) load(tab);
       }
     }
   }
+  // quantized chunk; residual window (a head's last chunk); otherwise one of
+  // the empty chunks that only weight the residual window in the split
+  __device__ __forceinline__ bool quant() const { return k < nq; }
+  __device__ __forceinline__ bool res() const { return k == nc - 1 && nres > 0; }
 };
 
 // The fp16 residual window of one head on the CUDA cores, 32 tokens at a
@@ -547,38 +559,37 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   // The key scale/zero rows are copied only where a score window starts or
   // the warp's range starts: every other chunk reuses the operand built
   // from an earlier stage.
+  // row index of token 0 of the producer's head in the code / value-meta
+  // planes, and of its group 0 in the key-meta planes (set per head)
+  size_t prow0 = 0, pgrp0 = 0;
+  auto set_prod_head = [&](const Cursor &cu) {
+    const size_t hd = (size_t)cu.b * geo.H_kv + cu.h;
+    prow0 = hd * geo.Tcap;
+    pgrp0 = hd * (geo.Tcap / G);
+  };
   auto issue = [&](const Cursor &cu, int s, int c) {
     if (c == args.fail_chunk) return;   // testing: a copy that never comes
-    const int Tq = tab.Tq[cu.b];
     const int t0 = cu.k * kC;
-    const int rem = Tq - t0;
+    const int rem = cu.Tq - t0;
     const int nvalid = rem < kC ? rem : kC;
     unsigned char *st = stage0 + s * C::S_BYTES;
-    const size_t hd = (size_t)cu.b * geo.H_kv + cu.h;
     const uint32_t b_codes = nvalid * ROW;
     const uint32_t b_vs = nvalid * NJ * 2;
     const bool with_ks = (t0 % C::WT) == 0 || c == lo_c;
     const int kg0 = ((t0 / G) / C::KG) * C::KG;
-    const int ngv = Tq / G - kg0;
+    const int ngv = cu.Tq / G - kg0;
     const uint32_t b_ks = with_ks ? (ngv < C::KG ? ngv : C::KG) * D * 2 : 0u;
     mbar_expect_tx(&bars[s], 2 * (b_codes + b_ks + b_vs));
-    const size_t row0 = hd * geo.Tcap + t0;
+    const size_t row0 = prow0 + t0;
     bulk_g2s(st + C::S_KC, pl.Kc + row0 * ROW, b_codes, &bars[s]);
     bulk_g2s(st + C::S_VC, pl.Vc + row0 * ROW, b_codes, &bars[s]);
     if (with_ks) {
-      const size_t kidx = (hd * (geo.Tcap / G) + kg0) * D;
+      const size_t kidx = (pgrp0 + kg0) * D;
       bulk_g2s(st + C::S_KS, pl.Ks + kidx, b_ks, &bars[s]);
       bulk_g2s(st + C::S_KZ, pl.Kz + kidx, b_ks, &bars[s]);
     }
     bulk_g2s(st + C::S_VS, pl.Vs + row0 * NJ, b_vs, &bars[s]);
     bulk_g2s(st + C::S_VZ, pl.Vz + row0 * NJ, b_vs, &bars[s]);
-  };
-  auto is_quant = [&](const Cursor &cu) { return cu.k < tab.nq[cu.b]; };
-  // a head's last chunk is its residual window (when it has one); the
-  // chunks between the quantized ones and it are empty: they only weight
-  // the residual window's cost in the equal split of the chunk space
-  auto is_res = [&](const Cursor &cu) {
-    return cu.k == tab.nc[cu.b] - 1 && tab.nres[cu.b] > 0;
   };
   // lane 0, when the producer cursor reaches a residual chunk: pull the
   // head's residual ring into L2, ST chunks before the window is read
@@ -588,18 +599,23 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     prefetch_l2(pl.Kr + hd * geo.Rcap * D, bytes);
     prefetch_l2(pl.Vr + hd * geo.Rcap * D, bytes);
   };
+  // the producer's step for the chunk at pc (copies, or the L2 prefetch of
+  // a residual window), into stage s
+  auto produce = [&](const Cursor &cu, int s, int c) {
+    if (cu.k == 0 || c == lo_c) set_prod_head(cu);
+    if (cu.quant())
+      issue(cu, s, c);
+    else if (cu.res())
+      prefetch_res(cu);
+  };
 
   Cursor pc;  // producer cursor: the next chunk to issue
   pc.init(lo_c, geo, tab);
   uint32_t phase = 0;    // bit s = parity to wait for on stage s
   uint32_t pending = 0;  // bit s = copies in flight into stage s
   for (int i = 0; i < ST && i < n_mine; ++i) {
-    if (is_quant(pc)) {
-      if (lane == 0) issue(pc, i, lo_c + i);
-      pending |= 1u << i;
-    } else if (lane == 0 && is_res(pc)) {
-      prefetch_res(pc);
-    }
+    if (lane == 0) produce(pc, i, lo_c + i);
+    if (pc.quant()) pending |= 1u << i;
     pc.next(geo, tab);
   }
   bool failed = false;
@@ -732,13 +748,12 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     unscale_t = exp2i(24 - __shfl_sync(kFull, k, 8 * tig));
   };
 
-  auto residual = [&](int b, int hd, int s) {
+  auto residual = [&](const Cursor &cu, int hd, int s) {
     float *ores = reinterpret_cast<float *>(stage0 + s * C::S_BYTES);
-    residual_window<D, GQP>(pl.Kr, pl.Vr, (size_t)hd * geo.Rcap, tab.Tq[b],
-                            tab.nres[b], geo.Rcap, GQ, qn, ores, ores + GQP * D,
-                            lane);
+    residual_window<D, GQP>(pl.Kr, pl.Vr, (size_t)hd * geo.Rcap, cu.Tq, cu.nres,
+                            geo.Rcap, GQ, qn, ores, ores + GQP * D, lane);
     res_o = ores;
-    has_res = tab.nres[b] > 0;
+    has_res = cu.nres > 0;
   };
 
   // write this warp's partial of head hd (slot wg + hd); k_merge_mma, run
@@ -787,10 +802,14 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     }
   };
 
-  // ---- one staged chunk: scores, softmax update, values.  FULL: all four
-  // m16 tiles hold tokens (every chunk but a head's last quantized one). ----
+  // ---- one staged chunk, in two halves of two m16 tiles (32 tokens):
+  // scores(0), softmax(0), then scores(1) and values(0) in one straight-line
+  // block (independent work the scheduler interleaves), softmax(1),
+  // values(1).  FULL: all four tiles hold tokens (every chunk but a head's
+  // last quantized one). ----
   auto chunk = [&](auto full_tag, const unsigned char *st, int t0, int nmt) {
     constexpr bool FULL = decltype(full_tag)::value;
+    constexpr int MPW = C::MPW;
     const uint4 *kc = reinterpret_cast<const uint4 *>(st + C::S_KC);
     const uint4 *vc = reinterpret_cast<const uint4 *>(st + C::S_VC);
     const __half *Ks = reinterpret_cast<const __half *>(st + C::S_KS);
@@ -799,289 +818,316 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     const __half *Vz = reinterpret_cast<const __half *>(st + C::S_VZ);
     const int G0 = t0 / G;                        // first key group
     const int kg0 = (G0 / C::KG) * C::KG;
-
-    // ---- scores, window by window; the tiles of a window interleave ----
     float sv[4][2];
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt) sv[mt][0] = sv[mt][1] = -INFINITY;
+    float p[4][2];
+
+    // score MMAs of tiles T0 .. T0+NT-1 (one window) with the current B
+    auto score_tiles = [&](auto t0_tag, auto nt_tag, float (&acc)[2][4]) {
+      constexpr int T0 = decltype(t0_tag)::value, NT = decltype(nt_tag)::value;
+      if constexpr (L::FRAG) {
+        // fragment order: lane group tig's D/64 words of a token row are
+        // contiguous; word hw holds K-steps 4hw ... 4hw+3
+        constexpr int NH = D / 64;
+        using RowW = std::conditional_t<NH == 2, uint2, uint32_t>;
+        RowW r0[NT], r1[NT];
 #pragma unroll
-    for (int win = 0; win < C::NWIN; ++win) {
-      constexpr int MPW = C::MPW;
-      const int mt0 = win * MPW;
-      if (FULL || mt0 < nmt) {
-        const int gw0 = ((G0 + (16 * mt0) / G) / WG) * WG;
-        if (gw0 != cur_w) {
-          build_score_b(Ks, Kz, gw0, kg0);
-          cur_w = gw0;
+        for (int m = 0; m < NT; ++m) {
+          const unsigned char *row = st + C::S_KC + (16 * (T0 + m) + gid) * ROW + 4 * NH * tig;
+          r0[m] = *reinterpret_cast<const RowW *>(row);
+          r1[m] = *reinterpret_cast<const RowW *>(row + 8 * ROW);
         }
-        float acc[MPW][4];
 #pragma unroll
-        for (int m = 0; m < MPW; ++m)
+        for (int hw = 0; hw < NH; ++hw) {
+          uint32_t w0[NT], w1[NT], s0[NT], s1[NT];
+#pragma unroll
+          for (int m = 0; m < NT; ++m) {
+            if constexpr (NH == 2) {
+              w0[m] = hw ? r0[m].y : r0[m].x;
+              w1[m] = hw ? r1[m].y : r1[m].x;
+            } else {
+              w0[m] = r0[m];
+              w1[m] = r1[m];
+            }
+            s0[m] = w0[m] >> 6;
+            s1[m] = w1[m] >> 6;
+          }
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const int ks = 4 * hw + kk;
+#pragma unroll
+            for (int m = 0; m < NT; ++m) {
+              if (FULL || T0 + m < nmt) {
+                mma16816(acc[m], L::field(w0[m], s0[m], 2 * kk),
+                         L::field(w1[m], s1[m], 2 * kk),
+                         L::field(w0[m], s0[m], 2 * kk + 1),
+                         L::field(w1[m], s1[m], 2 * kk + 1), Bs[ks][0], Bs[ks][1]);
+              }
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < KS / L::WPQ; ++q) {
+          uint4 r0[NT], r1[NT];
+#pragma unroll
+          for (int m = 0; m < NT; ++m) {
+            const uint4 *row = kc + (16 * (T0 + m) + gid) * ROWQ;
+            r0[m] = row[q];
+            r1[m] = row[8 * ROWQ + q];
+          }
+#pragma unroll
+          for (int kq = 0; kq < L::WPQ; ++kq) {
+            const int ks = q * L::WPQ + kq;
+#pragma unroll
+            for (int m = 0; m < NT; ++m) {
+              if (FULL || T0 + m < nmt) {
+                uint32_t a0, a1, a2, a3;
+                L::score_a(r0[m], ks, s_sel, a0, a2);
+                L::score_a(r1[m], ks, s_sel, a1, a3);
+                mma16816(acc[m], a0, a1, a2, a3, Bs[ks][0], Bs[ks][1]);
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < NT; ++m) {
+        const int mt = T0 + m;
+        if ((FULL || mt < nmt) && ((G0 + (16 * mt) / G) % WG) == gw_s) {
+          sv[mt][0] = fmaf(acc[m][0] + acc[m][1], unscale_t, beta_t);
+          sv[mt][1] = fmaf(acc[m][2] + acc[m][3], unscale_t, beta_t);
+        }
+      }
+    };
+
+    // scores of half H (tiles 2H, 2H+1), window by window.  A window that
+    // spans the chunk (NWIN == 1) may continue from the previous chunk; a
+    // smaller one is always new.
+    auto scores_half = [&](auto h_tag) {
+      constexpr int H = decltype(h_tag)::value;
+      constexpr int WA = (2 * H) / MPW, WB = (2 * H + 1) / MPW;
+#pragma unroll
+      for (int win = WA; win <= WB; ++win) {
+        const int ta = win * MPW > 2 * H ? win * MPW : 2 * H;   // first tile
+        if (!FULL && ta >= nmt) continue;
+        if (C::NWIN > 1 || H == 0) {
+          const int gw0 = ((G0 + (16 * win * MPW) / G) / WG) * WG;
+          if (C::NWIN > 1 || gw0 != cur_w) {
+            build_score_b(Ks, Kz, gw0, kg0);
+            cur_w = gw0;
+          }
+        }
+        float acc[2][4];
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
 #pragma unroll
           for (int r = 0; r < 4; ++r) acc[m][r] = 0.f;
-        if constexpr (L::FRAG) {
-          // fragment order: lane group tig's D/64 words of a token row are
-          // contiguous; word hw holds K-steps 4hw ... 4hw+3
-          constexpr int NH = D / 64;
-          using RowW = std::conditional_t<NH == 2, uint2, uint32_t>;
-          RowW r0[MPW], r1[MPW];
-#pragma unroll
-          for (int m = 0; m < MPW; ++m) {
-            const unsigned char *row = st + C::S_KC + (16 * (mt0 + m) + gid) * ROW + 4 * NH * tig;
-            r0[m] = *reinterpret_cast<const RowW *>(row);
-            r1[m] = *reinterpret_cast<const RowW *>(row + 8 * ROW);
-          }
-#pragma unroll
-          for (int hw = 0; hw < NH; ++hw) {
-            uint32_t w0[MPW], w1[MPW], s0[MPW], s1[MPW];
-#pragma unroll
-            for (int m = 0; m < MPW; ++m) {
-              if constexpr (NH == 2) {
-                w0[m] = hw ? r0[m].y : r0[m].x;
-                w1[m] = hw ? r1[m].y : r1[m].x;
-              } else {
-                w0[m] = r0[m];
-                w1[m] = r1[m];
-              }
-              s0[m] = w0[m] >> 6;
-              s1[m] = w1[m] >> 6;
-            }
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const int ks = 4 * hw + kk;
-#pragma unroll
-              for (int m = 0; m < MPW; ++m) {
-                if (FULL || mt0 + m < nmt) {
-                  mma16816(acc[m], L::field(w0[m], s0[m], 2 * kk),
-                           L::field(w1[m], s1[m], 2 * kk),
-                           L::field(w0[m], s0[m], 2 * kk + 1),
-                           L::field(w1[m], s1[m], 2 * kk + 1), Bs[ks][0], Bs[ks][1]);
-                }
-              }
-            }
-          }
+        if constexpr (MPW == 1) {
+          if (win == WA)
+            score_tiles(std::integral_constant<int, 2 * H>{}, std::integral_constant<int, 1>{}, acc);
+          else
+            score_tiles(std::integral_constant<int, 2 * H + 1>{}, std::integral_constant<int, 1>{}, acc);
         } else {
-#pragma unroll
-          for (int q = 0; q < KS / L::WPQ; ++q) {
-            uint4 r0[MPW], r1[MPW];
-#pragma unroll
-            for (int m = 0; m < MPW; ++m) {
-              const uint4 *row = kc + (16 * (mt0 + m) + gid) * ROWQ;
-              r0[m] = row[q];
-              r1[m] = row[8 * ROWQ + q];
-            }
-#pragma unroll
-            for (int kq = 0; kq < L::WPQ; ++kq) {
-              const int ks = q * L::WPQ + kq;
-#pragma unroll
-              for (int m = 0; m < MPW; ++m) {
-                if (FULL || mt0 + m < nmt) {
-                  uint32_t a0, a1, a2, a3;
-                  L::score_a(r0[m], ks, s_sel, a0, a2);
-                  L::score_a(r1[m], ks, s_sel, a1, a3);
-                  mma16816(acc[m], a0, a1, a2, a3, Bs[ks][0], Bs[ks][1]);
-                }
-              }
-            }
-          }
-        }
-#pragma unroll
-        for (int m = 0; m < MPW; ++m) {
-          const int mt = mt0 + m;
-          if ((FULL || mt < nmt) && ((G0 + (16 * mt) / G) % WG) == gw_s) {
-            sv[mt][0] = fmaf(acc[m][0] + acc[m][1], unscale_t, beta_t);
-            sv[mt][1] = fmaf(acc[m][2] + acc[m][3], unscale_t, beta_t);
-          }
+          score_tiles(std::integral_constant<int, 2 * H>{}, std::integral_constant<int, 2>{}, acc);
         }
       }
-    }
+    };
 
-    // ---- online softmax update for this lane's head.  The head maximum
-    // is reduced only when some lane holds a score above the running
-    // maximum (rare once a few chunks are in); otherwise m and the
-    // accumulators stay as they are. ----
-    float lmax = -INFINITY;
+    // online softmax update with the scores of half H; the head maximum is
+    // reduced only when some lane holds a score above the running maximum
+    auto softmax_half = [&](auto h_tag) {
+      constexpr int H = decltype(h_tag)::value;
+      const float lmax = fmaxf(fmaxf(sv[2 * H][0], sv[2 * H][1]),
+                               fmaxf(sv[2 * H + 1][0], sv[2 * H + 1][1]));
+      float alpha = 1.f;
+      if (__any_sync(kFull, lmax > m_run)) {
+        const float m_new = fmaxf(m_run, head_reduce<GQP>(lmax, MaxOp()));
+        alpha = m_run == -INFINITY ? 0.f : exp2_neg(m_run - m_new);
+        m_run = m_new;
+        const float2 a2 = f2(alpha, alpha);
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt) lmax = fmaxf(lmax, fmaxf(sv[mt][0], sv[mt][1]));
-    float alpha = 1.f;
-    if (__any_sync(kFull, lmax > m_run)) {
-      const float m_new = fmaxf(m_run, head_reduce<GQP>(lmax, MaxOp()));
-      alpha = m_run == -INFINITY ? 0.f : exp2_neg(m_run - m_new);
-      m_run = m_new;
-      const float2 a2 = f2(alpha, alpha);
+        for (int mv = 0; mv < KS; ++mv) {
+          const float2 o01 = __fmul2_rn(f2(O[mv][0], O[mv][1]), a2);
+          const float2 o23 = __fmul2_rn(f2(O[mv][2], O[mv][3]), a2);
+          O[mv][0] = o01.x; O[mv][1] = o01.y; O[mv][2] = o23.x; O[mv][3] = o23.y;
+        }
 #pragma unroll
-      for (int mv = 0; mv < KS; ++mv) {
-        const float2 o01 = __fmul2_rn(f2(O[mv][0], O[mv][1]), a2);
-        const float2 o23 = __fmul2_rn(f2(O[mv][2], O[mv][3]), a2);
-        O[mv][0] = o01.x; O[mv][1] = o01.y; O[mv][2] = o23.x; O[mv][3] = o23.y;
+        for (int j = 0; j < NJ; ++j) Z[j] *= alpha;
       }
 #pragma unroll
-      for (int j = 0; j < NJ; ++j) Z[j] *= alpha;
-    }
-    float p[4][2];
+      for (int mt = 2 * H; mt < 2 * H + 2; ++mt)
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-      for (int r = 0; r < 2; ++r) p[mt][r] = exp2_neg(sv[mt][r] - m_run);   // -inf -> 0
-    const float psum = ((p[0][0] + p[0][1]) + (p[1][0] + p[1][1])) +
-                       ((p[2][0] + p[2][1]) + (p[3][0] + p[3][1]));
-    l_run = fmaf(l_run, alpha, psum);
+        for (int r = 0; r < 2; ++r) p[mt][r] = exp2_neg(sv[mt][r] - m_run);   // -inf -> 0
+      const float psum = (p[2 * H][0] + p[2 * H][1]) + (p[2 * H + 1][0] + p[2 * H + 1][1]);
+      l_run = fmaf(l_run, alpha, psum);
+    };
 
-    // ---- values: K-step kt = tokens 16kt ... 16kt+15 of the chunk.  K
+    // ---- values of K-step kt = tokens 16kt ... 16kt+15 of the chunk.  K
     // slots (2tig, 2tig+1, 2tig+8, 2tig+9) <-> tokens (tig, tig+4, tig+8,
     // tig+12): the four rows a lane group reads hit distinct banks. ----
+    auto values_kt = [&](auto kt_tag) {
+      constexpr int kt = decltype(kt_tag)::value;
+      if (!FULL && kt >= nmt) return;
+      // zero-point term in the score layout (tokens gid, gid+8)
 #pragma unroll
-    for (int kt = 0; kt < 4; ++kt) {
-      if (FULL || kt < nmt) {
-        // zero-point term in the score layout (tokens gid, gid+8)
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          float vz[NJ];
-          load_halves<NJ>(Vz + (16 * kt + gid + 8 * r) * NJ, vz);
-          if constexpr (NJ == 1) {
-            Z[0] = fmaf(p[kt][r], vz[0], Z[0]);
-          } else {
-#pragma unroll
-            for (int j = 0; j < NJ; j += 2) {
-              const float2 z = __ffma2_rn(f2(p[kt][r], p[kt][r]), f2(vz[j], vz[j + 1]),
-                                          f2(Z[j], Z[j + 1]));
-              Z[j] = z.x; Z[j + 1] = z.y;
-            }
-          }
-        }
-        // p of head h_b for tokens tig, tig+4, tig+8, tig+12
-        const int src = ((G0 + (16 * kt) / G) % WG) * GQP + h_b;
-        const float p0 = __shfl_sync(kFull, p[kt][0], 4 * tig + src);
-        const float p1 = __shfl_sync(kFull, p[kt][0], 4 * tig + 16 + src);
-        const float p2 = __shfl_sync(kFull, p[kt][1], 4 * tig + src);
-        const float p3 = __shfl_sync(kFull, p[kt][1], 4 * tig + 16 + src);
-        const int ta = 16 * kt + tig;
-        // s_V of the four tokens: whole rows when every block needs a
-        // different group, single values otherwise
-        float vs[4][C::NVB];
-        if constexpr (C::NVB == NJ && NJ >= 2) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            float row[NJ];
-            load_halves<NJ>(Vs + (ta + 4 * u) * NJ, row);
-#pragma unroll
-            for (int vb = 0; vb < C::NVB; ++vb) vs[u][vb] = row[(4 * vb + pair_b) / GQP];
-          }
+      for (int r = 0; r < 2; ++r) {
+        float vz[NJ];
+        load_halves<NJ>(Vz + (16 * kt + gid + 8 * r) * NJ, vz);
+        if constexpr (NJ == 1) {
+          Z[0] = fmaf(p[kt][r], vz[0], Z[0]);
         } else {
 #pragma unroll
-          for (int vb = 0; vb < C::NVB; ++vb) {
-            const int jb = (4 * vb + pair_b) / GQP;
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              vs[u][vb] = jb < NJ ? __half2float(Vs[(ta + 4 * u) * NJ + jb]) : 0.f;
-          }
-        }
-        uint32_t bv[C::NVB][2];
-#pragma unroll
-        for (int vb = 0; vb < C::NVB; ++vb) {
-          const float2 w01 = hilo2(__fmul2_rn(f2(p0, p1), f2(vs[0][vb], vs[1][vb])), hls);
-          const float2 w23 = hilo2(__fmul2_rn(f2(p2, p3), f2(vs[2][vb], vs[3][vb])), hls);
-          bv[vb][0] = pack_half2(w01.x, w01.y);
-          bv[vb][1] = pack_half2(w23.x, w23.y);
-        }
-        if constexpr (L::FRAG) {
-          // fragment order: pair (ta, ta+4) is pair tig of block kt, pair
-          // (ta+8, ta+12) pair 4+tig; lane gid's D/64 words of a pair are
-          // contiguous, word hw covering tiles 4hw ... 4hw+3
-          constexpr int NV = D / 64;
-          using PairW = std::conditional_t<NV == 2, uint2, uint32_t>;
-          const unsigned char *blk = st + C::S_VC + kt * 16 * ROW;
-          const PairW pa = *reinterpret_cast<const PairW *>(blk + (8 * tig + gid) * 4 * NV);
-          const PairW pb = *reinterpret_cast<const PairW *>(blk + (8 * (4 + tig) + gid) * 4 * NV);
-#pragma unroll
-          for (int hw = 0; hw < NV; ++hw) {
-            uint32_t wa, wb;
-            if constexpr (NV == 2) {
-              wa = hw ? pa.y : pa.x;
-              wb = hw ? pb.y : pb.x;
-            } else {
-              wa = pa;
-              wb = pb;
-            }
-            const uint32_t sa = wa >> 6, sb = wb >> 6;
-#pragma unroll
-            for (int mm = 0; mm < 4; ++mm) {
-              const int mv = 4 * hw + mm;
-              const int vb = (((16 * mv) / G) * GQP) >> 2;
-              mma16816(O[mv], L::field(wa, sa, 2 * mm), L::field(wa, sa, 2 * mm + 1),
-                       L::field(wb, sb, 2 * mm), L::field(wb, sb, 2 * mm + 1),
-                       bv[vb][0], bv[vb][1]);
-            }
-          }
-        } else {
-          // m16 channel tiles, VTPQ per uint4 of the token rows
-#pragma unroll
-          for (int q = 0; q < KS / L::VTPQ; ++q) {
-            const uint4 xa = vc[ta * ROWQ + q];
-            const uint4 xb = vc[(ta + 4) * ROWQ + q];
-            const uint4 xc = vc[(ta + 8) * ROWQ + q];
-            const uint4 xd = vc[(ta + 12) * ROWQ + q];
-#pragma unroll
-            for (int u = 0; u < L::VTPQ; ++u) {
-              const int mv = q * L::VTPQ + u;
-              const int vb = (((16 * mv) / G) * GQP) >> 2;
-              uint32_t a0, a1, a2, a3;
-              L::value_a(__byte_perm(L::vword(xa, u, gid), L::vword(xb, u, gid), v_sel),
-                         gid, a0, a1);
-              L::value_a(__byte_perm(L::vword(xc, u, gid), L::vword(xd, u, gid), v_sel),
-                         gid, a2, a3);
-              mma16816(O[mv], a0, a1, a2, a3, bv[vb][0], bv[vb][1]);
-            }
+          for (int j = 0; j < NJ; j += 2) {
+            const float2 z = __ffma2_rn(f2(p[kt][r], p[kt][r]), f2(vz[j], vz[j + 1]),
+                                        f2(Z[j], Z[j + 1]));
+            Z[j] = z.x; Z[j + 1] = z.y;
           }
         }
       }
-    }
+      // p of head h_b for tokens tig, tig+4, tig+8, tig+12
+      const int src = ((G0 + (16 * kt) / G) % WG) * GQP + h_b;
+      const float p0 = __shfl_sync(kFull, p[kt][0], 4 * tig + src);
+      const float p1 = __shfl_sync(kFull, p[kt][0], 4 * tig + 16 + src);
+      const float p2 = __shfl_sync(kFull, p[kt][1], 4 * tig + src);
+      const float p3 = __shfl_sync(kFull, p[kt][1], 4 * tig + 16 + src);
+      const int ta = 16 * kt + tig;
+      // s_V of the four tokens: whole rows when every block needs a
+      // different group, single values otherwise
+      float vs[4][C::NVB];
+      if constexpr (C::NVB == NJ && NJ >= 2) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float row[NJ];
+          load_halves<NJ>(Vs + (ta + 4 * u) * NJ, row);
+#pragma unroll
+          for (int vb = 0; vb < C::NVB; ++vb) vs[u][vb] = row[(4 * vb + pair_b) / GQP];
+        }
+      } else {
+#pragma unroll
+        for (int vb = 0; vb < C::NVB; ++vb) {
+          const int jb = (4 * vb + pair_b) / GQP;
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            vs[u][vb] = jb < NJ ? __half2float(Vs[(ta + 4 * u) * NJ + jb]) : 0.f;
+        }
+      }
+      uint32_t bv[C::NVB][2];
+#pragma unroll
+      for (int vb = 0; vb < C::NVB; ++vb) {
+        const float2 w01 = hilo2(__fmul2_rn(f2(p0, p1), f2(vs[0][vb], vs[1][vb])), hls);
+        const float2 w23 = hilo2(__fmul2_rn(f2(p2, p3), f2(vs[2][vb], vs[3][vb])), hls);
+        bv[vb][0] = pack_half2(w01.x, w01.y);
+        bv[vb][1] = pack_half2(w23.x, w23.y);
+      }
+      if constexpr (L::FRAG) {
+        // fragment order: pair (ta, ta+4) is pair tig of block kt, pair
+        // (ta+8, ta+12) pair 4+tig; lane gid's D/64 words of a pair are
+        // contiguous, word hw covering tiles 4hw ... 4hw+3
+        constexpr int NV = D / 64;
+        using PairW = std::conditional_t<NV == 2, uint2, uint32_t>;
+        const unsigned char *blk = st + C::S_VC + kt * 16 * ROW;
+        const PairW pa = *reinterpret_cast<const PairW *>(blk + (8 * tig + gid) * 4 * NV);
+        const PairW pb = *reinterpret_cast<const PairW *>(blk + (8 * (4 + tig) + gid) * 4 * NV);
+#pragma unroll
+        for (int hw = 0; hw < NV; ++hw) {
+          uint32_t wa, wb;
+          if constexpr (NV == 2) {
+            wa = hw ? pa.y : pa.x;
+            wb = hw ? pb.y : pb.x;
+          } else {
+            wa = pa;
+            wb = pb;
+          }
+          const uint32_t sa = wa >> 6, sb = wb >> 6;
+#pragma unroll
+          for (int mm = 0; mm < 4; ++mm) {
+            const int mv = 4 * hw + mm;
+            const int vb = (((16 * mv) / G) * GQP) >> 2;
+            mma16816(O[mv], L::field(wa, sa, 2 * mm), L::field(wa, sa, 2 * mm + 1),
+                     L::field(wb, sb, 2 * mm), L::field(wb, sb, 2 * mm + 1),
+                     bv[vb][0], bv[vb][1]);
+          }
+        }
+      } else {
+        // m16 channel tiles, VTPQ per uint4 of the token rows
+#pragma unroll
+        for (int q = 0; q < KS / L::VTPQ; ++q) {
+          const uint4 xa = vc[ta * ROWQ + q];
+          const uint4 xb = vc[(ta + 4) * ROWQ + q];
+          const uint4 xc = vc[(ta + 8) * ROWQ + q];
+          const uint4 xd = vc[(ta + 12) * ROWQ + q];
+#pragma unroll
+          for (int u = 0; u < L::VTPQ; ++u) {
+            const int mv = q * L::VTPQ + u;
+            const int vb = (((16 * mv) / G) * GQP) >> 2;
+            uint32_t a0, a1, a2, a3;
+            L::value_a(__byte_perm(L::vword(xa, u, gid), L::vword(xb, u, gid), v_sel),
+                       gid, a0, a1);
+            L::value_a(__byte_perm(L::vword(xc, u, gid), L::vword(xd, u, gid), v_sel),
+                       gid, a2, a3);
+            mma16816(O[mv], a0, a1, a2, a3, bv[vb][0], bv[vb][1]);
+          }
+        }
+      }
+    };
+
+    using I0 = std::integral_constant<int, 0>;
+    using I1 = std::integral_constant<int, 1>;
+    using I2 = std::integral_constant<int, 2>;
+    using I3 = std::integral_constant<int, 3>;
+    scores_half(I0{});
+    softmax_half(I0{});
+    scores_half(I1{});
+    values_kt(I0{});
+    values_kt(I1{});
+    softmax_half(I1{});
+    values_kt(I2{});
+    values_kt(I3{});
   };
 
   // ---- main loop over my chunks ---------------------------------------------
   Cursor cu;
   cu.init(lo_c, geo, tab);
   int cur_hd = -1;
+  int s = 0;   // stage of chunk i (= i mod ST)
   for (int i = 0; i < n_mine; ++i) {
-    const int s = i % ST;
     const int hd = cu.b * geo.H_kv + cu.h;
     if (hd != cur_hd) {
       reset_state();
       load_q(cu.b, cu.h);
       cur_hd = hd;
     }
-    if (is_res(cu)) {
-      residual(cu.b, hd, s);
-    } else if (is_quant(cu)) {
+    if (cu.res()) {
+      residual(cu, hd, s);
+    } else if (cu.quant()) {
       const bool ok = __all_sync(kFull, mbar_wait(&bars[s], (phase >> s) & 1u));
       if (!ok) { failed = true; break; }
       phase ^= 1u << s;
       pending &= ~(1u << s);
       const unsigned char *st = stage0 + s * C::S_BYTES;
       const int t0 = cu.k * kC;
-      const int rem = tab.Tq[cu.b] - t0;
+      const int rem = cu.Tq - t0;
       if (rem >= kC) {
         chunk(std::true_type{}, st, t0, 4);
       } else {
         chunk(std::false_type{}, st, t0, rem >> 4);
       }
     }
-    const bool head_ends = cu.k == tab.nc[cu.b] - 1 || i == n_mine - 1;
+    const bool head_ends = cu.k == cu.nc - 1 || i == n_mine - 1;
     if (head_ends) flush(hd);
     __syncwarp();
     if (i + ST < n_mine) {
-      if (is_quant(pc)) {
-        if (lane == 0) {
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          issue(pc, s, lo_c + i + ST);
-        }
-        pending |= 1u << s;
-      } else if (lane == 0 && is_res(pc)) {
-        prefetch_res(pc);
+      if (lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        produce(pc, s, lo_c + i + ST);
       }
+      if (pc.quant()) pending |= 1u << s;
       pc.next(geo, tab);
     }
     cu.next(geo, tab);
+    if (++s == ST) s = 0;
   }
 
   if (failed) {

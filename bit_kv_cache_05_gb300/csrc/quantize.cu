@@ -29,6 +29,31 @@ __device__ __forceinline__ int find_seq(const int32_t *prefix, int B,
   return lo;
 }
 
+// Kernels here are launched as programmatic dependents of the stream's
+// previous kernel: wait for its writes, then let the next kernel be
+// scheduled as this one's CTAs retire.
+__device__ __forceinline__ void pdl_wait_and_release() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+}
+
+// launch with programmatic stream serialization
+template <typename... P, typename... A>
+cudaError_t launch_pdl(void (*fn)(P...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, A... args) {
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, args...);
+}
+
 __device__ __forceinline__ uint32_t quant_code(float x, float mn, float scale,
                                                int levels) {
   if (scale == 0.0f) return 0u;
@@ -154,6 +179,7 @@ template <int BITS>
 __global__ void __launch_bounds__(kMaxD)
 k_flush(Geometry geo, Planes pl, const __half *__restrict__ Kin,
         const __half *__restrict__ Vin, int64_t in_stride, FlushTable tab) {
+  pdl_wait_and_release();
   constexpr int levels = (1 << BITS) - 1;
   extern __shared__ __align__(16) unsigned char fsm[];
   const int D = geo.D, g = geo.g, H = geo.H_kv;
@@ -231,6 +257,7 @@ __global__ void __launch_bounds__(kThreads)
 k_tail(Geometry geo, Planes pl, const __half *__restrict__ Kin,
        const __half *__restrict__ Vin, int64_t in_stride, TailTable tab,
        int total) {
+  pdl_wait_and_release();
   const int D = geo.D;
   const int cpr = D / 8;                       // 16-byte chunks per row
   const int rows_per_block = kThreads / cpr;
@@ -297,13 +324,14 @@ cudaError_t launch_flush(const Geometry &geo, const Planes &pl,
     if (e != cudaSuccess) return e;
     opted[geo.bits] = true;
   }
+  cudaError_t e = cudaSuccess;
   switch (geo.bits) {
-    case 2: k_flush<2><<<grid, geo.D, smem, st>>>(geo, pl, Kin, Vin, in_stride, tab); break;
-    case 4: k_flush<4><<<grid, geo.D, smem, st>>>(geo, pl, Kin, Vin, in_stride, tab); break;
-    case 8: k_flush<8><<<grid, geo.D, smem, st>>>(geo, pl, Kin, Vin, in_stride, tab); break;
+    case 2: e = launch_pdl(k_flush<2>, grid, dim3(geo.D), smem, st, geo, pl, Kin, Vin, in_stride, tab); break;
+    case 4: e = launch_pdl(k_flush<4>, grid, dim3(geo.D), smem, st, geo, pl, Kin, Vin, in_stride, tab); break;
+    case 8: e = launch_pdl(k_flush<8>, grid, dim3(geo.D), smem, st, geo, pl, Kin, Vin, in_stride, tab); break;
   }
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_tail(const Geometry &geo, const Planes &pl,
@@ -313,10 +341,10 @@ cudaError_t launch_tail(const Geometry &geo, const Planes &pl,
   if (total_tokens <= 0) return cudaSuccess;
   const int rows_per_block = kThreads / (geo.D / 8);
   dim3 grid((total_tokens + rows_per_block - 1) / rows_per_block, geo.H_kv);
-  k_tail<<<grid, kThreads, 0, st>>>(geo, pl, Kin, Vin, in_stride, tab,
-                                    total_tokens);
+  const cudaError_t e = launch_pdl(k_tail, grid, dim3(kThreads), 0, st, geo, pl,
+                                  Kin, Vin, in_stride, tab, total_tokens);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 // kLayoutFrag2 plane -> packed order: one thread per packed 32-bit word
