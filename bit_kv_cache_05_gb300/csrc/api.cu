@@ -332,7 +332,7 @@ int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
       tab.Tq[b] = c->Tq[b];
       tab.nres[b] = c->nres[b];
       tab.nq[b] = (c->Tq[b] + c->plan.chunk - 1) / c->plan.chunk;
-      tab.nc[b] = tab.nq[b] + mma_residual_weight(c->nres[b]);
+      tab.nc[b] = tab.nq[b];
       tab.bprefix[b + 1] = tab.bprefix[b] + p.H_kv * tab.nc[b];
     }
     MmaArgs args;

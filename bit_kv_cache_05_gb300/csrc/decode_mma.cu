@@ -75,22 +75,14 @@ cudaError_t launch_decode_mma(const Geometry &geo, const Planes &pl,
   args.GQp = plan.GQp;
   args.KG = plan.KG;
   args.ST = plan.ST;
-  // sequences without tokens get an all-zero output (the kernel never
-  // visits them)
+  // sequences without any token get an all-zero output (no kernel writes it)
   for (int b = 0; b < geo.B; ++b) {
-    if (tab.nc[b] == 0) {
+    if (tab.nq[b] == 0 && tab.nres[b] == 0) {
       cudaError_t e = cudaMemsetAsync(args.out + (size_t)b * geo.H_q * geo.D, 0,
                                       sizeof(float) * geo.H_q * geo.D, st);
       if (e != cudaSuccess) return e;
     }
   }
-  if (args.N <= 0) return cudaSuccess;
-  mma::KernelInfo ki;
-  if (!pick(geo, plan.GQp, &ki)) return cudaErrorInvalidValue;
-  int64_t W = plan.warps_max;
-  if (W > args.N) W = args.N;
-  args.W = (int)W;
-  const int grid = (int)((W + kNW - 1) / kNW);
   // both kernels are programmatic dependents of the kernel before them in
   // the stream (they wait for its writes with griddepcontrol.wait), so a
   // launch's set-up overlaps the end of the previous kernel
@@ -98,15 +90,26 @@ cudaError_t launch_decode_mma(const Geometry &geo, const Planes &pl,
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kNW * 32);
-  cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = st;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, ki.fn, geo, pl, args, tab);
-  count_launch();
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  int64_t W = 1;
+  if (args.N > 0) {
+    mma::KernelInfo ki;
+    if (!pick(geo, plan.GQp, &ki)) return cudaErrorInvalidValue;
+    W = plan.warps_max;
+    if (W > args.N) W = args.N;
+    args.W = (int)W;
+    cfg.gridDim = dim3((unsigned)((W + kNW - 1) / kNW));
+    cfg.blockDim = dim3(kNW * 32);
+    cfg.dynamicSmemBytes = plan.smem;
+    e = cudaLaunchKernelEx(&cfg, ki.fn, geo, pl, args, tab);
+    count_launch();
+    if (e != cudaSuccess) return e;
+  } else {
+    args.W = 1;
+  }
   mma::MergeFn mf = nullptr;
   switch (geo.D * 8 + plan.GQp) {
     case 64 * 8 + 1: mf = mma::merge_fn<64, 1>(); break;
@@ -117,24 +120,35 @@ cudaError_t launch_decode_mma(const Geometry &geo, const Planes &pl,
     case 128 * 8 + 4: mf = mma::merge_fn<128, 4>(); break;
     default: return cudaErrorInvalidValue;
   }
-  // merge warps per CTA: enough for the largest partial count of a head to
-  // be read in one round
-  int64_t n_max = 1;
+  // merge warps per CTA: per query head enough for the largest partial
+  // count of a head, and overall enough for the longest residual window, to
+  // be read in one round; a multiple of the query heads per kv head
+  const int GQ = plan.GQ;
+  int64_t per = 1, nr = 1;
+  bool any = false;
   for (int b = 0; b < geo.B; ++b) {
-    if (tab.nc[b] == 0) continue;
+    if (tab.nq[b] == 0 && tab.nres[b] == 0) continue;
+    any = true;
+    const int64_t wr = (tab.nres[b] + mma::kMergeRT - 1) / mma::kMergeRT;
+    if (wr > nr) nr = wr;
+    if (tab.nq[b] == 0) continue;
     for (int h = 0; h < geo.H_kv; ++h) {
       const int64_t cs = tab.bprefix[b] + (int64_t)h * tab.nc[b];
       const int64_t ce = cs + tab.nc[b];
       const int64_t n = (ce * W - 1) / args.N - ((cs + 1) * W - 1) / args.N + 1;
-      if (n > n_max) n_max = n;
+      const int64_t wn = (n + mma::kMergeU - 1) / mma::kMergeU;
+      if (wn > per) per = wn;
     }
   }
-  int64_t nw = (n_max + mma::kMergeU - 1) / mma::kMergeU;
-  if (nw > mma::kMergeWarps) nw = mma::kMergeWarps;
-  cfg.gridDim = dim3(geo.B * geo.H_q, geo.D / 32);
+  if (!any) return cudaSuccess;
+  const int64_t per_max = mma::kMergeWarps / GQ;
+  if (per < (nr + GQ - 1) / GQ) per = (nr + GQ - 1) / GQ;
+  if (per > per_max) per = per_max;
+  const int64_t nw = per * GQ;
+  cfg.gridDim = dim3(geo.B * geo.H_kv, geo.D / 32);
   cfg.blockDim = dim3((unsigned)nw * 32);
   cfg.dynamicSmemBytes = 0;
-  e = cudaLaunchKernelEx(&cfg, mf, geo, args, tab);
+  e = cudaLaunchKernelEx(&cfg, mf, geo, pl, args, tab);
   count_launch();
   return e;
 }

@@ -27,13 +27,13 @@
 // group) pairs x (hi, lo); an m16 channel tile uses the block that holds its
 // value group.
 //
-// Work split: the (sequence, kv head, 64-token chunk) space, with each head's
-// fp16 residual window as one extra chunk, is cut into W equal contiguous
-// ranges, one per warp of a persistent grid.  A warp streams its chunks
-// through its own cp.async.bulk pipeline (one mbarrier per stage, bounded
-// waits), keeps (m, l, O) for the head it is in, and writes one partial per
-// head segment; the warp that finishes a head last (an atomic ticket per
-// head, no waiting) merges the head's partials with a log-sum-exp.
+// Work split: the (sequence, kv head, 64-token chunk) space of the quantized
+// tokens is cut into W equal contiguous ranges, one per warp of a persistent
+// grid.  A warp streams its chunks through its own cp.async.bulk pipeline
+// (one mbarrier per stage, bounded waits), keeps (m, l, O) for the head it
+// is in, and writes one partial per head segment.  k_merge_mma, launched
+// behind the decode kernel, adds each head's fp16 residual window and merges
+// the head's partials with a log-sum-exp.
 #pragma once
 
 #include <type_traits>
@@ -105,11 +105,6 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src,
       "[%0], [%1], %2, [%3];" ::"r"(smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
-}
-
-__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes)
-               : "memory");
 }
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0,
@@ -323,14 +318,10 @@ struct Cfg {
   static constexpr uint32_t S_VZ = S_VS + kC * NJ * 2;
   static constexpr uint32_t S_BYTES = (S_VZ + kC * NJ * 2 + 127) / 128 * 128;
   // per-warp layout: [mbarriers][q' GQP x D f32, channel c scaled by the
-  // 2^-sexp of its score slot][q' GQP x D f32][stages].  The residual
-  // window's (o, m, l) lives in the stage slot of the residual chunk, which
-  // receives no copy.
+  // 2^-sexp of its score slot][q' GQP x D f32][stages].
   static constexpr uint32_t W_QF = 128;
   static constexpr uint32_t W_QN = W_QF + GQP * D * 4;
   static constexpr uint32_t W_STAGE0 = (W_QN + GQP * D * 4 + 127) / 128 * 128;
-  static constexpr uint32_t RES_BYTES = GQP * D * 4 + 32;
-  static_assert(RES_BYTES <= S_BYTES, "residual output must fit a stage");
   static __host__ __device__ constexpr uint32_t warp_bytes(int ST) {
     return W_STAGE0 + ST * S_BYTES;
   }
@@ -372,13 +363,13 @@ __device__ __forceinline__ int find_seq(const int32_t *prefix, int B,
 }
 
 // Position in the flattened chunk space, advanced one chunk at a time, with
-// the counts of its sequence cached (nc chunks per head, nq of them
-// quantized, Tq quantized tokens, nres residual tokens).
+// the counts of its sequence cached (nc chunks per head, Tq quantized
+// tokens).
 struct Cursor {
   int b, h, k;
-  int nc, nq, Tq, nres;
+  int nc, Tq;
   __device__ __forceinline__ void load(const MmaTable &tab) {
-    nc = tab.nc[b]; nq = tab.nq[b]; Tq = tab.Tq[b]; nres = tab.nres[b];
+    nc = tab.nc[b]; Tq = tab.Tq[b];
   }
   __device__ __forceinline__ void init(int c, const Geometry &geo,
                                        const MmaTable &tab) {
@@ -398,127 +389,7 @@ struct Cursor {
       }
     }
   }
-  // quantized chunk; residual window (a head's last chunk); otherwise one of
-  // the empty chunks that only weight the residual window in the split
-  __device__ __forceinline__ bool quant() const { return k < nq; }
-  __device__ __forceinline__ bool res() const { return k == nc - 1 && nres > 0; }
 };
-
-// The fp16 residual window of one head on the CUDA cores, 32 tokens at a
-// time: each lane scores one token (its whole key row against every query
-// head), then the block's values are accumulated with lanes owning
-// channels.  Rows are loaded in unrolled batches (a quarter of a key row per
-// lane, 8 value rows), all in flight at once, so the window costs a few
-// memory round trips rather than one per token; deeper batches raise the
-// register demand of the call and slow the grouped-query instantiations.
-// Writes the window's (o, m, l) per query head to ores / mres.  Kept out of
-// line: it runs once per head, and inlined it would raise the register
-// demand of the whole decode loop.
-template <int D, int GQP>
-__device__ __noinline__ void residual_window(
-    const __half *__restrict__ Kr, const __half *__restrict__ Vr, size_t ring0,
-    int Tq, int nres, int Rcap, int GQ, const float *qn, float *ores,
-    float *mres, int lane) {
-  constexpr int CPL = D / 32;      // value channels per lane
-  constexpr int KQ = D / 8;        // uint4 per key row
-  constexpr int KB = KQ < 4 ? KQ : 4;   // key uint4 in flight per lane
-  float m[GQP], l[GQP], o[GQP][CPL];
-#pragma unroll
-  for (int hh = 0; hh < GQP; ++hh) {
-    m[hh] = -INFINITY; l[hh] = 0.f;
-#pragma unroll
-    for (int u = 0; u < CPL; ++u) o[hh][u] = 0.f;
-  }
-  for (int base = 0; base < nres; base += 32) {
-    const int t = base + lane;
-    const bool valid = t < nres;
-    const uint4 *krow = reinterpret_cast<const uint4 *>(
-        Kr + (ring0 + (Tq + (valid ? t : 0)) % Rcap) * D);
-    float sc[GQP];
-#pragma unroll
-    for (int hh = 0; hh < GQP; ++hh) sc[hh] = 0.f;
-#pragma unroll 1
-    for (int q0 = 0; q0 < KQ; q0 += KB) {
-      uint4 kw[KB];
-#pragma unroll
-      for (int u = 0; u < KB; ++u) kw[u] = krow[q0 + u];
-#pragma unroll
-      for (int u = 0; u < KB; ++u) {
-        const __half2 *kh = reinterpret_cast<const __half2 *>(&kw[u]);
-        float kf[8];
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const float2 f = __half22float2(kh[v]);
-          kf[2 * v] = f.x; kf[2 * v + 1] = f.y;
-        }
-#pragma unroll
-        for (int hh = 0; hh < GQP; ++hh) {
-          const float4 qa = reinterpret_cast<const float4 *>(qn + hh * D)[2 * (q0 + u)];
-          const float4 qc = reinterpret_cast<const float4 *>(qn + hh * D)[2 * (q0 + u) + 1];
-          sc[hh] = fmaf(qa.x, kf[0], fmaf(qa.y, kf[1], fmaf(qa.z, kf[2],
-                   fmaf(qa.w, kf[3], fmaf(qc.x, kf[4], fmaf(qc.y, kf[5],
-                   fmaf(qc.z, kf[6], fmaf(qc.w, kf[7], sc[hh]))))))));
-        }
-      }
-    }
-    float pv[GQP];
-#pragma unroll
-    for (int hh = 0; hh < GQP; ++hh) {
-      const float s_ = valid ? sc[hh] : -INFINITY;
-      float mb = s_;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1)
-        mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, off));
-      const float mn = fmaxf(m[hh], mb);
-      const float al = m[hh] == -INFINITY ? 0.f : exp2_neg(m[hh] - mn);
-      pv[hh] = exp2_neg(s_ - mn);
-      l[hh] = l[hh] * al + warp_sum(pv[hh]);
-#pragma unroll
-      for (int u = 0; u < CPL; ++u) o[hh][u] *= al;
-      m[hh] = mn;
-    }
-    const int nb = nres - base < 32 ? nres - base : 32;
-#pragma unroll 1
-    for (int t0 = 0; t0 < nb; t0 += 8) {
-      uint32_t raw[8][CPL / 2];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int tt = t0 + u < nb ? t0 + u : 0;
-        const __half *vr = Vr + (ring0 + (Tq + base + tt) % Rcap) * D + lane * CPL;
-        if constexpr (CPL == 4) {
-          const uint2 r2 = *reinterpret_cast<const uint2 *>(vr);
-          raw[u][0] = r2.x; raw[u][1] = r2.y;
-        } else {
-          raw[u][0] = *reinterpret_cast<const uint32_t *>(vr);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        float vf[CPL];
-#pragma unroll
-        for (int c = 0; c < CPL / 2; ++c) {
-          const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&raw[u][c]));
-          vf[2 * c] = f.x; vf[2 * c + 1] = f.y;
-        }
-#pragma unroll
-        for (int hh = 0; hh < GQP; ++hh) {
-          // lanes past nb hold p = 0, so their shuffled weight adds nothing
-          const float pt = __shfl_sync(kFull, pv[hh], (t0 + u) & 31);
-#pragma unroll
-          for (int c = 0; c < CPL; ++c) o[hh][c] = fmaf(pt, vf[c], o[hh][c]);
-        }
-      }
-    }
-  }
-  (void)GQ;
-#pragma unroll
-  for (int hh = 0; hh < GQP; ++hh) {
-#pragma unroll
-    for (int u = 0; u < CPL; ++u) ores[hh * D + lane * CPL + u] = o[hh][u];
-    if (lane == 0) { mres[hh] = m[hh]; mres[4 + hh] = l[hh]; }
-  }
-  __syncwarp();
-}
 
 template <class C>
 __global__ void __launch_bounds__(kNW * 32, kMinBlocks)
@@ -591,22 +462,10 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     bulk_g2s(st + C::S_VS, pl.Vs + row0 * NJ, b_vs, &bars[s]);
     bulk_g2s(st + C::S_VZ, pl.Vz + row0 * NJ, b_vs, &bars[s]);
   };
-  // lane 0, when the producer cursor reaches a residual chunk: pull the
-  // head's residual ring into L2, ST chunks before the window is read
-  auto prefetch_res = [&](const Cursor &cu) {
-    const size_t hd = (size_t)cu.b * geo.H_kv + cu.h;
-    const uint32_t bytes = geo.Rcap * D * 2;
-    prefetch_l2(pl.Kr + hd * geo.Rcap * D, bytes);
-    prefetch_l2(pl.Vr + hd * geo.Rcap * D, bytes);
-  };
-  // the producer's step for the chunk at pc (copies, or the L2 prefetch of
-  // a residual window), into stage s
+  // the producer's step for the chunk at pc: its copies into stage s
   auto produce = [&](const Cursor &cu, int s, int c) {
     if (cu.k == 0 || c == lo_c) set_prod_head(cu);
-    if (cu.quant())
-      issue(cu, s, c);
-    else if (cu.res())
-      prefetch_res(cu);
+    issue(cu, s, c);
   };
 
   Cursor pc;  // producer cursor: the next chunk to issue
@@ -615,7 +474,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   uint32_t pending = 0;  // bit s = copies in flight into stage s
   for (int i = 0; i < ST && i < n_mine; ++i) {
     if (lane == 0) produce(pc, i, lo_c + i);
-    if (pc.quant()) pending |= 1u << i;
+    pending |= 1u << i;
     pc.next(geo, tab);
   }
   bool failed = false;
@@ -640,8 +499,6 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   float beta_t = 0.f;    // zero-point term of pair tig, current window
   float unscale_t = 1.f; // 2^(24 - k) of pair tig, current window
   int cur_w = -1;
-  bool has_res = false;
-  const float *res_o = nullptr;   // residual window (o, m, l), when has_res
 
   auto reset_state = [&]() {
 #pragma unroll
@@ -653,7 +510,6 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     m_run = -INFINITY;
     l_run = 0.f;
     cur_w = -1;
-    has_res = false;
   };
 
   // q' of the head's GQP query heads: qn in channel order, qb with channel
@@ -748,14 +604,6 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     unscale_t = exp2i(24 - __shfl_sync(kFull, k, 8 * tig));
   };
 
-  auto residual = [&](const Cursor &cu, int hd, int s) {
-    float *ores = reinterpret_cast<float *>(stage0 + s * C::S_BYTES);
-    residual_window<D, GQP>(pl.Kr, pl.Vr, (size_t)hd * geo.Rcap, cu.Tq, cu.nres,
-                            geo.Rcap, GQ, qn, ores, ores + GQP * D, lane);
-    res_o = ores;
-    has_res = cu.nres > 0;
-  };
-
   // write this warp's partial of head hd (slot wg + hd); k_merge_mma, run
   // after the decode kernel, merges each head's partials
   auto flush = [&](int hd) {
@@ -763,15 +611,6 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     float Zt[NJ];
 #pragma unroll
     for (int j = 0; j < NJ; ++j) Zt[j] = head_reduce<GQP>(Z[j], AddOp());
-    float mf = m_run, aq = 1.f, ar = 0.f;
-    if (has_res) {
-      const float *mres = res_o + GQP * D;
-      const float mr = mres[h_s], lr = mres[4 + h_s];
-      mf = fmaxf(m_run, mr);
-      aq = m_run == -INFINITY ? 0.f : exp2_neg(m_run - mf);
-      ar = exp2_neg(mr - mf);
-      Lsum = Lsum * aq + lr * ar;
-    }
     if (h_s < GQ) {
       float *dst = args.part + ((size_t)(wg + hd) * GQP + h_s) * part_stride<D>();
 #pragma unroll
@@ -787,16 +626,12 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
           sa = exp2i(24 - L::fexp(2 * (mv & 3)));
           sb = exp2i(24 - L::fexp(2 * (mv & 3) + 1));
         }
-        float o0 = ((O[mv][0] + O[mv][1]) * sa + Zt[j]) * aq;
-        float o1 = ((O[mv][2] + O[mv][3]) * sb + Zt[j]) * aq;
-        if (has_res) {
-          o0 += res_o[h_s * D + c0] * ar;
-          o1 += res_o[h_s * D + c0 + 1] * ar;
-        }
+        const float o0 = (O[mv][0] + O[mv][1]) * sa + Zt[j];
+        const float o1 = (O[mv][2] + O[mv][3]) * sb + Zt[j];
         __stcg(reinterpret_cast<float2 *>(dst + c0), make_float2(o0, o1));
       }
       if (gid == 0 && tig < GQP) {
-        __stcg(dst + D, mf);
+        __stcg(dst + D, m_run);
         __stcg(dst + D + 1, Lsum);
       }
     }
@@ -1099,9 +934,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
       load_q(cu.b, cu.h);
       cur_hd = hd;
     }
-    if (cu.res()) {
-      residual(cu, hd, s);
-    } else if (cu.quant()) {
+    {
       const bool ok = __all_sync(kFull, mbar_wait(&bars[s], (phase >> s) & 1u));
       if (!ok) { failed = true; break; }
       phase ^= 1u << s;
@@ -1123,7 +956,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         produce(pc, s, lo_c + i + ST);
       }
-      if (pc.quant()) pending |= 1u << s;
+      pending |= 1u << s;
       pc.next(geo, tab);
     }
     cu.next(geo, tab);
@@ -1139,90 +972,150 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   }
 }
 
-// ---- merge of the per-warp partials ----------------------------------------
+// ---- merge of the per-warp partials and the fp16 residual window ---------
 //
-// The partials of kv head hd sit in slots w + hd for the warps w whose chunk
-// range touches the head; the log-sum-exp merge is M = max m_w,
-// L = sum 2^(m_w - M) l_w, o = sum 2^(m_w - M) o_w / L.  One CTA per
-// (sequence, query head, 32-channel slice) with nw <= kMergeWarps warps
-// (nw sized by the launcher to the largest partial count of a head); warp
-// j takes partials j, j + nw, ... with lanes on channels, keeping a running
-// (max, sum) of its own, and the warps' results are combined in shared
-// memory.  A warp reads its partials kMergeU at a time, all in flight, so a
-// head of up to nw * kMergeU partials costs one round of loads.
+// One CTA per (sequence, kv head, 32-channel slice) with nw <= kMergeWarps
+// warps (a multiple of the query heads per kv head, sized by the launcher),
+// serving the kv head's GQ query heads.  The partials of kv head hd sit in
+// slots w + hd for the warps w whose chunk range touches the head; warp j
+// merges query head j mod GQ's partials j/GQ, j/GQ + nw/GQ, ... (kMergeU at
+// a time, all in flight).  Then warp j takes the residual window's tokens
+// j, j + nw, ... (kMergeRT at a time): lanes hold 32-channel strides of the
+// key row and of every query head's q' (one warp-wide sum per head gives
+// the scores) and the slice's channel of the value row.  Every warp keeps a
+// running (max, sum, o) per query head; warp hh then combines all warps'
+// states of query head hh with a log-sum-exp.
 constexpr int kMergeWarps = 16;
 constexpr int kMergeU = 8;
+constexpr int kMergeRT = 4;
 
 template <int D, int GQP>
 __global__ void __launch_bounds__(kMergeWarps * 32)
-k_merge_mma(Geometry geo, MmaArgs args, MmaTable tab) {
-  __shared__ float sm_m[kMergeWarps], sm_l[kMergeWarps];
-  __shared__ float sm_o[kMergeWarps][32];
-  // programmatic dependent of the decode kernel: its partials are visible
-  // once this returns
+k_merge_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
+  constexpr int CPL = D / 32;
+  __shared__ float sm_m[kMergeWarps][GQP], sm_l[kMergeWarps][GQP];
+  __shared__ float sm_o[kMergeWarps][GQP][32];
+  // programmatic dependent of the decode kernel (or of the append before
+  // it): its writes are visible once this returns
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int b = blockIdx.x / geo.H_q, hq = blockIdx.x - b * geo.H_q;
-  if (tab.nc[b] == 0) return;   // the launcher zeroed this output
+  const int b = blockIdx.x / geo.H_kv, h = blockIdx.x - b * geo.H_kv;
+  const int nq = tab.nq[b], nres = tab.nres[b];
+  if (nq == 0 && nres == 0) return;   // no tokens: the launcher zeroed it
   const int GQ = args.GQ;
-  const int h = hq / GQ, hh = hq - h * GQ;
   const int hd = b * geo.H_kv + h;
-  const int64_t N = args.N, W = args.W;
-  const int64_t cs = tab.bprefix[b] + (int64_t)h * tab.nc[b];
-  const int64_t ce = cs + tab.nc[b];
-  const int w0 = (int)(((cs + 1) * W - 1) / N);
-  const int n = (int)((ce * W - 1) / N) - w0 + 1;
   const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
   const int nw = blockDim.x >> 5;
   const int c = blockIdx.y * 32 + lane;
-  auto entry = [&](int k) {
-    return args.part + ((size_t)(w0 + k + hd) * GQP + hh) * part_stride<D>();
+
+  float m_run[GQP], l_run[GQP], o_run[GQP];
+#pragma unroll
+  for (int hh = 0; hh < GQP; ++hh) { m_run[hh] = -INFINITY; l_run[hh] = 0.f; o_run[hh] = 0.f; }
+  // fold n entries (m_u, l_u, o_u) into head hh's running state; entries
+  // with m = -inf (partials of empty ranges, tokens past the end) weigh
+  // nothing
+  auto fold = [&](int hh, const float *mu, const float *lu, const float *ou, int n) {
+    float mr = m_run[hh];
+    for (int u = 0; u < n; ++u) mr = fmaxf(mr, mu[u]);
+    if (mr == -INFINITY) return;
+    const float a = m_run[hh] == -INFINITY ? 0.f : exp2_neg(m_run[hh] - mr);
+    float l = l_run[hh] * a, o = o_run[hh] * a;
+    for (int u = 0; u < n; ++u) {
+      const float f = mu[u] == -INFINITY ? 0.f : exp2_neg(mu[u] - mr);
+      l = fmaf(f, lu[u], l);
+      o = fmaf(f, ou[u], o);
+    }
+    m_run[hh] = mr; l_run[hh] = l; o_run[hh] = o;
   };
 
-  float m_run = -INFINITY, l_run = 0.f, o_run = 0.f;
-  for (int k0 = wp; k0 < n; k0 += nw * kMergeU) {
-    float mu[kMergeU], lu[kMergeU], ou[kMergeU];
+  // (1) the decode kernel's partials: warp wp serves query head wp mod GQ
+  const int hp = wp % GQ, per = nw / GQ;
+  if (nq > 0 && wp < per * GQ) {
+    const int64_t N = args.N, W = args.W;
+    const int64_t cs = tab.bprefix[b] + (int64_t)h * tab.nc[b];
+    const int64_t ce = cs + tab.nc[b];
+    const int w0 = (int)(((cs + 1) * W - 1) / N);
+    const int n = (int)((ce * W - 1) / N) - w0 + 1;
+    for (int k0 = wp / GQ; k0 < n; k0 += per * kMergeU) {
+      float mu[kMergeU], lu[kMergeU], ou[kMergeU];
 #pragma unroll
-    for (int u = 0; u < kMergeU; ++u) {
-      const int k = k0 + u * nw;
-      const bool ok = k < n;
-      const float *e = entry(ok ? k : k0);
-      mu[u] = ok ? __ldcg(e + D) : -INFINITY;
-      lu[u] = ok ? __ldcg(e + D + 1) : 0.f;
-      ou[u] = ok ? __ldcg(e + c) : 0.f;
+      for (int u = 0; u < kMergeU; ++u) {
+        const int k = k0 + u * per;
+        const bool ok = k < n;
+        const float *e = args.part +
+                         ((size_t)(w0 + (ok ? k : k0) + hd) * GQP + hp) * part_stride<D>();
+        mu[u] = ok ? __ldcg(e + D) : -INFINITY;
+        lu[u] = ok ? __ldcg(e + D + 1) : 0.f;
+        ou[u] = ok ? __ldcg(e + c) : 0.f;
+      }
+#pragma unroll
+      for (int hh = 0; hh < GQP; ++hh)
+        if (hh == hp) fold(hh, mu, lu, ou, kMergeU);
     }
-    float mr = m_run;
-#pragma unroll
-    for (int u = 0; u < kMergeU; ++u) mr = fmaxf(mr, mu[u]);
-    const float a = m_run == -INFINITY ? 0.f : exp2_neg(m_run - mr);
-    l_run *= a;
-    o_run *= a;
-#pragma unroll
-    for (int u = 0; u < kMergeU; ++u) {
-      // partials of warps whose range held only empty chunks carry
-      // m = -inf and weigh nothing (also when every m so far is -inf)
-      const float f = mu[u] == -INFINITY ? 0.f : exp2_neg(mu[u] - mr);
-      l_run = fmaf(f, lu[u], l_run);
-      o_run = fmaf(f, ou[u], o_run);
-    }
-    m_run = mr;
   }
-  if (lane == 0) { sm_m[wp] = m_run; sm_l[wp] = l_run; }
-  sm_o[wp][lane] = o_run;
+
+  // (2) the fp16 residual window: tokens T_q ... T_q + nres - 1 in ring
+  // slots (T_q + t) mod Rcap
+  if (nres > 0) {
+    float qv[GQP][CPL];
+#pragma unroll
+    for (int hh = 0; hh < GQP; ++hh) {
+      const __half *qrow = args.q + ((size_t)b * geo.H_q + h * GQ + (hh < GQ ? hh : 0)) * D;
+#pragma unroll
+      for (int u = 0; u < CPL; ++u) qv[hh][u] = __half2float(qrow[lane + 32 * u]) * args.scale_log2;
+    }
+    const size_t ring0 = (size_t)hd * geo.Rcap;
+    const int Tq = tab.Tq[b];
+    for (int t0 = wp; t0 < nres; t0 += nw * kMergeRT) {
+      float kv[kMergeRT][CPL], vv[kMergeRT];
+      bool ok[kMergeRT];
+#pragma unroll
+      for (int r = 0; r < kMergeRT; ++r) {
+        const int t = t0 + r * nw;
+        ok[r] = t < nres;
+        const size_t row = (ring0 + (Tq + (ok[r] ? t : t0)) % geo.Rcap) * D;
+#pragma unroll
+        for (int u = 0; u < CPL; ++u) kv[r][u] = __half2float(pl.Kr[row + lane + 32 * u]);
+        vv[r] = __half2float(pl.Vr[row + c]);
+      }
+#pragma unroll
+      for (int hh = 0; hh < GQP; ++hh) {
+        if (hh >= GQ) break;
+        float mu[kMergeRT], lu[kMergeRT];
+#pragma unroll
+        for (int r = 0; r < kMergeRT; ++r) {
+          float sc = 0.f;
+#pragma unroll
+          for (int u = 0; u < CPL; ++u) sc = fmaf(qv[hh][u], kv[r][u], sc);
+          sc = warp_sum(sc);
+          mu[r] = ok[r] ? sc : -INFINITY;
+          lu[r] = 1.f;
+        }
+        fold(hh, mu, lu, vv, kMergeRT);
+      }
+    }
+  }
+
+#pragma unroll
+  for (int hh = 0; hh < GQP; ++hh) {
+    if (lane == 0) { sm_m[wp][hh] = m_run[hh]; sm_l[wp][hh] = l_run[hh]; }
+    sm_o[wp][hh][lane] = o_run[hh];
+  }
   __syncthreads();
-  if (wp == 0) {
+  if (wp < GQ) {
+    const int hh = wp;
     float M = -INFINITY;
-    for (int j = 0; j < nw; ++j) M = fmaxf(M, sm_m[j]);
+    for (int j = 0; j < nw; ++j) M = fmaxf(M, sm_m[j][hh]);
     float L = 0.f, o = 0.f;
     for (int j = 0; j < nw; ++j) {
-      const float f = sm_m[j] == -INFINITY ? 0.f : exp2_neg(sm_m[j] - M);
-      L = fmaf(f, sm_l[j], L);
-      o = fmaf(f, sm_o[j][lane], o);
+      const float f = sm_m[j][hh] == -INFINITY ? 0.f : exp2_neg(sm_m[j][hh] - M);
+      L = fmaf(f, sm_l[j][hh], L);
+      o = fmaf(f, sm_o[j][hh][lane], o);
     }
-    args.out[((size_t)b * geo.H_q + hq) * D + c] = o / L;
+    args.out[((size_t)b * geo.H_q + h * GQ + hh) * D + c] = o / L;
   }
 }
 
-using MergeFn = void (*)(Geometry, MmaArgs, MmaTable);
+using MergeFn = void (*)(Geometry, Planes, MmaArgs, MmaTable);
 
 template <int D, int GQP>
 MergeFn merge_fn() {

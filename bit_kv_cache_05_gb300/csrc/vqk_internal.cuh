@@ -135,11 +135,10 @@ cudaError_t launch_decode(const Geometry &geo, const Planes &pl,
 
 // ---- decode on the tensor cores (D = 64/128, H_q/H_kv <= 4) ---------------
 
-// Flattened chunk space: sequence b owns chunks [bprefix[b], bprefix[b+1]),
-// H_kv heads of nc[b] chunks each: nq[b] quantized 64-token chunks and, when
-// nres[b] > 0, mma_residual_weight(nres[b]) more, the last of which is the
-// residual window (the ones before it are empty: they give the window, read
-// from global memory on the CUDA cores, its weight in the equal split).
+// Flattened chunk space of the quantized tokens: sequence b owns chunks
+// [bprefix[b], bprefix[b+1]), H_kv heads of nc[b] = nq[b] 64-token chunks
+// each.  The fp16 residual window (nres[b] tokens from Tq[b]) is read by the
+// merge kernel.
 struct MmaTable {
   int32_t bprefix[kMaxB + 1];
   int32_t nc[kMaxB];
@@ -169,10 +168,6 @@ struct MmaPlan {
 // false when the shape has no tensor-core kernel (then the CUDA-core kernel
 // of launch_decode serves it)
 bool mma_plan(const Geometry &geo, int sm_count, MmaPlan *plan);
-// chunks of the split given to a residual window of nres tokens
-inline int mma_residual_weight(int nres) {
-  return nres > 0 ? 1 + 2 * ((nres + 31) / 32) : 0;
-}
 size_t mma_part_floats(const Geometry &geo, const MmaPlan &plan);
 cudaError_t launch_decode_mma(const Geometry &geo, const Planes &pl,
                               const MmaPlan &plan, MmaArgs args,

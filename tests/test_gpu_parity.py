@@ -267,13 +267,16 @@ def test_split_count_invariance(lib, name):
     for tps in (0, 256, 512, 1024, 4096, 8192):
         c.set_split_tokens(tps)
         outs.append(c.decode_attend(inp["q"]).cpu().numpy())
-    # Partitions change only the fp32 summation order and the tensor-core
-    # operand scaling per segment; the fp16 hi/lo operands carry ~2^-21
-    # relative precision on sums of magnitude ~2 that cancel to the output
-    # (code part vs zero-point part), so partitions agree to ~1e-5; 1e-4 is
-    # ten times below the parity tolerance.
+    # Partitions change only the fp32 summation order: each warp accumulates
+    # its segment (up to a whole head here) in fp32, and on the value side
+    # the code sum and the zero-point sum, each of the size of the values,
+    # cancel to the output, which amplifies the rounding.  Measured spreads
+    # against the finest partition: up to 3e-5 (pages shape, outputs ~0.08)
+    # and 1e-4 (grouped-query case with outlier keys, outputs up to ~3).
+    # The bound is ten times below the parity tolerance, in the same form.
+    ref = outs[0]
     for o in outs[1:]:
-        assert np.abs(o - outs[0]).max() <= 1e-4
+        assert (np.abs(o - ref) <= 1e-4 + 1e-4 * np.abs(ref)).all()
     c.device_status()
     c.close()
 
