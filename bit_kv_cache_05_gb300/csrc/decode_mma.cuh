@@ -995,9 +995,6 @@ k_merge_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   constexpr int CPL = D / 32;
   __shared__ float sm_m[kMergeWarps][GQP], sm_l[kMergeWarps][GQP];
   __shared__ float sm_o[kMergeWarps][GQP][32];
-  // programmatic dependent of the decode kernel (or of the append before
-  // it): its writes are visible once this returns
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int b = blockIdx.x / geo.H_kv, h = blockIdx.x - b * geo.H_kv;
   const int nq = tab.nq[b], nres = tab.nres[b];
   if (nq == 0 && nres == 0) return;   // no tokens: the launcher zeroed it
@@ -1027,7 +1024,56 @@ k_merge_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     m_run[hh] = mr; l_run[hh] = l; o_run[hh] = o;
   };
 
-  // (1) the decode kernel's partials: warp wp serves query head wp mod GQ
+  // (1) the fp16 residual window: tokens T_q ... T_q + nres - 1 in ring
+  // slots (T_q + t) mod Rcap.  When the decode kernel ran (N > 0), the ring
+  // and q were written before it released this grid (it waits for the
+  // append first), so the window is read, from L2, while it drains;
+  // otherwise the append itself precedes this kernel and is waited for.
+  if (args.N <= 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (nres > 0) {
+    float qv[GQP][CPL];
+#pragma unroll
+    for (int hh = 0; hh < GQP; ++hh) {
+      const __half *qrow = args.q + ((size_t)b * geo.H_q + h * GQ + (hh < GQ ? hh : 0)) * D;
+#pragma unroll
+      for (int u = 0; u < CPL; ++u)
+        qv[hh][u] = __half2float(__ldcg(qrow + lane + 32 * u)) * args.scale_log2;
+    }
+    const size_t ring0 = (size_t)hd * geo.Rcap;
+    const int Tq = tab.Tq[b];
+    for (int t0 = wp; t0 < nres; t0 += nw * kMergeRT) {
+      float kv[kMergeRT][CPL], vv[kMergeRT];
+      bool ok[kMergeRT];
+#pragma unroll
+      for (int r = 0; r < kMergeRT; ++r) {
+        const int t = t0 + r * nw;
+        ok[r] = t < nres;
+        const size_t row = (ring0 + (Tq + (ok[r] ? t : t0)) % geo.Rcap) * D;
+#pragma unroll
+        for (int u = 0; u < CPL; ++u) kv[r][u] = __half2float(__ldcg(pl.Kr + row + lane + 32 * u));
+        vv[r] = __half2float(__ldcg(pl.Vr + row + c));
+      }
+#pragma unroll
+      for (int hh = 0; hh < GQP; ++hh) {
+        if (hh >= GQ) break;
+        float mu[kMergeRT], lu[kMergeRT];
+#pragma unroll
+        for (int r = 0; r < kMergeRT; ++r) {
+          float sc = 0.f;
+#pragma unroll
+          for (int u = 0; u < CPL; ++u) sc = fmaf(qv[hh][u], kv[r][u], sc);
+          sc = warp_sum(sc);
+          mu[r] = ok[r] ? sc : -INFINITY;
+          lu[r] = 1.f;
+        }
+        fold(hh, mu, lu, vv, kMergeRT);
+      }
+    }
+  }
+
+  // (2) the decode kernel's partials, visible once griddepcontrol.wait
+  // returns: warp wp serves query head wp mod GQ
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int hp = wp % GQ, per = nw / GQ;
   if (nq > 0 && wp < per * GQ) {
     const int64_t N = args.N, W = args.W;
@@ -1050,48 +1096,6 @@ k_merge_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
 #pragma unroll
       for (int hh = 0; hh < GQP; ++hh)
         if (hh == hp) fold(hh, mu, lu, ou, kMergeU);
-    }
-  }
-
-  // (2) the fp16 residual window: tokens T_q ... T_q + nres - 1 in ring
-  // slots (T_q + t) mod Rcap
-  if (nres > 0) {
-    float qv[GQP][CPL];
-#pragma unroll
-    for (int hh = 0; hh < GQP; ++hh) {
-      const __half *qrow = args.q + ((size_t)b * geo.H_q + h * GQ + (hh < GQ ? hh : 0)) * D;
-#pragma unroll
-      for (int u = 0; u < CPL; ++u) qv[hh][u] = __half2float(qrow[lane + 32 * u]) * args.scale_log2;
-    }
-    const size_t ring0 = (size_t)hd * geo.Rcap;
-    const int Tq = tab.Tq[b];
-    for (int t0 = wp; t0 < nres; t0 += nw * kMergeRT) {
-      float kv[kMergeRT][CPL], vv[kMergeRT];
-      bool ok[kMergeRT];
-#pragma unroll
-      for (int r = 0; r < kMergeRT; ++r) {
-        const int t = t0 + r * nw;
-        ok[r] = t < nres;
-        const size_t row = (ring0 + (Tq + (ok[r] ? t : t0)) % geo.Rcap) * D;
-#pragma unroll
-        for (int u = 0; u < CPL; ++u) kv[r][u] = __half2float(pl.Kr[row + lane + 32 * u]);
-        vv[r] = __half2float(pl.Vr[row + c]);
-      }
-#pragma unroll
-      for (int hh = 0; hh < GQP; ++hh) {
-        if (hh >= GQ) break;
-        float mu[kMergeRT], lu[kMergeRT];
-#pragma unroll
-        for (int r = 0; r < kMergeRT; ++r) {
-          float sc = 0.f;
-#pragma unroll
-          for (int u = 0; u < CPL; ++u) sc = fmaf(qv[hh][u], kv[r][u], sc);
-          sc = warp_sum(sc);
-          mu[r] = ok[r] ? sc : -INFINITY;
-          lu[r] = 1.f;
-        }
-        fold(hh, mu, lu, vv, kMergeRT);
-      }
     }
   }
 
