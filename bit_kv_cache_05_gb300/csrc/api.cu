@@ -25,6 +25,9 @@ struct vq_kivi_cache {
   int32_t tps_min;        // smallest split the workspace allows
   bool use_mma;           // tensor-core decode kernel for this shape
   int32_t fail_chunk;     // testing hook, -1 = off
+  bool flush_last;        // the last kernel launched for this cache is a
+                          // k_flush (it may still be writing planes when a
+                          // programmatic dependent starts)
   MmaPlan plan;
   unsigned *err;          // device word set by a kernel whose wait gave up
   int32_t S[kMaxB], Tq[kMaxB], nres[kMaxB];
@@ -251,6 +254,7 @@ int vq_kivi_quantize(const vq_kivi_params *p, const void *K, const void *V,
   e = launch_tail(geo, pl, (const __half *)K, (const __half *)V, s_stride, tt,
                   tt.prefix[p->B], st);
   if (e != cudaSuccess) return abort_create(e, "residual kernel launch");
+  c->flush_last = ft.prefix[p->B] > 0 && tt.prefix[p->B] == 0;
   *out = c;
   return VQ_OK;
 }
@@ -302,6 +306,10 @@ int vq_kivi_append(vq_kivi_cache *c, const void *K_new, const void *V_new,
   e = launch_tail(c->geo, c->pl, (const __half *)K_new, (const __half *)V_new,
                   n_stride, tt, tt.prefix[p.B], st);
   if (e != cudaSuccess) return cuda_fail(e, "residual kernel launch");
+  if (tt.prefix[p.B] > 0)
+    c->flush_last = false;
+  else if (ft.prefix[p.B] > 0)
+    c->flush_last = true;
   for (int b = 0; b < p.B; ++b) {
     c->S[b] += n_new[b];
     c->Tq[b] = Tq_new[b];
@@ -344,6 +352,7 @@ int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
     args.N = tab.bprefix[p.B];
     args.fail_chunk = c->fail_chunk;
     c->fail_chunk = -1;
+    args.early = c->flush_last ? 0 : 1;
     MmaPlan plan = c->plan;
     if (c->split_tokens > 0) {
       // a fixed partition: about split_tokens quantized tokens per warp
@@ -352,6 +361,7 @@ int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
       if (w < plan.warps_max) plan.warps_max = (int)(w > 0 ? w : 1);
     }
     cudaError_t e = launch_decode_mma(c->geo, c->pl, plan, args, tab, st);
+    c->flush_last = false;
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     c->last_stream = st;
     return VQ_OK;

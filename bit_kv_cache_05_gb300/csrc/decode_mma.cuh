@@ -399,11 +399,14 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   constexpr int G = C::G, ROW = C::ROW, ROWQ = C::ROWQ;
   extern __shared__ __align__(128) unsigned char smem[];
 
-  // launched as a programmatic dependent of the stream's previous kernel
-  // (an append): wait until its writes are visible, then let the merge
-  // kernel, launched behind this one, be scheduled as CTAs retire
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;");
+  // Launched as a programmatic dependent of the stream's previous kernel:
+  // griddepcontrol.wait returns once its writes are visible.  That kernel
+  // started only after everything before it completed (it waits before it
+  // releases this grid), so when it is not a k_flush of this cache
+  // (args.early) it writes nothing this kernel reads from the planes, and
+  // each warp's first copies are issued before the wait.  The merge kernel
+  // is released only after the wait (it reads the residual ring early).
+  if (!args.early) asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int wg = blockIdx.x * kNW + warp;
@@ -477,6 +480,8 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     pending |= 1u << i;
     pc.next(geo, tab);
   }
+  if (args.early) asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   bool failed = false;
 
   // ---- per-lane constants ------------------------------------------------
@@ -525,7 +530,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
       const int hh = j / PER, c = i - hh * D;
       float v = 0.f;
       if (hh < GQ)
-        v = __half2float(args.q[((size_t)b * geo.H_q + h * GQ + hh) * D + c]) *
+        v = __half2float(__ldcg(args.q + ((size_t)b * geo.H_q + h * GQ + hh) * D + c)) *
             args.scale_log2;
       const float vb = v * exp2i(-L::oexp(c));
       qn[i] = v;

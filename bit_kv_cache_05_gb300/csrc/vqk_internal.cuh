@@ -155,6 +155,9 @@ struct MmaArgs {
   float scale_log2;  // softmax scale * log2(e)
   int N;             // total chunks
   int fail_chunk;    // testing: chunk whose copies are not issued (-1: none)
+  int early;         // 1: the previous kernel in the stream writes no code or
+                     // metadata plane of this cache (it is not a k_flush of
+                     // it), so the first copies may precede griddepcontrol.wait
   int W;             // warps used (<= N), filled in by the launcher
   int GQ, GQp, KG, ST;
 };
