@@ -198,6 +198,7 @@ int vq_kivi_quantize(const vq_kivi_params *p, const void *K, const void *V,
   size_t o_Vr = off; off += round_up(sz_res, A);
   size_t o_part = off; off += round_up(sz_part, A);
   size_t o_err = off; off += A;
+  size_t o_ksmax = off; off += round_up(BH * sizeof(uint32_t), A);
   c->block_bytes = off;
 
   e = cudaMallocAsync(&c->block, c->block_bytes, st);
@@ -219,6 +220,7 @@ int vq_kivi_quantize(const vq_kivi_params *p, const void *K, const void *V,
   pl.Vr = (__half *)(base + o_Vr);
   pl.part = (float *)(base + o_part);
   c->err = (unsigned *)(base + o_err);
+  pl.ksmax = (uint32_t *)(base + o_ksmax);
   c->last_stream = st;
 
   auto abort_create = [&](cudaError_t err, const char *what) {

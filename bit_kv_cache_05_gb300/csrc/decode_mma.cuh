@@ -500,9 +500,8 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   float Z[NJ];
   float m_run = -INFINITY, l_run = 0.f;
   uint32_t Bs[KS][2];
-  float qmax_b = 0.f;    // max |q'| (slot-scaled) of query head h_b
   float beta_t = 0.f;    // zero-point term of pair tig, current window
-  float unscale_t = 1.f; // 2^(24 - k) of pair tig, current window
+  float unscale_t = 1.f; // 2^(24 - k) of this lane's score head
   int cur_w = -1;
 
   auto reset_state = [&]() {
@@ -517,14 +516,19 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     cur_w = -1;
   };
 
-  // q' of the head's GQP query heads: qn in channel order, qb with channel
-  // c scaled by 2^-sexp of its score slot; qmax_b = max |qb| of head h_b
+  // q' of the head's GQP query heads: qn in channel order; qb with channel
+  // c scaled by 2^-oexp(c) of its score slot and by the head's power of two
+  // 2^k, which puts the bound max|q'| * max s_K of the score operand's
+  // products (over every key group of the kv head) in [2^13, 2^14): no
+  // fp16 overflow, and the lo parts of the large products stay in fp16's
+  // normal range.  unscale_t = 2^(24 - k) of this lane's score head.
   auto load_q = [&](int b, int h) {
-    float mq[GQP];
+    constexpr int NQ = GQP * D / 32;
+    float mq[GQP], vb[NQ];
 #pragma unroll
     for (int hh = 0; hh < GQP; ++hh) mq[hh] = 0.f;
 #pragma unroll
-    for (int j = 0; j < GQP * D / 32; ++j) {
+    for (int j = 0; j < NQ; ++j) {
       const int i = lane + 32 * j;
       constexpr int PER = D / 32;
       const int hh = j / PER, c = i - hh * D;
@@ -532,55 +536,52 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
       if (hh < GQ)
         v = __half2float(__ldcg(args.q + ((size_t)b * geo.H_q + h * GQ + hh) * D + c)) *
             args.scale_log2;
-      const float vb = v * exp2i(-L::oexp(c));
+      vb[j] = v * exp2i(-L::oexp(c));
       qn[i] = v;
-      qb[i] = vb;
-      mq[hh] = fmaxf(mq[hh], fabsf(vb));
+      mq[hh] = fmaxf(mq[hh], fabsf(vb[j]));
     }
+    const float smax = __half2float(__ushort_as_half(
+        (unsigned short)__ldcg(pl.ksmax + (size_t)b * geo.H_kv + h)));
+    int kh[GQP];
 #pragma unroll
     for (int hh = 0; hh < GQP; ++hh) {
       float m = mq[hh];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1)
         m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
-      if (hh == h_b) qmax_b = m;
+      const int k = 13 - (((__float_as_int(m * smax) >> 23) & 0xff) - 127);
+      kh[hh] = k < -60 ? -60 : (k > 60 ? 60 : k);
     }
+#pragma unroll
+    for (int j = 0; j < NQ; ++j) {
+      constexpr int PER = D / 32;
+      qb[lane + 32 * j] = vb[j] * exp2i(kh[j / PER]);
+    }
+    int kl = kh[0];
+#pragma unroll
+    for (int hh = 1; hh < GQP; ++hh)
+      if (hh == h_s) kl = kh[hh];
+    unscale_t = exp2i(24 - kl);
     __syncwarp();
   };
 
   // B operand of the score MMA for the window starting at key group gw0 (the
-  // stage's key scale/zero region starts at group kg0), and, for this lane's
-  // column pair, the zero-point term beta and the factor that undoes the
-  // operand scaling.  Each column pair is scaled by the power of two 2^k
-  // that puts the bound max|q'| * max s of its products in [2^13, 2^14):
-  // no fp16 overflow, and the lo parts of the large products stay in fp16's
-  // normal range.
+  // stage's key scale/zero region starts at group kg0; qb carries the
+  // head's operand scaling), and, for this lane's column pair, the
+  // zero-point term beta.
   auto build_score_b = [&](const __half *Ks, const __half *Kz, int gw0, int kg0) {
     const int gr = gw0 + pair_b / GQP - kg0;   // group row in the region
     const float *qbh = qb + h_b * D + 4 * tig;
     const __half *ksr = Ks + gr * D + 4 * tig;
-    uint2 sraw[KS];
-    __half2 smx = __float2half2_rn(0.f);
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      sraw[ks] = *reinterpret_cast<const uint2 *>(ksr + 16 * ks);
-      smx = __hmax2(smx, __hmax2(*reinterpret_cast<const __half2 *>(&sraw[ks].x),
-                                 *reinterpret_cast<const __half2 *>(&sraw[ks].y)));
-    }
-    float smax = fmaxf(__low2float(smx), __high2float(smx));
-    smax = fmaxf(smax, __shfl_xor_sync(kFull, smax, 1));
-    smax = fmaxf(smax, __shfl_xor_sync(kFull, smax, 2));
-    int k = 13 - (((__float_as_int(qmax_b * smax) >> 23) & 0xff) - 127);
-    k = k < -60 ? -60 : (k > 60 ? 60 : k);
-    const float2 sc = f2(exp2i(k), exp2i(k));
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
+      const uint2 sraw = *reinterpret_cast<const uint2 *>(ksr + 16 * ks);
       const float4 qs = *reinterpret_cast<const float4 *>(qbh + 16 * ks);
-      const float2 s01 = __half22float2(*reinterpret_cast<const __half2 *>(&sraw[ks].x));
-      const float2 s23 = __half22float2(*reinterpret_cast<const __half2 *>(&sraw[ks].y));
+      const float2 s01 = __half22float2(*reinterpret_cast<const __half2 *>(&sraw.x));
+      const float2 s23 = __half22float2(*reinterpret_cast<const __half2 *>(&sraw.y));
       // channel order 4tig + 0..3
-      const float2 a01 = hilo2(__fmul2_rn(__fmul2_rn(f2(qs.x, qs.y), sc), s01), hls);
-      const float2 a23 = hilo2(__fmul2_rn(__fmul2_rn(f2(qs.z, qs.w), sc), s23), hls);
+      const float2 a01 = hilo2(__fmul2_rn(f2(qs.x, qs.y), s01), hls);
+      const float2 a23 = hilo2(__fmul2_rn(f2(qs.z, qs.w), s23), hls);
       const float a[4] = {a01.x, a01.y, a23.x, a23.y};
       // slot order: slot e holds channel 4tig + off(e)
       Bs[ks][0] = pack_half2(a[L::off(0)], a[L::off(1)]);
@@ -606,7 +607,6 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     zpart += __shfl_xor_sync(kFull, zpart, 4);   // hi + lo lanes of the pair
     // lane (gid, tig) needs the values of pair tig, held by lanes gid = 2*tig
     beta_t = __shfl_sync(kFull, zpart, 8 * tig);
-    unscale_t = exp2i(24 - __shfl_sync(kFull, k, 8 * tig));
   };
 
   // write this warp's partial of head hd (slot wg + hd); k_merge_mma, run

@@ -149,6 +149,7 @@ extern "C" int vq_kivi_decode_attend_static(
   pl.Kr = (__half *)planes->Kr;
   pl.Vr = (__half *)planes->Vr;
   pl.part = (float *)scratch;
+  pl.ksmax = nullptr;   // only the tensor-core decode reads it
 
   DecodeTable tab;
   tab.prefix[0] = 0;

@@ -207,8 +207,15 @@ k_flush(Geometry geo, Planes pl, const __half *__restrict__ Kin,
     const float scale = __fdiv_rn(__fsub_rn(mx, mn), (float)levels);
     const float rcp = scale != 0.0f ? __frcp_rn(scale) : 0.0f;
     const size_t idx = (bh * (geo.Tcap / g) + P0 / g) * D + c;
-    pl.Ks[idx] = __float2half_rn(scale);
+    const __half sh = __float2half_rn(scale);
+    pl.Ks[idx] = sh;
     pl.Kz[idx] = __float2half_rn(mn);
+    // running bound of the head's key scales (non-negative fp16 values
+    // order like their bit patterns)
+    if (pl.ksmax) {
+      const unsigned m = __reduce_max_sync(0xffffffffu, (unsigned)__half_as_ushort(sh));
+      if ((c & 31) == 0) atomicMax(pl.ksmax + bh, m);
+    }
     for (int i = 0; i < g; ++i)
       codes[i * D + c] = (uint8_t)quant_code_fast(__half2float(tile[i * D + c]),
                                                   mn, scale, rcp, levels);

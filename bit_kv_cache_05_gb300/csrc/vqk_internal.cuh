@@ -21,6 +21,8 @@ struct Planes {
   __half *Vs, *Vz;           // [B][H_kv][Tcap][D/g]        value scale / zero
   __half *Kr, *Vr;           // [B][H_kv][Rcap][D]          residual ring
   float *part;               // [B][H_q][max_items][D+2]    split partials
+  uint32_t *ksmax;           // [B][H_kv] fp16 bits of the largest key scale
+                             // flushed for the head (a bound for the decode)
 };
 
 // orders of the code planes (see "code-plane orders" below)
