@@ -433,39 +433,59 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   // The key scale/zero rows are copied only where a score window starts or
   // the warp's range starts: every other chunk reuses the operand built
   // from an earlier stage.
-  // row index of token 0 of the producer's head in the code / value-meta
-  // planes, and of its group 0 in the key-meta planes (set per head)
-  size_t prow0 = 0, pgrp0 = 0;
+  // ---- producer: a chunk's copies (key codes, value codes, the key scale /
+  // zero rows where a score window or the warp's range starts, value scale
+  // / zero rows) go out from lanes 0..5 at once, lane j holding plane j's
+  // base for the producer's head; lane 0 first posts the stage's
+  // transaction bytes.  The key scale / zero rows are copied only where a
+  // window or the range starts: every other chunk reuses the operand built
+  // from an earlier stage.
+  uint32_t prow = 0, psoff = 0;           // bytes per token (per key group
+                                          // for lanes 2, 3); stage offset
+  switch (lane) {
+    case 0: prow = ROW; psoff = C::S_KC; break;
+    case 1: prow = ROW; psoff = C::S_VC; break;
+    case 2: prow = D * 2; psoff = C::S_KS; break;
+    case 3: prow = D * 2; psoff = C::S_KZ; break;
+    case 4: prow = NJ * 2; psoff = C::S_VS; break;
+    case 5: prow = NJ * 2; psoff = C::S_VZ; break;
+    default: break;
+  }
+  const unsigned char *pbase = nullptr;   // plane base of the producer's head
   auto set_prod_head = [&](const Cursor &cu) {
     const size_t hd = (size_t)cu.b * geo.H_kv + cu.h;
-    prow0 = hd * geo.Tcap;
-    pgrp0 = hd * (geo.Tcap / G);
+    const size_t r0 = hd * geo.Tcap, g0 = hd * (geo.Tcap / G);
+    const unsigned char *b = nullptr;
+    if (lane == 0) b = pl.Kc + r0 * ROW;
+    if (lane == 1) b = pl.Vc + r0 * ROW;
+    if (lane == 2) b = reinterpret_cast<const unsigned char *>(pl.Ks + g0 * D);
+    if (lane == 3) b = reinterpret_cast<const unsigned char *>(pl.Kz + g0 * D);
+    if (lane == 4) b = reinterpret_cast<const unsigned char *>(pl.Vs + r0 * NJ);
+    if (lane == 5) b = reinterpret_cast<const unsigned char *>(pl.Vz + r0 * NJ);
+    pbase = b;
   };
   auto issue = [&](const Cursor &cu, int s, int c) {
-    if (c == args.fail_chunk) return;   // testing: a copy that never comes
     const int t0 = cu.k * kC;
     const int rem = cu.Tq - t0;
     const int nvalid = rem < kC ? rem : kC;
-    unsigned char *st = stage0 + s * C::S_BYTES;
-    const uint32_t b_codes = nvalid * ROW;
-    const uint32_t b_vs = nvalid * NJ * 2;
     const bool with_ks = (t0 % C::WT) == 0 || c == lo_c;
     const int kg0 = ((t0 / G) / C::KG) * C::KG;
     const int ngv = cu.Tq / G - kg0;
-    const uint32_t b_ks = with_ks ? (ngv < C::KG ? ngv : C::KG) * D * 2 : 0u;
-    mbar_expect_tx(&bars[s], 2 * (b_codes + b_ks + b_vs));
-    const size_t row0 = prow0 + t0;
-    bulk_g2s(st + C::S_KC, pl.Kc + row0 * ROW, b_codes, &bars[s]);
-    bulk_g2s(st + C::S_VC, pl.Vc + row0 * ROW, b_codes, &bars[s]);
-    if (with_ks) {
-      const size_t kidx = (pgrp0 + kg0) * D;
-      bulk_g2s(st + C::S_KS, pl.Ks + kidx, b_ks, &bars[s]);
-      bulk_g2s(st + C::S_KZ, pl.Kz + kidx, b_ks, &bars[s]);
+    const int ng = ngv < C::KG ? ngv : C::KG;
+    const bool go = c != args.fail_chunk;   // testing: copies that never come
+    if (lane == 0 && go)
+      mbar_expect_tx(&bars[s], 2 * (nvalid * (ROW + NJ * 2) + (with_ks ? ng * D * 2 : 0)));
+    __syncwarp();
+    const bool keymeta = lane == 2 || lane == 3;
+    if (go && lane < 6 && (!keymeta || with_ks)) {
+      const int idx = keymeta ? kg0 : t0;
+      const int cnt = keymeta ? ng : nvalid;
+      bulk_g2s(stage0 + s * C::S_BYTES + psoff, pbase + (size_t)idx * prow, cnt * prow,
+               &bars[s]);
     }
-    bulk_g2s(st + C::S_VS, pl.Vs + row0 * NJ, b_vs, &bars[s]);
-    bulk_g2s(st + C::S_VZ, pl.Vz + row0 * NJ, b_vs, &bars[s]);
   };
-  // the producer's step for the chunk at pc: its copies into stage s
+  // the producer's step for the chunk at pc: its copies into stage s (all
+  // lanes call it)
   auto produce = [&](const Cursor &cu, int s, int c) {
     if (cu.k == 0 || c == lo_c) set_prod_head(cu);
     issue(cu, s, c);
@@ -476,7 +496,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   uint32_t phase = 0;    // bit s = parity to wait for on stage s
   uint32_t pending = 0;  // bit s = copies in flight into stage s
   for (int i = 0; i < ST && i < n_mine; ++i) {
-    if (lane == 0) produce(pc, i, lo_c + i);
+    produce(pc, i, lo_c + i);
     pending |= 1u << i;
     pc.next(geo, tab);
   }
@@ -957,10 +977,9 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     if (head_ends) flush(hd);
     __syncwarp();
     if (i + ST < n_mine) {
-      if (lane == 0) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        produce(pc, s, lo_c + i + ST);
-      }
+      // every lane read the stage: order those reads before the copies
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      produce(pc, s, lo_c + i + ST);
       pending |= 1u << s;
       pc.next(geo, tab);
     }
