@@ -177,9 +177,9 @@ int vq_kivi_quantize(const vq_kivi_params *p, const void *K, const void *V,
   const size_t sz_vmeta = BH * geo.Tcap * (p->D / g) * sizeof(__half);
   const size_t sz_res = BH * geo.Rcap * p->D * sizeof(__half);
   c->use_mma = mma_plan(geo, c->sm_count, &c->plan);
-  // 2-bit caches decoded on the tensor cores keep their codes in the order
-  // the MMA fragments consume them
-  geo.layout = c->use_mma && p->bits == 2 ? kLayoutFrag2 : kLayoutPacked;
+  // 2- and 4-bit caches decoded on the tensor cores keep their codes in the
+  // order the MMA fragments consume them
+  geo.layout = c->use_mma && (p->bits == 2 || p->bits == 4) ? kLayoutFrag : kLayoutPacked;
   size_t n_part = (size_t)p->B * p->H_q * geo.max_items * (p->D + 2);
   if (c->use_mma) {
     const size_t n_mma = mma_part_floats(geo, c->plan);
@@ -465,8 +465,8 @@ int vq_kivi_export(const vq_kivi_cache *c, int which, void *dst,
     default: break;
   }
   cudaError_t e;
-  if ((which == 0 || which == 3) && c->geo.layout == kLayoutFrag2) {
-    e = launch_export_frag2(c->geo, (const uint8_t *)src, which == 3, dst, st);
+  if ((which == 0 || which == 3) && c->geo.layout == kLayoutFrag) {
+    e = launch_export_frag(c->geo, (const uint8_t *)src, which == 3, dst, st);
   } else if (src) {
     e = cudaMemcpyAsync(dst, src, need, cudaMemcpyDeviceToDevice, st);
   } else {

@@ -26,8 +26,10 @@ bool mma_plan(const Geometry &geo, int sm_count, MmaPlan *plan) {
   if (GQp > 4 || (geo.D != 64 && geo.D != 128)) return false;
   mma::KernelInfo ki;
   if (!pick(geo, GQp, &ki)) return false;
-  // the stage count (2..4) that keeps the most warps resident, and among
-  // those the deepest pipeline
+  // the stage count (1..4) that keeps the most warps resident, and among
+  // those the deepest pipeline (one stage per warp still streams: the other
+  // resident warps' copies hide a warp's own copy latency, and for wide
+  // codes it is what lets 12 warps share an SM's shared memory)
   if (cudaFuncSetAttribute((const void *)ki.fn,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            227 * 1024) != cudaSuccess) {
@@ -36,7 +38,7 @@ bool mma_plan(const Geometry &geo, int sm_count, MmaPlan *plan) {
   }
   int best_occ = 0, ST = 0;
   uint32_t smem = 0;
-  for (int st = 2; st <= mma::kMaxStages; ++st) {
+  for (int st = 1; st <= mma::kMaxStages; ++st) {
     const uint32_t sm = kNW * (ki.stage0 + st * ki.stage_bytes);
     if (sm > 227 * 1024) break;
     int occ = 0;

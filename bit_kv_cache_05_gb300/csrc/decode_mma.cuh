@@ -185,8 +185,8 @@ __device__ __forceinline__ void load_halves(const __half *p, float (&out)[NJ]) {
 // 4tig+3 of the K-step, slot e (0..3) being channel 4tig + off(e).  The code
 // of channel c arrives scaled by 2^(oexp(c) - 24); the score B operand
 // carries 2^-oexp(c) (folded into a copy of q'), so every product carries
-// exactly 2^-24.  4- and 8-bit codes use the packed order (a uint4 of a token
-// row holds WPQ K-steps, bytes permuted into place); 2-bit codes use the
+// exactly 2^-24.  8-bit codes use the packed order (a uint4 of a token row
+// holds WPQ K-steps, bytes permuted into place); 2- and 4-bit codes use the
 // fragment order, where masks alone place the codes.
 //
 // Value A fragment (rows = channels 2gid, 2gid+1 of an m16 tile, K = tokens
@@ -194,27 +194,33 @@ __device__ __forceinline__ void load_halves(const __half *p, float (&out)[NJ]) {
 // two tokens' words (vsel) and masks channel 2gid (vmask0) and 2gid+1
 // (vmask1), whose codes arrive scaled by 2^(vpos0 - 24) and 2^(vpos1 - 24);
 // a uint4 of a token row covers VTPQ m16 tiles, tile u of it uses word
-// vword(x, u, gid).  In the 2-bit fragment order the two tokens of a
-// register share a word and masks alone place them.  The output rows are
-// scaled back at the end.
+// vword(x, u, gid).  In the fragment order (2- and 4-bit codes) the two
+// tokens of a register share a word and masks alone place them.  The output
+// rows are scaled back at the end.
 template <int BITS> struct Layout;
 
-template <> struct Layout<2> {
-  // codes in kLayoutFrag2 order: a 32-bit word holds 16 fields, field r of
-  // each half at bits 2r (low half) and 16 + 2r (high half).  Fields 0..4
-  // are masked in place (exponent 2r); fields 5..7 are masked after one
-  // shift of the word by 6 (exponent 2r - 6): a field at bit p of a half is
-  // the fp16 subnormal code * 2^(p - 24).
+// Codes in kLayoutFrag order (2- and 4-bit): a 32-bit word holds two
+// halves of 16/B fields, field r at bits B*r of each half.  Fields whose
+// bits lie within 0..9 of the half (r < DIRECT) are masked in place
+// (exponent B*r); the rest are masked after one shift of the word by SHIFT
+// (exponent B*r - SHIFT): a field at bit p of a half is the fp16 subnormal
+// code * 2^(p - 24).  A word covers KPW = 8/B K-steps (keys) or m16 tiles
+// (values).  Score slot e of channel c (K-step ks = c/16, lane group
+// (c/4) mod 4, e = c mod 4) is field 2 (ks mod KPW) + e/2 of half e mod 2.
+template <int B, int DIRECT_, int SHIFT_>
+struct FragLayout {
   static constexpr bool FRAG = true;
-  static __host__ __device__ constexpr int fexp(int r) { return r < 5 ? 2 * r : 2 * r - 6; }
-  static __device__ __forceinline__ uint32_t field(uint32_t w, uint32_t w6, int r) {
-    return r < 5 ? (w & (0x00030003u << (2 * r))) : (w6 & (0x00030003u << (2 * r - 6)));
+  static constexpr int KPW = 8 / B, DIRECT = DIRECT_, SHIFT = SHIFT_;
+  static constexpr uint32_t M = ((1u << B) - 1u) * 0x00010001u;
+  static __host__ __device__ constexpr int fexp(int r) {
+    return r < DIRECT ? B * r : B * r - SHIFT;
   }
-  // score slot e of channel c (K-step c/16, lane group (c/4) mod 4, e = c
-  // mod 4) is field 2 (ks mod 4) + e/2 of half e mod 2
+  static __device__ __forceinline__ uint32_t field(uint32_t w, uint32_t ws, int r) {
+    return r < DIRECT ? (w & (M << (B * r))) : (ws & (M << (B * r - SHIFT)));
+  }
   static __host__ __device__ constexpr int off(int e) { return e; }
   static __device__ __forceinline__ int oexp(int c) {
-    return fexp(2 * ((c >> 4) & 3) + ((c & 3) >> 1));
+    return fexp(2 * ((c >> 4) % KPW) + ((c & 3) >> 1));
   }
   static __device__ __forceinline__ uint32_t score_sel(int) { return 0u; }
   static __device__ __forceinline__ uint32_t vsel(int) { return 0u; }
@@ -222,43 +228,8 @@ template <> struct Layout<2> {
   static __device__ __forceinline__ int vpos1(int) { return 0; }
 };
 
-template <> struct Layout<4> {
-  static constexpr int WPQ = 2;
-  static constexpr int VTPQ = 2;
-  // channels 4tig..4tig+3 are bytes B0 = 2(tig&1) and B0+1 of word
-  // 2ks + tig/2; one byte_perm picks the word and places B0 at bytes 0-1 and
-  // B0+1 at bytes 2-3
-  static __device__ __forceinline__ uint32_t score_sel(int tig) {
-    const uint32_t b = 2 * (tig & 1) + 4 * (tig >> 1);
-    return b | (b << 4) | ((b + 1) << 8) | ((b + 1) << 12);
-  }
-  static __device__ __forceinline__ void score_a(const uint4 &q, int ks,
-                                                 uint32_t sel, uint32_t &lo,
-                                                 uint32_t &hi) {
-    const uint32_t x = __byte_perm((&q.x)[2 * (ks & 1)], (&q.x)[2 * (ks & 1) + 1], sel);
-    lo = x & 0x000F000Fu;   // channel 4tig (x1), 4tig+2 (x1)
-    hi = x & 0x00F000F0u;   // channel 4tig+1 (x16), 4tig+3 (x16)
-  }
-  static __host__ __device__ constexpr int off(int e) { return (e & 1) * 2 + (e >> 1); }
-  static __host__ __device__ constexpr int sexp(int e) { return 4 * (e >> 1); }
-  static constexpr bool FRAG = false;
-  static __device__ __forceinline__ int oexp(int c) { return 4 * (c & 1); }
-  static __device__ __forceinline__ uint32_t vword(const uint4 &x, int u, int gid) {
-    const uint32_t w0 = u ? x.z : x.x, w1 = u ? x.w : x.y;
-    return (gid >> 2) ? w1 : w0;   // word 2u + gid/4
-  }
-  static __device__ __forceinline__ uint32_t vsel(int gid) {
-    const uint32_t b = gid & 3;
-    return b | (b << 4) | ((4 + b) << 8) | ((4 + b) << 12);
-  }
-  static __device__ __forceinline__ int vpos0(int) { return 0; }
-  static __device__ __forceinline__ int vpos1(int) { return 4; }
-  static __device__ __forceinline__ void value_a(uint32_t x, int,
-                                                 uint32_t &r0, uint32_t &r1) {
-    r0 = x & 0x000F000Fu;
-    r1 = x & 0x00F000F0u;
-  }
-};
+template <> struct Layout<2> : FragLayout<2, 5, 6> {};
+template <> struct Layout<4> : FragLayout<4, 2, 8> {};
 
 template <> struct Layout<8> {
   static constexpr int WPQ = 1;    // uint4 = one K-step (4 words, one per tig)
@@ -648,8 +619,8 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
         // 2^(p - 24) for the code's bit position p
         float sa = rs0, sb = rs1;
         if constexpr (L::FRAG) {
-          sa = exp2i(24 - L::fexp(2 * (mv & 3)));
-          sb = exp2i(24 - L::fexp(2 * (mv & 3) + 1));
+          sa = exp2i(24 - L::fexp(2 * (mv % L::KPW)));
+          sb = exp2i(24 - L::fexp(2 * (mv % L::KPW) + 1));
         }
         const float o0 = (O[mv][0] + O[mv][1]) * sa + Zt[j];
         const float o1 = (O[mv][2] + O[mv][3]) * sb + Zt[j];
@@ -687,10 +658,10 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     auto score_tiles = [&](auto t0_tag, auto nt_tag, float (&acc)[2][4]) {
       constexpr int T0 = decltype(t0_tag)::value, NT = decltype(nt_tag)::value;
       if constexpr (L::FRAG) {
-        // fragment order: lane group tig's D/64 words of a token row are
-        // contiguous; word hw holds K-steps 4hw ... 4hw+3
-        constexpr int NH = D / 64;
-        using RowW = std::conditional_t<NH == 2, uint2, uint32_t>;
+        // fragment order: lane group tig's NH words of a token row are
+        // contiguous; word hw holds K-steps KPW hw ... KPW hw + KPW - 1
+        constexpr int NH = D * C::BITS / 128, KPW = L::KPW;
+        using RowW = std::conditional_t<NH == 4, uint4, std::conditional_t<NH == 2, uint2, uint32_t>>;
         RowW r0[NT], r1[NT];
 #pragma unroll
         for (int m = 0; m < NT; ++m) {
@@ -703,19 +674,19 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
           uint32_t w0[NT], w1[NT], s0[NT], s1[NT];
 #pragma unroll
           for (int m = 0; m < NT; ++m) {
-            if constexpr (NH == 2) {
-              w0[m] = hw ? r0[m].y : r0[m].x;
-              w1[m] = hw ? r1[m].y : r1[m].x;
-            } else {
+            if constexpr (NH == 1) {
               w0[m] = r0[m];
               w1[m] = r1[m];
+            } else {
+              w0[m] = reinterpret_cast<const uint32_t *>(&r0[m])[hw];
+              w1[m] = reinterpret_cast<const uint32_t *>(&r1[m])[hw];
             }
-            s0[m] = w0[m] >> 6;
-            s1[m] = w1[m] >> 6;
+            s0[m] = w0[m] >> L::SHIFT;
+            s1[m] = w1[m] >> L::SHIFT;
           }
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const int ks = 4 * hw + kk;
+          for (int kk = 0; kk < KPW; ++kk) {
+            const int ks = KPW * hw + kk;
 #pragma unroll
             for (int m = 0; m < NT; ++m) {
               if (FULL || T0 + m < nmt) {
@@ -883,27 +854,27 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
       }
       if constexpr (L::FRAG) {
         // fragment order: pair (ta, ta+4) is pair tig of block kt, pair
-        // (ta+8, ta+12) pair 4+tig; lane gid's D/64 words of a pair are
-        // contiguous, word hw covering tiles 4hw ... 4hw+3
-        constexpr int NV = D / 64;
-        using PairW = std::conditional_t<NV == 2, uint2, uint32_t>;
+        // (ta+8, ta+12) pair 4+tig; lane gid's NV words of a pair are
+        // contiguous, word hw covering tiles KPW hw ... KPW hw + KPW - 1
+        constexpr int NV = D * C::BITS / 128, KPW = L::KPW;
+        using PairW = std::conditional_t<NV == 4, uint4, std::conditional_t<NV == 2, uint2, uint32_t>>;
         const unsigned char *blk = st + C::S_VC + kt * 16 * ROW;
         const PairW pa = *reinterpret_cast<const PairW *>(blk + (8 * tig + gid) * 4 * NV);
         const PairW pb = *reinterpret_cast<const PairW *>(blk + (8 * (4 + tig) + gid) * 4 * NV);
 #pragma unroll
         for (int hw = 0; hw < NV; ++hw) {
           uint32_t wa, wb;
-          if constexpr (NV == 2) {
-            wa = hw ? pa.y : pa.x;
-            wb = hw ? pb.y : pb.x;
-          } else {
+          if constexpr (NV == 1) {
             wa = pa;
             wb = pb;
+          } else {
+            wa = reinterpret_cast<const uint32_t *>(&pa)[hw];
+            wb = reinterpret_cast<const uint32_t *>(&pb)[hw];
           }
-          const uint32_t sa = wa >> 6, sb = wb >> 6;
+          const uint32_t sa = wa >> L::SHIFT, sb = wb >> L::SHIFT;
 #pragma unroll
-          for (int mm = 0; mm < 4; ++mm) {
-            const int mv = 4 * hw + mm;
+          for (int mm = 0; mm < KPW; ++mm) {
+            const int mv = KPW * hw + mm;
             const int vb = (((16 * mv) / G) * GQP) >> 2;
             mma16816(O[mv], L::field(wa, sa, 2 * mm), L::field(wa, sa, 2 * mm + 1),
                      L::field(wb, sb, 2 * mm), L::field(wb, sb, 2 * mm + 1),

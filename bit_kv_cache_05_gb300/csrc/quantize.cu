@@ -111,42 +111,46 @@ __device__ __forceinline__ void store_packed_tile(const uint8_t *codes, int g,
   }
 }
 
-// The g x D code tile in kLayoutFrag2 order (2-bit codes): one thread per
-// 32-bit word, whose 16 fields are gathered from the tile.
-__device__ __forceinline__ void store_frag2_keys(const uint8_t *codes, int g,
-                                                 int D, uint8_t *dst) {
-  const int wpr = D / 16, nh = D / 64;
+// The g x D code tile in kLayoutFrag order (2- or 4-bit codes): one thread
+// per 32-bit word, whose fields are gathered from the tile.
+template <int BITS>
+__device__ __forceinline__ void store_frag_keys(const uint8_t *codes, int g,
+                                                int D, uint8_t *dst) {
+  constexpr int F = 16 / BITS, KPW = 8 / BITS;   // fields per half
+  const int wpr = D * BITS / 32, nw = D * BITS / 128;
   for (int w = threadIdx.x; w < g * wpr; w += blockDim.x) {
     const int i = w / wpr, wi = w - i * wpr;
-    const int tig = wi / nh, hw = wi - tig * nh;
+    const int tig = wi / nw, hw = wi - tig * nw;
     uint32_t acc = 0;
 #pragma unroll
     for (int s = 0; s < 2; ++s)
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const int ks = 4 * hw + (r >> 1), e = 2 * (r & 1) + s;
-        acc |= (uint32_t)codes[i * D + 16 * ks + 4 * tig + e] << (16 * s + 2 * r);
+      for (int r = 0; r < F; ++r) {
+        const int ks = KPW * hw + (r >> 1), e = 2 * (r & 1) + s;
+        acc |= (uint32_t)codes[i * D + 16 * ks + 4 * tig + e] << (16 * s + BITS * r);
       }
     reinterpret_cast<uint32_t *>(dst)[w] = acc;
   }
 }
 
-__device__ __forceinline__ void store_frag2_values(const uint8_t *codes, int g,
-                                                   int D, uint8_t *dst) {
-  const int nv = D / 64;
-  for (int w = threadIdx.x; w < g * D / 16; w += blockDim.x) {
-    const int kb = w / D, wb = w - kb * D;
-    const int pi = wb / (8 * nv), rem = wb - pi * 8 * nv;
-    const int j = rem / nv, hw = rem - j * nv;
+template <int BITS>
+__device__ __forceinline__ void store_frag_values(const uint8_t *codes, int g,
+                                                  int D, uint8_t *dst) {
+  constexpr int F = 16 / BITS, KPW = 8 / BITS;
+  const int nw = D * BITS / 128, wpb = D * BITS / 2;   // words per block
+  for (int w = threadIdx.x; w < g * D * BITS / 32; w += blockDim.x) {
+    const int kb = w / wpb, wb = w - kb * wpb;
+    const int pi = wb / (8 * nw), rem = wb - pi * 8 * nw;
+    const int j = rem / nw, hw = rem - j * nw;
     const int tA = 16 * kb + (pi < 4 ? pi : pi + 4);
     uint32_t acc = 0;
 #pragma unroll
     for (int s = 0; s < 2; ++s)
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const int mv = 4 * hw + (r >> 1), rho = r & 1;
+      for (int r = 0; r < F; ++r) {
+        const int mv = KPW * hw + (r >> 1), rho = r & 1;
         acc |= (uint32_t)codes[(tA + 4 * s) * D + 16 * mv + 2 * j + rho]
-               << (16 * s + 2 * r);
+               << (16 * s + BITS * r);
       }
     reinterpret_cast<uint32_t *>(dst)[w] = acc;
   }
@@ -221,8 +225,8 @@ k_flush(Geometry geo, Planes pl, const __half *__restrict__ Kin,
                                                   mn, scale, rcp, levels);
   }
   __syncthreads();
-  if (BITS == 2 && geo.layout == kLayoutFrag2)
-    store_frag2_keys(codes, g, D, pl.Kc + (bh * geo.Tcap + P0) * geo.row);
+  if ((BITS == 2 || BITS == 4) && geo.layout == kLayoutFrag)
+    store_frag_keys<BITS>(codes, g, D, pl.Kc + (bh * geo.Tcap + P0) * geo.row);
   else
     store_packed_tile<BITS>(codes, g, D, pl.Kc + (bh * geo.Tcap + P0) * geo.row);
   __syncthreads();
@@ -253,8 +257,8 @@ k_flush(Geometry geo, Planes pl, const __half *__restrict__ Kin,
     }
   }
   __syncthreads();
-  if (BITS == 2 && geo.layout == kLayoutFrag2)
-    store_frag2_values(codes, g, D, pl.Vc + (bh * geo.Tcap + P0) * geo.row);
+  if ((BITS == 2 || BITS == 4) && geo.layout == kLayoutFrag)
+    store_frag_values<BITS>(codes, g, D, pl.Vc + (bh * geo.Tcap + P0) * geo.row);
   else
     store_packed_tile<BITS>(codes, g, D, pl.Vc + (bh * geo.Tcap + P0) * geo.row);
 }
@@ -354,36 +358,36 @@ cudaError_t launch_tail(const Geometry &geo, const Planes &pl,
   return e;
 }
 
-// kLayoutFrag2 plane -> packed order: one thread per packed 32-bit word
-// (16 codes of one token row), each field gathered from its fragment-order
-// position.  Covers all Tcap rows of every (b, h).
-__global__ void k_export_frag2(Geometry geo, const uint8_t *__restrict__ src,
-                               bool values, uint32_t *__restrict__ dst) {
-  const int D = geo.D, wpr = D / 16;
+// kLayoutFrag plane -> packed order: one thread per packed 32-bit word
+// (32/b codes of one token row), each field gathered from its
+// fragment-order position.  Covers all Tcap rows of every (b, h).
+__global__ void k_export_frag(Geometry geo, const uint8_t *__restrict__ src,
+                              bool values, uint32_t *__restrict__ dst) {
+  const int D = geo.D, b = geo.bits, cpw = 32 / b, wpr = D * b / 32;
+  const uint32_t mask = (1u << b) - 1u;
   const size_t total = (size_t)geo.B * geo.H_kv * geo.Tcap * wpr;
   for (size_t w = blockIdx.x * (size_t)blockDim.x + threadIdx.x; w < total;
        w += (size_t)gridDim.x * blockDim.x) {
     const size_t row = w / wpr;                 // (b, h, t)
-    const int w16 = (int)(w - row * wpr);
+    const int wr = (int)(w - row * wpr);
     const int t = (int)(row % geo.Tcap);
     const uint32_t *rw = reinterpret_cast<const uint32_t *>(src) + row * wpr;
     const uint32_t *blk = reinterpret_cast<const uint32_t *>(src) +
                           (row - (t & 15)) * wpr;   // the token's 16-row block
     uint32_t acc = 0;
-#pragma unroll 4
-    for (int f = 0; f < 16; ++f) {
-      const int c = 16 * w16 + f;
-      const FragPos pos = values ? frag2_value(D, t & 15, c) : frag2_key(D, c);
+    for (int f = 0; f < cpw; ++f) {
+      const int c = cpw * wr + f;
+      const FragPos pos = values ? frag_value(D, b, t & 15, c) : frag_key(D, b, c);
       const uint32_t word = values ? blk[pos.word] : rw[pos.word];
-      acc |= ((word >> pos.bit) & 3u) << (2 * f);
+      acc |= ((word >> pos.bit) & mask) << (b * f);
     }
     dst[w] = acc;
   }
 }
 
-cudaError_t launch_export_frag2(const Geometry &geo, const uint8_t *src,
-                                bool values, void *dst, cudaStream_t st) {
-  k_export_frag2<<<1024, 256, 0, st>>>(geo, src, values, (uint32_t *)dst);
+cudaError_t launch_export_frag(const Geometry &geo, const uint8_t *src,
+                               bool values, void *dst, cudaStream_t st) {
+  k_export_frag<<<1024, 256, 0, st>>>(geo, src, values, (uint32_t *)dst);
   count_launch();
   return cudaGetLastError();
 }

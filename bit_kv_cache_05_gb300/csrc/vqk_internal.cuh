@@ -27,7 +27,7 @@ struct Planes {
 
 // orders of the code planes (see "code-plane orders" below)
 constexpr int kLayoutPacked = 0;
-constexpr int kLayoutFrag2 = 1;
+constexpr int kLayoutFrag = 1;
 
 struct Geometry {
   int B, H_q, H_kv, D, bits, g, R;
@@ -42,35 +42,39 @@ struct Geometry {
 //
 // kLayoutPacked: the method's packing, code of channel c of a token row at
 // byte c*b/8, bit (c*b) mod 8 (LSB first); every export uses this order.
-// kLayoutFrag2: 2-bit codes of a cache decoded on the tensor cores, in the
-// order the decode kernel's MMA fragments consume them (same bytes per row
-// and per 16-token block, permuted so that one and-mask per register yields
-// two codes in place; no byte permutes):
-//  keys, per token row of D/16 32-bit words: channel c = 16 ks + 4 tig + e
-//    sits in word (D/64) tig + ks/4, half e mod 2, field r = 2 (ks mod 4) +
-//    e/2 (bits 16 (e mod 2) + 2 r);
-//  values, per 16-token block of D 32-bit words: the block's tokens pair up
-//    as (tl, tl + 4), tl in {0..3, 8..11}, pair index pi = tl (tl < 4) or
+// kLayoutFrag: 2- and 4-bit codes of a cache decoded on the tensor cores, in
+// the order the decode kernel's MMA fragments consume them (same bytes per
+// row and per 16-token block, permuted so that one and-mask per register,
+// after at most one shift of the word, yields two codes in place).  A 32-bit
+// word has two 16-bit halves of 16/b fields each; field r of a half sits at
+// bits 16*half + b*r.  With KPW = 8/b (K-steps, or value tiles, per word) and
+// NW = D*b/128 (words per lane group):
+//  keys, per token row of D*b/32 words: channel c = 16 ks + 4 tig + e sits
+//    in word NW tig + ks/KPW, half e mod 2, field 2 (ks mod KPW) + e/2;
+//  values, per 16-token block of D*b/2 words: the block's tokens pair up as
+//    (tl, tl + 4), tl in {0..3, 8..11}, pair index pi = tl (tl < 4) or
 //    tl - 4; channel c = 16 mv + 2 j + rho of both tokens of pair pi sits in
-//    word (8 pi + j) (D/64) + mv/4, field r = 2 (mv mod 4) + rho, the first
+//    word (8 pi + j) NW + mv/KPW, field 2 (mv mod KPW) + rho, the first
 //    token in the low half, the second in the high half.
 struct FragPos {
   int word;   // 32-bit word within the token row (keys) or block (values)
-  int bit;    // position of the 2-bit field in that word
+  int bit;    // position of the field in that word
 };
 
-__host__ __device__ inline FragPos frag2_key(int D, int c) {
+__host__ __device__ inline FragPos frag_key(int D, int b, int c) {
+  const int kpw = 8 / b, nw = D * b / 128;
   const int ks = c >> 4, tig = (c >> 2) & 3, e = c & 3;
-  const int r = 2 * (ks & 3) + (e >> 1);
-  return FragPos{(D / 64) * tig + (ks >> 2), 16 * (e & 1) + 2 * r};
+  const int r = 2 * (ks % kpw) + (e >> 1);
+  return FragPos{nw * tig + ks / kpw, 16 * (e & 1) + b * r};
 }
 
 // tl: token within its 16-token block
-__host__ __device__ inline FragPos frag2_value(int D, int tl, int c) {
+__host__ __device__ inline FragPos frag_value(int D, int b, int tl, int c) {
+  const int kpw = 8 / b, nw = D * b / 128;
   const int u = tl & 7, s = u >> 2, pi = 4 * (tl >> 3) + (u & 3);
   const int mv = c >> 4, j = (c & 15) >> 1, rho = c & 1;
-  const int r = 2 * (mv & 3) + rho;
-  return FragPos{(8 * pi + j) * (D / 64) + (mv >> 2), 16 * s + 2 * r};
+  const int r = 2 * (mv % kpw) + rho;
+  return FragPos{(8 * pi + j) * nw + mv / kpw, 16 * s + b * r};
 }
 
 // ---- quantize / flush ------------------------------------------------------
@@ -103,10 +107,10 @@ cudaError_t launch_tail(const Geometry &geo, const Planes &pl,
                         const __half *Kin, const __half *Vin,
                         int64_t in_stride, const TailTable &tab,
                         int total_tokens, cudaStream_t st);
-// code plane 0 (keys) or 3 (values) of a kLayoutFrag2 cache, converted to
+// code plane 0 (keys) or 3 (values) of a kLayoutFrag cache, converted to
 // the packed order, into dst
-cudaError_t launch_export_frag2(const Geometry &geo, const uint8_t *src,
-                                bool values, void *dst, cudaStream_t st);
+cudaError_t launch_export_frag(const Geometry &geo, const uint8_t *src,
+                               bool values, void *dst, cudaStream_t st);
 cudaError_t launch_export_residual(const Geometry &geo, const Planes &pl,
                                    int which, void *dst, const int32_t *Tq,
                                    const int32_t *nres, cudaStream_t st);
