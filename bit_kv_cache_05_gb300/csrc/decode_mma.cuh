@@ -990,6 +990,11 @@ k_merge_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   constexpr int CPL = D / 32;
   __shared__ float sm_m[kMergeWarps][GQP], sm_l[kMergeWarps][GQP];
   __shared__ float sm_o[kMergeWarps][GQP][32];
+  // let the stream's next kernel launch now: whatever it writes that this
+  // kernel reads (the residual ring for an append, the partials for a
+  // decode) it writes only after its own griddepcontrol.wait, which waits
+  // for this grid to complete
+  asm volatile("griddepcontrol.launch_dependents;");
   const int b = blockIdx.x / geo.H_kv, h = blockIdx.x - b * geo.H_kv;
   const int nq = tab.nq[b], nres = tab.nres[b];
   if (nq == 0 && nres == 0) return;   // no tokens: the launcher zeroed it
