@@ -29,7 +29,7 @@ bool mma_plan(const Geometry &geo, int sm_count, MmaPlan *plan) {
   // the stage count (1..4) that keeps the most warps resident, and among
   // those the deepest pipeline (one stage per warp still streams: the other
   // resident warps' copies hide a warp's own copy latency, and for wide
-  // codes it is what lets 12 warps share an SM's shared memory)
+  // codes it is what lets 16 warps share an SM's shared memory)
   if (cudaFuncSetAttribute((const void *)ki.fn,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            227 * 1024) != cudaSuccess) {

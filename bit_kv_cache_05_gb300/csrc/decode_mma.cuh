@@ -44,8 +44,12 @@ namespace vqk {
 namespace mma {
 
 constexpr int kC = 64;          // tokens per chunk (4 m16 tiles)
-constexpr int kNW = 4;          // warps per CTA
-constexpr int kMinBlocks = 3;   // CTAs per SM the register budget allows
+// One warp per CTA: everything a warp computes about its chunks (cursor,
+// stage and plane addresses, branch conditions) then derives from blockIdx
+// and the kernel arguments alone, so the compiler keeps it in uniform
+// registers and branches on it without divergence handling, and the bulk
+// copies take their addresses from uniform registers directly.
+constexpr int kNW = 1;          // warps per CTA
 constexpr int kMaxStages = 4;
 // a partial (o[D], m, l) per (warp segment, query head), padded to D + 4
 // floats so that the o rows stay 16-byte aligned
@@ -269,6 +273,11 @@ template <> struct Layout<8> {
 template <int D_, int BITS_, int GQP_, int G_>
 struct Cfg {
   static constexpr int D = D_, BITS = BITS_, GQP = GQP_, G = G_;
+  // CTAs per SM the register budget is cut for: 4-bit stages (10.75 KB at
+  // D = 128) allow one stage per warp only, so those kernels take more
+  // warps (16, at most 128 registers) in place of a deeper pipeline; the
+  // others keep 12-14 warps with two stages each
+  static constexpr int MINB = BITS == 4 && G >= 32 ? 16 : 12;
   static constexpr int KS = D / 16;            // score K-steps = value m16 tiles
   static constexpr int NJ = D / G;             // value groups per row
   static constexpr int WG = 4 / GQP;           // key groups per score window
@@ -363,7 +372,7 @@ struct Cursor {
 };
 
 template <class C>
-__global__ void __launch_bounds__(kNW * 32, kMinBlocks)
+__global__ void __launch_bounds__(kNW * 32, C::MINB)
 k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   using L = Layout<C::BITS>;
   constexpr int D = C::D, KS = C::KS, NJ = C::NJ, GQP = C::GQP, WG = C::WG;
@@ -378,9 +387,10 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   // each warp's first copies are issued before the wait.  The merge kernel
   // is released only after the wait (it reads the residual ring early).
   if (!args.early) asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  static_assert(kNW == 1, "one warp per CTA");
+  const int lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
-  const int wg = blockIdx.x * kNW + warp;
+  const int wg = blockIdx.x;
   if (wg >= args.W) return;
   const int64_t N = args.N, W = args.W;
   const int lo_c = (int)(wg * N / W), hi_c = (int)((wg + 1) * N / W);
@@ -388,7 +398,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   if (n_mine <= 0) return;
   const int ST = args.ST, GQ = args.GQ;
 
-  unsigned char *ws = smem + warp * C::warp_bytes(ST);
+  unsigned char *ws = smem;
   uint64_t *bars = reinterpret_cast<uint64_t *>(ws);
   float *qb = reinterpret_cast<float *>(ws + C::W_QF);      // [GQP][D], slot-scaled
   float *qn = reinterpret_cast<float *>(ws + C::W_QN);      // [GQP][D]
@@ -400,40 +410,24 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   }
   __syncwarp();
 
-  // ---- producer: lane 0 issues the bulk copies of the chunk at `cu` -----
-  // The key scale/zero rows are copied only where a score window starts or
-  // the warp's range starts: every other chunk reuses the operand built
-  // from an earlier stage.
-  // ---- producer: a chunk's copies (key codes, value codes, the key scale /
-  // zero rows where a score window or the warp's range starts, value scale
-  // / zero rows) go out from lanes 0..5 at once, lane j holding plane j's
-  // base for the producer's head; lane 0 first posts the stage's
+  // ---- producer: lane 0 issues a chunk's bulk copies (key codes, value
+  // codes, the key scale / zero rows where a score window or the warp's
+  // range starts, value scale / zero rows) after posting the stage's
   // transaction bytes.  The key scale / zero rows are copied only where a
   // window or the range starts: every other chunk reuses the operand built
-  // from an earlier stage.
-  uint32_t prow = 0, psoff = 0;           // bytes per token (per key group
-                                          // for lanes 2, 3); stage offset
-  switch (lane) {
-    case 0: prow = ROW; psoff = C::S_KC; break;
-    case 1: prow = ROW; psoff = C::S_VC; break;
-    case 2: prow = D * 2; psoff = C::S_KS; break;
-    case 3: prow = D * 2; psoff = C::S_KZ; break;
-    case 4: prow = NJ * 2; psoff = C::S_VS; break;
-    case 5: prow = NJ * 2; psoff = C::S_VZ; break;
-    default: break;
-  }
-  const unsigned char *pbase = nullptr;   // plane base of the producer's head
+  // from an earlier stage.  The plane bases of the producer's head are
+  // warp-uniform.
+  const unsigned char *pb_kc = nullptr, *pb_vc = nullptr, *pb_ks = nullptr,
+                      *pb_kz = nullptr, *pb_vs = nullptr, *pb_vz = nullptr;
   auto set_prod_head = [&](const Cursor &cu) {
     const size_t hd = (size_t)cu.b * geo.H_kv + cu.h;
     const size_t r0 = hd * geo.Tcap, g0 = hd * (geo.Tcap / G);
-    const unsigned char *b = nullptr;
-    if (lane == 0) b = pl.Kc + r0 * ROW;
-    if (lane == 1) b = pl.Vc + r0 * ROW;
-    if (lane == 2) b = reinterpret_cast<const unsigned char *>(pl.Ks + g0 * D);
-    if (lane == 3) b = reinterpret_cast<const unsigned char *>(pl.Kz + g0 * D);
-    if (lane == 4) b = reinterpret_cast<const unsigned char *>(pl.Vs + r0 * NJ);
-    if (lane == 5) b = reinterpret_cast<const unsigned char *>(pl.Vz + r0 * NJ);
-    pbase = b;
+    pb_kc = pl.Kc + r0 * ROW;
+    pb_vc = pl.Vc + r0 * ROW;
+    pb_ks = reinterpret_cast<const unsigned char *>(pl.Ks + g0 * D);
+    pb_kz = reinterpret_cast<const unsigned char *>(pl.Kz + g0 * D);
+    pb_vs = reinterpret_cast<const unsigned char *>(pl.Vs + r0 * NJ);
+    pb_vz = reinterpret_cast<const unsigned char *>(pl.Vz + r0 * NJ);
   };
   auto issue = [&](const Cursor &cu, int s, int c) {
     const int t0 = cu.k * kC;
@@ -444,16 +438,19 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     const int ngv = cu.Tq / G - kg0;
     const int ng = ngv < C::KG ? ngv : C::KG;
     const bool go = c != args.fail_chunk;   // testing: copies that never come
-    if (lane == 0 && go)
+    unsigned char *sb = stage0 + s * C::S_BYTES;
+    if (lane == 0 && go) {
       mbar_expect_tx(&bars[s], 2 * (nvalid * (ROW + NJ * 2) + (with_ks ? ng * D * 2 : 0)));
-    __syncwarp();
-    const bool keymeta = lane == 2 || lane == 3;
-    if (go && lane < 6 && (!keymeta || with_ks)) {
-      const int idx = keymeta ? kg0 : t0;
-      const int cnt = keymeta ? ng : nvalid;
-      bulk_g2s(stage0 + s * C::S_BYTES + psoff, pbase + (size_t)idx * prow, cnt * prow,
-               &bars[s]);
+      bulk_g2s(sb + C::S_KC, pb_kc + (size_t)t0 * ROW, nvalid * ROW, &bars[s]);
+      bulk_g2s(sb + C::S_VC, pb_vc + (size_t)t0 * ROW, nvalid * ROW, &bars[s]);
+      if (with_ks) {
+        bulk_g2s(sb + C::S_KS, pb_ks + (size_t)kg0 * D * 2, ng * D * 2, &bars[s]);
+        bulk_g2s(sb + C::S_KZ, pb_kz + (size_t)kg0 * D * 2, ng * D * 2, &bars[s]);
+      }
+      bulk_g2s(sb + C::S_VS, pb_vs + (size_t)t0 * NJ * 2, nvalid * NJ * 2, &bars[s]);
+      bulk_g2s(sb + C::S_VZ, pb_vz + (size_t)t0 * NJ * 2, nvalid * NJ * 2, &bars[s]);
     }
+    __syncwarp();
   };
   // the producer's step for the chunk at pc: its copies into stage s (all
   // lanes call it)
