@@ -485,7 +485,14 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
 
   // ---- running state of the current head segment ---------------------------
   float O[KS][4];
-  float Z[NJ];
+  // zero-point sums sum_t p_t z_t,j.  With one query head per kv head they
+  // are taken in the value B layout (ZB), where every lane holds the p of
+  // its tokens: Z[vb] covers column pair pair_b of value block vb over the
+  // lane's tokens.  Otherwise in the score layout: Z[j] of head h_s, group
+  // j over the lane's score rows.
+  constexpr bool ZB = GQP == 1;
+  constexpr int NZ = ZB ? C::NVB : NJ;
+  float Z[NZ];
   float m_run = -INFINITY, l_run = 0.f;
   uint32_t Bs[KS][2];
   float beta_t = 0.f;    // zero-point term of pair tig, current window
@@ -498,7 +505,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
 #pragma unroll
       for (int r = 0; r < 4; ++r) O[mv][r] = 0.f;
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) Z[j] = 0.f;
+    for (int j = 0; j < NZ; ++j) Z[j] = 0.f;
     m_run = -INFINITY;
     l_run = 0.f;
     cur_w = -1;
@@ -602,8 +609,27 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   auto flush = [&](int hd) {
     float Lsum = head_reduce<GQP>(l_run, AddOp());
     float Zt[NJ];
+    if constexpr (ZB) {
+      // pair tig of block vb is (head h_s, group (4 vb + tig) / GQP): sum
+      // over the lanes of column pair p (gid = 2p, 2p+1, every tig), then
+      // take pair tig's sum from lane 8 tig
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) Zt[j] = head_reduce<GQP>(Z[j], AddOp());
+      for (int j = 0; j < NJ; ++j) Zt[j] = 0.f;
+#pragma unroll
+      for (int vb = 0; vb < C::NVB; ++vb) {
+        float r = Z[vb];
+        r += __shfl_xor_sync(kFull, r, 1);
+        r += __shfl_xor_sync(kFull, r, 2);
+        r += __shfl_xor_sync(kFull, r, 4);
+        r = __shfl_sync(kFull, r, 8 * tig);
+#pragma unroll
+        for (int j = 0; j < NJ; ++j)
+          if (((j * GQP) >> 2) == vb) Zt[j] = r;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) Zt[j] = head_reduce<GQP>(Z[j], AddOp());
+    }
     if (h_s < GQ) {
       float *dst = args.part + ((size_t)(wg + hd) * GQP + h_s) * part_stride<D>();
 #pragma unroll
@@ -782,7 +808,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
           O[mv][0] = o01.x; O[mv][1] = o01.y; O[mv][2] = o23.x; O[mv][3] = o23.y;
         }
 #pragma unroll
-        for (int j = 0; j < NJ; ++j) Z[j] *= alpha;
+        for (int j = 0; j < NZ; ++j) Z[j] *= alpha;
       }
 #pragma unroll
       for (int mt = 2 * H; mt < 2 * H + 2; ++mt)
@@ -798,22 +824,6 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     auto values_kt = [&](auto kt_tag) {
       constexpr int kt = decltype(kt_tag)::value;
       if (!FULL && kt >= nmt) return;
-      // zero-point term in the score layout (tokens gid, gid+8)
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        float vz[NJ];
-        load_halves<NJ>(Vz + (16 * kt + gid + 8 * r) * NJ, vz);
-        if constexpr (NJ == 1) {
-          Z[0] = fmaf(p[kt][r], vz[0], Z[0]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < NJ; j += 2) {
-            const float2 z = __ffma2_rn(f2(p[kt][r], p[kt][r]), f2(vz[j], vz[j + 1]),
-                                        f2(Z[j], Z[j + 1]));
-            Z[j] = z.x; Z[j + 1] = z.y;
-          }
-        }
-      }
       // p of head h_b for tokens tig, tig+4, tig+8, tig+12
       const int src = ((G0 + (16 * kt) / G) % WG) * GQP + h_b;
       const float p0 = __shfl_sync(kFull, p[kt][0], 4 * tig + src);
@@ -821,6 +831,39 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
       const float p2 = __shfl_sync(kFull, p[kt][1], 4 * tig + src);
       const float p3 = __shfl_sync(kFull, p[kt][1], 4 * tig + 16 + src);
       const int ta = 16 * kt + tig;
+      if constexpr (ZB) {
+        // zero-point term in the B layout: the hi lane of a column pair
+        // takes tokens ta, ta+4, the lo lane ta+8, ta+12
+        const float pz0 = hl ? p2 : p0, pz1 = hl ? p3 : p1;
+        const int tz = ta + 8 * hl;
+#pragma unroll
+        for (int vb = 0; vb < C::NVB; ++vb) {
+          const int jb = (4 * vb + pair_b) / GQP;
+          if (jb < NJ) {
+            const float z0 = __half2float(Vz[tz * NJ + jb]);
+            const float z1 = __half2float(Vz[(tz + 4) * NJ + jb]);
+            Z[vb] = fmaf(pz0, z0, fmaf(pz1, z1, Z[vb]));
+          }
+        }
+      }
+      // zero-point term in the score layout (tokens gid, gid+8)
+      if constexpr (!ZB) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          float vz[NJ];
+          load_halves<NJ>(Vz + (16 * kt + gid + 8 * r) * NJ, vz);
+          if constexpr (NJ == 1) {
+            Z[0] = fmaf(p[kt][r], vz[0], Z[0]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < NJ; j += 2) {
+              const float2 z = __ffma2_rn(f2(p[kt][r], p[kt][r]), f2(vz[j], vz[j + 1]),
+                                          f2(Z[j], Z[j + 1]));
+              Z[j] = z.x; Z[j + 1] = z.y;
+            }
+          }
+        }
+      }
       // s_V of the four tokens: whole rows when every block needs a
       // different group, single values otherwise
       float vs[4][C::NVB];
