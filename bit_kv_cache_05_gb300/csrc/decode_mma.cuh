@@ -649,10 +649,8 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
         const float o1 = (O[mv][2] + O[mv][3]) * sb + Zt[j];
         __stcg(reinterpret_cast<float2 *>(dst + c0), make_float2(o0, o1));
       }
-      if (gid == 0 && tig < GQP) {
-        __stcg(dst + D, m_run);
-        __stcg(dst + D + 1, Lsum);
-      }
+      if (gid == 0 && tig < GQP)
+        __stcg(reinterpret_cast<float2 *>(dst + D), make_float2(m_run, Lsum));
     }
   };
 
@@ -1011,18 +1009,23 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
 //
 // One CTA per (sequence, kv head, 32-channel slice) with nw <= kMergeWarps
 // warps (a multiple of the query heads per kv head, sized by the launcher),
-// serving the kv head's GQ query heads.  The partials of kv head hd sit in
-// slots w + hd for the warps w whose chunk range touches the head; warp j
-// merges query head j mod GQ's partials j/GQ, j/GQ + nw/GQ, ... (kMergeU at
-// a time, all in flight).  Then warp j takes the residual window's tokens
-// j, j + nw, ... (kMergeRT at a time): lanes hold 32-channel strides of the
-// key row and of every query head's q' (one warp-wide sum per head gives
-// the scores) and the slice's channel of the value row.  Every warp keeps a
+// serving the kv head's GQ query heads.  Warp j first takes the residual
+// window's tokens j, j + nw, ... (kMergeRT at a time): lanes hold 32-channel
+// strides of the key row and of every query head's q' (one warp-wide sum
+// per head gives the scores) and the slice's channel of the value row.
+// Then, once the decode kernel's writes are visible, the partials: those of
+// kv head hd sit in slots w + hd for the warps w whose chunk range touches
+// the head, and warp j merges query head j mod GQ's partials j/GQ,
+// j/GQ + nw/GQ, ... (kMergeU at a time, all in flight).  Every warp keeps a
 // running (max, sum, o) per query head; warp hh then combines all warps'
-// states of query head hh with a log-sum-exp.
+// states of query head hh with a log-sum-exp.  The unroll depths keep the
+// CTAs small (4 warps for the usual window and partial counts), so that
+// every CTA of a large batch runs in one wave and, where the decode kernel
+// leaves room on an SM, the CTAs reside beside it and read the residual
+// window while it runs.
 constexpr int kMergeWarps = 16;
-constexpr int kMergeU = 8;
-constexpr int kMergeRT = 4;
+constexpr int kMergeU = 16;
+constexpr int kMergeRT = 8;
 
 template <int D, int GQP>
 __global__ void __launch_bounds__(kMergeWarps * 32)
@@ -1129,8 +1132,10 @@ k_merge_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
         const bool ok = k < n;
         const float *e = args.part +
                          ((size_t)(w0 + (ok ? k : k0) + hd) * GQP + hp) * part_stride<D>();
-        mu[u] = ok ? __ldcg(e + D) : -INFINITY;
-        lu[u] = ok ? __ldcg(e + D + 1) : 0.f;
+        const float2 ml = ok ? __ldcg(reinterpret_cast<const float2 *>(e + D))
+                             : make_float2(-INFINITY, 0.f);
+        mu[u] = ml.x;
+        lu[u] = ml.y;
         ou[u] = ok ? __ldcg(e + c) : 0.f;
       }
 #pragma unroll
