@@ -15,6 +15,7 @@ HBM bandwidth over the algorithmic bytes (packed codes + fp16 scale/zero
 planes + fp16 residual + q + out).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+  python bench.py --report [WORKLOAD ...]    # secondary figures, see run_report
 """
 from __future__ import annotations
 
@@ -440,6 +441,118 @@ def run_ours(args, w, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+REPORT_WORKLOADS = ("pages_S8192", "pages_S32768", "pages_S65536",
+                    "gqa_serving", "int4_append", "ragged_long")
+
+
+def _ev_times(fn, n):
+    """Median, p10 and p90 in us of n CUDA-event-timed calls fn(i), device
+    time: a spin kernel queued first keeps the device busy while the host
+    queues the calls, so no host launch time falls between the events."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(n * 1e5))   # ~50 us of spinning per queued call
+    for i in range(n):
+        ev[i][0].record()
+        fn(i)
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    ts = sorted(1e3 * a.elapsed_time(b) for a, b in ev)
+    return ts[n // 2], ts[n // 10], ts[(9 * n) // 10]
+
+
+def run_report(names):
+    """Secondary figures, one JSON line per workload: the decode from HBM
+    (rotating over cache copies larger than 4x L2) and hot (one cache,
+    repeated), the append (the workload's appended tokens per sequence, else
+    one), the quantize of the initial cache (prefill), and the unfused path
+    the pages compare the fused decode against: this library's dequantize to
+    fp16 K_hat / V_hat in memory, then torch's scaled_dot_product_attention
+    over them (a context row, not a target)."""
+    import torch
+    import torch.nn.functional as F
+    from bit_kv_cache_05_gb300 import synth
+    from bit_kv_cache_05_gb300.cache import KiviCache
+    peak, peak_kind = measured_peak_gbs()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    for name in names:
+        w = synth.workload(name)
+        inp = synth.make_inputs(w, device="cuda")
+        n_app = w.n_append if w.n_append else 1
+        S_dec = [s + n_app for s in w.seq_lens]
+        nb = decode_bytes(w, S_dec)
+        ncp = max(2, -(-4 * l2 // nb))
+        if nb * ncp > 8e9:
+            ncp = 2
+        caches = []
+
+        def make(i):
+            caches.append(KiviCache(inp["K"], inp["V"], w.seq_lens, H_q=w.H_q,
+                                    bits=w.bits, group=w.group,
+                                    residual=w.residual,
+                                    max_seq=w.max_seq + n_app + 8))
+        prefill = _ev_times(make, ncp)
+        K1, V1, _ = synth.decode_tokens(w, 1, device="cuda")
+        if w.n_append:
+            Kn = inp["K_new"]
+            Vn = inp["V_new"]
+        else:
+            Kn, Vn = K1[0], V1[0]
+        app = _ev_times(lambda i: caches[i].append(Kn, Vn, [n_app] * w.B), ncp)
+        del inp["K"], inp["V"]
+        q = inp["q"]
+        out = torch.empty(w.B, w.H_q, w.D, device="cuda")
+        for i in range(2 * ncp):
+            caches[i % ncp].decode_attend(q, out)
+        flushed = _ev_times(lambda i: caches[i % ncp].decode_attend(q, out), 100)
+        hot = _ev_times(lambda i: caches[0].decode_attend(q, out), 100)
+        caches[0].device_status()
+        fused = out.clone()
+        # the unfused context path
+        smax = max(S_dec)
+        shape = (w.B, w.H_kv, smax, w.D)
+        # zeroed: padding rows of short sequences stay finite under the mask
+        Kh = torch.zeros(shape, dtype=torch.float16, device="cuda")
+        Vh = torch.zeros(shape, dtype=torch.float16, device="cuda")
+        caches[0].dequantize(out=(Kh, Vh))
+        dq = _ev_times(lambda i: caches[0].dequantize(out=(Kh, Vh)), 10)
+        q4 = q.view(w.B, w.H_q, 1, w.D)
+        g = w.H_q // w.H_kv
+        kw = {"enable_gqa": True} if g > 1 else {}
+
+        def sdpa(i):
+            if min(S_dec) == smax:
+                return F.scaled_dot_product_attention(q4, Kh, Vh, **kw)
+            # ragged: one call per sequence over its own length (no mask)
+            return torch.cat([F.scaled_dot_product_attention(
+                q4[b:b + 1], Kh[b:b + 1, :, :S_dec[b]], Vh[b:b + 1, :, :S_dec[b]],
+                **kw) for b in range(w.B)])
+        ref = sdpa(0).float().view(w.B, w.H_q, w.D)
+        at = _ev_times(sdpa, 10)
+        line = {
+            "workload": name, "peak_gbs": peak, "peak_kind": peak_kind,
+            "decode_bytes": nb, "cache_copies": ncp,
+            "decode_us": round(flushed[0], 2),
+            "decode_p10_p90_us": [round(flushed[1], 2), round(flushed[2], 2)],
+            "decode_frac": round(nb / (flushed[0] * 1e-6) / 1e9 / peak, 3),
+            "decode_hot_us": round(hot[0], 2),
+            "append_tokens_per_seq": n_app, "append_us": round(app[0], 2),
+            "prefill_us": round(prefill[0], 1),
+            "unfused": {"dequantize_us": round(dq[0], 1),
+                        "sdpa_us": round(at[0], 1),
+                        "total_us": round(dq[0] + at[0], 1),
+                        "fused_speedup": round((dq[0] + at[0]) / flushed[0], 2),
+                        "max_abs_diff_vs_fused": float((ref - fused).abs().max())},
+        }
+        print(json.dumps(line), flush=True)
+        for c in caches:
+            c.close()
+        del caches, Kh, Vh, inp, ref
+        torch.cuda.empty_cache()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -448,9 +561,15 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--report", nargs="*", default=None,
+                    help="secondary figures for these workloads (all when "
+                         "none are named) instead of the benchmark line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.report is not None:
+        run_report(args.report or list(REPORT_WORKLOADS))
+        return
     from bit_kv_cache_05_gb300 import synth
     w = synth.workload(args.workload)
     rank, world, local = dist_env()

@@ -26,6 +26,7 @@ _NAMES = {VQ_ERR_ARG: "VQ_ERR_ARG", VQ_ERR_UNSUPPORTED: "VQ_ERR_UNSUPPORTED",
 EXPORTS = ("vq_kivi_quantize", "vq_kivi_append", "vq_kivi_decode_attend",
            "vq_kivi_free", "vq_kivi_last_error", "vq_kivi_lengths",
            "vq_kivi_get_params", "vq_kivi_plane_bytes", "vq_kivi_export",
+           "vq_kivi_dequantize",
            "vq_kivi_cache_bytes", "vq_kivi_set_split_tokens",
            "vq_kivi_launch_count", "vq_kivi_decode_attend_static",
            "vq_kivi_device_status", "vq_kivi_decode_kernel",
@@ -87,6 +88,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         L.vq_kivi_plane_bytes.restype = ctypes.c_size_t
         L.vq_kivi_plane_bytes.argtypes = [P, ctypes.c_int]
         L.vq_kivi_export.argtypes = [P, ctypes.c_int, P, ctypes.c_size_t, P]
+        L.vq_kivi_dequantize.argtypes = [P, P, P, i64, P]
         L.vq_kivi_cache_bytes.argtypes = [P, ctypes.POINTER(Bytes)]
         L.vq_kivi_set_split_tokens.argtypes = [P, i32]
         L.vq_kivi_device_status.argtypes = [P]

@@ -127,6 +127,22 @@ class KiviCache:
             return raw.view(B, H, -1, D // g)
         return raw.view(B, H, -1, D)
 
+    def dequantize(self, out=None, stream: Optional[torch.cuda.Stream] = None):
+        """fp16 K_hat, V_hat [B][H_kv][S_max][D] rebuilt from the cache (rows
+        past a sequence's length are left as allocated)."""
+        S, _, _ = self.lengths()
+        smax = max(max(S), 1)
+        if out is None:
+            shape = (self.B, self.H_kv, smax, self.D)
+            out = (torch.empty(shape, dtype=torch.float16, device=self.device),
+                   torch.empty(shape, dtype=torch.float16, device=self.device))
+        Kh, Vh = out
+        _lib.check(_lib.load().vq_kivi_dequantize(
+            self._h, _dev_ptr(Kh, torch.float16, "K_hat"),
+            _dev_ptr(Vh, torch.float16, "V_hat"), Kh.shape[2],
+            _stream_handle(stream)))
+        return Kh, Vh
+
     def cache_bytes(self) -> dict:
         b = _lib.Bytes()
         _lib.check(_lib.load().vq_kivi_cache_bytes(self._h, ctypes.byref(b)))

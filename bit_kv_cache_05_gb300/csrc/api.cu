@@ -476,6 +476,26 @@ int vq_kivi_export(const vq_kivi_cache *c, int which, void *dst,
   return VQ_OK;
 }
 
+int vq_kivi_dequantize(const vq_kivi_cache *c, void *K_hat, void *V_hat,
+                       int64_t s_stride, void *stream) {
+  int rc = check_cache(c);
+  if (rc) return rc;
+  if (!K_hat || !V_hat) return fail(VQ_ERR_ARG, "K_hat or V_hat is NULL");
+  if (((uintptr_t)K_hat | (uintptr_t)V_hat) & 15u)
+    return fail(VQ_ERR_ARG, "K_hat and V_hat must be 16-byte aligned");
+  int32_t smax = 0;
+  for (int b = 0; b < c->p.B; ++b)
+    if (c->S[b] > smax) smax = c->S[b];
+  if (s_stride < smax)
+    return fail(VQ_ERR_ARG, "s_stride=%lld < longest sequence %d",
+                (long long)s_stride, smax);
+  cudaError_t e = launch_dequantize(c->geo, c->pl, c->Tq, c->nres,
+                                    (__half *)K_hat, (__half *)V_hat, s_stride,
+                                    (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dequantize");
+  return VQ_OK;
+}
+
 int vq_kivi_cache_bytes(const vq_kivi_cache *c, vq_kivi_bytes *out) {
   if (!c || !out) return fail(VQ_ERR_ARG, "NULL argument");
   const vq_kivi_params &p = c->p;

@@ -85,11 +85,33 @@ __device__ __forceinline__ uint32_t quant_code_fast(float x, float mn,
   return (uint32_t)r;
 }
 
-// Packs the g x D code tile in shared memory into rows of D*BITS/8 bytes and
-// stores it with 16-byte vector stores (the tile is contiguous in global).
+// quant_code_fast for two values of one group at once (f32x2 arithmetic).
+// d = x - min is exact and >= 0, and t <= (max - min) / scale * (1 + 2^-21)
+// stays below 2^b - 1 + 1/2, so no clamp is needed; scale == 0 gives rcp = 0,
+// t = 0 and code 0 with no special case.  r = rint(t), f = t - r (exact):
+// t is near a half-integer exactly when |f| >= 1/2 - bound, with the bound of
+// quant_code_fast; then the correctly rounded quotient decides.
+__device__ __forceinline__ void quant2(float2 x, float mn, float scale,
+                                       float rcp, uint32_t &c0, uint32_t &c1) {
+  const float2 d = __fadd2_rn(x, make_float2(-mn, -mn));
+  const float2 t = __fmul2_rn(d, make_float2(rcp, rcp));
+  float2 r = make_float2(rintf(t.x), rintf(t.y));
+  const float2 f = __fadd2_rn(t, make_float2(-r.x, -r.y));
+  const float2 lim = __fadd2_rn(make_float2(0.5f, 0.5f),
+                                __ffma2_rn(t, make_float2(-9.5367431640625e-7f, -9.5367431640625e-7f),
+                                           make_float2(-1e-9f, -1e-9f)));
+  if (fabsf(f.x) >= lim.x) r.x = rintf(__fdiv_rn(d.x, scale));
+  if (fabsf(f.y) >= lim.y) r.y = rintf(__fdiv_rn(d.y, scale));
+  c0 = (uint32_t)r.x;
+  c1 = (uint32_t)r.y;
+}
+
+// Packs the g x D code tile in shared memory (row stride cs bytes) into rows
+// of D*BITS/8 bytes and stores it with 16-byte vector stores (the tile is
+// contiguous in global).
 template <int BITS>
-__device__ __forceinline__ void store_packed_tile(const uint8_t *codes, int g,
-                                                  int D, uint8_t *dst) {
+__device__ __forceinline__ void store_packed_tile(const uint8_t *codes, int cs,
+                                                  int g, int D, uint8_t *dst) {
   const int row = D * BITS / 8;
   const int nchunks = g * row / 16;
   constexpr int kPerWord = 32 / BITS;
@@ -97,7 +119,7 @@ __device__ __forceinline__ void store_packed_tile(const uint8_t *codes, int g,
     const int byte0 = 16 * k;
     const int i = byte0 / row;
     const int e0 = (byte0 % row) * 8 / BITS;
-    const uint8_t *src = codes + i * D + e0;
+    const uint8_t *src = codes + i * cs + e0;
     uint32_t w[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -114,8 +136,8 @@ __device__ __forceinline__ void store_packed_tile(const uint8_t *codes, int g,
 // The g x D code tile in kLayoutFrag order (2- or 4-bit codes): one thread
 // per 32-bit word, whose fields are gathered from the tile.
 template <int BITS>
-__device__ __forceinline__ void store_frag_keys(const uint8_t *codes, int g,
-                                                int D, uint8_t *dst) {
+__device__ __forceinline__ void store_frag_keys(const uint8_t *codes, int cs,
+                                                int g, int D, uint8_t *dst) {
   constexpr int F = 16 / BITS, KPW = 8 / BITS;   // fields per half
   const int wpr = D * BITS / 32, nw = D * BITS / 128;
   for (int w = threadIdx.x; w < g * wpr; w += blockDim.x) {
@@ -127,15 +149,15 @@ __device__ __forceinline__ void store_frag_keys(const uint8_t *codes, int g,
 #pragma unroll
       for (int r = 0; r < F; ++r) {
         const int ks = KPW * hw + (r >> 1), e = 2 * (r & 1) + s;
-        acc |= (uint32_t)codes[i * D + 16 * ks + 4 * tig + e] << (16 * s + BITS * r);
+        acc |= (uint32_t)codes[i * cs + 16 * ks + 4 * tig + e] << (16 * s + BITS * r);
       }
     reinterpret_cast<uint32_t *>(dst)[w] = acc;
   }
 }
 
 template <int BITS>
-__device__ __forceinline__ void store_frag_values(const uint8_t *codes, int g,
-                                                  int D, uint8_t *dst) {
+__device__ __forceinline__ void store_frag_values(const uint8_t *codes, int cs,
+                                                  int g, int D, uint8_t *dst) {
   constexpr int F = 16 / BITS, KPW = 8 / BITS;
   const int nw = D * BITS / 128, wpb = D * BITS / 2;   // words per block
   for (int w = threadIdx.x; w < g * D * BITS / 32; w += blockDim.x) {
@@ -149,7 +171,7 @@ __device__ __forceinline__ void store_frag_values(const uint8_t *codes, int g,
 #pragma unroll
       for (int r = 0; r < F; ++r) {
         const int mv = KPW * hw + (r >> 1), rho = r & 1;
-        acc |= (uint32_t)codes[(tA + 4 * s) * D + 16 * mv + 2 * j + rho]
+        acc |= (uint32_t)codes[(tA + 4 * s) * cs + 16 * mv + 2 * j + rho]
                << (16 * s + BITS * r);
       }
     reinterpret_cast<uint32_t *>(dst)[w] = acc;
@@ -175,10 +197,14 @@ __device__ __forceinline__ void load_tile(__half *tile, const __half *ring,
 }
 
 // One block = one group of g tokens of one (b, h), one thread per channel
-// (D threads): the group's key rows, then its value rows, are staged in a
-// shared tile; keys are quantized per channel (thread c walks column c),
-// values per (token, channel group) (thread t takes token t / (D/g), group
-// t % (D/g)).
+// (D threads).  Keys: the group's key rows are staged in a shared tile and
+// quantized per channel (thread c walks column c: consecutive threads read
+// consecutive halves).  Values: thread t takes (token t / (D/g), channel
+// group t % (D/g)) — D/g groups of g tokens is D items — and reads its g
+// values straight from global memory with 16-byte loads.  Codes go to a
+// shared code tile whose rows are padded to D + 4 bytes, so that the
+// threads of a warp writing (and the packers reading) different rows hit
+// different banks; the tile is then packed and stored.
 template <int BITS>
 __global__ void __launch_bounds__(kMaxD)
 k_flush(Geometry geo, Planes pl, const __half *__restrict__ Kin,
@@ -187,8 +213,9 @@ k_flush(Geometry geo, Planes pl, const __half *__restrict__ Kin,
   constexpr int levels = (1 << BITS) - 1;
   extern __shared__ __align__(16) unsigned char fsm[];
   const int D = geo.D, g = geo.g, H = geo.H_kv;
+  const int CS = D + 4;                                           // code row stride
   __half *tile = reinterpret_cast<__half *>(fsm);                 // [g][D]
-  uint8_t *codes = fsm + (size_t)g * D * sizeof(__half);         // [g][D]
+  uint8_t *codes = fsm + (size_t)g * D * sizeof(__half);         // [g][CS]
 
   const int item = blockIdx.x, h = blockIdx.y;
   const int b = find_seq(tab.prefix, geo.B, item);
@@ -201,12 +228,15 @@ k_flush(Geometry geo, Planes pl, const __half *__restrict__ Kin,
   load_tile(tile, pl.Kr, Kin, bh, in_stride, P0, split, g, D, geo.Rcap);
   __syncthreads();
   {
-    float mn = INFINITY, mx = -INFINITY;
-    for (int i = 0; i < g; ++i) {
-      const float v = __half2float(tile[i * D + c]);
-      mn = fminf(mn, v);
-      mx = fmaxf(mx, v);
+    // column c, two tokens per step as an fp16 pair (min / max are exact)
+    __half2 mn2 = __float2half2_rn(INFINITY), mx2 = __float2half2_rn(-INFINITY);
+    for (int i = 0; i < g; i += 2) {
+      const __half2 v = __halves2half2(tile[i * D + c], tile[(i + 1) * D + c]);
+      mn2 = __hmin2(mn2, v);
+      mx2 = __hmax2(mx2, v);
     }
+    float mn = fminf(__low2float(mn2), __high2float(mn2));
+    const float mx = fmaxf(__low2float(mx2), __high2float(mx2));
     mn = __fadd_rn(mn, 0.0f);  // a -0.0 minimum is stored as +0.0
     const float scale = __fdiv_rn(__fsub_rn(mx, mn), (float)levels);
     const float rcp = scale != 0.0f ? __frcp_rn(scale) : 0.0f;
@@ -220,47 +250,66 @@ k_flush(Geometry geo, Planes pl, const __half *__restrict__ Kin,
       const unsigned m = __reduce_max_sync(0xffffffffu, (unsigned)__half_as_ushort(sh));
       if ((c & 31) == 0) atomicMax(pl.ksmax + bh, m);
     }
-    for (int i = 0; i < g; ++i)
-      codes[i * D + c] = (uint8_t)quant_code_fast(__half2float(tile[i * D + c]),
-                                                  mn, scale, rcp, levels);
-  }
-  __syncthreads();
-  if ((BITS == 2 || BITS == 4) && geo.layout == kLayoutFrag)
-    store_frag_keys<BITS>(codes, g, D, pl.Kc + (bh * geo.Tcap + P0) * geo.row);
-  else
-    store_packed_tile<BITS>(codes, g, D, pl.Kc + (bh * geo.Tcap + P0) * geo.row);
-  __syncthreads();
-
-  // ---- values: per token over groups of g channels ----
-  load_tile(tile, pl.Vr, Vin, bh, in_stride, P0, split, g, D, geo.Rcap);
-  __syncthreads();
-  {
-    const int ngroups = D / g;
-    for (int t = c; t < g * ngroups; t += D) {
-      const int i = t / ngroups, j = t - i * ngroups;
-      const __half *row = tile + i * D + j * g;
-      float mn = INFINITY, mx = -INFINITY;
-      for (int k = 0; k < g; ++k) {
-        const float v = __half2float(row[k]);
-        mn = fminf(mn, v);
-        mx = fmaxf(mx, v);
-      }
-      mn = __fadd_rn(mn, 0.0f);  // a -0.0 minimum is stored as +0.0
-      const float scale = __fdiv_rn(__fsub_rn(mx, mn), (float)levels);
-      const float rcp = scale != 0.0f ? __frcp_rn(scale) : 0.0f;
-      for (int k = 0; k < g; ++k)
-        codes[i * D + j * g + k] =
-            (uint8_t)quant_code_fast(__half2float(row[k]), mn, scale, rcp, levels);
-      const size_t vidx = (bh * geo.Tcap + P0 + i) * ngroups + j;
-      pl.Vs[vidx] = __float2half_rn(scale);
-      pl.Vz[vidx] = __float2half_rn(mn);
+    for (int i = 0; i < g; i += 2) {
+      uint32_t c0, c1;
+      quant2(make_float2(__half2float(tile[i * D + c]), __half2float(tile[(i + 1) * D + c])),
+             mn, scale, rcp, c0, c1);
+      codes[i * CS + c] = (uint8_t)c0;
+      codes[(i + 1) * CS + c] = (uint8_t)c1;
     }
   }
   __syncthreads();
   if ((BITS == 2 || BITS == 4) && geo.layout == kLayoutFrag)
-    store_frag_values<BITS>(codes, g, D, pl.Vc + (bh * geo.Tcap + P0) * geo.row);
+    store_frag_keys<BITS>(codes, CS, g, D, pl.Kc + (bh * geo.Tcap + P0) * geo.row);
   else
-    store_packed_tile<BITS>(codes, g, D, pl.Vc + (bh * geo.Tcap + P0) * geo.row);
+    store_packed_tile<BITS>(codes, CS, g, D, pl.Kc + (bh * geo.Tcap + P0) * geo.row);
+  __syncthreads();
+
+  // ---- values: per token over groups of g channels ----
+  {
+    const int ngroups = D / g;
+    const int i = c / ngroups, j = c - i * ngroups;   // g * ngroups == D items
+    const int p = P0 + i;
+    const __half *row = (p < split ? pl.Vr + (bh * geo.Rcap + (p % geo.Rcap)) * D
+                                   : Vin + (bh * in_stride + (p - split)) * D) + j * g;
+    __half2 mn2 = __float2half2_rn(INFINITY), mx2 = __float2half2_rn(-INFINITY);
+    for (int k = 0; k < g; k += 8) {
+      const uint4 u = *reinterpret_cast<const uint4 *>(row + k);
+      const __half2 *h4 = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        mn2 = __hmin2(mn2, h4[e]);
+        mx2 = __hmax2(mx2, h4[e]);
+      }
+    }
+    float mn = fminf(__low2float(mn2), __high2float(mn2));
+    const float mx = fmaxf(__low2float(mx2), __high2float(mx2));
+    mn = __fadd_rn(mn, 0.0f);  // a -0.0 minimum is stored as +0.0
+    const float scale = __fdiv_rn(__fsub_rn(mx, mn), (float)levels);
+    const float rcp = scale != 0.0f ? __frcp_rn(scale) : 0.0f;
+    uint32_t *crow = reinterpret_cast<uint32_t *>(codes + i * CS + j * g);
+    for (int k = 0; k < g; k += 8) {
+      const uint4 u = *reinterpret_cast<const uint4 *>(row + k);
+      const __half2 *h4 = reinterpret_cast<const __half2 *>(&u);
+      uint32_t w[2] = {0u, 0u};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        uint32_t c0, c1;
+        quant2(__half22float2(h4[e]), mn, scale, rcp, c0, c1);
+        w[e >> 1] |= (c0 | (c1 << 8)) << (16 * (e & 1));
+      }
+      crow[k / 4] = w[0];
+      crow[k / 4 + 1] = w[1];
+    }
+    const size_t vidx = (bh * geo.Tcap + P0 + i) * ngroups + j;
+    pl.Vs[vidx] = __float2half_rn(scale);
+    pl.Vz[vidx] = __float2half_rn(mn);
+  }
+  __syncthreads();
+  if ((BITS == 2 || BITS == 4) && geo.layout == kLayoutFrag)
+    store_frag_values<BITS>(codes, CS, g, D, pl.Vc + (bh * geo.Tcap + P0) * geo.row);
+  else
+    store_packed_tile<BITS>(codes, CS, g, D, pl.Vc + (bh * geo.Tcap + P0) * geo.row);
 }
 
 // Residual ring writes: 16-byte chunks of fp16 rows.
@@ -318,7 +367,7 @@ cudaError_t launch_flush(const Geometry &geo, const Planes &pl,
                          int total_groups, cudaStream_t st) {
   if (total_groups <= 0) return cudaSuccess;
   dim3 grid(total_groups, geo.H_kv);
-  const size_t smem = (size_t)geo.g * geo.D * (sizeof(__half) + 1);
+  const size_t smem = (size_t)geo.g * (geo.D * sizeof(__half) + geo.D + 4);
   void *fn = nullptr;
   switch (geo.bits) {
     case 2: fn = (void *)k_flush<2>; break;
@@ -331,7 +380,7 @@ cudaError_t launch_flush(const Geometry &geo, const Planes &pl,
   if (!opted[geo.bits]) {
     cudaError_t e = cudaFuncSetAttribute(
         fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        128 * kMaxD * (int)(sizeof(__half) + 1));
+        128 * (kMaxD * (int)sizeof(__half) + kMaxD + 4));
     if (e != cudaSuccess) return e;
     opted[geo.bits] = true;
   }
@@ -400,6 +449,114 @@ cudaError_t launch_export_residual(const Geometry &geo, const Planes &pl,
   const __half *ring = which == 6 ? pl.Kr : pl.Vr;
   dim3 grid(geo.Rcap, geo.B * geo.H_kv);
   k_export_residual<<<grid, 128, 0, st>>>(geo, ring, (__half *)dst, lens);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ---- dequantized copy of the cache (the unfused baseline) ------------------
+//
+// Per (sequence, kv head): tokens t < T_q are rebuilt as fp16_rn(code * s +
+// z) (fp32 fma of the fp16 scale and zero), tokens T_q <= t < S copied from
+// the residual ring (slot t mod Rcap).  One thread per (token, 8 channels
+// c0 ... c0+7), one 16-byte store per plane.  The codes are read in the
+// cache's own order: packed (the 8 codes are b consecutive bytes) or
+// MMA-fragment (2 words for keys, 4 for values, by the position functions
+// specialised to 8 channels of one 16-channel step).
+__device__ inline void codes8(const Geometry &geo, const uint8_t *krow,
+                              const uint8_t *vblk, int tl, int c0,
+                              uint32_t (&kc)[8], uint32_t (&vc)[8]) {
+  const int b = geo.bits;
+  const uint32_t m = (1u << b) - 1u;
+  if (geo.layout == kLayoutFrag) {
+    const int kpw = 8 / b, nw = geo.D * b / 128;
+    const int ks = c0 >> 4, h = (c0 >> 3) & 1, r0 = 2 * (ks % kpw);
+    const uint32_t *kw = reinterpret_cast<const uint32_t *>(krow);
+    for (int q = 0; q < 2; ++q) {              // tig = 2h + q: channels 4q ... 4q+3
+      const uint32_t w = kw[nw * (2 * h + q) + ks / kpw];
+      for (int e = 0; e < 4; ++e)
+        kc[4 * q + e] = (w >> (16 * (e & 1) + b * (r0 + (e >> 1)))) & m;
+    }
+    const int u = tl & 7, sh = 16 * (u >> 2), pi = 4 * (tl >> 3) + (u & 3);
+    const uint32_t *vw = reinterpret_cast<const uint32_t *>(vblk);
+    for (int jj = 0; jj < 4; ++jj) {           // j = (c0 & 15) / 2 + jj
+      const uint32_t w = vw[(8 * pi + ((c0 & 15) >> 1) + jj) * nw + ks / kpw];
+      for (int rho = 0; rho < 2; ++rho)
+        vc[2 * jj + rho] = (w >> (sh + b * (r0 + rho))) & m;
+    }
+  } else {
+    // 8 codes = b bytes at byte c0 * b / 8
+    uint64_t kx = 0, vx = 0;
+    const uint8_t *kp = krow + c0 * b / 8, *vp = vblk + (size_t)tl * geo.row + c0 * b / 8;
+    for (int i = 0; i < b; ++i) {
+      kx |= (uint64_t)kp[i] << (8 * i);
+      vx |= (uint64_t)vp[i] << (8 * i);
+    }
+    for (int e = 0; e < 8; ++e) {
+      kc[e] = (uint32_t)(kx >> (b * e)) & m;
+      vc[e] = (uint32_t)(vx >> (b * e)) & m;
+    }
+  }
+}
+
+__global__ void k_dequantize(Geometry geo, Planes pl, LenTable lens,
+                             __half *__restrict__ Kh, __half *__restrict__ Vh,
+                             int64_t s_stride) {
+  const int hd = blockIdx.y, bq = hd / geo.H_kv;
+  const int D = geo.D, g = geo.g, NJ = D / g, c8 = D / 8;
+  const int Tq = lens.Tq[bq], S = Tq + lens.nres[bq];
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+       i < (int64_t)S * c8; i += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / c8), c0 = (int)(i - (int64_t)t * c8) * 8;
+    uint4 ko, vo;
+    if (t < Tq) {
+      const size_t r = (size_t)hd * geo.Tcap + t;
+      uint32_t kc[8], vc[8];
+      codes8(geo, pl.Kc + r * geo.row, pl.Vc + (r - (t & 15)) * geo.row, t & 15,
+             c0, kc, vc);
+      const size_t kg = ((size_t)hd * (geo.Tcap / g) + t / g) * D + c0;
+      const uint4 ksr = *reinterpret_cast<const uint4 *>(pl.Ks + kg);
+      const uint4 kzr = *reinterpret_cast<const uint4 *>(pl.Kz + kg);
+      const __half *ksh = reinterpret_cast<const __half *>(&ksr);
+      const __half *kzh = reinterpret_cast<const __half *>(&kzr);
+      const float vs = __half2float(pl.Vs[r * NJ + c0 / g]);
+      const float vz = __half2float(pl.Vz[r * NJ + c0 / g]);
+      __half kx[8], vx[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        kx[e] = __float2half_rn(__fmaf_rn((float)kc[e], __half2float(ksh[e]),
+                                          __half2float(kzh[e])));
+        vx[e] = __float2half_rn(__fmaf_rn((float)vc[e], vs, vz));
+      }
+      ko = *reinterpret_cast<const uint4 *>(kx);
+      vo = *reinterpret_cast<const uint4 *>(vx);
+    } else {
+      const size_t slot = ((size_t)hd * geo.Rcap + t % geo.Rcap) * D + c0;
+      ko = *reinterpret_cast<const uint4 *>(pl.Kr + slot);
+      vo = *reinterpret_cast<const uint4 *>(pl.Vr + slot);
+    }
+    const size_t o = ((size_t)hd * s_stride + t) * D + c0;
+    *reinterpret_cast<uint4 *>(Kh + o) = ko;
+    *reinterpret_cast<uint4 *>(Vh + o) = vo;
+  }
+}
+
+cudaError_t launch_dequantize(const Geometry &geo, const Planes &pl,
+                              const int32_t *Tq, const int32_t *nres,
+                              __half *Kh, __half *Vh, int64_t s_stride,
+                              cudaStream_t st) {
+  LenTable lens;
+  int64_t smax = 0;
+  for (int b = 0; b < geo.B; ++b) {
+    lens.Tq[b] = Tq[b];
+    lens.nres[b] = nres[b];
+    if (Tq[b] + nres[b] > smax) smax = Tq[b] + nres[b];
+  }
+  if (smax == 0) return cudaSuccess;
+  const int64_t items = smax * (geo.D / 8);
+  int64_t bx = (items + 255) / 256;
+  if (bx > 4096) bx = 4096;
+  dim3 grid((unsigned)bx, geo.B * geo.H_kv);
+  k_dequantize<<<grid, 256, 0, st>>>(geo, pl, lens, Kh, Vh, s_stride);
   count_launch();
   return cudaGetLastError();
 }

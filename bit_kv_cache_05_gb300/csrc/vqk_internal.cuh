@@ -111,6 +111,10 @@ cudaError_t launch_tail(const Geometry &geo, const Planes &pl,
 // the packed order, into dst
 cudaError_t launch_export_frag(const Geometry &geo, const uint8_t *src,
                                bool values, void *dst, cudaStream_t st);
+cudaError_t launch_dequantize(const Geometry &geo, const Planes &pl,
+                              const int32_t *Tq, const int32_t *nres,
+                              __half *Kh, __half *Vh, int64_t s_stride,
+                              cudaStream_t st);
 cudaError_t launch_export_residual(const Geometry &geo, const Planes &pl,
                                    int which, void *dst, const int32_t *Tq,
                                    const int32_t *nres, cudaStream_t st);

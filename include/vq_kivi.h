@@ -157,6 +157,21 @@ size_t vq_kivi_plane_bytes(const vq_kivi_cache *c, int which);
 int vq_kivi_export(const vq_kivi_cache *c, int which, void *dst,
                    size_t dst_bytes, void *stream);
 
+/* Dequantized copy of the cache: the unfused path that the pages measure the
+ * fused decode against (changelog v0.42.0, scalar_fused_decode_attend: a
+ * dequantize to fp16 K_hat / V_hat in memory, then a separate attention).
+ * For every sequence b, kv head h and token t < S[b]:
+ *   K_hat[b][h][t][c] = fp16_rn(fma(code, Ks, Kz)) for quantized tokens (the
+ *   fp32 fma of the fp16 scale and zero, then rounded to fp16), and the fp16
+ *   residual rows for the rest; V_hat likewise.  Rows t >= S[b] are not
+ *   written.
+ *   K_hat, V_hat  device, fp16, [B][H_kv][s_stride][D], 16-byte aligned,
+ *                 caller-owned
+ *   s_stride      >= the longest sequence
+ * Returns VQ_ERR_ARG for NULL or misaligned outputs or a short stride. */
+int vq_kivi_dequantize(const vq_kivi_cache *c, void *K_hat, void *V_hat,
+                       int64_t s_stride, void *stream);
+
 /* Bytes held, per the cache's byte accounting (changelog v0.8.0 "full
  * byte-accounting"): packed codes, fp16 scale/zero metadata and the fp16
  * residual, over the tokens currently stored (not the capacity), and the
