@@ -1,6 +1,8 @@
 // Host side of the tensor-core decode: kernel choice, launch plan (stages,
 // persistent grid size) and launch of the decode kernel and of the
 // log-sum-exp merge of its per-warp partials (both in decode_mma.cuh).
+#include <mutex>
+
 #include "decode_mma.cuh"
 
 namespace vqk {
@@ -61,8 +63,29 @@ bool mma_plan(const Geometry &geo, int sm_count, MmaPlan *plan) {
   plan->ST = ST;
   plan->smem = smem;
   plan->warps_max = sm_count * occ * kNW;
+  plan->sm_count = sm_count;
   plan->chunk = mma::kC;
   return true;
+}
+
+// resident CTAs per SM of a merge kernel at nw warps per CTA (cached; the
+// cache is shared by every thread of the process)
+static int merge_ctas_per_sm(mma::MergeFn mf, int nw) {
+  struct Entry { mma::MergeFn fn; int nw, occ; };
+  static Entry cache[64];
+  static int used = 0;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (cache[i].fn == mf && cache[i].nw == nw) return cache[i].occ;
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, (const void *)mf, nw * 32, 0) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (used < 64) cache[used++] = Entry{mf, nw, occ};
+  return occ;
 }
 
 size_t mma_part_floats(const Geometry &geo, const MmaPlan &plan) {
@@ -122,9 +145,11 @@ cudaError_t launch_decode_mma(const Geometry &geo, const Planes &pl,
     case 128 * 8 + 4: mf = mma::merge_fn<128, 4>(); break;
     default: return cudaErrorInvalidValue;
   }
-  // merge warps per CTA: per query head enough for the largest partial
-  // count of a head, and overall enough for the longest residual window, to
-  // be read in one round; a multiple of the query heads per kv head
+  // merge warps per CTA (a multiple of the query heads per kv head): per
+  // query head enough for the largest partial count of a head to be read in
+  // one round, and more, up to what reads the longest residual window in
+  // one round, only while every CTA of the grid still fits on the device at
+  // once (a second wave costs more than a second round of the window)
   const int GQ = plan.GQ;
   int64_t per = 1, nr = 1;
   bool any = false;
@@ -144,8 +169,16 @@ cudaError_t launch_decode_mma(const Geometry &geo, const Planes &pl,
   }
   if (!any) return cudaSuccess;
   const int64_t per_max = mma::kMergeWarps / GQ;
-  if (per < (nr + GQ - 1) / GQ) per = (nr + GQ - 1) / GQ;
   if (per > per_max) per = per_max;
+  int64_t per_res = (nr + GQ - 1) / GQ;
+  if (per_res > per_max) per_res = per_max;
+  const int64_t ctas = (int64_t)geo.B * geo.H_kv * (geo.D / 32);
+  for (int64_t pr = per_res; pr > per; --pr) {
+    if ((int64_t)merge_ctas_per_sm(mf, (int)(pr * GQ)) * plan.sm_count >= ctas) {
+      per = pr;
+      break;
+    }
+  }
   const int64_t nw = per * GQ;
   cfg.gridDim = dim3(geo.B * geo.H_kv, geo.D / 32);
   cfg.blockDim = dim3((unsigned)nw * 32);

@@ -176,6 +176,7 @@ struct MmaPlan {
   int GQ, GQp, KG, ST, chunk;
   unsigned smem;     // dynamic shared memory per CTA
   int warps_max;     // resident warps of the persistent grid
+  int sm_count;      // SMs of the device
 };
 
 // false when the shape has no tensor-core kernel (then the CUDA-core kernel
