@@ -550,7 +550,17 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
 #pragma unroll
     for (int j = 0; j < NQ; ++j) {
       constexpr int PER = D / 32;
-      qb[lane + 32 * j] = vb[j] * exp2i(kh[j / PER]);
+      const float x = vb[j] * exp2i(kh[j / PER]);
+      if constexpr (L::FRAG) {
+        // fp16 hi + lo of the scaled q' (qb's region holds the two halves
+        // arrays): the score operand is built from them in fp16 arithmetic
+        const __half xh = __float2half_rn(x);
+        reinterpret_cast<__half *>(qb)[lane + 32 * j] = xh;
+        reinterpret_cast<__half *>(qb)[GQP * D + lane + 32 * j] =
+            __float2half_rn(x - __half2float(xh));
+      } else {
+        qb[lane + 32 * j] = x;
+      }
     }
     int kl = kh[0];
 #pragma unroll
@@ -568,19 +578,46 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     const int gr = gw0 + pair_b / GQP - kg0;   // group row in the region
     const float *qbh = qb + h_b * D + 4 * tig;
     const __half *ksr = Ks + gr * D + 4 * tig;
+    if constexpr (L::FRAG) {
+      // products q' s in fp16 pairs: hi = RN(qh s), its exact rounding
+      // error e = qh s - hi (at most 11 significant bits: representable),
+      // lo = RN(ql s + e); hi + lo carries ~21 bits of q' s.  Slot order is
+      // channel order here, so a pair of channels is one register.
+      const __half *qhh = reinterpret_cast<const __half *>(qb) + h_b * D + 4 * tig;
+      const __half *qlh = qhh + GQP * D;
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      const uint2 sraw = *reinterpret_cast<const uint2 *>(ksr + 16 * ks);
-      const float4 qs = *reinterpret_cast<const float4 *>(qbh + 16 * ks);
-      const float2 s01 = __half22float2(*reinterpret_cast<const __half2 *>(&sraw.x));
-      const float2 s23 = __half22float2(*reinterpret_cast<const __half2 *>(&sraw.y));
-      // channel order 4tig + 0..3
-      const float2 a01 = hilo2(__fmul2_rn(f2(qs.x, qs.y), s01), hls);
-      const float2 a23 = hilo2(__fmul2_rn(f2(qs.z, qs.w), s23), hls);
-      const float a[4] = {a01.x, a01.y, a23.x, a23.y};
-      // slot order: slot e holds channel 4tig + off(e)
-      Bs[ks][0] = pack_half2(a[L::off(0)], a[L::off(1)]);
-      Bs[ks][1] = pack_half2(a[L::off(2)], a[L::off(3)]);
+      for (int ks = 0; ks < KS; ++ks) {
+        const uint2 sr = *reinterpret_cast<const uint2 *>(ksr + 16 * ks);
+        const uint2 hr = *reinterpret_cast<const uint2 *>(qhh + 16 * ks);
+        const uint2 lr = *reinterpret_cast<const uint2 *>(qlh + 16 * ks);
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+          const uint32_t sw = w ? sr.y : sr.x, hw = w ? hr.y : hr.x, lw = w ? lr.y : lr.x;
+          const __half2 sv2 = *reinterpret_cast<const __half2 *>(&sw);
+          const __half2 h2 = *reinterpret_cast<const __half2 *>(&hw);
+          const __half2 l2 = *reinterpret_cast<const __half2 *>(&lw);
+          const __half2 hi = __hmul2(h2, sv2);
+          const __half2 e = __hfma2(h2, sv2, __hneg2(hi));
+          const __half2 lo = __hfma2(l2, sv2, e);
+          const __half2 pick = hl ? lo : hi;
+          Bs[ks][w] = *reinterpret_cast<const uint32_t *>(&pick);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const uint2 sraw = *reinterpret_cast<const uint2 *>(ksr + 16 * ks);
+        const float4 qs = *reinterpret_cast<const float4 *>(qbh + 16 * ks);
+        const float2 s01 = __half22float2(*reinterpret_cast<const __half2 *>(&sraw.x));
+        const float2 s23 = __half22float2(*reinterpret_cast<const __half2 *>(&sraw.y));
+        // channel order 4tig + 0..3
+        const float2 a01 = hilo2(__fmul2_rn(f2(qs.x, qs.y), s01), hls);
+        const float2 a23 = hilo2(__fmul2_rn(f2(qs.z, qs.w), s23), hls);
+        const float a[4] = {a01.x, a01.y, a23.x, a23.y};
+        // slot order: slot e holds channel 4tig + off(e)
+        Bs[ks][0] = pack_half2(a[L::off(0)], a[L::off(1)]);
+        Bs[ks][1] = pack_half2(a[L::off(2)], a[L::off(3)]);
+      }
     }
     // zero-point term: the hi and lo lanes of a pair take half the K-steps
     const float *qnh = qn + h_b * D + 4 * tig;
