@@ -514,9 +514,12 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   // q' of the head's GQP query heads: qn in channel order; qb with channel
   // c scaled by 2^-oexp(c) of its score slot and by the head's power of two
   // 2^k, which puts the bound max|q'| * max s_K of the score operand's
-  // products (over every key group of the kv head) in [2^13, 2^14): no
+  // products (over every key group of the kv head) in [2^13, 2^14) — no
   // fp16 overflow, and the lo parts of the large products stay in fp16's
-  // normal range.  unscale_t = 2^(24 - k) of this lane's score head.
+  // normal range — unless that would take max|q'| itself past 2^15 (small
+  // key scales): q' enters the operand as fp16 hi + lo, so k is capped
+  // there, and the products then stay further below fp16's limit.
+  // unscale_t = 2^(24 - k) of this lane's score head.
   auto load_q = [&](int b, int h) {
     constexpr int NQ = GQP * D / 32;
     float mq[GQP], vb[NQ];
@@ -544,7 +547,11 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1)
         m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
-      const int k = 13 - (((__float_as_int(m * smax) >> 23) & 0xff) - 127);
+      int k = 13 - (((__float_as_int(m * smax) >> 23) & 0xff) - 127);
+      // q' itself stays below 2^15 (it enters the operand as fp16 hi + lo):
+      // with small key scales the product bound alone would overflow it
+      const int kq = 14 - (((__float_as_int(m) >> 23) & 0xff) - 127);
+      if (kq < k) k = kq;
       kh[hh] = k < -60 ? -60 : (k > 60 ? 60 : k);
     }
 #pragma unroll

@@ -188,6 +188,32 @@ def test_softmax_scale_argument(lib):
     c.close()
 
 
+@pytest.mark.parametrize("bits,g,Hq,Hkv,klo,khi,qmul", [
+    (2, 32, 8, 8, 1e-3, 1e-2, 1.0),     # tiny key scales
+    (2, 32, 8, 2, 50.0, 300.0, 1.0),    # large key scales (products near the bound)
+    (4, 64, 8, 8, 1e-3, 1e2, 1.0),      # five decades across channels
+    (2, 32, 4, 4, 0.5, 2.0, 1e-3),      # a nearly flat softmax
+    (2, 32, 8, 2, 0.5, 2.0, 20.0),      # a sharp softmax
+])
+def test_operand_scaling_extremes(lib, bits, g, Hq, Hkv, klo, khi, qmul):
+    """The score operand is q' * s_K carried as fp16 hi + lo, scaled per
+    head by a power of two from the largest key scale: key scales over
+    several decades and query magnitudes from 1e-3 to 20x stay within the
+    parity tolerance."""
+    lens = [1000, 333]
+    w = synth.Workload("extremes", len(lens), Hq, Hkv, 128, bits, g, g, lens,
+                       key_kind="chscale", chscale_lo=klo, chscale_hi=khi)
+    inp = synth.make_inputs(w, seed=13, device="cuda")
+    q = (inp["q"].float() * qmul).half()
+    c = gpu_cache(w, inp)
+    assert c.decode_kernel() == "tensor-core"
+    out = c.decode_attend(q)
+    oc = oracle_cache(w, inp["K"].cpu().numpy(), inp["V"].cpu().numpy(), lens)
+    assert_attn_close(out.cpu().numpy(), oc.attend(q.cpu().numpy()),
+                      f"b={bits} keys x[{klo}, {khi}] q x{qmul}")
+    c.close()
+
+
 # ---------------------------------------------------------------------------
 # append: prefill-vs-decode path independence, against the oracle's own
 # incremental procedure
