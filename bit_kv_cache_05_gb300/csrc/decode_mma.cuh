@@ -559,12 +559,22 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
       constexpr int PER = D / 32;
       const float x = vb[j] * exp2i(kh[j / PER]);
       if constexpr (L::FRAG) {
-        // fp16 hi + lo of the scaled q' (qb's region holds the two halves
-        // arrays): the score operand is built from them in fp16 arithmetic
+        // fp16 hi + lo of the scaled q' (qb's region holds them): the score
+        // operand is built from them in fp16 arithmetic.  With 4 query
+        // heads per kv head, per 4-channel group 4 hi then 4 lo halves (one
+        // 16-byte load per lane and K-step; measured faster there, while
+        // one head keeps two arrays of halves, which needs fewer registers)
+        const int i = lane + 32 * j;
         const __half xh = __float2half_rn(x);
-        reinterpret_cast<__half *>(qb)[lane + 32 * j] = xh;
-        reinterpret_cast<__half *>(qb)[GQP * D + lane + 32 * j] =
-            __float2half_rn(x - __half2float(xh));
+        const __half xl = __float2half_rn(x - __half2float(xh));
+        __half *q16 = reinterpret_cast<__half *>(qb);
+        if constexpr (GQP == 4) {
+          q16[2 * (i & ~3) + (i & 3)] = xh;
+          q16[2 * (i & ~3) + (i & 3) + 4] = xl;
+        } else {
+          q16[i] = xh;
+          q16[GQP * D + i] = xl;
+        }
       } else {
         qb[lane + 32 * j] = x;
       }
@@ -590,13 +600,20 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
       // error e = qh s - hi (at most 11 significant bits: representable),
       // lo = RN(ql s + e); hi + lo carries ~21 bits of q' s.  Slot order is
       // channel order here, so a pair of channels is one register.
-      const __half *qhh = reinterpret_cast<const __half *>(qb) + h_b * D + 4 * tig;
-      const __half *qlh = qhh + GQP * D;
+      const __half *q16 = reinterpret_cast<const __half *>(qb);
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         const uint2 sr = *reinterpret_cast<const uint2 *>(ksr + 16 * ks);
-        const uint2 hr = *reinterpret_cast<const uint2 *>(qhh + 16 * ks);
-        const uint2 lr = *reinterpret_cast<const uint2 *>(qlh + 16 * ks);
+        uint2 hr, lr;
+        if constexpr (GQP == 4) {
+          const uint4 q4 = *reinterpret_cast<const uint4 *>(
+              q16 + 2 * (h_b * D + 4 * tig) + 32 * ks);   // hi 4, lo 4
+          hr = make_uint2(q4.x, q4.y);
+          lr = make_uint2(q4.z, q4.w);
+        } else {
+          hr = *reinterpret_cast<const uint2 *>(q16 + h_b * D + 4 * tig + 16 * ks);
+          lr = *reinterpret_cast<const uint2 *>(q16 + GQP * D + h_b * D + 4 * tig + 16 * ks);
+        }
 #pragma unroll
         for (int w = 0; w < 2; ++w) {
           const uint32_t sw = w ? sr.y : sr.x, hw = w ? hr.y : hr.x, lw = w ? lr.y : lr.x;
