@@ -14,11 +14,13 @@
 //   scores   S^T[tok][col]  = codes[tok][ch] . A[ch][col],  A = q' s  (hi + lo)
 //   values   O^T[ch][col]  += codes^T[ch][tok] . W[tok][col], W = p s  (hi + lo)
 // The codes enter as exact fp16 subnormals (the b-bit field masked out of the
-// packed word, value = code * 2^(bit position - 24)); each fp32 factor is
-// split into two fp16 operands hi (top 11 bits) and lo (the fp32 remainder
-// rounded to fp16) in adjacent columns, so products keep about 21 bits.  The
-// zero-point sums (sum_c q'_c z_Gc and sum_t p_t z_t,j) run on the CUDA cores
-// in fp32.
+// packed word, value = code * 2^(bit position - 24)); each factor enters as
+// two fp16 operands hi and lo in adjacent columns, so products keep about 21
+// bits: p s as hi = its top 11 bits and lo = the fp32 remainder rounded to
+// fp16; q' s (2- and 4-bit caches) in fp16 pair arithmetic from a per-head
+// fp16 split of q' (hi = RN(qh s), lo = RN(ql s + the exact error of hi)).
+// The zero-point sums (sum_c q'_c z_Gc and sum_t p_t z_t,j) run on the CUDA
+// cores in fp32.
 //
 // MMA columns.  Scores: 8 columns = 4 (query head, key group) pairs x (hi,
 // lo): with GQP query heads per kv head, a "window" of 4/GQP consecutive key
@@ -297,8 +299,10 @@ struct Cfg {
   static constexpr uint32_t S_VS = S_KZ + KG * D * 2;
   static constexpr uint32_t S_VZ = S_VS + kC * NJ * 2;
   static constexpr uint32_t S_BYTES = (S_VZ + kC * NJ * 2 + 127) / 128 * 128;
-  // per-warp layout: [mbarriers][q' GQP x D f32, channel c scaled by the
-  // 2^-sexp of its score slot][q' GQP x D f32][stages].
+  // per-warp layout: [mbarriers][q' GQP x D, channel c scaled by the
+  // 2^-oexp of its score slot and the head's power of two: f32, or for
+  // fragment-order codes its fp16 hi and lo halves in the same bytes][q'
+  // GQP x D f32][stages].
   static constexpr uint32_t W_QF = 128;
   static constexpr uint32_t W_QN = W_QF + GQP * D * 4;
   static constexpr uint32_t W_STAGE0 = (W_QN + GQP * D * 4 + 127) / 128 * 128;
@@ -593,7 +597,6 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   // zero-point term beta.
   auto build_score_b = [&](const __half *Ks, const __half *Kz, int gw0, int kg0) {
     const int gr = gw0 + pair_b / GQP - kg0;   // group row in the region
-    const float *qbh = qb + h_b * D + 4 * tig;
     const __half *ksr = Ks + gr * D + 4 * tig;
     if constexpr (L::FRAG) {
       // products q' s in fp16 pairs: hi = RN(qh s), its exact rounding
@@ -628,6 +631,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
         }
       }
     } else {
+      const float *qbh = qb + h_b * D + 4 * tig;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         const uint2 sraw = *reinterpret_cast<const uint2 *>(ksr + 16 * ks);
