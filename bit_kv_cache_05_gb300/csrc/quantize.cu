@@ -375,14 +375,13 @@ cudaError_t launch_flush(const Geometry &geo, const Planes &pl,
     case 8: fn = (void *)k_flush<8>; break;
     default: return cudaErrorInvalidValue;
   }
-  // the largest tile (g = 128, D = 256) needs the opt-in limit; set once
-  static bool opted[9] = {false};
-  if (!opted[geo.bits]) {
-    cudaError_t e = cudaFuncSetAttribute(
-        fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        128 * (kMaxD * (int)sizeof(__half) + kMaxD + 4));
+  // tiles above the default 48 KB (g = 128 with D = 256) need the opt-in
+  // limit, which belongs to the current device's context: set it on every
+  // such launch (no process-wide flag to race on or to carry across devices)
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
     if (e != cudaSuccess) return e;
-    opted[geo.bits] = true;
   }
   cudaError_t e = cudaSuccess;
   switch (geo.bits) {
