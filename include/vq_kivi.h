@@ -150,8 +150,8 @@ int vq_kivi_get_params(const vq_kivi_cache *c, vq_kivi_params *p);
  * the size (0 for a bad `which`); vq_kivi_export writes the whole plane to
  * device memory `dst` of at least that size, on `stream`.  Only the valid
  * rows (tokens < T_q, slots < n_res) are defined.  A cache may hold its
- * code planes internally in another order of the same bytes (2-bit caches
- * decoded on the tensor cores keep them in the order the MMA fragments
+ * code planes internally in another order of the same bytes (2- and 4-bit
+ * caches decoded on the tensor cores keep them in the order the MMA fragments
  * consume them); the export always produces the packing described above. */
 size_t vq_kivi_plane_bytes(const vq_kivi_cache *c, int which);
 int vq_kivi_export(const vq_kivi_cache *c, int which, void *dst,
