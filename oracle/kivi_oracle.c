@@ -23,7 +23,7 @@
  * The pages print no formula; the fp32 formula used here is the plain reading
  * (scale = (max-min)/(2^b-1); code = clamp(rint((x-min)/scale), 0, 2^b-1);
  * scale stored as fp16 round-to-nearest-even, zero = min stored exactly,
- * with a minimum of -0.0 stored as +0.0).
+ * with a minimum of -0.0 stored as +0.0 and a zero range as the scale +0.0).
  *
  * Precision: quantization arithmetic in IEEE fp32 exactly as written (this
  * file must be compiled without fast-math and with -ffp-contract=off);
@@ -68,9 +68,12 @@ static void quant_group(const float *x, long stride, int n, int bits,
   }
   /* A group minimum of -0.0 is stored as +0.0 (the pages leave signed zero
    * open; -0 + +0 = +0 under round-to-nearest).  No code changes: x - min
-   * is the same number either way. */
+   * is the same number either way.  Likewise a zero range (a constant
+   * group, possibly of mixed-sign zeros) gives the scale +0.0 whatever the
+   * order of its elements: mx - mn alone is -0.0 when the first element,
+   * which the scan keeps as the maximum among equal zeros, is -0.0. */
   mn = mn + 0.0f;
-  float range = mx - mn;
+  float range = (mx - mn) + 0.0f;
   float scale = range / (float)levels;
   for (int i = 0; i < n; ++i) {
     int c = 0;

@@ -418,3 +418,101 @@ def test_negative_zero_minimum_stored_as_positive_zero(oracle_mod):
     x2 = np.array([0.0, -0.0, 0.0, -0.0], np.float32)
     codes, s32, s16, z16 = oracle_mod.quant_group(x2, 2)
     assert z16 == 0x0000 and s16 == 0 and (codes == 0).all()
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_signed_zero_groups_in_either_order(oracle_mod, bits):
+    """A group of zeros of mixed sign is a constant group: whatever the order
+    of its elements, the stored scale and zero are both +0.0 (bit pattern
+    0x0000) and every code is 0 -- the constant-group clause (scale 0, exact
+    reconstruction) with signed zeros read as one value."""
+    groups = [[-0.0, 0.0, 0.0, 0.0], [0.0, -0.0, 0.0, 0.0],
+              [-0.0, -0.0, -0.0, -0.0], [0.0, 0.0, -0.0, -0.0],
+              [-0.0, 0.0, -0.0, 0.0]]
+    for x in groups:
+        x = np.array(x, np.float32)
+        assert np.signbit(x).any() or not np.signbit(x).any()
+        codes, s32, s16, z16 = oracle_mod.quant_group(x, bits)
+        assert (s16, z16) == (0x0000, 0x0000), x
+        assert not np.signbit(np.float32(s32)), x
+        assert (codes == 0).all()
+
+
+def test_signed_zero_groups_through_the_cache(oracle_mod):
+    """The same through the cache, on both axes: a key channel group (g
+    tokens of one channel) and a value group (g channels of one token) made
+    of +-0 in both orders store scale and zero 0x0000 with all-zero codes;
+    the neighbouring groups are untouched by it."""
+    from oracle import OracleCache
+    rng = np.random.default_rng(15)
+    B, H, D, g, R = 1, 1, 16, 4, 4
+    S = 3 * g + R
+    K = rand_f16(rng, (B, H, S, D))
+    V = rand_f16(rng, (B, H, S, D))
+    nz = np.array([-0.0, 0.0, 0.0, -0.0], np.float16)
+    pz = np.array([0.0, -0.0, -0.0, 0.0], np.float16)
+    K[0, 0, 0:g, 3] = nz            # key group 0, channel 3: -0 first
+    K[0, 0, g:2 * g, 3] = pz        # key group 1, channel 3: +0 first
+    V[0, 0, 5, 4:8] = nz            # token 5, value group 1
+    V[0, 0, 6, 8:12] = pz           # token 6, value group 2
+    oc = OracleCache(B, H, H, D, 2, g, R, S)
+    oc.quantize(K, V, [S])
+    assert oc.lengths()[1][0] == 3 * g
+    ks, kz = oc.plane("Ks").view(np.uint16), oc.plane("Kz").view(np.uint16)
+    vs, vz = oc.plane("Vs").view(np.uint16), oc.plane("Vz").view(np.uint16)
+    for G in (0, 1):
+        assert ks[0, 0, G, 3] == 0 and kz[0, 0, G, 3] == 0
+        assert ks[0, 0, G, 2] != 0 and ks[0, 0, G, 4] != 0
+    assert vs[0, 0, 5, 1] == 0 and vz[0, 0, 5, 1] == 0
+    assert vs[0, 0, 6, 2] == 0 and vz[0, 0, 6, 2] == 0
+    assert vs[0, 0, 5, 0] != 0 and vs[0, 0, 6, 1] != 0
+    kc = np_unpack_rows(oc.plane("Kc")[0, 0, :3 * g], D, 2)
+    vc = np_unpack_rows(oc.plane("Vc")[0, 0, :3 * g], D, 2)
+    assert (kc[0:2 * g, 3] == 0).all()
+    assert (vc[5, 4:8] == 0).all() and (vc[6, 8:12] == 0).all()
+
+
+@pytest.mark.parametrize("bits,g", [(2, 4), (4, 8), (8, 4)])
+def test_whole_cache_reconstruction_bound(oracle_mod, bits, g):
+    """Every quantized element of a multi-sequence, multi-head ragged cache
+    is within half a step of the input it came from, on the axes the method
+    fixes: the key at (b, h, t, c) against the key group (t // g, c), the
+    value at (b, h, t, c) against the value group (t, c // g).  With only the
+    stored fp16 scale s16 at hand, the fp32 scale s32 it rounds from is
+    within half an fp16 unit of it, so the bound is
+    s16/2 + (2^b - 1 + 1/2) * u(s16), u = max(2^-11 s16, 2^-25) (the fp16
+    subnormal spacing is 2^-24).  Positions are indexed here independently
+    of the oracle, so a stride slip in the cache (wrong batch, head, token
+    or channel offset) breaks the bound."""
+    from oracle import OracleCache
+    rng = np.random.default_rng(16 + bits)
+    B, Hq, H, D, R = 3, 4, 2, 16, 5
+    lens = [3 * g + R + 2, R + 1, 7 * g + R]
+    S_max = max(lens) + 3
+    K = rand_f16(rng, (B, H, S_max, D), 3.0)
+    V = rand_f16(rng, (B, H, S_max, D), 0.5)
+    K += (np.arange(B)[:, None, None, None] * 10 +
+          np.arange(H)[None, :, None, None] * 4).astype(np.float16)
+    oc = OracleCache(B, Hq, H, D, bits, g, R, S_max)
+    oc.quantize(K, V, lens)
+    _, Tq, _ = oc.lengths()
+    P = (1 << bits) - 1
+    checked = 0
+    for b in range(B):
+        for h in range(H):
+            T = Tq[b]
+            if T == 0:
+                continue
+            kc = np_unpack_rows(oc.plane("Kc")[b, h, :T], D, bits).astype(np.float64)
+            vc = np_unpack_rows(oc.plane("Vc")[b, h, :T], D, bits).astype(np.float64)
+            ks = oc.plane("Ks")[b, h, :T // g].astype(np.float64)[np.arange(T) // g]
+            kz = oc.plane("Kz")[b, h, :T // g].astype(np.float64)[np.arange(T) // g]
+            vs = oc.plane("Vs")[b, h, :T].astype(np.float64)[:, np.arange(D) // g]
+            vz = oc.plane("Vz")[b, h, :T].astype(np.float64)[:, np.arange(D) // g]
+            for code, s, z, x in ((kc, ks, kz, K[b, h, :T]), (vc, vs, vz, V[b, h, :T])):
+                u = np.maximum(s * 2.0 ** -11, 2.0 ** -25)
+                bound = s / 2 + (P + 0.5) * u + 1e-12
+                err = np.abs(x.astype(np.float64) - (code * s + z))
+                assert (err <= bound).all(), (b, h, err.max())
+                checked += x.size
+    assert checked > 0
