@@ -9,7 +9,7 @@
 //   scale = (max - min) / (2^b - 1)
 //   code  = scale == 0 ? 0 : clamp(rint((x - min) / scale), 0, 2^b - 1)
 //   stored scale = fp16_rn(scale), stored zero = min (exact in fp16; a
-//   minimum of -0.0 is stored as +0.0).
+//   minimum of -0.0 is stored as +0.0, and a zero range as the scale +0.0).
 // Packing: code of channel e at byte e*b/8, bit (e*b) mod 8, LSB first.
 #include "vqk_internal.cuh"
 
@@ -238,7 +238,8 @@ k_flush(Geometry geo, Planes pl, const __half *__restrict__ Kin,
     float mn = fminf(__low2float(mn2), __high2float(mn2));
     const float mx = fmaxf(__low2float(mx2), __high2float(mx2));
     mn = __fadd_rn(mn, 0.0f);  // a -0.0 minimum is stored as +0.0
-    const float scale = __fdiv_rn(__fsub_rn(mx, mn), (float)levels);
+    // a zero range is +0.0 (max - min is -0.0 when the max is -0.0)
+    const float scale = __fdiv_rn(__fadd_rn(__fsub_rn(mx, mn), 0.0f), (float)levels);
     const float rcp = scale != 0.0f ? __frcp_rn(scale) : 0.0f;
     const size_t idx = (bh * (geo.Tcap / g) + P0 / g) * D + c;
     const __half sh = __float2half_rn(scale);
@@ -285,7 +286,8 @@ k_flush(Geometry geo, Planes pl, const __half *__restrict__ Kin,
     float mn = fminf(__low2float(mn2), __high2float(mn2));
     const float mx = fmaxf(__low2float(mx2), __high2float(mx2));
     mn = __fadd_rn(mn, 0.0f);  // a -0.0 minimum is stored as +0.0
-    const float scale = __fdiv_rn(__fsub_rn(mx, mn), (float)levels);
+    // a zero range is +0.0 (max - min is -0.0 when the max is -0.0)
+    const float scale = __fdiv_rn(__fadd_rn(__fsub_rn(mx, mn), 0.0f), (float)levels);
     const float rcp = scale != 0.0f ? __frcp_rn(scale) : 0.0f;
     uint32_t *crow = reinterpret_cast<uint32_t *>(codes + i * CS + j * g);
     for (int k = 0; k < g; k += 8) {

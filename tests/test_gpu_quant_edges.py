@@ -90,3 +90,26 @@ def test_half_integer_quotients(lib, bits, g):
     K = (m * 2.0 ** e_ch).astype(np.float16)[None, None]
     V = (m * 2.0 ** e_tok).astype(np.float16)[None, None]
     _compare(K, V, bits, g, R)
+
+
+@pytest.mark.parametrize("bits,g", [(2, 16), (4, 32), (8, 16)])
+def test_signed_zero_groups(lib, bits, g):
+    """Groups made only of +0.0 and -0.0, in both orders (a -0.0 first and a
+    +0.0 first), on key channels and on value groups: the stored scale and
+    zero are +0.0 and the codes 0, bit for bit as in the oracle, whatever the
+    order in which the kernel's min/max reduction meets the two zeros."""
+    rng = np.random.default_rng(200 + bits + g)
+    D, R = 64, 16
+    S = 4 * g + R
+    K = rng.standard_normal((1, 1, S, D)).astype(np.float16)
+    V = rng.standard_normal((1, 1, S, D)).astype(np.float16)
+    nf = np.resize(np.array([-0.0, 0.0], np.float16), g)   # -0 first
+    pf = np.resize(np.array([0.0, -0.0], np.float16), g)   # +0 first
+    allneg = np.full(g, -0.0, np.float16)
+    for G, col in enumerate((nf, pf, allneg, pf[::-1])):
+        K[0, 0, G * g:(G + 1) * g, 7 + G] = col
+        K[0, 0, G * g:(G + 1) * g, 40] = col if G % 2 else col[::-1]
+    for t, col in ((1, nf), (2, pf), (g + 3, allneg), (2 * g, nf[::-1])):
+        j = t % (D // g)
+        V[0, 0, t, j * g:(j + 1) * g] = col
+    _compare(K, V, bits, g, R)
