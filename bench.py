@@ -16,6 +16,14 @@ planes + fp16 residual + q + out).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
   python bench.py --report [WORKLOAD ...]    # secondary figures, see run_report
+  python bench.py --profile-decode WORKLOAD N  # N decodes of one cache (ncu)
+
+The timed region repeats passes of exactly K steps until about 0.6 s of
+device time has elapsed (so that the clock sampler sees the load); `value` is
+the median pass's time per step, with the 10th and 90th percentiles beside
+it.  The same line carries `targets`: the decode (and, for the 4-bit
+workload, the 512-token append) of every workload with S_kv >= 32768 or
+served in batches, each with its algorithmic bytes and HBM fraction.
 """
 from __future__ import annotations
 
@@ -35,6 +43,14 @@ if ROOT not in sys.path:
 METRIC = "fused 2-bit KV decode-attend: µs/step and HBM GB/s (% of GB300 peak)"
 UNIT = "us/step"
 DEFAULT_WORKLOAD = "pages_S65536"
+# GB300's nominal HBM3e bandwidth (about 8 TB/s); fractions against it are
+# reported beside the ones against the measured copy bandwidth
+NOMINAL_HBM_GBS = 8000.0
+# device seconds the sustained timed region lasts at least
+SUSTAIN_S = 0.6
+# the decode workloads reported in `targets` (S_kv >= 32768 or batched)
+TARGET_WORKLOADS = ("pages_S32768", "gqa_serving", "int4_append",
+                    "ragged_long")
 
 
 # ---------------------------------------------------------------------------
@@ -236,12 +252,14 @@ def oracle_steps(w, budget_s: float = 12.0, max_steps: int = 8, inputs=None):
 # main
 # ---------------------------------------------------------------------------
 
-def oracle_sampled_steps(w, warmup: int, steps: int):
-    """The CPU oracle on `warmup` + `steps` steps of the workload, each one a
-    bounded sample: the whole append (one token per sequence), then the
-    decode-attend of ONE query head (rotating over all B * H_q of them),
-    its time scaled by B * H_q to the full step.  Returns
-    (us_per_step over the timed steps, setup_s)."""
+def oracle_whole_steps(w, warmup: int, steps: int, budget_s: float = 200.0):
+    """The CPU oracle on `warmup` + `steps` steps of the workload: each step
+    appends one token per sequence and runs the decode-attend of every query
+    head (a whole step).  The first warm-up step is timed to project the
+    run; if whole steps would take longer than `budget_s`, each step instead
+    runs the decode-attend of a rotating subset of the query heads, its time
+    scaled to all of them (said in the returned sample text).  Returns
+    (us_per_step over the timed steps, setup_s, sample)."""
     import oracle
     from bit_kv_cache_05_gb300 import synth
     t0 = time.perf_counter()
@@ -253,28 +271,45 @@ def oracle_sampled_steps(w, warmup: int, steps: int):
     K1, V1, q = K1.numpy(), V1.numpy(), q.numpy()
     setup = time.perf_counter() - t0
     heads = w.B * w.H_q
-    total = 0.0
+    per_step = heads                   # query heads attended per step
+    total, cursor = 0.0, 0
     for i in range(warmup + steps):
         a = time.perf_counter()
         oc.append(K1[i], V1[i], [1] * w.B)
         b = time.perf_counter()
-        j = i % heads
-        oc.attend_one(j // w.H_q, j % w.H_q, q[i, j // w.H_q, j % w.H_q])
+        if per_step == heads:
+            oc.attend(q[i])
+        else:
+            for _ in range(per_step):
+                j = cursor % heads
+                cursor += 1
+                oc.attend_one(j // w.H_q, j % w.H_q, q[i, j // w.H_q, j % w.H_q])
         c = time.perf_counter()
+        if i == 0:
+            full = (b - a) + (c - b) * heads / per_step
+            left = warmup + steps - 1
+            if left * full > budget_s:
+                per_step = max(1, int(heads * budget_s / (left * full)))
         if i >= warmup:
-            total += (b - a) + (c - b) * heads
+            total += (b - a) + (c - b) * heads / per_step
     del oc
-    return 1e6 * total / max(steps, 1), setup
+    if per_step == heads:
+        sample = (f"{warmup} untimed + {steps} timed whole steps (append one "
+                  f"token per sequence, decode-attend all {heads} query "
+                  f"heads) after an untimed {setup:.1f}s prefill")
+    else:
+        sample = (f"{warmup} untimed + {steps} timed steps after an untimed "
+                  f"{setup:.1f}s prefill; each appends one token per sequence "
+                  f"and attends {per_step} of the {heads} query heads "
+                  f"(rotating), scaled to all (whole steps would exceed "
+                  f"{budget_s:.0f}s)")
+    return 1e6 * total / max(steps, 1), setup, sample
 
 
 def run_reference(args, w, rank, world):
     if rank != 0:
         return
-    us, setup = oracle_sampled_steps(w, args.warmup, args.steps)
-    sample = (f"{args.warmup} untimed + {args.steps} timed steps after an "
-              f"untimed {setup:.1f}s prefill; each step appends one token per "
-              f"sequence and runs the decode-attend of one query head "
-              f"(rotating), scaled by B*H_q = {w.B * w.H_q}")
+    us, setup, sample = oracle_whole_steps(w, args.warmup, args.steps)
     line = {
         "impl": "reference", "metric": METRIC, "value": round(us, 3),
         "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
@@ -292,11 +327,20 @@ def run_reference(args, w, rank, world):
 
 
 def config_of(w):
+    """The workload as both arms name it (identical keys and values)."""
     return {"workload": w.name, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv,
             "D": w.D, "bits": w.bits, "group": w.group,
             "residual": w.residual, "S_kv": w.seq_lens[0] if w.B == 1
             else w.seq_lens, "S_q": 1,
-            "step": "append 1 token per sequence + fused decode-attend"}
+            "step": "append 1 token per sequence + fused decode-attend",
+            "l2": "inputs larger than L2 (the GPU arm rotates cache copies "
+                  "totalling more than 4x L2)",
+            "parallelism": "replicas (one independent cache per GPU)"}
+
+
+def _pct(xs, q):
+    xs = sorted(xs)
+    return xs[min(len(xs) - 1, int(q * len(xs)))]
 
 
 def run_ours(args, w, rank, world, local):
@@ -309,62 +353,78 @@ def run_ours(args, w, rank, world, local):
     _lib.load()
     K_steps = args.steps
     W = args.warmup
-    n_total = W + K_steps
-    inp = synth.make_inputs(w, device=dev)
-    K1, V1, q = synth.decode_tokens(w, max(n_total, 1), device=dev)
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20
     step_bytes = decode_bytes(w, w.seq_lens)
     n_copies = max(2, -(-4 * l2 // step_bytes))
-    headroom = n_total + 64
+    # steps the run may take: warm-up, the sustained passes (at most
+    # max_sustain steps), the decode-alone and end-to-end loops
+    max_sustain = max(K_steps, 16384)
+    n_total = W + max_sustain + 2 * K_steps
+    inp = synth.make_inputs(w, device=dev)
+    K1, V1, q = synth.decode_tokens(w, 64, device=dev)
+    headroom = -(-n_total // n_copies) + 64
     caches = [KiviCache(inp["K"], inp["V"], w.seq_lens, H_q=w.H_q,
                         bits=w.bits, group=w.group, residual=w.residual,
-                        max_seq=w.max_seq + 3 * headroom)
+                        max_seq=w.max_seq + headroom)
               for _ in range(n_copies)]
     del inp
     out = torch.empty(w.B, w.H_q, w.D, dtype=torch.float32, device=dev)
     ones = [1] * w.B
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
+    cursor = [0]
 
-    def step(i):
+    def step():
+        i = cursor[0]
+        cursor[0] += 1
         c = caches[i % n_copies]
-        c.append(K1[i], V1[i], ones)
-        c.decode_attend(q[i], out)
+        c.append(K1[i % 64], V1[i % 64], ones)
+        c.decode_attend(q[i % 64], out)
 
-    # warm-up
-    for i in range(W):
-        step(i)
+    # warm-up, timed as a whole to size the sustained region
+    wa = torch.cuda.Event(enable_timing=True)
+    wb = torch.cuda.Event(enable_timing=True)
+    wa.record(stream)
+    for _ in range(W):
+        step()
+    wb.record(stream)
     torch.cuda.synchronize(dev)
+    est_ms = max(wa.elapsed_time(wb) / W, 1e-3)
+    passes = int(max(1, min(max_sustain // K_steps,
+                            -(-SUSTAIN_S * 1e3 // (est_ms * K_steps)))))
+    passes = int(max_over_ranks(passes, world, dev))
 
     peak, peak_kind = measured_peak_gbs()
     with ClockSampler(local) as clk:
-        # (1) the timed steps
+        # (1) the timed region: `passes` passes of exactly K steps each
         barrier(world)
         torch.cuda.synchronize(dev)
         l0 = _lib.launch_count()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(W, n_total):
-            step(i)
-        e1.record(stream)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(passes + 1)]
+        ev[0].record(stream)
+        for p in range(passes):
+            for _ in range(K_steps):
+                step()
+            ev[p + 1].record(stream)
         torch.cuda.synchronize(dev)
-        launches = _lib.launch_count() - l0
-        ms = e0.elapsed_time(e1) / K_steps
+        launches = (_lib.launch_count() - l0) / passes
+        pass_ms = [ev[p].elapsed_time(ev[p + 1]) / K_steps for p in range(passes)]
+        device_s = ev[0].elapsed_time(ev[passes]) / 1e3
+        ms = statistics.median(pass_ms)
         ms = max_over_ranks(ms, world, dev)
         barrier(world)
 
         # (2) the decode launch alone, per-launch events, rotating copies
-        ev = [(torch.cuda.Event(enable_timing=True),
+        dv = [(torch.cuda.Event(enable_timing=True),
                torch.cuda.Event(enable_timing=True)) for _ in range(K_steps)]
         for i in range(K_steps):
-            c = caches[(i + 1) % n_copies]
-            ev[i][0].record(stream)
-            c.decode_attend(q[i], out)
-            ev[i][1].record(stream)
+            c = caches[(cursor[0] + i) % n_copies]
+            dv[i][0].record(stream)
+            c.decode_attend(q[i % 64], out)
+            dv[i][1].record(stream)
         torch.cuda.synchronize(dev)
-        dec_ms = [a.elapsed_time(b) for a, b in ev]
+        dec_ms = [a.elapsed_time(b) for a, b in dv]
         dec_avg = sum(dec_ms) / len(dec_ms)
 
         # (3) end to end through the public API from pinned host memory
@@ -372,8 +432,8 @@ def run_ours(args, w, rank, world, local):
         # one pinned buffer, so that they cross in one copy; the cache calls
         # take views of the device copy
         nK, nV, nq = K1[0].numel(), V1[0].numel(), q[0].numel()
-        hin = torch.cat([K1.reshape(n_total, nK), V1.reshape(n_total, nV),
-                         q.reshape(n_total, nq)], dim=1).cpu().pin_memory()
+        hin = torch.cat([K1.reshape(64, nK), V1.reshape(64, nV),
+                         q.reshape(64, nq)], dim=1).cpu().pin_memory()
         hout = torch.empty(K_steps, w.B, w.H_q, w.D, dtype=torch.float32
                            ).pin_memory()
         din = torch.empty(nK + nV + nq, dtype=K1.dtype, device=dev)
@@ -386,8 +446,8 @@ def run_ours(args, w, rank, world, local):
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
         for i in range(K_steps):
-            c = caches[(i + 2) % n_copies]
-            din.copy_(hin[W + i], non_blocking=True)
+            c = caches[(cursor[0] + i) % n_copies]
+            din.copy_(hin[i % 64], non_blocking=True)
             c.append(dK, dV, ones)
             c.decode_attend(dq, out)
             hout[i].copy_(out, non_blocking=True)
@@ -396,11 +456,25 @@ def run_ours(args, w, rank, world, local):
         e2e_ms = max_over_ranks(t0.elapsed_time(t1) / K_steps, world, dev)
 
     clocks = clk.summary()
-    S_now = [s + n_total for s in w.seq_lens]
-    dec_bytes = decode_bytes(w, S_now)
+    S_dec = caches[cursor[0] % n_copies].lengths()[0]
+    dec_bytes = decode_bytes(w, S_dec)
     achieved = dec_bytes / (dec_avg * 1e-3) / 1e9
     h2d = (K1[0].numel() + V1[0].numel() + q[0].numel()) * 2
     d2h = out.numel() * 4
+    for c in caches:
+        c.close()
+    del caches
+    torch.cuda.empty_cache()
+
+    targets = None
+    if rank == 0 and not args.no_targets:
+        targets = {}
+        for name in TARGET_WORKLOADS:
+            if name == w.name:
+                continue
+            targets[name] = measure_workload(synth.workload(name), peak,
+                                             full=False)
+            torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -409,8 +483,6 @@ def run_ours(args, w, rank, world, local):
                "cores": 1,
                "sample": f"{n} whole steps (append 1 token/seq + decode-attend "
                          f"all heads) after an untimed {setup:.1f}s prefill"}
-    for c in caches:
-        c.close()
     if rank != 0:
         return
     line = {
@@ -419,9 +491,14 @@ def run_ours(args, w, rank, world, local):
         "ms_per_step": round(ms, 6), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded, N(0,1) fp16 K/V/q)",
-        "config": dict(config_of(w), l2=f"rotating {n_copies} cache copies "
-                       f"({n_copies * step_bytes / 1e6:.0f} MB > 4x L2)",
-                       parallelism=f"replicas x{world}"),
+        "config": config_of(w),
+        "timing": {"passes": passes, "steps_per_pass": K_steps,
+                   "stat": "median over passes of the pass time / K",
+                   "p10_us": round(_pct(pass_ms, 0.1) * 1e3, 3),
+                   "p90_us": round(_pct(pass_ms, 0.9) * 1e3, 3),
+                   "device_s": round(device_s, 3),
+                   "l2": f"rotating {n_copies} cache copies "
+                         f"({n_copies * step_bytes / 1e6:.0f} MB > 4x L2)"},
         "decode_us": round(dec_avg * 1e3, 3),
         "decode_gbs": round(achieved, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
@@ -429,16 +506,147 @@ def run_ours(args, w, rank, world, local):
                      "frac": round(achieved / peak, 4),
                      "traffic": measured_traffic(w.name),
                      "peak_kind": peak_kind,
+                     "frac_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "nominal_peak": NOMINAL_HBM_GBS,
                      "kernel": "fused decode-attend + partial merge "
                                "(k_decode_mma, k_merge_mma; timed together)",
                      "algorithmic_bytes": dec_bytes},
+        "targets": targets,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_ms * 1e3, 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": int(launches),
+        "gpu_launches": int(round(launches)),
+        "gpu_launches_per": "pass of K steps",
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
+
+
+def measure_workload(w, peak, full=True):
+    """The decode of workload `w` from HBM (rotating over cache copies larger
+    than 4x L2, the median of 100 launches), and the append of the
+    workload's appended tokens per sequence (one token when it appends none)
+    timed over at least 8 caches.  With `full`, also the decode hot (one
+    cache, repeated), the prefill (the quantize call) and the unfused path
+    the pages compare the fused decode against: this library's dequantize
+    to fp16 K_hat / V_hat in memory, then torch's
+    scaled_dot_product_attention over them (a context row, not a target)."""
+    import torch
+    import torch.nn.functional as F
+    from bit_kv_cache_05_gb300 import synth
+    from bit_kv_cache_05_gb300.cache import KiviCache
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    inp = synth.make_inputs(w, device="cuda")
+    n_app = w.n_append if w.n_append else 1
+    S_dec = [s + n_app for s in w.seq_lens]
+    nb = decode_bytes(w, S_dec)
+    ncp = max(2, -(-4 * l2 // nb))
+    if nb * ncp > 8e9:
+        ncp = 2
+    caches = []
+
+    def make(i):
+        caches.append(KiviCache(inp["K"], inp["V"], w.seq_lens, H_q=w.H_q,
+                                bits=w.bits, group=w.group,
+                                residual=w.residual,
+                                max_seq=w.max_seq + n_app + 8))
+    # prefill and append are timed over at least 8 caches; the decode
+    # rotates over the first ncp
+    na = max(ncp, 8)
+    prefill = _ev_times(make, na)
+    K1, V1, _ = synth.decode_tokens(w, 1, device="cuda")
+    if w.n_append:
+        Kn = inp["K_new"]
+        Vn = inp["V_new"]
+    else:
+        Kn, Vn = K1[0], V1[0]
+    app = _ev_times(lambda i: caches[i].append(Kn, Vn, [n_app] * w.B), na)
+    for c in caches[ncp:]:
+        c.close()
+    del caches[ncp:]
+    del inp["K"], inp["V"]
+    q = inp["q"]
+    out = torch.empty(w.B, w.H_q, w.D, device="cuda")
+    for i in range(2 * ncp):
+        caches[i % ncp].decode_attend(q, out)
+    flushed = _ev_times(lambda i: caches[i % ncp].decode_attend(q, out), 100)
+    caches[0].device_status()
+    ab = (append_bytes(w, n_app) if not w.n_append
+          else flush_append_bytes(w, n_app))
+    res = {
+        "config": {"B": w.B, "H_q": w.H_q, "H_kv": w.H_kv, "D": w.D,
+                   "bits": w.bits, "group": w.group, "residual": w.residual,
+                   "S_kv": S_dec[0] if len(set(S_dec)) == 1 else S_dec},
+        "decode_us": round(flushed[0], 2),
+        "decode_p10_p90_us": [round(flushed[1], 2), round(flushed[2], 2)],
+        "decode_bytes": nb,
+        "decode_frac": round(nb / (flushed[0] * 1e-6) / 1e9 / peak, 4),
+        "decode_frac_nominal": round(nb / (flushed[0] * 1e-6) / 1e9
+                                     / NOMINAL_HBM_GBS, 4),
+        "cache_copies": ncp,
+        "append_tokens_per_seq": n_app, "append_us": round(app[0], 2),
+        "append_bytes": ab,
+        "append_frac": round(ab / (app[0] * 1e-6) / 1e9 / peak, 4),
+    }
+    if full:
+        hot = _ev_times(lambda i: caches[0].decode_attend(q, out), 100)
+        fused = out.clone()
+        smax = max(S_dec)
+        shape = (w.B, w.H_kv, smax, w.D)
+        # zeroed: padding rows of short sequences stay finite under the mask
+        Kh = torch.zeros(shape, dtype=torch.float16, device="cuda")
+        Vh = torch.zeros(shape, dtype=torch.float16, device="cuda")
+        caches[0].dequantize(out=(Kh, Vh))
+        dq = _ev_times(lambda i: caches[0].dequantize(out=(Kh, Vh)), 10)
+        q4 = q.view(w.B, w.H_q, 1, w.D)
+        g = w.H_q // w.H_kv
+        kw = {"enable_gqa": True} if g > 1 else {}
+
+        def sdpa(i):
+            if min(S_dec) == smax:
+                return F.scaled_dot_product_attention(q4, Kh, Vh, **kw)
+            # ragged: one call per sequence over its own length (no mask)
+            return torch.cat([F.scaled_dot_product_attention(
+                q4[b:b + 1], Kh[b:b + 1, :, :S_dec[b]], Vh[b:b + 1, :, :S_dec[b]],
+                **kw) for b in range(w.B)])
+        ref = sdpa(0).float().view(w.B, w.H_q, w.D)
+        at = _ev_times(sdpa, 10)
+        res.update({
+            "decode_hot_us": round(hot[0], 2),
+            "prefill_us": round(prefill[0], 1),
+            "unfused": {"dequantize_us": round(dq[0], 1),
+                        "sdpa_us": round(at[0], 1),
+                        "total_us": round(dq[0] + at[0], 1),
+                        "fused_speedup": round((dq[0] + at[0]) / flushed[0], 2),
+                        "max_abs_diff_vs_fused": float((ref - fused).abs().max())},
+        })
+        del Kh, Vh, ref
+    for c in caches:
+        c.close()
+    del caches, inp
+    return res
+
+
+def flush_append_bytes(w, n_new):
+    """Algorithmic bytes of appending n_new tokens per sequence to a cache
+    whose residual holds w.residual tokens (the workload's state): read the
+    old residual and the new fp16 K/V rows, write the flushed groups as
+    packed codes plus fp16 scale/zero, and the tokens left in the ring."""
+    D, g, bits, R = w.D, w.group, w.bits, w.residual
+    row = D * bits // 8
+    tot = 0
+    for S in w.seq_lens:
+        Tq0 = 0 if S < R else g * ((S - R) // g)
+        S1 = S + n_new
+        Tq1 = 0 if S1 < R else g * ((S1 - R) // g)
+        nres0, nres1 = S - Tq0, S1 - Tq1
+        flushed = Tq1 - Tq0
+        rd = (nres0 + n_new) * D * 2 * 2
+        wr = flushed * (2 * row + (2 * D * 2) / g + 2 * (D // g) * 2)
+        # tokens that stay fp16: the new ones written to the ring
+        wr += min(nres1, n_new) * D * 2 * 2
+        tot += w.H_kv * (rd + wr)
+    return int(tot)
 
 
 REPORT_WORKLOADS = ("pages_S8192", "pages_S32768", "pages_S65536",
@@ -464,121 +672,93 @@ def _ev_times(fn, n):
 
 
 def run_report(names):
-    """Secondary figures, one JSON line per workload: the decode from HBM
-    (rotating over cache copies larger than 4x L2) and hot (one cache,
-    repeated), the append (the workload's appended tokens per sequence, else
-    one), the quantize of the initial cache (prefill), and the unfused path
-    the pages compare the fused decode against: this library's dequantize to
-    fp16 K_hat / V_hat in memory, then torch's scaled_dot_product_attention
-    over them (a context row, not a target)."""
+    """Secondary figures, one JSON line per workload (measure_workload with
+    the hot decode, the prefill and the unfused context path)."""
     import torch
-    import torch.nn.functional as F
     from bit_kv_cache_05_gb300 import synth
-    from bit_kv_cache_05_gb300.cache import KiviCache
     peak, peak_kind = measured_peak_gbs()
-    l2 = torch.cuda.get_device_properties(0).L2_cache_size
     for name in names:
-        w = synth.workload(name)
-        inp = synth.make_inputs(w, device="cuda")
-        n_app = w.n_append if w.n_append else 1
-        S_dec = [s + n_app for s in w.seq_lens]
-        nb = decode_bytes(w, S_dec)
-        ncp = max(2, -(-4 * l2 // nb))
-        if nb * ncp > 8e9:
-            ncp = 2
-        caches = []
-
-        def make(i):
-            caches.append(KiviCache(inp["K"], inp["V"], w.seq_lens, H_q=w.H_q,
-                                    bits=w.bits, group=w.group,
-                                    residual=w.residual,
-                                    max_seq=w.max_seq + n_app + 8))
-        # prefill and append are timed over at least 8 caches; the decode
-        # rotates over the first ncp
-        na = max(ncp, 8)
-        prefill = _ev_times(make, na)
-        K1, V1, _ = synth.decode_tokens(w, 1, device="cuda")
-        if w.n_append:
-            Kn = inp["K_new"]
-            Vn = inp["V_new"]
-        else:
-            Kn, Vn = K1[0], V1[0]
-        app = _ev_times(lambda i: caches[i].append(Kn, Vn, [n_app] * w.B), na)
-        for c in caches[ncp:]:
-            c.close()
-        del caches[ncp:]
-        del inp["K"], inp["V"]
-        q = inp["q"]
-        out = torch.empty(w.B, w.H_q, w.D, device="cuda")
-        for i in range(2 * ncp):
-            caches[i % ncp].decode_attend(q, out)
-        flushed = _ev_times(lambda i: caches[i % ncp].decode_attend(q, out), 100)
-        hot = _ev_times(lambda i: caches[0].decode_attend(q, out), 100)
-        caches[0].device_status()
-        fused = out.clone()
-        # the unfused context path
-        smax = max(S_dec)
-        shape = (w.B, w.H_kv, smax, w.D)
-        # zeroed: padding rows of short sequences stay finite under the mask
-        Kh = torch.zeros(shape, dtype=torch.float16, device="cuda")
-        Vh = torch.zeros(shape, dtype=torch.float16, device="cuda")
-        caches[0].dequantize(out=(Kh, Vh))
-        dq = _ev_times(lambda i: caches[0].dequantize(out=(Kh, Vh)), 10)
-        q4 = q.view(w.B, w.H_q, 1, w.D)
-        g = w.H_q // w.H_kv
-        kw = {"enable_gqa": True} if g > 1 else {}
-
-        def sdpa(i):
-            if min(S_dec) == smax:
-                return F.scaled_dot_product_attention(q4, Kh, Vh, **kw)
-            # ragged: one call per sequence over its own length (no mask)
-            return torch.cat([F.scaled_dot_product_attention(
-                q4[b:b + 1], Kh[b:b + 1, :, :S_dec[b]], Vh[b:b + 1, :, :S_dec[b]],
-                **kw) for b in range(w.B)])
-        ref = sdpa(0).float().view(w.B, w.H_q, w.D)
-        at = _ev_times(sdpa, 10)
-        line = {
-            "workload": name, "peak_gbs": peak, "peak_kind": peak_kind,
-            "decode_bytes": nb, "cache_copies": ncp,
-            "decode_us": round(flushed[0], 2),
-            "decode_p10_p90_us": [round(flushed[1], 2), round(flushed[2], 2)],
-            "decode_frac": round(nb / (flushed[0] * 1e-6) / 1e9 / peak, 3),
-            "decode_hot_us": round(hot[0], 2),
-            "append_tokens_per_seq": n_app, "append_us": round(app[0], 2),
-            "prefill_us": round(prefill[0], 1),
-            "unfused": {"dequantize_us": round(dq[0], 1),
-                        "sdpa_us": round(at[0], 1),
-                        "total_us": round(dq[0] + at[0], 1),
-                        "fused_speedup": round((dq[0] + at[0]) / flushed[0], 2),
-                        "max_abs_diff_vs_fused": float((ref - fused).abs().max())},
-        }
-        print(json.dumps(line), flush=True)
-        for c in caches:
-            c.close()
-        del caches, Kh, Vh, inp, ref
+        res = measure_workload(synth.workload(name), peak, full=True)
+        print(json.dumps(dict(workload=name, peak_gbs=peak, peak_kind=peak_kind,
+                              **res)), flush=True)
         torch.cuda.empty_cache()
 
 
+def run_profile_decode(name: str, n: int):
+    """One cache of a named workload and n decode launches on it, for ncu
+    captures of the decode kernels (and of the prefill's k_flush)."""
+    import torch
+    from bit_kv_cache_05_gb300 import synth
+    from bit_kv_cache_05_gb300.cache import KiviCache
+    w = synth.workload(name)
+    inp = synth.make_inputs(w, device="cuda")
+    c = KiviCache(inp["K"], inp["V"], w.seq_lens, H_q=w.H_q, bits=w.bits,
+                  group=w.group, residual=w.residual, max_seq=w.max_seq)
+    del inp["K"], inp["V"]
+    torch.cuda.synchronize()
+    out = None
+    for _ in range(n):
+        out = c.decode_attend(inp["q"])
+    torch.cuda.synchronize()
+    c.device_status()
+    print("ok", name, c.decode_kernel(),
+          float(out.abs().max()) if out is not None else 0.0)
+    c.close()
+
+
+def _respawn_under_torchrun(args, argv):
+    """`--gpus N` (N > 1) without a torch.distributed launcher: start N local
+    ranks with torch.distributed.run (rendezvous on 127.0.0.1) and return
+    its exit status."""
+    import socket
+    sock = socket.socket()
+    sock.bind(("127.0.0.1", 0))
+    port = sock.getsockname()[1]
+    sock.close()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1",
+           "--master-port", str(port), os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
 def main(argv=None):
+    argv = list(sys.argv[1:] if argv is None else argv)
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-targets", action="store_true",
+                    help="leave out the decode of the other target workloads")
     ap.add_argument("--report", nargs="*", default=None,
                     help="secondary figures for these workloads (all when "
                          "none are named) instead of the benchmark line")
+    ap.add_argument("--profile-decode", nargs=2, metavar=("WORKLOAD", "N"),
+                    default=None,
+                    help="build one cache and run N decodes (for ncu)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.steps < 1 or args.gpus < 1:
+        ap.error("--steps and --gpus must be >= 1")
+    if args.profile_decode is not None:
+        run_profile_decode(args.profile_decode[0], int(args.profile_decode[1]))
+        return 0
     if args.report is not None:
         run_report(args.report or list(REPORT_WORKLOADS))
-        return
+        return 0
+    rank, world, local = dist_env()
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        return _respawn_under_torchrun(args, argv)
+    if world != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; launch "
+              f"one rank per GPU (or run without a launcher and let bench.py "
+              f"start the ranks)", file=sys.stderr)
+        return 2
     from bit_kv_cache_05_gb300 import synth
     w = synth.workload(args.workload)
-    rank, world, local = dist_env()
     if world > 1:
         import torch.distributed as dist
         backend = "nccl" if args.impl == "ours" else "gloo"
@@ -595,7 +775,8 @@ def main(argv=None):
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()
+    return 0
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main())

@@ -218,7 +218,10 @@ int vq_kivi_debug_fail_chunk(vq_kivi_cache *c, int32_t chunk);
  * would synchronize the device).  It computes the same fused decode step as
  * vq_kivi_decode_attend, from cache planes that the caller keeps in its own
  * device memory, and allocates nothing: no cudaMalloc, no cudaFree, no
- * allocating library call.
+ * allocating library call.  It runs the CUDA-core split-KV kernel over
+ * packed-order planes for every shape (vq_kivi_decode_attend uses the
+ * tensor-core kernel for D = 64 or 128 with at most 4 query heads per kv
+ * head), so it is slower than the regular entry point on those shapes.
  *
  * Scratch: the split-KV partial results go to one fixed array of
  * VQ_KIVI_STATIC_SCRATCH_BYTES in this library's device memory, which every
@@ -228,7 +231,13 @@ int vq_kivi_debug_fail_chunk(vq_kivi_cache *c, int32_t chunk);
  * from two threads -- race and give wrong results: serialize them.  The first
  * call on each device looks up the array's device address on that device
  * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.
+ * before any stream capture.  With lazy module loading (CUDA_MODULE_LOADING
+ * = LAZY, the default) that first call is also when the driver loads this
+ * library's device code and the array onto the device: the one allocation
+ * this entry point causes, made by the driver, once per device; later calls
+ * allocate nothing.  The address stays valid for the life of the device's
+ * primary context: after cudaDeviceReset (or anything else that destroys
+ * that context) do not call this entry point again in the same process.
  *
  * Planes (device memory, 16-byte aligned; Tcap = ceil(max_seq/g)*g, at least
  * g; R = residual; per sequence T_q and n_res follow the residual rule):

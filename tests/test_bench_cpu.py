@@ -68,3 +68,53 @@ def test_reference_arm_prints_one_json_line():
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["e2e"]["d2h_bytes_per_step"] == 0
+    # whole steps (every query head attended), and the same config as the
+    # GPU arm names (both come from config_of)
+    assert "whole steps" in d["cpu_baseline"]["sample"]
+    import bench
+    from bit_kv_cache_05_gb300 import synth
+    assert d["config"] == json.loads(json.dumps(bench.config_of(synth.workload("tiny"))))
+
+
+def _run_bench(args, env_extra=None, drop=("RANK", "WORLD_SIZE", "LOCAL_RANK")):
+    env = {k: v for k, v in os.environ.items() if k not in drop}
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    env.update(env_extra or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args],
+                          capture_output=True, text=True, timeout=900, env=env,
+                          cwd=ROOT)
+
+
+def test_gpus_without_a_launcher_starts_the_ranks():
+    """--gpus 2 with no torch.distributed launcher: bench.py starts two local
+    ranks itself (torch.distributed.run on 127.0.0.1); for the reference arm
+    rank 0 alone prints its line and the other rank exits 0."""
+    r = _run_bench(["--impl", "reference", "--gpus", "2", "--workload", "tiny",
+                    "--steps", "1", "--warmup", "3"])
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [l for l in r.stdout.strip().splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
+
+
+def test_gpus_that_disagree_with_the_launcher_fail():
+    """A launcher that started a different number of ranks than --gpus asks
+    for is an error (exit status 2), not a silent single replica."""
+    r = _run_bench(["--impl", "reference", "--gpus", "2", "--workload", "tiny",
+                    "--steps", "1", "--warmup", "3"],
+                   env_extra={"WORLD_SIZE": "1", "RANK": "0", "LOCAL_RANK": "0"})
+    assert r.returncode == 2
+    assert "WORLD_SIZE" in r.stderr
+
+
+def test_flush_append_bytes_of_the_4bit_workload():
+    """The 512-token append of the 4-bit workload (R = 64 tokens in the
+    residual before it, 64 after): per (b, kv head) read 64 + 512 fp16 K and V
+    rows, write 512 quantized token-heads of 144 B and 64 fp16 K and V rows."""
+    import bench
+    from bit_kv_cache_05_gb300 import synth
+    w = synth.workload("int4_append")
+    per_head = (64 + 512) * 512 + 512 * 144 + 64 * 512
+    assert per_head == 401408
+    assert bench.flush_append_bytes(w, 512) == 8 * 32 * per_head

@@ -95,8 +95,15 @@ def test_static_decode_matches_regular_decode_twice(lib, w):
     out1 = torch.empty_like(ref1)
     out2 = torch.empty_like(ref2)
     call_static(lib, c, planes, q1, out1)
+    torch.cuda.synchronize()
+    # after the first call (which may load the library's device code and the
+    # scratch array), a call changes neither the device's free memory nor
+    # torch's pool
+    free0, reserved0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_reserved()
     call_static(lib, c, planes, q2, out2)
     torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert torch.cuda.memory_reserved() == reserved0
     close_enough(out1, ref1)
     close_enough(out2, ref2)
     c.close()
