@@ -64,6 +64,7 @@ def _load():
         lib.orc_append.argtypes = [P, P, P, i64, P]
         lib.orc_attend.argtypes = [P, P, f64, P]
         lib.orc_attend_one.argtypes = [P, i32, i32, P, f64, P]
+        lib.orc_attend_multi.argtypes = [P, P, i32, f64, P]
         lib.orc_lengths.argtypes = [P, P, P, P]
         lib.orc_dims.argtypes = [P, P, P]
         lib.orc_plane_bytes.restype = ctypes.c_size_t
@@ -183,6 +184,21 @@ class OracleCache:
         out = np.zeros((self.B, self.H_q, self.D), np.float32)
         sc = (1.0 / np.sqrt(self.D)) if scale is None else float(scale)
         self._lib.orc_attend(self._c, _ptr(q), sc, _ptr(out))
+        return out
+
+    def attend_multi(self, q, scale=None) -> np.ndarray:
+        """q: fp16 [B][H_q][S_q][D], the queries of each sequence's newest
+        S_q tokens (query i at position S - S_q + i, causal).  Returns fp32
+        [B][H_q][S_q][D]."""
+        q = _f16bits(q)
+        assert q.ndim == 4 and q.shape[:2] == (self.B, self.H_q)
+        assert q.shape[3] == self.D
+        out = np.zeros(q.shape, np.float32)
+        sc = (1.0 / np.sqrt(self.D)) if scale is None else float(scale)
+        rc = self._lib.orc_attend_multi(self._c, _ptr(q), q.shape[2], sc,
+                                        _ptr(out))
+        if rc != 0:
+            raise ValueError("oracle: a sequence is shorter than S_q")
         return out
 
     def attend_one(self, b: int, hq: int, q_row, scale=None) -> np.ndarray:

@@ -409,6 +409,57 @@ int orc_attend_one(const orc_cache *c, int b, int hq, const uint16_t *q_row,
   return 0;
 }
 
+/* Several query tokens per sequence (multi-query decode, chunked
+ * prefill-attend): the S_q queries of sequence b are its newest S_q tokens,
+ * already in the cache, so query i sits at position S[b] - S_q + i and
+ * attends every token t <= that position (causal; the S_q = 1 case is
+ * orc_attend_one).  q fp16 [B][Hq][S_q][D] -> out fp32 [B][Hq][S_q][D], the
+ * softmax in double as in orc_attend_one.  Returns 0, or -1 when some
+ * sequence holds fewer than S_q tokens (out untouched). */
+int orc_attend_multi(const orc_cache *c, const uint16_t *q, int S_q,
+                     double scale, float *out) {
+  const int D = c->D;
+  if (S_q <= 0) return -1;
+  for (int b = 0; b < c->B; ++b)
+    if (c->S[b] < S_q) return -1;
+  double *qd = (double *)malloc(sizeof(double) * D);
+  double *k = (double *)malloc(sizeof(double) * D);
+  double *v = (double *)malloc(sizeof(double) * D);
+  double *o = (double *)malloc(sizeof(double) * D);
+  for (int b = 0; b < c->B; ++b) {
+    const int S = c->S[b];
+    double *s = (double *)malloc(sizeof(double) * (size_t)S);
+    for (int hq = 0; hq < c->Hq; ++hq) {
+      const int h = hq / (c->Hq / c->Hkv);
+      for (int i = 0; i < S_q; ++i) {
+        const size_t row = (((size_t)b * c->Hq + hq) * S_q + i) * D;
+        const int pos = S - S_q + i; /* this query's own position */
+        for (int ch = 0; ch < D; ++ch) qd[ch] = h2f(q[row + ch]);
+        double m = -INFINITY;
+        for (int t = 0; t <= pos; ++t) {
+          token_hat(c, b, h, t, k, v);
+          double dot = 0.0;
+          for (int ch = 0; ch < D; ++ch) dot += qd[ch] * k[ch];
+          s[t] = scale * dot;
+          if (s[t] > m) m = s[t];
+        }
+        double l = 0.0;
+        for (int ch = 0; ch < D; ++ch) o[ch] = 0.0;
+        for (int t = 0; t <= pos; ++t) {
+          double p = exp(s[t] - m);
+          l += p;
+          token_hat(c, b, h, t, k, v);
+          for (int ch = 0; ch < D; ++ch) o[ch] += p * v[ch];
+        }
+        for (int ch = 0; ch < D; ++ch) out[row + ch] = (float)(o[ch] / l);
+      }
+    }
+    free(s);
+  }
+  free(qd); free(k); free(v); free(o);
+  return 0;
+}
+
 /* All heads: q fp16 [B][Hq][D] -> out fp32 [B][Hq][D]. */
 int orc_attend(const orc_cache *c, const uint16_t *q, double scale,
                float *out) {

@@ -516,3 +516,71 @@ def test_whole_cache_reconstruction_bound(oracle_mod, bits, g):
                 assert (err <= bound).all(), (b, h, err.max())
                 checked += x.size
     assert checked > 0
+
+
+# ---------------------------------------------------------------------------
+# several query tokens per sequence (multi-query decode, chunked prefill)
+# ---------------------------------------------------------------------------
+
+def np_causal_attention(qs, K, V, scale, S):
+    """Dense causal softmax attention in long double: query i of the newest
+    S_q tokens sits at position S - S_q + i and sees tokens 0 ... that
+    position."""
+    S_q = qs.shape[0]
+    out = []
+    for i in range(S_q):
+        pos = S - S_q + i
+        out.append(np_dense_attention(qs[i], K[: pos + 1], V[: pos + 1], scale))
+    return np.stack(out)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_multi_query_brute_force_tiny(oracle_mod, bits):
+    """Causal multi-query attention over k_hat / v_hat rebuilt by the
+    independent numpy unpacker, in long double, equals the oracle to 1e-12;
+    S_q spans the residual window and reaches into the quantized region."""
+    B, Hq, H, D, g, R = 3, 4, 2, 8, 4, 6
+    lens = [45, 17, 30]
+    oc, K, V = _cache(oracle_mod, B, Hq, H, D, bits, g, R, lens, seed=20)
+    rng = np.random.default_rng(120)
+    for S_q in (1, 3, 12, 17):
+        q = rand_f16(rng, (B, Hq, S_q, D))
+        scale = 0.29
+        got = oc.attend_multi(q, scale)
+        for b in range(B):
+            for hq in range(Hq):
+                k, v = np_dequant_sequence(oc, b, hq // 2)
+                ref = np_causal_attention(q[b, hq].astype(np.longdouble), k, v,
+                                          np.longdouble(scale), lens[b])
+                assert np.abs(got[b, hq] - ref.astype(np.float64)).max() <= 1e-6
+                # the fp32 output is the double result rounded once
+                assert np.abs(got[b, hq].astype(np.float64) -
+                              ref.astype(np.float64)).max() <= \
+                    1e-12 + 2.0 ** -24 * np.abs(ref.astype(np.float64)).max() * 2
+
+
+def test_multi_query_reduces_to_decode_and_to_single_tokens(oracle_mod):
+    """The last of S_q queries sees the whole sequence, as the one-query
+    decode does; with S_q = S the first query sees token 0 alone, so its
+    output is v_hat of token 0; S_q = 1 is the decode itself."""
+    B, Hq, H, D, g, R = 2, 2, 1, 8, 4, 4
+    lens = [23, 9]
+    oc, K, V = _cache(oracle_mod, B, Hq, H, D, 2, g, R, lens, seed=21)
+    rng = np.random.default_rng(121)
+    q = rand_f16(rng, (B, Hq, 5, D))
+    multi = oc.attend_multi(q)
+    dec = oc.attend(np.ascontiguousarray(q[:, :, -1]))
+    assert np.array_equal(multi[:, :, -1], dec)
+    assert np.array_equal(oc.attend_multi(q[:, :, -1:])[:, :, 0], dec)
+    qa = rand_f16(rng, (B, Hq, 9, D))
+    oc9, _, _ = _cache(oracle_mod, B, Hq, H, D, 2, g, R, [9, 9], seed=22)
+    out9 = oc9.attend_multi(qa)
+    for b in range(B):
+        _, v = np_dequant_sequence(oc9, b, 0)
+        assert np.allclose(out9[b, :, 0], v[0].astype(np.float64), rtol=0, atol=1e-7)
+
+
+def test_multi_query_rejects_more_queries_than_tokens(oracle_mod):
+    oc, _, _ = _cache(oracle_mod, 2, 2, 2, 8, 2, 4, 4, [10, 3])
+    with pytest.raises(ValueError):
+        oc.attend_multi(np.zeros((2, 2, 4, 8), np.float16))
