@@ -96,6 +96,22 @@ class KiviCache:
             _stream_handle(stream)))
         return out
 
+    def attend_multi(self, q: torch.Tensor, out: Optional[torch.Tensor] = None,
+                     scale: float = 0.0,
+                     stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+        """Causal attention of each sequence's newest S_q tokens (already
+        appended): q fp16 [B][H_q][S_q][D] -> fp32 [B][H_q][S_q][D]."""
+        if q.dim() != 4 or (q.shape[0], q.shape[1], q.shape[3]) != (
+                self.B, self.H_q, self.D):
+            raise ValueError(f"q must be [{self.B}][{self.H_q}][S_q][{self.D}]")
+        if out is None:
+            out = torch.empty(tuple(q.shape), dtype=torch.float32, device=q.device)
+        _lib.check(_lib.load().vq_kivi_attend_multi(
+            self._h, _dev_ptr(q, torch.float16, "q"), int(q.shape[2]),
+            _dev_ptr(out, torch.float32, "out"), float(scale),
+            _stream_handle(stream)))
+        return out
+
     # -- inspection ------------------------------------------------------------
 
     def lengths(self):

@@ -400,6 +400,54 @@ int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
   return VQ_OK;
 }
 
+int vq_kivi_attend_multi(vq_kivi_cache *c, const void *q, int32_t S_q,
+                         float *out, float softmax_scale, void *stream) {
+  int rc = check_cache(c);
+  if (rc) return rc;
+  if (!q || !out) return fail(VQ_ERR_ARG, "q or out is NULL");
+  if (!aligned(q, 16) || !aligned(out, 16))
+    return fail(VQ_ERR_ARG, "q and out must be 16-byte aligned");
+  if (!std::isfinite(softmax_scale))
+    return fail(VQ_ERR_ARG, "softmax_scale is not finite");
+  const vq_kivi_params &p = c->p;
+  if (S_q < 1) return fail(VQ_ERR_ARG, "S_q=%d < 1", S_q);
+  for (int b = 0; b < p.B; ++b)
+    if (c->S[b] < S_q)
+      return fail(VQ_ERR_ARG, "sequence %d holds %d tokens, fewer than S_q=%d",
+                  b, c->S[b], S_q);
+  const int GQ = p.H_q / p.H_kv;
+  if (p.D != 64 && p.D != 128)
+    return fail(VQ_ERR_UNSUPPORTED, "multi-query attend: D=%d (supported: 64, 128)", p.D);
+  if (GQ != 1 && GQ != 2 && GQ != 4 && GQ != 8)
+    return fail(VQ_ERR_UNSUPPORTED, "multi-query attend: H_q/H_kv=%d (supported: "
+                "1, 2, 4, 8)", GQ);
+  if ((int64_t)S_q * p.D * 2 * p.H_q * p.B > ((int64_t)1 << 40))
+    return fail(VQ_ERR_UNSUPPORTED, "multi-query attend: q too large");
+  const float scale = softmax_scale > 0.f ? softmax_scale
+                                          : 1.0f / std::sqrt((float)p.D);
+  MultiTable tab;
+  for (int b = 0; b < p.B; ++b) {
+    tab.S[b] = c->S[b];
+    tab.Tq[b] = c->Tq[b];
+  }
+  MultiArgs args;
+  args.q = (const __half *)q;
+  args.out = out;
+  args.err = c->err;
+  args.scale_log2 = scale * 1.4426950408889634f;
+  args.S_q = S_q;
+  args.GQ = GQ;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = launch_attend_multi(c->geo, c->pl, args, tab, st);
+  if (e == cudaErrorNotSupported)
+    return fail(VQ_ERR_UNSUPPORTED, "multi-query attend: the driver offers no "
+                "tensor-map encoder");
+  if (e != cudaSuccess) return cuda_fail(e, "multi-query attend launch");
+  c->flush_last = false;
+  c->last_stream = st;
+  return VQ_OK;
+}
+
 int vq_kivi_free(vq_kivi_cache *c) {
   if (!c) return VQ_OK;
   int dev = -1;

@@ -1,0 +1,543 @@
+// Several query tokens per sequence over the quantized cache, on the
+// Blackwell tensor cores: tcgen05.mma with its accumulators in tensor memory
+// (TMEM), the query tile brought in by a TMA tensor copy.
+//
+// Method: attention over the group-affine cache of VeloxQuant-MLX changelog
+// v0.42.0 "Added" (k_hat / v_hat rebuilt from codes and per-group (scale,
+// zero), never written to global memory), for S_q query tokens at once --
+// speculative multi-token decode, or a chunked prefill whose tokens were
+// just appended -- with a causal mask: query i of sequence b is the cache's
+// token S_b - S_q + i and sees the tokens up to its own position.  The pages
+// ship a matrix-tiled prefill / cross-attention companion for large S_q
+// (changelog v0.40.0 "Added"); that is prior art for the shape of the work,
+// not for this kernel.
+//
+// One CTA of 128 threads serves 128 rows of one (sequence, kv head); the
+// rows are (query head of the kv head, query) pairs, row r = hh * QPT + i
+// with QPT = 128 / GQ queries per tile, and thread r owns row r.  Key tiles
+// of 64 tokens stream through:
+//   1. the threads rebuild the tile: k_hat and v_hat of every token in fp32
+//      (code * scale + zero; residual-window rows are fp16 already), each
+//      split into fp16 hi = RN(x) and lo = RN(x - hi), stored in shared
+//      memory in the tensor cores' 128-byte-swizzled K-major layout: k_hat
+//      as [token][channel], v_hat transposed as [channel][token];
+//   2. one thread issues S = Q k_hat^T as Q K_hi^T + Q K_lo^T into TMEM
+//      (M = 128, N = 64, K = D; q is fp16, hence exact as an operand);
+//   3. each thread loads its row of S from TMEM, masks it causally and
+//      updates an online softmax in fp32 (base 2), writing p as fp16 hi + lo,
+//      the A operand of the next product;
+//   4. one thread issues O += P v_hat as P_hi V_hi + P_hi V_lo + P_lo V_hi
+//      into the TMEM accumulator O (N = D).
+// The running maximum of a row is raised lazily: O is rescaled in TMEM only
+// when a row's maximum grows by more than 8 (base 2), so p <= 2^8 stays in
+// fp16 range; the final O / l does not depend on which maximum was used.
+// Every wait on an mbarrier is bounded; a wait that gives up sets the
+// cache's error word (read by vq_kivi_device_status) and the CTA returns
+// after freeing its tensor memory.
+#include <cuda.h>   // CUtensorMap and its enums; the encoder is looked up at run time
+
+#include <cmath>
+#include <mutex>
+
+#include "vqk_internal.cuh"
+
+namespace vqk {
+namespace multi {
+
+constexpr int kRows = 128;     // M: rows per CTA (one per thread)
+constexpr int kTok = 64;       // tokens per key tile
+constexpr int kThreads = 128;
+constexpr uint32_t kTmemCols = 256;   // S in columns [0, 64), O in [128, 128 + D)
+constexpr uint32_t kOCol = 128;
+constexpr float kLazy = 8.f;   // rescale O when a row maximum grows by more
+
+__device__ __forceinline__ uint32_t saddr(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(bar)));
+}
+
+__device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(saddr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// bounded wait (~0.5 s); false when it gives up
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = now_ns();
+  while (!mbar_try(bar, parity))
+    if (now_ns() - t0 > 500000000ull) return false;
+  return true;
+}
+
+// ---- tcgen05 ---------------------------------------------------------------
+
+// Shared-memory matrix descriptor of a 128-byte-swizzled K-major tile whose
+// 8-row swizzle atoms (1024 B, 1024-byte aligned) follow one another: start
+// address >> 4 (bits 0-13), leading-dimension offset 16 B (unused by this
+// layout), stride between 8-row groups 1024 B (bits 32-45), descriptor
+// version 1 (bits 46-47), swizzle mode 128 B (value 2 in bits 61-63).
+// Moving 16 fp16 along K inside the atom adds 32 B to the start address.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) |
+         ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), A
+// and B fp16 (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3
+// in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t f16_idesc(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                     uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          saddr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (the warp reads
+// its 32 lanes); the load is complete when this returns
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+        "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+        "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]),
+      "f"(v[7]), "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]),
+      "f"(v[14]), "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]),
+      "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]),
+      "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// hi = RN(x), lo = RN(x - hi) as two packed fp16 pairs
+__device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t &lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 hf = __half22float2(h);
+  const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t *>(&h);
+  lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+// ---- shared-memory plan ------------------------------------------------------
+
+template <int D>
+struct Smem {
+  static constexpr int KB = D / 64;                       // 64-channel K-blocks
+  static constexpr uint32_t Q = 0;                        // [KB][128 rows][128 B]
+  static constexpr uint32_t KH = Q + KB * 16384;          // [KB][64 rows][128 B]
+  static constexpr uint32_t KL = KH + KB * 8192;
+  static constexpr uint32_t VH = KL + KB * 8192;          // [D rows][128 B]
+  static constexpr uint32_t VL = VH + D * 128;
+  static constexpr uint32_t PH = VL + D * 128;            // [128 rows][128 B]
+  static constexpr uint32_t PL = PH + 16384;
+  static constexpr uint32_t BAR = PL + 16384;             // 3 mbarriers + TMEM slot
+  static constexpr uint32_t BYTES = BAR + 64;
+  static constexpr uint32_t ALLOC = BYTES + 1024;         // room to align the base
+};
+
+// byte offset of the 16-byte chunk `chunk` of row `row` in a 128-byte-row
+// swizzled tile
+__device__ __forceinline__ uint32_t sw_off(int row, int chunk) {
+  return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
+               Planes pl, MultiArgs args, MultiTable tab) {
+  using SM = Smem<D>;
+  constexpr int KB = SM::KB, C8 = D / 8;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *sm = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *bar_q = reinterpret_cast<uint64_t *>(sm + SM::BAR);
+  uint64_t *bar_s = bar_q + 1, *bar_o = bar_q + 2;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(bar_q + 3);
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int GQ = args.GQ, QPT = kRows / GQ, S_q = args.S_q;
+  const int S = tab.S[b], Tq = tab.Tq[b];
+  const size_t hd = (size_t)b * geo.H_kv + h;
+  const int i0 = blockIdx.x * QPT;
+  const int hh = tid / QPT, qi = i0 + tid % QPT;
+  const bool valid = qi < S_q;
+  const int pos = valid ? S - S_q + qi : -1;       // this row's own token
+  const int last_i = min(S_q - 1, i0 + QPT - 1);
+  const int max_pos = S - S_q + last_i;            // furthest token any row sees
+
+  if (tid == 0) {
+    mbar_init(bar_q);
+    mbar_init(bar_s);
+    mbar_init(bar_o);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     saddr(tslot)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t t_lane = tmem + ((uint32_t)(32 * warp) << 16);   // this warp's lanes
+
+  // the query tile: KB boxes of 64 channels x QPT queries x GQ heads
+  if (tid == 0) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(bar_q)),
+                 "r"((uint32_t)(KB * 16384))
+                 : "memory");
+    for (int kb = 0; kb < KB; ++kb)
+      asm volatile(
+          "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+          "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(saddr(sm + SM::Q + kb * 16384)),
+          "l"(reinterpret_cast<uint64_t>(&qmap)), "r"(64 * kb), "r"(i0), "r"(h * GQ), "r"(b),
+          "r"(saddr(bar_q))
+          : "memory");
+  }
+  bool failed = !mbar_wait(bar_q, 0);
+
+  const float sl2 = args.scale_log2;
+  float m_run = -INFINITY, l_run = 0.f;
+  uint32_t ph_s = 0, ph_o = 0;
+  bool o_started = false;       // an O product has been issued
+  bool o_pending = false;       // the last O product is not yet waited for
+  const uint32_t idesc_s = f16_idesc(kRows, kTok), idesc_o = f16_idesc(kRows, D);
+  const uint32_t sbase = saddr(sm);
+
+  for (int t0 = 0; t0 <= max_pos && !failed; t0 += kTok) {
+    // (a) the previous O product read P and V_hat: wait before rewriting them
+    if (o_pending) {
+      const bool ok = mbar_wait(bar_o, ph_o);
+      ph_o ^= 1u;
+      o_pending = false;
+      if (__syncthreads_or(!ok)) { failed = true; break; }
+    }
+    // (b) rebuild k_hat, v_hat of tokens t0 ... t0+63 as fp16 hi + lo
+    for (int it = tid; it < kTok * C8; it += kThreads) {
+      const int tl = it % kTok, c0 = 8 * (it / kTok);
+      const int t = t0 + tl;
+      float kf[8], vf[8];
+      if (t < Tq) {
+        const size_t r = hd * geo.Tcap + t;
+        uint32_t kc[8], vc[8];
+        codes8(geo, pl.Kc + r * geo.row, pl.Vc + (r - (t & 15)) * geo.row, t & 15, c0, kc, vc);
+        const size_t kg = (hd * (geo.Tcap / geo.g) + t / geo.g) * D + c0;
+        const uint4 ksr = __ldg(reinterpret_cast<const uint4 *>(pl.Ks + kg));
+        const uint4 kzr = __ldg(reinterpret_cast<const uint4 *>(pl.Kz + kg));
+        const __half *ksh = reinterpret_cast<const __half *>(&ksr);
+        const __half *kzh = reinterpret_cast<const __half *>(&kzr);
+        const int NJ = D / geo.g;
+        const float vs = __half2float(pl.Vs[r * NJ + c0 / geo.g]);
+        const float vz = __half2float(pl.Vz[r * NJ + c0 / geo.g]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          kf[e] = fmaf((float)kc[e], __half2float(ksh[e]), __half2float(kzh[e]));
+          vf[e] = fmaf((float)vc[e], vs, vz);
+        }
+      } else if (t < S) {
+        const size_t slot = (hd * geo.Rcap + t % geo.Rcap) * D + c0;
+        const uint4 kr = __ldg(reinterpret_cast<const uint4 *>(pl.Kr + slot));
+        const uint4 vr = __ldg(reinterpret_cast<const uint4 *>(pl.Vr + slot));
+        const __half *kh = reinterpret_cast<const __half *>(&kr);
+        const __half *vh = reinterpret_cast<const __half *>(&vr);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          kf[e] = __half2float(kh[e]);
+          vf[e] = __half2float(vh[e]);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) kf[e] = vf[e] = 0.f;
+      }
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) split2(kf[2 * e], kf[2 * e + 1], hw[e], lw[e]);
+      const int kb = c0 >> 6;
+      const uint32_t ko = kb * 8192 + sw_off(tl, (c0 & 63) >> 3);
+      *reinterpret_cast<uint4 *>(sm + SM::KH + ko) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4 *>(sm + SM::KL + ko) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      // v_hat transposed: row = channel, 16-byte chunks of 8 tokens
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int ch = c0 + e;
+        const __half vh = __float2half_rn(vf[e]);
+        const __half vl = __float2half_rn(vf[e] - __half2float(vh));
+        const uint32_t vo = sw_off(ch, tl >> 3) + 2 * (tl & 7);
+        *reinterpret_cast<__half *>(sm + SM::VH + vo) = vh;
+        *reinterpret_cast<__half *>(sm + SM::VL + vo) = vl;
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+
+    // (c) S = Q K_hi^T + Q K_lo^T
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        const uint32_t kbase = sbase + (part ? SM::KL : SM::KH);
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma(tmem, sw128_desc(sbase + SM::Q + kb * 16384 + 32 * k),
+                 sw128_desc(kbase + kb * 8192 + 32 * k), idesc_s,
+                 (part | kb | k) != 0);
+      }
+      umma_commit(bar_s);
+    }
+    {
+      const bool ok = mbar_wait(bar_s, ph_s);
+      ph_s ^= 1u;
+      if (__syncthreads_or(!ok)) { failed = true; break; }
+    }
+    tc_fence_after();
+
+    // (d) this row's scores: causal mask, online softmax, p as fp16 hi + lo
+    float sc[kTok];
+    {
+      float tmp[32];
+      tmem_ld32(t_lane, tmp);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) sc[j] = tmp[j];
+      tmem_ld32(t_lane + 32, tmp);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) sc[32 + j] = tmp[j];
+    }
+    float mt = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kTok; ++j) {
+      sc[j] = (t0 + j <= pos) ? sc[j] * sl2 : -INFINITY;
+      mt = fmaxf(mt, sc[j]);
+    }
+    float alpha = 1.f;
+    const bool raise = mt > m_run + kLazy;   // false while both are -inf
+    if (raise) {
+      alpha = m_run == -INFINITY ? 0.f : ex2(m_run - mt);
+      m_run = mt;
+    }
+    if (o_started && __any_sync(0xffffffffu, raise)) {
+      // rescale this warp's rows of O in TMEM (rows that did not raise
+      // their maximum multiply by 1)
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        float o[32];
+        tmem_ld32(t_lane + kOCol + c, o);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] *= alpha;
+        tmem_st32(t_lane + kOCol + c, o);
+      }
+      tmem_wait_st();
+    }
+    float psum = 0.f;
+    unsigned char *prow_h = sm + SM::PH, *prow_l = sm + SM::PL;
+#pragma unroll
+    for (int j8 = 0; j8 < kTok / 8; ++j8) {
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float a = sc[8 * j8 + 2 * e], c = sc[8 * j8 + 2 * e + 1];
+        const float pa = a == -INFINITY ? 0.f : ex2(a - m_run);
+        const float pc = c == -INFINITY ? 0.f : ex2(c - m_run);
+        psum += pa + pc;
+        split2(pa, pc, hw[e], lw[e]);
+      }
+      const uint32_t po = sw_off(tid, j8);
+      *reinterpret_cast<uint4 *>(prow_h + po) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4 *>(prow_l + po) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+    l_run = fmaf(l_run, alpha, psum);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+
+    // (e) O += P_hi V_hi + P_hi V_lo + P_lo V_hi
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int part = 0; part < 3; ++part) {
+        const uint32_t pb = sbase + (part == 2 ? SM::PL : SM::PH);
+        const uint32_t vb = sbase + (part == 1 ? SM::VL : SM::VH);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma(tmem + kOCol, sw128_desc(pb + 32 * k), sw128_desc(vb + 32 * k), idesc_o,
+               (o_started || part || k) ? 1u : 0u);
+      }
+      umma_commit(bar_o);
+    }
+    o_started = true;
+    o_pending = true;
+  }
+
+  if (!failed && o_pending) {
+    const bool ok = mbar_wait(bar_o, ph_o);
+    ph_o ^= 1u;
+    o_pending = false;
+    failed = __syncthreads_or(!ok);
+  }
+  if (!failed && o_started) {
+    tc_fence_after();
+    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+    float *orow = args.out +
+                  (((size_t)b * geo.H_q + (size_t)h * GQ + hh) * S_q + (valid ? qi : 0)) * D;
+#pragma unroll
+    for (int c = 0; c < D; c += 32) {
+      float o[32];
+      tmem_ld32(t_lane + kOCol + c, o);
+      if (valid) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          __stcs(reinterpret_cast<float4 *>(orow + c + j),
+                 make_float4(o[j] * inv, o[j + 1] * inv, o[j + 2] * inv, o[j + 3] * inv));
+      }
+    }
+  }
+  if (failed) {
+    if (tid == 0) atomicOr(args.err, 2u);
+    // let an O product still in flight finish (bounded) before the tensor
+    // memory is released
+    if (o_pending) mbar_wait(bar_o, ph_o);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols));
+  }
+}
+
+// ---- host ------------------------------------------------------------------
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                 const cuuint32_t *, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                 CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+  static std::once_flag once;
+  static EncodeTiled fn = nullptr;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  });
+  return fn;
+}
+
+template <int D>
+cudaError_t launch_d(const Geometry &geo, const Planes &pl, const MultiArgs &args,
+                     const MultiTable &tab, cudaStream_t st) {
+  EncodeTiled enc = encoder();
+  if (!enc) return cudaErrorNotSupported;
+  // q [B][H_q][S_q][D] fp16 as a 4-D tensor (channel, query, head, sequence);
+  // one box = 64 channels x QPT queries x GQ heads of one sequence, 128-byte
+  // swizzled (the tensor cores' K-major layout)
+  const int QPT = kRows / args.GQ;
+  CUtensorMap map;
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)args.S_q, (cuuint64_t)geo.H_q,
+                              (cuuint64_t)geo.B};
+  const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)args.S_q * D * 2,
+                                 (cuuint64_t)geo.H_q * args.S_q * D * 2};
+  const cuuint32_t box[4] = {64, (cuuint32_t)QPT, (cuuint32_t)args.GQ, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<__half *>(args.q),
+                   dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  const size_t smem = Smem<D>::ALLOC;
+  cudaError_t e = cudaFuncSetAttribute(k_attend_multi<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((args.S_q + QPT - 1) / QPT, geo.H_kv, geo.B);
+  k_attend_multi<D><<<grid, kThreads, smem, st>>>(map, geo, pl, args, tab);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace multi
+
+cudaError_t launch_attend_multi(const Geometry &geo, const Planes &pl,
+                                const MultiArgs &args, const MultiTable &tab,
+                                cudaStream_t st) {
+  switch (geo.D) {
+    case 64: return multi::launch_d<64>(geo, pl, args, tab, st);
+    case 128: return multi::launch_d<128>(geo, pl, args, tab, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace vqk

@@ -463,42 +463,6 @@ cudaError_t launch_export_residual(const Geometry &geo, const Planes &pl,
 // cache's own order: packed (the 8 codes are b consecutive bytes) or
 // MMA-fragment (2 words for keys, 4 for values, by the position functions
 // specialised to 8 channels of one 16-channel step).
-__device__ inline void codes8(const Geometry &geo, const uint8_t *krow,
-                              const uint8_t *vblk, int tl, int c0,
-                              uint32_t (&kc)[8], uint32_t (&vc)[8]) {
-  const int b = geo.bits;
-  const uint32_t m = (1u << b) - 1u;
-  if (geo.layout == kLayoutFrag) {
-    const int kpw = 8 / b, nw = geo.D * b / 128;
-    const int ks = c0 >> 4, h = (c0 >> 3) & 1, r0 = 2 * (ks % kpw);
-    const uint32_t *kw = reinterpret_cast<const uint32_t *>(krow);
-    for (int q = 0; q < 2; ++q) {              // tig = 2h + q: channels 4q ... 4q+3
-      const uint32_t w = kw[nw * (2 * h + q) + ks / kpw];
-      for (int e = 0; e < 4; ++e)
-        kc[4 * q + e] = (w >> (16 * (e & 1) + b * (r0 + (e >> 1)))) & m;
-    }
-    const int u = tl & 7, sh = 16 * (u >> 2), pi = 4 * (tl >> 3) + (u & 3);
-    const uint32_t *vw = reinterpret_cast<const uint32_t *>(vblk);
-    for (int jj = 0; jj < 4; ++jj) {           // j = (c0 & 15) / 2 + jj
-      const uint32_t w = vw[(8 * pi + ((c0 & 15) >> 1) + jj) * nw + ks / kpw];
-      for (int rho = 0; rho < 2; ++rho)
-        vc[2 * jj + rho] = (w >> (sh + b * (r0 + rho))) & m;
-    }
-  } else {
-    // 8 codes = b bytes at byte c0 * b / 8
-    uint64_t kx = 0, vx = 0;
-    const uint8_t *kp = krow + c0 * b / 8, *vp = vblk + (size_t)tl * geo.row + c0 * b / 8;
-    for (int i = 0; i < b; ++i) {
-      kx |= (uint64_t)kp[i] << (8 * i);
-      vx |= (uint64_t)vp[i] << (8 * i);
-    }
-    for (int e = 0; e < 8; ++e) {
-      kc[e] = (uint32_t)(kx >> (b * e)) & m;
-      vc[e] = (uint32_t)(vx >> (b * e)) & m;
-    }
-  }
-}
-
 __global__ void k_dequantize(Geometry geo, Planes pl, LenTable lens,
                              __half *__restrict__ Kh, __half *__restrict__ Vh,
                              int64_t s_stride) {

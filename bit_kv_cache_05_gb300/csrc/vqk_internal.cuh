@@ -77,6 +77,48 @@ __host__ __device__ inline FragPos frag_value(int D, int b, int tl, int c) {
   return FragPos{(8 * pi + j) * nw + mv / kpw, 16 * s + b * r};
 }
 
+// Codes of channels c0 ... c0+7 (c0 a multiple of 8) of one quantized token:
+// keys from the token's row krow, values from the token's 16-token block
+// vblk (tl = token within the block), in the cache's own order: packed (the
+// 8 codes are b consecutive bytes of the row) or MMA-fragment (2 words for
+// keys, 4 for values, by frag_key / frag_value specialised to 8 channels of
+// one 16-channel step).
+__device__ inline void codes8(const Geometry &geo, const uint8_t *krow,
+                              const uint8_t *vblk, int tl, int c0,
+                              uint32_t (&kc)[8], uint32_t (&vc)[8]) {
+  const int b = geo.bits;
+  const uint32_t m = (1u << b) - 1u;
+  if (geo.layout == kLayoutFrag) {
+    const int kpw = 8 / b, nw = geo.D * b / 128;
+    const int ks = c0 >> 4, h = (c0 >> 3) & 1, r0 = 2 * (ks % kpw);
+    const uint32_t *kw = reinterpret_cast<const uint32_t *>(krow);
+    for (int q = 0; q < 2; ++q) {              // tig = 2h + q: channels 4q ... 4q+3
+      const uint32_t w = kw[nw * (2 * h + q) + ks / kpw];
+      for (int e = 0; e < 4; ++e)
+        kc[4 * q + e] = (w >> (16 * (e & 1) + b * (r0 + (e >> 1)))) & m;
+    }
+    const int u = tl & 7, sh = 16 * (u >> 2), pi = 4 * (tl >> 3) + (u & 3);
+    const uint32_t *vw = reinterpret_cast<const uint32_t *>(vblk);
+    for (int jj = 0; jj < 4; ++jj) {           // j = (c0 & 15) / 2 + jj
+      const uint32_t w = vw[(8 * pi + ((c0 & 15) >> 1) + jj) * nw + ks / kpw];
+      for (int rho = 0; rho < 2; ++rho)
+        vc[2 * jj + rho] = (w >> (sh + b * (r0 + rho))) & m;
+    }
+  } else {
+    // 8 codes = b bytes at byte c0 * b / 8
+    uint64_t kx = 0, vx = 0;
+    const uint8_t *kp = krow + c0 * b / 8, *vp = vblk + (size_t)tl * geo.row + c0 * b / 8;
+    for (int i = 0; i < b; ++i) {
+      kx |= (uint64_t)kp[i] << (8 * i);
+      vx |= (uint64_t)vp[i] << (8 * i);
+    }
+    for (int e = 0; e < 8; ++e) {
+      kc[e] = (uint32_t)(kx >> (b * e)) & m;
+      vc[e] = (uint32_t)(vx >> (b * e)) & m;
+    }
+  }
+}
+
 // ---- quantize / flush ------------------------------------------------------
 
 // One launch quantizes whole groups of g tokens of every (b, h).  Group k of
@@ -186,6 +228,28 @@ size_t mma_part_floats(const Geometry &geo, const MmaPlan &plan);
 cudaError_t launch_decode_mma(const Geometry &geo, const Planes &pl,
                               const MmaPlan &plan, MmaArgs args,
                               const MmaTable &tab, cudaStream_t st);
+
+// ---- several query tokens per sequence (tcgen05, attend_multi.cu) ---------
+
+struct MultiTable {
+  int32_t S[kMaxB];    // tokens per sequence
+  int32_t Tq[kMaxB];   // quantized tokens per sequence
+};
+
+struct MultiArgs {
+  const __half *q;     // [B][H_q][S_q][D]
+  float *out;          // [B][H_q][S_q][D]
+  unsigned *err;       // set to nonzero when a wait gave up
+  float scale_log2;    // softmax scale * log2(e)
+  int S_q;             // query tokens per sequence (its newest S_q tokens)
+  int GQ;              // query heads per kv head (1, 2, 4 or 8)
+};
+
+// D = 64 or 128; cudaErrorNotSupported when the driver offers no tensor-map
+// encoder
+cudaError_t launch_attend_multi(const Geometry &geo, const Planes &pl,
+                                const MultiArgs &args, const MultiTable &tab,
+                                cudaStream_t st);
 
 // counts every kernel launch made by the library
 void count_launch(int n = 1);

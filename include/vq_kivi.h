@@ -117,6 +117,29 @@ int vq_kivi_append(vq_kivi_cache *c, const void *K_new, const void *V_new,
 int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
                           float softmax_scale, void *stream);
 
+/* Several query tokens per sequence: multi-token (speculative) decode, or
+ * attention of a chunk of tokens that was just appended (chunked prefill).
+ * Attention over the same quantized cache (changelog v0.42.0 "Added":
+ * k_hat / v_hat rebuilt from the codes, never written to global memory),
+ * with a causal mask: the S_q queries of sequence b are its newest S_q
+ * tokens, already in the cache, so query i is token S_b - S_q + i and
+ * attends every token t <= S_b - S_q + i (quantized, residual window and
+ * its own).  The pages' matrix-tiled prefill companion of another cache
+ * (changelog v0.40.0 "Added") is the prior art for this shape of the work.
+ * Runs on the tensor cores (tcgen05 with tensor-memory accumulators; the
+ * query tile is brought in by a TMA tensor copy); k_hat, v_hat and the
+ * softmax weights enter as fp16 hi + lo pairs, the softmax is fp32.
+ *   q              device, fp16, [B][H_q][S_q][D], 16-byte aligned
+ *   S_q            >= 1, at most the length of every sequence
+ *   out            device, fp32, [B][H_q][S_q][D], 16-byte aligned
+ *   softmax_scale  <= 0 selects 1/sqrt(D)
+ * Supported: D = 64 or 128 and H_q/H_kv in {1, 2, 4, 8}
+ * (VQ_ERR_UNSUPPORTED otherwise); VQ_ERR_ARG when a sequence holds fewer
+ * than S_q tokens.  Uses no workspace of the cache, so it may follow or
+ * precede vq_kivi_decode_attend in any order on the cache's stream. */
+int vq_kivi_attend_multi(vq_kivi_cache *c, const void *q, int32_t S_q,
+                         float *out, float softmax_scale, void *stream);
+
 /* Release the cache.  NULL is accepted.  Frees are stream-ordered on the
  * stream of the last call that used the cache, then that stream is
  * synchronized, so the handle's memory is gone when this returns. */
