@@ -475,6 +475,11 @@ def run_ours(args, w, rank, world, local):
             targets[name] = measure_workload(synth.workload(name), peak,
                                              full=False)
             torch.cuda.empty_cache()
+        tpk, tpk_kind = measured_peak_tflops()
+        targets["int4_append_prefill_attend"] = dict(
+            measure_multi(synth.workload("int4_append"), 512, tpk),
+            peak_kind=tpk_kind)
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -627,6 +632,66 @@ def measure_workload(w, peak, full=True):
     return res
 
 
+def multi_flops(w, seq_lens, S_q):
+    """Algorithmic FLOPs of causal multi-query attention: per query head and
+    query i (position S - S_q + i), 2 D multiply-adds per visible token for
+    q . k and again for p v, i.e. 4 D (pos + 1)."""
+    tot = 0
+    for S in seq_lens:
+        vis = sum(S - S_q + i + 1 for i in range(S_q))
+        tot += w.H_q * 4 * w.D * vis
+    return tot
+
+
+def measure_multi(w, S_q, peak_tflops, reps=5):
+    """Chunked prefill attend: append S_q tokens to every sequence of the
+    workload's cache, then attend them causally over the whole cache
+    (vq_kivi_attend_multi), timed over `reps` caches (each larger than L2
+    rotates the cache out between launches)."""
+    import torch
+    from bit_kv_cache_05_gb300 import synth
+    from bit_kv_cache_05_gb300.cache import KiviCache
+    inp = synth.make_inputs(w, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(7)
+    Kn = torch.randn(w.B, w.H_kv, S_q, w.D, generator=g, device="cuda").half()
+    Vn = torch.randn(w.B, w.H_kv, S_q, w.D, generator=g, device="cuda").half()
+    q = torch.randn(w.B, w.H_q, S_q, w.D, generator=g, device="cuda").half()
+    caches = []
+    for _ in range(2):
+        c = KiviCache(inp["K"], inp["V"], w.seq_lens, H_q=w.H_q, bits=w.bits,
+                      group=w.group, residual=w.residual,
+                      max_seq=w.max_seq + S_q)
+        c.append(Kn, Vn, [S_q] * w.B)
+        caches.append(c)
+    del inp
+    out = torch.empty(w.B, w.H_q, S_q, w.D, device="cuda")
+    for c in caches:
+        c.attend_multi(q, out)
+    t = _ev_times(lambda i: caches[i % 2].attend_multi(q, out), reps)
+    caches[0].device_status()
+    S_now = [s + S_q for s in w.seq_lens]
+    fl = multi_flops(w, S_now, S_q)
+    for c in caches:
+        c.close()
+    tf = fl / (t[0] * 1e-6) / 1e12
+    return {"S_q": S_q, "S_kv": S_now[0] if len(set(S_now)) == 1 else S_now,
+            "us": round(t[0], 1), "p10_p90_us": [round(t[1], 1), round(t[2], 1)],
+            "algorithmic_flops": fl, "tflops": round(tf, 2),
+            "peak_tflops": peak_tflops, "frac": round(tf / peak_tflops, 4),
+            "kernel": "k_attend_multi (tcgen05, TMEM accumulators)"}
+
+
+def measured_peak_tflops():
+    """Dense fp16 tensor peak: the measured bf16 GEMM rate (fp16 and bf16
+    run at the same nominal rate on the tensor cores)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
 def flush_append_bytes(w, n_new):
     """Algorithmic bytes of appending n_new tokens per sequence to a cache
     whose residual holds w.residual tokens (the workload's state): read the
@@ -706,6 +771,31 @@ def run_profile_decode(name: str, n: int):
     c.close()
 
 
+def run_profile_multi(name: str, B: str, S_q: str, n: str):
+    import torch
+    from bit_kv_cache_05_gb300 import synth
+    from bit_kv_cache_05_gb300.cache import KiviCache
+    w0 = synth.workload(name)
+    w = synth.shrink(w0, w0.seq_lens[:int(B)], n_append=0)
+    S_q, n = int(S_q), int(n)
+    inp = synth.make_inputs(w, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(7)
+    Kn = torch.randn(w.B, w.H_kv, S_q, w.D, generator=g, device="cuda").half()
+    Vn = torch.randn(w.B, w.H_kv, S_q, w.D, generator=g, device="cuda").half()
+    q = torch.randn(w.B, w.H_q, S_q, w.D, generator=g, device="cuda").half()
+    c = KiviCache(inp["K"], inp["V"], w.seq_lens, H_q=w.H_q, bits=w.bits,
+                  group=w.group, residual=w.residual, max_seq=w.max_seq + S_q)
+    c.append(Kn, Vn, [S_q] * w.B)
+    del inp
+    out = None
+    for _ in range(n):
+        out = c.attend_multi(q)
+    torch.cuda.synchronize()
+    c.device_status()
+    print("ok", name, w.B, S_q, float(out.abs().max()) if out is not None else 0.0)
+    c.close()
+
+
 def _respawn_under_torchrun(args, argv):
     """`--gpus N` (N > 1) without a torch.distributed launcher: start N local
     ranks with torch.distributed.run (rendezvous on 127.0.0.1) and return
@@ -738,11 +828,18 @@ def main(argv=None):
     ap.add_argument("--profile-decode", nargs=2, metavar=("WORKLOAD", "N"),
                     default=None,
                     help="build one cache and run N decodes (for ncu)")
+    ap.add_argument("--profile-multi", nargs=4, metavar=("WORKLOAD", "B", "S_Q", "N"),
+                    default=None,
+                    help="append S_Q tokens to the first B sequences of a "
+                         "workload's cache and attend them N times (for ncu)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.steps < 1 or args.gpus < 1:
         ap.error("--steps and --gpus must be >= 1")
+    if args.profile_multi is not None:
+        run_profile_multi(*args.profile_multi)
+        return 0
     if args.profile_decode is not None:
         run_profile_decode(args.profile_decode[0], int(args.profile_decode[1]))
         return 0

@@ -184,6 +184,11 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t 
 
 // ---- shared-memory plan ------------------------------------------------------
 
+// P (128 rows x 64 tokens, hi and lo) is written only after the S product
+// that read K_hat has completed, and K_hat of the next tile only after the O
+// product that read P has completed, so at D = 128 P takes K_hat's place
+// (16 KB each for hi and lo); the CTA then needs 96 KB and two fit on an SM
+// (their tensor memory, 256 columns each, fills the SM's 512).
 template <int D>
 struct Smem {
   static constexpr int KB = D / 64;                       // 64-channel K-blocks
@@ -192,9 +197,10 @@ struct Smem {
   static constexpr uint32_t KL = KH + KB * 8192;
   static constexpr uint32_t VH = KL + KB * 8192;          // [D rows][128 B]
   static constexpr uint32_t VL = VH + D * 128;
-  static constexpr uint32_t PH = VL + D * 128;            // [128 rows][128 B]
-  static constexpr uint32_t PL = PH + 16384;
-  static constexpr uint32_t BAR = PL + 16384;             // 3 mbarriers + TMEM slot
+  static constexpr bool ALIAS = KB * 8192 >= 16384;
+  static constexpr uint32_t PH = ALIAS ? KH : VL + D * 128;   // [128 rows][128 B]
+  static constexpr uint32_t PL = ALIAS ? KL : PH + 16384;
+  static constexpr uint32_t BAR = ALIAS ? VL + D * 128 : PL + 16384;  // 3 mbarriers + TMEM slot
   static constexpr uint32_t BYTES = BAR + 64;
   static constexpr uint32_t ALLOC = BYTES + 1024;         // room to align the base
 };
@@ -205,12 +211,104 @@ __device__ __forceinline__ uint32_t sw_off(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+// ---- codes of the cache, per bit width and code order ----------------------
+//
+// FRAG: the MMA-fragment order of 2- and 4-bit caches decoded on the tensor
+// cores (a 32-bit word holds two 16-bit halves of 16/b fields; keys: channel
+// c = 16 ks + 4 tig + e of a token row in word NW tig + ks/KPW, half e mod
+// 2, field 2 (ks mod KPW) + e/2; values: the tokens of a 16-token block pair
+// up as (tl, tl + 4), and channel c = 16 mv + 2 j + rho of pair pi sits in
+// word (8 pi + j) NW + mv/KPW, field 2 (mv mod KPW) + rho, the first token
+// in the low half).  Otherwise the packed order: code of channel c of a
+// token row at byte c b / 8, bit (c b) mod 8.
+template <int D, int BITS, bool FRAG>
+struct Codes {
+  static constexpr uint32_t M = (1u << BITS) - 1u;
+  static constexpr int ROW = D * BITS / 8;
+
+  // the 16 codes of channels 16 ks ... 16 ks + 15 of a key row
+  static __device__ __forceinline__ void key16(const uint8_t *krow, int ks,
+                                               uint32_t (&c)[16]) {
+    if constexpr (FRAG) {
+      constexpr int KPW = 8 / BITS, NW = D * BITS / 128;
+      const uint32_t *w = reinterpret_cast<const uint32_t *>(krow);
+      const int r0 = 2 * (ks % KPW);
+#pragma unroll
+      for (int tig = 0; tig < 4; ++tig) {
+        const uint32_t x = __ldg(w + NW * tig + ks / KPW);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          c[4 * tig + e] = (x >> (16 * (e & 1) + BITS * (r0 + (e >> 1)))) & M;
+      }
+    } else {
+      // 16 codes = 2 BITS bytes at byte 2 BITS ks
+      uint32_t w[BITS / 2];
+      if constexpr (BITS == 2) {
+        w[0] = __ldg(reinterpret_cast<const uint32_t *>(krow + 4 * ks));
+      } else if constexpr (BITS == 4) {
+        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(krow + 8 * ks));
+        w[0] = v.x; w[1] = v.y;
+      } else {
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(krow + 16 * ks));
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+      }
+      constexpr int PER = 32 / BITS;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) c[e] = (w[e / PER] >> (BITS * (e % PER))) & M;
+    }
+  }
+
+  // codes of channels c0 ... c0+7 (c0 a multiple of 8) of the 8 tokens
+  // tb ... tb+7 (tb = 0 or 8) of the 16-token value block vblk: c[u][e] for
+  // token tb + u, channel c0 + e
+  static __device__ __forceinline__ void value8x8(const uint8_t *vblk, int tb, int c0,
+                                                  uint32_t (&c)[8][8]) {
+    if constexpr (FRAG) {
+      constexpr int KPW = 8 / BITS, NW = D * BITS / 128;
+      const uint32_t *w = reinterpret_cast<const uint32_t *>(vblk);
+      const int mv = c0 >> 4, j0 = (c0 & 15) >> 1, r0 = 2 * (mv % KPW);
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+        const int pi = (tb >> 1) + pp;          // pairs (tb + pp, tb + pp + 4)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const uint32_t x = __ldg(w + (8 * pi + j0 + jj) * NW + mv / KPW);
+#pragma unroll
+          for (int rho = 0; rho < 2; ++rho) {
+            c[pp][2 * jj + rho] = (x >> (BITS * (r0 + rho))) & M;
+            c[pp + 4][2 * jj + rho] = (x >> (16 + BITS * (r0 + rho))) & M;
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint8_t *p = vblk + (size_t)(tb + u) * ROW + c0 * BITS / 8;
+        uint32_t w0, w1 = 0;
+        if constexpr (BITS == 2) {
+          w0 = __ldg(reinterpret_cast<const uint16_t *>(p));
+        } else if constexpr (BITS == 4) {
+          w0 = __ldg(reinterpret_cast<const uint32_t *>(p));
+        } else {
+          const uint2 v = __ldg(reinterpret_cast<const uint2 *>(p));
+          w0 = v.x; w1 = v.y;
+        }
+        constexpr int PER = 32 / BITS;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          c[u][e] = ((e < PER ? w0 : w1) >> (BITS * (e % PER))) & M;
+      }
+    }
+  }
+};
+
+template <int D, int BITS, bool FRAG>
+__global__ void __launch_bounds__(kThreads, 2)
 k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
                Planes pl, MultiArgs args, MultiTable tab) {
   using SM = Smem<D>;
-  constexpr int KB = SM::KB, C8 = D / 8;
+  using CD = Codes<D, BITS, FRAG>;
+  constexpr int KB = SM::KB, KS = D / 16, C8 = D / 8, ROW = CD::ROW;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -222,6 +320,7 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
   const int b = blockIdx.z, h = blockIdx.y;
   const int GQ = args.GQ, QPT = kRows / GQ, S_q = args.S_q;
   const int S = tab.S[b], Tq = tab.Tq[b];
+  const int g = geo.g, NJ = D / g;
   const size_t hd = (size_t)b * geo.H_kv + h;
   const int i0 = blockIdx.x * QPT;
   const int hh = tid / QPT, qi = i0 + tid % QPT;
@@ -229,6 +328,14 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
   const int pos = valid ? S - S_q + qi : -1;       // this row's own token
   const int last_i = min(S_q - 1, i0 + QPT - 1);
   const int max_pos = S - S_q + last_i;            // furthest token any row sees
+  const uint8_t *kc_base = pl.Kc + hd * geo.Tcap * ROW;
+  const uint8_t *vc_base = pl.Vc + hd * geo.Tcap * ROW;
+  const __half *ks_base = pl.Ks + hd * (geo.Tcap / g) * D;
+  const __half *kz_base = pl.Kz + hd * (geo.Tcap / g) * D;
+  const __half *vs_base = pl.Vs + hd * geo.Tcap * NJ;
+  const __half *vz_base = pl.Vz + hd * geo.Tcap * NJ;
+  const __half *kr_base = pl.Kr + hd * geo.Rcap * D;
+  const __half *vr_base = pl.Vr + hd * geo.Rcap * D;
 
   if (tid == 0) {
     mbar_init(bar_q);
@@ -261,10 +368,12 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
           "r"(saddr(bar_q))
           : "memory");
   }
-  bool failed = !mbar_wait(bar_q, 0);
+  bool failed = __syncthreads_or(!mbar_wait(bar_q, 0));
 
   const float sl2 = args.scale_log2;
-  float m_run = -INFINITY, l_run = 0.f;
+  // rows without a query see no token; a finite maximum keeps their
+  // weights at exactly 0 (2^-inf) instead of NaN
+  float m_run = valid ? -INFINITY : 0.f, l_run = 0.f;
   uint32_t ph_s = 0, ph_o = 0;
   bool o_started = false;       // an O product has been issued
   bool o_pending = false;       // the last O product is not yet waited for
@@ -279,59 +388,105 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
       o_pending = false;
       if (__syncthreads_or(!ok)) { failed = true; break; }
     }
-    // (b) rebuild k_hat, v_hat of tokens t0 ... t0+63 as fp16 hi + lo
-    for (int it = tid; it < kTok * C8; it += kThreads) {
-      const int tl = it % kTok, c0 = 8 * (it / kTok);
+    // (b1) k_hat of tokens t0 ... t0+63, 16 channels per item, as fp16 hi + lo
+    for (int it = tid; it < kTok * KS; it += kThreads) {
+      const int tl = it % kTok, ks = it / kTok;
       const int t = t0 + tl;
-      float kf[8], vf[8];
+      float kf[16];
       if (t < Tq) {
-        const size_t r = hd * geo.Tcap + t;
-        uint32_t kc[8], vc[8];
-        codes8(geo, pl.Kc + r * geo.row, pl.Vc + (r - (t & 15)) * geo.row, t & 15, c0, kc, vc);
-        const size_t kg = (hd * (geo.Tcap / geo.g) + t / geo.g) * D + c0;
-        const uint4 ksr = __ldg(reinterpret_cast<const uint4 *>(pl.Ks + kg));
-        const uint4 kzr = __ldg(reinterpret_cast<const uint4 *>(pl.Kz + kg));
-        const __half *ksh = reinterpret_cast<const __half *>(&ksr);
-        const __half *kzh = reinterpret_cast<const __half *>(&kzr);
-        const int NJ = D / geo.g;
-        const float vs = __half2float(pl.Vs[r * NJ + c0 / geo.g]);
-        const float vz = __half2float(pl.Vz[r * NJ + c0 / geo.g]);
+        uint32_t c[16];
+        CD::key16(kc_base + (size_t)t * ROW, ks, c);
+        const __half *sp = ks_base + (size_t)(t / g) * D + 16 * ks;
+        const __half *zp = kz_base + (size_t)(t / g) * D + 16 * ks;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          kf[e] = fmaf((float)kc[e], __half2float(ksh[e]), __half2float(kzh[e]));
-          vf[e] = fmaf((float)vc[e], vs, vz);
+        for (int q = 0; q < 2; ++q) {
+          const uint4 sr = __ldg(reinterpret_cast<const uint4 *>(sp) + q);
+          const uint4 zr = __ldg(reinterpret_cast<const uint4 *>(zp) + q);
+          const __half2 *s2 = reinterpret_cast<const __half2 *>(&sr);
+          const __half2 *z2 = reinterpret_cast<const __half2 *>(&zr);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 sf = __half22float2(s2[e]), zf = __half22float2(z2[e]);
+            kf[8 * q + 2 * e] = fmaf((float)c[8 * q + 2 * e], sf.x, zf.x);
+            kf[8 * q + 2 * e + 1] = fmaf((float)c[8 * q + 2 * e + 1], sf.y, zf.y);
+          }
         }
       } else if (t < S) {
-        const size_t slot = (hd * geo.Rcap + t % geo.Rcap) * D + c0;
-        const uint4 kr = __ldg(reinterpret_cast<const uint4 *>(pl.Kr + slot));
-        const uint4 vr = __ldg(reinterpret_cast<const uint4 *>(pl.Vr + slot));
-        const __half *kh = reinterpret_cast<const __half *>(&kr);
-        const __half *vh = reinterpret_cast<const __half *>(&vr);
+        const uint4 *rp = reinterpret_cast<const uint4 *>(
+            kr_base + (size_t)(t % geo.Rcap) * D + 16 * ks);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          kf[e] = __half2float(kh[e]);
-          vf[e] = __half2float(vh[e]);
+        for (int q = 0; q < 2; ++q) {
+          const uint4 r = __ldg(rp + q);
+          const __half2 *r2 = reinterpret_cast<const __half2 *>(&r);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(r2[e]);
+            kf[8 * q + 2 * e] = f.x;
+            kf[8 * q + 2 * e + 1] = f.y;
+          }
         }
       } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) kf[e] = vf[e] = 0.f;
+        for (int e = 0; e < 16; ++e) kf[e] = 0.f;
       }
-      uint32_t hw[4], lw[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) split2(kf[2 * e], kf[2 * e + 1], hw[e], lw[e]);
-      const int kb = c0 >> 6;
-      const uint32_t ko = kb * 8192 + sw_off(tl, (c0 & 63) >> 3);
-      *reinterpret_cast<uint4 *>(sm + SM::KH + ko) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      *reinterpret_cast<uint4 *>(sm + SM::KL + ko) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-      // v_hat transposed: row = channel, 16-byte chunks of 8 tokens
+      for (int q = 0; q < 2; ++q) {
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          split2(kf[8 * q + 2 * e], kf[8 * q + 2 * e + 1], hw[e], lw[e]);
+        const int c0 = 16 * ks + 8 * q;
+        const uint32_t ko = (c0 >> 6) * 8192 + sw_off(tl, (c0 & 63) >> 3);
+        *reinterpret_cast<uint4 *>(sm + SM::KH + ko) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4 *>(sm + SM::KL + ko) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
+    }
+    // (b2) v_hat transposed, 8 channels x 8 tokens per item: V^T rows are
+    // channels, a 16-byte chunk holds 8 consecutive tokens
+    for (int it = tid; it < C8 * (kTok / 8); it += kThreads) {
+      const int t8 = it % (kTok / 8), c0 = 8 * (it / (kTok / 8));
+      const int ta = t0 + 8 * t8;                 // first token of the octet
+      float vf[8][8];
+      if (ta < Tq) {
+        // Tq is a multiple of g >= 16: the octet is wholly quantized
+        uint32_t c[8][8];
+        CD::value8x8(vc_base + (size_t)(ta & ~15) * ROW, ta & 8, c0, c);
+        const int j = c0 / g;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float sv = __half2float(vs_base[(size_t)(ta + u) * NJ + j]);
+          const float zv = __half2float(vz_base[(size_t)(ta + u) * NJ + j]);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) vf[u][e] = fmaf((float)c[u][e], sv, zv);
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int t = ta + u;
+          if (t < S) {
+            const uint4 r = __ldg(reinterpret_cast<const uint4 *>(
+                vr_base + (size_t)(t % geo.Rcap) * D + c0));
+            const __half2 *r2 = reinterpret_cast<const __half2 *>(&r);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __half22float2(r2[e]);
+              vf[u][2 * e] = f.x;
+              vf[u][2 * e + 1] = f.y;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) vf[u][e] = 0.f;
+          }
+        }
+      }
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const int ch = c0 + e;
-        const __half vh = __float2half_rn(vf[e]);
-        const __half vl = __float2half_rn(vf[e] - __half2float(vh));
-        const uint32_t vo = sw_off(ch, tl >> 3) + 2 * (tl & 7);
-        *reinterpret_cast<__half *>(sm + SM::VH + vo) = vh;
-        *reinterpret_cast<__half *>(sm + SM::VL + vo) = vl;
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) split2(vf[2 * u][e], vf[2 * u + 1][e], hw[u], lw[u]);
+        const uint32_t vo = sw_off(c0 + e, t8);
+        *reinterpret_cast<uint4 *>(sm + SM::VH + vo) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4 *>(sm + SM::VL + vo) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
       }
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -372,15 +527,23 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
       for (int j = 0; j < 32; ++j) sc[32 + j] = tmp[j];
     }
     float mt = -INFINITY;
+    if (t0 + kTok - 1 <= pos) {          // the whole tile is visible to this row
 #pragma unroll
-    for (int j = 0; j < kTok; ++j) {
-      sc[j] = (t0 + j <= pos) ? sc[j] * sl2 : -INFINITY;
-      mt = fmaxf(mt, sc[j]);
+      for (int j = 0; j < kTok; ++j) {
+        sc[j] *= sl2;
+        mt = fmaxf(mt, sc[j]);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kTok; ++j) {
+        sc[j] = (t0 + j <= pos) ? sc[j] * sl2 : -INFINITY;
+        mt = fmaxf(mt, sc[j]);
+      }
     }
     float alpha = 1.f;
     const bool raise = mt > m_run + kLazy;   // false while both are -inf
     if (raise) {
-      alpha = m_run == -INFINITY ? 0.f : ex2(m_run - mt);
+      alpha = ex2(m_run - mt);               // 2^-inf = 0 on the first raise
       m_run = mt;
     }
     if (o_started && __any_sync(0xffffffffu, raise)) {
@@ -397,21 +560,21 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
       tmem_wait_st();
     }
     float psum = 0.f;
-    unsigned char *prow_h = sm + SM::PH, *prow_l = sm + SM::PL;
 #pragma unroll
     for (int j8 = 0; j8 < kTok / 8; ++j8) {
       uint32_t hw[4], lw[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float a = sc[8 * j8 + 2 * e], c = sc[8 * j8 + 2 * e + 1];
-        const float pa = a == -INFINITY ? 0.f : ex2(a - m_run);
-        const float pc = c == -INFINITY ? 0.f : ex2(c - m_run);
+        // m_run is finite here (token 0 is in every valid row's first
+        // tile; rows without a query keep 0), so -inf scores give 0
+        const float pa = ex2(sc[8 * j8 + 2 * e] - m_run);
+        const float pc = ex2(sc[8 * j8 + 2 * e + 1] - m_run);
         psum += pa + pc;
         split2(pa, pc, hw[e], lw[e]);
       }
       const uint32_t po = sw_off(tid, j8);
-      *reinterpret_cast<uint4 *>(prow_h + po) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      *reinterpret_cast<uint4 *>(prow_l + po) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      *reinterpret_cast<uint4 *>(sm + SM::PH + po) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4 *>(sm + SM::PL + po) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
     l_run = fmaf(l_run, alpha, psum);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -496,8 +659,8 @@ EncodeTiled encoder() {
   return fn;
 }
 
-template <int D>
-cudaError_t launch_d(const Geometry &geo, const Planes &pl, const MultiArgs &args,
+template <int D, int BITS, bool FRAG>
+cudaError_t launch_k(const Geometry &geo, const Planes &pl, const MultiArgs &args,
                      const MultiTable &tab, cudaStream_t st) {
   EncodeTiled enc = encoder();
   if (!enc) return cudaErrorNotSupported;
@@ -518,14 +681,28 @@ cudaError_t launch_d(const Geometry &geo, const Planes &pl, const MultiArgs &arg
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   const size_t smem = Smem<D>::ALLOC;
-  cudaError_t e = cudaFuncSetAttribute(k_attend_multi<D>,
+  cudaError_t e = cudaFuncSetAttribute(k_attend_multi<D, BITS, FRAG>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((args.S_q + QPT - 1) / QPT, geo.H_kv, geo.B);
-  k_attend_multi<D><<<grid, kThreads, smem, st>>>(map, geo, pl, args, tab);
+  k_attend_multi<D, BITS, FRAG><<<grid, kThreads, smem, st>>>(map, geo, pl, args, tab);
   count_launch();
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const Geometry &geo, const Planes &pl, const MultiArgs &args,
+                     const MultiTable &tab, cudaStream_t st) {
+  const bool frag = geo.layout == kLayoutFrag;
+  switch (geo.bits) {
+    case 2: return frag ? launch_k<D, 2, true>(geo, pl, args, tab, st)
+                        : launch_k<D, 2, false>(geo, pl, args, tab, st);
+    case 4: return frag ? launch_k<D, 4, true>(geo, pl, args, tab, st)
+                        : launch_k<D, 4, false>(geo, pl, args, tab, st);
+    case 8: return launch_k<D, 8, false>(geo, pl, args, tab, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace multi

@@ -118,3 +118,16 @@ def test_flush_append_bytes_of_the_4bit_workload():
     per_head = (64 + 512) * 512 + 512 * 144 + 64 * 512
     assert per_head == 401408
     assert bench.flush_append_bytes(w, 512) == 8 * 32 * per_head
+
+
+def test_multi_query_flops_per_unit():
+    """Causal multi-query FLOPs: 4 D per (query head, query, visible token);
+    with S = 5 and S_q = 2 the two queries see 4 and 5 tokens."""
+    import bench
+    from bit_kv_cache_05_gb300 import synth
+    w = synth.Workload("t", 1, 2, 1, 4, 2, 4, 4, [5])
+    assert bench.multi_flops(w, [5], 2) == 2 * 4 * 4 * (4 + 5)
+    w4 = synth.workload("int4_append")
+    S = 33280
+    per_head = 4 * 128 * sum(S - 512 + i + 1 for i in range(512))
+    assert bench.multi_flops(w4, [S] * 8, 512) == 8 * 32 * per_head
