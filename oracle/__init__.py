@@ -32,7 +32,8 @@ _LIB_PATH = os.path.join(_BUILD, "libkivi_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
-PLANES = ("Kc", "Ks", "Kz", "Vc", "Vs", "Vz", "Kr", "Vr")
+PLANES = ("Kc", "Ks", "Kz", "Vc", "Vs", "Vz", "Kr", "Vr",
+          "sink_pos", "sink_k", "sink_v")
 
 
 def build(force: bool = False) -> str:
@@ -60,6 +61,7 @@ def _load():
         lib.orc_new.restype = P
         lib.orc_new.argtypes = [i32] * 8
         lib.orc_free.argtypes = [P]
+        lib.orc_set_sinks.argtypes = [P, i32]
         lib.orc_quantize.argtypes = [P, P, P, i64, P]
         lib.orc_append.argtypes = [P, P, P, i64, P]
         lib.orc_attend.argtypes = [P, P, f64, P]
@@ -134,20 +136,26 @@ class OracleCache:
 
     Canonical planes (row-major):
       Kc, Vc  uint8  [B][H_kv][Tcap][D*bits/8]   (LSB-first packing)
+      sink_pos int32 [B][H_kv][n_sink]           (KIVI-Sink: ascending, -1 unused)
+      sink_k, sink_v fp16 [B][H_kv][n_sink][D]
       Ks, Kz  fp16   [B][H_kv][Tcap/g][D]        (per channel, per key group)
       Vs, Vz  fp16   [B][H_kv][Tcap][D/g]        (per token, per channel group)
       Kr, Vr  fp16   [B][H_kv][R+g][D]           (slot i holds token Tq+i)
     """
 
-    def __init__(self, B, H_q, H_kv, D, bits, group, residual, max_seq):
+    def __init__(self, B, H_q, H_kv, D, bits, group, residual, max_seq,
+                 n_sink=0):
         self.B, self.H_q, self.H_kv, self.D = B, H_q, H_kv, D
         self.bits, self.group, self.residual, self.max_seq = (
             bits, group, residual, max_seq)
+        self.n_sink = n_sink
         self._lib = _load()
         self._c = self._lib.orc_new(B, H_q, H_kv, D, bits, group, residual,
                                     max_seq)
         if not self._c:
             raise ValueError("oracle: unsupported cache parameters")
+        if self._lib.orc_set_sinks(self._c, n_sink) != 0:
+            raise ValueError("oracle: bad sink count")
         tcap = np.zeros(1, np.int32)
         rcap = np.zeros(1, np.int32)
         self._lib.orc_dims(self._c, _ptr(tcap), _ptr(rcap))
@@ -229,4 +237,8 @@ class OracleCache:
             return raw.view(np.float16).reshape(B, H, self.Tcap // g, D)
         if name in ("Vs", "Vz"):
             return raw.view(np.float16).reshape(B, H, self.Tcap, D // g)
+        if name == "sink_pos":
+            return raw.view(np.int32).reshape(B, H, self.n_sink)
+        if name in ("sink_k", "sink_v"):
+            return raw.view(np.float16).reshape(B, H, self.n_sink, D)
         return raw.view(np.float16).reshape(B, H, self.Rcap, D)

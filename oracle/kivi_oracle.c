@@ -131,6 +131,11 @@ typedef struct orc_cache {
   uint16_t *Vs, *Vz;       /* [B][Hkv][Tcap][D/g] */
   uint16_t *Kr, *Vr;       /* [B][Hkv][Rcap][D]; slot i holds token Tq+i */
   int32_t *S, *Tq, *nres;  /* [B] */
+  /* KIVI-Sink (0 sinks = plain KIVI): per (b, h) the positions of the sink
+   * tokens, ascending, -1 in unused slots, and their fp16 key / value rows */
+  int n_sink;
+  int32_t *sink_pos;       /* [B][Hkv][n_sink] */
+  uint16_t *sink_k, *sink_v; /* [B][Hkv][n_sink][D] */
 } orc_cache;
 
 static int n_quantized(int S, int R, int g) {
@@ -182,7 +187,79 @@ void orc_free(orc_cache *c) {
   if (!c) return;
   free(c->Kc); free(c->Vc); free(c->Ks); free(c->Kz); free(c->Vs);
   free(c->Vz); free(c->Kr); free(c->Vr); free(c->S); free(c->Tq);
-  free(c->nres); free(c);
+  free(c->nres); free(c->sink_pos); free(c->sink_k); free(c->sink_v);
+  free(c);
+}
+
+/* KIVI-Sink (changelog v0.9.0 "New"): tokens with the largest key L2 norms
+ * are kept in fp16 and left out of the groups' min/max.  Call before
+ * orc_quantize; n_sink = 0 is plain KIVI.  Returns 0, or -1 on a bad count
+ * or a failed allocation. */
+int orc_set_sinks(orc_cache *c, int n_sink) {
+  if (n_sink < 0 || n_sink > 64) return -1;
+  free(c->sink_pos); free(c->sink_k); free(c->sink_v);
+  c->sink_pos = NULL; c->sink_k = NULL; c->sink_v = NULL;
+  c->n_sink = n_sink;
+  if (n_sink == 0) return 0;
+  size_t slots = (size_t)c->B * c->Hkv * n_sink;
+  c->sink_pos = (int32_t *)malloc(4 * slots);
+  c->sink_k = (uint16_t *)calloc(slots * c->D, 2);
+  c->sink_v = (uint16_t *)calloc(slots * c->D, 2);
+  if (!c->sink_pos || !c->sink_k || !c->sink_v) return -1;
+  for (size_t i = 0; i < slots; ++i) c->sink_pos[i] = -1;
+  return 0;
+}
+
+static int is_sink(const orc_cache *c, int b, int h, int t) {
+  const int32_t *sp = c->sink_pos + ((size_t)b * c->Hkv + h) * c->n_sink;
+  for (int k = 0; k < c->n_sink; ++k)
+    if (sp[k] == t) return 1;
+  return 0;
+}
+
+/* Squared L2 norm of an fp16 key row in fp32, channel 0 first (each square
+ * of an fp16 value is exact in fp32; the sums round to nearest). */
+static float key_norm2(const uint16_t *row, int D) {
+  float acc = 0.0f;
+  for (int ch = 0; ch < D; ++ch) {
+    float x = h2f(row[ch]);
+    acc = acc + x * x;
+  }
+  return acc;
+}
+
+/* Sinks of one (b, h): the min(n_sink, S) tokens among the S prefill tokens
+ * with the largest key norms (a larger norm first, an earlier position on
+ * equal norms), stored by ascending position with their fp16 rows. */
+static void pick_sinks(orc_cache *c, int b, int h, const uint16_t *Kbh,
+                       const uint16_t *Vbh, int S) {
+  const int D = c->D, n = c->n_sink;
+  size_t base = ((size_t)b * c->Hkv + h) * n;
+  int32_t *sp = c->sink_pos + base;
+  int count = 0;
+  for (int k = 0; k < n; ++k) sp[k] = -1;
+  char *taken = (char *)calloc(S > 0 ? S : 1, 1);
+  for (int k = 0; k < n && k < S; ++k) {
+    int best = -1;
+    float bn = 0.0f;
+    for (int t = 0; t < S; ++t) {
+      if (taken[t]) continue;
+      float nt = key_norm2(Kbh + (size_t)t * D, D);
+      if (best < 0 || nt > bn) { best = t; bn = nt; }
+    }
+    taken[best] = 1;
+    sp[count++] = best;
+  }
+  free(taken);
+  /* ascending positions */
+  for (int i = 1; i < count; ++i)
+    for (int j = i; j > 0 && sp[j - 1] > sp[j]; --j) {
+      int32_t tmp = sp[j]; sp[j] = sp[j - 1]; sp[j - 1] = tmp;
+    }
+  for (int k = 0; k < count; ++k) {
+    memcpy(c->sink_k + (base + k) * D, Kbh + (size_t)sp[k] * D, 2 * (size_t)D);
+    memcpy(c->sink_v + (base + k) * D, Vbh + (size_t)sp[k] * D, 2 * (size_t)D);
+  }
 }
 
 /* Quantize one key group (g tokens, all D channels, per channel) and the
@@ -197,17 +274,35 @@ static void quantize_group_of_tokens(orc_cache *c, int b, int h, int G,
   size_t bh = (size_t)b * c->Hkv + h;
   float *x = (float *)malloc(sizeof(float) * (size_t)g * D);
   uint8_t *codes = (uint8_t *)malloc((size_t)g * D);
-  /* keys: per channel over the g tokens */
+  /* sink tokens of this group (KIVI-Sink): left out of every min/max,
+   * their codes 0 and their own value groups empty */
+  char sink[4096];
+  int n_keep = 0;
   for (int i = 0; i < g; ++i) {
-    const uint16_t *r = krow(ctx, i);
-    for (int ch = 0; ch < D; ++ch) x[(size_t)i * D + ch] = h2f(r[ch]);
+    sink[i] = c->n_sink > 0 && is_sink(c, b, h, G * g + i);
+    if (!sink[i]) ++n_keep;
   }
+  /* keys: per channel over the group's (non-sink) tokens */
+  for (int i = 0, k = 0; i < g; ++i) {
+    if (sink[i]) continue;
+    const uint16_t *r = krow(ctx, i);
+    for (int ch = 0; ch < D; ++ch) x[(size_t)k * D + ch] = h2f(r[ch]);
+    ++k;
+  }
+  uint8_t *kept = (uint8_t *)malloc((size_t)(n_keep ? n_keep : 1) * D);
   for (int ch = 0; ch < D; ++ch) {
-    uint16_t s16, z16;
-    quant_group(x + ch, D, g, c->bits, codes + ch, D, NULL, &s16, &z16);
+    uint16_t s16 = 0, z16 = 0; /* a group of sinks only: scale and zero +0 */
+    if (n_keep > 0)
+      quant_group(x + ch, D, n_keep, c->bits, kept + ch, D, NULL, &s16, &z16);
     c->Ks[(bh * (c->Tcap / g) + G) * D + ch] = s16;
     c->Kz[(bh * (c->Tcap / g) + G) * D + ch] = z16;
   }
+  for (int i = 0, k = 0; i < g; ++i) {
+    for (int ch = 0; ch < D; ++ch)
+      codes[(size_t)i * D + ch] = sink[i] ? 0 : kept[(size_t)k * D + ch];
+    if (!sink[i]) ++k;
+  }
+  free(kept);
   for (int i = 0; i < g; ++i) {
     size_t t = (size_t)G * g + i;
     orc_pack_codes(codes + (size_t)i * D, D, c->bits,
@@ -221,8 +316,12 @@ static void quantize_group_of_tokens(orc_cache *c, int b, int h, int G,
     uint8_t cv[4096];
     for (int ch = 0; ch < D; ++ch) xv[ch] = h2f(r[ch]);
     for (int j = 0; j < D / g; ++j) {
-      uint16_t s16, z16;
-      quant_group(xv + j * g, 1, g, c->bits, cv + j * g, 1, NULL, &s16, &z16);
+      uint16_t s16 = 0, z16 = 0;
+      if (sink[i]) {
+        memset(cv + j * g, 0, (size_t)g); /* no member left: scale, zero +0 */
+      } else {
+        quant_group(xv + j * g, 1, g, c->bits, cv + j * g, 1, NULL, &s16, &z16);
+      }
       c->Vs[(bh * c->Tcap + t) * (D / g) + j] = s16;
       c->Vz[(bh * c->Tcap + t) * (D / g) + j] = z16;
     }
@@ -270,6 +369,7 @@ int orc_quantize(orc_cache *c, const uint16_t *K, const uint16_t *V,
     c->nres[b] = S - Tq;
     for (int h = 0; h < c->Hkv; ++h) {
       size_t off = ((size_t)b * c->Hkv + h) * (size_t)s_stride * c->D;
+      if (c->n_sink > 0) pick_sinks(c, b, h, K + off, V + off, S);
       for (int G = 0; G < Tq / c->g; ++G) {
         dense_ctx kd = {K + off, c->D, G * c->g};
         dense_ctx vd = {V + off, c->D, G * c->g};
@@ -349,6 +449,17 @@ static void token_hat(const orc_cache *c, int b, int h, int t, double *k,
                       double *v) {
   const int D = c->D, g = c->g;
   size_t bh = (size_t)b * c->Hkv + h;
+  if (t < c->Tq[b] && c->n_sink > 0 && is_sink(c, b, h, t)) {
+    /* a sink token of the quantized region: its exact fp16 rows */
+    const int32_t *sp = c->sink_pos + bh * c->n_sink;
+    int slot = 0;
+    while (sp[slot] != t) ++slot;
+    for (int ch = 0; ch < D; ++ch) {
+      k[ch] = h2f(c->sink_k[(bh * c->n_sink + slot) * D + ch]);
+      v[ch] = h2f(c->sink_v[(bh * c->n_sink + slot) * D + ch]);
+    }
+    return;
+  }
   if (t < c->Tq[b]) {
     uint8_t codes[4096];
     int G = t / g;
@@ -498,6 +609,8 @@ size_t orc_plane_bytes(const orc_cache *c, int which) {
     case 1: case 2: return bh * (c->Tcap / c->g) * c->D * 2;
     case 4: case 5: return bh * c->Tcap * (c->D / c->g) * 2;
     case 6: case 7: return bh * c->Rcap * c->D * 2;
+    case 8: return bh * c->n_sink * 4;
+    case 9: case 10: return bh * c->n_sink * c->D * 2;
     default: return 0;
   }
 }
@@ -513,8 +626,12 @@ int orc_get_plane(const orc_cache *c, int which, void *dst) {
     case 5: src = c->Vz; break;
     case 6: src = c->Kr; break;
     case 7: src = c->Vr; break;
+    case 8: src = c->sink_pos; break;
+    case 9: src = c->sink_k; break;
+    case 10: src = c->sink_v; break;
     default: return -1;
   }
+  if (!src) return orc_plane_bytes(c, which) == 0 ? 0 : -1;
   memcpy(dst, src, orc_plane_bytes(c, which));
   return 0;
 }

@@ -584,3 +584,173 @@ def test_multi_query_rejects_more_queries_than_tokens(oracle_mod):
     oc, _, _ = _cache(oracle_mod, 2, 2, 2, 8, 2, 4, 4, [10, 3])
     with pytest.raises(ValueError):
         oc.attend_multi(np.zeros((2, 2, 4, 8), np.float16))
+
+
+# ---------------------------------------------------------------------------
+# KIVI-Sink: top key-norm tokens kept fp16, out of the groups' min/max
+# (changelog v0.9.0 "New")
+# ---------------------------------------------------------------------------
+
+def _sink_cache(oracle_mod, n_sink, K, V, lens, Hq, bits=2, g=4, R=4):
+    from oracle import OracleCache
+    B, H, S_max, D = K.shape
+    oc = OracleCache(B, Hq, H, D, bits, g, R, S_max, n_sink=n_sink)
+    oc.quantize(K, V, lens)
+    return oc
+
+
+def test_sink_zero_is_plain_kivi_bit_for_bit(oracle_mod):
+    """n_sink = 0 reproduces plain KIVI bit for bit (the pages' own
+    invariant): every plane and the attention are identical."""
+    from oracle import OracleCache
+    rng = np.random.default_rng(30)
+    B, Hq, H, D, g, R = 2, 4, 2, 16, 4, 6
+    lens = [37, 22]
+    K = rand_f16(rng, (B, H, 40, D), 3.0)
+    V = rand_f16(rng, (B, H, 40, D))
+    a = OracleCache(B, Hq, H, D, 2, g, R, 40)
+    a.quantize(K, V, lens)
+    b = _sink_cache(oracle_mod, 0, K, V, lens, Hq, 2, g, R)
+    for name in ("Kc", "Ks", "Kz", "Vc", "Vs", "Vz", "Kr", "Vr"):
+        assert np.array_equal(a.plane(name).view(np.uint8), b.plane(name).view(np.uint8)), name
+    q = rand_f16(rng, (B, Hq, D))
+    assert np.array_equal(a.attend(q), b.attend(q))
+
+
+def test_sink_selection_by_key_norm(oracle_mod):
+    """Sinks are the n_sink tokens with the largest key L2 norms, the
+    earlier position first among equal norms, stored by ascending position
+    with their exact fp16 rows."""
+    rng = np.random.default_rng(31)
+    B, H, D, S = 1, 2, 8, 30
+    K = rand_f16(rng, (B, H, S, D), 0.1)
+    V = rand_f16(rng, (B, H, S, D))
+    # head 0: norms 4 at t = 20, 3 at t = 3 and t = 11 (a tie), 2 at t = 25
+    for t, a in ((20, 4.0), (3, 3.0), (11, 3.0), (25, 2.0)):
+        K[0, 0, t] = 0
+        K[0, 0, t, 5] = a
+    # head 1: one big key at t = 0
+    K[0, 1, 0] = 10.0
+    oc = _sink_cache(oracle_mod, 3, K, V, [S], Hq=2)
+    pos = oc.plane("sink_pos")
+    assert pos[0, 0].tolist() == [3, 11, 20]
+    assert pos[0, 1][0] == 0 and len(set(pos[0, 1].tolist())) == 3
+    for k, t in enumerate(pos[0, 0]):
+        assert np.array_equal(oc.plane("sink_k")[0, 0, k], K[0, 0, t])
+        assert np.array_equal(oc.plane("sink_v")[0, 0, k], V[0, 0, t])
+    # fewer tokens than sinks: every token is a sink
+    oc2 = _sink_cache(oracle_mod, 3, K[:, :, :2].copy(), V[:, :, :2].copy(), [2], Hq=2)
+    assert oc2.plane("sink_pos")[0, 0].tolist() == [0, 1, -1]
+
+
+def test_sink_is_left_out_of_its_groups(oracle_mod):
+    """The sink's key group is quantized from the other g - 1 tokens alone
+    (the group quantizer on the reduced group gives the same scale, zero and
+    codes), the sink's code is 0, and its own value groups are empty
+    (scale and zero +0, codes 0)."""
+    rng = np.random.default_rng(32)
+    B, H, D, g, R, S = 1, 1, 8, 4, 4, 20
+    K = rand_f16(rng, (B, H, S, D))
+    V = rand_f16(rng, (B, H, S, D))
+    K[0, 0, 6] = 50.0                     # token 6 (key group 1) is the sink
+    oc = _sink_cache(oracle_mod, 1, K, V, [S], Hq=1, bits=2, g=g, R=R)
+    assert oc.plane("sink_pos")[0, 0].tolist() == [6]
+    Ks = oc.plane("Ks")[0, 0].view(np.uint16)
+    Kz = oc.plane("Kz")[0, 0].view(np.uint16)
+    kc = np_unpack_rows(oc.plane("Kc")[0, 0], D, 2)
+    others = [4, 5, 7]
+    for ch in range(D):
+        codes, _, s16, z16 = oracle_mod.quant_group(
+            K[0, 0, others, ch].astype(np.float32), 2)
+        assert (Ks[1, ch], Kz[1, ch]) == (s16, z16)
+        assert kc[others, ch].tolist() == codes.tolist()
+        assert kc[6, ch] == 0
+    assert (oc.plane("Vs")[0, 0, 6].view(np.uint16) == 0).all()
+    assert (oc.plane("Vz")[0, 0, 6].view(np.uint16) == 0).all()
+    assert (np_unpack_rows(oc.plane("Vc")[0, 0], D, 2)[6] == 0).all()
+
+
+def np_dequant_sinks(oc, b, h):
+    """k_hat, v_hat [S][D] in long double, sink tokens of the quantized
+    region from the sink rows."""
+    k, v = np_dequant_sequence(oc, b, h)
+    _, Tq, _ = oc.lengths()
+    for slot, t in enumerate(oc.plane("sink_pos")[b, h]):
+        if 0 <= t < Tq[b]:
+            k[t] = oc.plane("sink_k")[b, h, slot].astype(np.longdouble)
+            v[t] = oc.plane("sink_v")[b, h, slot].astype(np.longdouble)
+    return k, v
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_sink_attention_brute_force(oracle_mod, bits):
+    """Attention with sinks: long-double dense softmax over k_hat / v_hat
+    rebuilt independently (sink rows exact) equals the oracle to 1e-12, for
+    one query and for causal multi-query attention."""
+    rng = np.random.default_rng(33 + bits)
+    B, Hq, H, D, g, R = 2, 4, 2, 8, 4, 5
+    lens = [41, 19]
+    K = rand_f16(rng, (B, H, 45, D))
+    V = rand_f16(rng, (B, H, 45, D))
+    K[0, 0, 2] *= 20
+    K[0, 1, 30] *= 15
+    K[1, 0, 9] *= 30
+    oc = _sink_cache(oracle_mod, 3, K, V, lens, Hq, bits=bits, g=g, R=R)
+    q = rand_f16(rng, (B, Hq, D))
+    out = oc.attend(q, 0.4)
+    q4 = rand_f16(rng, (B, Hq, 6, D))
+    outm = oc.attend_multi(q4, 0.4)
+    for b in range(B):
+        for hq in range(Hq):
+            k, v = np_dequant_sinks(oc, b, hq // 2)
+            ref = np_dense_attention(q[b, hq].astype(np.longdouble), k, v, np.longdouble(0.4))
+            assert np.abs(oc.attend_one(b, hq, q[b, hq], 0.4) - ref.astype(np.float64)).max() <= 1e-12
+            assert np.abs(out[b, hq] - ref.astype(np.float64)).max() <= 1e-6
+            refm = np_causal_attention(q4[b, hq].astype(np.longdouble), k, v,
+                                       np.longdouble(0.4), lens[b])
+            assert np.abs(outm[b, hq] - refm.astype(np.float64)).max() <= 1e-6
+
+
+def test_sink_protection_lowers_group_error(oracle_mod):
+    """An outlier key inflates its group's scale under plain KIVI; with it
+    kept as a sink, the other tokens of its groups reconstruct with a lower
+    error (the pages' 'MSE improvement over plain KIVI')."""
+    rng = np.random.default_rng(34)
+    B, H, D, g, R, S = 1, 1, 16, 8, 8, 40
+    K = rand_f16(rng, (B, H, S, D))
+    V = rand_f16(rng, (B, H, S, D))
+    K[0, 0, 3] = 40.0
+    plain = _sink_cache(oracle_mod, 0, K, V, [S], Hq=1, g=g, R=R)
+    sunk = _sink_cache(oracle_mod, 1, K, V, [S], Hq=1, g=g, R=R)
+    kp, _ = np_dequant_sequence(plain, 0, 0)
+    ks, _ = np_dequant_sinks(sunk, 0, 0)
+    others = [t for t in range(g) if t != 3]
+    x = K[0, 0, others].astype(np.float64)
+    e_plain = ((kp[others].astype(np.float64) - x) ** 2).mean()
+    e_sink = ((ks[others].astype(np.float64) - x) ** 2).mean()
+    assert e_sink < 0.1 * e_plain
+    assert np.array_equal(ks[3].astype(np.float64), K[0, 0, 3].astype(np.float64))
+
+
+def test_sink_in_the_window_is_left_out_when_flushed(oracle_mod):
+    """Sinks are chosen at prefill; a sink still in the fp16 window is left
+    out of its group's min/max when a later append flushes the group, and
+    appended tokens never become sinks."""
+    from oracle import OracleCache
+    rng = np.random.default_rng(35)
+    B, H, D, g, R = 1, 1, 8, 4, 4
+    K = rand_f16(rng, (B, H, 30, D))
+    V = rand_f16(rng, (B, H, 30, D))
+    K[0, 0, 9] = 30.0                  # in the window after a 10-token prefill
+    oc = OracleCache(B, 1, H, D, 2, g, R, 30, n_sink=1)
+    oc.quantize(K, V, [10])
+    assert oc.lengths()[1][0] == 4 and oc.plane("sink_pos")[0, 0].tolist() == [9]
+    Kn = K[:, :, 10:].copy()
+    Kn[0, 0, 5] = 99.0                 # a larger key among the appended ones
+    oc.append(Kn, V[:, :, 10:].copy(), [20])
+    assert oc.plane("sink_pos")[0, 0].tolist() == [9]
+    # group 2 (tokens 8 ... 11) was quantized without token 9
+    Ks = oc.plane("Ks")[0, 0].view(np.uint16)
+    for ch in range(D):
+        _, _, s16, _ = oracle_mod.quant_group(K[0, 0, [8, 10, 11], ch].astype(np.float32), 2)
+        assert Ks[2, ch] == s16
