@@ -23,7 +23,8 @@ _NAMES = {VQ_ERR_ARG: "VQ_ERR_ARG", VQ_ERR_UNSUPPORTED: "VQ_ERR_UNSUPPORTED",
           VQ_ERR_CUDA: "VQ_ERR_CUDA"}
 
 # every symbol include/vq_kivi.h declares
-EXPORTS = ("vq_kivi_quantize", "vq_kivi_append", "vq_kivi_decode_attend",
+EXPORTS = ("vq_kivi_quantize", "vq_kivi_quantize_ex", "vq_kivi_append",
+           "vq_kivi_decode_attend",
            "vq_kivi_free", "vq_kivi_attend_multi", "vq_kivi_last_error", "vq_kivi_lengths",
            "vq_kivi_get_params", "vq_kivi_plane_bytes", "vq_kivi_export",
            "vq_kivi_dequantize",
@@ -50,9 +51,14 @@ class Planes(ctypes.Structure):
                 ("Kc", "Ks", "Kz", "Vc", "Vs", "Vz", "Kr", "Vr")]
 
 
+class Options(ctypes.Structure):
+    _fields_ = [("n_sink", ctypes.c_int32)]
+
+
 class Bytes(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in
-                ("code_bytes", "meta_bytes", "residual_bytes", "fp16_bytes")]
+                ("code_bytes", "meta_bytes", "residual_bytes", "fp16_bytes",
+                 "sink_bytes")]
 
 
 _lock = threading.Lock()
@@ -79,6 +85,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
         L.vq_kivi_quantize.argtypes = [ctypes.POINTER(Params), P, P, i64, P, P,
                                        ctypes.POINTER(P)]
+        L.vq_kivi_quantize_ex.argtypes = [ctypes.POINTER(Params),
+                                          ctypes.POINTER(Options), P, P, i64,
+                                          P, P, ctypes.POINTER(P)]
         L.vq_kivi_append.argtypes = [P, P, P, i64, P, P]
         L.vq_kivi_decode_attend.argtypes = [P, P, P, ctypes.c_float, P]
         L.vq_kivi_attend_multi.argtypes = [P, P, i32, P, ctypes.c_float, P]

@@ -14,7 +14,8 @@ import torch
 
 from . import _lib
 
-PLANES = ("Kc", "Ks", "Kz", "Vc", "Vs", "Vz", "Kr", "Vr")
+PLANES = ("Kc", "Ks", "Kz", "Vc", "Vs", "Vz", "Kr", "Vr",
+          "sink_pos", "sink_k", "sink_v")
 
 
 def _stream_handle(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
@@ -45,7 +46,7 @@ class KiviCache:
 
     def __init__(self, K: torch.Tensor, V: torch.Tensor, seq_lens, *, H_q: int,
                  bits: int, group: int, residual: int,
-                 max_seq: Optional[int] = None,
+                 max_seq: Optional[int] = None, n_sink: int = 0,
                  stream: Optional[torch.cuda.Stream] = None):
         L = _lib.load()
         if K.shape != V.shape or K.dim() != 4:
@@ -62,10 +63,13 @@ class KiviCache:
         self._h = ctypes.c_void_p()
         kp = _dev_ptr(K, torch.float16, "K")
         vp = _dev_ptr(V, torch.float16, "V")
-        _lib.check(L.vq_kivi_quantize(ctypes.byref(self.params), kp, vp,
-                                      S_stride, _i32_array(lens),
-                                      _stream_handle(stream),
-                                      ctypes.byref(self._h)))
+        self.n_sink = int(n_sink)
+        opts = _lib.Options(self.n_sink)
+        _lib.check(L.vq_kivi_quantize_ex(ctypes.byref(self.params),
+                                         ctypes.byref(opts), kp, vp,
+                                         S_stride, _i32_array(lens),
+                                         _stream_handle(stream),
+                                         ctypes.byref(self._h)))
         self.device = K.device
 
     # -- steps ---------------------------------------------------------------
@@ -134,6 +138,10 @@ class KiviCache:
             _stream_handle(stream)))
         B, H, D, g = self.B, self.H_kv, self.D, self.group
         row = D * self.bits // 8
+        if name == "sink_pos":
+            return raw.view(torch.int32).view(B, H, self.n_sink)
+        if name in ("sink_k", "sink_v"):
+            return raw.view(torch.float16).view(B, H, self.n_sink, D)
         if name in ("Kc", "Vc"):
             return raw.view(B, H, -1, row)
         raw = raw.view(torch.float16)

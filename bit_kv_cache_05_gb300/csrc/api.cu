@@ -124,8 +124,18 @@ uint64_t vq_kivi_launch_count(void) { return g_launches.load(); }
 int vq_kivi_quantize(const vq_kivi_params *p, const void *K, const void *V,
                      int64_t s_stride, const int32_t *seq_lens, void *stream,
                      vq_kivi_cache **out) {
+  return vq_kivi_quantize_ex(p, nullptr, K, V, s_stride, seq_lens, stream, out);
+}
+
+int vq_kivi_quantize_ex(const vq_kivi_params *p, const vq_kivi_options *opt,
+                        const void *K, const void *V, int64_t s_stride,
+                        const int32_t *seq_lens, void *stream,
+                        vq_kivi_cache **out) {
   int rc = check_params(p);
   if (rc) return rc;
+  const vq_kivi_options o = opt ? *opt : vq_kivi_options{0};
+  if (o.n_sink < 0 || o.n_sink > kMaxSink)
+    return fail(VQ_ERR_ARG, "n_sink=%d outside [0, %d]", o.n_sink, kMaxSink);
   if (!out) return fail(VQ_ERR_ARG, "out is NULL");
   if (!seq_lens) return fail(VQ_ERR_ARG, "seq_lens is NULL");
   int32_t smax = 0;
@@ -166,6 +176,7 @@ int vq_kivi_quantize(const vq_kivi_params *p, const void *K, const void *V,
   geo.Tcap = (int)round_up(p->max_seq > 0 ? p->max_seq : 1, g);
   geo.Rcap = p->residual + g;
   geo.row = p->D * p->bits / 8;
+  geo.n_sink = o.n_sink;
   const int32_t unit = split_unit(g);
   const int32_t tps_for_cap = (int32_t)round_up((geo.Tcap + 1023) / 1024, unit);
   c->tps_min = tps_for_cap > 256 ? tps_for_cap : 256;
@@ -199,6 +210,9 @@ int vq_kivi_quantize(const vq_kivi_params *p, const void *K, const void *V,
   size_t o_part = off; off += round_up(sz_part, A);
   size_t o_err = off; off += A;
   size_t o_ksmax = off; off += round_up(BH * sizeof(uint32_t), A);
+  size_t o_spos = off; off += round_up(BH * o.n_sink * sizeof(int32_t), A);
+  size_t o_sk = off; off += round_up(BH * o.n_sink * p->D * sizeof(__half), A);
+  size_t o_sv = off; off += round_up(BH * o.n_sink * p->D * sizeof(__half), A);
   c->block_bytes = off;
 
   e = cudaMallocAsync(&c->block, c->block_bytes, st);
@@ -221,6 +235,11 @@ int vq_kivi_quantize(const vq_kivi_params *p, const void *K, const void *V,
   pl.part = (float *)(base + o_part);
   c->err = (unsigned *)(base + o_err);
   pl.ksmax = (uint32_t *)(base + o_ksmax);
+  if (o.n_sink > 0) {
+    pl.sink_pos = (int32_t *)(base + o_spos);
+    pl.sink_k = (__half *)(base + o_sk);
+    pl.sink_v = (__half *)(base + o_sv);
+  }
   c->last_stream = st;
 
   auto abort_create = [&](cudaError_t err, const char *what) {
@@ -249,6 +268,13 @@ int vq_kivi_quantize(const vq_kivi_params *p, const void *K, const void *V,
     tt.prefix[b + 1] = tt.prefix[b] + (S - Tq);
     tt.row0[b] = Tq;
     tt.pos0[b] = Tq;
+  }
+  if (geo.n_sink > 0) {
+    SinkTable sk;
+    for (int b = 0; b < p->B; ++b) sk.S[b] = seq_lens[b];
+    e = launch_pick_sinks(geo, pl, (const __half *)K, (const __half *)V, s_stride,
+                          sk, st);
+    if (e != cudaSuccess) return abort_create(e, "sink selection launch");
   }
   e = launch_flush(geo, pl, (const __half *)K, (const __half *)V, s_stride, ft,
                    ft.prefix[p->B], st);
@@ -487,6 +513,8 @@ size_t vq_kivi_plane_bytes(const vq_kivi_cache *c, int which) {
     case 1: case 2: return BH * (geo.Tcap / geo.g) * geo.D * sizeof(__half);
     case 4: case 5: return BH * geo.Tcap * (geo.D / geo.g) * sizeof(__half);
     case 6: case 7: return BH * geo.Rcap * geo.D * sizeof(__half);
+    case 8: return BH * geo.n_sink * sizeof(int32_t);
+    case 9: case 10: return BH * geo.n_sink * geo.D * sizeof(__half);
     default: return 0;
   }
 }
@@ -496,6 +524,7 @@ int vq_kivi_export(const vq_kivi_cache *c, int which, void *dst,
   int rc = check_cache(c);
   if (rc) return rc;
   const size_t need = vq_kivi_plane_bytes(c, which);
+  if (need == 0 && which >= 8 && which <= 10) return VQ_OK;   // no sinks
   if (need == 0) return fail(VQ_ERR_ARG, "which=%d is not a plane", which);
   if (!dst) return fail(VQ_ERR_ARG, "dst is NULL");
   if (dst_bytes < need)
@@ -510,6 +539,9 @@ int vq_kivi_export(const vq_kivi_cache *c, int which, void *dst,
     case 3: src = c->pl.Vc; break;
     case 4: src = c->pl.Vs; break;
     case 5: src = c->pl.Vz; break;
+    case 8: src = c->pl.sink_pos; break;
+    case 9: src = c->pl.sink_k; break;
+    case 10: src = c->pl.sink_v; break;
     default: break;
   }
   cudaError_t e;
@@ -555,6 +587,25 @@ int vq_kivi_cache_bytes(const vq_kivi_cache *c, vq_kivi_bytes *out) {
     r.meta_bytes += H * ((Tq / p.group) * p.D * 4 + Tq * (p.D / p.group) * 4);
     r.residual_bytes += H * (uint64_t)c->nres[b] * p.D * 4;
     r.fp16_bytes += H * (uint64_t)c->S[b] * p.D * 4;
+  }
+  r.sink_bytes = 0;
+  if (c->geo.n_sink > 0) {
+    // sinks of the quantized region (their positions live on the device)
+    const size_t n = (size_t)p.B * p.H_kv * c->geo.n_sink;
+    int32_t *pos = new (std::nothrow) int32_t[n];
+    if (!pos) return fail(VQ_ERR_OOM, "host allocation failed");
+    cudaError_t e = cudaMemcpyAsync(pos, c->pl.sink_pos, n * sizeof(int32_t),
+                                    cudaMemcpyDeviceToHost, c->last_stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c->last_stream);
+    if (e != cudaSuccess) {
+      delete[] pos;
+      return cuda_fail(e, "reading the sink positions");
+    }
+    for (size_t i = 0; i < n; ++i) {
+      const int b = (int)(i / ((size_t)p.H_kv * c->geo.n_sink));
+      if (pos[i] >= 0 && pos[i] < c->Tq[b]) r.sink_bytes += (uint64_t)p.D * 4;
+    }
+    delete[] pos;
   }
   *out = r;
   return VQ_OK;

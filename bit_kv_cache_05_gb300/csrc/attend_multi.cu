@@ -368,7 +368,21 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
           "r"(saddr(bar_q))
           : "memory");
   }
+  // KIVI-Sink: the sinks of the quantized region (the rest are -1); their
+  // k_hat / v_hat are their fp16 rows
+  __shared__ int ssk[kMaxSink];
+  const int nsk = geo.n_sink;
+  if (tid < nsk) {
+    const int p = pl.sink_pos[hd * nsk + tid];
+    ssk[tid] = p < Tq ? p : -1;
+  }
   bool failed = __syncthreads_or(!mbar_wait(bar_q, 0));
+  auto sink_slot = [&](int t) {
+    int slot = -1;
+    for (int j = 0; j < nsk; ++j)
+      if (ssk[j] == t) slot = j;
+    return slot;
+  };
 
   const float sl2 = args.scale_log2;
   // rows without a query see no token; a finite maximum keeps their
@@ -387,6 +401,12 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
       ph_o ^= 1u;
       o_pending = false;
       if (__syncthreads_or(!ok)) { failed = true; break; }
+    }
+    // sinks in this tile: bit (t - t0)
+    uint64_t tmask = 0;
+    for (int j = 0; j < nsk; ++j) {
+      const int d = ssk[j] - t0;
+      if (ssk[j] >= 0 && d >= 0 && d < kTok) tmask |= 1ull << d;
     }
     // (b1) k_hat of tokens t0 ... t0+63, 16 channels per item, as fp16 hi + lo
     for (int it = tid; it < kTok * KS; it += kThreads) {
@@ -428,6 +448,21 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
       } else {
 #pragma unroll
         for (int e = 0; e < 16; ++e) kf[e] = 0.f;
+      }
+      if ((tmask >> tl) & 1ull) {
+        const uint4 *rp = reinterpret_cast<const uint4 *>(
+            pl.sink_k + (hd * nsk + sink_slot(t)) * D + 16 * ks);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const uint4 r = __ldg(rp + q);
+          const __half2 *r2 = reinterpret_cast<const __half2 *>(&r);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(r2[e]);
+            kf[8 * q + 2 * e] = f.x;
+            kf[8 * q + 2 * e + 1] = f.y;
+          }
+        }
       }
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
@@ -476,6 +511,21 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
           } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e) vf[u][e] = 0.f;
+          }
+        }
+      }
+      if ((tmask >> (8 * t8)) & 0xffull) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (!((tmask >> (8 * t8 + u)) & 1ull)) continue;
+          const uint4 r = __ldg(reinterpret_cast<const uint4 *>(
+              pl.sink_v + (hd * nsk + sink_slot(ta + u)) * D + c0));
+          const __half2 *r2 = reinterpret_cast<const __half2 *>(&r);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(r2[e]);
+            vf[u][2 * e] = f.x;
+            vf[u][2 * e + 1] = f.y;
           }
         }
       }

@@ -85,6 +85,15 @@ k_decode_split(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
     m[hh] = mn;
   };
 
+  // KIVI-Sink: the sinks of this (b, h); a sink of the quantized region is
+  // read from its fp16 rows
+  __shared__ int ssk[kMaxSink];
+  const int nsk = geo.n_sink;
+  if (nsk > 0) {
+    if (threadIdx.x < nsk) ssk[threadIdx.x] = pl.sink_pos[bh * nsk + threadIdx.x];
+    __syncthreads();
+  }
+
   if (k < tab.nq[b]) {
     const int t0 = k * args.tps;
     const int t1 = min(t0 + args.tps, tab.Tq[b]);
@@ -107,6 +116,28 @@ k_decode_split(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
         beta[hh] = warp_sum(part);
       }
       for (int t = G * g; t < G * g + g; ++t) {
+        int slot = -1;
+        for (int j = 0; j < nsk; ++j)
+          if (ssk[j] == t) slot = j;
+        if (slot >= 0) {
+          const __half *kr = pl.sink_k + (bh * nsk + slot) * D;
+          const __half *vr = pl.sink_v + (bh * nsk + slot) * D;
+          float kv[CPL], v[CPL];
+#pragma unroll
+          for (int u = 0; u < CPL; ++u) {
+            kv[u] = __half2float(kr[lane * CPL + u]);
+            v[u] = __half2float(vr[lane * CPL + u]);
+          }
+#pragma unroll
+          for (int hh = 0; hh < GQ; ++hh) {
+            if (hh >= gq) break;
+            float part = 0.f;
+#pragma unroll
+            for (int u = 0; u < CPL; ++u) part += sq[hh][lane * CPL + u] * kv[u];
+            online(hh, warp_sum(part) * args.scale_log2, v);
+          }
+          continue;
+        }
         const uint8_t *krow = pl.Kc + (bh * geo.Tcap + t) * geo.row;
         const uint8_t *vrow = pl.Vc + (bh * geo.Tcap + t) * geo.row;
         float kc[CPL], v[CPL];

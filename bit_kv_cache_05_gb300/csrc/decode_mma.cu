@@ -11,10 +11,14 @@ namespace {
 using mma::kNW;
 
 bool pick(const Geometry &geo, int GQp, mma::KernelInfo *ki) {
+  const bool sink = geo.n_sink > 0;   // KIVI-Sink: the masking instantiation
   switch (geo.bits) {
-    case 2: return mma::kernel_b2(geo.D, GQp, geo.g, ki);
-    case 4: return mma::kernel_b4(geo.D, GQp, geo.g, ki);
-    case 8: return mma::kernel_b8(geo.D, GQp, geo.g, ki);
+    case 2: return sink ? mma::kernel_sink_b2(geo.D, GQp, geo.g, ki)
+                        : mma::kernel_b2(geo.D, GQp, geo.g, ki);
+    case 4: return sink ? mma::kernel_sink_b4(geo.D, GQp, geo.g, ki)
+                        : mma::kernel_b4(geo.D, GQp, geo.g, ki);
+    case 8: return sink ? mma::kernel_sink_b8(geo.D, GQp, geo.g, ki)
+                        : mma::kernel_b8(geo.D, GQp, geo.g, ki);
     default: return false;
   }
 }

@@ -272,9 +272,11 @@ template <> struct Layout<8> {
 
 // ---- compile-time configuration ---------------------------------------------
 
-template <int D_, int BITS_, int GQP_, int G_>
+template <int D_, int BITS_, int GQP_, int G_, bool SINK_ = false>
 struct Cfg {
   static constexpr int D = D_, BITS = BITS_, GQP = GQP_, G = G_;
+  // KIVI-Sink caches: the instantiation that masks sink tokens' scores
+  static constexpr bool SINK = SINK_;
   // CTAs per SM the register budget is cut for: 4-bit stages (10.75 KB at
   // D = 128) allow one stage per warp only, so those kernels take more
   // warps (16, at most 128 registers) in place of a deeper pipeline; the
@@ -502,6 +504,20 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   float beta_t = 0.f;    // zero-point term of pair tig, current window
   float unscale_t = 1.f; // 2^(24 - k) of this lane's score head
   int cur_w = -1;
+  // KIVI-Sink: the head's sinks in the quantized region, one position per
+  // lane (-1: none); sk_lo / sk_hi bound them (a chunk outside skips the
+  // per-token test).  Their scores are masked here; the merge kernel adds
+  // them from their fp16 rows.
+  int my_sink = -1, sk_lo = 0x7fffffff, sk_hi = -1;
+  auto load_sinks = [&](int b, int h, int Tq) {
+    my_sink = -1;
+    if (lane < geo.n_sink) {
+      const int p = __ldg(pl.sink_pos + ((size_t)b * geo.H_kv + h) * geo.n_sink + lane);
+      if (p >= 0 && p < Tq) my_sink = p;
+    }
+    sk_lo = __reduce_min_sync(kFull, my_sink >= 0 ? my_sink : 0x7fffffff);
+    sk_hi = __reduce_max_sync(kFull, my_sink);
+  };
 
   auto reset_state = [&]() {
 #pragma unroll
@@ -724,7 +740,8 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   // block (independent work the scheduler interleaves), softmax(1),
   // values(1).  FULL: all four tiles hold tokens (every chunk but a head's
   // last quantized one). ----
-  auto chunk = [&](auto full_tag, const unsigned char *st, int t0, int nmt) {
+  auto chunk = [&](auto full_tag, const unsigned char *st, int t0, int nmt,
+                   uint64_t smask) {
     constexpr bool FULL = decltype(full_tag)::value;
     constexpr int MPW = C::MPW;
     const uint4 *kc = reinterpret_cast<const uint4 *>(st + C::S_KC);
@@ -856,6 +873,14 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     // reduced only when some lane holds a score above the running maximum
     auto softmax_half = [&](auto h_tag) {
       constexpr int H = decltype(h_tag)::value;
+      if (smask) {
+        // sink tokens of this chunk: bit (token - t0) of smask
+#pragma unroll
+        for (int mt = 2 * H; mt < 2 * H + 2; ++mt)
+#pragma unroll
+          for (int r = 0; r < 2; ++r)
+            if ((smask >> (16 * mt + gid + 8 * r)) & 1ull) sv[mt][r] = -INFINITY;
+      }
       const float lmax = fmaxf(fmaxf(sv[2 * H][0], sv[2 * H][1]),
                                fmaxf(sv[2 * H + 1][0], sv[2 * H + 1][1]));
       float alpha = 1.f;
@@ -873,10 +898,13 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
 #pragma unroll
         for (int j = 0; j < NZ; ++j) Z[j] *= alpha;
       }
+      // with sinks masked a head's first half may hold no score at all
+      // (m_run still -inf): subtract 0 there, so that every weight is 0
+      const float msub = (smask && m_run == -INFINITY) ? 0.f : m_run;
 #pragma unroll
       for (int mt = 2 * H; mt < 2 * H + 2; ++mt)
 #pragma unroll
-        for (int r = 0; r < 2; ++r) p[mt][r] = exp2_neg(sv[mt][r] - m_run);   // -inf -> 0
+        for (int r = 0; r < 2; ++r) p[mt][r] = exp2_neg(sv[mt][r] - msub);   // -inf -> 0
       const float psum = (p[2 * H][0] + p[2 * H][1]) + (p[2 * H + 1][0] + p[2 * H + 1][1]);
       l_run = fmaf(l_run, alpha, psum);
     };
@@ -1031,6 +1059,7 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     if (hd != cur_hd) {
       reset_state();
       load_q(cu.b, cu.h);
+      if constexpr (C::SINK) load_sinks(cu.b, cu.h, cu.Tq);
       cur_hd = hd;
     }
     {
@@ -1041,10 +1070,18 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
       const unsigned char *st = stage0 + s * C::S_BYTES;
       const int t0 = cu.k * kC;
       const int rem = cu.Tq - t0;
+      uint64_t smask = 0;
+      if (C::SINK && sk_hi >= t0 && sk_lo < t0 + kC) {
+        const int d = my_sink - t0;
+        const bool in = my_sink >= 0 && d >= 0 && d < kC;
+        const unsigned lo = __reduce_or_sync(kFull, in && d < 32 ? 1u << d : 0u);
+        const unsigned hi = __reduce_or_sync(kFull, in && d >= 32 ? 1u << (d - 32) : 0u);
+        smask = (uint64_t)lo | ((uint64_t)hi << 32);
+      }
       if (rem >= kC) {
-        chunk(std::true_type{}, st, t0, 4);
+        chunk(std::true_type{}, st, t0, 4, smask);
       } else {
-        chunk(std::false_type{}, st, t0, rem >> 4);
+        chunk(std::false_type{}, st, t0, rem >> 4, smask);
       }
     }
     const bool head_ends = cu.k == cu.nc - 1 || i == n_mine - 1;
@@ -1179,6 +1216,33 @@ k_merge_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
     }
   }
 
+  // (1b) KIVI-Sink: sinks of the quantized region, from their fp16 rows
+  // (written at prefill; the decode kernel masked their quantized slots)
+  if (geo.n_sink > 0) {
+    const int Tq = tab.Tq[b];
+    for (int k = wp; k < geo.n_sink; k += nw) {
+      const int t = __ldg(pl.sink_pos + (size_t)hd * geo.n_sink + k);
+      if (t < 0 || t >= Tq) continue;
+      const size_t row = ((size_t)hd * geo.n_sink + k) * D;
+      float kv[CPL];
+#pragma unroll
+      for (int u = 0; u < CPL; ++u) kv[u] = __half2float(__ldg(pl.sink_k + row + lane + 32 * u));
+      const float vv = __half2float(__ldg(pl.sink_v + row + c));
+#pragma unroll
+      for (int hh = 0; hh < GQP; ++hh) {
+        if (hh >= GQ) break;
+        const __half *qrow = args.q + ((size_t)b * geo.H_q + h * GQ + hh) * D;
+        float sc = 0.f;
+#pragma unroll
+        for (int u = 0; u < CPL; ++u)
+          sc = fmaf(__half2float(__ldcg(qrow + lane + 32 * u)) * args.scale_log2, kv[u], sc);
+        sc = warp_sum(sc);
+        const float one = 1.f;
+        fold(hh, &sc, &one, &vv, 1);
+      }
+    }
+  }
+
   // (2) the decode kernel's partials, visible once griddepcontrol.wait
   // returns: warp wp serves query head wp mod GQ
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -1248,10 +1312,14 @@ KernelInfo info() {
   return KernelInfo{&k_decode_mma<C>, C::S_BYTES, C::W_STAGE0};
 }
 
-// the instantiations of one bit width (decode_mma_b{2,4,8}.cu)
+// the instantiations of one bit width (decode_mma_b{2,4,8}.cu; with sink
+// masking, decode_mma_sink_b{2,4,8}.cu)
 bool kernel_b2(int D, int GQP, int G, KernelInfo *out);
 bool kernel_b4(int D, int GQP, int G, KernelInfo *out);
 bool kernel_b8(int D, int GQP, int G, KernelInfo *out);
+bool kernel_sink_b2(int D, int GQP, int G, KernelInfo *out);
+bool kernel_sink_b4(int D, int GQP, int G, KernelInfo *out);
+bool kernel_sink_b8(int D, int GQP, int G, KernelInfo *out);
 
 }  // namespace mma
 }  // namespace vqk

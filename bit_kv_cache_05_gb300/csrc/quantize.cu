@@ -224,10 +224,52 @@ k_flush(Geometry geo, Planes pl, const __half *__restrict__ Kin,
   const size_t bh = (size_t)b * H + h;
   const int c = threadIdx.x;   // blockDim.x == D
 
+  // KIVI-Sink: bit i of sinkm = token P0 + i is a sink (left out of every
+  // min/max; its codes 0, its own value groups empty)
+  __shared__ uint32_t sinkm[4];
+  const bool sinks = geo.n_sink > 0;
+  if (sinks) {
+    if (c < 4) sinkm[c] = 0u;
+    __syncthreads();
+    if (c < geo.n_sink) {
+      const int p = pl.sink_pos[bh * geo.n_sink + c];
+      if (p >= P0 && p < P0 + g) atomicOr(&sinkm[(p - P0) >> 5], 1u << ((p - P0) & 31));
+    }
+  }
+  auto is_sink = [&](int i) { return sinks && ((sinkm[i >> 5] >> (i & 31)) & 1u); };
+
   // ---- keys: per channel over the g tokens ----
   load_tile(tile, pl.Kr, Kin, bh, in_stride, P0, split, g, D, geo.Rcap);
   __syncthreads();
-  {
+  if (sinks) {
+    // the group's non-sink tokens only
+    float mn = INFINITY, mx = -INFINITY;
+    for (int i = 0; i < g; ++i) {
+      if (is_sink(i)) continue;
+      const float v = __half2float(tile[i * D + c]);
+      mn = fminf(mn, v);
+      mx = fmaxf(mx, v);
+    }
+    if (mn > mx) { mn = 0.f; mx = 0.f; }   // sinks only: scale and zero +0
+    mn = __fadd_rn(mn, 0.0f);
+    const float scale = __fdiv_rn(__fadd_rn(__fsub_rn(mx, mn), 0.0f), (float)levels);
+    const float rcp = scale != 0.0f ? __frcp_rn(scale) : 0.0f;
+    const size_t idx = (bh * (geo.Tcap / g) + P0 / g) * D + c;
+    const __half sh = __float2half_rn(scale);
+    pl.Ks[idx] = sh;
+    pl.Kz[idx] = __float2half_rn(mn);
+    if (pl.ksmax) {
+      const unsigned m = __reduce_max_sync(0xffffffffu, (unsigned)__half_as_ushort(sh));
+      if ((c & 31) == 0) atomicMax(pl.ksmax + bh, m);
+    }
+    for (int i = 0; i < g; i += 2) {
+      uint32_t c0, c1;
+      quant2(make_float2(__half2float(tile[i * D + c]), __half2float(tile[(i + 1) * D + c])),
+             mn, scale, rcp, c0, c1);
+      codes[i * CS + c] = is_sink(i) ? 0 : (uint8_t)c0;
+      codes[(i + 1) * CS + c] = is_sink(i + 1) ? 0 : (uint8_t)c1;
+    }
+  } else {
     // column c, two tokens per step as an fp16 pair (min / max are exact)
     __half2 mn2 = __float2half2_rn(INFINITY), mx2 = __float2half2_rn(-INFINITY);
     for (int i = 0; i < g; i += 2) {
@@ -271,6 +313,7 @@ k_flush(Geometry geo, Planes pl, const __half *__restrict__ Kin,
     const int ngroups = D / g;
     const int i = c / ngroups, j = c - i * ngroups;   // g * ngroups == D items
     const int p = P0 + i;
+    const bool empty = is_sink(i);   // a sink's value groups have no member
     const __half *row = (p < split ? pl.Vr + (bh * geo.Rcap + (p % geo.Rcap)) * D
                                    : Vin + (bh * in_stride + (p - split)) * D) + j * g;
     __half2 mn2 = __float2half2_rn(INFINITY), mx2 = __float2half2_rn(-INFINITY);
@@ -285,9 +328,9 @@ k_flush(Geometry geo, Planes pl, const __half *__restrict__ Kin,
     }
     float mn = fminf(__low2float(mn2), __high2float(mn2));
     const float mx = fmaxf(__low2float(mx2), __high2float(mx2));
-    mn = __fadd_rn(mn, 0.0f);  // a -0.0 minimum is stored as +0.0
+    mn = empty ? 0.f : __fadd_rn(mn, 0.0f);  // a -0.0 minimum is stored as +0.0
     // a zero range is +0.0 (max - min is -0.0 when the max is -0.0)
-    const float scale = __fdiv_rn(__fadd_rn(__fsub_rn(mx, mn), 0.0f), (float)levels);
+    const float scale = empty ? 0.f : __fdiv_rn(__fadd_rn(__fsub_rn(mx, mn), 0.0f), (float)levels);
     const float rcp = scale != 0.0f ? __frcp_rn(scale) : 0.0f;
     uint32_t *crow = reinterpret_cast<uint32_t *>(codes + i * CS + j * g);
     for (int k = 0; k < g; k += 8) {
@@ -473,7 +516,14 @@ __global__ void k_dequantize(Geometry geo, Planes pl, LenTable lens,
        i < (int64_t)S * c8; i += (int64_t)gridDim.x * blockDim.x) {
     const int t = (int)(i / c8), c0 = (int)(i - (int64_t)t * c8) * 8;
     uint4 ko, vo;
-    if (t < Tq) {
+    int slot = -1;   // KIVI-Sink: a sink of the quantized region is exact
+    for (int j = 0; j < geo.n_sink && t < Tq; ++j)
+      if (pl.sink_pos[(size_t)hd * geo.n_sink + j] == t) slot = j;
+    if (slot >= 0) {
+      const size_t sr = ((size_t)hd * geo.n_sink + slot) * D + c0;
+      ko = *reinterpret_cast<const uint4 *>(pl.sink_k + sr);
+      vo = *reinterpret_cast<const uint4 *>(pl.sink_v + sr);
+    } else if (t < Tq) {
       const size_t r = (size_t)hd * geo.Tcap + t;
       uint32_t kc[8], vc[8];
       codes8(geo, pl.Kc + r * geo.row, pl.Vc + (r - (t & 15)) * geo.row, t & 15,

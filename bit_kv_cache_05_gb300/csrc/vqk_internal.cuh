@@ -23,7 +23,14 @@ struct Planes {
   float *part;               // [B][H_q][max_items][D+2]    split partials
   uint32_t *ksmax;           // [B][H_kv] fp16 bits of the largest key scale
                              // flushed for the head (a bound for the decode)
+  // KIVI-Sink store (Geometry::n_sink > 0): per (b, h) the sink tokens'
+  // positions, ascending, -1 in unused slots, and their fp16 rows
+  int32_t *sink_pos = nullptr;   // [B][H_kv][n_sink]
+  __half *sink_k = nullptr;      // [B][H_kv][n_sink][D]
+  __half *sink_v = nullptr;      // [B][H_kv][n_sink][D]
 };
+
+constexpr int kMaxSink = 16;     // sinks per (sequence, kv head)
 
 // orders of the code planes (see "code-plane orders" below)
 constexpr int kLayoutPacked = 0;
@@ -36,6 +43,7 @@ struct Geometry {
   int row;    // packed bytes per token row (D*bits/8)
   int max_items;  // decode work items per sequence (quantized splits + 1)
   int layout = kLayoutPacked;   // order of the code planes (below)
+  int n_sink = 0;               // KIVI-Sink tokens per (sequence, kv head)
 };
 
 // ---- code-plane orders --------------------------------------------------
@@ -145,6 +153,17 @@ cudaError_t launch_flush(const Geometry &geo, const Planes &pl,
                          const __half *Kin, const __half *Vin,
                          int64_t in_stride, const FlushTable &tab,
                          int total_groups, cudaStream_t st);
+// KIVI-Sink: per (b, h) the min(n_sink, S_b) prefill tokens with the
+// largest key norms (fp32 sum of squares in channel order; equal norms: the
+// earlier token), their positions ascending in pl.sink_pos and their rows
+// copied into pl.sink_k / pl.sink_v.  K, V: the prefill inputs.
+struct SinkTable {
+  int32_t S[kMaxB];
+};
+cudaError_t launch_pick_sinks(const Geometry &geo, const Planes &pl,
+                              const __half *K, const __half *V,
+                              int64_t s_stride, const SinkTable &tab,
+                              cudaStream_t st);
 cudaError_t launch_tail(const Geometry &geo, const Planes &pl,
                         const __half *Kin, const __half *Vin,
                         int64_t in_stride, const TailTable &tab,

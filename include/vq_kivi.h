@@ -97,6 +97,28 @@ int vq_kivi_quantize(const vq_kivi_params *p, const void *K, const void *V,
                      int64_t s_stride, const int32_t *seq_lens, void *stream,
                      vq_kivi_cache **out);
 
+/* Options of a cache beyond the problem statement (all zero: plain KIVI).
+ *   n_sink  KIVI-Sink (changelog v0.9.0 "New"): per (sequence, kv head) the
+ *           n_sink prefill tokens with the largest key L2 norms (fp32 sum of
+ *           squares, channel 0 first; on equal norms the earlier token) are
+ *           kept in fp16 beside the cache and left out of their groups'
+ *           min/max: a key group is quantized from its other tokens (the
+ *           sink's codes are 0; a group of sinks only stores scale and zero
+ *           +0), and a sink's own value groups are empty (scale, zero and
+ *           codes 0).  Attention reads a sink of the quantized region from
+ *           its fp16 rows.  Chosen once, at vq_kivi_quantize_ex, among all
+ *           the prefill tokens; appended tokens never become sinks.
+ *           0 <= n_sink <= 16; 0 is plain KIVI, bit for bit. */
+typedef struct vq_kivi_options {
+  int32_t n_sink;
+} vq_kivi_options;
+
+/* vq_kivi_quantize with options (NULL options = all zero). */
+int vq_kivi_quantize_ex(const vq_kivi_params *p, const vq_kivi_options *opt,
+                        const void *K, const void *V, int64_t s_stride,
+                        const int32_t *seq_lens, void *stream,
+                        vq_kivi_cache **out);
+
 /* Append n_new[b] tokens to sequence b: push them onto the fp16 residual and
  * flush the oldest whole groups so that the residual rule holds again
  * (changelog v0.8.0 update_and_fetch; v0.28.0 chunk-flush).  The result is
@@ -169,6 +191,9 @@ int vq_kivi_get_params(const vq_kivi_cache *c, vq_kivi_params *p);
  *   5 Vz  fp16  [B][H_kv][Tcap][D/g]       value zeros
  *   6 Kr  fp16  [B][H_kv][R+g][D]          residual keys, slot i = token T_q+i
  *   7 Vr  fp16  [B][H_kv][R+g][D]          residual values
+ *   8 sink positions  int32 [B][H_kv][n_sink]  ascending, -1 when unused
+ *   9 sink keys       fp16  [B][H_kv][n_sink][D]
+ *  10 sink values     fp16  [B][H_kv][n_sink][D]  (8-10: size 0 without sinks)
  * where Tcap = ceil(max_seq/g)*g (at least g).  vq_kivi_plane_bytes gives
  * the size (0 for a bad `which`); vq_kivi_export writes the whole plane to
  * device memory `dst` of at least that size, on `stream`.  Only the valid
@@ -201,6 +226,9 @@ int vq_kivi_dequantize(const vq_kivi_cache *c, void *K_hat, void *V_hat,
  * fp16 size of the same tokens for comparison. */
 typedef struct vq_kivi_bytes {
   uint64_t code_bytes, meta_bytes, residual_bytes, fp16_bytes;
+  uint64_t sink_bytes;  /* fp16 K and V of the sinks in the quantized region
+                           (a sink still in the residual window is counted
+                           there, once) */
 } vq_kivi_bytes;
 int vq_kivi_cache_bytes(const vq_kivi_cache *c, vq_kivi_bytes *out);
 
