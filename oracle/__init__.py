@@ -33,7 +33,7 @@ _lock = threading.Lock()
 _lib = None
 
 PLANES = ("Kc", "Ks", "Kz", "Vc", "Vs", "Vz", "Kr", "Vr",
-          "sink_pos", "sink_k", "sink_v")
+          "sink_pos", "sink_k", "sink_v", "Kmask", "Vf")
 
 
 def build(force: bool = False) -> str:
@@ -62,6 +62,7 @@ def _load():
         lib.orc_new.argtypes = [i32] * 8
         lib.orc_free.argtypes = [P]
         lib.orc_set_sinks.argtypes = [P, i32]
+        lib.orc_set_kitty.argtypes = [P, i32]
         lib.orc_quantize.argtypes = [P, P, P, i64, P]
         lib.orc_append.argtypes = [P, P, P, i64, P]
         lib.orc_attend.argtypes = [P, P, f64, P]
@@ -144,7 +145,7 @@ class OracleCache:
     """
 
     def __init__(self, B, H_q, H_kv, D, bits, group, residual, max_seq,
-                 n_sink=0):
+                 n_sink=0, kitty_hi=None):
         self.B, self.H_q, self.H_kv, self.D = B, H_q, H_kv, D
         self.bits, self.group, self.residual, self.max_seq = (
             bits, group, residual, max_seq)
@@ -156,6 +157,9 @@ class OracleCache:
             raise ValueError("oracle: unsupported cache parameters")
         if self._lib.orc_set_sinks(self._c, n_sink) != 0:
             raise ValueError("oracle: bad sink count")
+        self.kitty_hi = kitty_hi
+        if kitty_hi is not None and self._lib.orc_set_kitty(self._c, kitty_hi) != 0:
+            raise ValueError("oracle: bad Kitty parameters")
         tcap = np.zeros(1, np.int32)
         rcap = np.zeros(1, np.int32)
         self._lib.orc_dims(self._c, _ptr(tcap), _ptr(rcap))
@@ -231,6 +235,13 @@ class OracleCache:
         self._lib.orc_get_plane(self._c, which, _ptr(raw))
         B, H, D, g = self.B, self.H_kv, self.D, self.group
         row = D * self.bits // 8
+        if name == "Kc" and self.kitty_hi is not None:
+            krow = (self.kitty_hi * 4 + (D - self.kitty_hi) * 2) // 8
+            return raw.reshape(B, H, self.Tcap, krow)
+        if name == "Kmask":
+            return raw.view(np.uint32).reshape(B, H, self.Tcap // g, D // 32)
+        if name == "Vf":
+            return raw.view(np.float16).reshape(B, H, self.Tcap, D)
         if name in ("Kc", "Vc"):
             return raw.reshape(B, H, self.Tcap, row)
         if name in ("Ks", "Kz"):

@@ -136,6 +136,16 @@ typedef struct orc_cache {
   int n_sink;
   int32_t *sink_pos;       /* [B][Hkv][n_sink] */
   uint16_t *sink_k, *sink_v; /* [B][Hkv][n_sink][D] */
+  /* Kitty (0 = plain KIVI): kitty_hi channels of every key group get 4-bit
+   * codes, the other D - kitty_hi 2-bit; values stay fp16.  Per (b, h,
+   * channel) the running sums of the quantized keys as integers in units of
+   * 2^-24 (every fp16 value is an integer multiple of 2^-24). */
+  int kitty_hi;
+  int krow;                /* key code bytes per token row */
+  uint32_t *Kmask;         /* [B][Hkv][Tcap/g][D/32] 4-bit channels */
+  uint16_t *Vf;            /* [B][Hkv][Tcap][D] fp16 values */
+  int64_t *ksum;           /* [B][Hkv][D] */
+  unsigned __int128 *ksq;  /* [B][Hkv][D] */
 } orc_cache;
 
 static int n_quantized(int S, int R, int g) {
@@ -188,7 +198,72 @@ void orc_free(orc_cache *c) {
   free(c->Kc); free(c->Vc); free(c->Ks); free(c->Kz); free(c->Vs);
   free(c->Vz); free(c->Kr); free(c->Vr); free(c->S); free(c->Tq);
   free(c->nres); free(c->sink_pos); free(c->sink_k); free(c->sink_v);
+  free(c->Kmask); free(c->Vf); free(c->ksum); free(c->ksq);
   free(c);
+}
+
+/* Kitty (changelog v0.11.0 "New"): channel-wise mixed-precision keys.  For
+ * every key group the hi channels with the largest running variance get
+ * 4-bit codes, the rest 2-bit; values are kept in fp16.  Call on a fresh
+ * cache of bits = 2, before orc_quantize.  hi in [0, D], a multiple of 8.
+ * Returns 0, or -1 on bad arguments or a failed allocation. */
+int orc_set_kitty(orc_cache *c, int hi) {
+  if (hi < 0 || hi > c->D || hi % 8 != 0 || c->bits != 2 || c->n_sink != 0 ||
+      c->D % 32 != 0 || c->max_seq > (1 << 20) || c->Kmask)
+    return -1;
+  c->kitty_hi = hi;
+  c->krow = (hi * 4 + (c->D - hi) * 2) / 8;
+  size_t bh = (size_t)c->B * c->Hkv;
+  free(c->Kc);
+  c->Kc = (uint8_t *)calloc(bh * c->Tcap * c->krow, 1);
+  c->Kmask = (uint32_t *)calloc(bh * (c->Tcap / c->g) * (c->D / 32), 4);
+  c->Vf = (uint16_t *)calloc(bh * c->Tcap * c->D, 2);
+  c->ksum = (int64_t *)calloc(bh * c->D, 8);
+  c->ksq = (unsigned __int128 *)calloc(bh * c->D, sizeof(unsigned __int128));
+  if (!c->Kc || !c->Kmask || !c->Vf || !c->ksum || !c->ksq) return -1;
+  return 0;
+}
+
+/* fp16 bits -> the value as an integer multiple of 2^-24 (exact) */
+static int64_t f16_units(uint16_t bits) {
+  int e = (bits >> 10) & 31;
+  int64_t m = bits & 1023;
+  if (e == 0) return (bits & 0x8000) ? -m : m;      /* subnormal: m 2^-24 */
+  int64_t v = (m | 1024) << (e - 1);                /* (1024 + m) 2^(e-25) */
+  return (bits & 0x8000) ? -v : v;
+}
+
+/* Kitty: rank the channels of key group G of (b, h) after adding the
+ * group's keys (rows krow(ctx, i)) to the running sums: the hi channels
+ * with the largest N sum(x^2) - (sum x)^2 (N times the population
+ * variance, exact in 128-bit integers; the smaller channel first on equal
+ * values), as a bit mask in mask[D/32]. */
+static void kitty_rank(orc_cache *c, int b, int h, int G, const uint16_t **rows,
+                       uint32_t *mask) {
+  const int D = c->D, g = c->g;
+  size_t bh = (size_t)b * c->Hkv + h;
+  int64_t *ks = c->ksum + bh * D;
+  unsigned __int128 *kq = c->ksq + bh * D;
+  unsigned __int128 *var = (unsigned __int128 *)malloc(sizeof(unsigned __int128) * D);
+  const unsigned __int128 N = (unsigned __int128)((G + 1) * g);
+  for (int ch = 0; ch < D; ++ch) {
+    for (int i = 0; i < g; ++i) {
+      int64_t m = f16_units(rows[i][ch]);
+      ks[ch] += m;
+      kq[ch] += (unsigned __int128)((__int128)m * m);
+    }
+    __int128 sm = ks[ch];
+    unsigned __int128 s2 = (unsigned __int128)(sm < 0 ? -sm : sm);
+    var[ch] = N * kq[ch] - s2 * s2;
+  }
+  for (int w = 0; w < D / 32; ++w) mask[w] = 0;
+  for (int ch = 0; ch < D; ++ch) {
+    int rank = 0; /* channels ranked before ch */
+    for (int o = 0; o < D; ++o)
+      if (var[o] > var[ch] || (var[o] == var[ch] && o < ch)) ++rank;
+    if (rank < c->kitty_hi) mask[ch / 32] |= 1u << (ch % 32);
+  }
+  free(var);
 }
 
 /* KIVI-Sink (changelog v0.9.0 "New"): tokens with the largest key L2 norms
@@ -272,6 +347,44 @@ static void quantize_group_of_tokens(orc_cache *c, int b, int h, int G,
                                      const void *ctx) {
   const int D = c->D, g = c->g;
   size_t bh = (size_t)b * c->Hkv + h;
+  if (c->Kmask) {
+    /* Kitty: rank, then per channel 4- or 2-bit codes over the g tokens;
+     * row layout: the 4-bit channels' codes in ascending channel order
+     * (LSB-first), then the 2-bit channels' */
+    const uint16_t *rows[4096];
+    for (int i = 0; i < g; ++i) rows[i] = krow(ctx, i);
+    uint32_t *mask = c->Kmask + (bh * (c->Tcap / g) + G) * (D / 32);
+    kitty_rank(c, b, h, G, rows, mask);
+    float *xk = (float *)malloc(sizeof(float) * g);
+    uint8_t *ck = (uint8_t *)malloc((size_t)g * D);
+    for (int ch = 0; ch < D; ++ch) {
+      const int hi = (mask[ch / 32] >> (ch % 32)) & 1;
+      uint16_t s16, z16;
+      for (int i = 0; i < g; ++i) xk[i] = h2f(rows[i][ch]);
+      uint8_t cc[4096];
+      quant_group(xk, 1, g, hi ? 4 : 2, cc, 1, NULL, &s16, &z16);
+      for (int i = 0; i < g; ++i) ck[(size_t)i * D + ch] = cc[i];
+      c->Ks[(bh * (c->Tcap / g) + G) * D + ch] = s16;
+      c->Kz[(bh * (c->Tcap / g) + G) * D + ch] = z16;
+    }
+    for (int i = 0; i < g; ++i) {
+      size_t t = (size_t)G * g + i;
+      uint8_t *row = c->Kc + (bh * c->Tcap + t) * c->krow;
+      int bit = 0;
+      memset(row, 0, (size_t)c->krow);
+      for (int pass = 0; pass < 2; ++pass)   /* 4-bit channels, then 2-bit */
+        for (int ch = 0; ch < D; ++ch) {
+          const int hi = (mask[ch / 32] >> (ch % 32)) & 1;
+          if (hi != (pass == 0)) continue;
+          row[bit / 8] |= (uint8_t)(ck[(size_t)i * D + ch] << (bit % 8));
+          bit += hi ? 4 : 2;
+        }
+      memcpy(c->Vf + (bh * c->Tcap + t) * D, vrow(ctx, i), 2 * (size_t)D);
+    }
+    free(xk);
+    free(ck);
+    return;
+  }
   float *x = (float *)malloc(sizeof(float) * (size_t)g * D);
   uint8_t *codes = (uint8_t *)malloc((size_t)g * D);
   /* sink tokens of this group (KIVI-Sink): left out of every min/max,
@@ -361,6 +474,10 @@ int orc_quantize(orc_cache *c, const uint16_t *K, const uint16_t *V,
   for (int b = 0; b < c->B; ++b)
     if (seq_lens[b] < 0 || seq_lens[b] > c->max_seq || seq_lens[b] > s_stride)
       return -1;
+  if (c->Kmask) { /* Kitty: the running sums start over */
+    memset(c->ksum, 0, sizeof(int64_t) * (size_t)c->B * c->Hkv * c->D);
+    memset(c->ksq, 0, sizeof(unsigned __int128) * (size_t)c->B * c->Hkv * c->D);
+  }
   for (int b = 0; b < c->B; ++b) {
     int S = seq_lens[b];
     int Tq = n_quantized(S, c->R, c->g);
@@ -458,6 +575,25 @@ static void token_hat(const orc_cache *c, int b, int h, int t, double *k,
       k[ch] = h2f(c->sink_k[(bh * c->n_sink + slot) * D + ch]);
       v[ch] = h2f(c->sink_v[(bh * c->n_sink + slot) * D + ch]);
     }
+    return;
+  }
+  if (t < c->Tq[b] && c->Kmask) {
+    const int G = t / g;
+    const uint32_t *mask = c->Kmask + (bh * (c->Tcap / g) + G) * (D / 32);
+    const uint8_t *row = c->Kc + (bh * c->Tcap + t) * c->krow;
+    int bit = 0;
+    for (int pass = 0; pass < 2; ++pass)
+      for (int ch = 0; ch < D; ++ch) {
+        const int hi = (mask[ch / 32] >> (ch % 32)) & 1;
+        if (hi != (pass == 0)) continue;
+        const int w = hi ? 4 : 2;
+        const int code = (row[bit / 8] >> (bit % 8)) & ((1 << w) - 1);
+        bit += w;
+        double sc = h2f(c->Ks[(bh * (c->Tcap / g) + G) * D + ch]);
+        double z = h2f(c->Kz[(bh * (c->Tcap / g) + G) * D + ch]);
+        k[ch] = (double)code * sc + z;
+      }
+    for (int ch = 0; ch < D; ++ch) v[ch] = h2f(c->Vf[(bh * c->Tcap + t) * D + ch]);
     return;
   }
   if (t < c->Tq[b]) {
@@ -605,12 +741,15 @@ void orc_dims(const orc_cache *c, int32_t *Tcap, int32_t *Rcap) {
 size_t orc_plane_bytes(const orc_cache *c, int which) {
   size_t bh = (size_t)c->B * c->Hkv;
   switch (which) {
-    case 0: case 3: return bh * c->Tcap * c->row;
+    case 0: return bh * c->Tcap * (c->Kmask ? c->krow : c->row);
+    case 3: return bh * c->Tcap * c->row;
     case 1: case 2: return bh * (c->Tcap / c->g) * c->D * 2;
     case 4: case 5: return bh * c->Tcap * (c->D / c->g) * 2;
     case 6: case 7: return bh * c->Rcap * c->D * 2;
     case 8: return bh * c->n_sink * 4;
     case 9: case 10: return bh * c->n_sink * c->D * 2;
+    case 11: return c->Kmask ? bh * (c->Tcap / c->g) * (c->D / 32) * 4 : 0;
+    case 12: return c->Vf ? bh * c->Tcap * c->D * 2 : 0;
     default: return 0;
   }
 }
@@ -629,6 +768,8 @@ int orc_get_plane(const orc_cache *c, int which, void *dst) {
     case 8: src = c->sink_pos; break;
     case 9: src = c->sink_k; break;
     case 10: src = c->sink_v; break;
+    case 11: src = c->Kmask; break;
+    case 12: src = c->Vf; break;
     default: return -1;
   }
   if (!src) return orc_plane_bytes(c, which) == 0 ? 0 : -1;

@@ -754,3 +754,180 @@ def test_sink_in_the_window_is_left_out_when_flushed(oracle_mod):
     for ch in range(D):
         _, _, s16, _ = oracle_mod.quant_group(K[0, 0, [8, 10, 11], ch].astype(np.float32), 2)
         assert Ks[2, ch] == s16
+
+
+# ---------------------------------------------------------------------------
+# Kitty: per key group, the kitty_hi channels of largest running variance in
+# 4 bits, the rest in 2 bits; values in fp16 (changelog v0.11.0 "New")
+# ---------------------------------------------------------------------------
+
+def np_kitty_keys(oc, b, h):
+    """k_hat [Tq][D] in long double from the Kitty planes: per token row the
+    4-bit channels' codes in ascending channel order, then the 2-bit ones,
+    LSB first; the group's mask marks the 4-bit channels."""
+    _, Tq, _ = oc.lengths()
+    D, g = oc.D, oc.group
+    kc = oc.plane("Kc")[b, h]
+    masks = oc.plane("Kmask")[b, h]
+    Ks = oc.plane("Ks")[b, h].astype(np.longdouble)
+    Kz = oc.plane("Kz")[b, h].astype(np.longdouble)
+    out = np.zeros((Tq[b], D), np.longdouble)
+    for t in range(Tq[b]):
+        G = t // g
+        hi = [(int(masks[G, c // 32]) >> (c % 32)) & 1 for c in range(D)]
+        bits = "".join(format(int(x), "08b")[::-1] for x in kc[t])   # LSB first
+        pos = 0
+        for want in (1, 0):
+            for c in range(D):
+                if hi[c] != want:
+                    continue
+                w = 4 if want else 2
+                code = int(bits[pos:pos + w][::-1], 2)
+                pos += w
+                out[t, c] = code * Ks[G, c] + Kz[G, c]
+    return out
+
+
+def _kitty(oracle_mod, hi, K, V, lens, Hq=None, g=8, R=8):
+    from oracle import OracleCache
+    B, H, S_max, D = K.shape
+    oc = OracleCache(B, Hq or H, H, D, 2, g, R, S_max, kitty_hi=hi)
+    oc.quantize(K, V, lens)
+    return oc
+
+
+def test_kitty_ranks_channels_by_variance(oracle_mod):
+    """Channel c alternates +a_c / -a_c inside every key group, so its
+    running variance is a_c^2: the 4-bit channels are the hi largest a_c,
+    the smaller channel index first among equal a_c."""
+    B, H, D, g = 1, 1, 32, 8
+    S = 5 * g + 8
+    # the 8th place is a tie between channels 2 and 4 (a = 2): channel 2 wins
+    a = np.array([1, 7, 2, 7, 2, 9, 4, 0.5, 6, 5, 8, 1.5] + [0.25] * 20, np.float64)
+    sign = np.where(np.arange(S) % 2 == 0, 1.0, -1.0)
+    K = (sign[:, None] * a[None, :]).astype(np.float16)[None, None]
+    V = np.zeros_like(K)
+    oc = _kitty(oracle_mod, 8, K, V, [S], g=g, R=8)
+    want = sorted(range(D), key=lambda c: (-a[c], c))[:8]
+    mask = oc.plane("Kmask")[0, 0]
+    for G in range(oc.lengths()[1][0] // g):
+        got = [c for c in range(D) if (int(mask[G, c // 32]) >> (c % 32)) & 1]
+        assert got == sorted(want), G
+
+
+def test_kitty_hi_zero_and_all_reduce_to_kivi_keys(oracle_mod):
+    """kitty_hi = 0 quantizes every key channel in 2 bits and kitty_hi = D
+    every one in 4 bits: the key codes, scales and zeros are then those of a
+    plain KIVI cache of that width (same packing), and the values are the
+    fp16 inputs unchanged."""
+    from oracle import OracleCache
+    rng = np.random.default_rng(40)
+    B, H, D, g, R = 2, 2, 32, 8, 8
+    lens = [60, 35]
+    K = rand_f16(rng, (B, H, 64, D), 2.0)
+    V = rand_f16(rng, (B, H, 64, D))
+    for hi, bits in ((0, 2), (D, 4)):
+        kt = _kitty(oracle_mod, hi, K, V, lens, g=g, R=R)
+        kv = OracleCache(B, H, H, D, bits, g, R, 64)
+        kv.quantize(K, V, lens)
+        _, Tq, _ = kv.lengths()
+        for b in range(B):
+            for name in ("Kc", "Ks", "Kz"):
+                assert np.array_equal(kt.plane(name)[b, :, :Tq[b] // (g if name != "Kc" else 1)].view(np.uint8),
+                                      kv.plane(name)[b, :, :Tq[b] // (g if name != "Kc" else 1)].view(np.uint8)), (hi, name)
+            assert np.array_equal(kt.plane("Vf")[b, :, :Tq[b]], V[b, :, :Tq[b]])
+
+
+def test_kitty_hi_channels_err_less_and_beat_uniform_2bit(oracle_mod):
+    """Each channel reconstructs within half its step: (max-min)/15 for the
+    4-bit channels, /3 for the 2-bit ones; on keys whose variance sits in a
+    quarter of the channels, Kitty's key error is well below uniform 2-bit
+    KIVI's."""
+    from oracle import OracleCache
+    rng = np.random.default_rng(41)
+    B, H, D, g, R, S = 1, 1, 64, 16, 16, 96
+    scale = np.ones(D)
+    scale[rng.permutation(D)[:16]] = 12.0
+    K = (rng.standard_normal((B, H, S, D)) * scale).astype(np.float16)
+    V = rand_f16(rng, (B, H, S, D))
+    oc = _kitty(oracle_mod, 16, K, V, [S], g=g, R=R)
+    k = np_kitty_keys(oc, 0, 0).astype(np.float64)
+    Tq = oc.lengths()[1][0]
+    x = K[0, 0, :Tq].astype(np.float64)
+    mask = oc.plane("Kmask")[0, 0]
+    for G in range(Tq // g):
+        rows = slice(G * g, (G + 1) * g)
+        rng_c = x[rows].max(0) - x[rows].min(0)
+        for c in range(D):
+            hi = (int(mask[G, c // 32]) >> (c % 32)) & 1
+            step = rng_c[c] / (15 if hi else 3)
+            assert np.abs(k[rows, c] - x[rows, c]).max() <= step / 2 * (1 + 1e-3) + 2.0 ** -20
+    kv = OracleCache(B, H, H, D, 2, g, R, S)
+    kv.quantize(K, V, [S])
+    k2, _ = np_dequant_sequence(kv, 0, 0)
+    e_kitty = ((k - x) ** 2).mean()
+    e_kivi = ((k2[:Tq].astype(np.float64) - x) ** 2).mean()
+    assert e_kitty < 0.3 * e_kivi
+
+
+def test_kitty_prefill_equals_appends(oracle_mod):
+    """The ranking of a group uses the running sums up to that group's last
+    token, so prefill and any chunking of appends give the same cache, bit
+    for bit."""
+    from oracle import OracleCache
+    rng = np.random.default_rng(42)
+    B, H, D, g, R = 2, 1, 32, 8, 5
+    S_final = [70, 41]
+    K = rand_f16(rng, (B, H, 72, D), 3.0)
+    V = rand_f16(rng, (B, H, 72, D))
+    ref = _kitty(oracle_mod, 8, K, V, S_final, g=g, R=R)
+    oc = OracleCache(B, H, H, D, 2, g, R, 72, kitty_hi=8)
+    oc.quantize(K, V, [3, 3])
+    cur = [3, 3]
+    step = 0
+    while cur != S_final:
+        n = [min([1, 9, 4][(step + b) % 3], S_final[b] - cur[b]) for b in range(B)]
+        Kn = np.zeros((B, H, max(n), D), np.float16)
+        Vn = np.zeros_like(Kn)
+        for b in range(B):
+            Kn[b, :, :n[b]] = K[b, :, cur[b]:cur[b] + n[b]]
+            Vn[b, :, :n[b]] = V[b, :, cur[b]:cur[b] + n[b]]
+        oc.append(Kn, Vn, n)
+        cur = [c + x for c, x in zip(cur, n)]
+        step += 1
+    _, Tq, _ = ref.lengths()
+    for b in range(B):
+        for name in ("Kc", "Ks", "Kz", "Kmask", "Vf"):
+            n = Tq[b] // g if name in ("Ks", "Kz", "Kmask") else Tq[b]
+            assert np.array_equal(oc.plane(name)[b, :, :n].view(np.uint8),
+                                  ref.plane(name)[b, :, :n].view(np.uint8)), name
+
+
+def test_kitty_attention_brute_force(oracle_mod):
+    """Attention over Kitty keys (independent unpacker) and exact fp16
+    values, long double, equals the oracle to 1e-12 (one query; causal
+    multi-query to 1e-6)."""
+    rng = np.random.default_rng(43)
+    B, Hq, H, D, g, R = 2, 4, 2, 32, 8, 6
+    lens = [53, 30]
+    K = rand_f16(rng, (B, H, 56, D), 2.0)
+    V = rand_f16(rng, (B, H, 56, D))
+    oc = _kitty(oracle_mod, 8, K, V, lens, Hq=Hq, g=g, R=R)
+    q = rand_f16(rng, (B, Hq, D))
+    q3 = rand_f16(rng, (B, Hq, 3, D))
+    outm = oc.attend_multi(q3, 0.3)
+    _, Tq, nres = oc.lengths()
+    for b in range(B):
+        for hq in range(Hq):
+            h = hq // 2
+            kq = np_kitty_keys(oc, b, h)
+            kr = oc.plane("Kr")[b, h, :nres[b]].astype(np.longdouble)
+            vq = oc.plane("Vf")[b, h, :Tq[b]].astype(np.longdouble)
+            vr = oc.plane("Vr")[b, h, :nres[b]].astype(np.longdouble)
+            k = np.concatenate([kq, kr])
+            v = np.concatenate([vq, vr])
+            ref = np_dense_attention(q[b, hq].astype(np.longdouble), k, v, np.longdouble(0.3))
+            assert np.abs(oc.attend_one(b, hq, q[b, hq], 0.3) - ref.astype(np.float64)).max() <= 1e-12
+            refm = np_causal_attention(q3[b, hq].astype(np.longdouble), k, v,
+                                       np.longdouble(0.3), lens[b])
+            assert np.abs(outm[b, hq] - refm.astype(np.float64)).max() <= 1e-6
