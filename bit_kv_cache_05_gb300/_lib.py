@@ -52,13 +52,14 @@ class Planes(ctypes.Structure):
 
 
 class Options(ctypes.Structure):
-    _fields_ = [("n_sink", ctypes.c_int32)]
+    _fields_ = [("n_sink", ctypes.c_int32), ("kitty", ctypes.c_int32),
+                ("kitty_hi", ctypes.c_int32)]
 
 
 class Bytes(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in
                 ("code_bytes", "meta_bytes", "residual_bytes", "fp16_bytes",
-                 "sink_bytes")]
+                 "sink_bytes", "value_fp16_bytes")]
 
 
 _lock = threading.Lock()

@@ -15,7 +15,7 @@ import torch
 from . import _lib
 
 PLANES = ("Kc", "Ks", "Kz", "Vc", "Vs", "Vz", "Kr", "Vr",
-          "sink_pos", "sink_k", "sink_v")
+          "sink_pos", "sink_k", "sink_v", "Kmask", "Vf")
 
 
 def _stream_handle(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
@@ -47,6 +47,7 @@ class KiviCache:
     def __init__(self, K: torch.Tensor, V: torch.Tensor, seq_lens, *, H_q: int,
                  bits: int, group: int, residual: int,
                  max_seq: Optional[int] = None, n_sink: int = 0,
+                 kitty_hi: Optional[int] = None,
                  stream: Optional[torch.cuda.Stream] = None):
         L = _lib.load()
         if K.shape != V.shape or K.dim() != 4:
@@ -64,7 +65,9 @@ class KiviCache:
         kp = _dev_ptr(K, torch.float16, "K")
         vp = _dev_ptr(V, torch.float16, "V")
         self.n_sink = int(n_sink)
-        opts = _lib.Options(self.n_sink)
+        self.kitty_hi = kitty_hi
+        opts = _lib.Options(self.n_sink, 0 if kitty_hi is None else 1,
+                            0 if kitty_hi is None else int(kitty_hi))
         _lib.check(L.vq_kivi_quantize_ex(ctypes.byref(self.params),
                                          ctypes.byref(opts), kp, vp,
                                          S_stride, _i32_array(lens),
@@ -138,6 +141,12 @@ class KiviCache:
             _stream_handle(stream)))
         B, H, D, g = self.B, self.H_kv, self.D, self.group
         row = D * self.bits // 8
+        if name == "Kc" and self.kitty_hi is not None:
+            return raw.view(B, H, -1, (D + self.kitty_hi) // 4)
+        if name == "Kmask":
+            return raw.view(torch.int32).view(B, H, -1, D // 32)
+        if name == "Vf":
+            return raw.view(torch.float16).view(B, H, -1, D)
         if name == "sink_pos":
             return raw.view(torch.int32).view(B, H, self.n_sink)
         if name in ("sink_k", "sink_v"):

@@ -133,9 +133,19 @@ int vq_kivi_quantize_ex(const vq_kivi_params *p, const vq_kivi_options *opt,
                         vq_kivi_cache **out) {
   int rc = check_params(p);
   if (rc) return rc;
-  const vq_kivi_options o = opt ? *opt : vq_kivi_options{0};
+  const vq_kivi_options o = opt ? *opt : vq_kivi_options{0, 0, 0};
   if (o.n_sink < 0 || o.n_sink > kMaxSink)
     return fail(VQ_ERR_ARG, "n_sink=%d outside [0, %d]", o.n_sink, kMaxSink);
+  if (o.kitty) {
+    if (p->bits != 2 || o.n_sink != 0 || p->D % 32 != 0)
+      return fail(VQ_ERR_UNSUPPORTED, "Kitty needs bits=2, n_sink=0 and D a "
+                  "multiple of 32");
+    if (o.kitty_hi < 0 || o.kitty_hi > p->D || o.kitty_hi % 16 != 0)
+      return fail(VQ_ERR_ARG, "kitty_hi=%d: a multiple of 16 in [0, D=%d]",
+                  o.kitty_hi, p->D);
+    if (p->max_seq > (1 << 20))
+      return fail(VQ_ERR_UNSUPPORTED, "Kitty: max_seq=%d > 2^20", p->max_seq);
+  }
   if (!out) return fail(VQ_ERR_ARG, "out is NULL");
   if (!seq_lens) return fail(VQ_ERR_ARG, "seq_lens is NULL");
   int32_t smax = 0;
@@ -177,17 +187,24 @@ int vq_kivi_quantize_ex(const vq_kivi_params *p, const vq_kivi_options *opt,
   geo.Rcap = p->residual + g;
   geo.row = p->D * p->bits / 8;
   geo.n_sink = o.n_sink;
+  geo.kitty = o.kitty ? 1 : 0;
+  geo.kitty_hi = o.kitty ? o.kitty_hi : 0;
   const int32_t unit = split_unit(g);
   const int32_t tps_for_cap = (int32_t)round_up((geo.Tcap + 1023) / 1024, unit);
   c->tps_min = tps_for_cap > 256 ? tps_for_cap : 256;
   geo.max_items = (geo.Tcap + c->tps_min - 1) / c->tps_min + 1;
 
   const size_t BH = (size_t)p->B * p->H_kv;
+  const bool kitty = geo.kitty != 0;
+  const size_t krow = (size_t)(p->D + geo.kitty_hi) / 4;
   const size_t sz_codes = BH * geo.Tcap * geo.row;
+  const size_t sz_kcodes = kitty ? BH * geo.Tcap * krow : sz_codes;
+  const size_t sz_vcodes = kitty ? 0 : sz_codes;
   const size_t sz_kmeta = BH * (geo.Tcap / g) * p->D * sizeof(__half);
-  const size_t sz_vmeta = BH * geo.Tcap * (p->D / g) * sizeof(__half);
+  const size_t sz_vmeta = kitty ? 0 : BH * geo.Tcap * (p->D / g) * sizeof(__half);
   const size_t sz_res = BH * geo.Rcap * p->D * sizeof(__half);
-  c->use_mma = mma_plan(geo, c->sm_count, &c->plan);
+  // Kitty: the CUDA-core decode over mixed-width key rows
+  c->use_mma = !kitty && mma_plan(geo, c->sm_count, &c->plan);
   // 2- and 4-bit caches decoded on the tensor cores keep their codes in the
   // order the MMA fragments consume them
   geo.layout = c->use_mma && (p->bits == 2 || p->bits == 4) ? kLayoutFrag : kLayoutPacked;
@@ -199,8 +216,8 @@ int vq_kivi_quantize_ex(const vq_kivi_params *p, const vq_kivi_options *opt,
   const size_t sz_part = n_part * sizeof(float);
   const size_t A = 256;
   size_t off = 0;
-  size_t o_Kc = off; off += round_up(sz_codes, A);
-  size_t o_Vc = off; off += round_up(sz_codes, A);
+  size_t o_Kc = off; off += round_up(sz_kcodes, A);
+  size_t o_Vc = off; off += round_up(sz_vcodes, A);
   size_t o_Ks = off; off += round_up(sz_kmeta, A);
   size_t o_Kz = off; off += round_up(sz_kmeta, A);
   size_t o_Vs = off; off += round_up(sz_vmeta, A);
@@ -213,6 +230,10 @@ int vq_kivi_quantize_ex(const vq_kivi_params *p, const vq_kivi_options *opt,
   size_t o_spos = off; off += round_up(BH * o.n_sink * sizeof(int32_t), A);
   size_t o_sk = off; off += round_up(BH * o.n_sink * p->D * sizeof(__half), A);
   size_t o_sv = off; off += round_up(BH * o.n_sink * p->D * sizeof(__half), A);
+  size_t o_kmask = off; off += round_up(kitty ? BH * (geo.Tcap / g) * (p->D / 32) * 4 : 0, A);
+  size_t o_vf = off; off += round_up(kitty ? BH * geo.Tcap * p->D * sizeof(__half) : 0, A);
+  size_t o_ksum = off; off += round_up(kitty ? BH * p->D * 8 : 0, A);
+  size_t o_ksq = off; off += round_up(kitty ? BH * p->D * 16 : 0, A);
   c->block_bytes = off;
 
   e = cudaMallocAsync(&c->block, c->block_bytes, st);
@@ -239,6 +260,12 @@ int vq_kivi_quantize_ex(const vq_kivi_params *p, const vq_kivi_options *opt,
     pl.sink_pos = (int32_t *)(base + o_spos);
     pl.sink_k = (__half *)(base + o_sk);
     pl.sink_v = (__half *)(base + o_sv);
+  }
+  if (kitty) {
+    pl.kmask = (uint32_t *)(base + o_kmask);
+    pl.Vf = (__half *)(base + o_vf);
+    pl.ksum = (long long *)(base + o_ksum);
+    pl.ksq = (unsigned long long *)(base + o_ksq);
   }
   c->last_stream = st;
 
@@ -276,8 +303,10 @@ int vq_kivi_quantize_ex(const vq_kivi_params *p, const vq_kivi_options *opt,
                           sk, st);
     if (e != cudaSuccess) return abort_create(e, "sink selection launch");
   }
-  e = launch_flush(geo, pl, (const __half *)K, (const __half *)V, s_stride, ft,
-                   ft.prefix[p->B], st);
+  e = kitty ? launch_flush_kitty(geo, pl, (const __half *)K, (const __half *)V,
+                                 s_stride, ft, ft.prefix[p->B], st)
+            : launch_flush(geo, pl, (const __half *)K, (const __half *)V, s_stride, ft,
+                           ft.prefix[p->B], st);
   if (e != cudaSuccess) return abort_create(e, "quantize kernel launch");
   e = launch_tail(geo, pl, (const __half *)K, (const __half *)V, s_stride, tt,
                   tt.prefix[p->B], st);
@@ -327,9 +356,12 @@ int vq_kivi_append(vq_kivi_cache *c, const void *K_new, const void *V_new,
     tt.row0[b] = keep0 - S_old;
     tt.pos0[b] = keep0;
   }
-  cudaError_t e = launch_flush(c->geo, c->pl, (const __half *)K_new,
-                               (const __half *)V_new, n_stride, ft,
-                               ft.prefix[p.B], st);
+  cudaError_t e = c->geo.kitty
+      ? launch_flush_kitty(c->geo, c->pl, (const __half *)K_new, (const __half *)V_new,
+                           n_stride, ft, ft.prefix[p.B], st)
+      : launch_flush(c->geo, c->pl, (const __half *)K_new,
+                     (const __half *)V_new, n_stride, ft,
+                     ft.prefix[p.B], st);
   if (e != cudaSuccess) return cuda_fail(e, "flush kernel launch");
   e = launch_tail(c->geo, c->pl, (const __half *)K_new, (const __half *)V_new,
                   n_stride, tt, tt.prefix[p.B], st);
@@ -442,6 +474,8 @@ int vq_kivi_attend_multi(vq_kivi_cache *c, const void *q, int32_t S_q,
       return fail(VQ_ERR_ARG, "sequence %d holds %d tokens, fewer than S_q=%d",
                   b, c->S[b], S_q);
   const int GQ = p.H_q / p.H_kv;
+  if (c->geo.kitty)
+    return fail(VQ_ERR_UNSUPPORTED, "multi-query attend: not for Kitty caches");
   if (p.D != 64 && p.D != 128)
     return fail(VQ_ERR_UNSUPPORTED, "multi-query attend: D=%d (supported: 64, 128)", p.D);
   if (GQ != 1 && GQ != 2 && GQ != 4 && GQ != 8)
@@ -508,10 +542,14 @@ size_t vq_kivi_plane_bytes(const vq_kivi_cache *c, int which) {
   if (!c) return 0;
   const Geometry &geo = c->geo;
   const size_t BH = (size_t)geo.B * geo.H_kv;
+  const bool kitty = geo.kitty != 0;
   switch (which) {
-    case 0: case 3: return BH * geo.Tcap * geo.row;
+    case 0: return BH * geo.Tcap * (kitty ? (size_t)(geo.D + geo.kitty_hi) / 4 : geo.row);
+    case 3: return kitty ? 0 : BH * geo.Tcap * geo.row;
     case 1: case 2: return BH * (geo.Tcap / geo.g) * geo.D * sizeof(__half);
-    case 4: case 5: return BH * geo.Tcap * (geo.D / geo.g) * sizeof(__half);
+    case 4: case 5: return kitty ? 0 : BH * geo.Tcap * (geo.D / geo.g) * sizeof(__half);
+    case 11: return kitty ? BH * (geo.Tcap / geo.g) * (geo.D / 32) * 4 : 0;
+    case 12: return kitty ? BH * geo.Tcap * geo.D * sizeof(__half) : 0;
     case 6: case 7: return BH * geo.Rcap * geo.D * sizeof(__half);
     case 8: return BH * geo.n_sink * sizeof(int32_t);
     case 9: case 10: return BH * geo.n_sink * geo.D * sizeof(__half);
@@ -524,7 +562,10 @@ int vq_kivi_export(const vq_kivi_cache *c, int which, void *dst,
   int rc = check_cache(c);
   if (rc) return rc;
   const size_t need = vq_kivi_plane_bytes(c, which);
-  if (need == 0 && which >= 8 && which <= 10) return VQ_OK;   // no sinks
+  // an empty plane (no sinks, no Kitty, or a Kitty cache's value codes)
+  if (need == 0 && which >= 0 && which <= 12 && which != 1 && which != 2 &&
+      which != 6 && which != 7)
+    return VQ_OK;
   if (need == 0) return fail(VQ_ERR_ARG, "which=%d is not a plane", which);
   if (!dst) return fail(VQ_ERR_ARG, "dst is NULL");
   if (dst_bytes < need)
@@ -542,10 +583,12 @@ int vq_kivi_export(const vq_kivi_cache *c, int which, void *dst,
     case 8: src = c->pl.sink_pos; break;
     case 9: src = c->pl.sink_k; break;
     case 10: src = c->pl.sink_v; break;
+    case 11: src = c->pl.kmask; break;
+    case 12: src = c->pl.Vf; break;
     default: break;
   }
   cudaError_t e;
-  if ((which == 0 || which == 3) && c->geo.layout == kLayoutFrag) {
+  if ((which == 0 || which == 3) && c->geo.layout == kLayoutFrag && !c->geo.kitty) {
     e = launch_export_frag(c->geo, (const uint8_t *)src, which == 3, dst, st);
   } else if (src) {
     e = cudaMemcpyAsync(dst, src, need, cudaMemcpyDeviceToDevice, st);
@@ -560,6 +603,8 @@ int vq_kivi_dequantize(const vq_kivi_cache *c, void *K_hat, void *V_hat,
                        int64_t s_stride, void *stream) {
   int rc = check_cache(c);
   if (rc) return rc;
+  if (c->geo.kitty)
+    return fail(VQ_ERR_UNSUPPORTED, "dequantize: not for Kitty caches");
   if (!K_hat || !V_hat) return fail(VQ_ERR_ARG, "K_hat or V_hat is NULL");
   if (((uintptr_t)K_hat | (uintptr_t)V_hat) & 15u)
     return fail(VQ_ERR_ARG, "K_hat and V_hat must be 16-byte aligned");
@@ -580,9 +625,20 @@ int vq_kivi_cache_bytes(const vq_kivi_cache *c, vq_kivi_bytes *out) {
   if (!c || !out) return fail(VQ_ERR_ARG, "NULL argument");
   const vq_kivi_params &p = c->p;
   const uint64_t row = (uint64_t)c->geo.row;
-  vq_kivi_bytes r = {0, 0, 0, 0};
+  vq_kivi_bytes r = {0, 0, 0, 0, 0, 0};
+  const bool kitty = c->geo.kitty != 0;
   for (int b = 0; b < p.B; ++b) {
     const uint64_t Tq = (uint64_t)c->Tq[b], H = (uint64_t)p.H_kv;
+    if (kitty) {
+      // mixed-width key rows, key scale/zero and the 4-bit channel masks,
+      // fp16 values
+      r.code_bytes += H * Tq * (uint64_t)((p.D + c->geo.kitty_hi) / 4);
+      r.meta_bytes += H * ((Tq / p.group) * p.D * 4 + (Tq / p.group) * (p.D / 8));
+      r.value_fp16_bytes += H * Tq * p.D * 2;
+      r.residual_bytes += H * (uint64_t)c->nres[b] * p.D * 4;
+      r.fp16_bytes += H * (uint64_t)c->S[b] * p.D * 4;
+      continue;
+    }
     r.code_bytes += 2 * H * Tq * row;
     r.meta_bytes += H * ((Tq / p.group) * p.D * 4 + Tq * (p.D / p.group) * 4);
     r.residual_bytes += H * (uint64_t)c->nres[b] * p.D * 4;

@@ -232,6 +232,7 @@ __global__ void k_combine(Geometry geo, Planes pl, DecodeArgs args,
 cudaError_t launch_decode(const Geometry &geo, const Planes &pl,
                           const DecodeArgs &args, const DecodeTable &tab,
                           cudaStream_t st) {
+  if (geo.kitty) return launch_decode_kitty(geo, pl, args, tab, st);
   if (args.total_items > 0) {
     dim3 grid(args.total_items, geo.H_kv);
 #define VQK_CASE(DD, BB)                                                    \
@@ -247,6 +248,12 @@ cudaError_t launch_decode(const Geometry &geo, const Planes &pl,
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  return launch_combine(geo, pl, args, tab, st);
+}
+
+cudaError_t launch_combine(const Geometry &geo, const Planes &pl,
+                           const DecodeArgs &args, const DecodeTable &tab,
+                           cudaStream_t st) {
   k_combine<<<geo.B * geo.H_q, min(geo.D, 256), 0, st>>>(geo, pl, args, tab);
   count_launch();
   return cudaGetLastError();

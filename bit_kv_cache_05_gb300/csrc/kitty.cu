@@ -1,0 +1,349 @@
+// Kitty: channel-wise mixed-precision keys (4-bit channels of high running
+// variance, 2-bit for the rest) and fp16 values; its flush and its fused
+// decode.
+//
+// Method: VeloxQuant-MLX changelog v0.11.0 "New" (Kitty: key channels ranked
+// by online per-channel variance, the top 25% quantized in 4 bits and the
+// rest in 2 bits with KIVI's asymmetric group quantization; values left at
+// fp16) on the KIVI cache of v0.8.0 (key groups of g tokens per channel,
+// fp16 residual window).  The ranking of a key group uses the running
+// variance over the tokens up to the group's last one, computed exactly:
+// every fp16 value is an integer multiple of 2^-24, so with m = x * 2^24
+// the sums S1 = sum m (int64) and S2 = sum m^2 (a 128-bit integer) are
+// exact and N S2 - S1^2 = N^2 var is compared as a 128-bit integer (N <=
+// 2^20 keeps it below 2^120).  The smaller channel wins a tie.
+#include "vqk_internal.cuh"
+
+namespace vqk {
+namespace {
+
+typedef unsigned __int128 u128;
+
+__device__ __forceinline__ int find_seq(const int32_t *prefix, int B, int item) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// fp16 bits -> the value in units of 2^-24 (exact)
+__device__ __forceinline__ long long f16_units(unsigned short bits) {
+  const int e = (bits >> 10) & 31;
+  const long long m = bits & 1023;
+  const long long v = e == 0 ? m : (m | 1024) << (e - 1);
+  return (bits & 0x8000) ? -v : v;
+}
+
+// the fp16 row of token position p of (b, h) during a flush: the residual
+// ring below src_split, the input rows above (as in the KIVI flush)
+__device__ __forceinline__ const __half *src_row(const Geometry &geo, const Planes &pl,
+                                                 const __half *in, int64_t in_stride,
+                                                 size_t bh, int p, int split) {
+  return p < split ? pl.Kr + (bh * geo.Rcap + (p % geo.Rcap)) * geo.D
+                   : in + (bh * in_stride + (p - split)) * geo.D;
+}
+
+// One CTA per (kv head, sequence), one thread per channel: walks the groups
+// this flush quantizes, in token order, adding each group's keys to the
+// running sums and ranking the channels after each group.
+__global__ void k_kitty_rank(Geometry geo, Planes pl, const __half *__restrict__ Kin,
+                             int64_t in_stride, FlushTable tab) {
+  __shared__ unsigned long long vlo[kMaxD], vhi[kMaxD];
+  const int h = blockIdx.x, b = blockIdx.y, c = threadIdx.x;
+  const int D = geo.D, g = geo.g;
+  const int n = tab.prefix[b + 1] - tab.prefix[b];
+  if (n == 0) return;
+  const size_t bh = (size_t)b * geo.H_kv + h;
+  long long s1 = pl.ksum[bh * D + c];
+  u128 s2 = ((u128)pl.ksq[(bh * D + c) * 2 + 1] << 64) | pl.ksq[(bh * D + c) * 2];
+  const int split = tab.src_split[b];
+  for (int k = 0; k < n; ++k) {
+    const int P0 = tab.first_pos[b] + k * g;
+    for (int i = 0; i < g; ++i) {
+      const __half *row = src_row(geo, pl, Kin, in_stride, bh, P0 + i, split);
+      const long long m = f16_units(__half_as_ushort(row[c]));
+      s1 += m;
+      s2 += (u128)((__int128)m * m);
+    }
+    const u128 N = (u128)(P0 + g);
+    const u128 a = (u128)(s1 < 0 ? -s1 : s1);
+    const u128 var = N * s2 - a * a;
+    vlo[c] = (unsigned long long)var;
+    vhi[c] = (unsigned long long)(var >> 64);
+    __syncthreads();
+    int rank = 0;
+    for (int o = 0; o < D; ++o) {
+      const u128 vo = ((u128)vhi[o] << 64) | vlo[o];
+      rank += (vo > var || (vo == var && o < c)) ? 1 : 0;
+    }
+    const unsigned word = __ballot_sync(0xffffffffu, rank < geo.kitty_hi);
+    if ((c & 31) == 0)
+      pl.kmask[(bh * (geo.Tcap / g) + P0 / g) * (D / 32) + (c >> 5)] = word;
+    __syncthreads();
+  }
+  pl.ksum[bh * D + c] = s1;
+  pl.ksq[(bh * D + c) * 2] = (unsigned long long)s2;
+  pl.ksq[(bh * D + c) * 2 + 1] = (unsigned long long)(s2 >> 64);
+}
+
+// One CTA per (group, kv head), one thread per channel: per channel a 4- or
+// 2-bit group quantizer (fp32, IEEE, ties to even, as the KIVI flush), the
+// codes OR-ed into the group's packed rows in shared memory (4- and 2-bit
+// fields never straddle a 32-bit word), then the rows and the group's fp16
+// values stored.
+__global__ void k_flush_kitty(Geometry geo, Planes pl, const __half *__restrict__ Kin,
+                              const __half *__restrict__ Vin, int64_t in_stride,
+                              FlushTable tab) {
+  extern __shared__ __align__(16) unsigned char ksm[];
+  const int D = geo.D, g = geo.g, c = threadIdx.x;
+  const int krow = (D + geo.kitty_hi) / 4;              // bytes per token row
+  uint32_t *rows = reinterpret_cast<uint32_t *>(ksm);   // [g][krow / 4]
+  const int item = blockIdx.x, h = blockIdx.y;
+  const int b = find_seq(tab.prefix, geo.B, item);
+  const int P0 = tab.first_pos[b] + (item - tab.prefix[b]) * g;
+  const int split = tab.src_split[b];
+  const size_t bh = (size_t)b * geo.H_kv + h;
+  for (int i = c; i < g * krow / 4; i += blockDim.x) rows[i] = 0u;
+
+  // this channel's width and bit offset within a row
+  const uint32_t *mk = pl.kmask + (bh * (geo.Tcap / g) + P0 / g) * (D / 32);
+  int below = 0;
+  for (int w = 0; w < (c >> 5); ++w) below += __popc(mk[w]);
+  const uint32_t mw = mk[c >> 5];
+  below += __popc(mw & ((1u << (c & 31)) - 1u));
+  const bool hi = (mw >> (c & 31)) & 1u;
+  const int off = hi ? 4 * below : 4 * geo.kitty_hi + 2 * (c - below);
+  const int levels = hi ? 15 : 3;
+  __syncthreads();
+
+  float mn = INFINITY, mx = -INFINITY;
+  for (int i = 0; i < g; ++i) {
+    const float x = __half2float(src_row(geo, pl, Kin, in_stride, bh, P0 + i, split)[c]);
+    mn = fminf(mn, x);
+    mx = fmaxf(mx, x);
+  }
+  mn = __fadd_rn(mn, 0.0f);   // a -0.0 minimum is stored as +0.0
+  const float scale = __fdiv_rn(__fadd_rn(__fsub_rn(mx, mn), 0.0f), (float)levels);
+  const size_t gi = (bh * (geo.Tcap / g) + P0 / g) * D + c;
+  pl.Ks[gi] = __float2half_rn(scale);
+  pl.Kz[gi] = __float2half_rn(mn);
+  for (int i = 0; i < g; ++i) {
+    uint32_t code = 0;
+    if (scale != 0.0f) {
+      const float x = __half2float(src_row(geo, pl, Kin, in_stride, bh, P0 + i, split)[c]);
+      float r = rintf(__fdiv_rn(__fsub_rn(x, mn), scale));
+      r = fminf(fmaxf(r, 0.0f), (float)levels);
+      code = (uint32_t)r;
+    }
+    if (code) atomicOr(&rows[i * (krow / 4) + (off >> 5)], code << (off & 31));
+  }
+  __syncthreads();
+  // the group's rows are contiguous: g * krow bytes (a multiple of 16)
+  uint4 *dst = reinterpret_cast<uint4 *>(pl.Kc + (bh * geo.Tcap + P0) * krow);
+  const uint4 *srow = reinterpret_cast<const uint4 *>(rows);
+  for (int i = c; i < g * krow / 16; i += blockDim.x) dst[i] = srow[i];
+  // the fp16 values of the group's tokens
+  const int cpr = D / 8;
+  for (int idx = c; idx < g * cpr; idx += blockDim.x) {
+    const int i = idx / cpr, c8 = (idx - i * cpr) * 8;
+    const int p = P0 + i;
+    const __half *vs = p < split ? pl.Vr + (bh * geo.Rcap + (p % geo.Rcap)) * D
+                                 : Vin + (bh * in_stride + (p - split)) * D;
+    *reinterpret_cast<uint4 *>(pl.Vf + (bh * geo.Tcap + p) * D + c8) =
+        *reinterpret_cast<const uint4 *>(vs + c8);
+  }
+}
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Fused decode over a Kitty cache: one CTA per (work item, kv head), each
+// warp owns whole key groups (or residual tokens) and keeps (m, l, o) per
+// query head; lane owns channels lane*CPL ... lane*CPL + CPL-1.  Keys: per
+// group the lane's fields (width and offset in the row) and q'.s, q'.z are
+// set once; per token the codes come from the row's 32-bit words.  Values:
+// the fp16 row.  Partials as the CUDA-core KIVI decode (launch_combine
+// merges them).
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+k_decode_kitty(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
+  constexpr int CPL = D / 32;
+  constexpr int GQ = kMaxGroupHeads;
+  __shared__ float sq[GQ][D];
+  __shared__ float sm[kWarps][GQ], sl[kWarps][GQ];
+  __shared__ float so[kWarps][GQ][D];
+  const int item = blockIdx.x, h = blockIdx.y;
+  const int b = find_seq(tab.prefix, geo.B, item);
+  const int k = item - tab.prefix[b];
+  const int gq = geo.H_q / geo.H_kv, g = geo.g;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const size_t bh = (size_t)b * geo.H_kv + h;
+  const int krow = (D + geo.kitty_hi) / 4;
+  for (int i = threadIdx.x; i < gq * D; i += kThreads) {
+    const int hh = i / D, c = i % D;
+    sq[hh][c] = __half2float(args.q[((size_t)b * geo.H_q + h * gq + hh) * D + c]);
+  }
+  __syncthreads();
+  float m[GQ], l[GQ], o[GQ][CPL];
+#pragma unroll
+  for (int hh = 0; hh < GQ; ++hh) {
+    m[hh] = -INFINITY; l[hh] = 0.f;
+#pragma unroll
+    for (int u = 0; u < CPL; ++u) o[hh][u] = 0.f;
+  }
+  auto online = [&](int hh, float s2, const float *v) {
+    const float mn = fmaxf(m[hh], s2);
+    const float alpha = exp2f(m[hh] - mn);
+    const float p = exp2f(s2 - mn);
+    l[hh] = l[hh] * alpha + p;
+#pragma unroll
+    for (int u = 0; u < CPL; ++u) o[hh][u] = o[hh][u] * alpha + p * v[u];
+    m[hh] = mn;
+  };
+
+  if (k < tab.nq[b]) {
+    const int t0 = k * args.tps, t1 = min(t0 + args.tps, tab.Tq[b]);
+    for (int G = t0 / g + warp; G * g < t1; G += kWarps) {
+      const size_t gidx = (bh * (geo.Tcap / g) + G) * D;
+      const uint32_t *mk = pl.kmask + (bh * (geo.Tcap / g) + G) * (D / 32);
+      int word[CPL], sh[CPL];
+      uint32_t msk[CPL];
+      float a[GQ][CPL], beta[GQ];
+#pragma unroll
+      for (int u = 0; u < CPL; ++u) {
+        const int c = lane * CPL + u;
+        int below = 0;
+        for (int w = 0; w < (c >> 5); ++w) below += __popc(mk[w]);
+        const uint32_t mw = mk[c >> 5];
+        below += __popc(mw & ((1u << (c & 31)) - 1u));
+        const bool hi = (mw >> (c & 31)) & 1u;
+        const int off = hi ? 4 * below : 4 * geo.kitty_hi + 2 * (c - below);
+        word[u] = off >> 5;
+        sh[u] = off & 31;
+        msk[u] = hi ? 15u : 3u;
+      }
+#pragma unroll
+      for (int hh = 0; hh < GQ; ++hh) {
+        float part = 0.f;
+#pragma unroll
+        for (int u = 0; u < CPL; ++u) {
+          const int c = lane * CPL + u;
+          const float s = __half2float(pl.Ks[gidx + c]);
+          const float z = __half2float(pl.Kz[gidx + c]);
+          const float qc = hh < gq ? sq[hh][c] : 0.f;
+          a[hh][u] = qc * s;
+          part += qc * z;
+        }
+        beta[hh] = warp_sum(part);
+      }
+      for (int t = G * g; t < G * g + g; ++t) {
+        const uint32_t *row = reinterpret_cast<const uint32_t *>(
+            pl.Kc + (bh * geo.Tcap + t) * krow);
+        float kc[CPL], v[CPL];
+        const __half *vrow = pl.Vf + (bh * geo.Tcap + t) * D + lane * CPL;
+#pragma unroll
+        for (int u = 0; u < CPL; ++u) {
+          kc[u] = (float)((__ldg(row + word[u]) >> sh[u]) & msk[u]);
+          v[u] = __half2float(vrow[u]);
+        }
+#pragma unroll
+        for (int hh = 0; hh < GQ; ++hh) {
+          if (hh >= gq) break;
+          float part = 0.f;
+#pragma unroll
+          for (int u = 0; u < CPL; ++u) part += a[hh][u] * kc[u];
+          online(hh, (warp_sum(part) + beta[hh]) * args.scale_log2, v);
+        }
+      }
+    }
+  } else {
+    const int Tq = tab.Tq[b];
+    for (int i = warp; i < tab.nres[b]; i += kWarps) {
+      const int slot = (Tq + i) % geo.Rcap;
+      const __half *kr = pl.Kr + (bh * geo.Rcap + slot) * D;
+      const __half *vr = pl.Vr + (bh * geo.Rcap + slot) * D;
+      float kv[CPL], v[CPL];
+#pragma unroll
+      for (int u = 0; u < CPL; ++u) {
+        kv[u] = __half2float(kr[lane * CPL + u]);
+        v[u] = __half2float(vr[lane * CPL + u]);
+      }
+#pragma unroll
+      for (int hh = 0; hh < GQ; ++hh) {
+        if (hh >= gq) break;
+        float part = 0.f;
+#pragma unroll
+        for (int u = 0; u < CPL; ++u) part += sq[hh][lane * CPL + u] * kv[u];
+        online(hh, warp_sum(part) * args.scale_log2, v);
+      }
+    }
+  }
+
+#pragma unroll
+  for (int hh = 0; hh < GQ; ++hh) {
+    if (hh >= gq) break;
+    if (lane == 0) { sm[warp][hh] = m[hh]; sl[warp][hh] = l[hh]; }
+#pragma unroll
+    for (int u = 0; u < CPL; ++u) so[warp][hh][lane * CPL + u] = o[hh][u];
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < gq * (D + 2); i += kThreads) {
+    const int hh = i / (D + 2), c = i % (D + 2);
+    float M = -INFINITY;
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm[w][hh]);
+    float acc = 0.f;
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = sm[w][hh] == -INFINITY ? 0.f : exp2f(sm[w][hh] - M);
+      acc += f * (c < D ? so[w][hh][c] : sl[w][hh]);
+    }
+    const int hq = h * gq + hh;
+    float *dst = pl.part + (((size_t)b * geo.H_q + hq) * geo.max_items + k) * (D + 2);
+    dst[c] = c == D ? M : acc;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_flush_kitty(const Geometry &geo, const Planes &pl,
+                               const __half *Kin, const __half *Vin,
+                               int64_t in_stride, const FlushTable &tab,
+                               int total_groups, cudaStream_t st) {
+  if (total_groups <= 0) return cudaSuccess;
+  k_kitty_rank<<<dim3(geo.H_kv, geo.B), geo.D, 0, st>>>(geo, pl, Kin, in_stride, tab);
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t smem = (size_t)geo.g * (geo.D + geo.kitty_hi) / 4;
+  k_flush_kitty<<<dim3(total_groups, geo.H_kv), geo.D, smem, st>>>(geo, pl, Kin, Vin,
+                                                                   in_stride, tab);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_kitty(const Geometry &geo, const Planes &pl,
+                                const DecodeArgs &args, const DecodeTable &tab,
+                                cudaStream_t st) {
+  if (args.total_items > 0) {
+    dim3 grid(args.total_items, geo.H_kv);
+    switch (geo.D) {
+      case 64: k_decode_kitty<64><<<grid, kThreads, 0, st>>>(geo, pl, args, tab); break;
+      case 128: k_decode_kitty<128><<<grid, kThreads, 0, st>>>(geo, pl, args, tab); break;
+      case 256: k_decode_kitty<256><<<grid, kThreads, 0, st>>>(geo, pl, args, tab); break;
+      default: return cudaErrorInvalidValue;
+    }
+    count_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return launch_combine(geo, pl, args, tab, st);
+}
+
+}  // namespace vqk

@@ -28,6 +28,14 @@ struct Planes {
   int32_t *sink_pos = nullptr;   // [B][H_kv][n_sink]
   __half *sink_k = nullptr;      // [B][H_kv][n_sink][D]
   __half *sink_v = nullptr;      // [B][H_kv][n_sink][D]
+  // Kitty (Geometry::kitty): the 4-bit channels of every key group, the
+  // fp16 values of the quantized tokens, and per (b, h, channel) the running
+  // sums of the quantized keys in 2^-24 units (sum x: int64; sum x^2: a
+  // 128-bit integer as two uint64, low word first)
+  uint32_t *kmask = nullptr;     // [B][H_kv][Tcap/g][D/32]
+  __half *Vf = nullptr;          // [B][H_kv][Tcap][D]
+  long long *ksum = nullptr;     // [B][H_kv][D]
+  unsigned long long *ksq = nullptr;  // [B][H_kv][D][2]
 };
 
 constexpr int kMaxSink = 16;     // sinks per (sequence, kv head)
@@ -44,6 +52,8 @@ struct Geometry {
   int max_items;  // decode work items per sequence (quantized splits + 1)
   int layout = kLayoutPacked;   // order of the code planes (below)
   int n_sink = 0;               // KIVI-Sink tokens per (sequence, kv head)
+  int kitty = 0;                // Kitty cache (mixed 4/2-bit keys, fp16 values)
+  int kitty_hi = 0;             // Kitty: 4-bit channels per key group
 };
 
 // ---- code-plane orders --------------------------------------------------
@@ -203,6 +213,27 @@ struct DecodeArgs {
 cudaError_t launch_decode(const Geometry &geo, const Planes &pl,
                           const DecodeArgs &args, const DecodeTable &tab,
                           cudaStream_t st);
+// the log-sum-exp merge of the split partials of launch_decode
+cudaError_t launch_combine(const Geometry &geo, const Planes &pl,
+                           const DecodeArgs &args, const DecodeTable &tab,
+                           cudaStream_t st);
+
+// ---- Kitty (kitty.cu): channel-wise mixed-precision keys, fp16 values ------
+//
+// Per key group of g tokens the kitty_hi channels with the largest running
+// variance (N sum x^2 - (sum x)^2 over tokens 0 ... the group's last, in
+// 128-bit integers of 2^-24 units; the smaller channel first on ties) get
+// 4-bit codes, the other 2-bit.  A token row of Kc holds krow = (D +
+// kitty_hi) / 4 bytes: the 4-bit channels' codes in ascending channel order,
+// LSB first, then the 2-bit channels'.  Kmask marks the 4-bit channels of
+// each group; values of quantized tokens are kept in fp16 in Vf.
+cudaError_t launch_flush_kitty(const Geometry &geo, const Planes &pl,
+                               const __half *Kin, const __half *Vin,
+                               int64_t in_stride, const FlushTable &tab,
+                               int total_groups, cudaStream_t st);
+cudaError_t launch_decode_kitty(const Geometry &geo, const Planes &pl,
+                                const DecodeArgs &args, const DecodeTable &tab,
+                                cudaStream_t st);
 
 // ---- decode on the tensor cores (D = 64/128, H_q/H_kv <= 4) ---------------
 

@@ -111,6 +111,22 @@ int vq_kivi_quantize(const vq_kivi_params *p, const void *K, const void *V,
  *           0 <= n_sink <= 16; 0 is plain KIVI, bit for bit. */
 typedef struct vq_kivi_options {
   int32_t n_sink;
+  /* Kitty (changelog v0.11.0 "New"), kitty != 0: channel-wise
+   * mixed-precision keys and fp16 values.  Every key group of g tokens
+   * quantizes its kitty_hi channels of largest running variance in 4 bits
+   * and the others in 2 bits (KIVI's per-channel group quantizer at that
+   * width); the running variance of a group is taken over the tokens up to
+   * the group's last one, exactly (N sum x^2 - (sum x)^2 in 128-bit
+   * integers of 2^-24 units), the smaller channel first on ties.  Values
+   * of quantized tokens are kept in fp16.  A key row holds (D + kitty_hi)/4
+   * bytes: the 4-bit channels' codes in ascending channel order, LSB
+   * first, then the 2-bit channels'.  Requires bits = 2, n_sink = 0,
+   * kitty_hi a multiple of 16 in [0, D], max_seq <= 2^20.  The pages'
+   * default is kitty_hi = D / 4.  Decode runs on the CUDA cores;
+   * vq_kivi_attend_multi and vq_kivi_dequantize do not serve Kitty caches
+   * (VQ_ERR_UNSUPPORTED). */
+  int32_t kitty;
+  int32_t kitty_hi;
 } vq_kivi_options;
 
 /* vq_kivi_quantize with options (NULL options = all zero). */
@@ -194,6 +210,11 @@ int vq_kivi_get_params(const vq_kivi_cache *c, vq_kivi_params *p);
  *   8 sink positions  int32 [B][H_kv][n_sink]  ascending, -1 when unused
  *   9 sink keys       fp16  [B][H_kv][n_sink][D]
  *  10 sink values     fp16  [B][H_kv][n_sink][D]  (8-10: size 0 without sinks)
+ *  11 Kitty 4-bit channel masks  uint32 [B][H_kv][Tcap/g][D/32]
+ *  12 Kitty fp16 values          fp16   [B][H_kv][Tcap][D]
+ * A Kitty cache's plane 0 has rows of (D + kitty_hi)/4 bytes (see
+ * vq_kivi_options) and planes 3-5 are empty; without Kitty 11-12 are empty.
+ * An empty plane has size 0 and its export does nothing.
  * where Tcap = ceil(max_seq/g)*g (at least g).  vq_kivi_plane_bytes gives
  * the size (0 for a bad `which`); vq_kivi_export writes the whole plane to
  * device memory `dst` of at least that size, on `stream`.  Only the valid
@@ -229,6 +250,7 @@ typedef struct vq_kivi_bytes {
   uint64_t sink_bytes;  /* fp16 K and V of the sinks in the quantized region
                            (a sink still in the residual window is counted
                            there, once) */
+  uint64_t value_fp16_bytes;  /* Kitty: fp16 values of the quantized tokens */
 } vq_kivi_bytes;
 int vq_kivi_cache_bytes(const vq_kivi_cache *c, vq_kivi_bytes *out);
 
