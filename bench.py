@@ -485,6 +485,12 @@ def run_ours(args, w, rank, world, local):
             measure_workload(synth.workload("pages_S32768"), peak, full=False,
                              n_sink=5), n_sink=5)
         torch.cuda.empty_cache()
+        # Kitty decode at the pages' shape (a quarter of the key channels in
+        # 4 bits, the pages' default kitty_hi_fraction)
+        targets["pages_S32768_kitty"] = dict(
+            measure_workload(synth.workload("pages_S32768"), peak, full=False,
+                             kitty_hi=32), kitty_hi=32)
+        torch.cuda.empty_cache()
         tpk, tpk_kind = measured_peak_tflops()
         targets["int4_append_prefill_attend"] = dict(
             measure_multi(synth.workload("int4_append"), 512, tpk),
@@ -537,7 +543,7 @@ def run_ours(args, w, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
-def measure_workload(w, peak, full=True, n_sink=0):
+def measure_workload(w, peak, full=True, n_sink=0, kitty_hi=None):
     """The decode of workload `w` from HBM (rotating over cache copies larger
     than 4x L2, the median of 100 launches), and the append of the
     workload's appended tokens per sequence (one token when it appends none)
@@ -564,7 +570,8 @@ def measure_workload(w, peak, full=True, n_sink=0):
         caches.append(KiviCache(inp["K"], inp["V"], w.seq_lens, H_q=w.H_q,
                                 bits=w.bits, group=w.group,
                                 residual=w.residual,
-                                max_seq=w.max_seq + n_app + 8, n_sink=n_sink))
+                                max_seq=w.max_seq + n_app + 8, n_sink=n_sink,
+                                kitty_hi=kitty_hi))
     # prefill and append are timed over at least 8 caches; the decode
     # rotates over the first ncp
     na = max(ncp, 8)
@@ -587,7 +594,14 @@ def measure_workload(w, peak, full=True, n_sink=0):
     flushed = _ev_times(lambda i: caches[i % ncp].decode_attend(q, out), 100)
     caches[0].device_status()
     # KIVI-Sink: the fp16 rows of the sinks of the quantized region
-    nb += caches[0].cache_bytes()["sink_bytes"]
+    cb = caches[0].cache_bytes()
+    nb += cb["sink_bytes"]
+    if kitty_hi is not None:
+        # Kitty: mixed-width key rows + key scale/zero + channel masks, fp16
+        # values and residual window, q and out
+        gq = w.H_q // w.H_kv
+        nb = (cb["code_bytes"] + cb["meta_bytes"] + cb["value_fp16_bytes"] +
+              cb["residual_bytes"] + w.B * w.H_q * w.D * (2 + 4))
     ab = (append_bytes(w, n_app) if not w.n_append
           else flush_append_bytes(w, n_app))
     res = {

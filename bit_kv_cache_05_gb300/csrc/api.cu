@@ -137,9 +137,9 @@ int vq_kivi_quantize_ex(const vq_kivi_params *p, const vq_kivi_options *opt,
   if (o.n_sink < 0 || o.n_sink > kMaxSink)
     return fail(VQ_ERR_ARG, "n_sink=%d outside [0, %d]", o.n_sink, kMaxSink);
   if (o.kitty) {
-    if (p->bits != 2 || o.n_sink != 0 || p->D % 32 != 0)
-      return fail(VQ_ERR_UNSUPPORTED, "Kitty needs bits=2, n_sink=0 and D a "
-                  "multiple of 32");
+    if (p->bits != 2 || o.n_sink != 0 || (p->D != 64 && p->D != 128))
+      return fail(VQ_ERR_UNSUPPORTED, "Kitty needs bits=2, n_sink=0 and D = 64 "
+                  "or 128");
     if (o.kitty_hi < 0 || o.kitty_hi > p->D || o.kitty_hi % 16 != 0)
       return fail(VQ_ERR_ARG, "kitty_hi=%d: a multiple of 16 in [0, D=%d]",
                   o.kitty_hi, p->D);
@@ -432,7 +432,9 @@ int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
   int32_t tps = c->split_tokens;
   const int32_t unit = split_unit(p.group);
   if (tps == 0) {
-    const int64_t target_items = 4LL * c->sm_count;
+    // Kitty streams fp16 values: more, shorter items keep more loads in
+    // flight per SM
+    const int64_t target_items = (c->geo.kitty ? 16LL : 4LL) * c->sm_count;
     int64_t t = (total_tq * p.H_kv + target_items - 1) / target_items;
     tps = (int32_t)round_up((size_t)(t > 1 ? t : 1), unit);
   }

@@ -121,7 +121,7 @@ typedef struct vq_kivi_options {
    * of quantized tokens are kept in fp16.  A key row holds (D + kitty_hi)/4
    * bytes: the 4-bit channels' codes in ascending channel order, LSB
    * first, then the 2-bit channels'.  Requires bits = 2, n_sink = 0,
-   * kitty_hi a multiple of 16 in [0, D], max_seq <= 2^20.  The pages'
+   * D = 64 or 128, kitty_hi a multiple of 16 in [0, D], max_seq <= 2^20.  The pages'
    * default is kitty_hi = D / 4.  Decode runs on the CUDA cores;
    * vq_kivi_attend_multi and vq_kivi_dequantize do not serve Kitty caches
    * (VQ_ERR_UNSUPPORTED). */
