@@ -33,7 +33,7 @@ _lock = threading.Lock()
 _lib = None
 
 PLANES = ("Kc", "Ks", "Kz", "Vc", "Vs", "Vz", "Kr", "Vr",
-          "sink_pos", "sink_k", "sink_v", "Kmask", "Vf")
+          "sink_pos", "sink_k", "sink_v", "Kmask", "Vf", "tier")
 
 
 def build(force: bool = False) -> str:
@@ -63,6 +63,7 @@ def _load():
         lib.orc_free.argtypes = [P]
         lib.orc_set_sinks.argtypes = [P, i32]
         lib.orc_set_kitty.argtypes = [P, i32]
+        lib.orc_set_age.argtypes = [P, i32, i32, i32, i32, i32]
         lib.orc_quantize.argtypes = [P, P, P, i64, P]
         lib.orc_append.argtypes = [P, P, P, i64, P]
         lib.orc_attend.argtypes = [P, P, f64, P]
@@ -145,7 +146,7 @@ class OracleCache:
     """
 
     def __init__(self, B, H_q, H_kv, D, bits, group, residual, max_seq,
-                 n_sink=0, kitty_hi=None):
+                 n_sink=0, kitty_hi=None, age=None):
         self.B, self.H_q, self.H_kv, self.D = B, H_q, H_kv, D
         self.bits, self.group, self.residual, self.max_seq = (
             bits, group, residual, max_seq)
@@ -160,6 +161,10 @@ class OracleCache:
         self.kitty_hi = kitty_hi
         if kitty_hi is not None and self._lib.orc_set_kitty(self._c, kitty_hi) != 0:
             raise ValueError("oracle: bad Kitty parameters")
+        # AgeTieredKV: (boundary 1, boundary 2, bits of the three tiers)
+        self.age = age
+        if age is not None and self._lib.orc_set_age(self._c, *age) != 0:
+            raise ValueError("oracle: bad AgeTieredKV parameters")
         tcap = np.zeros(1, np.int32)
         rcap = np.zeros(1, np.int32)
         self._lib.orc_dims(self._c, _ptr(tcap), _ptr(rcap))
@@ -242,6 +247,8 @@ class OracleCache:
             return raw.view(np.uint32).reshape(B, H, self.Tcap // g, D // 32)
         if name == "Vf":
             return raw.view(np.float16).reshape(B, H, self.Tcap, D)
+        if name == "tier":
+            return raw.view(np.int8).reshape(B, H, self.Tcap // g)
         if name in ("Kc", "Vc"):
             return raw.reshape(B, H, self.Tcap, row)
         if name in ("Ks", "Kz"):

@@ -146,6 +146,13 @@ typedef struct orc_cache {
   uint16_t *Vf;            /* [B][Hkv][Tcap][D] fp16 values */
   int64_t *ksum;           /* [B][Hkv][D] */
   unsigned __int128 *ksq;  /* [B][Hkv][D] */
+  /* AgeTieredKV (tier == NULL: off): a quantized group's width follows its
+   * age, counted from its newest token: age < age_b1 -> age_bits[0], age <
+   * age_b2 -> age_bits[1], else age_bits[2].  Codes sit in the first
+   * D * bits / 8 bytes of a D-byte row (the rest zero); tier[] is each
+   * group's current tier. */
+  int age_b1, age_b2, age_bits[3];
+  int8_t *tier;            /* [B][Hkv][Tcap/g] */
 } orc_cache;
 
 static int n_quantized(int S, int R, int g) {
@@ -198,8 +205,107 @@ void orc_free(orc_cache *c) {
   free(c->Kc); free(c->Vc); free(c->Ks); free(c->Kz); free(c->Vs);
   free(c->Vz); free(c->Kr); free(c->Vr); free(c->S); free(c->Tq);
   free(c->nres); free(c->sink_pos); free(c->sink_k); free(c->sink_v);
-  free(c->Kmask); free(c->Vf); free(c->ksum); free(c->ksq);
+  free(c->Kmask); free(c->Vf); free(c->ksum); free(c->ksq); free(c->tier);
   free(c);
+}
+
+/* AgeTieredKV (method overview, AgeTieredKV entry): three tiers of the
+ * shared min/max group quantizer chosen by token age against two
+ * boundaries.  Call on a fresh cache of bits = 8 (its rows hold the widest
+ * tier) before orc_quantize.  0 < b1 < b2, multiples of g; widths from
+ * {2, 4, 8}, non-increasing.  Returns 0, or -1. */
+int orc_set_age(orc_cache *c, int b1, int b2, int bits0, int bits1, int bits2) {
+  const int ok_bits[3] = {bits0, bits1, bits2};
+  if (c->bits != 8 || c->n_sink || c->Kmask || c->tier) return -1;
+  if (b1 <= 0 || b2 <= b1 || b1 % c->g || b2 % c->g) return -1;
+  for (int i = 0; i < 3; ++i) {
+    if (ok_bits[i] != 2 && ok_bits[i] != 4 && ok_bits[i] != 8) return -1;
+    if (i && ok_bits[i] > ok_bits[i - 1]) return -1;
+    c->age_bits[i] = ok_bits[i];
+  }
+  c->age_b1 = b1;
+  c->age_b2 = b2;
+  c->tier = (int8_t *)calloc((size_t)c->B * c->Hkv * (c->Tcap / c->g), 1);
+  return c->tier ? 0 : -1;
+}
+
+static int age_tier(const orc_cache *c, int S, int G) {
+  const int age = S - (G + 1) * c->g; /* tokens newer than the group's last */
+  return age < c->age_b1 ? 0 : (age < c->age_b2 ? 1 : 2);
+}
+
+/* codes of a row at width w (LSB-first, D * w / 8 bytes), rest zero */
+static void age_put_row(uint8_t *row, const uint8_t *codes, int D, int w) {
+  memset(row, 0, (size_t)D);
+  orc_pack_codes(codes, D, w, row);
+}
+
+/* Move group G of (b, h) one tier down: rebuild its keys and values in fp32
+ * (code * scale rounded, then + zero rounded) and quantize them again at
+ * the next tier's width with the same group quantizer. */
+static void age_demote(orc_cache *c, int b, int h, int G) {
+  const int D = c->D, g = c->g;
+  size_t bh = (size_t)b * c->Hkv + h;
+  int8_t *tr = c->tier + bh * (c->Tcap / g) + G;
+  const int wf = c->age_bits[*tr], wt = c->age_bits[*tr + 1];
+  float *x = (float *)malloc(sizeof(float) * (size_t)g * D);
+  uint8_t *codes = (uint8_t *)malloc((size_t)g * D);
+  uint8_t row[4096];
+  /* keys, per channel */
+  for (int i = 0; i < g; ++i) {
+    const uint8_t *r = c->Kc + (bh * c->Tcap + (size_t)G * g + i) * c->row;
+    orc_unpack_codes(r, D, wf, row);
+    for (int ch = 0; ch < D; ++ch) {
+      float sc = h2f(c->Ks[(bh * (c->Tcap / g) + G) * D + ch]);
+      float z = h2f(c->Kz[(bh * (c->Tcap / g) + G) * D + ch]);
+      float prod = (float)row[ch] * sc;
+      x[(size_t)i * D + ch] = prod + z;
+    }
+  }
+  for (int ch = 0; ch < D; ++ch) {
+    uint16_t s16, z16;
+    quant_group(x + ch, D, g, wt, codes + ch, D, NULL, &s16, &z16);
+    c->Ks[(bh * (c->Tcap / g) + G) * D + ch] = s16;
+    c->Kz[(bh * (c->Tcap / g) + G) * D + ch] = z16;
+  }
+  for (int i = 0; i < g; ++i)
+    age_put_row(c->Kc + (bh * c->Tcap + (size_t)G * g + i) * c->row,
+                codes + (size_t)i * D, D, wt);
+  /* values, per token over groups of g channels */
+  for (int i = 0; i < g; ++i) {
+    size_t t = (size_t)G * g + i;
+    uint8_t *r = c->Vc + (bh * c->Tcap + t) * c->row;
+    orc_unpack_codes(r, D, wf, row);
+    float xv[4096];
+    uint8_t cv[4096];
+    for (int ch = 0; ch < D; ++ch) {
+      float sc = h2f(c->Vs[(bh * c->Tcap + t) * (D / g) + ch / g]);
+      float z = h2f(c->Vz[(bh * c->Tcap + t) * (D / g) + ch / g]);
+      float prod = (float)row[ch] * sc;
+      xv[ch] = prod + z;
+    }
+    for (int j = 0; j < D / g; ++j) {
+      uint16_t s16, z16;
+      quant_group(xv + j * g, 1, g, wt, cv + j * g, 1, NULL, &s16, &z16);
+      c->Vs[(bh * c->Tcap + t) * (D / g) + j] = s16;
+      c->Vz[(bh * c->Tcap + t) * (D / g) + j] = z16;
+    }
+    age_put_row(r, cv, D, wt);
+  }
+  *tr += 1;
+  free(x);
+  free(codes);
+}
+
+/* after a change of length: every group of b demoted to its age's tier */
+static void age_update(orc_cache *c, int b) {
+  if (!c->tier) return;
+  for (int h = 0; h < c->Hkv; ++h)
+    for (int G = 0; G < c->Tq[b] / c->g; ++G) {
+      const int want = age_tier(c, c->S[b], G);
+      while (c->tier[((size_t)b * c->Hkv + h) * (c->Tcap / c->g) + G] < want)
+        age_demote(c, b, h, G);
+    }
 }
 
 /* Kitty (changelog v0.11.0 "New"): channel-wise mixed-precision keys.  For
@@ -387,6 +493,45 @@ static void quantize_group_of_tokens(orc_cache *c, int b, int h, int G,
   }
   float *x = (float *)malloc(sizeof(float) * (size_t)g * D);
   uint8_t *codes = (uint8_t *)malloc((size_t)g * D);
+  if (c->tier) {
+    /* AgeTieredKV: a new group enters at the top tier */
+    const int w = c->age_bits[0];
+    uint8_t *codes2 = (uint8_t *)malloc((size_t)g * D);
+    float *xk = (float *)malloc(sizeof(float) * (size_t)g * D);
+    for (int i = 0; i < g; ++i) {
+      const uint16_t *r = krow(ctx, i);
+      for (int ch = 0; ch < D; ++ch) xk[(size_t)i * D + ch] = h2f(r[ch]);
+    }
+    for (int ch = 0; ch < D; ++ch) {
+      uint16_t s16, z16;
+      quant_group(xk + ch, D, g, w, codes2 + ch, D, NULL, &s16, &z16);
+      c->Ks[(bh * (c->Tcap / g) + G) * D + ch] = s16;
+      c->Kz[(bh * (c->Tcap / g) + G) * D + ch] = z16;
+    }
+    for (int i = 0; i < g; ++i)
+      age_put_row(c->Kc + (bh * c->Tcap + (size_t)G * g + i) * c->row,
+                  codes2 + (size_t)i * D, D, w);
+    for (int i = 0; i < g; ++i) {
+      const uint16_t *r = vrow(ctx, i);
+      size_t t = (size_t)G * g + i;
+      float xv[4096];
+      uint8_t cv[4096];
+      for (int ch = 0; ch < D; ++ch) xv[ch] = h2f(r[ch]);
+      for (int j = 0; j < D / g; ++j) {
+        uint16_t s16, z16;
+        quant_group(xv + j * g, 1, g, w, cv + j * g, 1, NULL, &s16, &z16);
+        c->Vs[(bh * c->Tcap + t) * (D / g) + j] = s16;
+        c->Vz[(bh * c->Tcap + t) * (D / g) + j] = z16;
+      }
+      age_put_row(c->Vc + (bh * c->Tcap + t) * c->row, cv, D, w);
+    }
+    c->tier[bh * (c->Tcap / g) + G] = 0;
+    free(codes2);
+    free(xk);
+    free(x);
+    free(codes);
+    return;
+  }
   /* sink tokens of this group (KIVI-Sink): left out of every min/max,
    * their codes 0 and their own value groups empty */
   char sink[4096];
@@ -501,6 +646,7 @@ int orc_quantize(orc_cache *c, const uint16_t *K, const uint16_t *V,
                V + off + (size_t)(Tq + i) * c->D, 2 * (size_t)c->D);
       }
     }
+    age_update(c, b);
   }
   return 0;
 }
@@ -553,6 +699,7 @@ int orc_append(orc_cache *c, const uint16_t *Kn, const uint16_t *Vn,
       free(ks);
       free(vs);
     }
+    age_update(c, b);
   }
   return 0;
 }
@@ -599,13 +746,14 @@ static void token_hat(const orc_cache *c, int b, int h, int t, double *k,
   if (t < c->Tq[b]) {
     uint8_t codes[4096];
     int G = t / g;
-    orc_unpack_codes(c->Kc + (bh * c->Tcap + t) * c->row, D, c->bits, codes);
+    const int w = c->tier ? c->age_bits[c->tier[bh * (c->Tcap / g) + G]] : c->bits;
+    orc_unpack_codes(c->Kc + (bh * c->Tcap + t) * c->row, D, w, codes);
     for (int ch = 0; ch < D; ++ch) {
       double s = h2f(c->Ks[(bh * (c->Tcap / g) + G) * D + ch]);
       double z = h2f(c->Kz[(bh * (c->Tcap / g) + G) * D + ch]);
       k[ch] = (double)codes[ch] * s + z;
     }
-    orc_unpack_codes(c->Vc + (bh * c->Tcap + t) * c->row, D, c->bits, codes);
+    orc_unpack_codes(c->Vc + (bh * c->Tcap + t) * c->row, D, w, codes);
     for (int ch = 0; ch < D; ++ch) {
       double s = h2f(c->Vs[(bh * c->Tcap + t) * (D / g) + ch / g]);
       double z = h2f(c->Vz[(bh * c->Tcap + t) * (D / g) + ch / g]);
@@ -749,6 +897,7 @@ size_t orc_plane_bytes(const orc_cache *c, int which) {
     case 8: return bh * c->n_sink * 4;
     case 9: case 10: return bh * c->n_sink * c->D * 2;
     case 11: return c->Kmask ? bh * (c->Tcap / c->g) * (c->D / 32) * 4 : 0;
+    case 13: return c->tier ? bh * (c->Tcap / c->g) : 0;
     case 12: return c->Vf ? bh * c->Tcap * c->D * 2 : 0;
     default: return 0;
   }
@@ -770,6 +919,7 @@ int orc_get_plane(const orc_cache *c, int which, void *dst) {
     case 10: src = c->sink_v; break;
     case 11: src = c->Kmask; break;
     case 12: src = c->Vf; break;
+    case 13: src = c->tier; break;
     default: return -1;
   }
   if (!src) return orc_plane_bytes(c, which) == 0 ? 0 : -1;

@@ -931,3 +931,183 @@ def test_kitty_attention_brute_force(oracle_mod):
             refm = np_causal_attention(q3[b, hq].astype(np.longdouble), k, v,
                                        np.longdouble(0.3), lens[b])
             assert np.abs(outm[b, hq] - refm.astype(np.float64)).max() <= 1e-6
+
+
+# ---------------------------------------------------------------------------
+# AgeTieredKV: three widths by token age (method overview, AgeTieredKV)
+# ---------------------------------------------------------------------------
+
+def np_age_hat(oc, b, h):
+    """k_hat, v_hat [Tq][D] in long double from the age-tiered planes: each
+    group's codes at its tier's width in the leading bytes of a D-byte
+    row."""
+    _, Tq, _ = oc.lengths()
+    D, g = oc.D, oc.group
+    b1, b2, *widths = oc.age
+    tiers = oc.plane("tier")[b, h]
+    k = np.zeros((Tq[b], D), np.longdouble)
+    v = np.zeros((Tq[b], D), np.longdouble)
+    Ks = oc.plane("Ks")[b, h].astype(np.longdouble)
+    Kz = oc.plane("Kz")[b, h].astype(np.longdouble)
+    Vs = oc.plane("Vs")[b, h].astype(np.longdouble)
+    Vz = oc.plane("Vz")[b, h].astype(np.longdouble)
+    for G in range(Tq[b] // g):
+        w = widths[tiers[G]]
+        rows = slice(G * g, (G + 1) * g)
+        kc = np_unpack_rows(oc.plane("Kc")[b, h, rows, : D * w // 8], D, w)
+        vc = np_unpack_rows(oc.plane("Vc")[b, h, rows, : D * w // 8], D, w)
+        k[rows] = kc * Ks[G] + Kz[G]
+        v[rows] = vc * Vs[rows][:, np.arange(D) // g] + Vz[rows][:, np.arange(D) // g]
+    return k, v
+
+
+def _age(oracle_mod, age, K, V, lens, Hq=None, g=8, R=0):
+    from oracle import OracleCache
+    B, H, S_max, D = K.shape
+    oc = OracleCache(B, Hq or H, H, D, 8, g, R, S_max, age=age)
+    oc.quantize(K, V, lens)
+    return oc
+
+
+def test_age_tiers_follow_the_age_rule(oracle_mod):
+    """A group's tier: 0 while fewer than b1 tokens are newer than its last
+    token, 1 while fewer than b2, else 2."""
+    rng = np.random.default_rng(50)
+    B, H, D, g = 2, 1, 16, 8
+    lens = [123, 60]
+    K = rand_f16(rng, (B, H, 128, D))
+    V = rand_f16(rng, (B, H, 128, D))
+    oc = _age(oracle_mod, (16, 48, 8, 4, 2), K, V, lens, g=g)
+    _, Tq, _ = oc.lengths()
+    for b in range(B):
+        for G in range(Tq[b] // g):
+            age = lens[b] - (G + 1) * g
+            want = 0 if age < 16 else (1 if age < 48 else 2)
+            assert oc.plane("tier")[b, 0, G] == want, (b, G)
+
+
+@pytest.mark.parametrize("w", [8, 4, 2])
+def test_age_without_demotion_is_kivi(oracle_mod, w):
+    """While no group is old enough to move (boundaries beyond the
+    sequence), the age-tiered cache holds plain KIVI codes at the top
+    tier's width, scales and zeros bit for bit."""
+    from oracle import OracleCache
+    rng = np.random.default_rng(51)
+    B, H, D, g, R = 2, 2, 16, 8, 4
+    lens = [70, 33]
+    K = rand_f16(rng, (B, H, 72, D), 2.0)
+    V = rand_f16(rng, (B, H, 72, D))
+    oa = _age(oracle_mod, (1024, 2048, w, 2, 2), K, V, lens, g=g, R=R)
+    ok = OracleCache(B, H, H, D, w, g, R, 72)
+    ok.quantize(K, V, lens)
+    _, Tq, _ = ok.lengths()
+    for b in range(B):
+        T = Tq[b]
+        assert np.array_equal(oa.plane("Kc")[b, :, :T, : D * w // 8], ok.plane("Kc")[b, :, :T])
+        assert np.array_equal(oa.plane("Vc")[b, :, :T, : D * w // 8], ok.plane("Vc")[b, :, :T])
+        assert (oa.plane("Kc")[b, :, :T, D * w // 8:] == 0).all()
+        for name in ("Ks", "Kz"):
+            assert np.array_equal(oa.plane(name)[b, :, : T // g].view(np.uint16),
+                                  ok.plane(name)[b, :, : T // g].view(np.uint16))
+        for name in ("Vs", "Vz"):
+            assert np.array_equal(oa.plane(name)[b, :, :T].view(np.uint16),
+                                  ok.plane(name)[b, :, :T].view(np.uint16))
+
+
+def test_age_demotion_requantizes_the_rebuilt_values(oracle_mod):
+    """A group that moved 8 -> 4 bits holds the group quantizer's result on
+    its 8-bit values rebuilt in fp32 (code * scale rounded, then + zero
+    rounded), the keys per channel and the values per token: checked against
+    an independent numpy rebuild and the (pinned) quantizer."""
+    rng = np.random.default_rng(52)
+    B, H, D, g = 1, 1, 16, 8
+    S = 40
+    K = rand_f16(rng, (B, H, S, D), 3.0)
+    V = rand_f16(rng, (B, H, S, D))
+    o8 = _age(oracle_mod, (1024, 2048, 8, 4, 2), K, V, [S], g=g)   # no demotion
+    o4 = _age(oracle_mod, (8, 2048, 8, 4, 2), K, V, [S], g=g)      # groups 0..3 -> 4 bits
+    assert o4.plane("tier")[0, 0].tolist()[:5] == [1, 1, 1, 1, 0]
+    f32 = np.float32
+    for G in range(4):
+        rows = slice(G * g, (G + 1) * g)
+        kc8 = np_unpack_rows(o8.plane("Kc")[0, 0, rows], D, 8).astype(f32)
+        ks8 = o8.plane("Ks")[0, 0, G].astype(f32)
+        kz8 = o8.plane("Kz")[0, 0, G].astype(f32)
+        xk = (kc8 * ks8).astype(f32) + kz8                       # two roundings
+        kc4 = np_unpack_rows(o4.plane("Kc")[0, 0, rows, : D // 2], D, 4)
+        for ch in range(D):
+            codes, _, s16, z16 = oracle_mod.quant_group(xk[:, ch].astype(f32), 4)
+            assert kc4[:, ch].tolist() == codes.tolist()
+            assert o4.plane("Ks")[0, 0, G, ch].view(np.uint16) == s16
+            assert o4.plane("Kz")[0, 0, G, ch].view(np.uint16) == z16
+        vc8 = np_unpack_rows(o8.plane("Vc")[0, 0, rows], D, 8).astype(f32)
+        vs8 = o8.plane("Vs")[0, 0, rows].astype(f32)[:, np.arange(D) // g]
+        vz8 = o8.plane("Vz")[0, 0, rows].astype(f32)[:, np.arange(D) // g]
+        xv = (vc8 * vs8).astype(f32) + vz8
+        vc4 = np_unpack_rows(o4.plane("Vc")[0, 0, rows, : D // 2], D, 4)
+        for i in range(g):
+            for j in range(D // g):
+                codes, _, s16, _ = oracle_mod.quant_group(xv[i, j * g:(j + 1) * g], 4)
+                assert vc4[i, j * g:(j + 1) * g].tolist() == codes.tolist()
+                assert o4.plane("Vs")[0, 0, G * g + i, j].view(np.uint16) == s16
+
+
+def test_age_prefill_equals_appends(oracle_mod):
+    """A group always passes the tiers in order, one at a time, so a prefill
+    and any chunking of appends reach the same cache, bit for bit."""
+    from oracle import OracleCache
+    rng = np.random.default_rng(53)
+    B, H, D, g, R = 2, 1, 16, 8, 3
+    S_final = [150, 61]
+    K = rand_f16(rng, (B, H, 152, D), 2.0)
+    V = rand_f16(rng, (B, H, 152, D))
+    age = (16, 64, 8, 4, 2)
+    ref = _age(oracle_mod, age, K, V, S_final, g=g, R=R)
+    oc = OracleCache(B, H, H, D, 8, g, R, 152, age=age)
+    oc.quantize(K, V, [2, 2])
+    cur = [2, 2]
+    step = 0
+    while cur != S_final:
+        n = [min([1, 13, 40, 5][(step + b) % 4], S_final[b] - cur[b]) for b in range(B)]
+        Kn = np.zeros((B, H, max(n), D), np.float16)
+        Vn = np.zeros_like(Kn)
+        for b in range(B):
+            Kn[b, :, :n[b]] = K[b, :, cur[b]:cur[b] + n[b]]
+            Vn[b, :, :n[b]] = V[b, :, cur[b]:cur[b] + n[b]]
+        oc.append(Kn, Vn, n)
+        cur = [c + x for c, x in zip(cur, n)]
+        step += 1
+    _, Tq, _ = ref.lengths()
+    for b in range(B):
+        T = Tq[b]
+        for name, n in (("Kc", T), ("Vc", T), ("Ks", T // g), ("Kz", T // g),
+                        ("Vs", T), ("Vz", T), ("tier", T // g)):
+            assert np.array_equal(oc.plane(name)[b, :, :n].view(np.uint8),
+                                  ref.plane(name)[b, :, :n].view(np.uint8)), name
+
+
+def test_age_attention_brute_force_and_error_grows_with_age(oracle_mod):
+    """Attention over k_hat / v_hat rebuilt at each group's width (long
+    double) equals the oracle to 1e-12; and old (2-bit) groups reconstruct
+    the inputs with a larger error than recent (8-bit) ones."""
+    rng = np.random.default_rng(54)
+    B, Hq, H, D, g, R = 1, 2, 1, 16, 8, 0
+    S = 200
+    K = rand_f16(rng, (B, H, S, D))
+    V = rand_f16(rng, (B, H, S, D))
+    oc = _age(oracle_mod, (32, 96, 8, 4, 2), K, V, [S], Hq=Hq, g=g, R=R)
+    q = rand_f16(rng, (B, Hq, D))
+    k, v = np_age_hat(oc, 0, 0)
+    _, Tq, nres = oc.lengths()
+    kr = oc.plane("Kr")[0, 0, :nres[0]].astype(np.longdouble)
+    vr = oc.plane("Vr")[0, 0, :nres[0]].astype(np.longdouble)
+    kk = np.concatenate([k, kr])
+    vv = np.concatenate([v, vr])
+    for hq in range(Hq):
+        ref = np_dense_attention(q[0, hq].astype(np.longdouble), kk, vv, np.longdouble(0.25))
+        assert np.abs(oc.attend_one(0, hq, q[0, hq], 0.25) - ref.astype(np.float64)).max() <= 1e-12
+    tiers = oc.plane("tier")[0, 0, : Tq[0] // g]
+    err = np.abs(k.astype(np.float64) - K[0, 0, : Tq[0]].astype(np.float64))
+    per_group = err.reshape(-1, g, D).mean(axis=(1, 2))
+    assert per_group[tiers == 2].mean() > 4 * per_group[tiers == 0].mean()
+    assert {0, 1, 2} <= set(tiers.tolist())
