@@ -53,7 +53,9 @@ class Planes(ctypes.Structure):
 
 class Options(ctypes.Structure):
     _fields_ = [("n_sink", ctypes.c_int32), ("kitty", ctypes.c_int32),
-                ("kitty_hi", ctypes.c_int32)]
+                ("kitty_hi", ctypes.c_int32), ("age_recent", ctypes.c_int32),
+                ("age_mid", ctypes.c_int32), ("age_bits_recent", ctypes.c_int32),
+                ("age_bits_mid", ctypes.c_int32), ("age_bits_old", ctypes.c_int32)]
 
 
 class Bytes(ctypes.Structure):

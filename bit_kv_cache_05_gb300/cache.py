@@ -15,7 +15,7 @@ import torch
 from . import _lib
 
 PLANES = ("Kc", "Ks", "Kz", "Vc", "Vs", "Vz", "Kr", "Vr",
-          "sink_pos", "sink_k", "sink_v", "Kmask", "Vf")
+          "sink_pos", "sink_k", "sink_v", "Kmask", "Vf", "tier")
 
 
 def _stream_handle(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
@@ -47,7 +47,7 @@ class KiviCache:
     def __init__(self, K: torch.Tensor, V: torch.Tensor, seq_lens, *, H_q: int,
                  bits: int, group: int, residual: int,
                  max_seq: Optional[int] = None, n_sink: int = 0,
-                 kitty_hi: Optional[int] = None,
+                 kitty_hi: Optional[int] = None, age=None,
                  stream: Optional[torch.cuda.Stream] = None):
         L = _lib.load()
         if K.shape != V.shape or K.dim() != 4:
@@ -66,8 +66,11 @@ class KiviCache:
         vp = _dev_ptr(V, torch.float16, "V")
         self.n_sink = int(n_sink)
         self.kitty_hi = kitty_hi
+        # age: (recent boundary, mid boundary, bits recent, mid, old)
+        self.age = tuple(age) if age is not None else None
         opts = _lib.Options(self.n_sink, 0 if kitty_hi is None else 1,
-                            0 if kitty_hi is None else int(kitty_hi))
+                            0 if kitty_hi is None else int(kitty_hi),
+                            *(self.age if self.age else (0, 0, 0, 0, 0)))
         _lib.check(L.vq_kivi_quantize_ex(ctypes.byref(self.params),
                                          ctypes.byref(opts), kp, vp,
                                          S_stride, _i32_array(lens),
@@ -147,6 +150,8 @@ class KiviCache:
             return raw.view(torch.int32).view(B, H, -1, D // 32)
         if name == "Vf":
             return raw.view(torch.float16).view(B, H, -1, D)
+        if name == "tier":
+            return raw.view(torch.int8).view(B, H, -1)
         if name == "sink_pos":
             return raw.view(torch.int32).view(B, H, self.n_sink)
         if name in ("sink_k", "sink_v"):

@@ -1,6 +1,7 @@
 // C ABI of the KIVI cache: argument checks, the cache handle, device memory
 // and the launch sequence of each call.  See include/vq_kivi.h.
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -133,7 +134,7 @@ int vq_kivi_quantize_ex(const vq_kivi_params *p, const vq_kivi_options *opt,
                         vq_kivi_cache **out) {
   int rc = check_params(p);
   if (rc) return rc;
-  const vq_kivi_options o = opt ? *opt : vq_kivi_options{0, 0, 0};
+  const vq_kivi_options o = opt ? *opt : vq_kivi_options{0, 0, 0, 0, 0, 0, 0, 0};
   if (o.n_sink < 0 || o.n_sink > kMaxSink)
     return fail(VQ_ERR_ARG, "n_sink=%d outside [0, %d]", o.n_sink, kMaxSink);
   if (o.kitty) {
@@ -145,6 +146,19 @@ int vq_kivi_quantize_ex(const vq_kivi_params *p, const vq_kivi_options *opt,
                   o.kitty_hi, p->D);
     if (p->max_seq > (1 << 20))
       return fail(VQ_ERR_UNSUPPORTED, "Kitty: max_seq=%d > 2^20", p->max_seq);
+  }
+  if (o.age_recent > 0) {
+    if (p->bits != 8 || o.n_sink != 0 || o.kitty || (p->D != 64 && p->D != 128))
+      return fail(VQ_ERR_UNSUPPORTED, "AgeTieredKV needs bits=8 (the row "
+                  "capacity), no sinks, no Kitty and D = 64 or 128");
+    const int wb[3] = {o.age_bits_recent, o.age_bits_mid, o.age_bits_old};
+    for (int i = 0; i < 3; ++i)
+      if ((wb[i] != 2 && wb[i] != 4 && wb[i] != 8) || (i && wb[i] > wb[i - 1]))
+        return fail(VQ_ERR_ARG, "AgeTieredKV widths %d/%d/%d: each of 2, 4, 8, "
+                    "non-increasing", wb[0], wb[1], wb[2]);
+    if (o.age_mid <= o.age_recent || o.age_recent % p->group || o.age_mid % p->group)
+      return fail(VQ_ERR_ARG, "AgeTieredKV boundaries %d < %d, multiples of g=%d",
+                  o.age_recent, o.age_mid, p->group);
   }
   if (!out) return fail(VQ_ERR_ARG, "out is NULL");
   if (!seq_lens) return fail(VQ_ERR_ARG, "seq_lens is NULL");
@@ -189,6 +203,14 @@ int vq_kivi_quantize_ex(const vq_kivi_params *p, const vq_kivi_options *opt,
   geo.n_sink = o.n_sink;
   geo.kitty = o.kitty ? 1 : 0;
   geo.kitty_hi = o.kitty ? o.kitty_hi : 0;
+  if (o.age_recent > 0) {
+    geo.age_b1 = o.age_recent;
+    geo.age_b2 = o.age_mid;
+    geo.age_bits[0] = o.age_bits_recent;
+    geo.age_bits[1] = o.age_bits_mid;
+    geo.age_bits[2] = o.age_bits_old;
+  }
+  const bool aged = geo.age_b1 > 0;
   const int32_t unit = split_unit(g);
   const int32_t tps_for_cap = (int32_t)round_up((geo.Tcap + 1023) / 1024, unit);
   c->tps_min = tps_for_cap > 256 ? tps_for_cap : 256;
@@ -204,7 +226,7 @@ int vq_kivi_quantize_ex(const vq_kivi_params *p, const vq_kivi_options *opt,
   const size_t sz_vmeta = kitty ? 0 : BH * geo.Tcap * (p->D / g) * sizeof(__half);
   const size_t sz_res = BH * geo.Rcap * p->D * sizeof(__half);
   // Kitty: the CUDA-core decode over mixed-width key rows
-  c->use_mma = !kitty && mma_plan(geo, c->sm_count, &c->plan);
+  c->use_mma = !kitty && !aged && mma_plan(geo, c->sm_count, &c->plan);
   // 2- and 4-bit caches decoded on the tensor cores keep their codes in the
   // order the MMA fragments consume them
   geo.layout = c->use_mma && (p->bits == 2 || p->bits == 4) ? kLayoutFrag : kLayoutPacked;
@@ -234,6 +256,7 @@ int vq_kivi_quantize_ex(const vq_kivi_params *p, const vq_kivi_options *opt,
   size_t o_vf = off; off += round_up(kitty ? BH * geo.Tcap * p->D * sizeof(__half) : 0, A);
   size_t o_ksum = off; off += round_up(kitty ? BH * p->D * 8 : 0, A);
   size_t o_ksq = off; off += round_up(kitty ? BH * p->D * 16 : 0, A);
+  size_t o_tier = off; off += round_up(aged ? BH * (geo.Tcap / g) : 0, A);
   c->block_bytes = off;
 
   e = cudaMallocAsync(&c->block, c->block_bytes, st);
@@ -261,6 +284,7 @@ int vq_kivi_quantize_ex(const vq_kivi_params *p, const vq_kivi_options *opt,
     pl.sink_k = (__half *)(base + o_sk);
     pl.sink_v = (__half *)(base + o_sv);
   }
+  if (aged) pl.tier = (int8_t *)(base + o_tier);
   if (kitty) {
     pl.kmask = (uint32_t *)(base + o_kmask);
     pl.Vf = (__half *)(base + o_vf);
@@ -303,10 +327,25 @@ int vq_kivi_quantize_ex(const vq_kivi_params *p, const vq_kivi_options *opt,
                           sk, st);
     if (e != cudaSuccess) return abort_create(e, "sink selection launch");
   }
-  e = kitty ? launch_flush_kitty(geo, pl, (const __half *)K, (const __half *)V,
-                                 s_stride, ft, ft.prefix[p->B], st)
-            : launch_flush(geo, pl, (const __half *)K, (const __half *)V, s_stride, ft,
-                           ft.prefix[p->B], st);
+  if (aged) {
+    AgeTable at;
+    at.prefix[0] = 0;
+    for (int b = 0; b < p->B; ++b) {
+      at.gn0[b] = 0;
+      at.gn1[b] = c->Tq[b] / g;
+      at.gd0[b] = at.gd1[b] = 0;
+      at.src_split[b] = 0;
+      at.S_old[b] = 0;
+      at.S_new[b] = c->S[b];
+      at.prefix[b + 1] = at.prefix[b] + at.gn1[b];
+    }
+    e = launch_age_flush(geo, pl, (const __half *)K, (const __half *)V, s_stride, at, st);
+  } else {
+    e = kitty ? launch_flush_kitty(geo, pl, (const __half *)K, (const __half *)V,
+                                   s_stride, ft, ft.prefix[p->B], st)
+              : launch_flush(geo, pl, (const __half *)K, (const __half *)V, s_stride, ft,
+                             ft.prefix[p->B], st);
+  }
   if (e != cudaSuccess) return abort_create(e, "quantize kernel launch");
   e = launch_tail(geo, pl, (const __half *)K, (const __half *)V, s_stride, tt,
                   tt.prefix[p->B], st);
@@ -356,12 +395,43 @@ int vq_kivi_append(vq_kivi_cache *c, const void *K_new, const void *V_new,
     tt.row0[b] = keep0 - S_old;
     tt.pos0[b] = keep0;
   }
-  cudaError_t e = c->geo.kitty
-      ? launch_flush_kitty(c->geo, c->pl, (const __half *)K_new, (const __half *)V_new,
-                           n_stride, ft, ft.prefix[p.B], st)
-      : launch_flush(c->geo, c->pl, (const __half *)K_new,
-                     (const __half *)V_new, n_stride, ft,
-                     ft.prefix[p.B], st);
+  cudaError_t e;
+  if (c->geo.age_b1 > 0) {
+    // AgeTieredKV: new groups, and the stored groups whose age crossed a
+    // boundary: for boundary x the groups G with S_old - (G+1) g < x <=
+    // S_new - (G+1) g, i.e. floor((S_old - x)/g) <= G < floor((S_new - x)/g)
+    auto floordiv = [](int64_t a, int64_t d) { return a >= 0 ? a / d : -((-a + d - 1) / d); };
+    AgeTable at;
+    at.prefix[0] = 0;
+    for (int b = 0; b < p.B; ++b) {
+      const int32_t S_old = c->S[b], S_new = S_old + n_new[b];
+      at.gn0[b] = c->Tq[b] / g;
+      at.gn1[b] = Tq_new[b] / g;
+      int64_t lo = INT32_MAX, hi = 0;
+      for (int x : {c->geo.age_b1, c->geo.age_b2}) {
+        const int64_t l = floordiv(S_old - x, g), u = floordiv(S_new - x, g);
+        if (u > l) { lo = l < lo ? l : lo; hi = u > hi ? u : hi; }
+      }
+      if (lo < 0) lo = 0;
+      if (hi > c->Tq[b] / g) hi = c->Tq[b] / g;
+      if (hi < lo) hi = lo;
+      at.gd0[b] = (int32_t)(hi > lo ? lo : 0);
+      at.gd1[b] = (int32_t)(hi > lo ? hi : 0);
+      at.src_split[b] = S_old;
+      at.S_old[b] = S_old;
+      at.S_new[b] = S_new;
+      at.prefix[b + 1] = at.prefix[b] + (at.gn1[b] - at.gn0[b]) + (at.gd1[b] - at.gd0[b]);
+    }
+    e = launch_age_flush(c->geo, c->pl, (const __half *)K_new, (const __half *)V_new,
+                         n_stride, at, st);
+  } else {
+    e = c->geo.kitty
+        ? launch_flush_kitty(c->geo, c->pl, (const __half *)K_new, (const __half *)V_new,
+                             n_stride, ft, ft.prefix[p.B], st)
+        : launch_flush(c->geo, c->pl, (const __half *)K_new,
+                       (const __half *)V_new, n_stride, ft,
+                       ft.prefix[p.B], st);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "flush kernel launch");
   e = launch_tail(c->geo, c->pl, (const __half *)K_new, (const __half *)V_new,
                   n_stride, tt, tt.prefix[p.B], st);
@@ -476,8 +546,9 @@ int vq_kivi_attend_multi(vq_kivi_cache *c, const void *q, int32_t S_q,
       return fail(VQ_ERR_ARG, "sequence %d holds %d tokens, fewer than S_q=%d",
                   b, c->S[b], S_q);
   const int GQ = p.H_q / p.H_kv;
-  if (c->geo.kitty)
-    return fail(VQ_ERR_UNSUPPORTED, "multi-query attend: not for Kitty caches");
+  if (c->geo.kitty || c->geo.age_b1 > 0)
+    return fail(VQ_ERR_UNSUPPORTED, "multi-query attend: not for Kitty or "
+                "AgeTieredKV caches");
   if (p.D != 64 && p.D != 128)
     return fail(VQ_ERR_UNSUPPORTED, "multi-query attend: D=%d (supported: 64, 128)", p.D);
   if (GQ != 1 && GQ != 2 && GQ != 4 && GQ != 8)
@@ -552,6 +623,7 @@ size_t vq_kivi_plane_bytes(const vq_kivi_cache *c, int which) {
     case 4: case 5: return kitty ? 0 : BH * geo.Tcap * (geo.D / geo.g) * sizeof(__half);
     case 11: return kitty ? BH * (geo.Tcap / geo.g) * (geo.D / 32) * 4 : 0;
     case 12: return kitty ? BH * geo.Tcap * geo.D * sizeof(__half) : 0;
+    case 13: return geo.age_b1 > 0 ? BH * (geo.Tcap / geo.g) : 0;
     case 6: case 7: return BH * geo.Rcap * geo.D * sizeof(__half);
     case 8: return BH * geo.n_sink * sizeof(int32_t);
     case 9: case 10: return BH * geo.n_sink * geo.D * sizeof(__half);
@@ -565,7 +637,7 @@ int vq_kivi_export(const vq_kivi_cache *c, int which, void *dst,
   if (rc) return rc;
   const size_t need = vq_kivi_plane_bytes(c, which);
   // an empty plane (no sinks, no Kitty, or a Kitty cache's value codes)
-  if (need == 0 && which >= 0 && which <= 12 && which != 1 && which != 2 &&
+  if (need == 0 && which >= 0 && which <= 13 && which != 1 && which != 2 &&
       which != 6 && which != 7)
     return VQ_OK;
   if (need == 0) return fail(VQ_ERR_ARG, "which=%d is not a plane", which);
@@ -587,6 +659,7 @@ int vq_kivi_export(const vq_kivi_cache *c, int which, void *dst,
     case 10: src = c->pl.sink_v; break;
     case 11: src = c->pl.kmask; break;
     case 12: src = c->pl.Vf; break;
+    case 13: src = c->pl.tier; break;
     default: break;
   }
   cudaError_t e;
@@ -605,8 +678,8 @@ int vq_kivi_dequantize(const vq_kivi_cache *c, void *K_hat, void *V_hat,
                        int64_t s_stride, void *stream) {
   int rc = check_cache(c);
   if (rc) return rc;
-  if (c->geo.kitty)
-    return fail(VQ_ERR_UNSUPPORTED, "dequantize: not for Kitty caches");
+  if (c->geo.kitty || c->geo.age_b1 > 0)
+    return fail(VQ_ERR_UNSUPPORTED, "dequantize: not for Kitty or AgeTieredKV caches");
   if (!K_hat || !V_hat) return fail(VQ_ERR_ARG, "K_hat or V_hat is NULL");
   if (((uintptr_t)K_hat | (uintptr_t)V_hat) & 15u)
     return fail(VQ_ERR_ARG, "K_hat and V_hat must be 16-byte aligned");
@@ -641,7 +714,14 @@ int vq_kivi_cache_bytes(const vq_kivi_cache *c, vq_kivi_bytes *out) {
       r.fp16_bytes += H * (uint64_t)c->S[b] * p.D * 4;
       continue;
     }
-    r.code_bytes += 2 * H * Tq * row;
+    if (c->geo.age_b1 > 0) {
+      // codes at each group's tier width (a row's capacity is D bytes)
+      for (int G = 0; G < (int)(Tq / p.group); ++G)
+        r.code_bytes += 2 * H * (uint64_t)p.group * p.D *
+                        c->geo.age_bits[age_tier(c->geo, c->S[b], G)] / 8;
+    } else {
+      r.code_bytes += 2 * H * Tq * row;
+    }
     r.meta_bytes += H * ((Tq / p.group) * p.D * 4 + Tq * (p.D / p.group) * 4);
     r.residual_bytes += H * (uint64_t)c->nres[b] * p.D * 4;
     r.fp16_bytes += H * (uint64_t)c->S[b] * p.D * 4;

@@ -233,6 +233,7 @@ cudaError_t launch_decode(const Geometry &geo, const Planes &pl,
                           const DecodeArgs &args, const DecodeTable &tab,
                           cudaStream_t st) {
   if (geo.kitty) return launch_decode_kitty(geo, pl, args, tab, st);
+  if (geo.age_b1 > 0) return launch_decode_age(geo, pl, args, tab, st);
   if (args.total_items > 0) {
     dim3 grid(args.total_items, geo.H_kv);
 #define VQK_CASE(DD, BB)                                                    \

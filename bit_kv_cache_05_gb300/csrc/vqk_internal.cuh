@@ -36,6 +36,8 @@ struct Planes {
   __half *Vf = nullptr;          // [B][H_kv][Tcap][D]
   long long *ksum = nullptr;     // [B][H_kv][D]
   unsigned long long *ksq = nullptr;  // [B][H_kv][D][2]
+  // AgeTieredKV (Geometry::age_b1 > 0): each group's current tier
+  int8_t *tier = nullptr;        // [B][H_kv][Tcap/g]
 };
 
 constexpr int kMaxSink = 16;     // sinks per (sequence, kv head)
@@ -54,7 +56,36 @@ struct Geometry {
   int n_sink = 0;               // KIVI-Sink tokens per (sequence, kv head)
   int kitty = 0;                // Kitty cache (mixed 4/2-bit keys, fp16 values)
   int kitty_hi = 0;             // Kitty: 4-bit channels per key group
+  // AgeTieredKV (age_b1 > 0): a group whose newest token has fewer than
+  // age_b1 newer tokens is stored at age_bits[0], fewer than age_b2 at
+  // age_bits[1], else at age_bits[2]; rows are D bytes (the widest width),
+  // the codes in their leading D * bits / 8 bytes
+  int age_b1 = 0, age_b2 = 0;
+  int age_bits[3] = {0, 0, 0};
 };
+
+// AgeTieredKV tier of group G of a sequence of S tokens
+__host__ __device__ inline int age_tier(const Geometry &geo, int S, int G) {
+  const int age = S - (G + 1) * geo.g;
+  return age < geo.age_b1 ? 0 : (age < geo.age_b2 ? 1 : 2);
+}
+
+// One AgeTieredKV flush: per sequence b, new groups [gn0, gn1) quantized
+// from fp16 (token position p from the residual ring below src_split, else
+// input row p - src_split) to their tier at length S_new, and stored groups
+// in [gd0, gd1) moved from their tier at S_old to their tier at S_new.
+struct AgeTable {
+  int32_t prefix[kMaxB + 1];   // items (new groups, then demotions) per b
+  int32_t gn0[kMaxB], gn1[kMaxB];
+  int32_t gd0[kMaxB], gd1[kMaxB];
+  int32_t src_split[kMaxB];
+  int32_t S_old[kMaxB], S_new[kMaxB];
+};
+cudaError_t launch_age_flush(const Geometry &geo, const Planes &pl,
+                             const __half *Kin, const __half *Vin,
+                             int64_t in_stride, const AgeTable &tab,
+                             cudaStream_t st);
+
 
 // ---- code-plane orders --------------------------------------------------
 //
@@ -234,6 +265,11 @@ cudaError_t launch_flush_kitty(const Geometry &geo, const Planes &pl,
 cudaError_t launch_decode_kitty(const Geometry &geo, const Planes &pl,
                                 const DecodeArgs &args, const DecodeTable &tab,
                                 cudaStream_t st);
+// decode over an AgeTieredKV cache (tables as the CUDA-core decode); S =
+// Tq + nres of a sequence gives every group's tier (age.cu)
+cudaError_t launch_decode_age(const Geometry &geo, const Planes &pl,
+                              const DecodeArgs &args, const DecodeTable &tab,
+                              cudaStream_t st);
 
 // ---- decode on the tensor cores (D = 64/128, H_q/H_kv <= 4) ---------------
 

@@ -127,6 +127,23 @@ typedef struct vq_kivi_options {
    * (VQ_ERR_UNSUPPORTED). */
   int32_t kitty;
   int32_t kitty_hi;
+  /* AgeTieredKV (method overview, AgeTieredKV entry), age_recent > 0: three
+   * widths of the group quantizer by token age.  A quantized group whose
+   * newest token has fewer than age_recent newer tokens holds
+   * age_bits_recent-bit codes, fewer than age_mid age_bits_mid-bit codes,
+   * else age_bits_old-bit codes.  A group enters at the top tier and moves
+   * down one tier at a time as it ages (on an append), re-quantized from
+   * its values rebuilt in fp32 (code * scale, then + zero, each rounded to
+   * nearest), so a prefill and any chunking of appends give the same
+   * cache.  Rows of planes 0 and 3 are D bytes (the widest tier): a group's
+   * codes fill their leading D * bits / 8 bytes, the rest zero.  Requires
+   * bits = 8 (the row capacity), n_sink = 0, no Kitty, D = 64 or 128,
+   * 0 < age_recent < age_mid, both multiples of g, widths in {2, 4, 8},
+   * non-increasing.  The pages' defaults: 128, 1024, 8 / 4 / 2 bits.
+   * Decode runs on the CUDA cores; vq_kivi_attend_multi and
+   * vq_kivi_dequantize do not serve these caches (VQ_ERR_UNSUPPORTED). */
+  int32_t age_recent, age_mid;
+  int32_t age_bits_recent, age_bits_mid, age_bits_old;
 } vq_kivi_options;
 
 /* vq_kivi_quantize with options (NULL options = all zero). */
@@ -212,8 +229,10 @@ int vq_kivi_get_params(const vq_kivi_cache *c, vq_kivi_params *p);
  *  10 sink values     fp16  [B][H_kv][n_sink][D]  (8-10: size 0 without sinks)
  *  11 Kitty 4-bit channel masks  uint32 [B][H_kv][Tcap/g][D/32]
  *  12 Kitty fp16 values          fp16   [B][H_kv][Tcap][D]
+ *  13 AgeTieredKV group tiers    int8   [B][H_kv][Tcap/g]  (0 recent, 1 mid, 2 old)
  * A Kitty cache's plane 0 has rows of (D + kitty_hi)/4 bytes (see
- * vq_kivi_options) and planes 3-5 are empty; without Kitty 11-12 are empty.
+ * vq_kivi_options) and planes 3-5 are empty; without Kitty 11-12 are empty,
+ * without AgeTieredKV 13.
  * An empty plane has size 0 and its export does nothing.
  * where Tcap = ceil(max_seq/g)*g (at least g).  vq_kivi_plane_bytes gives
  * the size (0 for a bad `which`); vq_kivi_export writes the whole plane to
