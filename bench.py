@@ -491,6 +491,14 @@ def run_ours(args, w, rank, world, local):
             measure_workload(synth.workload("pages_S32768"), peak, full=False,
                              kitty_hi=32), kitty_hi=32)
         torch.cuda.empty_cache()
+        # AgeTieredKV decode at the pages' shape, the pages' default tiers
+        # (8 / 4 / 2 bits below 128 / 1024 tokens of age); 8-bit row capacity
+        age = (128, 1024, 8, 4, 2)
+        wa = synth.dataclasses.replace(synth.workload("pages_S32768"), bits=8,
+                                       residual=0)
+        targets["pages_S32768_age"] = dict(
+            measure_workload(wa, peak, full=False, age=age), age=list(age))
+        torch.cuda.empty_cache()
         tpk, tpk_kind = measured_peak_tflops()
         targets["int4_append_prefill_attend"] = dict(
             measure_multi(synth.workload("int4_append"), 512, tpk),
@@ -543,7 +551,7 @@ def run_ours(args, w, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
-def measure_workload(w, peak, full=True, n_sink=0, kitty_hi=None):
+def measure_workload(w, peak, full=True, n_sink=0, kitty_hi=None, age=None):
     """The decode of workload `w` from HBM (rotating over cache copies larger
     than 4x L2, the median of 100 launches), and the append of the
     workload's appended tokens per sequence (one token when it appends none)
@@ -571,7 +579,7 @@ def measure_workload(w, peak, full=True, n_sink=0, kitty_hi=None):
                                 bits=w.bits, group=w.group,
                                 residual=w.residual,
                                 max_seq=w.max_seq + n_app + 8, n_sink=n_sink,
-                                kitty_hi=kitty_hi))
+                                kitty_hi=kitty_hi, age=age))
     # prefill and append are timed over at least 8 caches; the decode
     # rotates over the first ncp
     na = max(ncp, 8)
@@ -596,9 +604,10 @@ def measure_workload(w, peak, full=True, n_sink=0, kitty_hi=None):
     # KIVI-Sink: the fp16 rows of the sinks of the quantized region
     cb = caches[0].cache_bytes()
     nb += cb["sink_bytes"]
-    if kitty_hi is not None:
+    if kitty_hi is not None or age is not None:
         # Kitty: mixed-width key rows + key scale/zero + channel masks, fp16
-        # values and residual window, q and out
+        # values and residual window, q and out; AgeTieredKV: codes at each
+        # group's width + scales / zeros + residual, q and out
         gq = w.H_q // w.H_kv
         nb = (cb["code_bytes"] + cb["meta_bytes"] + cb["value_fp16_bytes"] +
               cb["residual_bytes"] + w.B * w.H_q * w.D * (2 + 4))

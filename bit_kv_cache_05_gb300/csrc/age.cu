@@ -12,6 +12,8 @@
 // chunking of appends give the same cache.  Rows are D bytes (the widest
 // tier); a group's codes fill the leading D * bits / 8 bytes, packed LSB
 // first, the rest zero.
+#include <type_traits>
+
 #include "vqk_internal.cuh"
 
 namespace vqk {
@@ -255,17 +257,32 @@ k_decode_age(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
         if (lane < bt) {
           const uint32_t *row = reinterpret_cast<const uint32_t *>(
               pl.Kc + (bh * geo.Tcap + tb + lane) * D);
-          const int per = 32 / w;
-#pragma unroll 1
-          for (int wi = 0; wi < D * w / 32; ++wi) {
-            const uint32_t x = __ldg(row + wi);
-            for (int e = 0; e < per; ++e) {
-              const float code = (float)((x >> (w * e)) & cm);
+          // the lane's row at the group's width, the field loop unrolled per
+          // width
+          auto walk = [&](auto w_tag) {
+            constexpr int W = decltype(w_tag)::value, PER = 32 / W;
+            constexpr uint32_t CM = (1u << W) - 1u;
+#pragma unroll 2
+            for (int wi = 0; wi < D * W / 32; ++wi) {
+              const uint32_t x = __ldg(row + wi);
 #pragma unroll
-              for (int hh = 0; hh < GQ; ++hh)
-                acc[hh] = fmaf(sa[warp][hh][wi * per + e], code, acc[hh]);
+              for (int e = 0; e < PER; e += 4) {
+#pragma unroll
+                for (int hh = 0; hh < GQ; ++hh) {
+                  const float4 a4 = *reinterpret_cast<const float4 *>(&sa[warp][hh][wi * PER + e]);
+                  float r = acc[hh];
+                  r = fmaf(a4.x, (float)((x >> (W * e)) & CM), r);
+                  r = fmaf(a4.y, (float)((x >> (W * (e + 1))) & CM), r);
+                  r = fmaf(a4.z, (float)((x >> (W * (e + 2))) & CM), r);
+                  r = fmaf(a4.w, (float)((x >> (W * (e + 3))) & CM), r);
+                  acc[hh] = r;
+                }
+              }
             }
-          }
+          };
+          if (w == 2) walk(std::integral_constant<int, 2>{});
+          else if (w == 4) walk(std::integral_constant<int, 4>{});
+          else walk(std::integral_constant<int, 8>{});
         }
         float s[GQ], p[GQ];
 #pragma unroll
@@ -273,7 +290,7 @@ k_decode_age(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
         fold(s, p);
         // values: o_c += sum_t p_t (code_tc s_tj + z_tj)
         const int c0 = lane * CPL, j = c0 / g;
-#pragma unroll 4
+#pragma unroll 8
         for (int jj = 0; jj < bt; ++jj) {
           const size_t r = bh * geo.Tcap + tb + jj;
           const float vs = __half2float(pl.Vs[r * NJ + j]);

@@ -502,9 +502,10 @@ int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
   int32_t tps = c->split_tokens;
   const int32_t unit = split_unit(p.group);
   if (tps == 0) {
-    // Kitty streams fp16 values: more, shorter items keep more loads in
-    // flight per SM
-    const int64_t target_items = (c->geo.kitty ? 16LL : 4LL) * c->sm_count;
+    // Kitty and AgeTieredKV caches (one token per lane, loads in flight
+    // limited by the block): more, shorter items keep more of them per SM
+    const int64_t target_items =
+        (c->geo.kitty || c->geo.age_b1 > 0 ? 16LL : 4LL) * c->sm_count;
     int64_t t = (total_tq * p.H_kv + target_items - 1) / target_items;
     tps = (int32_t)round_up((size_t)(t > 1 ? t : 1), unit);
   }
