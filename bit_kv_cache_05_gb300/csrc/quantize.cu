@@ -357,6 +357,237 @@ k_flush(Geometry geo, Planes pl, const __half *__restrict__ Kin,
     store_packed_tile<BITS>(codes, CS, g, D, pl.Vc + (bh * geo.Tcap + P0) * geo.row);
 }
 
+// The flush for the common shapes (D = 64 or 128, g = 32 or 64), with D,
+// g and the code width known at compile time: every index of the tile, the
+// code tile and the packers is a constant or a shift, the g source rows of
+// the group are looked up once (the residual ring's slot arithmetic per
+// token, not per 16-byte chunk), and each thread keeps its key column and
+// its value group in registers from the one read to the quantization.
+// Same arithmetic as k_flush, bit for bit.
+template <int BITS, int D, int G>
+__device__ __forceinline__ void store_frag_keys_t(const uint8_t *codes, uint8_t *dst) {
+  constexpr int F = 16 / BITS, KPW = 8 / BITS, CS = D + 4;
+  constexpr int WPR = D * BITS / 32, NWD = D * BITS / 128;
+#pragma unroll
+  for (int k = 0; k < G * WPR / D; ++k) {
+    const int w = threadIdx.x + k * D;
+    const int i = w / WPR, wi = w % WPR;
+    const int tig = wi / NWD, hw = wi % NWD;
+    uint32_t acc = 0;
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+#pragma unroll
+      for (int r = 0; r < F; ++r) {
+        const int ks = KPW * hw + (r >> 1), e = 2 * (r & 1) + s;
+        acc |= (uint32_t)codes[i * CS + 16 * ks + 4 * tig + e] << (16 * s + BITS * r);
+      }
+    reinterpret_cast<uint32_t *>(dst)[w] = acc;
+  }
+}
+
+template <int BITS, int D, int G>
+__device__ __forceinline__ void store_frag_values_t(const uint8_t *codes, uint8_t *dst) {
+  constexpr int F = 16 / BITS, KPW = 8 / BITS, CS = D + 4;
+  constexpr int NWD = D * BITS / 128, WPB = D * BITS / 2;
+#pragma unroll
+  for (int k = 0; k < G * D * BITS / 32 / D; ++k) {
+    const int w = threadIdx.x + k * D;
+    const int kb = w / WPB, wb = w % WPB;
+    const int pi = wb / (8 * NWD), rem = wb % (8 * NWD);
+    const int j = rem / NWD, hw = rem % NWD;
+    const int tA = 16 * kb + (pi < 4 ? pi : pi + 4);
+    uint32_t acc = 0;
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+#pragma unroll
+      for (int r = 0; r < F; ++r) {
+        const int mv = KPW * hw + (r >> 1), rho = r & 1;
+        acc |= (uint32_t)codes[(tA + 4 * s) * CS + 16 * mv + 2 * j + rho]
+               << (16 * s + BITS * r);
+      }
+    reinterpret_cast<uint32_t *>(dst)[w] = acc;
+  }
+}
+
+template <int BITS, int D, int G>
+__device__ __forceinline__ void store_packed_tile_t(const uint8_t *codes, uint8_t *dst) {
+  constexpr int ROW = D * BITS / 8, CS = D + 4, PER = 32 / BITS;
+#pragma unroll
+  for (int k = 0; k < (G * ROW / 16 + D - 1) / D; ++k) {
+    const int q16 = threadIdx.x + k * D;
+    if (q16 >= G * ROW / 16) break;
+    const int byte0 = 16 * q16;
+    const int i = byte0 / ROW, e0 = (byte0 % ROW) * 8 / BITS;
+    const uint8_t *src = codes + i * CS + e0;
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t acc = 0;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc |= (uint32_t)src[q * PER + e] << (BITS * e);
+      w[q] = acc;
+    }
+    *reinterpret_cast<uint4 *>(dst + byte0) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+template <int BITS, int D, int G>
+__global__ void __launch_bounds__(D)
+k_flush_t(Geometry geo, Planes pl, const __half *__restrict__ Kin,
+          const __half *__restrict__ Vin, int64_t in_stride, FlushTable tab) {
+  pdl_wait_and_release();
+  constexpr int levels = (1 << BITS) - 1, CS = D + 4, ROW = D * BITS / 8;
+  constexpr int NJ = D / G, CPR = D / 8;
+  extern __shared__ __align__(16) unsigned char fsm[];
+  __half *tile = reinterpret_cast<__half *>(fsm);                 // [G][D]
+  uint8_t *codes = fsm + (size_t)G * D * sizeof(__half);         // [G][CS]
+  __shared__ const __half *sk[G], *sv[G];
+  __shared__ uint32_t sinkm[4];
+  const int c = threadIdx.x, item = blockIdx.x, h = blockIdx.y;
+  const int b = find_seq(tab.prefix, geo.B, item);
+  const int P0 = tab.first_pos[b] + (item - tab.prefix[b]) * G;
+  const int split = tab.src_split[b];
+  const size_t bh = (size_t)b * geo.H_kv + h;
+  if (c < G) {
+    // the source rows of the group's tokens: residual ring, then input
+    const int p = P0 + c;
+    if (p < split) {
+      const size_t off = (bh * geo.Rcap + (p % geo.Rcap)) * D;
+      sk[c] = pl.Kr + off;
+      sv[c] = pl.Vr + off;
+    } else {
+      const size_t off = (bh * in_stride + (p - split)) * D;
+      sk[c] = Kin + off;
+      sv[c] = Vin + off;
+    }
+  }
+  const bool sinks = geo.n_sink > 0;
+  if (sinks && c < 4) sinkm[c] = 0u;
+  __syncthreads();
+  if (sinks && c < geo.n_sink) {
+    const int p = pl.sink_pos[bh * geo.n_sink + c];
+    if (p >= P0 && p < P0 + G) atomicOr(&sinkm[(p - P0) >> 5], 1u << ((p - P0) & 31));
+  }
+  // key tile: G rows of D fp16 values, 16-byte loads
+#pragma unroll
+  for (int k = 0; k < G * CPR / D; ++k) {
+    const int idx = c + k * D, i = idx / CPR, c8 = (idx % CPR) * 8;
+    *reinterpret_cast<uint4 *>(tile + i * D + c8) =
+        *reinterpret_cast<const uint4 *>(sk[i] + c8);
+  }
+  __syncthreads();
+  auto is_sink = [&](int i) { return sinks && ((sinkm[i >> 5] >> (i & 31)) & 1u); };
+
+  // ---- keys: channel c over the G tokens, held as fp16 pairs ----
+  {
+    __half2 col[G / 2];
+#pragma unroll
+    for (int k = 0; k < G / 2; ++k)
+      col[k] = __halves2half2(tile[(2 * k) * D + c], tile[(2 * k + 1) * D + c]);
+    float mn, mx;
+    if (!sinks) {
+      __half2 mn2 = col[0], mx2 = col[0];
+#pragma unroll
+      for (int k = 1; k < G / 2; ++k) {
+        mn2 = __hmin2(mn2, col[k]);
+        mx2 = __hmax2(mx2, col[k]);
+      }
+      mn = fminf(__low2float(mn2), __high2float(mn2));
+      mx = fmaxf(__low2float(mx2), __high2float(mx2));
+    } else {
+      mn = INFINITY;
+      mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < G / 2; ++k) {
+        const float2 f = __half22float2(col[k]);
+        if (!is_sink(2 * k)) { mn = fminf(mn, f.x); mx = fmaxf(mx, f.x); }
+        if (!is_sink(2 * k + 1)) { mn = fminf(mn, f.y); mx = fmaxf(mx, f.y); }
+      }
+      if (mn > mx) { mn = 0.f; mx = 0.f; }   // sinks only: scale and zero +0
+    }
+    mn = __fadd_rn(mn, 0.0f);  // a -0.0 minimum is stored as +0.0
+    // a zero range is +0.0 (max - min is -0.0 when the max is -0.0)
+    const float scale = __fdiv_rn(__fadd_rn(__fsub_rn(mx, mn), 0.0f), (float)levels);
+    const float rcp = scale != 0.0f ? __frcp_rn(scale) : 0.0f;
+    const size_t idx = (bh * (geo.Tcap / G) + P0 / G) * D + c;
+    const __half sh = __float2half_rn(scale);
+    pl.Ks[idx] = sh;
+    pl.Kz[idx] = __float2half_rn(mn);
+    if (pl.ksmax) {
+      const unsigned m = __reduce_max_sync(0xffffffffu, (unsigned)__half_as_ushort(sh));
+      if ((c & 31) == 0) atomicMax(pl.ksmax + bh, m);
+    }
+#pragma unroll
+    for (int k = 0; k < G / 2; ++k) {
+      uint32_t c0, c1;
+      quant2(__half22float2(col[k]), mn, scale, rcp, c0, c1);
+      codes[(2 * k) * CS + c] = is_sink(2 * k) ? 0 : (uint8_t)c0;
+      codes[(2 * k + 1) * CS + c] = is_sink(2 * k + 1) ? 0 : (uint8_t)c1;
+    }
+  }
+  __syncthreads();
+  if constexpr (BITS == 2 || BITS == 4) {
+    if (geo.layout == kLayoutFrag)
+      store_frag_keys_t<BITS, D, G>(codes, pl.Kc + (bh * geo.Tcap + P0) * ROW);
+    else
+      store_packed_tile_t<BITS, D, G>(codes, pl.Kc + (bh * geo.Tcap + P0) * ROW);
+  } else {
+    store_packed_tile_t<BITS, D, G>(codes, pl.Kc + (bh * geo.Tcap + P0) * ROW);
+  }
+  __syncthreads();
+
+  // ---- values: token i over channels j*G ... j*G+G-1, in registers ----
+  {
+    const int i = c / NJ, j = c % NJ;
+    const bool empty = is_sink(i);   // a sink's value groups have no member
+    const uint4 *row = reinterpret_cast<const uint4 *>(sv[i] + j * G);
+    uint4 u[G / 8];
+#pragma unroll
+    for (int k = 0; k < G / 8; ++k) u[k] = row[k];
+    __half2 mn2 = *reinterpret_cast<const __half2 *>(&u[0].x), mx2 = mn2;
+#pragma unroll
+    for (int k = 0; k < G / 8; ++k) {
+      const __half2 *h4 = reinterpret_cast<const __half2 *>(&u[k]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        mn2 = __hmin2(mn2, h4[e]);
+        mx2 = __hmax2(mx2, h4[e]);
+      }
+    }
+    float mn = fminf(__low2float(mn2), __high2float(mn2));
+    const float mx = fmaxf(__low2float(mx2), __high2float(mx2));
+    mn = empty ? 0.f : __fadd_rn(mn, 0.0f);
+    const float scale = empty ? 0.f : __fdiv_rn(__fadd_rn(__fsub_rn(mx, mn), 0.0f), (float)levels);
+    const float rcp = scale != 0.0f ? __frcp_rn(scale) : 0.0f;
+    uint32_t *crow = reinterpret_cast<uint32_t *>(codes + i * CS + j * G);
+#pragma unroll
+    for (int k = 0; k < G / 8; ++k) {
+      const __half2 *h4 = reinterpret_cast<const __half2 *>(&u[k]);
+      uint32_t w[2] = {0u, 0u};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        uint32_t c0, c1;
+        quant2(__half22float2(h4[e]), mn, scale, rcp, c0, c1);
+        w[e >> 1] |= (c0 | (c1 << 8)) << (16 * (e & 1));
+      }
+      crow[2 * k] = w[0];
+      crow[2 * k + 1] = w[1];
+    }
+    const size_t vidx = (bh * geo.Tcap + P0 + i) * NJ + j;
+    pl.Vs[vidx] = __float2half_rn(scale);
+    pl.Vz[vidx] = __float2half_rn(mn);
+  }
+  __syncthreads();
+  if constexpr (BITS == 2 || BITS == 4) {
+    if (geo.layout == kLayoutFrag)
+      store_frag_values_t<BITS, D, G>(codes, pl.Vc + (bh * geo.Tcap + P0) * ROW);
+    else
+      store_packed_tile_t<BITS, D, G>(codes, pl.Vc + (bh * geo.Tcap + P0) * ROW);
+  } else {
+    store_packed_tile_t<BITS, D, G>(codes, pl.Vc + (bh * geo.Tcap + P0) * ROW);
+  }
+}
+
 // Residual ring writes: 16-byte chunks of fp16 rows.
 __global__ void __launch_bounds__(kThreads)
 k_tail(Geometry geo, Planes pl, const __half *__restrict__ Kin,
@@ -413,6 +644,20 @@ cudaError_t launch_flush(const Geometry &geo, const Planes &pl,
   if (total_groups <= 0) return cudaSuccess;
   dim3 grid(total_groups, geo.H_kv);
   const size_t smem = (size_t)geo.g * (geo.D * sizeof(__half) + geo.D + 4);
+  // the common shapes: the compile-time specialised flush
+#define VQK_FT(BB, DD, GG)                                                     \
+  if (geo.bits == BB && geo.D == DD && geo.g == GG) {                          \
+    const cudaError_t e2 = launch_pdl(k_flush_t<BB, DD, GG>, grid, dim3(DD),   \
+                                      smem, st, geo, pl, Kin, Vin, in_stride,  \
+                                      tab);                                    \
+    count_launch();                                                            \
+    return e2;                                                                 \
+  }
+#define VQK_FT_B(BB) VQK_FT(BB, 64, 32) VQK_FT(BB, 64, 64) VQK_FT(BB, 128, 32) \
+  VQK_FT(BB, 128, 64)
+  VQK_FT_B(2) VQK_FT_B(4) VQK_FT_B(8)
+#undef VQK_FT_B
+#undef VQK_FT
   void *fn = nullptr;
   switch (geo.bits) {
     case 2: fn = (void *)k_flush<2>; break;
