@@ -69,6 +69,7 @@ def _load():
         lib.orc_attend.argtypes = [P, P, f64, P]
         lib.orc_attend_one.argtypes = [P, i32, i32, P, f64, P]
         lib.orc_attend_multi.argtypes = [P, P, i32, f64, P]
+        lib.orc_attend_prefix.argtypes = [P, i32, i32, P, i32, f64, P]
         lib.orc_lengths.argtypes = [P, P, P, P]
         lib.orc_dims.argtypes = [P, P, P]
         lib.orc_plane_bytes.restype = ctypes.c_size_t
@@ -216,6 +217,19 @@ class OracleCache:
                                         _ptr(out))
         if rc != 0:
             raise ValueError("oracle: a sequence is shorter than S_q")
+        return out
+
+    def attend_prefix(self, b: int, hq: int, q_row, last: int,
+                      scale=None) -> np.ndarray:
+        """One query of head hq attending tokens 0 ... last of sequence b
+        (the causal prefix of the query at position last)."""
+        q_row = _f16bits(q_row).reshape(-1)
+        assert q_row.size == self.D
+        out = np.zeros(self.D, np.float64)
+        sc = (1.0 / np.sqrt(self.D)) if scale is None else float(scale)
+        if self._lib.orc_attend_prefix(self._c, b, hq, _ptr(q_row), last, sc,
+                                       _ptr(out)) != 0:
+            raise ValueError("oracle: position outside the sequence")
         return out
 
     def attend_one(self, b: int, hq: int, q_row, scale=None) -> np.ndarray:

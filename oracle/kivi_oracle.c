@@ -811,47 +811,56 @@ int orc_attend_one(const orc_cache *c, int b, int hq, const uint16_t *q_row,
  * orc_attend_one).  q fp16 [B][Hq][S_q][D] -> out fp32 [B][Hq][S_q][D], the
  * softmax in double as in orc_attend_one.  Returns 0, or -1 when some
  * sequence holds fewer than S_q tokens (out untouched). */
+/* One query of head hq of sequence b attending tokens 0 ... last (the
+ * causal prefix of the query at position last); out: D doubles.  Returns
+ * 0, or -1 when last is outside [0, S - 1]. */
+int orc_attend_prefix(const orc_cache *c, int b, int hq, const uint16_t *q_row,
+                      int last, double scale, double *out) {
+  const int D = c->D;
+  const int h = hq / (c->Hq / c->Hkv);
+  if (last < 0 || last >= c->S[b]) return -1;
+  double *qd = (double *)malloc(sizeof(double) * D);
+  double *k = (double *)malloc(sizeof(double) * D);
+  double *v = (double *)malloc(sizeof(double) * D);
+  double *s = (double *)malloc(sizeof(double) * (size_t)(last + 1));
+  for (int ch = 0; ch < D; ++ch) qd[ch] = h2f(q_row[ch]);
+  double m = -INFINITY;
+  for (int t = 0; t <= last; ++t) {
+    token_hat(c, b, h, t, k, v);
+    double dot = 0.0;
+    for (int ch = 0; ch < D; ++ch) dot += qd[ch] * k[ch];
+    s[t] = scale * dot;
+    if (s[t] > m) m = s[t];
+  }
+  double l = 0.0;
+  for (int ch = 0; ch < D; ++ch) out[ch] = 0.0;
+  for (int t = 0; t <= last; ++t) {
+    double p = exp(s[t] - m);
+    l += p;
+    token_hat(c, b, h, t, k, v);
+    for (int ch = 0; ch < D; ++ch) out[ch] += p * v[ch];
+  }
+  for (int ch = 0; ch < D; ++ch) out[ch] /= l;
+  free(qd); free(k); free(v); free(s);
+  return 0;
+}
+
 int orc_attend_multi(const orc_cache *c, const uint16_t *q, int S_q,
                      double scale, float *out) {
   const int D = c->D;
   if (S_q <= 0) return -1;
   for (int b = 0; b < c->B; ++b)
     if (c->S[b] < S_q) return -1;
-  double *qd = (double *)malloc(sizeof(double) * D);
-  double *k = (double *)malloc(sizeof(double) * D);
-  double *v = (double *)malloc(sizeof(double) * D);
   double *o = (double *)malloc(sizeof(double) * D);
-  for (int b = 0; b < c->B; ++b) {
-    const int S = c->S[b];
-    double *s = (double *)malloc(sizeof(double) * (size_t)S);
-    for (int hq = 0; hq < c->Hq; ++hq) {
-      const int h = hq / (c->Hq / c->Hkv);
+  for (int b = 0; b < c->B; ++b)
+    for (int hq = 0; hq < c->Hq; ++hq)
       for (int i = 0; i < S_q; ++i) {
         const size_t row = (((size_t)b * c->Hq + hq) * S_q + i) * D;
-        const int pos = S - S_q + i; /* this query's own position */
-        for (int ch = 0; ch < D; ++ch) qd[ch] = h2f(q[row + ch]);
-        double m = -INFINITY;
-        for (int t = 0; t <= pos; ++t) {
-          token_hat(c, b, h, t, k, v);
-          double dot = 0.0;
-          for (int ch = 0; ch < D; ++ch) dot += qd[ch] * k[ch];
-          s[t] = scale * dot;
-          if (s[t] > m) m = s[t];
-        }
-        double l = 0.0;
-        for (int ch = 0; ch < D; ++ch) o[ch] = 0.0;
-        for (int t = 0; t <= pos; ++t) {
-          double p = exp(s[t] - m);
-          l += p;
-          token_hat(c, b, h, t, k, v);
-          for (int ch = 0; ch < D; ++ch) o[ch] += p * v[ch];
-        }
-        for (int ch = 0; ch < D; ++ch) out[row + ch] = (float)(o[ch] / l);
+        /* query i sits at position S - S_q + i and sees tokens up to it */
+        orc_attend_prefix(c, b, hq, q + row, c->S[b] - S_q + i, scale, o);
+        for (int ch = 0; ch < D; ++ch) out[row + ch] = (float)o[ch];
       }
-    }
-    free(s);
-  }
-  free(qd); free(k); free(v); free(o);
+  free(o);
   return 0;
 }
 

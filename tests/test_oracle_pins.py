@@ -1111,3 +1111,26 @@ def test_age_attention_brute_force_and_error_grows_with_age(oracle_mod):
     per_group = err.reshape(-1, g, D).mean(axis=(1, 2))
     assert per_group[tiers == 2].mean() > 4 * per_group[tiers == 0].mean()
     assert {0, 1, 2} <= set(tiers.tolist())
+
+
+def test_prefix_attention_reduces_to_decode_and_multi(oracle_mod):
+    """A query attending the prefix that ends at the last token is the
+    one-query decode, bit for bit; prefixes ending earlier are the causal
+    multi-query outputs of those positions."""
+    B, Hq, H, D, g, R = 2, 4, 2, 8, 4, 5
+    lens = [33, 12]
+    oc, K, V = _cache(oracle_mod, B, Hq, H, D, 2, g, R, lens, seed=23)
+    rng = np.random.default_rng(123)
+    q = rand_f16(rng, (B, Hq, D))
+    dec = oc.attend(q)
+    q3 = np.ascontiguousarray(np.repeat(q[:, :, None], 3, axis=2))
+    multi = oc.attend_multi(q3)
+    for b in range(B):
+        for hq in range(Hq):
+            full = oc.attend_prefix(b, hq, q[b, hq], lens[b] - 1)
+            assert np.array_equal(full.astype(np.float32), dec[b, hq])
+            for i in range(3):
+                pre = oc.attend_prefix(b, hq, q[b, hq], lens[b] - 3 + i)
+                assert np.array_equal(pre.astype(np.float32), multi[b, hq, i])
+    with pytest.raises(ValueError):
+        oc.attend_prefix(1, 0, q[1, 0], lens[1])
