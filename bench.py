@@ -811,14 +811,29 @@ def run_report(names):
 
 def run_profile_decode(name: str, n: int):
     """One cache of a named workload and n decode launches on it, for ncu
-    captures of the decode kernels (and of the prefill's k_flush)."""
+    captures of the decode kernels (and of the prefill's k_flush).  A
+    suffix picks the variant the benchmark times beside the plain cache:
+    ":sink5" (5 sink tokens), ":kitty" (32 of 128 key channels in 4 bits),
+    ":age" (8 / 4 / 2-bit tiers below 128 / 1024 tokens of age)."""
     import torch
     from bit_kv_cache_05_gb300 import synth
     from bit_kv_cache_05_gb300.cache import KiviCache
+    name, _, variant = name.partition(":")
     w = synth.workload(name)
+    extra = {}
+    if variant == "sink5":
+        extra = dict(n_sink=5)
+    elif variant == "kitty":
+        extra = dict(kitty_hi=w.D // 4)
+    elif variant == "age":
+        w = synth.dataclasses.replace(w, bits=8, residual=0)
+        extra = dict(age=(128, 1024, 8, 4, 2))
+    elif variant:
+        raise SystemExit(f"unknown decode variant {variant!r}")
     inp = synth.make_inputs(w, device="cuda")
     c = KiviCache(inp["K"], inp["V"], w.seq_lens, H_q=w.H_q, bits=w.bits,
-                  group=w.group, residual=w.residual, max_seq=w.max_seq)
+                  group=w.group, residual=w.residual, max_seq=w.max_seq,
+                  **extra)
     del inp["K"], inp["V"]
     torch.cuda.synchronize()
     out = None
