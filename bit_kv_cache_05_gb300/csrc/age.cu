@@ -1,5 +1,6 @@
 // AgeTieredKV: quantization width by token age (three tiers of the KIVI
-// group quantizer), its flush (quantize and demote) and its fused decode.
+// group quantizer): its flush (quantize and demote), the export of its code
+// planes and the launch of its fused decode (age_decode.cuh).
 //
 // Method: VeloxQuant-MLX method overview, AgeTieredKV entry (three tiers,
 // default 8 / 4 / 2 bits, chosen by current position minus token position
@@ -9,12 +10,13 @@
 // counts from its newest token; a group enters at the top tier and moves
 // down one tier at a time, re-quantized from its values rebuilt in fp32
 // (code * scale rounded, then + zero rounded), so that a prefill and any
-// chunking of appends give the same cache.  Rows are D bytes (the widest
-// tier); a group's codes fill the leading D * bits / 8 bytes, packed LSB
-// first, the rest zero.
-#include <type_traits>
-
-#include "vqk_internal.cuh"
+// chunking of appends give the same cache.  A group owns g * D bytes of
+// each code plane; at width w its rows (D * w / 8 bytes, codes LSB first)
+// are packed densely from the start of that block, so that a decode reads
+// only the group's bytes (rows of D bytes with the codes in their leading
+// bytes made DRAM fetch every row's whole line: 2.9x the bytes at 2 bits).
+// The export expands the rows to D bytes.
+#include "age_decode.cuh"
 
 namespace vqk {
 namespace {
@@ -81,13 +83,14 @@ __global__ void k_age_flush(Geometry geo, Planes pl, const __half *__restrict__ 
       xv[idx] = __half2float(p < split ? pl.Vr[src] : Vin[src]);
     }
   } else {
-    const int w = geo.age_bits[t];
+    const int w = age_width(geo, t);
     const uint32_t m = (1u << w) - 1u;
     for (int idx = c; idx < g * D; idx += blockDim.x) {
       const int i = idx / D, ch = idx - i * D;
       const int bit = ch * w;
-      const uint8_t kb = pl.Kc[(r0 + i) * D + (bit >> 3)];
-      const uint8_t vb = pl.Vc[(r0 + i) * D + (bit >> 3)];
+      const size_t ro = age_row_off(geo, bh, G, i, w) + (bit >> 3);
+      const uint8_t kb = pl.Kc[ro];
+      const uint8_t vb = pl.Vc[ro];
       const float kcode = (float)((kb >> (bit & 7)) & m);
       const float vcode = (float)((vb >> (bit & 7)) & m);
       xk[idx] = __fadd_rn(__fmul_rn(kcode, __half2float(pl.Ks[kg + ch])),
@@ -104,7 +107,7 @@ __global__ void k_age_flush(Geometry geo, Planes pl, const __half *__restrict__ 
   const int vi_tok = c / NJ, vi_grp = c - (c / NJ) * NJ;   // thread's value group
   while (t < t_to) {
     ++t;
-    const int levels = (1 << geo.age_bits[t]) - 1;
+    const int levels = (1 << age_width(geo, t)) - 1;
     // keys: channel c over the g tokens
     {
       float mn = INFINITY, mx = -INFINITY;
@@ -149,229 +152,60 @@ __global__ void k_age_flush(Geometry geo, Planes pl, const __half *__restrict__ 
   pl.Kz[kg + c] = __float2half_rn(kzero);
   pl.Vs[(r0 + vi_tok) * NJ + vi_grp] = __float2half_rn(vscale);
   pl.Vz[(r0 + vi_tok) * NJ + vi_grp] = __float2half_rn(vzero);
-  const int w = geo.age_bits[t_to];
-  const int per = 32 / w, words = D / 4;                   // 32-bit words per row
-  for (int idx = c; idx < g * words; idx += blockDim.x) {
-    const int i = idx / words, k = idx - i * words;
+  // rows packed densely at the final width (the group block's leading
+  // g * D * w / 8 bytes); every read of the old rows is behind the
+  // barriers above, so the block is rewritten in place
+  const int w = age_width(geo, t_to);
+  const int per = 32 / w, wpr = D * w / 32;                // fields, words per row
+  for (int idx = c; idx < g * wpr; idx += blockDim.x) {
+    const int i = idx / wpr, k = idx - i * wpr;
     uint32_t ak = 0, av = 0;
-    if (k < D * w / 32) {
-      for (int e = 0; e < per; ++e) {
-        ak |= (uint32_t)ck[i * D + k * per + e] << (w * e);
-        av |= (uint32_t)cv[i * D + k * per + e] << (w * e);
-      }
+    for (int e = 0; e < per; ++e) {
+      ak |= (uint32_t)ck[i * D + k * per + e] << (w * e);
+      av |= (uint32_t)cv[i * D + k * per + e] << (w * e);
     }
-    reinterpret_cast<uint32_t *>(pl.Kc + (r0 + i) * D)[k] = ak;
-    reinterpret_cast<uint32_t *>(pl.Vc + (r0 + i) * D)[k] = av;
+    const size_t wo = age_row_off(geo, bh, G, i, w) / 4 + k;
+    reinterpret_cast<uint32_t *>(pl.Kc)[wo] = ak;
+    reinterpret_cast<uint32_t *>(pl.Vc)[wo] = av;
   }
   if (c == 0) pl.tier[bh * (geo.Tcap / g) + G] = (int8_t)t_to;
 }
 
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// Fused decode over an age-tiered cache: one CTA per (work item, kv head);
-// each warp owns whole key groups, in blocks of up to 32 tokens: one token
-// per lane for the scores (q'.s per channel in shared memory, the lane's
-// row read at the group's width), a per-block online softmax, then the
-// values with the lane owning channels lane*CPL ...: the weighted code sums
-// sum_t p_t s_t,j code_t,c and the zero-point sums sum_t p_t z_t,j.
-template <int D, int GQ>
-__global__ void __launch_bounds__(kThreads)
-k_decode_age(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
-  constexpr int CPL = D / 32;
-  __shared__ float sq[GQ][D];
-  __shared__ __align__(16) float sa[kWarps][GQ][D];
-  __shared__ float sm[kWarps][GQ], sl[kWarps][GQ];
-  __shared__ float so[kWarps][GQ][D];
-  const int item = blockIdx.x, h = blockIdx.y;
-  const int b = find_seq(tab.prefix, geo.B, item);
-  const int k = item - tab.prefix[b];
-  const int g = geo.g, NJ = D / g;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const size_t bh = (size_t)b * geo.H_kv + h;
-  const int S = tab.Tq[b] + tab.nres[b];
-  for (int i = threadIdx.x; i < GQ * D; i += kThreads) {
-    const int hh = i / D, c = i % D;
-    sq[hh][c] = __half2float(args.q[((size_t)b * geo.H_q + h * GQ + hh) * D + c]) *
-                args.scale_log2;
-  }
-  __syncthreads();
-  float m[GQ], l[GQ], o[GQ][CPL];
-#pragma unroll
-  for (int hh = 0; hh < GQ; ++hh) {
-    m[hh] = -INFINITY; l[hh] = 0.f;
-#pragma unroll
-    for (int u = 0; u < CPL; ++u) o[hh][u] = 0.f;
-  }
-  // online softmax of a block (one score per lane, -inf when absent);
-  // returns the lane's weight
-  auto fold = [&](float (&s)[GQ], float (&p)[GQ]) {
-#pragma unroll
-    for (int hh = 0; hh < GQ; ++hh) {
-      float mb = s[hh];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1)
-        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
-      const float mn = fmaxf(m[hh], mb);
-      const float alpha = m[hh] == -INFINITY ? 0.f : exp2f(m[hh] - mn);
-      p[hh] = s[hh] == -INFINITY ? 0.f : exp2f(s[hh] - mn);
-      l[hh] = l[hh] * alpha + warp_sum(p[hh]);
-#pragma unroll
-      for (int u = 0; u < CPL; ++u) o[hh][u] *= alpha;
-      m[hh] = mn;
+// D-byte rows of an AgeTieredKV code plane (the packed row order the oracle
+// and the export use): one thread per 32-bit word of the output.
+__global__ void k_age_export(Geometry geo, const uint8_t *__restrict__ src,
+                             const int8_t *__restrict__ tier, LenTable lens,
+                             uint32_t *__restrict__ dst) {
+  const int D = geo.D, wrow = D / 4;
+  const size_t words = (size_t)geo.B * geo.H_kv * geo.Tcap * wrow;
+  for (size_t x = (size_t)blockIdx.x * blockDim.x + threadIdx.x; x < words;
+       x += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = x / wrow;
+    const int k = (int)(x - r * wrow);
+    const size_t bh = r / geo.Tcap;
+    const int t = (int)(r - bh * geo.Tcap);
+    const int b = (int)(bh / geo.H_kv);
+    uint32_t v = 0;
+    if (t < lens.Tq[b]) {
+      const int G = t / geo.g, i = t - G * geo.g;
+      const int w = age_width(geo, tier[bh * (geo.Tcap / geo.g) + G]);
+      if (k < D * w / 32)
+        v = reinterpret_cast<const uint32_t *>(src + age_row_off(geo, bh, G, i, w))[k];
     }
-  };
-
-  if (k < tab.nq[b]) {
-    const int t0 = k * args.tps, t1 = min(t0 + args.tps, tab.Tq[b]);
-    const int bt = g < 32 ? g : 32;
-    for (int G = t0 / g + warp; G * g < t1; G += kWarps) {
-      const int w = geo.age_bits[age_tier(geo, S, G)];
-      const uint32_t cm = (1u << w) - 1u;
-      const size_t gidx = (bh * (geo.Tcap / g) + G) * D;
-      float beta[GQ];
-      __syncwarp();
-#pragma unroll
-      for (int hh = 0; hh < GQ; ++hh) {
-        float part = 0.f;
-#pragma unroll
-        for (int u = 0; u < CPL; ++u) {
-          const int c = lane * CPL + u;
-          const float qc = sq[hh][c];
-          part = fmaf(qc, __half2float(pl.Kz[gidx + c]), part);
-          sa[warp][hh][c] = qc * __half2float(pl.Ks[gidx + c]);
-        }
-        beta[hh] = warp_sum(part);
-      }
-      __syncwarp();
-      for (int tb = G * g; tb < G * g + g; tb += bt) {
-        float acc[GQ];
-#pragma unroll
-        for (int hh = 0; hh < GQ; ++hh) acc[hh] = 0.f;
-        if (lane < bt) {
-          const uint32_t *row = reinterpret_cast<const uint32_t *>(
-              pl.Kc + (bh * geo.Tcap + tb + lane) * D);
-          // the lane's row at the group's width, the field loop unrolled per
-          // width
-          auto walk = [&](auto w_tag) {
-            constexpr int W = decltype(w_tag)::value, PER = 32 / W;
-            constexpr uint32_t CM = (1u << W) - 1u;
-#pragma unroll 2
-            for (int wi = 0; wi < D * W / 32; ++wi) {
-              const uint32_t x = __ldg(row + wi);
-#pragma unroll
-              for (int e = 0; e < PER; e += 4) {
-#pragma unroll
-                for (int hh = 0; hh < GQ; ++hh) {
-                  const float4 a4 = *reinterpret_cast<const float4 *>(&sa[warp][hh][wi * PER + e]);
-                  float r = acc[hh];
-                  r = fmaf(a4.x, (float)((x >> (W * e)) & CM), r);
-                  r = fmaf(a4.y, (float)((x >> (W * (e + 1))) & CM), r);
-                  r = fmaf(a4.z, (float)((x >> (W * (e + 2))) & CM), r);
-                  r = fmaf(a4.w, (float)((x >> (W * (e + 3))) & CM), r);
-                  acc[hh] = r;
-                }
-              }
-            }
-          };
-          if (w == 2) walk(std::integral_constant<int, 2>{});
-          else if (w == 4) walk(std::integral_constant<int, 4>{});
-          else walk(std::integral_constant<int, 8>{});
-        }
-        float s[GQ], p[GQ];
-#pragma unroll
-        for (int hh = 0; hh < GQ; ++hh) s[hh] = lane < bt ? acc[hh] + beta[hh] : -INFINITY;
-        fold(s, p);
-        // values: o_c += sum_t p_t (code_tc s_tj + z_tj)
-        const int c0 = lane * CPL, j = c0 / g;
-#pragma unroll 8
-        for (int jj = 0; jj < bt; ++jj) {
-          const size_t r = bh * geo.Tcap + tb + jj;
-          const float vs = __half2float(pl.Vs[r * NJ + j]);
-          const float vz = __half2float(pl.Vz[r * NJ + j]);
-          // the lane's CPL codes: CPL * w bits at bit c0 * w of the row
-          const int bit = c0 * w;
-          uint32_t x;
-          if (CPL * w <= 8) x = pl.Vc[r * D + (bit >> 3)] >> (bit & 7);
-          else if (CPL * w <= 16) x = *reinterpret_cast<const uint16_t *>(pl.Vc + r * D + (bit >> 3));
-          else x = *reinterpret_cast<const uint32_t *>(pl.Vc + r * D + (bit >> 3));
-          float v[CPL];
-#pragma unroll
-          for (int u = 0; u < CPL; ++u) v[u] = fmaf((float)((x >> (w * u)) & cm), vs, vz);
-#pragma unroll
-          for (int hh = 0; hh < GQ; ++hh) {
-            const float pj = __shfl_sync(0xffffffffu, p[hh], jj);
-#pragma unroll
-            for (int u = 0; u < CPL; ++u) o[hh][u] = fmaf(pj, v[u], o[hh][u]);
-          }
-        }
-      }
-    }
-  } else {
-    const int Tq = tab.Tq[b];
-    for (int i0 = warp * 32; i0 < tab.nres[b]; i0 += kWarps * 32) {
-      const int i = i0 + lane;
-      const bool ok = i < tab.nres[b];
-      const __half *kr = pl.Kr + (bh * geo.Rcap + (Tq + (ok ? i : i0)) % geo.Rcap) * D;
-      float acc[GQ];
-#pragma unroll
-      for (int hh = 0; hh < GQ; ++hh) acc[hh] = 0.f;
-#pragma unroll 4
-      for (int c = 0; c < D; c += 2) {
-        const float2 kv = __half22float2(*reinterpret_cast<const __half2 *>(kr + c));
-#pragma unroll
-        for (int hh = 0; hh < GQ; ++hh)
-          acc[hh] = fmaf(sq[hh][c], kv.x, fmaf(sq[hh][c + 1], kv.y, acc[hh]));
-      }
-      float s[GQ], p[GQ];
-#pragma unroll
-      for (int hh = 0; hh < GQ; ++hh) s[hh] = ok ? acc[hh] : -INFINITY;
-      fold(s, p);
-      const int nb = min(32, tab.nres[b] - i0);
-      for (int jj = 0; jj < nb; ++jj) {
-        const __half *vr = pl.Vr + (bh * geo.Rcap + (Tq + i0 + jj) % geo.Rcap) * D + lane * CPL;
-        float v[CPL];
-#pragma unroll
-        for (int u = 0; u < CPL; ++u) v[u] = __half2float(vr[u]);
-#pragma unroll
-        for (int hh = 0; hh < GQ; ++hh) {
-          const float pj = __shfl_sync(0xffffffffu, p[hh], jj);
-#pragma unroll
-          for (int u = 0; u < CPL; ++u) o[hh][u] = fmaf(pj, v[u], o[hh][u]);
-        }
-      }
-    }
-  }
-
-#pragma unroll
-  for (int hh = 0; hh < GQ; ++hh) {
-    if (lane == 0) { sm[warp][hh] = m[hh]; sl[warp][hh] = l[hh]; }
-#pragma unroll
-    for (int u = 0; u < CPL; ++u) so[warp][hh][lane * CPL + u] = o[hh][u];
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < GQ * (D + 2); i += kThreads) {
-    const int hh = i / (D + 2), c = i % (D + 2);
-    float M = -INFINITY;
-    for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, sm[ww][hh]);
-    float acc = 0.f;
-    for (int ww = 0; ww < kWarps; ++ww) {
-      const float f = sm[ww][hh] == -INFINITY ? 0.f : exp2f(sm[ww][hh] - M);
-      acc += f * (c < D ? so[ww][hh][c] : sl[ww][hh]);
-    }
-    const int hq = h * GQ + hh;
-    float *dst = pl.part + (((size_t)b * geo.H_q + hq) * geo.max_items + k) * (D + 2);
-    dst[c] = c == D ? M : acc;
+    dst[x] = v;
   }
 }
 
 }  // namespace
+
+using agedec::AgeKernel;
+
+static AgeKernel pick_age_kernel(const Geometry &geo) {
+  const int gq = geo.H_q / geo.H_kv;
+  if (geo.D == 64) return agedec::pick_d64(gq);
+  if (geo.D == 128) return agedec::pick_d128(gq);
+  return {};
+}
 
 cudaError_t launch_age_flush(const Geometry &geo, const Planes &pl,
                              const __half *Kin, const __half *Vin,
@@ -391,24 +225,55 @@ cudaError_t launch_age_flush(const Geometry &geo, const Planes &pl,
   return cudaGetLastError();
 }
 
+cudaError_t launch_age_export(const Geometry &geo, const Planes &pl, bool values,
+                              void *dst, const int32_t *Tq, cudaStream_t st) {
+  LenTable lens;
+  for (int b = 0; b < geo.B; ++b) { lens.Tq[b] = Tq[b]; lens.nres[b] = 0; }
+  k_age_export<<<1024, 256, 0, st>>>(geo, values ? pl.Vc : pl.Kc, pl.tier, lens,
+                                     (uint32_t *)dst);
+  count_launch();
+  return cudaGetLastError();
+}
+
+int age_decode_ctas_per_sm(const Geometry &geo) {
+  const AgeKernel kf = pick_age_kernel(geo);
+  return kf.occ > 0 ? kf.occ : 1;
+}
+
+// The split is planned for one wave: a launch of fewer CTAs than the SMs
+// hold would let the block scheduler stack some SMs fuller than others, so
+// the dynamic shared memory request is padded until an SM holds at most
+// ceil(CTAs / SMs) of them.
 cudaError_t launch_decode_age(const Geometry &geo, const Planes &pl,
                               const DecodeArgs &args, const DecodeTable &tab,
                               cudaStream_t st) {
   if (args.total_items > 0) {
-    dim3 grid(args.total_items, geo.H_kv);
-    const int gq = geo.H_q / geo.H_kv;
-#define VQK_AGE(DD, QQ)                                                   \
-  if (geo.D == DD && gq == QQ) {                                          \
-    k_decode_age<DD, QQ><<<grid, kThreads, 0, st>>>(geo, pl, args, tab); \
-  } else
-#define VQK_AGE_D(DD) VQK_AGE(DD, 1) VQK_AGE(DD, 2) VQK_AGE(DD, 3) VQK_AGE(DD, 4) \
-  VQK_AGE(DD, 5) VQK_AGE(DD, 6) VQK_AGE(DD, 7) VQK_AGE(DD, 8)
-    VQK_AGE_D(64) VQK_AGE_D(128)
-    { return cudaErrorInvalidValue; }
-#undef VQK_AGE_D
-#undef VQK_AGE
+    const AgeKernel kf = pick_age_kernel(geo);
+    if (!kf.f) return cudaErrorInvalidValue;
+    int dev = 0, sms = 0, smem_sm = 0, reserved = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+      e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e == cudaSuccess)
+      e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    if (e != cudaSuccess) return e;
+    const int64_t ctas = (int64_t)args.total_items * geo.H_kv;
+    const int64_t occ = (ctas + sms - 1) / (sms > 0 ? sms : 1);
+    size_t smem = (size_t)kf.smem;
+    if (occ >= 1 && occ < kf.occ) {
+      const int64_t per = ((int64_t)smem_sm / occ - reserved - kf.smem_static) / 128 * 128;
+      if (per > (int64_t)smem) smem = (size_t)per;
+    }
+    Geometry g2 = geo;
+    Planes p2 = pl;
+    DecodeArgs a2 = args;
+    DecodeTable t2 = tab;
+    void *params[] = {&g2, &p2, &a2, &t2};
+    e = cudaLaunchKernel(kf.f, dim3(args.total_items, geo.H_kv),
+                         dim3(agedec::kDecodeThreads), params, smem, st);
     count_launch();
-    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   return launch_combine(geo, pl, args, tab, st);

@@ -1,0 +1,11 @@
+// AgeTieredKV fused decode, D = 128: the instances for 1 ... 8 query heads
+// per kv head (a translation unit of their own, compiled in parallel).
+#include "age_decode.cuh"
+
+namespace vqk {
+namespace agedec {
+
+AgeKernel pick_d128(int gq) { return pick<128>(gq); }
+
+}  // namespace agedec
+}  // namespace vqk

@@ -32,6 +32,10 @@ struct vq_kivi_cache {
   MmaPlan plan;
   unsigned *err;          // device word set by a kernel whose wait gave up
   int32_t S[kMaxB], Tq[kMaxB], nres[kMaxB];
+  // AgeTieredKV: the automatic split last planned and the T_q it was
+  // planned for (the plan is a search, redone when a flush moves T_q)
+  int32_t age_tps;
+  int32_t age_Tq[kMaxB];
 };
 
 namespace {
@@ -501,11 +505,48 @@ int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
   for (int b = 0; b < p.B; ++b) total_tq += c->Tq[b];
   int32_t tps = c->split_tokens;
   const int32_t unit = split_unit(p.group);
-  if (tps == 0) {
-    // Kitty and AgeTieredKV caches (one token per lane, loads in flight
-    // limited by the block): more, shorter items keep more of them per SM
-    const int64_t target_items =
-        (c->geo.kitty || c->geo.age_b1 > 0 ? 16LL : 4LL) * c->sm_count;
+  if (tps == 0 && c->geo.age_b1 > 0) {
+    // AgeTieredKV: one wave of CTAs, each streaming its groups through
+    // per-warp pipelines (a CTA's start costs a pipeline fill, so items are
+    // long); a sequence's last item also takes its residual window.  Among
+    // the splits whose items fit one wave, take the one with the fewest
+    // tokens on the busiest SM, ceil(items / SMs) items of tps tokens (the
+    // launcher caps the CTAs per SM at that count).
+    if (c->age_tps > 0 && !memcmp(c->age_Tq, c->Tq, sizeof(int32_t) * p.B)) {
+      tps = c->age_tps;
+    } else {
+      const int64_t sms = c->sm_count;
+      const int64_t cap = (int64_t)age_decode_ctas_per_sm(c->geo) * sms;
+      auto items = [&](int64_t t) {
+        int64_t n = 0;
+        for (int b = 0; b < p.B; ++b) {
+          const int64_t nq = (c->Tq[b] + t - 1) / t;
+          n += nq > 0 ? nq : (c->nres[b] > 0 ? 1 : 0);
+        }
+        return n * p.H_kv;
+      };
+      int32_t tq_max = 1;
+      for (int b = 0; b < p.B; ++b) tq_max = c->Tq[b] > tq_max ? c->Tq[b] : tq_max;
+      const int64_t t_top = (int64_t)round_up((size_t)tq_max, unit);
+      int64_t t = (total_tq * p.H_kv + cap - 1) / (cap > 0 ? cap : 1);
+      t = (int64_t)round_up((size_t)(t > 1 ? t : 1), unit);
+      // more (sequence, head) pairs than CTA slots: one item each
+      while (items(t) > cap && t < t_top) t += unit;
+      int64_t best = t, best_cost = -1;
+      for (int i = 0; i < 64; ++i, t += unit) {
+        const int64_t n = items(t);
+        const int64_t cost = (n + sms - 1) / sms * (t + 64);
+        if (best_cost < 0 || cost < best_cost) { best = t; best_cost = cost; }
+        if (n <= p.H_kv) break;   // one item per sequence and head
+      }
+      tps = (int32_t)best;
+      c->age_tps = tps;
+      memcpy(c->age_Tq, c->Tq, sizeof(int32_t) * p.B);
+    }
+  } else if (tps == 0) {
+    // Kitty caches (one token per lane, loads in flight limited by the
+    // block): more, shorter items keep more of them per SM
+    const int64_t target_items = (c->geo.kitty ? 16LL : 4LL) * c->sm_count;
     int64_t t = (total_tq * p.H_kv + target_items - 1) / target_items;
     tps = (int32_t)round_up((size_t)(t > 1 ? t : 1), unit);
   }
@@ -513,11 +554,19 @@ int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
 
   DecodeTable tab;
   tab.prefix[0] = 0;
+  const bool aged = c->geo.age_b1 > 0;
   for (int b = 0; b < p.B; ++b) {
     tab.Tq[b] = c->Tq[b];
     tab.nres[b] = c->nres[b];
     tab.nq[b] = (c->Tq[b] + tps - 1) / tps;
-    tab.prefix[b + 1] = tab.prefix[b] + tab.nq[b] + (c->nres[b] > 0 ? 1 : 0);
+    if (aged) {
+      // the last quantized item takes the residual window (an item of its
+      // own when there is no quantized token)
+      if (tab.nq[b] == 0 && c->nres[b] > 0) tab.nq[b] = 1;
+      tab.prefix[b + 1] = tab.prefix[b] + tab.nq[b];
+    } else {
+      tab.prefix[b + 1] = tab.prefix[b] + tab.nq[b] + (c->nres[b] > 0 ? 1 : 0);
+    }
   }
   DecodeArgs args;
   args.q = (const __half *)q;
@@ -525,6 +574,7 @@ int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
   args.scale_log2 = scale * 1.4426950408889634f;
   args.tps = tps;
   args.total_items = tab.prefix[p.B];
+  args.err = c->err;
   cudaError_t e = launch_decode(c->geo, c->pl, args, tab, st);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
   c->last_stream = st;
@@ -664,7 +714,9 @@ int vq_kivi_export(const vq_kivi_cache *c, int which, void *dst,
     default: break;
   }
   cudaError_t e;
-  if ((which == 0 || which == 3) && c->geo.layout == kLayoutFrag && !c->geo.kitty) {
+  if ((which == 0 || which == 3) && c->geo.age_b1 > 0) {
+    e = launch_age_export(c->geo, c->pl, which == 3, dst, c->Tq, st);
+  } else if ((which == 0 || which == 3) && c->geo.layout == kLayoutFrag && !c->geo.kitty) {
     e = launch_export_frag(c->geo, (const uint8_t *)src, which == 3, dst, st);
   } else if (src) {
     e = cudaMemcpyAsync(dst, src, need, cudaMemcpyDeviceToDevice, st);

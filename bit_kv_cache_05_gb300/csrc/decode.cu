@@ -52,6 +52,8 @@ k_decode_split(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
   __shared__ float sq[GQ][D];
   __shared__ float sm[kWarps][GQ], sl[kWarps][GQ];
   __shared__ float so[kWarps][GQ][D];
+  // the combine kernel behind this one waits for its completion
+  asm volatile("griddepcontrol.launch_dependents;");
 
   const int item = blockIdx.x, h = blockIdx.y;
   const int b = find_seq(tab.prefix, geo.B, item);
@@ -207,22 +209,62 @@ k_decode_split(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
   }
 }
 
-// out[b][hq] = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k
-__global__ void k_combine(Geometry geo, Planes pl, DecodeArgs args,
-                          DecodeTable tab) {
+// out[b][hq] = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k over the n
+// split partials of (b, hq).  Launched as a programmatic dependent of the
+// decode kernel (which releases it early): it waits for the partials, then
+// reads the n (m_k, l_k) pairs at once, builds the weights 2^(m_k - M) in
+// shared memory, and reads the partial rows with every load in flight.
+constexpr int kCombineThreads = 128;
+
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float *red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float x = __shfl_xor_sync(0xffffffffu, v, o);
+    v = is_max ? fmaxf(v, x) : v + x;
+  }
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  v = red[0];
+  for (int w = 1; w < kCombineThreads / 32; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
+  __syncthreads();
+  return v;
+}
+
+__global__ void __launch_bounds__(kCombineThreads)
+k_combine(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
+  extern __shared__ float fw[];                  // [max_items] weights
+  __shared__ float red[kCombineThreads / 32];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   const int b = blockIdx.x / geo.H_q, hq = blockIdx.x % geo.H_q;
-  const int D = geo.D;
+  const int D = geo.D, P = D + 2;
   const int n = tab.prefix[b + 1] - tab.prefix[b];
-  const float *base = pl.part + ((size_t)b * geo.H_q + hq) * geo.max_items * (D + 2);
-  float M = -INFINITY;
-  for (int k = 0; k < n; ++k) M = fmaxf(M, base[k * (D + 2) + D]);
-  float L = 0.f;
-  for (int k = 0; k < n; ++k)
-    L += exp2f(base[k * (D + 2) + D] - M) * base[k * (D + 2) + D + 1];
-  for (int c = threadIdx.x; c < D; c += blockDim.x) {
-    float acc = 0.f;
-    for (int k = 0; k < n; ++k)
-      acc += exp2f(base[k * (D + 2) + D] - M) * base[k * (D + 2) + c];
+  const float *base = pl.part + ((size_t)b * geo.H_q + hq) * geo.max_items * P;
+  float mloc = -INFINITY;
+  for (int k = threadIdx.x; k < n; k += kCombineThreads) {
+    fw[k] = __ldcg(base + (size_t)k * P + D);
+    mloc = fmaxf(mloc, fw[k]);
+  }
+  const float M = block_reduce(mloc, true, red);
+  float lloc = 0.f;
+  for (int k = threadIdx.x; k < n; k += kCombineThreads) {
+    const float f = fw[k] == -INFINITY ? 0.f : exp2f(fw[k] - M);
+    lloc += f * __ldcg(base + (size_t)k * P + D + 1);
+    fw[k] = f;
+  }
+  const float L = block_reduce(lloc, false, red);   // its barriers publish fw
+  for (int c = threadIdx.x; c < D; c += kCombineThreads) {
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    int k = 0;
+    for (; k + 4 <= n; k += 4) {
+      a0 = fmaf(fw[k], __ldcg(base + (size_t)k * P + c), a0);
+      a1 = fmaf(fw[k + 1], __ldcg(base + (size_t)(k + 1) * P + c), a1);
+      a2 = fmaf(fw[k + 2], __ldcg(base + (size_t)(k + 2) * P + c), a2);
+      a3 = fmaf(fw[k + 3], __ldcg(base + (size_t)(k + 3) * P + c), a3);
+    }
+    for (; k < n; ++k) a0 = fmaf(fw[k], __ldcg(base + (size_t)k * P + c), a0);
+    const float acc = (a0 + a1) + (a2 + a3);
     args.out[((size_t)b * geo.H_q + hq) * D + c] = n ? acc / L : 0.f;
   }
 }
@@ -255,9 +297,10 @@ cudaError_t launch_decode(const Geometry &geo, const Planes &pl,
 cudaError_t launch_combine(const Geometry &geo, const Planes &pl,
                            const DecodeArgs &args, const DecodeTable &tab,
                            cudaStream_t st) {
-  k_combine<<<geo.B * geo.H_q, min(geo.D, 256), 0, st>>>(geo, pl, args, tab);
+  cudaError_t e = launch_pdl(k_combine, dim3(geo.B * geo.H_q), dim3(kCombineThreads),
+                             sizeof(float) * geo.max_items, st, geo, pl, args, tab);
   count_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace vqk

@@ -186,6 +186,8 @@ k_decode_kitty(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
   __shared__ __align__(16) float sa[kWarps][GQ][D]; // a in field order
   __shared__ float sm[kWarps][GQ], sl[kWarps][GQ];
   __shared__ float so[kWarps][GQ][D];
+  // the combine kernel behind this one waits for its completion
+  asm volatile("griddepcontrol.launch_dependents;");
   const int item = blockIdx.x, h = blockIdx.y;
   const int b = find_seq(tab.prefix, geo.B, item);
   const int k = item - tab.prefix[b];

@@ -37,23 +37,6 @@ __device__ __forceinline__ void pdl_wait_and_release() {
   asm volatile("griddepcontrol.launch_dependents;");
 }
 
-// launch with programmatic stream serialization
-template <typename... P, typename... A>
-cudaError_t launch_pdl(void (*fn)(P...), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t st, A... args) {
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fn, args...);
-}
-
 __device__ __forceinline__ uint32_t quant_code(float x, float mn, float scale,
                                                int levels) {
   if (scale == 0.0f) return 0u;
@@ -612,11 +595,6 @@ k_tail(Geometry geo, Planes pl, const __half *__restrict__ Kin,
   *reinterpret_cast<uint4 *>(pl.Vr + dst) =
       *reinterpret_cast<const uint4 *>(Vin + src);
 }
-
-struct LenTable {
-  int32_t Tq[kMaxB];
-  int32_t nres[kMaxB];
-};
 
 // Residual ring -> canonical linear layout (slot i = token T_q + i), zero
 // beyond n_res.  One block per (slot, b*H_kv + h).

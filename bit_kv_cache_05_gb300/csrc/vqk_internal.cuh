@@ -58,8 +58,9 @@ struct Geometry {
   int kitty_hi = 0;             // Kitty: 4-bit channels per key group
   // AgeTieredKV (age_b1 > 0): a group whose newest token has fewer than
   // age_b1 newer tokens is stored at age_bits[0], fewer than age_b2 at
-  // age_bits[1], else at age_bits[2]; rows are D bytes (the widest width),
-  // the codes in their leading D * bits / 8 bytes
+  // age_bits[1], else at age_bits[2].  A group owns g * D bytes of a code
+  // plane (its rows at the widest width); at width w its g rows are packed
+  // densely in the leading g * D * w / 8 bytes (age_row_off)
   int age_b1 = 0, age_b2 = 0;
   int age_bits[3] = {0, 0, 0};
 };
@@ -68,6 +69,22 @@ struct Geometry {
 __host__ __device__ inline int age_tier(const Geometry &geo, int S, int G) {
   const int age = S - (G + 1) * geo.g;
   return age < geo.age_b1 ? 0 : (age < geo.age_b2 ? 1 : 2);
+}
+
+// width of AgeTieredKV tier t (selects, so that a kernel does not index its
+// parameter block at run time)
+__host__ __device__ inline int age_width(const Geometry &geo, int t) {
+  return t == 0 ? geo.age_bits[0] : (t == 1 ? geo.age_bits[1] : geo.age_bits[2]);
+}
+
+// Byte offset in an AgeTieredKV code plane of row i (0 <= i < g) of group G
+// of (sequence, kv head) bh, the group stored at width w: the group's block
+// starts at its first token's row of D bytes, its rows follow at D * w / 8
+// bytes (LSB-first codes, as a packed row).  The export expands them to
+// D-byte rows.
+__host__ __device__ inline size_t age_row_off(const Geometry &geo, size_t bh,
+                                              int G, int i, int w) {
+  return (bh * geo.Tcap + (size_t)G * geo.g) * geo.D + (size_t)i * (geo.D * w / 8);
 }
 
 // One AgeTieredKV flush: per sequence b, new groups [gn0, gn1) quantized
@@ -226,6 +243,12 @@ cudaError_t launch_export_residual(const Geometry &geo, const Planes &pl,
 // Work list of one decode: for sequence b, items prefix[b] ... prefix[b+1]-1;
 // local item k < nq[b] covers quantized tokens [k*tps, min((k+1)*tps, Tq[b])),
 // local item k == nq[b] (present when nres[b] > 0) covers the residual.
+// per sequence: quantized tokens and residual-window tokens
+struct LenTable {
+  int32_t Tq[kMaxB];
+  int32_t nres[kMaxB];
+};
+
 struct DecodeTable {
   int32_t prefix[kMaxB + 1];
   int32_t Tq[kMaxB];
@@ -239,6 +262,7 @@ struct DecodeArgs {
   float scale_log2; // softmax scale * log2(e)
   int tps;          // quantized tokens per split item
   int total_items;
+  unsigned *err = nullptr;  // set to nonzero when a pipeline wait gave up
 };
 
 cudaError_t launch_decode(const Geometry &geo, const Planes &pl,
@@ -265,6 +289,14 @@ cudaError_t launch_flush_kitty(const Geometry &geo, const Planes &pl,
 cudaError_t launch_decode_kitty(const Geometry &geo, const Planes &pl,
                                 const DecodeArgs &args, const DecodeTable &tab,
                                 cudaStream_t st);
+// CTAs of the AgeTieredKV decode resident per SM (its split is planned
+// for one wave)
+int age_decode_ctas_per_sm(const Geometry &geo);
+// plane 0 (keys) or 3 (values) of an AgeTieredKV cache in D-byte rows (the
+// packed row order): token t < T_q of each sequence holds its codes in the
+// leading D * w / 8 bytes, zeros after them; rows t >= T_q are zero
+cudaError_t launch_age_export(const Geometry &geo, const Planes &pl, bool values,
+                              void *dst, const int32_t *Tq, cudaStream_t st);
 // decode over an AgeTieredKV cache (tables as the CUDA-core decode); S =
 // Tq + nres of a sequence gives every group's tier (age.cu)
 cudaError_t launch_decode_age(const Geometry &geo, const Planes &pl,
@@ -339,6 +371,26 @@ cudaError_t launch_attend_multi(const Geometry &geo, const Planes &pl,
 
 // counts every kernel launch made by the library
 void count_launch(int n = 1);
+
+// launch with programmatic stream serialization: the kernel may be
+// scheduled once the stream's previous kernel has released its dependents
+// (griddepcontrol.launch_dependents), and waits for that kernel's writes
+// with griddepcontrol.wait
+template <typename... P, typename... A>
+cudaError_t launch_pdl(void (*fn)(P...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, A... args) {
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, args...);
+}
 
 // sets the message vq_kivi_last_error() returns on the calling thread
 void set_last_error(const char *msg);

@@ -49,20 +49,29 @@ def _planes_equal(c, oc, g):
 
 
 CASES = [
-    # recipe, lengths, residual, (recent, mid, bits)
-    ("pages_S512", [1500, 700], 0, (128, 1024, 8, 4, 2)),
-    ("gqa_serving", [1300, 260, 40], 32, (128, 1024, 8, 4, 2)),
-    ("tiny", [400, 333], 0, (64, 192, 8, 4, 2)),
-    ("pages_S512", [900], 0, (96, 512, 4, 4, 2)),
+    # recipe, lengths, residual, (recent, mid, bits), group (None: the recipe's)
+    ("pages_S512", [1500, 700], 0, (128, 1024, 8, 4, 2), None),
+    ("gqa_serving", [1300, 260, 40], 32, (128, 1024, 8, 4, 2), None),
+    ("tiny", [400, 333], 0, (64, 192, 8, 4, 2), None),
+    ("pages_S512", [900], 0, (96, 512, 4, 4, 2), None),
+    # groups of 64 (two or four staged blocks per group), of 16 (blocks of
+    # one group), of 128; every tier at 8 bits (16-token blocks throughout)
+    ("pages_S512", [1100, 600], 0, (128, 512, 8, 4, 2), 64),
+    ("tiny", [300, 170], 16, (32, 96, 8, 4, 2), 16),
+    ("gqa_serving", [900, 300], 32, (128, 256, 4, 2, 2), 128),
+    ("pages_S512", [700], 0, (64, 256, 8, 8, 8), None),
 ]
 
 
-@pytest.mark.parametrize("name,lens,R,age", CASES,
-                         ids=[f"{c[0]}-{c[3][0]}-{c[3][2]}{c[3][3]}{c[3][4]}" for c in CASES])
-def test_age_planes_and_decode(lib, name, lens, R, age):
+@pytest.mark.parametrize("name,lens,R,age,group", CASES,
+                         ids=[f"{c[0]}-{c[3][0]}-{c[3][2]}{c[3][3]}{c[3][4]}-g{c[4]}"
+                              for c in CASES])
+def test_age_planes_and_decode(lib, name, lens, R, age, group):
     import oracle
     from bit_kv_cache_05_gb300.cache import KiviCache
     w = synth.shrink(synth.workload(name), lens, n_append=0)
+    if group is not None:
+        w = synth.dataclasses.replace(w, group=group)
     inp = synth.make_inputs(w, seed=70, device="cpu")
     c = KiviCache(inp["K"].cuda(), inp["V"].cuda(), w.seq_lens, H_q=w.H_q,
                   bits=8, group=w.group, residual=R, max_seq=w.max_seq, age=age)
