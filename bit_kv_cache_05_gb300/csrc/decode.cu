@@ -211,10 +211,13 @@ k_decode_split(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
 
 // out[b][hq] = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k over the n
 // split partials of (b, hq).  Launched as a programmatic dependent of the
-// decode kernel (which releases it early): it waits for the partials, then
-// reads the n (m_k, l_k) pairs at once, builds the weights 2^(m_k - M) in
-// shared memory, and reads the partial rows with every load in flight.
-constexpr int kCombineThreads = 128;
+// decode kernel (which releases it early): it waits for the partials, reads
+// the n (m_k, l_k) pairs at once and builds the weights 2^(m_k - M) in
+// shared memory; then warp w sums the partial rows w, w + 8, ... (lanes
+// over channel pairs, four rows in flight per warp) and the warps' sums are
+// added in shared memory.
+constexpr int kCombineWarps = 8;
+constexpr int kCombineThreads = kCombineWarps * 32;
 
 __device__ __forceinline__ float block_reduce(float v, bool is_max, float *red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -226,19 +229,22 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float *red) 
   if (lane == 0) red[warp] = v;
   __syncthreads();
   v = red[0];
-  for (int w = 1; w < kCombineThreads / 32; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
+  for (int w = 1; w < kCombineWarps; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
   __syncthreads();
   return v;
 }
 
 __global__ void __launch_bounds__(kCombineThreads)
 k_combine(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
-  extern __shared__ float fw[];                  // [max_items] weights
-  __shared__ float red[kCombineThreads / 32];
+  extern __shared__ float csm[];   // weights [max_items], then [8][D] sums
+  __shared__ float red[kCombineWarps];
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   const int b = blockIdx.x / geo.H_q, hq = blockIdx.x % geo.H_q;
-  const int D = geo.D, P = D + 2;
+  const int D = geo.D, P = D + 2, PPL = D / 64;   // channel pairs per lane
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float *fw = csm;
+  float *ws = csm + ((geo.max_items + 1) & ~1);   // 8-byte aligned
   const int n = tab.prefix[b + 1] - tab.prefix[b];
   const float *base = pl.part + ((size_t)b * geo.H_q + hq) * geo.max_items * P;
   float mloc = -INFINITY;
@@ -254,18 +260,36 @@ k_combine(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
     fw[k] = f;
   }
   const float L = block_reduce(lloc, false, red);   // its barriers publish fw
-  for (int c = threadIdx.x; c < D; c += kCombineThreads) {
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-    int k = 0;
-    for (; k + 4 <= n; k += 4) {
-      a0 = fmaf(fw[k], __ldcg(base + (size_t)k * P + c), a0);
-      a1 = fmaf(fw[k + 1], __ldcg(base + (size_t)(k + 1) * P + c), a1);
-      a2 = fmaf(fw[k + 2], __ldcg(base + (size_t)(k + 2) * P + c), a2);
-      a3 = fmaf(fw[k + 3], __ldcg(base + (size_t)(k + 3) * P + c), a3);
+  float2 acc[4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) acc[p] = make_float2(0.f, 0.f);
+  for (int k0 = warp; k0 < n; k0 += 4 * kCombineWarps) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int k = k0 + u * kCombineWarps;
+      if (k < n) {
+        const float f = fw[k];
+        const float2 *row = reinterpret_cast<const float2 *>(base + (size_t)k * P);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          if (p < PPL) {
+            const float2 v = __ldcg(row + lane + 32 * p);
+            acc[p].x = fmaf(f, v.x, acc[p].x);
+            acc[p].y = fmaf(f, v.y, acc[p].y);
+          }
+        }
+      }
     }
-    for (; k < n; ++k) a0 = fmaf(fw[k], __ldcg(base + (size_t)k * P + c), a0);
-    const float acc = (a0 + a1) + (a2 + a3);
-    args.out[((size_t)b * geo.H_q + hq) * D + c] = n ? acc / L : 0.f;
+  }
+#pragma unroll
+  for (int p = 0; p < 4; ++p)
+    if (p < PPL) reinterpret_cast<float2 *>(ws + warp * D)[lane + 32 * p] = acc[p];
+  __syncthreads();
+  for (int c = threadIdx.x; c < D; c += kCombineThreads) {
+    float o = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w) o += ws[w * D + c];
+    args.out[((size_t)b * geo.H_q + hq) * D + c] = n ? o / L : 0.f;
   }
 }
 
@@ -298,7 +322,8 @@ cudaError_t launch_combine(const Geometry &geo, const Planes &pl,
                            const DecodeArgs &args, const DecodeTable &tab,
                            cudaStream_t st) {
   cudaError_t e = launch_pdl(k_combine, dim3(geo.B * geo.H_q), dim3(kCombineThreads),
-                             sizeof(float) * geo.max_items, st, geo, pl, args, tab);
+                             sizeof(float) * (geo.max_items + 1 + kCombineWarps * geo.D), st,
+                             geo, pl, args, tab);
   count_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }

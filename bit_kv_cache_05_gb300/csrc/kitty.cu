@@ -45,47 +45,84 @@ __device__ __forceinline__ const __half *src_row(const Geometry &geo, const Plan
                    : in + (bh * in_stride + (p - split)) * geo.D;
 }
 
-// One CTA per (kv head, sequence), one thread per channel: walks the groups
-// this flush quantizes, in token order, adding each group's keys to the
-// running sums and ranking the channels after each group.
-__global__ void k_kitty_rank(Geometry geo, Planes pl, const __half *__restrict__ Kin,
-                             int64_t in_stride, FlushTable tab) {
-  __shared__ unsigned long long vlo[kMaxD], vhi[kMaxD];
-  const int h = blockIdx.x, b = blockIdx.y, c = threadIdx.x;
-  const int D = geo.D, g = geo.g;
+// One CTA of kRankThreads per (kv head, sequence): NS = kRankThreads / D
+// slices of one thread per channel take NS consecutive groups of this
+// flush at a time.  Each slice sums its group's keys (m and m^2 per
+// channel, its rows' loads all in flight), the slices' sums are carried in
+// shared memory (slice j adds slices 0 ... j to the running sums), and
+// every slice ranks its channels by the running variance through its
+// group's last token.
+constexpr int kRankThreads = 1024;
+
+__global__ void __launch_bounds__(kRankThreads)
+k_kitty_rank(Geometry geo, Planes pl, const __half *__restrict__ Kin,
+             int64_t in_stride, FlushTable tab) {
+  extern __shared__ unsigned long long rsm[];
+  const int D = geo.D, g = geo.g, NS = kRankThreads / D;
+  const int c = threadIdx.x % D, sl = threadIdx.x / D;
+  // per (slice, channel): the group's sums, then the running variance
+  unsigned long long *q1 = rsm, *q2lo = q1 + NS * D, *q2hi = q2lo + NS * D;
+  unsigned long long *vlo = q2hi + NS * D, *vhi = vlo + NS * D;
+  const int h = blockIdx.x, b = blockIdx.y;
   const int n = tab.prefix[b + 1] - tab.prefix[b];
   if (n == 0) return;
   const size_t bh = (size_t)b * geo.H_kv + h;
   long long s1 = pl.ksum[bh * D + c];
   u128 s2 = ((u128)pl.ksq[(bh * D + c) * 2 + 1] << 64) | pl.ksq[(bh * D + c) * 2];
   const int split = tab.src_split[b];
-  for (int k = 0; k < n; ++k) {
+  for (int k0 = 0; k0 < n; k0 += NS) {
+    const int k = k0 + sl;
     const int P0 = tab.first_pos[b] + k * g;
-    for (int i = 0; i < g; ++i) {
-      const __half *row = src_row(geo, pl, Kin, in_stride, bh, P0 + i, split);
-      const long long m = f16_units(__half_as_ushort(row[c]));
-      s1 += m;
-      s2 += (u128)((__int128)m * m);
+    long long g1 = 0;
+    u128 g2 = 0;
+    if (k < n) {
+#pragma unroll 8
+      for (int i = 0; i < g; ++i) {
+        const __half *row = src_row(geo, pl, Kin, in_stride, bh, P0 + i, split);
+        const long long m = f16_units(__half_as_ushort(row[c]));
+        g1 += m;
+        g2 += (u128)((__int128)m * m);
+      }
     }
-    const u128 N = (u128)(P0 + g);
-    const u128 a = (u128)(s1 < 0 ? -s1 : s1);
-    const u128 var = N * s2 - a * a;
-    vlo[c] = (unsigned long long)var;
-    vhi[c] = (unsigned long long)(var >> 64);
+    q1[sl * D + c] = (unsigned long long)g1;
+    q2lo[sl * D + c] = (unsigned long long)g2;
+    q2hi[sl * D + c] = (unsigned long long)(g2 >> 64);
     __syncthreads();
-    int rank = 0;
-    for (int o = 0; o < D; ++o) {
-      const u128 vo = ((u128)vhi[o] << 64) | vlo[o];
-      rank += (vo > var || (vo == var && o < c)) ? 1 : 0;
+    // running sums through this slice's group (r), and through all NS
+    // groups (the next step's start)
+    long long r1 = 0;
+    u128 r2 = 0;
+    for (int j = 0; j < NS; ++j) {
+      s1 += (long long)q1[j * D + c];
+      s2 += ((u128)q2hi[j * D + c] << 64) | q2lo[j * D + c];
+      if (j == sl) { r1 = s1; r2 = s2; }
     }
-    const unsigned word = __ballot_sync(0xffffffffu, rank < geo.kitty_hi);
-    if ((c & 31) == 0)
-      pl.kmask[(bh * (geo.Tcap / g) + P0 / g) * (D / 32) + (c >> 5)] = word;
+    u128 var = 0;
+    if (k < n) {
+      const u128 N = (u128)(P0 + g);
+      const u128 a = (u128)(r1 < 0 ? -r1 : r1);
+      var = N * r2 - a * a;
+    }
+    vlo[sl * D + c] = (unsigned long long)var;
+    vhi[sl * D + c] = (unsigned long long)(var >> 64);
+    __syncthreads();
+    if (k < n) {
+      int rank = 0;
+      for (int o = 0; o < D; ++o) {
+        const u128 vo = ((u128)vhi[sl * D + o] << 64) | vlo[sl * D + o];
+        rank += (vo > var || (vo == var && o < c)) ? 1 : 0;
+      }
+      const unsigned word = __ballot_sync(0xffffffffu, rank < geo.kitty_hi);
+      if ((c & 31) == 0)
+        pl.kmask[(bh * (geo.Tcap / g) + P0 / g) * (D / 32) + (c >> 5)] = word;
+    }
     __syncthreads();
   }
-  pl.ksum[bh * D + c] = s1;
-  pl.ksq[(bh * D + c) * 2] = (unsigned long long)s2;
-  pl.ksq[(bh * D + c) * 2 + 1] = (unsigned long long)(s2 >> 64);
+  if (sl == 0) {
+    pl.ksum[bh * D + c] = s1;
+    pl.ksq[(bh * D + c) * 2] = (unsigned long long)s2;
+    pl.ksq[(bh * D + c) * 2 + 1] = (unsigned long long)(s2 >> 64);
+  }
 }
 
 // One CTA per (group, kv head), one thread per channel: per channel a 4- or
@@ -422,7 +459,13 @@ cudaError_t launch_flush_kitty(const Geometry &geo, const Planes &pl,
                                int64_t in_stride, const FlushTable &tab,
                                int total_groups, cudaStream_t st) {
   if (total_groups <= 0) return cudaSuccess;
-  k_kitty_rank<<<dim3(geo.H_kv, geo.B), geo.D, 0, st>>>(geo, pl, Kin, in_stride, tab);
+  const size_t rsmem = (size_t)5 * kRankThreads * sizeof(unsigned long long);
+  if (rsmem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_kitty_rank, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)rsmem);
+    if (e != cudaSuccess) return e;
+  }
+  k_kitty_rank<<<dim3(geo.H_kv, geo.B), kRankThreads, rsmem, st>>>(geo, pl, Kin, in_stride, tab);
   count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
