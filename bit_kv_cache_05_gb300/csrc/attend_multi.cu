@@ -15,7 +15,10 @@
 // One CTA of 128 threads serves 128 rows of one (sequence, kv head); the
 // rows are (query head of the kv head, query) pairs, row r = hh * QPT + i
 // with QPT = 128 / GQ queries per tile, and thread r owns row r.  Key tiles
-// of 64 tokens stream through:
+// of 64 tokens stream through; a tile's codes, scales and zeros arrive in a
+// shared-memory stage by bulk copies (cp.async.bulk, one mbarrier), issued
+// for the next tile as soon as this tile's rebuild has read the stage, so
+// that they land while the products and the softmax run:
 //   1. the threads rebuild the tile: k_hat and v_hat of every token in fp32
 //      (code * scale + zero; residual-window rows are fp16 already), each
 //      split into fp16 hi = RN(x) and lo = RN(x - hi), stored in shared
@@ -39,6 +42,7 @@
 #include <cmath>
 #include <mutex>
 
+#include "bulk_pipe.cuh"
 #include "vqk_internal.cuh"
 
 namespace vqk {
@@ -189,9 +193,14 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t 
 // product that read P has completed, so at D = 128 P takes K_hat's place
 // (16 KB each for hi and lo); the CTA then needs 96 KB and two fit on an SM
 // (their tensor memory, 256 columns each, fills the SM's 512).
-template <int D>
+// The stage (the tile's quantized rows as stored, bulk-copied) follows:
+// key codes and value codes (64 rows each), the key scale and zero rows of
+// the tile's groups (up to 4, at g = 16), the value scale and zero rows of
+// its tokens.
+template <int D, int BITS>
 struct Smem {
   static constexpr int KB = D / 64;                       // 64-channel K-blocks
+  static constexpr int ROW = D * BITS / 8;                // code bytes per token
   static constexpr uint32_t Q = 0;                        // [KB][128 rows][128 B]
   static constexpr uint32_t KH = Q + KB * 16384;          // [KB][64 rows][128 B]
   static constexpr uint32_t KL = KH + KB * 8192;
@@ -200,8 +209,14 @@ struct Smem {
   static constexpr bool ALIAS = KB * 8192 >= 16384;
   static constexpr uint32_t PH = ALIAS ? KH : VL + D * 128;   // [128 rows][128 B]
   static constexpr uint32_t PL = ALIAS ? KL : PH + 16384;
-  static constexpr uint32_t BAR = ALIAS ? VL + D * 128 : PL + 16384;  // 3 mbarriers + TMEM slot
-  static constexpr uint32_t BYTES = BAR + 64;
+  static constexpr uint32_t BAR = ALIAS ? VL + D * 128 : PL + 16384;  // 4 mbarriers + TMEM slot
+  static constexpr uint32_t SKC = BAR + 64;               // stage
+  static constexpr uint32_t SVC = SKC + 64 * ROW;
+  static constexpr uint32_t SKS = SVC + 64 * ROW;
+  static constexpr uint32_t SKZ = SKS + 8 * D;
+  static constexpr uint32_t SVS = SKZ + 8 * D;
+  static constexpr uint32_t SVZ = SVS + 8 * D;
+  static constexpr uint32_t BYTES = SVZ + 8 * D;
   static constexpr uint32_t ALLOC = BYTES + 1024;         // room to align the base
 };
 
@@ -226,7 +241,8 @@ struct Codes {
   static constexpr uint32_t M = (1u << BITS) - 1u;
   static constexpr int ROW = D * BITS / 8;
 
-  // the 16 codes of channels 16 ks ... 16 ks + 15 of a key row
+  // the 16 codes of channels 16 ks ... 16 ks + 15 of a key row (a row of
+  // the shared-memory stage)
   static __device__ __forceinline__ void key16(const uint8_t *krow, int ks,
                                                uint32_t (&c)[16]) {
     if constexpr (FRAG) {
@@ -235,7 +251,7 @@ struct Codes {
       const int r0 = 2 * (ks % KPW);
 #pragma unroll
       for (int tig = 0; tig < 4; ++tig) {
-        const uint32_t x = __ldg(w + NW * tig + ks / KPW);
+        const uint32_t x = w[NW * tig + ks / KPW];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
           c[4 * tig + e] = (x >> (16 * (e & 1) + BITS * (r0 + (e >> 1)))) & M;
@@ -244,12 +260,12 @@ struct Codes {
       // 16 codes = 2 BITS bytes at byte 2 BITS ks
       uint32_t w[BITS / 2];
       if constexpr (BITS == 2) {
-        w[0] = __ldg(reinterpret_cast<const uint32_t *>(krow + 4 * ks));
+        w[0] = *reinterpret_cast<const uint32_t *>(krow + 4 * ks);
       } else if constexpr (BITS == 4) {
-        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(krow + 8 * ks));
+        const uint2 v = *reinterpret_cast<const uint2 *>(krow + 8 * ks);
         w[0] = v.x; w[1] = v.y;
       } else {
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(krow + 16 * ks));
+        const uint4 v = *reinterpret_cast<const uint4 *>(krow + 16 * ks);
         w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
       }
       constexpr int PER = 32 / BITS;
@@ -272,7 +288,7 @@ struct Codes {
         const int pi = (tb >> 1) + pp;          // pairs (tb + pp, tb + pp + 4)
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-          const uint32_t x = __ldg(w + (8 * pi + j0 + jj) * NW + mv / KPW);
+          const uint32_t x = w[(8 * pi + j0 + jj) * NW + mv / KPW];
 #pragma unroll
           for (int rho = 0; rho < 2; ++rho) {
             c[pp][2 * jj + rho] = (x >> (BITS * (r0 + rho))) & M;
@@ -286,11 +302,11 @@ struct Codes {
         const uint8_t *p = vblk + (size_t)(tb + u) * ROW + c0 * BITS / 8;
         uint32_t w0, w1 = 0;
         if constexpr (BITS == 2) {
-          w0 = __ldg(reinterpret_cast<const uint16_t *>(p));
+          w0 = *reinterpret_cast<const uint16_t *>(p);
         } else if constexpr (BITS == 4) {
-          w0 = __ldg(reinterpret_cast<const uint32_t *>(p));
+          w0 = *reinterpret_cast<const uint32_t *>(p);
         } else {
-          const uint2 v = __ldg(reinterpret_cast<const uint2 *>(p));
+          const uint2 v = *reinterpret_cast<const uint2 *>(p);
           w0 = v.x; w1 = v.y;
         }
         constexpr int PER = 32 / BITS;
@@ -306,15 +322,15 @@ template <int D, int BITS, bool FRAG>
 __global__ void __launch_bounds__(kThreads, 2)
 k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
                Planes pl, MultiArgs args, MultiTable tab) {
-  using SM = Smem<D>;
+  using SM = Smem<D, BITS>;
   using CD = Codes<D, BITS, FRAG>;
   constexpr int KB = SM::KB, KS = D / 16, C8 = D / 8, ROW = CD::ROW;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bar_q = reinterpret_cast<uint64_t *>(sm + SM::BAR);
-  uint64_t *bar_s = bar_q + 1, *bar_o = bar_q + 2;
-  uint32_t *tslot = reinterpret_cast<uint32_t *>(bar_q + 3);
+  uint64_t *bar_s = bar_q + 1, *bar_o = bar_q + 2, *bar_k = bar_q + 3;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(bar_q + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int b = blockIdx.z, h = blockIdx.y;
@@ -341,6 +357,7 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
     mbar_init(bar_q);
     mbar_init(bar_s);
     mbar_init(bar_o);
+    mbar_init(bar_k);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -368,6 +385,22 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
           "r"(saddr(bar_q))
           : "memory");
   }
+  // the quantized rows of the tile at ta (ta < Tq) into the stage
+  auto stage_tile = [&](int ta) {
+    const int nq = min(kTok, Tq - ta);        // a multiple of 16 (g >= 16)
+    const int G0 = ta / g, ng = (ta + nq - 1) / g - G0 + 1;
+    mbar_expect_tx(bar_k, 2u * (nq * ROW + ng * D * 2 + nq * NJ * 2));
+    bulk_g2s(sm + SM::SKC, kc_base + (size_t)ta * ROW, nq * ROW, bar_k);
+    bulk_g2s(sm + SM::SVC, vc_base + (size_t)ta * ROW, nq * ROW, bar_k);
+    bulk_g2s(sm + SM::SKS, ks_base + (size_t)G0 * D, ng * D * 2, bar_k);
+    bulk_g2s(sm + SM::SKZ, kz_base + (size_t)G0 * D, ng * D * 2, bar_k);
+    bulk_g2s(sm + SM::SVS, vs_base + (size_t)ta * NJ, nq * NJ * 2, bar_k);
+    bulk_g2s(sm + SM::SVZ, vz_base + (size_t)ta * NJ, nq * NJ * 2, bar_k);
+  };
+  uint32_t ph_k = 0;
+  bool k_pending = false;       // a stage copy is in flight
+  if (tid == 0 && Tq > 0) stage_tile(0);
+  k_pending = Tq > 0;
   // KIVI-Sink: the sinks of the quantized region (the rest are -1); their
   // k_hat / v_hat are their fp16 rows
   __shared__ int ssk[kMaxSink];
@@ -402,26 +435,37 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
       o_pending = false;
       if (__syncthreads_or(!ok)) { failed = true; break; }
     }
+    // the tile's quantized rows in the stage
+    if (t0 < Tq) {
+      const bool ok = mbar_wait(bar_k, ph_k);
+      ph_k ^= 1u;
+      k_pending = false;
+      if (__syncthreads_or(!ok)) { failed = true; break; }
+    }
+    const int G0t = t0 / g;
     // sinks in this tile: bit (t - t0)
     uint64_t tmask = 0;
     for (int j = 0; j < nsk; ++j) {
       const int d = ssk[j] - t0;
       if (ssk[j] >= 0 && d >= 0 && d < kTok) tmask |= 1ull << d;
     }
-    // (b1) k_hat of tokens t0 ... t0+63, 16 channels per item, as fp16 hi + lo
+    // (b1) k_hat of tokens t0 ... t0+63, 16 channels per item, as fp16 hi + lo;
+    // consecutive threads take a token's consecutive 16-channel steps, so a
+    // warp reads few stage rows (and writes whole swizzled rows)
     for (int it = tid; it < kTok * KS; it += kThreads) {
-      const int tl = it % kTok, ks = it / kTok;
+      const int tl = it / KS, ks = it % KS;
       const int t = t0 + tl;
       float kf[16];
       if (t < Tq) {
         uint32_t c[16];
-        CD::key16(kc_base + (size_t)t * ROW, ks, c);
-        const __half *sp = ks_base + (size_t)(t / g) * D + 16 * ks;
-        const __half *zp = kz_base + (size_t)(t / g) * D + 16 * ks;
+        CD::key16(sm + SM::SKC + tl * ROW, ks, c);
+        const int gr = t / g - G0t;
+        const __half *sp = reinterpret_cast<const __half *>(sm + SM::SKS) + gr * D + 16 * ks;
+        const __half *zp = reinterpret_cast<const __half *>(sm + SM::SKZ) + gr * D + 16 * ks;
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-          const uint4 sr = __ldg(reinterpret_cast<const uint4 *>(sp) + q);
-          const uint4 zr = __ldg(reinterpret_cast<const uint4 *>(zp) + q);
+          const uint4 sr = reinterpret_cast<const uint4 *>(sp)[q];
+          const uint4 zr = reinterpret_cast<const uint4 *>(zp)[q];
           const __half2 *s2 = reinterpret_cast<const __half2 *>(&sr);
           const __half2 *z2 = reinterpret_cast<const __half2 *>(&zr);
 #pragma unroll
@@ -485,12 +529,14 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
       if (ta < Tq) {
         // Tq is a multiple of g >= 16: the octet is wholly quantized
         uint32_t c[8][8];
-        CD::value8x8(vc_base + (size_t)(ta & ~15) * ROW, ta & 8, c0, c);
+        CD::value8x8(sm + SM::SVC + ((ta & ~15) - t0) * ROW, ta & 8, c0, c);
         const int j = c0 / g;
+        const __half *svs = reinterpret_cast<const __half *>(sm + SM::SVS);
+        const __half *svz = reinterpret_cast<const __half *>(sm + SM::SVZ);
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const float sv = __half2float(vs_base[(size_t)(ta + u) * NJ + j]);
-          const float zv = __half2float(vz_base[(size_t)(ta + u) * NJ + j]);
+          const float sv = __half2float(svs[(ta + u - t0) * NJ + j]);
+          const float zv = __half2float(svz[(ta + u - t0) * NJ + j]);
 #pragma unroll
           for (int e = 0; e < 8; ++e) vf[u][e] = fmaf((float)c[u][e], sv, zv);
         }
@@ -541,6 +587,13 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
+
+    // every thread's reads of the stage are done: the next tile's copies
+    const int tn = t0 + kTok;
+    if (tn <= max_pos && tn < Tq) {
+      if (tid == 0) stage_tile(tn);
+      k_pending = true;
+    }
 
     // (c) S = Q K_hi^T + Q K_lo^T
     if (tid == 0) {
@@ -675,8 +728,9 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
   if (failed) {
     if (tid == 0) atomicOr(args.err, 2u);
     // let an O product still in flight finish (bounded) before the tensor
-    // memory is released
+    // memory is released, and a stage copy land before the CTA ends
     if (o_pending) mbar_wait(bar_o, ph_o);
+    if (k_pending) mbar_wait(bar_k, ph_k);
   }
   tc_fence_before();
   __syncthreads();
@@ -730,7 +784,7 @@ cudaError_t launch_k(const Geometry &geo, const Planes &pl, const MultiArgs &arg
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  const size_t smem = Smem<D>::ALLOC;
+  const size_t smem = Smem<D, BITS>::ALLOC;
   cudaError_t e = cudaFuncSetAttribute(k_attend_multi<D, BITS, FRAG>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
