@@ -212,7 +212,10 @@ struct Smem {
   static constexpr uint32_t BAR = ALIAS ? VL + D * 128 : PL + 16384;  // 4 mbarriers + TMEM slot
   static constexpr uint32_t SKC = BAR + 64;               // stage
   static constexpr uint32_t SVC = SKC + 64 * ROW;
-  static constexpr uint32_t SKS = SVC + 64 * ROW;
+  // value codes per 16-token block, 16 bytes of padding between blocks (a
+  // warp's reads of different blocks then fall in different banks)
+  static constexpr uint32_t VBS = 16 * ROW + 16;
+  static constexpr uint32_t SKS = SVC + 4 * VBS;
   static constexpr uint32_t SKZ = SKS + 8 * D;
   static constexpr uint32_t SVS = SKZ + 8 * D;
   static constexpr uint32_t SVZ = SVS + 8 * D;
@@ -326,8 +329,9 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
   using CD = Codes<D, BITS, FRAG>;
   constexpr int KB = SM::KB, KS = D / 16, C8 = D / 8, ROW = CD::ROW;
   extern __shared__ unsigned char smem_raw[];
-  unsigned char *sm = reinterpret_cast<unsigned char *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned (the swizzle atoms); pointer arithmetic on the shared
+  // array, so that accesses through it compile as shared-memory ones
+  unsigned char *sm = smem_raw + ((1024u - (saddr(smem_raw) & 1023u)) & 1023u);
   uint64_t *bar_q = reinterpret_cast<uint64_t *>(sm + SM::BAR);
   uint64_t *bar_s = bar_q + 1, *bar_o = bar_q + 2, *bar_k = bar_q + 3;
   uint32_t *tslot = reinterpret_cast<uint32_t *>(bar_q + 4);
@@ -391,7 +395,9 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
     const int G0 = ta / g, ng = (ta + nq - 1) / g - G0 + 1;
     mbar_expect_tx(bar_k, 2u * (nq * ROW + ng * D * 2 + nq * NJ * 2));
     bulk_g2s(sm + SM::SKC, kc_base + (size_t)ta * ROW, nq * ROW, bar_k);
-    bulk_g2s(sm + SM::SVC, vc_base + (size_t)ta * ROW, nq * ROW, bar_k);
+    for (int k = 0; k < nq / 16; ++k)
+      bulk_g2s(sm + SM::SVC + k * SM::VBS, vc_base + (size_t)(ta + 16 * k) * ROW, 16 * ROW,
+               bar_k);
     bulk_g2s(sm + SM::SKS, ks_base + (size_t)G0 * D, ng * D * 2, bar_k);
     bulk_g2s(sm + SM::SKZ, kz_base + (size_t)G0 * D, ng * D * 2, bar_k);
     bulk_g2s(sm + SM::SVS, vs_base + (size_t)ta * NJ, nq * NJ * 2, bar_k);
@@ -529,7 +535,7 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
       if (ta < Tq) {
         // Tq is a multiple of g >= 16: the octet is wholly quantized
         uint32_t c[8][8];
-        CD::value8x8(sm + SM::SVC + ((ta & ~15) - t0) * ROW, ta & 8, c0, c);
+        CD::value8x8(sm + SM::SVC + (((ta & ~15) - t0) >> 4) * SM::VBS, ta & 8, c0, c);
         const int j = c0 / g;
         const __half *svs = reinterpret_cast<const __half *>(sm + SM::SVS);
         const __half *svz = reinterpret_cast<const __half *>(sm + SM::SVZ);
