@@ -469,6 +469,7 @@ def run_ours(args, w, rank, world, local):
         barrier(world)
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
+        h0 = time.perf_counter()
         t0.record(stream)
         for i in range(K_steps):
             c = caches[(cursor[0] + i) % n_copies]
@@ -477,8 +478,21 @@ def run_ours(args, w, rank, world, local):
             c.decode_attend(dq, out)
             hout[i].copy_(out, non_blocking=True)
         t1.record(stream)
+        host_us = (time.perf_counter() - h0) * 1e6 / K_steps
         torch.cuda.synchronize(dev)
         e2e_ms = max_over_ranks(t0.elapsed_time(t1) / K_steps, world, dev)
+        # where the end-to-end time goes: the host's time to issue a step
+        # (the loop above returns before the device finishes) and the two
+        # copies alone on the device
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for i in range(K_steps):
+            din.copy_(hin[i % 64], non_blocking=True)
+            hout[i].copy_(out, non_blocking=True)
+        c1.record(stream)
+        torch.cuda.synchronize(dev)
+        copies_us = c0.elapsed_time(c1) * 1e3 / K_steps
 
     clocks = clk.summary()
     S_dec = caches[cursor[0] % n_copies].lengths()[0]
@@ -568,7 +582,16 @@ def run_ours(args, w, rank, world, local):
         "targets": targets,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_ms * 1e3, 3), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "breakdown": {
+                    "host_issue_us": round(host_us, 2),
+                    "copies_device_us": round(copies_us, 2),
+                    "step_device_us": round(ms * 1e3, 2),
+                    "reading": "the device runs the copies, the append and "
+                               "the decode back to back; when the host "
+                               "takes longer to issue a step than the "
+                               "device takes to run it, the step time is "
+                               "the host's"}},
         "gpu_launches": int(round(launches)),
         "gpu_launches_per": "pass of K steps",
         "clocks": clocks,

@@ -32,7 +32,7 @@ struct vq_kivi_cache {
   MmaPlan plan;
   unsigned *err;          // device word set by a kernel whose wait gave up
   int32_t S[kMaxB], Tq[kMaxB], nres[kMaxB];
-  // AgeTieredKV: the automatic split last planned and the T_q it was
+  // AgeTieredKV and Kitty: the automatic split last planned and the T_q it was
   // planned for (the plan is a search, redone when a flush moves T_q)
   int32_t age_tps;
   int32_t age_Tq[kMaxB];
@@ -505,8 +505,9 @@ int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
   for (int b = 0; b < p.B; ++b) total_tq += c->Tq[b];
   int32_t tps = c->split_tokens;
   const int32_t unit = split_unit(p.group);
-  if (tps == 0 && c->geo.age_b1 > 0) {
-    // AgeTieredKV: one wave of CTAs, each streaming its groups through
+  const bool one_wave = c->geo.age_b1 > 0 || c->geo.kitty;
+  if (tps == 0 && one_wave) {
+    // AgeTieredKV and Kitty: one wave of CTAs, each streaming its groups through
     // per-warp pipelines (a CTA's start costs a pipeline fill, so items are
     // long); a sequence's last item also takes its residual window.  Among
     // the splits whose items fit one wave, take the one with the fewest
@@ -516,7 +517,8 @@ int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
       tps = c->age_tps;
     } else {
       const int64_t sms = c->sm_count;
-      const int64_t cap = (int64_t)age_decode_ctas_per_sm(c->geo) * sms;
+      const int64_t cap = (int64_t)(c->geo.kitty ? kitty_decode_ctas_per_sm(c->geo)
+                                                 : age_decode_ctas_per_sm(c->geo)) * sms;
       auto items = [&](int64_t t) {
         int64_t n = 0;
         for (int b = 0; b < p.B; ++b) {
@@ -544,9 +546,7 @@ int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
       memcpy(c->age_Tq, c->Tq, sizeof(int32_t) * p.B);
     }
   } else if (tps == 0) {
-    // Kitty caches (one token per lane, loads in flight limited by the
-    // block): more, shorter items keep more of them per SM
-    const int64_t target_items = (c->geo.kitty ? 16LL : 4LL) * c->sm_count;
+    const int64_t target_items = 4LL * c->sm_count;
     int64_t t = (total_tq * p.H_kv + target_items - 1) / target_items;
     tps = (int32_t)round_up((size_t)(t > 1 ? t : 1), unit);
   }
@@ -554,12 +554,11 @@ int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
 
   DecodeTable tab;
   tab.prefix[0] = 0;
-  const bool aged = c->geo.age_b1 > 0;
   for (int b = 0; b < p.B; ++b) {
     tab.Tq[b] = c->Tq[b];
     tab.nres[b] = c->nres[b];
     tab.nq[b] = (c->Tq[b] + tps - 1) / tps;
-    if (aged) {
+    if (one_wave) {
       // the last quantized item takes the residual window (an item of its
       // own when there is no quantized token)
       if (tab.nq[b] == 0 && c->nres[b] > 0) tab.nq[b] = 1;

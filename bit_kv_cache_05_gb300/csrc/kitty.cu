@@ -1,6 +1,6 @@
 // Kitty: channel-wise mixed-precision keys (4-bit channels of high running
-// variance, 2-bit for the rest) and fp16 values; its flush and its fused
-// decode.
+// variance, 2-bit for the rest) and fp16 values: its flush and the launch
+// of its fused decode (kitty_decode.cuh).
 //
 // Method: VeloxQuant-MLX changelog v0.11.0 "New" (Kitty: key channels ranked
 // by online per-channel variance, the top 25% quantized in 4 bits and the
@@ -12,6 +12,7 @@
 // the sums S1 = sum m (int64) and S2 = sum m^2 (a 128-bit integer) are
 // exact and N S2 - S1^2 = N^2 var is compared as a 128-bit integer (N <=
 // 2^20 keeps it below 2^120).  The smaller channel wins a tie.
+#include "kitty_decode.cuh"
 #include "vqk_internal.cuh"
 
 namespace vqk {
@@ -193,266 +194,14 @@ __global__ void k_flush_kitty(Geometry geo, Planes pl, const __half *__restrict_
   }
 }
 
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// Fused decode over a Kitty cache: one CTA per (work item, kv head); each
-// warp owns whole key groups and takes them in blocks of 32 tokens, one
-// token per lane for the scores and all lanes over the channels for the
-// values.  Scores: q . k_hat_t = sum_j a_j f_tj + beta, where f_tj is field
-// j of token t's row (the 4-bit channels' codes, then the 2-bit ones) and
-// a_j = q_c s_Gc of the channel c it belongs to: a is laid out in field
-// order in shared memory once per group (and per query head), and each lane
-// walks its own row's fields against it (broadcast reads).  Softmax: per
-// block, the maximum and the sum over the warp, one rescale of the lane's
-// output channels.  Values: the block's p_t passed by shuffles, the fp16
-// rows read 8 bytes per lane (lane owns channels lane*CPL ...).  The fp16
-// residual window is its own work item (one token per step).  Partials as
-// the CUDA-core KIVI decode (launch_combine merges them).
-template <int D, int GQ>
-__global__ void __launch_bounds__(kThreads)
-k_decode_kitty(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
-  constexpr int CPL = D / 32;   // GQ: query heads per kv head
-  __shared__ float sq[GQ][D];
-  __shared__ __align__(16) float sa[kWarps][GQ][D]; // a in field order
-  __shared__ float sm[kWarps][GQ], sl[kWarps][GQ];
-  __shared__ float so[kWarps][GQ][D];
-  // the combine kernel behind this one waits for its completion
-  asm volatile("griddepcontrol.launch_dependents;");
-  const int item = blockIdx.x, h = blockIdx.y;
-  const int b = find_seq(tab.prefix, geo.B, item);
-  const int k = item - tab.prefix[b];
-  constexpr int gq = GQ;
-  const int g = geo.g;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const size_t bh = (size_t)b * geo.H_kv + h;
-  const int HI = geo.kitty_hi;
-  const int krow = (D + HI) / 4;                // bytes per row, a multiple of 4
-  for (int i = threadIdx.x; i < GQ * D; i += kThreads) {
-    const int hh = i / D, c = i % D;
-    sq[hh][c] = __half2float(args.q[((size_t)b * geo.H_q + h * GQ + hh) * D + c]) *
-                args.scale_log2;
-  }
-  __syncthreads();
-  float m[GQ], l[GQ], o[GQ][CPL];
-#pragma unroll
-  for (int hh = 0; hh < GQ; ++hh) {
-    m[hh] = -INFINITY; l[hh] = 0.f;
-#pragma unroll
-    for (int u = 0; u < CPL; ++u) o[hh][u] = 0.f;
-  }
-  // fold a block of scores (one per lane, -inf for absent tokens) of head
-  // hh: returns this lane's weight
-  auto block_softmax = [&](int hh, float s) {
-    float mb = s;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
-    const float mn = fmaxf(m[hh], mb);
-    const float alpha = m[hh] == -INFINITY ? 0.f : exp2f(m[hh] - mn);
-    const float p = s == -INFINITY ? 0.f : exp2f(s - mn);
-    float ps = p;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-    l[hh] = l[hh] * alpha + ps;
-#pragma unroll
-    for (int u = 0; u < CPL; ++u) o[hh][u] *= alpha;
-    m[hh] = mn;
-    return p;
-  };
-
-  if (k < tab.nq[b]) {
-    const int t0 = k * args.tps, t1 = min(t0 + args.tps, tab.Tq[b]);
-    const int bt = g < 32 ? g : 32;             // tokens per block
-    for (int G = t0 / g + warp; G * g < t1; G += kWarps) {
-      const size_t gidx = (bh * (geo.Tcap / g) + G) * D;
-      const uint32_t *mk = pl.kmask + (bh * (geo.Tcap / g) + G) * (D / 32);
-      // field index of each of the lane's channels
-      int fj[CPL];
-      float s_c[CPL], z_c[CPL];
-#pragma unroll
-      for (int u = 0; u < CPL; ++u) {
-        const int c = lane * CPL + u;
-        int below = 0;
-        for (int w = 0; w < (c >> 5); ++w) below += __popc(mk[w]);
-        const uint32_t mw = mk[c >> 5];
-        below += __popc(mw & ((1u << (c & 31)) - 1u));
-        fj[u] = ((mw >> (c & 31)) & 1u) ? below : HI + (c - below);
-        s_c[u] = __half2float(pl.Ks[gidx + c]);
-        z_c[u] = __half2float(pl.Kz[gidx + c]);
-      }
-      float beta[GQ];
-      __syncwarp();
-#pragma unroll
-      for (int hh = 0; hh < GQ; ++hh) {
-        float part = 0.f;
-#pragma unroll
-        for (int u = 0; u < CPL; ++u) {
-          const float qc = sq[hh][lane * CPL + u];
-          part = fmaf(qc, z_c[u], part);
-          sa[warp][hh][fj[u]] = qc * s_c[u];
-        }
-        beta[hh] = warp_sum(part);
-      }
-      __syncwarp();
-      for (int tb = G * g; tb < G * g + g; tb += bt) {
-        float acc[GQ];
-#pragma unroll
-        for (int hh = 0; hh < GQ; ++hh) acc[hh] = 0.f;
-        if (lane < bt) {
-          const uint32_t *row = reinterpret_cast<const uint32_t *>(
-              pl.Kc + (bh * geo.Tcap + tb + lane) * krow);
-          // 4-bit fields: 8 per word
-#pragma unroll 1
-          for (int w = 0; w < HI / 8; ++w) {
-            const uint32_t x = __ldg(row + w);
-#pragma unroll
-            for (int hh = 0; hh < GQ; ++hh) {
-              const float4 a0 = *reinterpret_cast<const float4 *>(&sa[warp][hh][8 * w]);
-              const float4 a1 = *reinterpret_cast<const float4 *>(&sa[warp][hh][8 * w + 4]);
-              float r = acc[hh];
-              r = fmaf(a0.x, (float)(x & 15u), r);
-              r = fmaf(a0.y, (float)((x >> 4) & 15u), r);
-              r = fmaf(a0.z, (float)((x >> 8) & 15u), r);
-              r = fmaf(a0.w, (float)((x >> 12) & 15u), r);
-              r = fmaf(a1.x, (float)((x >> 16) & 15u), r);
-              r = fmaf(a1.y, (float)((x >> 20) & 15u), r);
-              r = fmaf(a1.z, (float)((x >> 24) & 15u), r);
-              r = fmaf(a1.w, (float)(x >> 28), r);
-              acc[hh] = r;
-            }
-          }
-          // 2-bit fields: 16 per word
-#pragma unroll 1
-          for (int w = 0; w < (D - HI) / 16; ++w) {
-            const uint32_t x = __ldg(row + HI / 8 + w);
-#pragma unroll
-            for (int hh = 0; hh < GQ; ++hh) {
-              const float *aw = &sa[warp][hh][HI + 16 * w];
-              float r = acc[hh];
-#pragma unroll
-              for (int e = 0; e < 16; e += 4) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(aw + e);
-                r = fmaf(a4.x, (float)((x >> (2 * e)) & 3u), r);
-                r = fmaf(a4.y, (float)((x >> (2 * e + 2)) & 3u), r);
-                r = fmaf(a4.z, (float)((x >> (2 * e + 4)) & 3u), r);
-                r = fmaf(a4.w, (float)((x >> (2 * e + 6)) & 3u), r);
-              }
-              acc[hh] = r;
-            }
-          }
-        }
-        float p[GQ];
-#pragma unroll
-        for (int hh = 0; hh < GQ; ++hh) {
-          // online softmax over the block (written out here so that every
-          // index of m, l, o stays a compile-time constant)
-          const float s = lane < bt ? acc[hh] + beta[hh] : -INFINITY;
-          float mb = s;
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1)
-            mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
-          const float mn = fmaxf(m[hh], mb);
-          const float alpha = m[hh] == -INFINITY ? 0.f : exp2f(m[hh] - mn);
-          p[hh] = s == -INFINITY ? 0.f : exp2f(s - mn);
-          const float ps = warp_sum(p[hh]);
-          l[hh] = l[hh] * alpha + ps;
-#pragma unroll
-          for (int u = 0; u < CPL; ++u) o[hh][u] *= alpha;
-          m[hh] = mn;
-        }
-        // values of the block's tokens
-        const __half *vbase = pl.Vf + (bh * geo.Tcap + tb) * D + lane * CPL;
-        // 8 rows in flight per lane: the loads of a block do not depend on
-        // one another, only the accumulation does
-#pragma unroll 8
-        for (int j = 0; j < bt; ++j) {
-          const __half *vr = vbase + (size_t)j * D;
-          float v[CPL];
-          if constexpr (CPL == 4) {
-            const uint2 r = __ldg(reinterpret_cast<const uint2 *>(vr));
-            const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&r.x));
-            const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&r.y));
-            v[0] = v01.x; v[1] = v01.y; v[2] = v23.x; v[3] = v23.y;
-          } else {
-#pragma unroll
-            for (int u = 0; u < CPL; ++u) v[u] = __half2float(vr[u]);
-          }
-#pragma unroll
-          for (int hh = 0; hh < GQ; ++hh) {
-            const float pj = __shfl_sync(0xffffffffu, p[hh], j);
-#pragma unroll
-            for (int u = 0; u < CPL; ++u) o[hh][u] = fmaf(pj, v[u], o[hh][u]);
-          }
-        }
-      }
-    }
-  } else {
-    const int Tq = tab.Tq[b];
-    for (int i0 = warp * 32; i0 < tab.nres[b]; i0 += kWarps * 32) {
-      // a block of up to 32 residual tokens: lane i scores token Tq + i0 + i
-      const int i = i0 + lane;
-      const bool ok = i < tab.nres[b];
-      const int slot = (Tq + (ok ? i : i0)) % geo.Rcap;
-      const __half *kr = pl.Kr + (bh * geo.Rcap + slot) * D;
-      float acc[GQ];
-#pragma unroll
-      for (int hh = 0; hh < GQ; ++hh) acc[hh] = 0.f;
-#pragma unroll 4
-      for (int c = 0; c < D; c += 2) {
-        const float2 kv = __half22float2(*reinterpret_cast<const __half2 *>(kr + c));
-#pragma unroll
-        for (int hh = 0; hh < GQ; ++hh)
-          acc[hh] = fmaf(sq[hh][c], kv.x, fmaf(sq[hh][c + 1], kv.y, acc[hh]));
-      }
-      float p[GQ];
-#pragma unroll
-      for (int hh = 0; hh < GQ; ++hh) p[hh] = block_softmax(hh, ok ? acc[hh] : -INFINITY);
-      const int nb = min(32, tab.nres[b] - i0);
-      for (int j = 0; j < nb; ++j) {
-        const __half *vr = pl.Vr + (bh * geo.Rcap + (Tq + i0 + j) % geo.Rcap) * D + lane * CPL;
-        float v[CPL];
-#pragma unroll
-        for (int u = 0; u < CPL; ++u) v[u] = __half2float(vr[u]);
-#pragma unroll
-        for (int hh = 0; hh < GQ; ++hh) {
-          const float pj = __shfl_sync(0xffffffffu, p[hh], j);
-#pragma unroll
-          for (int u = 0; u < CPL; ++u) o[hh][u] = fmaf(pj, v[u], o[hh][u]);
-        }
-      }
-    }
-  }
-
-#pragma unroll
-  for (int hh = 0; hh < GQ; ++hh) {
-    if (hh >= gq) break;
-    if (lane == 0) { sm[warp][hh] = m[hh]; sl[warp][hh] = l[hh]; }
-#pragma unroll
-    for (int u = 0; u < CPL; ++u) so[warp][hh][lane * CPL + u] = o[hh][u];
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < gq * (D + 2); i += kThreads) {
-    const int hh = i / (D + 2), c = i % (D + 2);
-    float M = -INFINITY;
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm[w][hh]);
-    float acc = 0.f;
-    for (int w = 0; w < kWarps; ++w) {
-      const float f = sm[w][hh] == -INFINITY ? 0.f : exp2f(sm[w][hh] - M);
-      acc += f * (c < D ? so[w][hh][c] : sl[w][hh]);
-    }
-    const int hq = h * gq + hh;
-    float *dst = pl.part + (((size_t)b * geo.H_q + hq) * geo.max_items + k) * (D + 2);
-    dst[c] = c == D ? M : acc;
-  }
-}
-
 }  // namespace
+
+static kitdec::KitKernel pick_kitty_kernel(const Geometry &geo) {
+  const int gq = geo.H_q / geo.H_kv;
+  if (geo.D == 64) return kitdec::pick_d64(gq);
+  if (geo.D == 128) return kitdec::pick_d128(gq);
+  return {};
+}
 
 cudaError_t launch_flush_kitty(const Geometry &geo, const Planes &pl,
                                const __half *Kin, const __half *Vin,
@@ -476,25 +225,45 @@ cudaError_t launch_flush_kitty(const Geometry &geo, const Planes &pl,
   return cudaGetLastError();
 }
 
+int kitty_decode_ctas_per_sm(const Geometry &geo) {
+  const kitdec::KitKernel kf = pick_kitty_kernel(geo);
+  return kf.occ > 0 ? kf.occ : 1;
+}
+
+// The split is planned for one wave (as the AgeTieredKV decode's): the
+// dynamic shared memory request is padded until an SM holds at most
+// ceil(CTAs / SMs) CTAs, so that the block scheduler cannot stack some SMs
+// fuller than others.
 cudaError_t launch_decode_kitty(const Geometry &geo, const Planes &pl,
                                 const DecodeArgs &args, const DecodeTable &tab,
                                 cudaStream_t st) {
   if (args.total_items > 0) {
-    dim3 grid(args.total_items, geo.H_kv);
-    const int gq = geo.H_q / geo.H_kv;
-#define VQK_KITTY(DD, QQ)                                                   \
-  if (geo.D == DD && gq == QQ) {                                            \
-    k_decode_kitty<DD, QQ><<<grid, kThreads, 0, st>>>(geo, pl, args, tab); \
-  } else
-#define VQK_KITTY_D(DD) VQK_KITTY(DD, 1) VQK_KITTY(DD, 2) VQK_KITTY(DD, 3)  \
-  VQK_KITTY(DD, 4) VQK_KITTY(DD, 5) VQK_KITTY(DD, 6) VQK_KITTY(DD, 7)       \
-  VQK_KITTY(DD, 8)
-    VQK_KITTY_D(64) VQK_KITTY_D(128)
-    { return cudaErrorInvalidValue; }
-#undef VQK_KITTY_D
-#undef VQK_KITTY
+    const kitdec::KitKernel kf = pick_kitty_kernel(geo);
+    if (!kf.f) return cudaErrorInvalidValue;
+    int dev = 0, sms = 0, smem_sm = 0, reserved = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+      e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e == cudaSuccess)
+      e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    if (e != cudaSuccess) return e;
+    const int64_t ctas = (int64_t)args.total_items * geo.H_kv;
+    const int64_t occ = (ctas + sms - 1) / (sms > 0 ? sms : 1);
+    size_t smem = (size_t)kf.smem;
+    if (occ >= 1 && occ < kf.occ) {
+      const int64_t per = ((int64_t)smem_sm / occ - reserved - kf.smem_static) / 128 * 128;
+      if (per > (int64_t)smem) smem = (size_t)per;
+    }
+    Geometry g2 = geo;
+    Planes p2 = pl;
+    DecodeArgs a2 = args;
+    DecodeTable t2 = tab;
+    void *params[] = {&g2, &p2, &a2, &t2};
+    e = cudaLaunchKernel(kf.f, dim3(args.total_items, geo.H_kv),
+                         dim3(kitdec::kThreads), params, smem, st);
     count_launch();
-    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   return launch_combine(geo, pl, args, tab, st);

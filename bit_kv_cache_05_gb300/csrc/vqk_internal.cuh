@@ -286,6 +286,9 @@ cudaError_t launch_flush_kitty(const Geometry &geo, const Planes &pl,
                                const __half *Kin, const __half *Vin,
                                int64_t in_stride, const FlushTable &tab,
                                int total_groups, cudaStream_t st);
+// CTAs of the Kitty decode resident per SM (its split is planned for one
+// wave, as the AgeTieredKV decode's)
+int kitty_decode_ctas_per_sm(const Geometry &geo);
 cudaError_t launch_decode_kitty(const Geometry &geo, const Planes &pl,
                                 const DecodeArgs &args, const DecodeTable &tab,
                                 cudaStream_t st);

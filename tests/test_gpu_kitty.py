@@ -47,21 +47,29 @@ def _planes_equal(c, oc, g):
 
 
 CASES = [
-    ("gqa_serving", [700, 1000, 96], 32),   # 8 outlier key channels x10, GQA
-    ("pages_S512", [900], 32),
-    ("pages_S512", [300, 64], 0),           # every channel 2-bit
-    ("ragged_long", [1500, 200], 128),      # every channel 4-bit
-    ("tiny", [256, 50], 16),                # D = 64
+    # recipe, lengths, 4-bit channels, group (None: the recipe's)
+    ("gqa_serving", [700, 1000, 96], 32, None),   # 8 outlier key channels x10, GQA
+    ("pages_S512", [900], 32, None),
+    ("pages_S512", [300, 64], 0, None),           # every channel 2-bit
+    ("ragged_long", [1500, 200], 128, None),      # every channel 4-bit
+    ("tiny", [256, 50], 16, None),                # D = 64
+    # groups of 64 (two staged blocks per group), 16 (a block is a group;
+    # D = 64: 8-byte channel masks), 128
+    ("pages_S512", [1100, 333], 32, 64),
+    ("tiny", [300, 170], 16, 16),
+    ("gqa_serving", [900, 300], 48, 128),
 ]
 
 
-@pytest.mark.parametrize("name,lens,hi", CASES,
-                         ids=[f"{c[0]}-hi{c[2]}" for c in CASES])
-def test_kitty_planes_and_decode(lib, name, lens, hi):
+@pytest.mark.parametrize("name,lens,hi,group", CASES,
+                         ids=[f"{c[0]}-hi{c[2]}-g{c[3]}" for c in CASES])
+def test_kitty_planes_and_decode(lib, name, lens, hi, group):
     import oracle
     from bit_kv_cache_05_gb300.cache import KiviCache
     w = synth.shrink(synth.workload(name), lens, n_append=0)
     w = synth.dataclasses.replace(w, bits=2)
+    if group is not None:
+        w = synth.dataclasses.replace(w, group=group)
     inp = synth.make_inputs(w, seed=60, device="cpu")
     c = KiviCache(inp["K"].cuda(), inp["V"].cuda(), w.seq_lens, H_q=w.H_q,
                   bits=2, group=w.group, residual=w.residual, max_seq=w.max_seq,
