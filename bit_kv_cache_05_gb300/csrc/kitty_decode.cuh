@@ -20,7 +20,11 @@ namespace kitdec {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 2;
+// One stage per warp: a block's 8 KB of fp16 values make a stage 10.9 KB,
+// so a single stage keeps four to five CTAs on an SM, whose warps hide one
+// another's copy latency (two stages per warp allowed two CTAs: 87 against
+// 74.7 us at the pages' shape)
+constexpr int kStages = 1;
 constexpr unsigned kFull = 0xffffffffu;
 // Code fields enter the key products as fp32 subnormals (a field masked in
 // place at bit pos of a 32-bit word, pos + width <= 16, reads as
@@ -78,8 +82,8 @@ __device__ __forceinline__ int kit_pos(int f, int HI) {
 
 // Fused decode over a Kitty cache.  One CTA of 4 warps per (work item, kv
 // head); an item takes the key groups k, k + nq, k + 2 nq, ... of its
-// sequence and the warps take those groups round robin, each streaming its
-// blocks (32 tokens, at most g) through its own bulk-copy pipeline.  Per
+// sequence and the warps take those groups round robin, each copying its
+// blocks (32 tokens, at most g) into its own stage by bulk copies.  Per
 // group a' = q' s in field order (the field of channel c follows from the
 // group's mask: the 4-bit channels first, ascending, then the 2-bit ones)
 // and beta = q'.z; per block:
