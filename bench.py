@@ -174,7 +174,8 @@ def barrier(world: int):
 
 
 DECODE_KERNEL_SOURCES = ("bit_kv_cache_05_gb300/csrc/decode_mma.cuh",
-                         "bit_kv_cache_05_gb300/csrc/decode_mma.cu")
+                         "bit_kv_cache_05_gb300/csrc/decode_mma.cu",
+                         "bit_kv_cache_05_gb300/csrc/bulk_pipe.cuh")
 
 
 def decode_kernel_hash() -> str:
