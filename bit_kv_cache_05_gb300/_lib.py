@@ -24,7 +24,7 @@ _NAMES = {VQ_ERR_ARG: "VQ_ERR_ARG", VQ_ERR_UNSUPPORTED: "VQ_ERR_UNSUPPORTED",
 
 # every symbol include/vq_kivi.h declares
 EXPORTS = ("vq_kivi_quantize", "vq_kivi_quantize_ex", "vq_kivi_append",
-           "vq_kivi_decode_attend",
+           "vq_kivi_decode_attend", "vq_kivi_step_host",
            "vq_kivi_free", "vq_kivi_attend_multi", "vq_kivi_last_error", "vq_kivi_lengths",
            "vq_kivi_get_params", "vq_kivi_plane_bytes", "vq_kivi_export",
            "vq_kivi_dequantize",
@@ -93,6 +93,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
                                           P, P, ctypes.POINTER(P)]
         L.vq_kivi_append.argtypes = [P, P, P, i64, P, P]
         L.vq_kivi_decode_attend.argtypes = [P, P, P, ctypes.c_float, P]
+        L.vq_kivi_step_host.argtypes = [P, P, P, P, P, ctypes.c_float, P]
         L.vq_kivi_attend_multi.argtypes = [P, P, i32, P, ctypes.c_float, P]
         L.vq_kivi_free.argtypes = [P]
         L.vq_kivi_last_error.restype = ctypes.c_char_p

@@ -18,9 +18,30 @@ PLANES = ("Kc", "Ks", "Kz", "Vc", "Vs", "Vz", "Kr", "Vr",
           "sink_pos", "sink_k", "sink_v", "Kmask", "Vf", "tier")
 
 
-def _stream_handle(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream],
+                   device: Optional[int] = None) -> ctypes.c_void_p:
+    """The stream to launch on: `stream`, else torch's current stream of
+    `device` (the current device when None).  torch's raw lookup skips the
+    Stream object that torch.cuda.current_stream() builds (~3 us a call)."""
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
+    if _raw_stream is not None:
+        dev = torch.cuda.current_device() if device is None else device
+        return ctypes.c_void_p(_raw_stream(dev))
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _host_ptr(t: torch.Tensor, dtype: torch.dtype, name: str) -> ctypes.c_void_p:
+    if t.is_cuda or not t.is_pinned():
+        raise ValueError(f"{name} must be a pinned host tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _dev_ptr(t: torch.Tensor, dtype: torch.dtype, name: str) -> ctypes.c_void_p:
@@ -90,7 +111,7 @@ class KiviCache:
         _lib.check(_lib.load().vq_kivi_append(
             self._h, _dev_ptr(K_new, torch.float16, "K_new"),
             _dev_ptr(V_new, torch.float16, "V_new"), K_new.shape[2],
-            _i32_array(n), _stream_handle(stream)))
+            _i32_array(n), _stream_handle(stream, self.device.index)))
 
     def decode_attend(self, q: torch.Tensor, out: Optional[torch.Tensor] = None,
                       scale: float = 0.0,
@@ -103,7 +124,26 @@ class KiviCache:
         _lib.check(_lib.load().vq_kivi_decode_attend(
             self._h, _dev_ptr(q, torch.float16, "q"),
             _dev_ptr(out, torch.float32, "out"), float(scale),
-            _stream_handle(stream)))
+            _stream_handle(stream, self.device.index)))
+        return out
+
+    def step_host(self, K_new: torch.Tensor, V_new: torch.Tensor, q: torch.Tensor,
+                  out: torch.Tensor, scale: float = 0.0,
+                  stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+        """One serving step from pinned host memory (vq_kivi_step_host):
+        append one token per sequence (K_new, V_new fp16 [B][H_kv][D]) and
+        decode q (fp16 [B][H_q][D]) into out (fp32 [B][H_q][D]), all pinned
+        host tensors.  Asynchronous: out holds the result once the stream
+        has reached the end of the step."""
+        if tuple(K_new.shape) != (self.B, self.H_kv, self.D) or K_new.shape != V_new.shape:
+            raise ValueError(f"K_new and V_new must be [{self.B}][{self.H_kv}][{self.D}]")
+        if tuple(q.shape) != (self.B, self.H_q, self.D) or q.shape != out.shape:
+            raise ValueError(f"q and out must be [{self.B}][{self.H_q}][{self.D}]")
+        _lib.check(_lib.load().vq_kivi_step_host(
+            self._h, _host_ptr(K_new, torch.float16, "K_new"),
+            _host_ptr(V_new, torch.float16, "V_new"),
+            _host_ptr(q, torch.float16, "q"), _host_ptr(out, torch.float32, "out"),
+            float(scale), _stream_handle(stream, self.device.index)))
         return out
 
     def attend_multi(self, q: torch.Tensor, out: Optional[torch.Tensor] = None,

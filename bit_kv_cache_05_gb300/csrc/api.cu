@@ -8,10 +8,38 @@
 #include <cstring>
 #include <new>
 #include <string>
+#include <vector>
 
 #include "vqk_internal.cuh"
 
 using namespace vqk;
+
+// vq_kivi_step_host's state: two device slots for a step's inputs (the
+// token's K and V, the query), the copy stream that fills them, and per slot
+// the event its copy completes and the event its last step's kernels (which
+// read the slot) complete.
+struct StepIO {
+  cudaStream_t cs = nullptr;
+  void *slot[2] = {nullptr, nullptr};
+  cudaEvent_t copied[2] = {nullptr, nullptr};
+  cudaEvent_t used[2] = {nullptr, nullptr};
+  std::vector<int32_t> ones;
+  size_t off_v = 0, off_q = 0;
+  int next = 0;
+};
+
+static void free_step_io(StepIO *io) {
+  if (!io) return;
+  if (io->cs) cudaStreamSynchronize(io->cs);
+  for (int i = 0; i < 2; ++i) {
+    if (io->used[i]) cudaEventSynchronize(io->used[i]);
+    if (io->slot[i]) cudaFree(io->slot[i]);
+    if (io->copied[i]) cudaEventDestroy(io->copied[i]);
+    if (io->used[i]) cudaEventDestroy(io->used[i]);
+  }
+  if (io->cs) cudaStreamDestroy(io->cs);
+  delete io;
+}
 
 struct vq_kivi_cache {
   vq_kivi_params p;
@@ -36,6 +64,7 @@ struct vq_kivi_cache {
   // planned for (the plan is a search, redone when a flush moves T_q)
   int32_t age_tps;
   int32_t age_Tq[kMaxB];
+  StepIO *io;             // vq_kivi_step_host's slots (first call)
 };
 
 namespace {
@@ -580,6 +609,76 @@ int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
   return VQ_OK;
 }
 
+namespace {
+// the device address of pinned host memory, or nullptr when `p` is not
+// pinned host memory
+void *pinned_device_ptr(const void *p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+}  // namespace
+
+int vq_kivi_step_host(vq_kivi_cache *c, const void *h_k_new, const void *h_v_new,
+                      const void *h_q, float *h_out, float softmax_scale,
+                      void *stream) {
+  int rc = check_cache(c);
+  if (rc) return rc;
+  if (!h_k_new || !h_v_new || !h_q || !h_out)
+    return fail(VQ_ERR_ARG, "step_host: NULL argument");
+  if (!pinned_device_ptr(h_k_new) || !pinned_device_ptr(h_v_new) || !pinned_device_ptr(h_q))
+    return fail(VQ_ERR_ARG, "step_host: the inputs must be pinned host memory");
+  float *d_out = static_cast<float *>(pinned_device_ptr(h_out));
+  if (!d_out) return fail(VQ_ERR_ARG, "step_host: h_out must be pinned host memory");
+  const vq_kivi_params &p = c->p;
+  const size_t kv_bytes = (size_t)p.B * p.H_kv * p.D * sizeof(__half);
+  const size_t q_bytes = (size_t)p.B * p.H_q * p.D * sizeof(__half);
+  cudaError_t e;
+  if (!c->io) {
+    StepIO *io = new (std::nothrow) StepIO();
+    if (!io) return fail(VQ_ERR_OOM, "step_host: host allocation failed");
+    io->off_v = round_up(kv_bytes, 256);
+    io->off_q = io->off_v + round_up(kv_bytes, 256);
+    io->ones.assign(p.B, 1);
+    e = cudaStreamCreateWithFlags(&io->cs, cudaStreamNonBlocking);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+      e = cudaMalloc(&io->slot[i], io->off_q + q_bytes);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&io->copied[i], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&io->used[i], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) {
+      free_step_io(io);
+      return cuda_fail(e, "step_host: slot allocation");
+    }
+    c->io = io;
+  }
+  StepIO *io = c->io;
+  const int s = io->next;
+  cudaStream_t st = (cudaStream_t)stream;
+  uint8_t *slot = static_cast<uint8_t *>(io->slot[s]);
+  // the slot's previous step has read it (waiting on a never-recorded
+  // event returns at once)
+  e = cudaStreamWaitEvent(io->cs, io->used[s], 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(slot, h_k_new, kv_bytes, cudaMemcpyHostToDevice, io->cs);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(slot + io->off_v, h_v_new, kv_bytes, cudaMemcpyHostToDevice, io->cs);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(slot + io->off_q, h_q, q_bytes, cudaMemcpyHostToDevice, io->cs);
+  if (e == cudaSuccess) e = cudaEventRecord(io->copied[s], io->cs);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, io->copied[s], 0);
+  if (e != cudaSuccess) return cuda_fail(e, "step_host: input copy");
+  io->next ^= 1;
+  rc = vq_kivi_append(c, slot, slot + io->off_v, 1, io->ones.data(), stream);
+  if (rc == VQ_OK) rc = vq_kivi_decode_attend(c, slot + io->off_q, d_out, softmax_scale, stream);
+  // the slot is free again once this step's kernels have run
+  e = cudaEventRecord(io->used[s], st);
+  if (rc == VQ_OK && e != cudaSuccess) return cuda_fail(e, "step_host: event");
+  return rc;
+}
+
 int vq_kivi_attend_multi(vq_kivi_cache *c, const void *q, int32_t S_q,
                          float *out, float softmax_scale, void *stream) {
   int rc = check_cache(c);
@@ -636,6 +735,8 @@ int vq_kivi_free(vq_kivi_cache *c) {
   int dev = -1;
   cudaGetDevice(&dev);
   if (dev != c->device) cudaSetDevice(c->device);
+  free_step_io(c->io);
+  c->io = nullptr;
   cudaError_t e = cudaFreeAsync(c->block, c->last_stream);
   cudaError_t e2 = cudaStreamSynchronize(c->last_stream);
   if (dev != c->device && dev >= 0) cudaSetDevice(dev);

@@ -86,6 +86,7 @@ def test_null_handles(vqlib):
     assert vqlib.vq_kivi_set_split_tokens(None, 0) == -1
     assert vqlib.vq_kivi_decode_attend(None, None, None, 0.0, None) == -1
     assert vqlib.vq_kivi_append(None, None, None, 0, None, None) == -1
+    assert vqlib.vq_kivi_step_host(None, None, None, None, None, 0.0, None) == -1
     assert vqlib.vq_kivi_export(None, 0, None, 0, None) == -1
     assert isinstance(vqlib.vq_kivi_launch_count(), int)
 
