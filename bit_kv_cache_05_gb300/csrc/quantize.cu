@@ -89,6 +89,40 @@ __device__ __forceinline__ void quant2(float2 x, float mn, float scale,
   c1 = (uint32_t)r.y;
 }
 
+// quant2's fast path only: the codes from the reciprocal, and whether each
+// value is near a half-integer (where quant2 takes the correctly rounded
+// quotient instead; the caller redoes those values with quant_exact).  No
+// branch, so a loop over many pairs carries no divergence bookkeeping.
+__device__ __forceinline__ void quant2_flag(float2 x, float mn, float rcp,
+                                            uint32_t &c0, uint32_t &c1,
+                                            bool &n0, bool &n1) {
+  const float2 d = __fadd2_rn(x, make_float2(-mn, -mn));
+  const float2 t = __fmul2_rn(d, make_float2(rcp, rcp));
+  const float2 r = make_float2(rintf(t.x), rintf(t.y));
+  const float2 f = __fadd2_rn(t, make_float2(-r.x, -r.y));
+  const float2 lim = __fadd2_rn(make_float2(0.5f, 0.5f),
+                                __ffma2_rn(t, make_float2(-9.5367431640625e-7f, -9.5367431640625e-7f),
+                                           make_float2(-1e-9f, -1e-9f)));
+  n0 = fabsf(f.x) >= lim.x;
+  n1 = fabsf(f.y) >= lim.y;
+  c0 = (uint32_t)r.x;
+  c1 = (uint32_t)r.y;
+}
+
+// 16-byte asynchronous global -> shared copy (completed by cp.async.wait_group)
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+
+// quant2's near-tie path for one value: rint of the correctly rounded
+// quotient
+__device__ __noinline__ uint32_t quant_exact(float x, float mn, float scale) {
+  return (uint32_t)rintf(__fdiv_rn(__fsub_rn(x, mn), scale));
+}
+
 // Packs the g x D code tile in shared memory (row stride cs bytes) into rows
 // of D*BITS/8 bytes and stores it with 16-byte vector stores (the tile is
 // contiguous in global).
@@ -344,8 +378,9 @@ k_flush(Geometry geo, Planes pl, const __half *__restrict__ Kin,
 // g and the code width known at compile time: every index of the tile, the
 // code tile and the packers is a constant or a shift, the g source rows of
 // the group are looked up once (the residual ring's slot arithmetic per
-// token, not per 16-byte chunk), and each thread keeps its key column and
-// its value group in registers from the one read to the quantization.
+// token, not per 16-byte chunk), the key and value tiles arrive together
+// by asynchronous copies, and the near-tie test flags values in one
+// branch-free pass that a rare second pass redoes exactly.
 // Same arithmetic as k_flush, bit for bit.
 template <int BITS, int D, int G>
 __device__ __forceinline__ void store_frag_keys_t(const uint8_t *codes, uint8_t *dst) {
@@ -421,9 +456,11 @@ k_flush_t(Geometry geo, Planes pl, const __half *__restrict__ Kin,
   pdl_wait_and_release();
   constexpr int levels = (1 << BITS) - 1, CS = D + 4, ROW = D * BITS / 8;
   constexpr int NJ = D / G, CPR = D / 8;
+  constexpr int VS = D + 8;   // value row stride (halves): 16 bytes of padding
   extern __shared__ __align__(16) unsigned char fsm[];
   __half *tile = reinterpret_cast<__half *>(fsm);                 // [G][D]
   uint8_t *codes = fsm + (size_t)G * D * sizeof(__half);         // [G][CS]
+  __half *vtile = reinterpret_cast<__half *>(codes + G * CS);    // [G][VS]
   __shared__ const __half *sk[G], *sv[G];
   __shared__ uint32_t sinkm[4];
   const int c = threadIdx.x, item = blockIdx.x, h = blockIdx.y;
@@ -451,13 +488,15 @@ k_flush_t(Geometry geo, Planes pl, const __half *__restrict__ Kin,
     const int p = pl.sink_pos[bh * geo.n_sink + c];
     if (p >= P0 && p < P0 + G) atomicOr(&sinkm[(p - P0) >> 5], 1u << ((p - P0) & 31));
   }
-  // key tile: G rows of D fp16 values, 16-byte loads
+  // the key and value tiles (G rows of D fp16 values each) by 16-byte
+  // asynchronous copies, all in flight together
 #pragma unroll
   for (int k = 0; k < G * CPR / D; ++k) {
     const int idx = c + k * D, i = idx / CPR, c8 = (idx % CPR) * 8;
-    *reinterpret_cast<uint4 *>(tile + i * D + c8) =
-        *reinterpret_cast<const uint4 *>(sk[i] + c8);
+    cp_async16(tile + i * D + c8, sk[i] + c8);
+    cp_async16(vtile + i * VS + c8, sv[i] + c8);
   }
+  asm volatile("cp.async.commit_group;\n cp.async.wait_group 0;" ::: "memory");
   __syncthreads();
   auto is_sink = [&](int i) { return sinks && ((sinkm[i >> 5] >> (i & 31)) & 1u); };
 
@@ -500,12 +539,22 @@ k_flush_t(Geometry geo, Planes pl, const __half *__restrict__ Kin,
       const unsigned m = __reduce_max_sync(0xffffffffu, (unsigned)__half_as_ushort(sh));
       if ((c & 31) == 0) atomicMax(pl.ksmax + bh, m);
     }
+    uint64_t near = 0;   // bit i: token i's value is near a half-integer
 #pragma unroll
     for (int k = 0; k < G / 2; ++k) {
       uint32_t c0, c1;
-      quant2(__half22float2(col[k]), mn, scale, rcp, c0, c1);
+      bool n0, n1;
+      quant2_flag(__half22float2(col[k]), mn, rcp, c0, c1, n0, n1);
+      near |= ((uint64_t)n0 << (2 * k)) | ((uint64_t)n1 << (2 * k + 1));
       codes[(2 * k) * CS + c] = is_sink(2 * k) ? 0 : (uint8_t)c0;
       codes[(2 * k + 1) * CS + c] = is_sink(2 * k + 1) ? 0 : (uint8_t)c1;
+    }
+    // the rare near-ties: the correctly rounded quotient (scale == 0 gives
+    // rcp = 0, t = 0 and no near-tie)
+    while (near) {
+      const int i = __ffsll((long long)near) - 1;
+      near &= near - 1;
+      if (!is_sink(i)) codes[i * CS + c] = (uint8_t)quant_exact(__half2float(tile[i * D + c]), mn, scale);
     }
   }
   __syncthreads();
@@ -523,7 +572,7 @@ k_flush_t(Geometry geo, Planes pl, const __half *__restrict__ Kin,
   {
     const int i = c / NJ, j = c % NJ;
     const bool empty = is_sink(i);   // a sink's value groups have no member
-    const uint4 *row = reinterpret_cast<const uint4 *>(sv[i] + j * G);
+    const uint4 *row = reinterpret_cast<const uint4 *>(vtile + i * VS + j * G);
     uint4 u[G / 8];
 #pragma unroll
     for (int k = 0; k < G / 8; ++k) u[k] = row[k];
@@ -543,6 +592,7 @@ k_flush_t(Geometry geo, Planes pl, const __half *__restrict__ Kin,
     const float scale = empty ? 0.f : __fdiv_rn(__fadd_rn(__fsub_rn(mx, mn), 0.0f), (float)levels);
     const float rcp = scale != 0.0f ? __frcp_rn(scale) : 0.0f;
     uint32_t *crow = reinterpret_cast<uint32_t *>(codes + i * CS + j * G);
+    uint64_t near = 0;   // bit v: value v of the group is near a half-integer
 #pragma unroll
     for (int k = 0; k < G / 8; ++k) {
       const __half2 *h4 = reinterpret_cast<const __half2 *>(&u[k]);
@@ -550,11 +600,19 @@ k_flush_t(Geometry geo, Planes pl, const __half *__restrict__ Kin,
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         uint32_t c0, c1;
-        quant2(__half22float2(h4[e]), mn, scale, rcp, c0, c1);
+        bool n0, n1;
+        quant2_flag(__half22float2(h4[e]), mn, rcp, c0, c1, n0, n1);
+        near |= ((uint64_t)n0 << (8 * k + 2 * e)) | ((uint64_t)n1 << (8 * k + 2 * e + 1));
         w[e >> 1] |= (c0 | (c1 << 8)) << (16 * (e & 1));
       }
       crow[2 * k] = w[0];
       crow[2 * k + 1] = w[1];
+    }
+    // the rare near-ties
+    while (near) {
+      const int v = __ffsll((long long)near) - 1;
+      near &= near - 1;
+      codes[i * CS + j * G + v] = (uint8_t)quant_exact(__half2float(vtile[i * VS + j * G + v]), mn, scale);
     }
     const size_t vidx = (bh * geo.Tcap + P0 + i) * NJ + j;
     pl.Vs[vidx] = __float2half_rn(scale);
@@ -622,11 +680,13 @@ cudaError_t launch_flush(const Geometry &geo, const Planes &pl,
   if (total_groups <= 0) return cudaSuccess;
   dim3 grid(total_groups, geo.H_kv);
   const size_t smem = (size_t)geo.g * (geo.D * sizeof(__half) + geo.D + 4);
+  // the specialised flush also stages the value tile (rows padded by 8 halves)
+  const size_t smem_t = smem + (size_t)geo.g * (geo.D + 8) * sizeof(__half);
   // the common shapes: the compile-time specialised flush
 #define VQK_FT(BB, DD, GG)                                                     \
   if (geo.bits == BB && geo.D == DD && geo.g == GG) {                          \
     const cudaError_t e2 = launch_pdl(k_flush_t<BB, DD, GG>, grid, dim3(DD),   \
-                                      smem, st, geo, pl, Kin, Vin, in_stride,  \
+                                      smem_t, st, geo, pl, Kin, Vin, in_stride, \
                                       tab);                                    \
     count_launch();                                                            \
     return e2;                                                                 \
