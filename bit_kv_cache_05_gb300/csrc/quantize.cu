@@ -93,20 +93,24 @@ __device__ __forceinline__ void quant2(float2 x, float mn, float scale,
 // value is near a half-integer (where quant2 takes the correctly rounded
 // quotient instead; the caller redoes those values with quant_exact).  No
 // branch, so a loop over many pairs carries no divergence bookkeeping.
+// The rounding adds 2^23: for 0 <= t < 2^22 the sum's low mantissa bits
+// are rint(t) (round to nearest, ties to even, as rintf), so the code comes
+// out of the float's bits with no conversion.
 __device__ __forceinline__ void quant2_flag(float2 x, float mn, float rcp,
                                             uint32_t &c0, uint32_t &c1,
                                             bool &n0, bool &n1) {
   const float2 d = __fadd2_rn(x, make_float2(-mn, -mn));
   const float2 t = __fmul2_rn(d, make_float2(rcp, rcp));
-  const float2 r = make_float2(rintf(t.x), rintf(t.y));
+  const float2 tm = __fadd2_rn(t, make_float2(8388608.f, 8388608.f));
+  const float2 r = __fadd2_rn(tm, make_float2(-8388608.f, -8388608.f));
   const float2 f = __fadd2_rn(t, make_float2(-r.x, -r.y));
   const float2 lim = __fadd2_rn(make_float2(0.5f, 0.5f),
                                 __ffma2_rn(t, make_float2(-9.5367431640625e-7f, -9.5367431640625e-7f),
                                            make_float2(-1e-9f, -1e-9f)));
   n0 = fabsf(f.x) >= lim.x;
   n1 = fabsf(f.y) >= lim.y;
-  c0 = (uint32_t)r.x;
-  c1 = (uint32_t)r.y;
+  c0 = __float_as_uint(tm.x) & 0xFFu;
+  c1 = __float_as_uint(tm.y) & 0xFFu;
 }
 
 // 16-byte asynchronous global -> shared copy (completed by cp.async.wait_group)
@@ -546,15 +550,27 @@ k_flush_t(Geometry geo, Planes pl, const __half *__restrict__ Kin,
       bool n0, n1;
       quant2_flag(__half22float2(col[k]), mn, rcp, c0, c1, n0, n1);
       near |= ((uint64_t)n0 << (2 * k)) | ((uint64_t)n1 << (2 * k + 1));
-      codes[(2 * k) * CS + c] = is_sink(2 * k) ? 0 : (uint8_t)c0;
-      codes[(2 * k + 1) * CS + c] = is_sink(2 * k + 1) ? 0 : (uint8_t)c1;
+      codes[(2 * k) * CS + c] = (uint8_t)c0;
+      codes[(2 * k + 1) * CS + c] = (uint8_t)c1;
     }
     // the rare near-ties: the correctly rounded quotient (scale == 0 gives
     // rcp = 0, t = 0 and no near-tie)
     while (near) {
       const int i = __ffsll((long long)near) - 1;
       near &= near - 1;
-      if (!is_sink(i)) codes[i * CS + c] = (uint8_t)quant_exact(__half2float(tile[i * D + c]), mn, scale);
+      codes[i * CS + c] = (uint8_t)quant_exact(__half2float(tile[i * D + c]), mn, scale);
+    }
+    // sink tokens hold code 0 (their rows are kept in fp16)
+    if (sinks) {
+#pragma unroll
+      for (int w = 0; w < (G + 31) / 32; ++w) {
+        uint32_t m = sinkm[w];
+        while (m) {
+          const int i = 32 * w + __ffs(m) - 1;
+          m &= m - 1;
+          codes[i * CS + c] = 0;
+        }
+      }
     }
   }
   __syncthreads();
