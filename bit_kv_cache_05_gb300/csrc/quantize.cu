@@ -395,6 +395,24 @@ __device__ __forceinline__ void store_frag_keys_t(const uint8_t *codes, uint8_t 
     const int w = threadIdx.x + k * D;
     const int i = w / WPR, wi = w % WPR;
     const int tig = wi / NWD, hw = wi % NWD;
+    if constexpr (BITS == 4) {
+      // the word's 8 fields are channels 16 ks + 4 tig + e, e = 0 ... 3, of
+      // K-steps ks = 2 hw and 2 hw + 1: two 4-byte runs of the token's code
+      // row.  Field (r, s) of the word (e = 2 (r & 1) + s) sits at bit
+      // 16 s + 4 r: bytes e0, e1 of a run go to bits 0 and 16, bytes e2,
+      // e3 to bits 4 and 20, the second run 8 bits higher.
+      uint32_t acc = 0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t x = *reinterpret_cast<const uint32_t *>(
+            codes + i * CS + 16 * (2 * hw + h) + 4 * tig);
+        const uint32_t lo = __byte_perm(x, 0u, 0x4140);   // e0 | e1 << 16
+        const uint32_t hi = __byte_perm(x, 0u, 0x4342);   // e2 | e3 << 16
+        acc |= (lo | (hi << 4)) << (8 * h);
+      }
+      reinterpret_cast<uint32_t *>(dst)[w] = acc;
+      continue;
+    }
     uint32_t acc = 0;
 #pragma unroll
     for (int s = 0; s < 2; ++s)
