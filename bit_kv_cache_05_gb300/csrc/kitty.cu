@@ -46,37 +46,102 @@ __device__ __forceinline__ const __half *src_row(const Geometry &geo, const Plan
                    : in + (bh * in_stride + (p - split)) * geo.D;
 }
 
-// One CTA of kRankThreads per (kv head, sequence): NS = kRankThreads / D
-// slices of one thread per channel take NS consecutive groups of this
-// flush at a time.  Each slice sums its group's keys (m and m^2 per
-// channel, its rows' loads all in flight), the slices' sums are carried in
-// shared memory (slice j adds slices 0 ... j to the running sums), and
-// every slice ranks its channels by the running variance through its
-// group's last token.
+// The ranking is a scan over a flush's groups (a group's ranking uses the
+// running sums through its last token), cut into C chunks per (sequence,
+// kv head) so that it spreads over the GPU: k_kitty_chunk_sums sums each
+// chunk's keys, k_kitty_rank ranks each chunk's groups from the running
+// sums before the chunk (the cache's sums plus the earlier chunks' totals),
+// k_kitty_sums_update adds every chunk's total to the cache's sums.  The
+// totals (int64 sum m, 128-bit sum m^2 as two words, per channel) sit in a
+// scratch area of 3 * D words per (sequence, kv head, chunk).
 constexpr int kRankThreads = 1024;
 
+// groups [k0, k1) of chunk ch of sequence b's n groups
+__device__ __forceinline__ void chunk_range(int n, int C, int ch, int &k0, int &k1) {
+  k0 = (int)((int64_t)n * ch / C);
+  k1 = (int)((int64_t)n * (ch + 1) / C);
+}
+
+// One CTA of kRankThreads per (chunk, kv head, sequence): NS = kRankThreads
+// / D slices of one thread per channel take the chunk's groups NS apart and
+// sum their keys (the rows' loads in flight together); the slices' sums are
+// added in shared memory.
+__global__ void __launch_bounds__(kRankThreads)
+k_kitty_chunk_sums(Geometry geo, Planes pl, const __half *__restrict__ Kin,
+                   int64_t in_stride, FlushTable tab, int C,
+                   unsigned long long *__restrict__ scratch) {
+  __shared__ unsigned long long r1[kRankThreads], r2lo[kRankThreads], r2hi[kRankThreads];
+  const int D = geo.D, g = geo.g, NS = kRankThreads / D;
+  const int c = threadIdx.x % D, sl = threadIdx.x / D;
+  const int ch = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int n = tab.prefix[b + 1] - tab.prefix[b];
+  int k0, k1;
+  chunk_range(n, C, ch, k0, k1);
+  const size_t bh = (size_t)b * geo.H_kv + h;
+  const int split = tab.src_split[b];
+  long long s1 = 0;
+  u128 s2 = 0;
+  for (int k = k0 + sl; k < k1; k += NS) {
+    const int P0 = tab.first_pos[b] + k * g;
+#pragma unroll 8
+    for (int i = 0; i < g; ++i) {
+      const __half *row = src_row(geo, pl, Kin, in_stride, bh, P0 + i, split);
+      const long long m = f16_units(__half_as_ushort(row[c]));
+      s1 += m;
+      s2 += (u128)((__int128)m * m);
+    }
+  }
+  r1[threadIdx.x] = (unsigned long long)s1;
+  r2lo[threadIdx.x] = (unsigned long long)s2;
+  r2hi[threadIdx.x] = (unsigned long long)(s2 >> 64);
+  __syncthreads();
+  if (sl == 0) {
+    for (int j = 1; j < NS; ++j) {
+      s1 += (long long)r1[j * D + c];
+      s2 += ((u128)r2hi[j * D + c] << 64) | r2lo[j * D + c];
+    }
+    unsigned long long *dst = scratch + ((bh * C + ch) * 3) * D;
+    dst[c] = (unsigned long long)s1;
+    dst[D + c] = (unsigned long long)s2;
+    dst[2 * D + c] = (unsigned long long)(s2 >> 64);
+  }
+}
+
+// One CTA of kRankThreads per (chunk, kv head, sequence): the running sums
+// before the chunk, then its groups NS at a time: each slice sums its
+// group's keys, the slices' sums are carried in shared memory (slice j adds
+// slices 0 ... j to the running sums), and every slice ranks its channels by
+// the running variance through its group's last token.
 __global__ void __launch_bounds__(kRankThreads)
 k_kitty_rank(Geometry geo, Planes pl, const __half *__restrict__ Kin,
-             int64_t in_stride, FlushTable tab) {
+             int64_t in_stride, FlushTable tab, int C,
+             const unsigned long long *__restrict__ scratch) {
   extern __shared__ unsigned long long rsm[];
   const int D = geo.D, g = geo.g, NS = kRankThreads / D;
   const int c = threadIdx.x % D, sl = threadIdx.x / D;
   // per (slice, channel): the group's sums, then the running variance
   unsigned long long *q1 = rsm, *q2lo = q1 + NS * D, *q2hi = q2lo + NS * D;
   unsigned long long *vlo = q2hi + NS * D, *vhi = vlo + NS * D;
-  const int h = blockIdx.x, b = blockIdx.y;
+  const int ch = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int n = tab.prefix[b + 1] - tab.prefix[b];
-  if (n == 0) return;
+  int kb, ke;
+  chunk_range(n, C, ch, kb, ke);
+  if (kb >= ke) return;
   const size_t bh = (size_t)b * geo.H_kv + h;
   long long s1 = pl.ksum[bh * D + c];
   u128 s2 = ((u128)pl.ksq[(bh * D + c) * 2 + 1] << 64) | pl.ksq[(bh * D + c) * 2];
+  for (int j = 0; j < ch; ++j) {
+    const unsigned long long *t = scratch + ((bh * C + j) * 3) * D;
+    s1 += (long long)t[c];
+    s2 += ((u128)t[2 * D + c] << 64) | t[D + c];
+  }
   const int split = tab.src_split[b];
-  for (int k0 = 0; k0 < n; k0 += NS) {
+  for (int k0 = kb; k0 < ke; k0 += NS) {
     const int k = k0 + sl;
     const int P0 = tab.first_pos[b] + k * g;
     long long g1 = 0;
     u128 g2 = 0;
-    if (k < n) {
+    if (k < ke) {
 #pragma unroll 8
       for (int i = 0; i < g; ++i) {
         const __half *row = src_row(geo, pl, Kin, in_stride, bh, P0 + i, split);
@@ -99,7 +164,7 @@ k_kitty_rank(Geometry geo, Planes pl, const __half *__restrict__ Kin,
       if (j == sl) { r1 = s1; r2 = s2; }
     }
     u128 var = 0;
-    if (k < n) {
+    if (k < ke) {
       const u128 N = (u128)(P0 + g);
       const u128 a = (u128)(r1 < 0 ? -r1 : r1);
       var = N * r2 - a * a;
@@ -107,7 +172,7 @@ k_kitty_rank(Geometry geo, Planes pl, const __half *__restrict__ Kin,
     vlo[sl * D + c] = (unsigned long long)var;
     vhi[sl * D + c] = (unsigned long long)(var >> 64);
     __syncthreads();
-    if (k < n) {
+    if (k < ke) {
       int rank = 0;
       for (int o = 0; o < D; ++o) {
         const u128 vo = ((u128)vhi[sl * D + o] << 64) | vlo[sl * D + o];
@@ -119,11 +184,26 @@ k_kitty_rank(Geometry geo, Planes pl, const __half *__restrict__ Kin,
     }
     __syncthreads();
   }
-  if (sl == 0) {
-    pl.ksum[bh * D + c] = s1;
-    pl.ksq[(bh * D + c) * 2] = (unsigned long long)s2;
-    pl.ksq[(bh * D + c) * 2 + 1] = (unsigned long long)(s2 >> 64);
+}
+
+// The cache's running sums += every chunk's total: one thread per (channel,
+// kv head, sequence).
+__global__ void k_kitty_sums_update(Geometry geo, Planes pl, FlushTable tab, int C,
+                                    const unsigned long long *__restrict__ scratch) {
+  const int D = geo.D;
+  const int c = threadIdx.x, h = blockIdx.x, b = blockIdx.y;
+  if (tab.prefix[b + 1] == tab.prefix[b]) return;
+  const size_t bh = (size_t)b * geo.H_kv + h;
+  long long s1 = pl.ksum[bh * D + c];
+  u128 s2 = ((u128)pl.ksq[(bh * D + c) * 2 + 1] << 64) | pl.ksq[(bh * D + c) * 2];
+  for (int j = 0; j < C; ++j) {
+    const unsigned long long *t = scratch + ((bh * C + j) * 3) * D;
+    s1 += (long long)t[c];
+    s2 += ((u128)t[2 * D + c] << 64) | t[D + c];
   }
+  pl.ksum[bh * D + c] = s1;
+  pl.ksq[(bh * D + c) * 2] = (unsigned long long)s2;
+  pl.ksq[(bh * D + c) * 2 + 1] = (unsigned long long)(s2 >> 64);
 }
 
 // One CTA per (group, kv head), one thread per channel: per channel a 4- or
@@ -208,13 +288,35 @@ cudaError_t launch_flush_kitty(const Geometry &geo, const Planes &pl,
                                int64_t in_stride, const FlushTable &tab,
                                int total_groups, cudaStream_t st) {
   if (total_groups <= 0) return cudaSuccess;
+  // chunks per (sequence, kv head): enough CTAs to spread over the GPU,
+  // each chunk at least a step of NS groups, the totals within the decode's
+  // partial buffer (idle during a flush; at least B * H_q * max_items *
+  // (D + 2) floats)
+  const int NS = kRankThreads / geo.D;
+  int n_max = 0;
+  for (int b = 0; b < geo.B; ++b) {
+    const int n = tab.prefix[b + 1] - tab.prefix[b];
+    if (n > n_max) n_max = n;
+  }
+  const size_t part_words = (size_t)geo.B * geo.H_q * geo.max_items * (geo.D + 2) / 2;
+  const size_t per_chunk = (size_t)geo.B * geo.H_kv * 3 * geo.D;
+  int C = n_max / NS;
+  if (C > 16) C = 16;
+  if ((size_t)C * per_chunk > part_words) C = (int)(part_words / per_chunk);
+  if (C < 1) C = 1;
+  unsigned long long *scratch = reinterpret_cast<unsigned long long *>(pl.part);
+  const dim3 grid(C, geo.H_kv, geo.B);
+  k_kitty_chunk_sums<<<grid, kRankThreads, 0, st>>>(geo, pl, Kin, in_stride, tab, C, scratch);
+  count_launch();
   const size_t rsmem = (size_t)5 * kRankThreads * sizeof(unsigned long long);
   if (rsmem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k_kitty_rank, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)rsmem);
     if (e != cudaSuccess) return e;
   }
-  k_kitty_rank<<<dim3(geo.H_kv, geo.B), kRankThreads, rsmem, st>>>(geo, pl, Kin, in_stride, tab);
+  k_kitty_rank<<<grid, kRankThreads, rsmem, st>>>(geo, pl, Kin, in_stride, tab, C, scratch);
+  count_launch();
+  k_kitty_sums_update<<<dim3(geo.H_kv, geo.B), geo.D, 0, st>>>(geo, pl, tab, C, scratch);
   count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
