@@ -263,7 +263,7 @@ int vq_kivi_quantize_ex(const vq_kivi_params *p, const vq_kivi_options *opt,
   // 2- and 4-bit caches decoded on the tensor cores keep their codes in the
   // order the MMA fragments consume them
   geo.layout = c->use_mma && (p->bits == 2 || p->bits == 4) ? kLayoutFrag : kLayoutPacked;
-  size_t n_part = (size_t)p->B * p->H_q * geo.max_items * (p->D + 2);
+  size_t n_part = part_floats(geo);
   if (c->use_mma) {
     const size_t n_mma = mma_part_floats(geo, c->plan);
     if (n_mma > n_part) n_part = n_mma;

@@ -290,16 +290,16 @@ cudaError_t launch_flush_kitty(const Geometry &geo, const Planes &pl,
   if (total_groups <= 0) return cudaSuccess;
   // chunks per (sequence, kv head): enough CTAs to spread over the GPU,
   // each chunk at least a step of NS groups, the totals within the decode's
-  // partial buffer (idle during a flush; at least B * H_q * max_items *
-  // (D + 2) floats)
+  // partial buffer (idle during a flush; part_floats(geo) floats, at least
+  // one chunk's totals)
   const int NS = kRankThreads / geo.D;
   int n_max = 0;
   for (int b = 0; b < geo.B; ++b) {
     const int n = tab.prefix[b + 1] - tab.prefix[b];
     if (n > n_max) n_max = n;
   }
-  const size_t part_words = (size_t)geo.B * geo.H_q * geo.max_items * (geo.D + 2) / 2;
-  const size_t per_chunk = (size_t)geo.B * geo.H_kv * 3 * geo.D;
+  const size_t part_words = part_floats(geo) / 2;
+  const size_t per_chunk = kitty_chunk_words(geo);
   int C = n_max / NS;
   if (C > 16) C = 16;
   if ((size_t)C * per_chunk > part_words) C = (int)(part_words / per_chunk);

@@ -65,6 +65,21 @@ struct Geometry {
   int age_bits[3] = {0, 0, 0};
 };
 
+// 64-bit words of one chunk of a Kitty flush's ranking totals: an int64 sum
+// and a 128-bit sum of squares per (sequence, kv head, channel)
+inline size_t kitty_chunk_words(const Geometry &geo) {
+  return (size_t)geo.B * geo.H_kv * 3 * geo.D;
+}
+
+// floats of the decode's partial buffer (CUDA-core and staged decodes):
+// B * H_q * max_items * (D + 2).  A Kitty flush borrows the buffer for its
+// ranking totals, so a Kitty cache's holds at least one chunk of them.
+inline size_t part_floats(const Geometry &geo) {
+  size_t n = (size_t)geo.B * geo.H_q * geo.max_items * (geo.D + 2);
+  if (geo.kitty && 2 * kitty_chunk_words(geo) > n) n = 2 * kitty_chunk_words(geo);
+  return n;
+}
+
 // AgeTieredKV tier of group G of a sequence of S tokens
 __host__ __device__ inline int age_tier(const Geometry &geo, int S, int G) {
   const int age = S - (G + 1) * geo.g;

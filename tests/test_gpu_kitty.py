@@ -86,14 +86,25 @@ def test_kitty_planes_and_decode(lib, name, lens, hi, group):
     c.close()
 
 
-def test_kitty_appends_match_the_oracle(lib):
+APPEND_CASES = [
+    ("gqa_serving", [100, 37], (1, 7, 64, 100, 128)),
+    # one query head per kv head and a short cache: the decode's partial
+    # buffer, which a flush borrows for its ranking totals, is small; single
+    # tokens up to a flush, then a few more
+    ("pages_S512", [500], (1,) * 40 + (3,)),
+]
+
+
+@pytest.mark.parametrize("name,lens,chunks", APPEND_CASES,
+                         ids=[c[0] for c in APPEND_CASES])
+def test_kitty_appends_match_the_oracle(lib, name, lens, chunks):
     """Appends in several chunk sizes: the running sums carry over between
     flushes exactly as in the oracle's incremental procedure."""
     import oracle
     from bit_kv_cache_05_gb300.cache import KiviCache
-    w = synth.shrink(synth.workload("gqa_serving"), [100, 37], n_append=0)
+    w = synth.shrink(synth.workload(name), lens, n_append=0)
     inp = synth.make_inputs(w, seed=61, device="cpu")
-    n_tot = 300
+    n_tot = sum(chunks)
     g = torch.Generator().manual_seed(4)
     Kn = (torch.randn(w.B, w.H_kv, n_tot, w.D, generator=g) *
           torch.linspace(0.2, 6, w.D)).half()
@@ -105,7 +116,7 @@ def test_kitty_appends_match_the_oracle(lib):
                             max(w.seq_lens) + n_tot, kitty_hi=32)
     oc.quantize(inp["K"].numpy(), inp["V"].numpy(), w.seq_lens)
     at = 0
-    for chunk in (1, 7, 64, 100, 128):
+    for chunk in chunks:
         c.append(Kn[:, :, at:at + chunk].contiguous().cuda(),
                  Vn[:, :, at:at + chunk].contiguous().cuda(), [chunk] * w.B)
         oc.append(Kn[:, :, at:at + chunk].numpy(), Vn[:, :, at:at + chunk].numpy(),
