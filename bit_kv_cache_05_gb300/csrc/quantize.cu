@@ -95,20 +95,23 @@ __device__ __forceinline__ void quant2(float2 x, float mn, float scale,
 // branch, so a loop over many pairs carries no divergence bookkeeping.
 // The rounding adds 2^23: for 0 <= t < 2^22 the sum's low mantissa bits
 // are rint(t) (round to nearest, ties to even, as rintf), so the code comes
-// out of the float's bits with no conversion.
+// out of the float's bits with no conversion.  Within a group t stays below
+// LEVELS + 1, so the band of quant2, 2^-20 t + 1e-9, is inside the constant
+// band (LEVELS + 1) 2^-20: flagging that band flags every value quant2
+// would send to the exact quotient (and a few more, about 2 (LEVELS + 1)
+// 2^-20 of the values, which the exact quotient gives the same code).
+template <int LEVELS>
 __device__ __forceinline__ void quant2_flag(float2 x, float mn, float rcp,
                                             uint32_t &c0, uint32_t &c1,
                                             bool &n0, bool &n1) {
+  constexpr float kLim = 0.5f - (LEVELS + 1) * 9.5367431640625e-7f;
   const float2 d = __fadd2_rn(x, make_float2(-mn, -mn));
   const float2 t = __fmul2_rn(d, make_float2(rcp, rcp));
   const float2 tm = __fadd2_rn(t, make_float2(8388608.f, 8388608.f));
   const float2 r = __fadd2_rn(tm, make_float2(-8388608.f, -8388608.f));
   const float2 f = __fadd2_rn(t, make_float2(-r.x, -r.y));
-  const float2 lim = __fadd2_rn(make_float2(0.5f, 0.5f),
-                                __ffma2_rn(t, make_float2(-9.5367431640625e-7f, -9.5367431640625e-7f),
-                                           make_float2(-1e-9f, -1e-9f)));
-  n0 = fabsf(f.x) >= lim.x;
-  n1 = fabsf(f.y) >= lim.y;
+  n0 = fabsf(f.x) >= kLim;
+  n1 = fabsf(f.y) >= kLim;
   c0 = __float_as_uint(tm.x) & 0xFFu;
   c1 = __float_as_uint(tm.y) & 0xFFu;
 }
@@ -471,8 +474,14 @@ __device__ __forceinline__ void store_packed_tile_t(const uint8_t *codes, uint8_
   }
 }
 
+// CTAs per SM the register budget is cut for: the shared memory of a
+// 64-token group of 128 channels (41 KB with both staged tiles) leaves room
+// for five, which at most 96 registers a thread allow (four at 100)
+template <int D, int G>
+constexpr int flush_min_ctas() { return D * G == 128 * 64 || D * G == 128 * 32 ? 5 : 1; }
+
 template <int BITS, int D, int G>
-__global__ void __launch_bounds__(D)
+__global__ void __launch_bounds__(D, flush_min_ctas<D, G>())
 k_flush_t(Geometry geo, Planes pl, const __half *__restrict__ Kin,
           const __half *__restrict__ Vin, int64_t in_stride, FlushTable tab) {
   pdl_wait_and_release();
@@ -566,7 +575,7 @@ k_flush_t(Geometry geo, Planes pl, const __half *__restrict__ Kin,
     for (int k = 0; k < G / 2; ++k) {
       uint32_t c0, c1;
       bool n0, n1;
-      quant2_flag(__half22float2(col[k]), mn, rcp, c0, c1, n0, n1);
+      quant2_flag<levels>(__half22float2(col[k]), mn, rcp, c0, c1, n0, n1);
       near |= ((uint64_t)n0 << (2 * k)) | ((uint64_t)n1 << (2 * k + 1));
       codes[(2 * k) * CS + c] = (uint8_t)c0;
       codes[(2 * k + 1) * CS + c] = (uint8_t)c1;
@@ -635,7 +644,7 @@ k_flush_t(Geometry geo, Planes pl, const __half *__restrict__ Kin,
       for (int e = 0; e < 4; ++e) {
         uint32_t c0, c1;
         bool n0, n1;
-        quant2_flag(__half22float2(h4[e]), mn, rcp, c0, c1, n0, n1);
+        quant2_flag<levels>(__half22float2(h4[e]), mn, rcp, c0, c1, n0, n1);
         near |= ((uint64_t)n0 << (8 * k + 2 * e)) | ((uint64_t)n1 << (8 * k + 2 * e + 1));
         w[e >> 1] |= (c0 | (c1 << 8)) << (16 * (e & 1));
       }
@@ -663,29 +672,39 @@ k_flush_t(Geometry geo, Planes pl, const __half *__restrict__ Kin,
   }
 }
 
-// Residual ring writes: 16-byte chunks of fp16 rows.
+// Residual ring writes: 16-byte chunks of fp16 rows.  The rows come from
+// the input, complete before this grid starts (the kernel before it in the
+// stream releases it only after its own wait); the ring slots they go to
+// may still be read by that kernel (a flush reads the old residual rows, a
+// merge the window).  So each thread loads its chunks, then waits, then
+// stores: the loads overlap the previous kernel's end.
 __global__ void __launch_bounds__(kThreads)
 k_tail(Geometry geo, Planes pl, const __half *__restrict__ Kin,
        const __half *__restrict__ Vin, int64_t in_stride, TailTable tab,
        int total) {
-  pdl_wait_and_release();
   const int D = geo.D;
   const int cpr = D / 8;                       // 16-byte chunks per row
   const int rows_per_block = kThreads / cpr;
   const int tok = blockIdx.x * rows_per_block + threadIdx.x / cpr;
   const int ch = (threadIdx.x % cpr) * 8;
-  if (tok >= total) return;
-  const int h = blockIdx.y;
-  const int b = find_seq(tab.prefix, geo.B, tok);
-  const int i = tok - tab.prefix[b];
-  const size_t bh = (size_t)b * geo.H_kv + h;
-  const int64_t src = (int64_t)(bh * in_stride + tab.row0[b] + i) * D + ch;
-  const int slot = (tab.pos0[b] + i) % geo.Rcap;
-  const size_t dst = (bh * geo.Rcap + slot) * D + ch;
-  *reinterpret_cast<uint4 *>(pl.Kr + dst) =
-      *reinterpret_cast<const uint4 *>(Kin + src);
-  *reinterpret_cast<uint4 *>(pl.Vr + dst) =
-      *reinterpret_cast<const uint4 *>(Vin + src);
+  const bool ok = tok < total;
+  uint4 kx = make_uint4(0u, 0u, 0u, 0u), vx = kx;
+  size_t dst = 0;
+  if (ok) {
+    const int h = blockIdx.y;
+    const int b = find_seq(tab.prefix, geo.B, tok);
+    const int i = tok - tab.prefix[b];
+    const size_t bh = (size_t)b * geo.H_kv + h;
+    const int64_t src = (int64_t)(bh * in_stride + tab.row0[b] + i) * D + ch;
+    const int slot = (tab.pos0[b] + i) % geo.Rcap;
+    dst = (bh * geo.Rcap + slot) * D + ch;
+    kx = *reinterpret_cast<const uint4 *>(Kin + src);
+    vx = *reinterpret_cast<const uint4 *>(Vin + src);
+  }
+  pdl_wait_and_release();
+  if (!ok) return;
+  *reinterpret_cast<uint4 *>(pl.Kr + dst) = kx;
+  *reinterpret_cast<uint4 *>(pl.Vr + dst) = vx;
 }
 
 // Residual ring -> canonical linear layout (slot i = token T_q + i), zero
