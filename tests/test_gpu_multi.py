@@ -62,7 +62,7 @@ CASES = [
     # (workload recipe, lengths, S_q values)
     ("tiny", [256], (1, 5, 40, 129)),
     ("pages_S512", [700, 333], (3, 64, 200)),
-    ("gqa_serving", [900, 260, 517], (1, 7, 33, 100)),
+    ("gqa_serving", [900, 260, 517], (1, 7, 33, 70, 100)),   # 70: 3 tiles of 32
     ("int4_append", [1000, 450], (2, 65, 130)),
 ]
 
