@@ -14,30 +14,17 @@
 
 using namespace vqk;
 
-// vq_kivi_step_host's state: two device slots for a step's inputs (the
-// token's K and V, the query), the copy stream that fills them, and per slot
-// the event its copy completes and the event its last step's kernels (which
-// read the slot) complete.
+// vq_kivi_step_host's state: the device slot for a step's inputs (the
+// token's K and V at 0 and off_v, the query at off_q).
 struct StepIO {
-  cudaStream_t cs = nullptr;
-  void *slot[2] = {nullptr, nullptr};
-  cudaEvent_t copied[2] = {nullptr, nullptr};
-  cudaEvent_t used[2] = {nullptr, nullptr};
+  void *slot = nullptr;
   std::vector<int32_t> ones;
   size_t off_v = 0, off_q = 0;
-  int next = 0;
 };
 
 static void free_step_io(StepIO *io) {
   if (!io) return;
-  if (io->cs) cudaStreamSynchronize(io->cs);
-  for (int i = 0; i < 2; ++i) {
-    if (io->used[i]) cudaEventSynchronize(io->used[i]);
-    if (io->slot[i]) cudaFree(io->slot[i]);
-    if (io->copied[i]) cudaEventDestroy(io->copied[i]);
-    if (io->used[i]) cudaEventDestroy(io->used[i]);
-  }
-  if (io->cs) cudaStreamDestroy(io->cs);
+  if (io->slot) cudaFree(io->slot);   // waits for the kernels using it
   delete io;
 }
 
@@ -146,6 +133,32 @@ int32_t split_unit(int g) { return g > 64 ? g : 64; }
 
 namespace vqk {
 void count_launch(int n) { g_launches.fetch_add((uint64_t)n); }
+
+// vq_kivi_step_host's inputs into the cache's slot: 16-byte chunks of the
+// token's K and V (nkv chunks each) and of the query (nq), read through the
+// pinned buffers' device mappings before the programmatic wait (the host
+// wrote them before the call) and stored after it, when every earlier
+// kernel of the stream (the previous step's readers of the slot among
+// them) has completed.
+__global__ void k_stage_inputs(const uint4 *__restrict__ hk, const uint4 *__restrict__ hv,
+                               const uint4 *__restrict__ hq, uint4 *__restrict__ dk,
+                               uint4 *__restrict__ dv, uint4 *__restrict__ dq, int nkv,
+                               int nq) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a, q = a;
+  if (i < nkv) {
+    a = hk[i];
+    b = hv[i];
+  }
+  if (i < nq) q = hq[i];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (i < nkv) {
+    dk[i] = a;
+    dv[i] = b;
+  }
+  if (i < nq) dq[i] = q;
+}
 void set_last_error(const char *msg) { g_err = msg; }
 }  // namespace vqk
 
@@ -381,15 +394,28 @@ int vq_kivi_quantize_ex(const vq_kivi_params *p, const vq_kivi_options *opt,
   }
   if (e != cudaSuccess) return abort_create(e, "quantize kernel launch");
   e = launch_tail(geo, pl, (const __half *)K, (const __half *)V, s_stride, tt,
-                  tt.prefix[p->B], st);
+                  tt.prefix[p->B], true, st);
   if (e != cudaSuccess) return abort_create(e, "residual kernel launch");
   c->flush_last = ft.prefix[p->B] > 0 && tt.prefix[p->B] == 0;
   *out = c;
   return VQ_OK;
 }
 
+// vq_kivi_append; input_ready: K_new / V_new were written before the call
+// (not by the stream's last kernel), so the ring append may load them
+// before its programmatic wait
+static int append_impl(vq_kivi_cache *c, const void *K_new, const void *V_new,
+                       int64_t n_stride, const int32_t *n_new, void *stream,
+                       bool input_ready);
+
 int vq_kivi_append(vq_kivi_cache *c, const void *K_new, const void *V_new,
                    int64_t n_stride, const int32_t *n_new, void *stream) {
+  return append_impl(c, K_new, V_new, n_stride, n_new, stream, true);
+}
+
+static int append_impl(vq_kivi_cache *c, const void *K_new, const void *V_new,
+                       int64_t n_stride, const int32_t *n_new, void *stream,
+                       bool input_ready) {
   int rc = check_cache(c);
   if (rc) return rc;
   if (!n_new) return fail(VQ_ERR_ARG, "n_new is NULL");
@@ -467,7 +493,7 @@ int vq_kivi_append(vq_kivi_cache *c, const void *K_new, const void *V_new,
   }
   if (e != cudaSuccess) return cuda_fail(e, "flush kernel launch");
   e = launch_tail(c->geo, c->pl, (const __half *)K_new, (const __half *)V_new,
-                  n_stride, tt, tt.prefix[p.B], st);
+                  n_stride, tt, tt.prefix[p.B], input_ready, st);
   if (e != cudaSuccess) return cuda_fail(e, "residual kernel launch");
   if (tt.prefix[p.B] > 0)
     c->flush_last = false;
@@ -629,10 +655,14 @@ int vq_kivi_step_host(vq_kivi_cache *c, const void *h_k_new, const void *h_v_new
   if (rc) return rc;
   if (!h_k_new || !h_v_new || !h_q || !h_out)
     return fail(VQ_ERR_ARG, "step_host: NULL argument");
-  if (!pinned_device_ptr(h_k_new) || !pinned_device_ptr(h_v_new) || !pinned_device_ptr(h_q))
+  const void *d_k = pinned_device_ptr(h_k_new), *d_v = pinned_device_ptr(h_v_new),
+             *d_q = pinned_device_ptr(h_q);
+  if (!d_k || !d_v || !d_q)
     return fail(VQ_ERR_ARG, "step_host: the inputs must be pinned host memory");
   float *d_out = static_cast<float *>(pinned_device_ptr(h_out));
   if (!d_out) return fail(VQ_ERR_ARG, "step_host: h_out must be pinned host memory");
+  if (!aligned(d_k, 16) || !aligned(d_v, 16) || !aligned(d_q, 16))
+    return fail(VQ_ERR_ARG, "step_host: the inputs must be 16-byte aligned");
   const vq_kivi_params &p = c->p;
   const size_t kv_bytes = (size_t)p.B * p.H_kv * p.D * sizeof(__half);
   const size_t q_bytes = (size_t)p.B * p.H_q * p.D * sizeof(__half);
@@ -643,39 +673,31 @@ int vq_kivi_step_host(vq_kivi_cache *c, const void *h_k_new, const void *h_v_new
     io->off_v = round_up(kv_bytes, 256);
     io->off_q = io->off_v + round_up(kv_bytes, 256);
     io->ones.assign(p.B, 1);
-    e = cudaStreamCreateWithFlags(&io->cs, cudaStreamNonBlocking);
-    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
-      e = cudaMalloc(&io->slot[i], io->off_q + q_bytes);
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&io->copied[i], cudaEventDisableTiming);
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&io->used[i], cudaEventDisableTiming);
-    }
+    e = cudaMalloc(&io->slot, io->off_q + q_bytes);
     if (e != cudaSuccess) {
+      io->slot = nullptr;
       free_step_io(io);
       return cuda_fail(e, "step_host: slot allocation");
     }
     c->io = io;
   }
   StepIO *io = c->io;
-  const int s = io->next;
   cudaStream_t st = (cudaStream_t)stream;
-  uint8_t *slot = static_cast<uint8_t *>(io->slot[s]);
-  // the slot's previous step has read it (waiting on a never-recorded
-  // event returns at once)
-  e = cudaStreamWaitEvent(io->cs, io->used[s], 0);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(slot, h_k_new, kv_bytes, cudaMemcpyHostToDevice, io->cs);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(slot + io->off_v, h_v_new, kv_bytes, cudaMemcpyHostToDevice, io->cs);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(slot + io->off_q, h_q, q_bytes, cudaMemcpyHostToDevice, io->cs);
-  if (e == cudaSuccess) e = cudaEventRecord(io->copied[s], io->cs);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, io->copied[s], 0);
-  if (e != cudaSuccess) return cuda_fail(e, "step_host: input copy");
-  io->next ^= 1;
-  rc = vq_kivi_append(c, slot, slot + io->off_v, 1, io->ones.data(), stream);
+  uint8_t *slot = static_cast<uint8_t *>(io->slot);
+  // the inputs into the slot: a programmatic dependent of the stream's last
+  // kernel (the previous step's merge), then the append (its ring copy waits
+  // for the slot before reading it) and the decode
+  const int nkv = (int)(kv_bytes / 16), nq = (int)(q_bytes / 16);
+  const int n = nkv > nq ? nkv : nq;
+  e = launch_pdl(k_stage_inputs, dim3((n + 255) / 256), dim3(256), 0, st,
+                 static_cast<const uint4 *>(d_k), static_cast<const uint4 *>(d_v),
+                 static_cast<const uint4 *>(d_q), reinterpret_cast<uint4 *>(slot),
+                 reinterpret_cast<uint4 *>(slot + io->off_v),
+                 reinterpret_cast<uint4 *>(slot + io->off_q), nkv, nq);
+  count_launch();
+  if (e != cudaSuccess) return cuda_fail(e, "step_host: input staging launch");
+  rc = append_impl(c, slot, slot + io->off_v, 1, io->ones.data(), stream, false);
   if (rc == VQ_OK) rc = vq_kivi_decode_attend(c, slot + io->off_q, d_out, softmax_scale, stream);
-  // the slot is free again once this step's kernels have run
-  e = cudaEventRecord(io->used[s], st);
-  if (rc == VQ_OK && e != cudaSuccess) return cuda_fail(e, "step_host: event");
   return rc;
 }
 

@@ -672,16 +672,19 @@ k_flush_t(Geometry geo, Planes pl, const __half *__restrict__ Kin,
   }
 }
 
-// Residual ring writes: 16-byte chunks of fp16 rows.  The rows come from
-// the input, complete before this grid starts (the kernel before it in the
-// stream releases it only after its own wait); the ring slots they go to
-// may still be read by that kernel (a flush reads the old residual rows, a
-// merge the window).  So each thread loads its chunks, then waits, then
-// stores: the loads overlap the previous kernel's end.
+// Residual ring writes: 16-byte chunks of fp16 rows.  The ring slots they
+// go to may still be read by the kernel before this one in the stream (a
+// flush reads the old residual rows, a merge the window), so the stores
+// follow the programmatic wait.  When the input was complete before the
+// append's first kernel (input_ready: that kernel releases this grid only
+// after its own wait), each thread loads its chunks before the wait, and
+// the loads overlap the previous kernel's end; otherwise (the kernel
+// before wrote the input) after it.
 __global__ void __launch_bounds__(kThreads)
 k_tail(Geometry geo, Planes pl, const __half *__restrict__ Kin,
        const __half *__restrict__ Vin, int64_t in_stride, TailTable tab,
-       int total) {
+       int total, int input_ready) {
+  if (!input_ready) asm volatile("griddepcontrol.wait;" ::: "memory");
   const int D = geo.D;
   const int cpr = D / 8;                       // 16-byte chunks per row
   const int rows_per_block = kThreads / cpr;
@@ -777,12 +780,13 @@ cudaError_t launch_flush(const Geometry &geo, const Planes &pl,
 cudaError_t launch_tail(const Geometry &geo, const Planes &pl,
                         const __half *Kin, const __half *Vin,
                         int64_t in_stride, const TailTable &tab,
-                        int total_tokens, cudaStream_t st) {
+                        int total_tokens, bool input_ready, cudaStream_t st) {
   if (total_tokens <= 0) return cudaSuccess;
   const int rows_per_block = kThreads / (geo.D / 8);
   dim3 grid((total_tokens + rows_per_block - 1) / rows_per_block, geo.H_kv);
   const cudaError_t e = launch_pdl(k_tail, grid, dim3(kThreads), 0, st, geo, pl,
-                                  Kin, Vin, in_stride, tab, total_tokens);
+                                  Kin, Vin, in_stride, tab, total_tokens,
+                                  input_ready ? 1 : 0);
   count_launch();
   return e;
 }

@@ -237,10 +237,12 @@ cudaError_t launch_pick_sinks(const Geometry &geo, const Planes &pl,
                               const __half *K, const __half *V,
                               int64_t s_stride, const SinkTable &tab,
                               cudaStream_t st);
+// input_ready: Kin / Vin were complete before the append's first kernel
+// (not written by the kernel before the ring append)
 cudaError_t launch_tail(const Geometry &geo, const Planes &pl,
                         const __half *Kin, const __half *Vin,
                         int64_t in_stride, const TailTable &tab,
-                        int total_tokens, cudaStream_t st);
+                        int total_tokens, bool input_ready, cudaStream_t st);
 // code plane 0 (keys) or 3 (values) of a kLayoutFrag cache, converted to
 // the packed order, into dst
 cudaError_t launch_export_frag(const Geometry &geo, const uint8_t *src,

@@ -175,23 +175,23 @@ int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
 /* One serving step from host memory: append one token per sequence, then
  * the fused decode step (the two calls above, changelog v0.8.0 and
  * v0.42.0), with the inputs in pinned host memory and the output written
- * into pinned host memory.  The token's K and V and the query are copied
- * into one of two device slots held by the cache, on a copy stream of the
- * cache's own, so that a step's input copy overlaps the previous step's
- * kernels; `stream` waits for the copy, then runs the append and the
- * decode, whose output rows are stored straight into h_out through its
- * device mapping (no separate device-to-host copy).  Asynchronous like
- * cudaMemcpyAsync: h_out holds the result once `stream` has reached the
- * end of the step, and the inputs may be overwritten once the step's copy
- * has run (the next call on the same cache orders itself after it).
- *   h_k_new, h_v_new  pinned host, fp16, [B][H_kv][D]
- *   h_q               pinned host, fp16, [B][H_q][D]
+ * into pinned host memory.  A first kernel on `stream` reads the token's K
+ * and V and the query through the pinned buffers' device mappings (no
+ * copy engine, no second stream) while the previous step's last kernel
+ * finishes, and stores them into a device slot held by the cache; the
+ * append and the decode follow, and the decode stores its output rows
+ * straight into h_out through its device mapping (no separate
+ * device-to-host copy).  Asynchronous like cudaMemcpyAsync: h_out holds the
+ * result once `stream` has reached the end of the step, and the inputs may
+ * be overwritten once the step's first kernel has run.
+ *   h_k_new, h_v_new  pinned host, fp16, [B][H_kv][D], 16-byte aligned
+ *   h_q               pinned host, fp16, [B][H_q][D], 16-byte aligned
  *   h_out             pinned host, fp32, [B][H_q][D], 16-byte aligned
  *   softmax_scale     <= 0 selects 1/sqrt(D)
- * VQ_ERR_ARG when a pointer is NULL or not pinned host memory;
- * VQ_ERR_CAPACITY as vq_kivi_append (cache unchanged).  The first call
- * allocates the slots (2 x B x (2 H_kv + H_q) x D x 2 bytes), a stream and
- * four events, released by vq_kivi_free. */
+ * VQ_ERR_ARG when a pointer is NULL, not pinned host memory or not
+ * aligned; VQ_ERR_CAPACITY as vq_kivi_append (cache unchanged).  The first
+ * call allocates the slot (B x (2 H_kv + H_q) x D x 2 bytes), released by
+ * vq_kivi_free. */
 int vq_kivi_step_host(vq_kivi_cache *c, const void *h_k_new,
                       const void *h_v_new, const void *h_q, float *h_out,
                       float softmax_scale, void *stream);
