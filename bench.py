@@ -582,11 +582,12 @@ def run_ours(args, w, rank, world, local):
                 "breakdown": {
                     "host_issue_us": round(host_us, 2),
                     "step_device_us": round(ms * 1e3, 2),
-                    "reading": "a step's first kernel reads its inputs "
-                               "from the pinned buffers while the previous "
-                               "step's last kernel finishes; the step time "
-                               "is the larger of the device step and the "
-                               "host's time to issue it"}},
+                    "reading": "the kernels read a step's inputs from "
+                               "the pinned buffers through their device "
+                               "mappings (a step that quantizes a group "
+                               "stages them first); the step time is the "
+                               "larger of the device step and the host's "
+                               "time to issue it"}},
         "gpu_launches": int(round(launches)),
         "gpu_launches_per": "pass of K steps",
         "clocks": clocks,

@@ -684,9 +684,23 @@ int vq_kivi_step_host(vq_kivi_cache *c, const void *h_k_new, const void *h_v_new
   StepIO *io = c->io;
   cudaStream_t st = (cudaStream_t)stream;
   uint8_t *slot = static_cast<uint8_t *>(io->slot);
-  // the inputs into the slot: a programmatic dependent of the stream's last
-  // kernel (the previous step's merge), then the append (its ring copy waits
-  // for the slot before reading it) and the decode
+  // A step that flushes no group (and no AgeTieredKV tier) only copies the
+  // token's rows into the residual ring: the ring append reads them, and
+  // the decode kernels q, through the pinned buffers' device mappings (the
+  // host wrote them before this call, so the loads may precede the kernels'
+  // programmatic waits), and no staging kernel runs.
+  bool flushes = c->geo.age_b1 > 0;
+  for (int b = 0; b < p.B && !flushes; ++b)
+    flushes = n_quantized(c->S[b] + 1, p.residual, p.group) > c->Tq[b];
+  if (!flushes) {
+    rc = append_impl(c, d_k, d_v, 1, io->ones.data(), stream, true);
+    if (rc == VQ_OK) rc = vq_kivi_decode_attend(c, d_q, d_out, softmax_scale, stream);
+    return rc;
+  }
+  // Otherwise the inputs go into the slot first: a programmatic dependent
+  // of the stream's last kernel (the previous step's merge), then the
+  // append (the flush and the ring copy read the slot after their waits)
+  // and the decode.
   const int nkv = (int)(kv_bytes / 16), nq = (int)(q_bytes / 16);
   const int n = nkv > nq ? nkv : nq;
   e = launch_pdl(k_stage_inputs, dim3((n + 255) / 256), dim3(256), 0, st,

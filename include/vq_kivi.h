@@ -175,15 +175,16 @@ int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
 /* One serving step from host memory: append one token per sequence, then
  * the fused decode step (the two calls above, changelog v0.8.0 and
  * v0.42.0), with the inputs in pinned host memory and the output written
- * into pinned host memory.  A first kernel on `stream` reads the token's K
- * and V and the query through the pinned buffers' device mappings (no
- * copy engine, no second stream) while the previous step's last kernel
- * finishes, and stores them into a device slot held by the cache; the
- * append and the decode follow, and the decode stores its output rows
- * straight into h_out through its device mapping (no separate
- * device-to-host copy).  Asynchronous like cudaMemcpyAsync: h_out holds the
- * result once `stream` has reached the end of the step, and the inputs may
- * be overwritten once the step's first kernel has run.
+ * into pinned host memory.  The kernels read the token's K and V and the
+ * query through the pinned buffers' device mappings (no copy engine, no
+ * second stream): a step that only adds the token to the residual window
+ * reads them where they are; a step that also quantizes a group first
+ * stores them into a device slot held by the cache, while the previous
+ * step's last kernel finishes.  The decode stores its output rows straight
+ * into h_out through its device mapping (no separate device-to-host copy).
+ * Asynchronous like cudaMemcpyAsync: h_out holds the result once `stream`
+ * has reached the end of the step, and the inputs may be overwritten only
+ * then.
  *   h_k_new, h_v_new  pinned host, fp16, [B][H_kv][D], 16-byte aligned
  *   h_q               pinned host, fp16, [B][H_q][D], 16-byte aligned
  *   h_out             pinned host, fp32, [B][H_q][D], 16-byte aligned
