@@ -149,11 +149,11 @@ cudaError_t launch_decode_mma(const Geometry &geo, const Planes &pl,
     case 128 * 8 + 4: mf = mma::merge_fn<128, 4>(); break;
     default: return cudaErrorInvalidValue;
   }
-  // merge warps per CTA (a multiple of the query heads per kv head): per
-  // query head enough for the largest partial count of a head to be read in
-  // one round, and more, up to what reads the longest residual window in
-  // one round, only while every CTA of the grid still fits on the device at
-  // once (a second wave costs more than a second round of the window)
+  // merge warps per CTA (one query head, one channel slice): enough for the
+  // largest partial count of a head to be read in one round, and more, up
+  // to what reads the longest residual window in one round, only while
+  // every CTA of the grid still fits on the device at once (a second wave
+  // costs more than a second round of the window)
   const int GQ = plan.GQ;
   int64_t per = 1, nr = 1;
   bool any = false;
@@ -172,20 +172,19 @@ cudaError_t launch_decode_mma(const Geometry &geo, const Planes &pl,
     }
   }
   if (!any) return cudaSuccess;
-  const int64_t per_max = mma::kMergeWarps / GQ;
+  const int64_t per_max = mma::kMergeWarps;
   if (per > per_max) per = per_max;
-  int64_t per_res = (nr + GQ - 1) / GQ;
-  if (per_res > per_max) per_res = per_max;
-  const int64_t ctas = (int64_t)geo.B * geo.H_kv * (geo.D / 32);
-  for (int64_t pr = per_res; pr > per; --pr) {
-    if ((int64_t)merge_ctas_per_sm(mf, (int)(pr * GQ)) * plan.sm_count >= ctas) {
+  if (nr > per_max) nr = per_max;
+  const int nsl = geo.D == 64 ? (plan.GQp == 4 ? 1 : 2) : 4 / plan.GQp;
+  const int64_t ctas = (int64_t)geo.B * geo.H_kv * GQ * nsl;
+  for (int64_t pr = nr; pr > per; --pr) {
+    if ((int64_t)merge_ctas_per_sm(mf, (int)pr) * plan.sm_count >= ctas) {
       per = pr;
       break;
     }
   }
-  const int64_t nw = per * GQ;
-  cfg.gridDim = dim3(geo.B * geo.H_kv, geo.D / 32);
-  cfg.blockDim = dim3((unsigned)nw * 32);
+  cfg.gridDim = dim3(geo.B * geo.H_kv, GQ, nsl);
+  cfg.blockDim = dim3((unsigned)per * 32);
   cfg.dynamicSmemBytes = 0;
   e = cudaLaunchKernelEx(&cfg, mf, geo, pl, args, tab);
   count_launch();

@@ -1057,64 +1057,74 @@ k_decode_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
 
 // ---- merge of the per-warp partials and the fp16 residual window ---------
 //
-// One CTA per (sequence, kv head, 32-channel slice) with nw <= kMergeWarps
-// warps (a multiple of the query heads per kv head, sized by the launcher),
-// serving the kv head's GQ query heads.  Warp j first takes the residual
-// window's tokens j, j + nw, ... (kMergeRT at a time): lanes hold 32-channel
-// strides of the key row and of every query head's q' (one warp-wide sum
-// per head gives the scores) and the slice's channel of the value row.
-// Then, once the decode kernel's writes are visible, the partials: those of
-// kv head hd sit in slots w + hd for the warps w whose chunk range touches
-// the head, and warp j merges query head j mod GQ's partials j/GQ,
-// j/GQ + nw/GQ, ... (kMergeU at a time, all in flight).  Every warp keeps a
-// running (max, sum, o) per query head; warp hh then combines all warps'
-// states of query head hh with a log-sum-exp.  The unroll depths keep the
-// CTAs small (4 warps for the usual window and partial counts), so that
-// every CTA of a large batch runs in one wave and, where the decode kernel
-// leaves room on an SM, the CTAs reside beside it and read the residual
-// window while it runs.
+// One CTA per (sequence, kv head, query head, channel slice): NSL =
+// min(4 / GQP, D / 32) slices of D / NSL channels, so that one query head
+// per kv head keeps four CTAs of 32 channels and four query heads one CTA
+// each over all channels (every window score is then computed once per
+// slice, never once per head and slice).  nw <= kMergeWarps warps, sized by
+// the launcher.  Warp j first takes the residual window's tokens j,
+// j + nw, ... (kMergeRT at a time): lanes hold 32-channel strides of the
+// key row and of the head's q' (one warp-wide sum gives a score) and the
+// slice's channels of the value row.  Then, once the decode kernel's
+// writes are visible, the partials: those of kv head hd sit in slots w + hd
+// for the warps w whose chunk range touches the head, and warp j merges
+// partials j, j + nw, ... (kMergeU at a time, all in flight).  Every warp
+// keeps a running (max, sum, o); warp 0 then combines the warps' states
+// with a log-sum-exp.  The unroll depths keep the CTAs small (4 warps for
+// the usual window and partial counts), so that every CTA of a large batch
+// runs in one wave and, where the decode kernel leaves room on an SM, the
+// CTAs reside beside it and read the residual window while it runs.
 constexpr int kMergeWarps = 16;
 constexpr int kMergeU = 16;
 constexpr int kMergeRT = 8;
 
+template <int D, int GQP> __host__ __device__ constexpr int merge_slices() {
+  return (4 / GQP) < (D / 32) ? (4 / GQP) : (D / 32);
+}
+
 template <int D, int GQP>
 __global__ void __launch_bounds__(kMergeWarps * 32)
 k_merge_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
-  constexpr int CPL = D / 32;
-  __shared__ float sm_m[kMergeWarps][GQP], sm_l[kMergeWarps][GQP];
-  __shared__ float sm_o[kMergeWarps][GQP][32];
+  constexpr int CPL = D / 32;                       // key channels per lane
+  constexpr int NSL = merge_slices<D, GQP>();
+  constexpr int SW = D / NSL, OC = SW / 32;         // slice width, o per lane
+  __shared__ float sm_m[kMergeWarps], sm_l[kMergeWarps];
+  __shared__ float sm_o[kMergeWarps][SW];
   // let the stream's next kernel launch now: whatever it writes that this
   // kernel reads (the residual ring for an append, the partials for a
   // decode) it writes only after its own griddepcontrol.wait, which waits
   // for this grid to complete
   asm volatile("griddepcontrol.launch_dependents;");
   const int b = blockIdx.x / geo.H_kv, h = blockIdx.x - b * geo.H_kv;
+  const int hq = blockIdx.y;                        // query head of the kv head
   const int nq = tab.nq[b], nres = tab.nres[b];
   if (nq == 0 && nres == 0) return;   // no tokens: the launcher zeroed it
   const int GQ = args.GQ;
   const int hd = b * geo.H_kv + h;
   const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
   const int nw = blockDim.x >> 5;
-  const int c = blockIdx.y * 32 + lane;
+  const int c0 = blockIdx.z * SW + lane;            // channel of o[0]; o[u] at c0 + 32 u
 
-  float m_run[GQP], l_run[GQP], o_run[GQP];
+  float m_run = -INFINITY, l_run = 0.f, o_run[OC];
 #pragma unroll
-  for (int hh = 0; hh < GQP; ++hh) { m_run[hh] = -INFINITY; l_run[hh] = 0.f; o_run[hh] = 0.f; }
-  // fold n entries (m_u, l_u, o_u) into head hh's running state; entries
-  // with m = -inf (partials of empty ranges, tokens past the end) weigh
-  // nothing
-  auto fold = [&](int hh, const float *mu, const float *lu, const float *ou, int n) {
-    float mr = m_run[hh];
-    for (int u = 0; u < n; ++u) mr = fmaxf(mr, mu[u]);
+  for (int u = 0; u < OC; ++u) o_run[u] = 0.f;
+  // fold n entries (m_e, l_e, o_e) into the running state; entries with
+  // m = -inf (empty partial slots, tokens past the end) weigh nothing
+  auto fold = [&](const float *me, const float *le, const float (*oe)[OC], int n) {
+    float mr = m_run;
+    for (int e = 0; e < n; ++e) mr = fmaxf(mr, me[e]);
     if (mr == -INFINITY) return;
-    const float a = m_run[hh] == -INFINITY ? 0.f : exp2_neg(m_run[hh] - mr);
-    float l = l_run[hh] * a, o = o_run[hh] * a;
-    for (int u = 0; u < n; ++u) {
-      const float f = mu[u] == -INFINITY ? 0.f : exp2_neg(mu[u] - mr);
-      l = fmaf(f, lu[u], l);
-      o = fmaf(f, ou[u], o);
+    const float a = m_run == -INFINITY ? 0.f : exp2_neg(m_run - mr);
+    l_run *= a;
+#pragma unroll
+    for (int u = 0; u < OC; ++u) o_run[u] *= a;
+    for (int e = 0; e < n; ++e) {
+      const float f = me[e] == -INFINITY ? 0.f : exp2_neg(me[e] - mr);
+      l_run = fmaf(f, le[e], l_run);
+#pragma unroll
+      for (int u = 0; u < OC; ++u) o_run[u] = fmaf(f, oe[e][u], o_run[u]);
     }
-    m_run[hh] = mr; l_run[hh] = l; o_run[hh] = o;
+    m_run = mr;
   };
 
   // (1) the fp16 residual window: tokens T_q ... T_q + nres - 1 in ring
@@ -1124,18 +1134,17 @@ k_merge_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   // otherwise the append itself precedes this kernel and is waited for.
   if (args.N <= 0) asm volatile("griddepcontrol.wait;" ::: "memory");
   if (nres > 0) {
-    float qv[GQP][CPL];
-#pragma unroll
-    for (int hh = 0; hh < GQP; ++hh) {
-      const __half *qrow = args.q + ((size_t)b * geo.H_q + h * GQ + (hh < GQ ? hh : 0)) * D;
+    float qv[CPL];
+    {
+      const __half *qrow = args.q + ((size_t)b * geo.H_q + h * GQ + hq) * D;
 #pragma unroll
       for (int u = 0; u < CPL; ++u)
-        qv[hh][u] = __half2float(__ldcg(qrow + lane + 32 * u)) * args.scale_log2;
+        qv[u] = __half2float(__ldcg(qrow + lane + 32 * u)) * args.scale_log2;
     }
     const size_t ring0 = (size_t)hd * geo.Rcap;
     const int Tq = tab.Tq[b];
     for (int t0 = wp; t0 < nres; t0 += nw * kMergeRT) {
-      float kv[kMergeRT][CPL], vv[kMergeRT];
+      float kv[kMergeRT][CPL], vv[kMergeRT][OC], me[kMergeRT], le[kMergeRT];
       bool ok[kMergeRT];
 #pragma unroll
       for (int r = 0; r < kMergeRT; ++r) {
@@ -1144,23 +1153,19 @@ k_merge_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
         const size_t row = (ring0 + (Tq + (ok[r] ? t : t0)) % geo.Rcap) * D;
 #pragma unroll
         for (int u = 0; u < CPL; ++u) kv[r][u] = __half2float(__ldcg(pl.Kr + row + lane + 32 * u));
-        vv[r] = __half2float(__ldcg(pl.Vr + row + c));
+#pragma unroll
+        for (int u = 0; u < OC; ++u) vv[r][u] = __half2float(__ldcg(pl.Vr + row + c0 + 32 * u));
       }
 #pragma unroll
-      for (int hh = 0; hh < GQP; ++hh) {
-        if (hh >= GQ) break;
-        float mu[kMergeRT], lu[kMergeRT];
+      for (int r = 0; r < kMergeRT; ++r) {
+        float sc = 0.f;
 #pragma unroll
-        for (int r = 0; r < kMergeRT; ++r) {
-          float sc = 0.f;
-#pragma unroll
-          for (int u = 0; u < CPL; ++u) sc = fmaf(qv[hh][u], kv[r][u], sc);
-          sc = warp_sum(sc);
-          mu[r] = ok[r] ? sc : -INFINITY;
-          lu[r] = 1.f;
-        }
-        fold(hh, mu, lu, vv, kMergeRT);
+        for (int u = 0; u < CPL; ++u) sc = fmaf(qv[u], kv[r][u], sc);
+        sc = warp_sum(sc);
+        me[r] = ok[r] ? sc : -INFINITY;
+        le[r] = 1.f;
       }
+      fold(me, le, vv, kMergeRT);
     }
   }
 
@@ -1168,76 +1173,73 @@ k_merge_mma(Geometry geo, Planes pl, MmaArgs args, MmaTable tab) {
   // (written at prefill; the decode kernel masked their quantized slots)
   if (geo.n_sink > 0) {
     const int Tq = tab.Tq[b];
+    const __half *qrow = args.q + ((size_t)b * geo.H_q + h * GQ + hq) * D;
     for (int k = wp; k < geo.n_sink; k += nw) {
       const int t = __ldg(pl.sink_pos + (size_t)hd * geo.n_sink + k);
       if (t < 0 || t >= Tq) continue;
       const size_t row = ((size_t)hd * geo.n_sink + k) * D;
-      float kv[CPL];
+      float sc = 0.f;
 #pragma unroll
-      for (int u = 0; u < CPL; ++u) kv[u] = __half2float(__ldg(pl.sink_k + row + lane + 32 * u));
-      const float vv = __half2float(__ldg(pl.sink_v + row + c));
+      for (int u = 0; u < CPL; ++u)
+        sc = fmaf(__half2float(__ldcg(qrow + lane + 32 * u)) * args.scale_log2,
+                  __half2float(__ldg(pl.sink_k + row + lane + 32 * u)), sc);
+      sc = warp_sum(sc);
+      float vv[1][OC];
 #pragma unroll
-      for (int hh = 0; hh < GQP; ++hh) {
-        if (hh >= GQ) break;
-        const __half *qrow = args.q + ((size_t)b * geo.H_q + h * GQ + hh) * D;
-        float sc = 0.f;
-#pragma unroll
-        for (int u = 0; u < CPL; ++u)
-          sc = fmaf(__half2float(__ldcg(qrow + lane + 32 * u)) * args.scale_log2, kv[u], sc);
-        sc = warp_sum(sc);
-        const float one = 1.f;
-        fold(hh, &sc, &one, &vv, 1);
-      }
+      for (int u = 0; u < OC; ++u) vv[0][u] = __half2float(__ldg(pl.sink_v + row + c0 + 32 * u));
+      const float one = 1.f;
+      fold(&sc, &one, vv, 1);
     }
   }
 
   // (2) the decode kernel's partials, visible once griddepcontrol.wait
-  // returns: warp wp serves query head wp mod GQ
+  // returns
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int hp = wp % GQ, per = nw / GQ;
-  if (nq > 0 && wp < per * GQ) {
+  if (nq > 0) {
     const int64_t N = args.N, W = args.W;
     const int64_t cs = tab.bprefix[b] + (int64_t)h * tab.nc[b];
     const int64_t ce = cs + tab.nc[b];
     const int w0 = (int)(((cs + 1) * W - 1) / N);
     const int n = (int)((ce * W - 1) / N) - w0 + 1;
-    for (int k0 = wp / GQ; k0 < n; k0 += per * kMergeU) {
-      float mu[kMergeU], lu[kMergeU], ou[kMergeU];
+    for (int k0 = wp; k0 < n; k0 += nw * kMergeU) {
+      float me[kMergeU], le[kMergeU], oe[kMergeU][OC];
 #pragma unroll
       for (int u = 0; u < kMergeU; ++u) {
-        const int k = k0 + u * per;
+        const int k = k0 + u * nw;
         const bool ok = k < n;
         const float *e = args.part +
-                         ((size_t)(w0 + (ok ? k : k0) + hd) * GQP + hp) * part_stride<D>();
+                         ((size_t)(w0 + (ok ? k : k0) + hd) * GQP + hq) * part_stride<D>();
         const float2 ml = ok ? __ldcg(reinterpret_cast<const float2 *>(e + D))
                              : make_float2(-INFINITY, 0.f);
-        mu[u] = ml.x;
-        lu[u] = ml.y;
-        ou[u] = ok ? __ldcg(e + c) : 0.f;
-      }
+        me[u] = ml.x;
+        le[u] = ml.y;
 #pragma unroll
-      for (int hh = 0; hh < GQP; ++hh)
-        if (hh == hp) fold(hh, mu, lu, ou, kMergeU);
+        for (int v = 0; v < OC; ++v) oe[u][v] = ok ? __ldcg(e + c0 + 32 * v) : 0.f;
+      }
+      fold(me, le, oe, kMergeU);
     }
   }
 
+  // (3) the warps' states combined
+  if (lane == 0) { sm_m[wp] = m_run; sm_l[wp] = l_run; }
 #pragma unroll
-  for (int hh = 0; hh < GQP; ++hh) {
-    if (lane == 0) { sm_m[wp][hh] = m_run[hh]; sm_l[wp][hh] = l_run[hh]; }
-    sm_o[wp][hh][lane] = o_run[hh];
-  }
+  for (int u = 0; u < OC; ++u) sm_o[wp][lane + 32 * u] = o_run[u];
   __syncthreads();
-  if (wp < GQ) {
-    const int hh = wp;
+  if (wp == 0) {
     float M = -INFINITY;
-    for (int j = 0; j < nw; ++j) M = fmaxf(M, sm_m[j][hh]);
-    float L = 0.f, o = 0.f;
+    for (int j = 0; j < nw; ++j) M = fmaxf(M, sm_m[j]);
+    float L = 0.f, o[OC];
+#pragma unroll
+    for (int u = 0; u < OC; ++u) o[u] = 0.f;
     for (int j = 0; j < nw; ++j) {
-      const float f = sm_m[j][hh] == -INFINITY ? 0.f : exp2_neg(sm_m[j][hh] - M);
-      L = fmaf(f, sm_l[j][hh], L);
-      o = fmaf(f, sm_o[j][hh][lane], o);
+      const float f = sm_m[j] == -INFINITY ? 0.f : exp2_neg(sm_m[j] - M);
+      L = fmaf(f, sm_l[j], L);
+#pragma unroll
+      for (int u = 0; u < OC; ++u) o[u] = fmaf(f, sm_o[j][lane + 32 * u], o[u]);
     }
-    args.out[((size_t)b * geo.H_q + h * GQ + hh) * D + c] = o / L;
+    float *orow = args.out + ((size_t)b * geo.H_q + h * GQ + hq) * D;
+#pragma unroll
+    for (int u = 0; u < OC; ++u) orow[c0 + 32 * u] = o[u] / L;
   }
 }
 
