@@ -351,27 +351,53 @@ k_decode_kitty(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
     // the sequence's last item also takes the fp16 residual window, folded
     // into the same running state: scores one token per lane, values lanes
     // over channels
-    for (int i0 = warp * 32; i0 < tab.nres[b]; i0 += kWarps * 32) {
+    // blocks of kWinT tokens spread over the warps (lanes 0 ... kWinT - 1
+    // take a token each), so that every warp's loads are few rounds
+    constexpr int kWinT = 8;
+    for (int i0 = warp * kWinT; i0 < tab.nres[b]; i0 += kWarps * kWinT) {
       const int i = i0 + lane;
-      const bool ok = i < tab.nres[b];
-      const __half *kr = pl.Kr + (bh * geo.Rcap + (Tq + (ok ? i : i0)) % geo.Rcap) * D;
+      const bool ok = lane < kWinT && i < tab.nres[b];
+      // ring slots: the block's first token's, then one wrap at most (the
+      // window holds fewer than Rcap tokens)
+      const int s0 = (Tq + i0) % geo.Rcap;
+      int sl = s0 + lane;
+      if (sl >= geo.Rcap) sl -= geo.Rcap;
+      // this lane's key row in 16-byte loads, half of them in flight at a
+      // time (two rounds; the loop keeps q' in shared memory)
+      const uint4 *kr = reinterpret_cast<const uint4 *>(
+          pl.Kr + (bh * geo.Rcap + (ok ? sl : s0)) * D);
+      constexpr int KB = D / 16;
       float acc[GQ];
 #pragma unroll
       for (int hh = 0; hh < GQ; ++hh) acc[hh] = 0.f;
-#pragma unroll 4
-      for (int c = 0; c < D; c += 2) {
-        const float2 kv = __half22float2(*reinterpret_cast<const __half2 *>(kr + c));
+#pragma unroll 1
+      for (int j0 = 0; j0 < D / 8; j0 += KB) {
+        uint4 kx[KB];
 #pragma unroll
-        for (int hh = 0; hh < GQ; ++hh)
-          acc[hh] = fmaf(sq[hh * D + c], kv.x, fmaf(sq[hh * D + c + 1], kv.y, acc[hh]));
+        for (int j = 0; j < KB; ++j) kx[j] = kr[j0 + j];
+#pragma unroll
+        for (int j = 0; j < KB; ++j) {
+          const __half2 *k2 = reinterpret_cast<const __half2 *>(&kx[j]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 kv = __half22float2(k2[e]);
+            const int c = 8 * (j0 + j) + 2 * e;
+#pragma unroll
+            for (int hh = 0; hh < GQ; ++hh)
+              acc[hh] = fmaf(sq[hh * D + c], kv.x, fmaf(sq[hh * D + c + 1], kv.y, acc[hh]));
+          }
+        }
       }
       float sc[GQ], p[GQ];
 #pragma unroll
       for (int hh = 0; hh < GQ; ++hh) sc[hh] = ok ? acc[hh] : -INFINITY;
       fold(sc, p);
-      const int nb = min(32, tab.nres[b] - i0);
+      const int nb = min(kWinT, tab.nres[b] - i0);
+#pragma unroll 4
       for (int jj = 0; jj < nb; ++jj) {
-        const __half *vr = pl.Vr + (bh * geo.Rcap + (Tq + i0 + jj) % geo.Rcap) * D + lane * CPL;
+        int sj = s0 + jj;
+        if (sj >= geo.Rcap) sj -= geo.Rcap;
+        const __half *vr = pl.Vr + (bh * geo.Rcap + sj) * D + lane * CPL;
         float v[CPL];
 #pragma unroll
         for (int u = 0; u < CPL; ++u) v[u] = __half2float(vr[u]);
