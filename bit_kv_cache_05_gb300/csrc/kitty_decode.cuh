@@ -347,14 +347,18 @@ k_decode_kitty(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
         if (pending & (1u << j)) mbar_wait(&bars[j], (phase >> j) & 1u);
     }
   }
-  if (k == tab.nq[b] - 1) {
-    // the sequence's last item also takes the fp16 residual window, folded
-    // into the same running state: scores one token per lane, values lanes
-    // over channels
-    // blocks of kWinT tokens spread over the warps (lanes 0 ... kWinT - 1
-    // take a token each), so that every warp's loads are few rounds
+  {
+    // the fp16 residual window, folded into the running states of the
+    // sequence's last items: block j of kWinT tokens goes to item
+    // nq - 1 - (j mod nq), warp j mod kWarps of it (lanes 0 ... kWinT - 1
+    // score a token each, lanes over channels sum the values), so that no
+    // CTA carries much more than its share and every warp's loads are few
+    // rounds
     constexpr int kWinT = 8;
-    for (int i0 = warp * kWinT; i0 < tab.nres[b]; i0 += kWarps * kWinT) {
+    const int nblk = (tab.nres[b] + kWinT - 1) / kWinT;
+    for (int j = tab.nq[b] - 1 - k; j < nblk; j += tab.nq[b]) {
+      if (j % kWarps != warp) continue;
+      const int i0 = j * kWinT;
       const int i = i0 + lane;
       const bool ok = lane < kWinT && i < tab.nres[b];
       // ring slots: the block's first token's, then one wrap at most (the
