@@ -227,6 +227,75 @@ k_decode_kitty(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
       pending |= 1u << s;
       advance(pc);
     }
+    {
+      // (run before the first stage lands: its loads overlap the pipeline's
+      // first copies)
+      // the fp16 residual window, folded into the running states of the
+      // sequence's last items: block j of kWinT tokens goes to item
+      // nq - 1 - (j mod nq), warp j mod kWarps of it (lanes 0 ... kWinT - 1
+      // score a token each, lanes over channels sum the values), so that no
+      // CTA carries much more than its share and every warp's loads are few
+      // rounds
+      constexpr int kWinT = 8;
+      const int nblk = (tab.nres[b] + kWinT - 1) / kWinT;
+      for (int j = tab.nq[b] - 1 - k; j < nblk; j += tab.nq[b]) {
+        if (j % kWarps != warp) continue;
+        const int i0 = j * kWinT;
+        const int i = i0 + lane;
+        const bool ok = lane < kWinT && i < tab.nres[b];
+        // ring slots: the block's first token's, then one wrap at most (the
+        // window holds fewer than Rcap tokens)
+        const int s0 = (Tq + i0) % geo.Rcap;
+        int sl = s0 + lane;
+        if (sl >= geo.Rcap) sl -= geo.Rcap;
+        // this lane's key row in 16-byte loads, half of them in flight at a
+        // time (two rounds; the loop keeps q' in shared memory)
+        const uint4 *kr = reinterpret_cast<const uint4 *>(
+            pl.Kr + (bh * geo.Rcap + (ok ? sl : s0)) * D);
+        constexpr int KB = D / 16;
+        float acc[GQ];
+  #pragma unroll
+        for (int hh = 0; hh < GQ; ++hh) acc[hh] = 0.f;
+  #pragma unroll 1
+        for (int j0 = 0; j0 < D / 8; j0 += KB) {
+          uint4 kx[KB];
+  #pragma unroll
+          for (int j = 0; j < KB; ++j) kx[j] = kr[j0 + j];
+  #pragma unroll
+          for (int j = 0; j < KB; ++j) {
+            const __half2 *k2 = reinterpret_cast<const __half2 *>(&kx[j]);
+  #pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 kv = __half22float2(k2[e]);
+              const int c = 8 * (j0 + j) + 2 * e;
+  #pragma unroll
+              for (int hh = 0; hh < GQ; ++hh)
+                acc[hh] = fmaf(sq[hh * D + c], kv.x, fmaf(sq[hh * D + c + 1], kv.y, acc[hh]));
+            }
+          }
+        }
+        float sc[GQ], p[GQ];
+  #pragma unroll
+        for (int hh = 0; hh < GQ; ++hh) sc[hh] = ok ? acc[hh] : -INFINITY;
+        fold(sc, p);
+        const int nb = min(kWinT, tab.nres[b] - i0);
+  #pragma unroll 4
+        for (int jj = 0; jj < nb; ++jj) {
+          int sj = s0 + jj;
+          if (sj >= geo.Rcap) sj -= geo.Rcap;
+          const __half *vr = pl.Vr + (bh * geo.Rcap + sj) * D + lane * CPL;
+          float v[CPL];
+  #pragma unroll
+          for (int u = 0; u < CPL; ++u) v[u] = __half2float(vr[u]);
+  #pragma unroll
+          for (int hh = 0; hh < GQ; ++hh) {
+            const float pj = __shfl_sync(kFull, p[hh], jj);
+  #pragma unroll
+            for (int u = 0; u < CPL; ++u) o[hh][u] = fmaf(pj, v[u], o[hh][u]);
+          }
+        }
+      }
+    }
     float beta[GQ];
 #pragma unroll
     for (int hh = 0; hh < GQ; ++hh) beta[hh] = 0.f;
@@ -345,73 +414,6 @@ k_decode_kitty(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
       // let the copies still in flight land (bounded) before the CTA ends
       for (int j = 0; j < kStages; ++j)
         if (pending & (1u << j)) mbar_wait(&bars[j], (phase >> j) & 1u);
-    }
-  }
-  {
-    // the fp16 residual window, folded into the running states of the
-    // sequence's last items: block j of kWinT tokens goes to item
-    // nq - 1 - (j mod nq), warp j mod kWarps of it (lanes 0 ... kWinT - 1
-    // score a token each, lanes over channels sum the values), so that no
-    // CTA carries much more than its share and every warp's loads are few
-    // rounds
-    constexpr int kWinT = 8;
-    const int nblk = (tab.nres[b] + kWinT - 1) / kWinT;
-    for (int j = tab.nq[b] - 1 - k; j < nblk; j += tab.nq[b]) {
-      if (j % kWarps != warp) continue;
-      const int i0 = j * kWinT;
-      const int i = i0 + lane;
-      const bool ok = lane < kWinT && i < tab.nres[b];
-      // ring slots: the block's first token's, then one wrap at most (the
-      // window holds fewer than Rcap tokens)
-      const int s0 = (Tq + i0) % geo.Rcap;
-      int sl = s0 + lane;
-      if (sl >= geo.Rcap) sl -= geo.Rcap;
-      // this lane's key row in 16-byte loads, half of them in flight at a
-      // time (two rounds; the loop keeps q' in shared memory)
-      const uint4 *kr = reinterpret_cast<const uint4 *>(
-          pl.Kr + (bh * geo.Rcap + (ok ? sl : s0)) * D);
-      constexpr int KB = D / 16;
-      float acc[GQ];
-#pragma unroll
-      for (int hh = 0; hh < GQ; ++hh) acc[hh] = 0.f;
-#pragma unroll 1
-      for (int j0 = 0; j0 < D / 8; j0 += KB) {
-        uint4 kx[KB];
-#pragma unroll
-        for (int j = 0; j < KB; ++j) kx[j] = kr[j0 + j];
-#pragma unroll
-        for (int j = 0; j < KB; ++j) {
-          const __half2 *k2 = reinterpret_cast<const __half2 *>(&kx[j]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 kv = __half22float2(k2[e]);
-            const int c = 8 * (j0 + j) + 2 * e;
-#pragma unroll
-            for (int hh = 0; hh < GQ; ++hh)
-              acc[hh] = fmaf(sq[hh * D + c], kv.x, fmaf(sq[hh * D + c + 1], kv.y, acc[hh]));
-          }
-        }
-      }
-      float sc[GQ], p[GQ];
-#pragma unroll
-      for (int hh = 0; hh < GQ; ++hh) sc[hh] = ok ? acc[hh] : -INFINITY;
-      fold(sc, p);
-      const int nb = min(kWinT, tab.nres[b] - i0);
-#pragma unroll 4
-      for (int jj = 0; jj < nb; ++jj) {
-        int sj = s0 + jj;
-        if (sj >= geo.Rcap) sj -= geo.Rcap;
-        const __half *vr = pl.Vr + (bh * geo.Rcap + sj) * D + lane * CPL;
-        float v[CPL];
-#pragma unroll
-        for (int u = 0; u < CPL; ++u) v[u] = __half2float(vr[u]);
-#pragma unroll
-        for (int hh = 0; hh < GQ; ++hh) {
-          const float pj = __shfl_sync(kFull, p[hh], jj);
-#pragma unroll
-          for (int u = 0; u < CPL; ++u) o[hh][u] = fmaf(pj, v[u], o[hh][u]);
-        }
-      }
     }
   }
 
