@@ -52,6 +52,9 @@ struct vq_kivi_cache {
   int32_t age_tps;
   int32_t age_Tq[kMaxB];
   StepIO *io;             // vq_kivi_step_host's slots (first call)
+  // the multi-query attend's key-range partials (grown on demand)
+  void *mq_scratch;
+  size_t mq_scratch_bytes;
 };
 
 namespace {
@@ -756,6 +759,28 @@ int vq_kivi_attend_multi(vq_kivi_cache *c, const void *q, int32_t S_q,
   args.S_q = S_q;
   args.GQ = GQ;
   cudaStream_t st = (cudaStream_t)stream;
+  // key-range splits: the partials of all but the first range and every
+  // range's (max, sum) rows live in the cache's scratch
+  args.splits = multi_splits(c->geo, args, tab, c->sm_count, c->split_tokens);
+  if (args.splits > 1) {
+    const size_t rows = (size_t)p.B * p.H_q * S_q;
+    const size_t o_bytes = round_up((size_t)(args.splits - 1) * rows * p.D * sizeof(float), 256);
+    const size_t need = o_bytes + (size_t)args.splits * rows * sizeof(float2);
+    if (need > c->mq_scratch_bytes) {
+      if (c->mq_scratch) cudaFree(c->mq_scratch);   // waits for its last users
+      c->mq_scratch = nullptr;
+      c->mq_scratch_bytes = 0;
+      cudaError_t ea = cudaMalloc(&c->mq_scratch, need);
+      if (ea != cudaSuccess) {
+        cudaGetLastError();
+        c->mq_scratch = nullptr;
+        return fail(VQ_ERR_OOM, "multi-query attend: scratch of %zu bytes", need);
+      }
+      c->mq_scratch_bytes = need;
+    }
+    args.part_o = static_cast<float *>(c->mq_scratch);
+    args.part_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(c->mq_scratch) + o_bytes);
+  }
   cudaError_t e = launch_attend_multi(c->geo, c->pl, args, tab, st);
   if (e == cudaErrorNotSupported)
     return fail(VQ_ERR_UNSUPPORTED, "multi-query attend: the driver offers no "
@@ -773,6 +798,8 @@ int vq_kivi_free(vq_kivi_cache *c) {
   if (dev != c->device) cudaSetDevice(c->device);
   free_step_io(c->io);
   c->io = nullptr;
+  if (c->mq_scratch) cudaFree(c->mq_scratch);
+  c->mq_scratch = nullptr;
   cudaError_t e = cudaFreeAsync(c->block, c->last_stream);
   cudaError_t e2 = cudaStreamSynchronize(c->last_stream);
   if (dev != c->device && dev >= 0) cudaSetDevice(dev);

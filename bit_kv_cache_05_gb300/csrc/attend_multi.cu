@@ -342,12 +342,18 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
   const int S = tab.S[b], Tq = tab.Tq[b];
   const int g = geo.g, NJ = D / g;
   const size_t hd = (size_t)b * geo.H_kv + h;
-  const int i0 = blockIdx.x * QPT;
+  const int splits = args.splits;
+  const int sp = blockIdx.x % splits;              // this CTA's key range
+  const int i0 = (blockIdx.x / splits) * QPT;
   const int hh = tid / QPT, qi = i0 + tid % QPT;
   const bool valid = qi < S_q;
   const int pos = valid ? S - S_q + qi : -1;       // this row's own token
   const int last_i = min(S_q - 1, i0 + QPT - 1);
   const int max_pos = S - S_q + last_i;            // furthest token any row sees
+  // key tiles [kt_lo, kt_hi) of the nkt the rows see: tokens t_lo ... t_hi - 1
+  const int nkt = max_pos / kTok + 1;
+  const int t_lo = (int)((int64_t)nkt * sp / splits) * kTok;
+  const int t_hi = min((int)((int64_t)nkt * (sp + 1) / splits) * kTok, max_pos + 1);
   const uint8_t *kc_base = pl.Kc + hd * geo.Tcap * ROW;
   const uint8_t *vc_base = pl.Vc + hd * geo.Tcap * ROW;
   const __half *ks_base = pl.Ks + hd * (geo.Tcap / g) * D;
@@ -405,8 +411,8 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
   };
   uint32_t ph_k = 0;
   bool k_pending = false;       // a stage copy is in flight
-  if (tid == 0 && Tq > 0) stage_tile(0);
-  k_pending = Tq > 0;
+  if (tid == 0 && t_lo < Tq && t_lo < t_hi) stage_tile(t_lo);
+  k_pending = t_lo < Tq && t_lo < t_hi;
   // KIVI-Sink: the sinks of the quantized region (the rest are -1); their
   // k_hat / v_hat are their fp16 rows
   __shared__ int ssk[kMaxSink];
@@ -433,7 +439,7 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
   const uint32_t idesc_s = f16_idesc(kRows, kTok), idesc_o = f16_idesc(kRows, D);
   const uint32_t sbase = saddr(sm);
 
-  for (int t0 = 0; t0 <= max_pos && !failed; t0 += kTok) {
+  for (int t0 = t_lo; t0 < t_hi && !failed; t0 += kTok) {
     // (a) the previous O product read P and V_hat: wait before rewriting them
     if (o_pending) {
       const bool ok = mbar_wait(bar_o, ph_o);
@@ -596,7 +602,7 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
 
     // every thread's reads of the stage are done: the next tile's copies
     const int tn = t0 + kTok;
-    if (tn <= max_pos && tn < Tq) {
+    if (tn < t_hi && tn < Tq) {
       if (tid == 0) stage_tile(tn);
       k_pending = true;
     }
@@ -669,15 +675,16 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
       tmem_wait_st();
     }
     float psum = 0.f;
+    // a row that has seen no token of its key range yet keeps m_run = -inf:
+    // subtract 0 there, so that its -inf scores give 0
+    const float msub = m_run == -INFINITY ? 0.f : m_run;
 #pragma unroll
     for (int j8 = 0; j8 < kTok / 8; ++j8) {
       uint32_t hw[4], lw[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        // m_run is finite here (token 0 is in every valid row's first
-        // tile; rows without a query keep 0), so -inf scores give 0
-        const float pa = ex2(sc[8 * j8 + 2 * e] - m_run);
-        const float pc = ex2(sc[8 * j8 + 2 * e + 1] - m_run);
+        const float pa = ex2(sc[8 * j8 + 2 * e] - msub);
+        const float pc = ex2(sc[8 * j8 + 2 * e + 1] - msub);
         psum += pa + pc;
         split2(pa, pc, hw[e], lw[e]);
       }
@@ -714,11 +721,15 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
     o_pending = false;
     failed = __syncthreads_or(!ok);
   }
+  // this row's result: normalised into out, or with several key ranges
+  // unnormalised into this range's rows and its (max, sum) beside them
+  const size_t row = ((size_t)b * geo.H_q + (size_t)h * GQ + hh) * S_q + (valid ? qi : 0);
+  const size_t rows = (size_t)geo.B * geo.H_q * S_q;
+  if (!failed && valid && splits > 1) args.part_ml[sp * rows + row] = make_float2(m_run, l_run);
   if (!failed && o_started) {
     tc_fence_after();
-    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-    float *orow = args.out +
-                  (((size_t)b * geo.H_q + (size_t)h * GQ + hh) * S_q + (valid ? qi : 0)) * D;
+    const float inv = splits > 1 ? 1.f : (l_run > 0.f ? 1.f / l_run : 0.f);
+    float *orow = (sp == 0 ? args.out : args.part_o + (sp - 1) * rows * D) + row * D;
 #pragma unroll
     for (int c = 0; c < D; c += 32) {
       float o[32];
@@ -730,6 +741,11 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
                  make_float4(o[j] * inv, o[j + 1] * inv, o[j + 2] * inv, o[j + 3] * inv));
       }
     }
+  } else if (!failed && valid && splits > 1) {
+    // a key range without any product (none of its tiles issued one)
+    float *orow = (sp == 0 ? args.out : args.part_o + (sp - 1) * rows * D) + row * D;
+    for (int c = 0; c < D; c += 4)
+      __stcs(reinterpret_cast<float4 *>(orow + c), make_float4(0.f, 0.f, 0.f, 0.f));
   }
   if (failed) {
     if (tid == 0) atomicOr(args.err, 2u);
@@ -745,6 +761,48 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols));
   }
+}
+
+// Merge of the key ranges of a split multi-query attend: one warp per row
+// (sequence, query head, query), lanes over channels; the ranges' rows are
+// weighted by 2^(m_k - M) with M their largest maximum and divided by the
+// weighted sum of their sums.
+template <int D>
+__global__ void __launch_bounds__(256)
+k_attend_combine(MultiArgs args, int64_t rows) {
+  constexpr int CPL = D / 32;
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int lane = threadIdx.x & 31;
+  const int splits = args.splits;
+  float M = -INFINITY;
+  for (int k = 0; k < splits; ++k) M = fmaxf(M, args.part_ml[k * rows + row].x);
+  float L = 0.f, o[CPL];
+#pragma unroll
+  for (int u = 0; u < CPL; ++u) o[u] = 0.f;
+  for (int k = 0; k < splits; ++k) {
+    const float2 ml = args.part_ml[k * rows + row];
+    const float f = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
+    L = fmaf(f, ml.y, L);
+    const float *src = (k == 0 ? args.out : args.part_o + (k - 1) * rows * D) + row * D +
+                       lane * CPL;
+    float v[CPL];
+    if constexpr (CPL == 4) {
+      const float4 x = __ldcs(reinterpret_cast<const float4 *>(src));
+      v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    } else {
+      const float2 x = __ldcs(reinterpret_cast<const float2 *>(src));
+      v[0] = x.x; v[1] = x.y;
+    }
+#pragma unroll
+    for (int u = 0; u < CPL; ++u) o[u] = fmaf(f, v[u], o[u]);
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  float *dst = args.out + row * D + lane * CPL;
+  if constexpr (CPL == 4)
+    *reinterpret_cast<float4 *>(dst) = make_float4(o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
+  else
+    *reinterpret_cast<float2 *>(dst) = make_float2(o[0] * inv, o[1] * inv);
 }
 
 // ---- host ------------------------------------------------------------------
@@ -795,8 +853,13 @@ cudaError_t launch_k(const Geometry &geo, const Planes &pl, const MultiArgs &arg
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((args.S_q + QPT - 1) / QPT, geo.H_kv, geo.B);
+  dim3 grid((args.S_q + QPT - 1) / QPT * args.splits, geo.H_kv, geo.B);
   k_attend_multi<D, BITS, FRAG><<<grid, kThreads, smem, st>>>(map, geo, pl, args, tab);
+  count_launch();
+  e = cudaGetLastError();
+  if (e != cudaSuccess || args.splits == 1) return e;
+  const int64_t rows = (int64_t)geo.B * geo.H_q * args.S_q;
+  k_attend_combine<D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(args, rows);
   count_launch();
   return cudaGetLastError();
 }
@@ -816,6 +879,30 @@ cudaError_t launch_d(const Geometry &geo, const Planes &pl, const MultiArgs &arg
 }
 
 }  // namespace multi
+
+int multi_splits(const Geometry &geo, const MultiArgs &args, const MultiTable &tab,
+                 int sm_count, int split_tokens) {
+  const int QPT = multi::kRows / args.GQ;
+  const int64_t tiles = (args.S_q + QPT - 1) / QPT;
+  int S_max = 0;
+  for (int b = 0; b < geo.B; ++b) S_max = tab.S[b] > S_max ? tab.S[b] : S_max;
+  const int nkt = (S_max + multi::kTok - 1) / multi::kTok;
+  if (split_tokens > 0) {
+    int s = (S_max + split_tokens - 1) / split_tokens;
+    if (s > 8) s = 8;
+    if (s > nkt) s = nkt;
+    return s < 1 ? 1 : s;
+  }
+  // about 16 waves of CTAs (two per SM): the tiles' CTAs differ in length,
+  // and finer ones fill the last waves (measured on 1024 CTAs of 520 key
+  // tiles: 1, 2, 4, 5 ranges: 10.49, 10.18, 9.78, 9.61 ms; 6 and 8 no
+  // faster); at most 8 ranges, each at least 8 key tiles
+  const int64_t ctas = tiles * geo.H_kv * geo.B, slots = 2 * (int64_t)sm_count;
+  int64_t s = (16 * slots + ctas - 1) / ctas;
+  if (s > 8) s = 8;
+  while (s > 1 && nkt / s < 8) --s;
+  return s < 1 ? 1 : (int)s;
+}
 
 cudaError_t launch_attend_multi(const Geometry &geo, const Planes &pl,
                                 const MultiArgs &args, const MultiTable &tab,

@@ -381,7 +381,21 @@ struct MultiArgs {
   float scale_log2;    // softmax scale * log2(e)
   int S_q;             // query tokens per sequence (its newest S_q tokens)
   int GQ;              // query heads per kv head (1, 2, 4 or 8)
+  // key-range splits per query tile (1: none).  With several, split 0
+  // leaves its unnormalised rows in out, split k > 0 in part_o + (k - 1)
+  // rows x D, and every split its rows' (max, sum) in part_ml + k rows; a
+  // combine kernel merges them into out
+  int splits = 1;
+  float *part_o = nullptr;
+  float2 *part_ml = nullptr;
 };
+
+// key-range splits for a multi-query attend: about 16 waves of CTAs (two
+// per SM), at most 8 splits, each at least 8 key tiles of 64 tokens;
+// split_tokens > 0 asks for about that many keys per split instead (tests,
+// tuning)
+int multi_splits(const Geometry &geo, const MultiArgs &args, const MultiTable &tab,
+                 int sm_count, int split_tokens);
 
 // D = 64 or 128; cudaErrorNotSupported when the driver offers no tensor-map
 // encoder

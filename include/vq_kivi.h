@@ -213,10 +213,19 @@ int vq_kivi_step_host(vq_kivi_cache *c, const void *h_k_new,
  *   S_q            >= 1, at most the length of every sequence
  *   out            device, fp32, [B][H_q][S_q][D], 16-byte aligned
  *   softmax_scale  <= 0 selects 1/sqrt(D)
+ * When the query tiles make few waves on the GPU (e.g. a 512-token chunk
+ * of 8 sequences: 1024 CTAs on 304 slots) each tile's keys are cut into up
+ * to 8 ranges (5 there), whose partial rows a second kernel merges with a
+ * log-sum-exp;
+ * their partials live in a scratch the cache allocates on first need
+ * ((ranges - 1) x B x H_q x S_q x D x 4 bytes, plus 8 bytes per row and
+ * range) and keeps.
  * Supported: D = 64 or 128 and H_q/H_kv in {1, 2, 4, 8}
  * (VQ_ERR_UNSUPPORTED otherwise); VQ_ERR_ARG when a sequence holds fewer
- * than S_q tokens.  Uses no workspace of the cache, so it may follow or
- * precede vq_kivi_decode_attend in any order on the cache's stream. */
+ * than S_q tokens; VQ_ERR_OOM when the scratch cannot be allocated.  Uses
+ * none of the decode's workspace, so it may follow or precede
+ * vq_kivi_decode_attend in any order on the cache's stream (two multi-query
+ * calls on one cache share the scratch: one in flight at a time). */
 int vq_kivi_attend_multi(vq_kivi_cache *c, const void *q, int32_t S_q,
                          float *out, float softmax_scale, void *stream);
 
@@ -300,8 +309,9 @@ int vq_kivi_cache_bytes(const vq_kivi_cache *c, vq_kivi_bytes *out);
 
 /* Decode work partition: about this many quantized tokens per split-KV work
  * item (a multiple of 64 and of g, at least the workspace minimum of 256),
- * or 0 for the automatic choice (the default).  Results are invariant to it
- * up to fp32 rounding; exposed for tests and tuning. */
+ * or 0 for the automatic choice (the default); for the multi-query attend,
+ * about this many keys per key range (at most 8 ranges).  Results are
+ * invariant to it up to fp32 rounding; exposed for tests and tuning. */
 int vq_kivi_set_split_tokens(vq_kivi_cache *c, int32_t tokens_per_split);
 
 /* Number of kernels this library has launched in this process. */

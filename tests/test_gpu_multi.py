@@ -121,6 +121,27 @@ def test_chunk_appended_then_attended(lib):
     c.close()
 
 
+@pytest.mark.parametrize("split_tokens", [256, 640])
+def test_key_ranges_match_the_oracle(lib, split_tokens):
+    """Key ranges per query tile (forced through the split hook): partial
+    rows merged by the combine kernel, the same result within tolerance;
+    ranges that lie wholly past some rows' own tokens leave those rows
+    empty partials."""
+    from bit_kv_cache_05_gb300 import _lib
+    w = synth.shrink(synth.workload("gqa_serving"), [900, 260, 517], n_append=0)
+    c, oc = _pair(w, seed=46)
+    _lib.check(lib.vq_kivi_set_split_tokens(c._h, split_tokens))
+    g = torch.Generator().manual_seed(8)
+    for S_q in (40, 200):
+        q = (torch.randn(w.B, w.H_q, S_q, w.D, generator=g)).half()
+        got = c.attend_multi(q.cuda())
+        torch.cuda.synchronize()
+        _close(got.cpu().numpy(), oc.attend_multi(q.numpy()),
+               f"split_tokens={split_tokens} S_q={S_q}")
+    c.device_status()
+    c.close()
+
+
 def test_one_query_equals_the_decode(lib):
     w = synth.shrink(synth.workload("pages_S512"), [512], n_append=0)
     c, _ = _pair(w, seed=45)
