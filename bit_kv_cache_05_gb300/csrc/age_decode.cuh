@@ -41,6 +41,8 @@ constexpr unsigned kFull = 0xffffffffu;
 // 2^-62 of the largest.  This needs IEEE subnormals on the FMA path (the
 // library is built without flush-to-zero).
 constexpr int kCarry = 64;
+// tokens of a residual-window block (lanes 0 ... kWinT - 1 score one each)
+constexpr int kWinT = 8;
 
 __device__ __forceinline__ float pow2(int e) {   // 2^e, -126 <= e <= 127
   return __int_as_float((127 + e) << 23);
@@ -79,21 +81,23 @@ template <int D, int GQ> struct AgeSmem {
 };
 
 // Fused decode over an age-tiered cache.  One CTA of 4 warps per (work
-// item, kv head); the warps take the item's key groups round robin, each
-// streaming its blocks through its own bulk-copy pipeline (kStages stages,
-// one mbarrier each, bounded waits).  Per block:
+// item, kv head); the sequence's staged blocks are dealt round robin over
+// its items' warps, each warp streaming its blocks through its own
+// bulk-copy pipeline (kStages stages, one mbarrier each, bounded waits).
+// Per block:
 //  - scores, one token per lane: its key row's fields against
-//    a'_c = q'_c s_Gc (the group's a' built once per group), plus the group's
-//    zero-point term beta = sum_c q'_c z_Gc;
+//    a'_c = q'_c s_Gc (the group's a' built when the warp's block is of
+//    another group than its previous one), plus the group's zero-point term
+//    beta = sum_c q'_c z_Gc;
 //  - a per-block online softmax per query head (the warp maximum reduced
 //    only when some score exceeds the running one; sums stay per lane);
 //  - value weights, one token per lane: w' = p s_tj and u = p z_tj per value
 //    group j, through shared memory;
 //  - values, lanes over channels (lane*CPL ...): o_c += w' code_tc per token
 //    and the zero-point sum sum_t u_tj.
-// A sequence's last item also folds in the fp16 residual window (one token
-// per lane, read from global memory).  The CTA's warps are merged with a
-// log-sum-exp into one partial per item.
+// The fp16 residual window's blocks are dealt after the groups', read from
+// global memory.  The CTA's warps are merged with a log-sum-exp into one
+// partial per item.
 template <int D, int GQ>
 __global__ void __launch_bounds__(kThreads)
 k_decode_age(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
@@ -118,6 +122,29 @@ k_decode_age(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
   const size_t bh = (size_t)b * geo.H_kv + h;
   const int Tq = tab.Tq[b];
   const int S = Tq + tab.nres[b];
+  // The sequence's work in staged blocks: its Gend quantized key groups,
+  // each in nb = max(1, g w / 64) blocks of 64 / w tokens at its tier's
+  // width w (tier 2's groups first, then tier 1's, then tier 0's), then the
+  // fp16 residual window in kWinT-token blocks.  Block x goes to item
+  // x mod nq, warp (x / nq) mod kWarps: every warp of every item takes the
+  // same mix of widths and window blocks, whatever their relative costs
+  // (groups of the recent, wider tiers are several blocks; a whole group per
+  // warp left the warps that held one a block or more behind the rest).
+  const int nq = tab.nq[b];
+  const int Gend = Tq / g;
+  // tiers by group index (age_tier): groups G < Ga are in tier 2, G < Gb
+  // in tier 1 or 2, the rest in tier 0
+  const int Ga = min(max(0, (S - geo.age_b2) / g), Gend);
+  const int Gb = min(max(Ga, (S - geo.age_b1) / g), Gend);
+  const int wA = geo.age_bits[2], wB = geo.age_bits[1], wC = geo.age_bits[0];
+  // log2 of the blocks per group (g is 16 ... 128 and w 2, 4 or 8, so
+  // nb is a power of two)
+  const int lA = __ffs(max(1, g * wA / 64)) - 1, lB = __ffs(max(1, g * wB / 64)) - 1,
+            lC = __ffs(max(1, g * wC / 64)) - 1;
+  const int XA = Ga << lA, XB = XA + ((Gb - Ga) << lB), XQ = XB + ((Gend - Gb) << lC);
+  const int nblk = (tab.nres[b] + kWinT - 1) / kWinT;
+  const int stride = nq * kWarps;
+  const int x0 = k + nq * warp;         // this warp's first block
   if (lane == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(&bars[s]);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -167,18 +194,6 @@ k_decode_age(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
   bool failed = false;
   uint32_t phase = 0, pending = 0;
   {
-    // the item's key groups: k, k + nq, k + 2 nq, ... of the sequence's
-    // Gend quantized groups (strided, so that every item of a sequence gets
-    // the same mix of tiers: the recent, wider tiers cost more per token)
-    const int nq = tab.nq[b];
-    const int Gend = Tq / g;
-    // tiers by group index (age_tier): groups G < Ga are in tier 2, G < Gb
-    // in tier 1 or 2, the rest in tier 0
-    const int Ga = max(0, (S - geo.age_b2) / g), Gb = max(0, (S - geo.age_b1) / g);
-    const int wA = geo.age_bits[2], wB = geo.age_bits[1], wC = geo.age_bits[0];
-    auto width = [&](int G) { return G < Ga ? wA : (G < Gb ? wB : wC); };
-    // stage blocks per group at 2 / 4 / 8 bits: bt = 64 / w tokens, at most g
-    const int nb2 = g >= 32 ? g / 32 : 1, nb4 = g / 16, nb8 = g / 8;
     // the (b, h) planes
     const unsigned char *kc0 = pl.Kc + bh * geo.Tcap * D;
     const unsigned char *vc0 = pl.Vc + bh * geo.Tcap * D;
@@ -186,16 +201,26 @@ k_decode_age(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
     const __half *vz0 = pl.Vz + bh * geo.Tcap * NJ;
     const __half *ks0 = pl.Ks + bh * (geo.Tcap / g) * D;
     const __half *kz0 = pl.Kz + bh * (geo.Tcap / g) * D;
-    // this warp's blocks in order: groups k + nq (warp + kWarps i), each in
-    // nb blocks
-    struct Cur { int G, blk, nb, w; };
-    auto at = [&](int G) {
-      const int w = width(G);
-      return Cur{G, 0, w == 2 ? nb2 : (w == 4 ? nb4 : nb8), w};
+    // this warp's blocks in order, x0 + stride i < XQ: block x is block
+    // blk of group G at width w; `first` when the warp's previous block was
+    // of another group (the stage then also takes the group's key scale and
+    // zero rows, and the warp builds the group's a' and beta)
+    struct Cur { int x, G, blk, w; bool first; };
+    auto at = [&](int x, int Gprev) {
+      Cur c{x, Gend, 0, 2, false};
+      if (x < XA) {
+        c.G = x >> lA; c.blk = x & ((1 << lA) - 1); c.w = wA;
+      } else if (x < XB) {
+        const int y = x - XA;
+        c.G = Ga + (y >> lB); c.blk = y & ((1 << lB) - 1); c.w = wB;
+      } else if (x < XQ) {
+        const int y = x - XB;
+        c.G = Gb + (y >> lC); c.blk = y & ((1 << lC) - 1); c.w = wC;
+      }
+      c.first = c.G != Gprev;
+      return c;
     };
-    auto advance = [&](Cur &c) {
-      if (++c.blk == c.nb) c = at(c.G + kWarps * nq);
-    };
+    auto advance = [&](Cur &c) { c = at(c.x + stride, c.G); };
     auto issue = [&](const Cur &c, int s) {
       if (lane == 0) {
         const int bt = min(g, 64 / c.w);
@@ -203,20 +228,20 @@ k_decode_age(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
         unsigned char *st = stage0 + s * SG::BYTES;
         const int r0 = c.G * g + c.blk * bt;      // first token of the block
         const size_t co = (size_t)c.G * g * D + (size_t)c.blk * cb;
-        mbar_expect_tx(&bars[s], 2 * cb + 2 * vb + (c.blk == 0 ? 4 * D : 0));
+        mbar_expect_tx(&bars[s], 2 * cb + 2 * vb + (c.first ? 4 * D : 0));
         bulk_g2s(st + SG::KC, kc0 + co, cb, &bars[s]);
         bulk_g2s(st + SG::VC, vc0 + co, cb, &bars[s]);
         bulk_g2s(st + SG::VS, vs0 + (size_t)r0 * NJ, vb, &bars[s]);
         bulk_g2s(st + SG::VZ, vz0 + (size_t)r0 * NJ, vb, &bars[s]);
-        if (c.blk == 0) {
+        if (c.first) {
           bulk_g2s(st + SG::KS, ks0 + (size_t)c.G * D, 2 * D, &bars[s]);
           bulk_g2s(st + SG::KZ, kz0 + (size_t)c.G * D, 2 * D, &bars[s]);
         }
       }
     };
-    Cur pc = at(k + warp * nq);   // next block to copy
+    Cur pc = at(x0, -1);          // next block to copy
     Cur cc = pc;                  // next block to compute
-    for (int s = 0; s < kStages && pc.G < Gend; ++s) {
+    for (int s = 0; s < kStages && pc.x < XQ; ++s) {
       issue(pc, s);
       pending |= 1u << s;
       advance(pc);
@@ -226,13 +251,13 @@ k_decode_age(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
     for (int hh = 0; hh < GQ; ++hh) beta[hh] = 0.f;
 
     // one staged block at width W
-    auto block = [&](auto w_tag, auto bt_tag, const unsigned char *st, int blk) {
+    auto block = [&](auto w_tag, auto bt_tag, const unsigned char *st, bool first) {
       constexpr int W = decltype(w_tag)::value;
       constexpr int bt = decltype(bt_tag)::value;   // tokens of the block
       constexpr uint32_t CM = (1u << W) - 1u;
       constexpr int PER = 32 / W;         // fields per 32-bit word
       constexpr int RB = D * W / 8;       // row bytes
-      if (blk == 0) {
+      if (first) {
         // the group's a' = q' s 2^(149 - kCarry - pos), pos = c W mod 16 (the
         // field's place after the key loop's optional 16-bit shift), and
         // beta = q'.z, lanes over channels
@@ -366,7 +391,7 @@ k_decode_age(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
     };
 
     int s = 0;
-    while (cc.G < Gend) {
+    while (cc.x < XQ) {
       const bool ok = __all_sync(kFull, mbar_wait(&bars[s], (phase >> s) & 1u));
       if (!ok) { failed = true; break; }
       phase ^= 1u << s;
@@ -377,15 +402,15 @@ k_decode_age(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
       using I16 = std::integral_constant<int, 16>;
       using I32 = std::integral_constant<int, 32>;
       if (w == 2) {
-        if (g >= 32) block(std::integral_constant<int, 2>{}, I32{}, st, cc.blk);
-        else block(std::integral_constant<int, 2>{}, I16{}, st, cc.blk);
+        if (g >= 32) block(std::integral_constant<int, 2>{}, I32{}, st, cc.first);
+        else block(std::integral_constant<int, 2>{}, I16{}, st, cc.first);
       } else if (w == 4) {
-        block(std::integral_constant<int, 4>{}, I16{}, st, cc.blk);
+        block(std::integral_constant<int, 4>{}, I16{}, st, cc.first);
       } else {
-        block(std::integral_constant<int, 8>{}, I8{}, st, cc.blk);
+        block(std::integral_constant<int, 8>{}, I8{}, st, cc.first);
       }
       __syncwarp();
-      if (pc.G < Gend) {
+      if (pc.x < XQ) {
         // every lane's reads of the stage come before the copies into it
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         issue(pc, s);
@@ -412,17 +437,15 @@ k_decode_age(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
     }
   }
   {
-    // the fp16 residual window, folded into the running states of the
-    // sequence's last items: block j of kWinT tokens goes to item
-    // nq - 1 - (j mod nq), warp j mod kWarps of it (lanes 0 ... kWinT - 1
-    // score a token each, lanes over channels sum the values), so that no
-    // CTA carries much more than its share and every warp's loads are few
-    // rounds
-    constexpr int kWinT = 8;
-    const int nblk = (tab.nres[b] + kWinT - 1) / kWinT;
-    for (int j = tab.nq[b] - 1 - k; j < nblk; j += tab.nq[b]) {
-      if (j % kWarps != warp) continue;
-      const int i0 = j * kWinT;
+    // this warp's blocks of the fp16 residual window (block x = XQ + j is
+    // window block j), folded into the running states after the groups (the
+    // value sums are at true scale by now); lanes 0 ... kWinT - 1 score a
+    // token each, lanes over channels sum the values
+    int xw = x0;
+    if (xw < XQ) xw += (XQ - xw + stride - 1) / stride * stride;
+#pragma unroll 1
+    for (; xw < XQ + nblk; xw += stride) {
+      const int i0 = (xw - XQ) * kWinT;
       const int i = i0 + lane;
       const bool ok = lane < kWinT && i < tab.nres[b];
       // ring slots: the block's first token's, then one wrap at most (the
