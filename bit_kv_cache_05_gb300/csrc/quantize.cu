@@ -520,14 +520,20 @@ k_flush_t(Geometry geo, Planes pl, const __half *__restrict__ Kin,
     if (p >= P0 && p < P0 + G) atomicOr(&sinkm[(p - P0) >> 5], 1u << ((p - P0) & 31));
   }
   // the key and value tiles (G rows of D fp16 values each) by 16-byte
-  // asynchronous copies, all in flight together
+  // asynchronous copies, all in flight together, in two groups: the keys
+  // are quantized while the value tile still lands
 #pragma unroll
   for (int k = 0; k < G * CPR / D; ++k) {
     const int idx = c + k * D, i = idx / CPR, c8 = (idx % CPR) * 8;
     cp_async16(tile + i * D + c8, sk[i] + c8);
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+#pragma unroll
+  for (int k = 0; k < G * CPR / D; ++k) {
+    const int idx = c + k * D, i = idx / CPR, c8 = (idx % CPR) * 8;
     cp_async16(vtile + i * VS + c8, sv[i] + c8);
   }
-  asm volatile("cp.async.commit_group;\n cp.async.wait_group 0;" ::: "memory");
+  asm volatile("cp.async.commit_group;\n cp.async.wait_group 1;" ::: "memory");
   __syncthreads();
   auto is_sink = [&](int i) { return sinks && ((sinkm[i >> 5] >> (i & 31)) & 1u); };
 
@@ -570,22 +576,30 @@ k_flush_t(Geometry geo, Planes pl, const __half *__restrict__ Kin,
       const unsigned m = __reduce_max_sync(0xffffffffu, (unsigned)__half_as_ushort(sh));
       if ((c & 31) == 0) atomicMax(pl.ksmax + bh, m);
     }
-    uint64_t near = 0;   // bit i: token i's value is near a half-integer
+    // bit k: a value of token pair k is near a half-integer (one bit per
+    // pair: one select and one or per two values)
+    uint32_t near = 0;
 #pragma unroll
     for (int k = 0; k < G / 2; ++k) {
       uint32_t c0, c1;
       bool n0, n1;
       quant2_flag<levels>(__half22float2(col[k]), mn, rcp, c0, c1, n0, n1);
-      near |= ((uint64_t)n0 << (2 * k)) | ((uint64_t)n1 << (2 * k + 1));
+      near |= (uint32_t)(n0 | n1) << k;
       codes[(2 * k) * CS + c] = (uint8_t)c0;
       codes[(2 * k + 1) * CS + c] = (uint8_t)c1;
     }
-    // the rare near-ties: the correctly rounded quotient (scale == 0 gives
-    // rcp = 0, t = 0 and no near-tie)
+    // the rare near-ties: the pair's flags again, and the correctly rounded
+    // quotient for the flagged values (scale == 0 gives rcp = 0, t = 0 and
+    // no near-tie)
     while (near) {
-      const int i = __ffsll((long long)near) - 1;
+      const int k = __ffs(near) - 1;
       near &= near - 1;
-      codes[i * CS + c] = (uint8_t)quant_exact(__half2float(tile[i * D + c]), mn, scale);
+      const __half2 x2 = __halves2half2(tile[(2 * k) * D + c], tile[(2 * k + 1) * D + c]);
+      uint32_t c0, c1;
+      bool n0, n1;
+      quant2_flag<levels>(__half22float2(x2), mn, rcp, c0, c1, n0, n1);
+      if (n0) codes[(2 * k) * CS + c] = (uint8_t)quant_exact(__low2float(x2), mn, scale);
+      if (n1) codes[(2 * k + 1) * CS + c] = (uint8_t)quant_exact(__high2float(x2), mn, scale);
     }
     // sink tokens hold code 0 (their rows are kept in fp16)
     if (sinks) {
@@ -609,6 +623,8 @@ k_flush_t(Geometry geo, Planes pl, const __half *__restrict__ Kin,
   } else {
     store_packed_tile_t<BITS, D, G>(codes, pl.Kc + (bh * geo.Tcap + P0) * ROW);
   }
+  // this thread's value copies complete, then every thread's
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
   __syncthreads();
 
   // ---- values: token i over channels j*G ... j*G+G-1, in registers ----
@@ -635,7 +651,7 @@ k_flush_t(Geometry geo, Planes pl, const __half *__restrict__ Kin,
     const float scale = empty ? 0.f : __fdiv_rn(__fadd_rn(__fsub_rn(mx, mn), 0.0f), (float)levels);
     const float rcp = scale != 0.0f ? __frcp_rn(scale) : 0.0f;
     uint32_t *crow = reinterpret_cast<uint32_t *>(codes + i * CS + j * G);
-    uint64_t near = 0;   // bit v: value v of the group is near a half-integer
+    uint32_t near = 0;   // bit v: a value of pair v of the group is near a half-integer
 #pragma unroll
     for (int k = 0; k < G / 8; ++k) {
       const __half2 *h4 = reinterpret_cast<const __half2 *>(&u[k]);
@@ -645,17 +661,23 @@ k_flush_t(Geometry geo, Planes pl, const __half *__restrict__ Kin,
         uint32_t c0, c1;
         bool n0, n1;
         quant2_flag<levels>(__half22float2(h4[e]), mn, rcp, c0, c1, n0, n1);
-        near |= ((uint64_t)n0 << (8 * k + 2 * e)) | ((uint64_t)n1 << (8 * k + 2 * e + 1));
+        near |= (uint32_t)(n0 | n1) << (4 * k + e);
         w[e >> 1] |= (c0 | (c1 << 8)) << (16 * (e & 1));
       }
       crow[2 * k] = w[0];
       crow[2 * k + 1] = w[1];
     }
-    // the rare near-ties
+    // the rare near-ties: the pair's flags again
     while (near) {
-      const int v = __ffsll((long long)near) - 1;
+      const int v = __ffs(near) - 1;
       near &= near - 1;
-      codes[i * CS + j * G + v] = (uint8_t)quant_exact(__half2float(vtile[i * VS + j * G + v]), mn, scale);
+      const __half2 x2 = reinterpret_cast<const __half2 *>(vtile + i * VS + j * G)[v];
+      uint32_t c0, c1;
+      bool n0, n1;
+      quant2_flag<levels>(__half22float2(x2), mn, rcp, c0, c1, n0, n1);
+      uint8_t *cv = codes + i * CS + j * G + 2 * v;
+      if (n0) cv[0] = (uint8_t)quant_exact(__low2float(x2), mn, scale);
+      if (n1) cv[1] = (uint8_t)quant_exact(__high2float(x2), mn, scale);
     }
     const size_t vidx = (bh * geo.Tcap + P0 + i) * NJ + j;
     pl.Vs[vidx] = __float2half_rn(scale);
