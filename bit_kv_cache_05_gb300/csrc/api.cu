@@ -568,9 +568,9 @@ int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
     // AgeTieredKV and Kitty: one wave of CTAs, each streaming its groups through
     // per-warp pipelines (a CTA's start costs a pipeline fill, so items are
     // long); a sequence's last item also takes its residual window.  Among
-    // the splits whose items fit one wave, take the one with the fewest
-    // tokens on the busiest SM, ceil(items / SMs) items of tps tokens (the
-    // launcher caps the CTAs per SM at that count).
+    // the splits whose items fit one wave, take the one whose busiest SM
+    // (ceil(items / SMs) items of tps tokens; the launcher caps the CTAs per
+    // SM at that count) finishes first by the cost below.
     if (c->age_tps > 0 && !memcmp(c->age_Tq, c->Tq, sizeof(int32_t) * p.B)) {
       tps = c->age_tps;
     } else {
@@ -592,10 +592,17 @@ int vq_kivi_decode_attend(vq_kivi_cache *c, const void *q, float *out,
       t = (int64_t)round_up((size_t)(t > 1 ? t : 1), unit);
       // more (sequence, head) pairs than CTA slots: one item each
       while (items(t) > cap && t < t_top) t += unit;
-      int64_t best = t, best_cost = -1;
+      // the busiest SM holds k = ceil(items / SMs) CTAs of t tokens (plus a
+      // pipeline fill each); an SM's throughput grows with its CTAs (their
+      // warps hide one another's latency: per-CTA timestamps of the
+      // AgeTieredKV decode, two CTAs on an SM 1.7 times one alone), taken
+      // here as k^0.75, so the cost is k^0.25 (t + 64)
+      int64_t best = t;
+      double best_cost = -1.0;
       for (int i = 0; i < 64; ++i, t += unit) {
         const int64_t n = items(t);
-        const int64_t cost = (n + sms - 1) / sms * (t + 64);
+        const double k = (double)((n + sms - 1) / sms);
+        const double cost = std::pow(k, 0.25) * (double)(t + 64);
         if (best_cost < 0 || cost < best_cost) { best = t; best_cost = cost; }
         if (n <= p.H_kv) break;   // one item per sequence and head
       }
