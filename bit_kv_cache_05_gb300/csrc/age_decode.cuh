@@ -298,12 +298,13 @@ k_decode_age(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
       // scores: lane = token
       float sc[GQ];
       {
-        // one partial sum per word of a 16-byte load: four FMA chains
-        float acc[GQ][4];
+        // one partial sum per word of a 16-byte load: four chains of packed
+        // two-channel FMAs (f32x2: two fields per instruction)
+        float2 acc[GQ][4];
 #pragma unroll
         for (int hh = 0; hh < GQ; ++hh)
 #pragma unroll
-          for (int jw = 0; jw < 4; ++jw) acc[hh][jw] = 0.f;
+          for (int jw = 0; jw < 4; ++jw) acc[hh][jw] = make_float2(0.f, 0.f);
         if (lane < bt) {
           const uint4 *row = reinterpret_cast<const uint4 *>(st + SG::KC + lane * RB);
 #pragma unroll 2
@@ -326,11 +327,9 @@ k_decode_age(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
 #pragma unroll
                 for (int hh = 0; hh < GQ; ++hh) {
                   const float4 a4 = *reinterpret_cast<const float4 *>(sa + hh * D + cw + e);
-                  float r = acc[hh][jw];
-                  r = fmaf(a4.x, f[0], r);
-                  r = fmaf(a4.y, f[1], r);
-                  r = fmaf(a4.z, f[2], r);
-                  r = fmaf(a4.w, f[3], r);
+                  float2 r = acc[hh][jw];
+                  r = __ffma2_rn(make_float2(a4.x, a4.y), make_float2(f[0], f[1]), r);
+                  r = __ffma2_rn(make_float2(a4.z, a4.w), make_float2(f[2], f[3]), r);
                   acc[hh][jw] = r;
                 }
               }
@@ -339,7 +338,8 @@ k_decode_age(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
         }
 #pragma unroll
         for (int hh = 0; hh < GQ; ++hh) {
-          const float a = (acc[hh][0] + acc[hh][1]) + (acc[hh][2] + acc[hh][3]);
+          const float a = ((acc[hh][0].x + acc[hh][0].y) + (acc[hh][1].x + acc[hh][1].y)) +
+                          ((acc[hh][2].x + acc[hh][2].y) + (acc[hh][3].x + acc[hh][3].y));
           sc[hh] = lane < bt ? fmaf(a, pow2(kCarry), beta[hh]) : -INFINITY;
         }
       }
@@ -383,8 +383,14 @@ k_decode_age(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
 #pragma unroll
         for (int hh = 0; hh < GQ; ++hh) {
           const float2 q2 = wh[hh][jj];
+          // two channels per packed FMA
 #pragma unroll
-          for (int u = 0; u < CPL; ++u) o[hh][u] = fmaf(q2.x, f[u], o[hh][u]);
+          for (int u = 0; u < CPL; u += 2) {
+            const float2 r = __ffma2_rn(make_float2(q2.x, q2.x), make_float2(f[u], f[u + 1]),
+                                        make_float2(o[hh][u], o[hh][u + 1]));
+            o[hh][u] = r.x;
+            o[hh][u + 1] = r.y;
+          }
           zl[hh] += q2.y;
         }
       }
