@@ -177,8 +177,14 @@ k_decode_kitty(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
 #pragma unroll
       for (int hh = 0; hh < GQ; ++hh) {
         const float pj = __shfl_sync(kFull, p[hh], jj);
+        // two channels per packed (f32x2) FMA
 #pragma unroll
-        for (int u = 0; u < CPL; ++u) o[hh][u] = fmaf(pj, v[u], o[hh][u]);
+        for (int u = 0; u < CPL; u += 2) {
+          const float2 r = __ffma2_rn(make_float2(pj, pj), make_float2(v[u], v[u + 1]),
+                                      make_float2(o[hh][u], o[hh][u + 1]));
+          o[hh][u] = r.x;
+          o[hh][u + 1] = r.y;
+        }
       }
     }
   };
@@ -337,12 +343,13 @@ k_decode_kitty(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
         for (int hh = 0; hh < GQ; ++hh) beta[hh] = warp_sum(part[hh]);
         __syncwarp();
       }
-      // scores: lane = token; its row's 4-bit words, then its 2-bit words
+      // scores: lane = token; its row's 4-bit words, then its 2-bit words,
+      // two fields per packed (f32x2) FMA
       float sc[GQ];
       {
-        float acc[GQ][2];
+        float2 acc[GQ][2];
 #pragma unroll
-        for (int hh = 0; hh < GQ; ++hh) acc[hh][0] = acc[hh][1] = 0.f;
+        for (int hh = 0; hh < GQ; ++hh) acc[hh][0] = acc[hh][1] = make_float2(0.f, 0.f);
         if (lane < bt) {
           const uint32_t *row = reinterpret_cast<const uint32_t *>(st + SG::KC + lane * krow);
 #pragma unroll 2
@@ -352,15 +359,15 @@ k_decode_kitty(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
             for (int hh = 0; hh < GQ; ++hh) {
               const float4 a0 = *reinterpret_cast<const float4 *>(sa + hh * D + 8 * w);
               const float4 a1 = *reinterpret_cast<const float4 *>(sa + hh * D + 8 * w + 4);
-              float r0 = acc[hh][0], r1 = acc[hh][1];
-              r0 = fmaf(a0.x, __uint_as_float(x & 0xFu), r0);
-              r0 = fmaf(a0.y, __uint_as_float(x & 0xF0u), r0);
-              r0 = fmaf(a0.z, __uint_as_float(x & 0xF00u), r0);
-              r0 = fmaf(a0.w, __uint_as_float(x & 0xF000u), r0);
-              r1 = fmaf(a1.x, __uint_as_float(y & 0xFu), r1);
-              r1 = fmaf(a1.y, __uint_as_float(y & 0xF0u), r1);
-              r1 = fmaf(a1.z, __uint_as_float(y & 0xF00u), r1);
-              r1 = fmaf(a1.w, __uint_as_float(y & 0xF000u), r1);
+              float2 r0 = acc[hh][0], r1 = acc[hh][1];
+              r0 = __ffma2_rn(make_float2(a0.x, a0.y),
+                              make_float2(__uint_as_float(x & 0xFu), __uint_as_float(x & 0xF0u)), r0);
+              r0 = __ffma2_rn(make_float2(a0.z, a0.w),
+                              make_float2(__uint_as_float(x & 0xF00u), __uint_as_float(x & 0xF000u)), r0);
+              r1 = __ffma2_rn(make_float2(a1.x, a1.y),
+                              make_float2(__uint_as_float(y & 0xFu), __uint_as_float(y & 0xF0u)), r1);
+              r1 = __ffma2_rn(make_float2(a1.z, a1.w),
+                              make_float2(__uint_as_float(y & 0xF00u), __uint_as_float(y & 0xF000u)), r1);
               acc[hh][0] = r0;
               acc[hh][1] = r1;
             }
@@ -371,19 +378,23 @@ k_decode_kitty(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
 #pragma unroll
             for (int hh = 0; hh < GQ; ++hh) {
               const float *aw = sa + hh * D + HI + 16 * w;
-              float r0 = acc[hh][0], r1 = acc[hh][1];
+              float2 r0 = acc[hh][0], r1 = acc[hh][1];
 #pragma unroll
               for (int e = 0; e < 8; e += 4) {
                 const float4 a4 = *reinterpret_cast<const float4 *>(aw + e);
-                r0 = fmaf(a4.x, __uint_as_float(x & (3u << (2 * e))), r0);
-                r0 = fmaf(a4.y, __uint_as_float(x & (3u << (2 * e + 2))), r0);
-                r0 = fmaf(a4.z, __uint_as_float(x & (3u << (2 * e + 4))), r0);
-                r0 = fmaf(a4.w, __uint_as_float(x & (3u << (2 * e + 6))), r0);
+                r0 = __ffma2_rn(make_float2(a4.x, a4.y),
+                                make_float2(__uint_as_float(x & (3u << (2 * e))),
+                                            __uint_as_float(x & (3u << (2 * e + 2)))), r0);
+                r0 = __ffma2_rn(make_float2(a4.z, a4.w),
+                                make_float2(__uint_as_float(x & (3u << (2 * e + 4))),
+                                            __uint_as_float(x & (3u << (2 * e + 6)))), r0);
                 const float4 b4 = *reinterpret_cast<const float4 *>(aw + 8 + e);
-                r1 = fmaf(b4.x, __uint_as_float(y & (3u << (2 * e))), r1);
-                r1 = fmaf(b4.y, __uint_as_float(y & (3u << (2 * e + 2))), r1);
-                r1 = fmaf(b4.z, __uint_as_float(y & (3u << (2 * e + 4))), r1);
-                r1 = fmaf(b4.w, __uint_as_float(y & (3u << (2 * e + 6))), r1);
+                r1 = __ffma2_rn(make_float2(b4.x, b4.y),
+                                make_float2(__uint_as_float(y & (3u << (2 * e))),
+                                            __uint_as_float(y & (3u << (2 * e + 2)))), r1);
+                r1 = __ffma2_rn(make_float2(b4.z, b4.w),
+                                make_float2(__uint_as_float(y & (3u << (2 * e + 4))),
+                                            __uint_as_float(y & (3u << (2 * e + 6)))), r1);
               }
               acc[hh][0] = r0;
               acc[hh][1] = r1;
@@ -392,7 +403,8 @@ k_decode_kitty(Geometry geo, Planes pl, DecodeArgs args, DecodeTable tab) {
         }
 #pragma unroll
         for (int hh = 0; hh < GQ; ++hh)
-          sc[hh] = lane < bt ? fmaf(acc[hh][0] + acc[hh][1], pow2(kCarry), beta[hh])
+          sc[hh] = lane < bt ? fmaf((acc[hh][0].x + acc[hh][0].y) + (acc[hh][1].x + acc[hh][1].y),
+                                    pow2(kCarry), beta[hh])
                              : -INFINITY;
       }
       float p[GQ];
