@@ -483,8 +483,10 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 sf = __half22float2(s2[e]), zf = __half22float2(z2[e]);
-            kf[8 * q + 2 * e] = fmaf((float)c[8 * q + 2 * e], sf.x, zf.x);
-            kf[8 * q + 2 * e + 1] = fmaf((float)c[8 * q + 2 * e + 1], sf.y, zf.y);
+            const float2 r = __ffma2_rn(make_float2((float)c[8 * q + 2 * e],
+                                                    (float)c[8 * q + 2 * e + 1]), sf, zf);
+            kf[8 * q + 2 * e] = r.x;
+            kf[8 * q + 2 * e + 1] = r.y;
           }
         }
       } else if (t < S) {
@@ -550,7 +552,12 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
           const float sv = __half2float(svs[(ta + u - t0) * NJ + j]);
           const float zv = __half2float(svz[(ta + u - t0) * NJ + j]);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) vf[u][e] = fmaf((float)c[u][e], sv, zv);
+          for (int e = 0; e < 8; e += 2) {
+            const float2 r = __ffma2_rn(make_float2((float)c[u][e], (float)c[u][e + 1]),
+                                        make_float2(sv, sv), make_float2(zv, zv));
+            vf[u][e] = r.x;
+            vf[u][e + 1] = r.y;
+          }
         }
       } else {
 #pragma unroll
