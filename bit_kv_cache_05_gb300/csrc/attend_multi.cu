@@ -648,20 +648,21 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
 #pragma unroll
       for (int j = 0; j < 32; ++j) sc[32 + j] = tmp[j];
     }
+    // the row maximum of the raw scores, then scaled (sl2 > 0: the same
+    // value as the maximum of the scaled scores); the weights below scale
+    // each score inside one packed fma
     float mt = -INFINITY;
     if (t0 + kTok - 1 <= pos) {          // the whole tile is visible to this row
 #pragma unroll
-      for (int j = 0; j < kTok; ++j) {
-        sc[j] *= sl2;
-        mt = fmaxf(mt, sc[j]);
-      }
+      for (int j = 0; j < kTok; ++j) mt = fmaxf(mt, sc[j]);
     } else {
 #pragma unroll
       for (int j = 0; j < kTok; ++j) {
-        sc[j] = (t0 + j <= pos) ? sc[j] * sl2 : -INFINITY;
+        sc[j] = (t0 + j <= pos) ? sc[j] : -INFINITY;
         mt = fmaxf(mt, sc[j]);
       }
     }
+    mt *= sl2;
     float alpha = 1.f;
     const bool raise = mt > m_run + kLazy;   // false while both are -inf
     if (raise) {
@@ -681,7 +682,7 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
       }
       tmem_wait_st();
     }
-    float psum = 0.f;
+    float2 psum2 = make_float2(0.f, 0.f);
     // a row that has seen no token of its key range yet keeps m_run = -inf:
     // subtract 0 there, so that its -inf scores give 0
     const float msub = m_run == -INFINITY ? 0.f : m_run;
@@ -690,16 +691,19 @@ k_attend_multi(const __grid_constant__ CUtensorMap qmap, Geometry geo,
       uint32_t hw[4], lw[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float pa = ex2(sc[8 * j8 + 2 * e] - msub);
-        const float pc = ex2(sc[8 * j8 + 2 * e + 1] - msub);
-        psum += pa + pc;
+        // p = 2^(s sl2 - m) for two scores: one packed fma
+        const float2 x = __ffma2_rn(make_float2(sc[8 * j8 + 2 * e], sc[8 * j8 + 2 * e + 1]),
+                                    make_float2(sl2, sl2), make_float2(-msub, -msub));
+        const float pa = ex2(x.x);
+        const float pc = ex2(x.y);
+        psum2 = __fadd2_rn(psum2, make_float2(pa, pc));
         split2(pa, pc, hw[e], lw[e]);
       }
       const uint32_t po = sw_off(tid, j8);
       *reinterpret_cast<uint4 *>(sm + SM::PH + po) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
       *reinterpret_cast<uint4 *>(sm + SM::PL + po) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
-    l_run = fmaf(l_run, alpha, psum);
+    l_run = fmaf(l_run, alpha, psum2.x + psum2.y);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc_fence_before();
     __syncthreads();
